@@ -1,0 +1,276 @@
+"""The MoE layer in plain FP64 (oracle; test infrastructure).
+
+Steps and rounding points (DGPP pages: page 1 README "Exact" bullet and
+"exactness / levers" paragraph; page 3 README "Execution and performance"
+table, rows engine.prefill_bf16_partials and engine.prefill_fold_scales;
+page 4 forum post 1 quantisation table, "Activations stay BF16"):
+
+  x            BF16 activations [T, H]
+  logits       l[t, e] = fl32( sum_h x[t, h] * Wr[e, h] )   correctly rounded FP32
+               (+ fl32 addition of an optional per-expert bias)
+  top-k        experts ordered by (l descending, e ascending), first k kept
+  weights      w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k selected,
+               in FP64, stored as FP32 (equal to a full softmax renormalised
+               over the top-k; the shared denominator cancels)
+  dispatch     pairs p = t*k + j grouped by expert, ascending p within an expert
+  per pair     g = W_gate x, u = W_up x (FP64), h = bf16( silu(g) * u ),
+               P = W_down h (FP64)
+  combine      y_t = bf16( sum_j w_tj * P_tj  +  S_t ), S_t the shared expert
+               (weight 1, no gate) computed the same way
+
+Weights are decoded exactly (``formats.decode``); the only roundings are the
+FP32 logits and weights and the two BF16 roundings of h and y, which is the
+"FP32 accumulation, BF16 activations" chain evaluated without accumulation
+error.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+from typing import Optional
+
+import numpy as np
+
+from . import formats as F
+
+_U64 = 2.0 ** -53
+
+
+# ---------------------------------------------------------------- router ----
+
+def _fl32_exact(products: list) -> np.float32:
+    """Correctly rounded FP32 of the exact sum of FP64-exact products."""
+    d = math.fsum(products)                  # correctly rounded FP64 of the exact sum
+    f = np.float32(d)
+    fd = float(f)
+    if fd == d:
+        return f
+    other = np.nextafter(f, np.float32(np.inf) if d > fd else np.float32(-np.inf))
+    mid = (fd + float(other)) / 2.0          # exact in FP64
+    if d != mid:
+        return f                             # d strictly inside f's rounding interval
+    # d sits exactly on an FP32 midpoint: decide with the exact rational sum.
+    s = sum(Fraction(p) for p in products)
+    m = Fraction(mid)
+    if s > m:
+        return np.float32(max(fd, float(other)))
+    if s < m:
+        return np.float32(min(fd, float(other)))
+    return f if (f.view(np.uint32) & 1) == 0 else other   # exact tie: even
+
+
+def router_logits(x_bits: np.ndarray, Wr: np.ndarray, bias: Optional[np.ndarray] = None):
+    """Correctly rounded FP32 router logits.
+
+    Returns (logits f32 [T, E], near_midpoint bool [T, E]).  Each BF16 x FP32
+    product is exact in FP64.  The FP64 BLAS dot carries at most
+    gamma_n * sum|x_h Wr_eh| error; where that bound cannot separate the FP64
+    result from an FP32 rounding midpoint, the logit is recomputed with an
+    exactly rounded sum (math.fsum, then exact rationals at a midpoint).
+    ``near_midpoint`` marks logits whose exact value lies within 2^-40
+    (relative) of an FP32 rounding midpoint: a compensated FP32 dot may round
+    those differently, so callers report them.
+    """
+    X = F.bf16_to_f64(x_bits)
+    W = np.asarray(Wr, dtype=np.float32).astype(np.float64)
+    T, H = X.shape
+    d = X @ W.T
+    n = H
+    gamma = n * _U64 / (1.0 - n * _U64)
+    bound = gamma * (np.abs(X) @ np.abs(W).T) * (1.0 + 1e-9) + 1e-300
+    l32 = d.astype(np.float32)
+    f = l32.astype(np.float64)
+    up = np.nextafter(l32, np.float32(np.inf)).astype(np.float64)
+    dn = np.nextafter(l32, np.float32(-np.inf)).astype(np.float64)
+    mid_up, mid_dn = (f + up) / 2.0, (f + dn) / 2.0
+    safe = (d + bound < mid_up) & (d - bound > mid_dn)
+    for t, e in zip(*np.nonzero(~safe)):
+        prods = [float(a) * float(b) for a, b in zip(X[t], W[e])]
+        l32[t, e] = _fl32_exact(prods)
+    f = l32.astype(np.float64)
+    up = np.nextafter(l32, np.float32(np.inf)).astype(np.float64)
+    dn = np.nextafter(l32, np.float32(-np.inf)).astype(np.float64)
+    dist = np.minimum(np.abs(d - (f + up) / 2.0), np.abs(d - (f + dn) / 2.0))
+    near = dist <= 2.0 ** -40 * np.maximum(np.abs(d), 1e-300) + bound
+    if bias is not None:
+        l32 = (l32 + np.asarray(bias, dtype=np.float32)[None, :]).astype(np.float32)
+    return l32, near
+
+
+def topk(l32: np.ndarray, k: int) -> np.ndarray:
+    """Top-k expert ids per token, ordered by (logit desc, expert id asc)."""
+    T, E = l32.shape
+    ids = np.arange(E)
+    out = np.empty((T, k), dtype=np.int32)
+    for t in range(T):
+        order = np.lexsort((ids, -l32[t].astype(np.float64)))
+        out[t] = order[:k]
+    return out
+
+
+def topk_weights(l32: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """Renormalised softmax weights over the selected experts, FP64 -> FP32."""
+    sel = np.take_along_axis(l32.astype(np.float64), idx.astype(np.int64), axis=1)
+    z = np.exp(sel - sel[:, :1])
+    return (z / z.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
+def topk_weights_full_softmax(l32: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """Same weights via a softmax over all experts followed by renormalisation (FP64)."""
+    L = l32.astype(np.float64)
+    p = np.exp(L - L.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    sel = np.take_along_axis(p, idx.astype(np.int64), axis=1)
+    return sel / sel.sum(axis=1, keepdims=True)
+
+
+def route(x_bits, Wr, bias, k):
+    l32, near = router_logits(x_bits, Wr, bias)
+    idx = topk(l32, k)
+    w = topk_weights(l32, idx)
+    return l32, near, idx, w
+
+
+# -------------------------------------------------------------- dispatch ----
+
+def dispatch(idx: np.ndarray, E: int):
+    """Stable counting sort of pairs p = t*k + j by expert.
+
+    Returns (cnt [E] i32, off [E+1] i32, pair [T*k] i32): the pairs routed to
+    expert e are pair[off[e]:off[e+1]], in ascending p.
+    """
+    flat = np.asarray(idx, dtype=np.int64).reshape(-1)
+    cnt = np.bincount(flat, minlength=E).astype(np.int32)
+    off = np.zeros(E + 1, dtype=np.int32)
+    np.cumsum(cnt, out=off[1:])
+    pair = np.argsort(flat, kind="stable").astype(np.int32)
+    return cnt, off, pair
+
+
+# ---------------------------------------------------------------- experts ----
+
+def silu(z: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def swiglu_mlp(Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray, X: np.ndarray,
+               act_quant: bool = False) -> tuple:
+    """One SwiGLU expert on token rows X [n, H] (FP64 values).
+
+    Returns (h, P): h = bf16(silu(X Wg^T) * (X Wu^T)) [n, I] as FP64 values,
+    P = h Wd^T [n, H] in FP64.  With act_quant the token rows and h are
+    replaced by their NVFP4-quantised values before each projection.
+    """
+    if act_quant:
+        X = nvfp4_fake_quant(X)
+    g = X @ Wg.T
+    u = X @ Wu.T
+    h = F.round_bf16(silu(g) * u)
+    hq = nvfp4_fake_quant(h) if act_quant else h
+    P = hq @ Wd.T
+    return h, P
+
+
+# ------------------------------------------------ W4A4 activation quantizer ----
+
+def nvfp4_quantize_act(a: np.ndarray):
+    """NVFP4 quantisation of activation rows in 16-element blocks, tensor scale 1.
+
+    Per block: s = e4m3_rne_sat( fl32(amax / 6) ); code = e2m1_rne_sat( fl32(a / s) ),
+    with FP32 division emulated as an FP64 divide rounded to FP32 (correct
+    because 53 >= 2*24 + 2).  A block whose scale rounds to zero gets all-zero
+    codes.  Returns (codes [.., K] u8 0..15, scale codes [.., K/16] u8).
+    """
+    a = np.asarray(a, dtype=np.float64)
+    *lead, K = a.shape
+    blk = a.reshape(*lead, K // 16, 16)
+    amax = np.abs(blk).max(axis=-1)
+    s_code = F.e4m3_encode_rne_sat(np.float32(amax / 6.0).astype(np.float64))
+    s = F.E4M3_TABLE[s_code]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.float32(blk / s[..., None]).astype(np.float64)
+    q = np.where((s > 0)[..., None], q, 0.0)
+    codes = F.e2m1_encode_rne(q)
+    codes = np.where((s > 0)[..., None], codes, 0).astype(np.uint8)
+    return codes.reshape(*lead, K), s_code.astype(np.uint8)
+
+
+def nvfp4_dequantize_act(codes: np.ndarray, s_code: np.ndarray) -> np.ndarray:
+    *lead, K = codes.shape
+    v = F.E2M1_TABLE[codes].reshape(*lead, K // 16, 16) * F.E4M3_TABLE[s_code][..., None]
+    return v.reshape(*lead, K)
+
+
+def nvfp4_fake_quant(a: np.ndarray) -> np.ndarray:
+    return nvfp4_dequantize_act(*nvfp4_quantize_act(a))
+
+
+# ------------------------------------------------------------------ layer ----
+
+def _decoded(qm, e):
+    return F.decode_qmat(qm, e)
+
+
+def layer_forward(layer, x_bits: np.ndarray, act_quant: bool = False, tokens=None, expert_cache=None):
+    """Full MoE layer on host-resident checkpoint data (a synth.HostLayer).
+
+    tokens: optional subset of token rows whose outputs are wanted (routing is
+    still computed for every token, so the dispatch index is complete).
+    expert_cache: optional callable e -> (Wg, Wu, Wd) FP64, to regenerate
+    experts lazily instead of reading them from ``layer``.
+    Returns a dict of every intermediate the CUDA path exposes.
+    """
+    cfg = layer.cfg
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    T = x_bits.shape[0]
+    l32, near, idx, w = route(x_bits, layer.router_w, layer.router_b, cfg.k)
+    cnt, off, pair = dispatch(idx, cfg.E)
+    want = np.arange(T) if tokens is None else np.asarray(sorted(set(int(t) for t in tokens)))
+    X = F.bf16_to_f64(x_bits)
+    acc = {int(t): np.zeros(cfg.H) for t in want}
+    h_out = {}
+    want_set = set(int(t) for t in want)
+    for e in range(cfg.E):
+        ps = [int(p) for p in pair[off[e]:off[e + 1]] if int(p) // cfg.k in want_set]
+        if not ps:
+            continue
+        if expert_cache is not None:
+            Wg, Wu, Wd = expert_cache(e)
+        else:
+            Wg, Wu, Wd = _decoded(layer.gate, e), _decoded(layer.up, e), _decoded(layer.down, e)
+        rows = np.array([p // cfg.k for p in ps])
+        h, P = swiglu_mlp(Wg, Wu, Wd, X[rows], act_quant)
+        for i, p in enumerate(ps):
+            t, j = divmod(p, cfg.k)
+            acc[t] += float(w[t, j]) * P[i]
+            h_out[p] = h[i]
+    S = None
+    if layer.shared_gate is not None:
+        Wg, Wu, Wd = (_decoded(layer.shared_gate, 0), _decoded(layer.shared_up, 0),
+                      _decoded(layer.shared_down, 0))
+        _, S = swiglu_mlp(Wg, Wu, Wd, X[want], act_quant)
+    y = np.zeros((len(want), cfg.H))
+    for i, t in enumerate(want):
+        y[i] = acc[int(t)] + (S[i] if S is not None else 0.0)
+    return {
+        "logits": l32, "near_midpoint": near, "topk_idx": idx, "topk_w": w,
+        "expert_cnt": cnt, "expert_off": off, "pair_list": pair,
+        "tokens": want, "y_f64": y, "y_bits": F.f64_to_bf16_bits(y), "h": h_out, "shared": S,
+    }
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of BF16 values at |v| (the unit in the last place)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    _, e = np.frexp(np.where(a > 0, a, 1.0))
+    ulp = np.ldexp(1.0, np.maximum(e - 8, -133))
+    return np.where(a > 0, ulp, 2.0 ** -133)
+
+
+def within_tolerance(y_test: np.ndarray, y_ref: np.ndarray, ulps: float = 2.0, abs_tol: float = 1e-3):
+    """Elementwise |y_test - y_ref| <= max(ulps * ulp_bf16(y_ref), abs_tol)."""
+    y_test = np.asarray(y_test, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    tol = np.maximum(ulps * bf16_ulp(y_ref), abs_tol)
+    return np.abs(y_test - y_ref) <= tol

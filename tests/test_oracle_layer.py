@@ -1,0 +1,239 @@
+"""Pins for the oracle's MoE layer.
+
+* one expert, top-1, weight 1.0 reduces to a plain SwiGLU MLP, computed here
+  with torch CPU float64 ops on weights decoded independently through torch's
+  float8 casts;
+* the shared expert adds exactly a plain SwiGLU MLP (same independent path);
+* duplicated experts: a top-2 layer whose two experts are identical equals
+  the top-1 layer (the weights sum to one);
+* permuting expert ids permutes the routing and leaves y unchanged;
+* batch invariance: a token's output does not depend on the other tokens;
+* the W4A4 activation quantizer round-trips on-grid blocks and matches
+  brute force;
+* planted mistakes in the oracle are caught by these pins.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import formats as F
+from oracle import moe as M
+from synth.configs import FMT_FP8_B128, FMT_INT4_G64, FMT_INT8_G64, FMT_MXFP4, FMT_NVFP4, LayerConfig
+
+
+def _torch_e2m1(codes: np.ndarray) -> torch.Tensor:
+    """E2M1 codes -> float64 through torch's float8_e4m3fn decoder (bit-field re-encoding)."""
+    c = torch.from_numpy(codes.astype(np.int32))
+    s, e, m = (c >> 3) & 1, (c >> 1) & 3, c & 1
+    body = torch.where(e == 0, torch.where(m == 0, 0, 6 << 3), ((e + 6) << 3) | (m << 2))
+    return ((s << 7) | body).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+
+
+def _torch_decode(qm, e=0) -> torch.Tensor:
+    """Independent decoder (torch casts + explicit layout handling), float64 [N, K]."""
+    N, K, d = qm.N, qm.K, qm.data[e]
+    if qm.fmt in (FMT_NVFP4, FMT_MXFP4, FMT_INT4_G64):
+        lo, hi = d & 0xF, d >> 4
+        codes = np.stack([lo, hi], axis=-1).reshape(N, K)
+    if qm.fmt == FMT_NVFP4:
+        v = _torch_e2m1(codes)
+        s = torch.from_numpy(qm.scales[e]).view(torch.float8_e4m3fn).to(torch.float64)
+        return v * s.repeat_interleave(16, dim=1) * float(qm.ts[e])
+    if qm.fmt == FMT_MXFP4:
+        v = _torch_e2m1(codes)
+        s = torch.from_numpy(qm.scales[e]).view(torch.float8_e8m0fnu).to(torch.float64)
+        return v * s.repeat_interleave(32, dim=1)
+    if qm.fmt == FMT_INT4_G64:
+        q = torch.from_numpy(codes.astype(np.int8))
+        q = torch.where(q >= 8, q - 16, q).to(torch.float64)
+        s = torch.from_numpy(qm.scales[e].view(np.int16)).view(torch.bfloat16).to(torch.float64)
+        return q * s.repeat_interleave(64, dim=1)
+    if qm.fmt == FMT_INT8_G64:
+        q = torch.from_numpy(d.view(np.int8)).to(torch.float64)
+        s = torch.from_numpy(qm.scales[e].view(np.int16)).view(torch.bfloat16).to(torch.float64)
+        return q * s.repeat_interleave(64, dim=1)
+    if qm.fmt == FMT_FP8_B128:
+        q = torch.from_numpy(d).view(torch.float8_e4m3fn).to(torch.float64)
+        s = torch.from_numpy(qm.scales[e]).to(torch.float64)
+        return q * s.repeat_interleave(128, 0).repeat_interleave(128, 1)
+    raise ValueError
+
+
+def _torch_mlp(Wg, Wu, Wd, X):
+    g = X @ Wg.T
+    u = X @ Wu.T
+    h = torch.nn.functional.silu(g) * u
+    h = h.to(torch.float32).to(torch.bfloat16).to(torch.float64)   # bf16 activation (via fp32)
+    return h @ Wd.T
+
+
+def _small(fmt, shared_fmt=0, E=1, k=1, H=128, I=64):
+    return LayerConfig(f"small_{fmt}", fmt, H=H, E=E, k=k, I=I, shared_fmt=shared_fmt,
+                       shared_I=128 if shared_fmt == FMT_FP8_B128 else (I if shared_fmt else 0))
+
+
+@pytest.mark.parametrize("fmt,H,I", [(FMT_NVFP4, 128, 64), (FMT_MXFP4, 128, 64), (FMT_INT4_G64, 128, 128),
+                                     (FMT_INT8_G64, 128, 128)])
+def test_single_expert_equals_plain_swiglu_mlp(fmt, H, I):
+    cfg = _small(fmt, H=H, I=I)
+    lay = synth.make_layer(cfg, seed=3)
+    x = synth.make_tokens(cfg, 5, seed=3)
+    out = M.layer_forward(lay, x)
+    assert np.all(out["topk_idx"] == 0) and np.all(out["topk_w"] == 1.0)
+    X = torch.from_numpy(F.bf16_to_f64(x))
+    y_ref = _torch_mlp(_torch_decode(lay.gate), _torch_decode(lay.up), _torch_decode(lay.down), X).numpy()
+    ok = M.within_tolerance(F.bf16_to_f64(out["y_bits"]), y_ref, ulps=1.0, abs_tol=1e-6)
+    assert ok.all(), np.abs(F.bf16_to_f64(out["y_bits"]) - y_ref).max()
+
+
+@pytest.mark.parametrize("shared_fmt", [FMT_FP8_B128, FMT_INT8_G64])
+def test_shared_expert_adds_plain_mlp(shared_fmt):
+    cfg = _small(FMT_NVFP4, shared_fmt, E=4, k=2, H=128, I=64)
+    lay = synth.make_layer(cfg, seed=4)
+    x = synth.make_tokens(cfg, 3, seed=4)
+    with_shared = M.layer_forward(lay, x)
+    lay_ns = synth.HostLayer(cfg.with_(shared_fmt=0, shared_I=0), lay.seed, lay.router_w, lay.router_b,
+                             lay.gate, lay.up, lay.down)
+    without = M.layer_forward(lay_ns, x)
+    X = torch.from_numpy(F.bf16_to_f64(x))
+    S = _torch_mlp(_torch_decode(lay.shared_gate), _torch_decode(lay.shared_up), _torch_decode(lay.shared_down),
+                   X).numpy()
+    assert np.allclose(with_shared["y_f64"] - without["y_f64"], S, rtol=1e-12, atol=1e-12)
+
+
+def test_identical_experts_top2_equals_top1():
+    cfg1 = _small(FMT_NVFP4, E=1, k=1)
+    lay1 = synth.make_layer(cfg1, seed=5)
+    cfg2 = cfg1.with_(E=2, k=2)
+    dup = lambda q: synth.QMat(q.fmt, q.N, q.K, np.concatenate([q.data, q.data]),
+                               np.concatenate([q.scales, q.scales]), np.concatenate([q.ts, q.ts]))
+    rw = np.concatenate([lay1.router_w, lay1.router_w * np.float32(0.5)])
+    lay2 = synth.HostLayer(cfg2, 5, rw, None, dup(lay1.gate), dup(lay1.up), dup(lay1.down))
+    x = synth.make_tokens(cfg1, 4, seed=5)
+    y1 = M.layer_forward(lay1, x)["y_f64"]
+    o2 = M.layer_forward(lay2, x)
+    assert np.allclose(o2["topk_w"].astype(np.float64).sum(1), 1.0, atol=2 ** -23)
+    scale = o2["topk_w"].astype(np.float64).sum(1, keepdims=True)
+    assert np.allclose(o2["y_f64"], y1 * scale, rtol=1e-12, atol=1e-15)
+
+
+def test_permuting_expert_ids_permutes_routing_only():
+    cfg = _small(FMT_NVFP4, E=6, k=3)
+    lay = synth.make_layer(cfg, seed=6)
+    x = synth.make_tokens(cfg, 7, seed=6)
+    base = M.layer_forward(lay, x)
+    perm = np.array([3, 5, 0, 1, 4, 2])                # new id i holds old expert perm[i]
+    inv = np.argsort(perm)
+    sub = lambda q: synth.QMat(q.fmt, q.N, q.K, q.data[perm], q.scales[perm], q.ts[perm])
+    lp = synth.HostLayer(cfg, 6, lay.router_w[perm], None, sub(lay.gate), sub(lay.up), sub(lay.down))
+    out = M.layer_forward(lp, x)
+    # same experts chosen, renamed (ordering among equal logits may differ only on exact ties)
+    assert np.array_equal(perm[out["topk_idx"]], base["topk_idx"]) or np.array_equal(
+        np.sort(perm[out["topk_idx"]], 1), np.sort(base["topk_idx"], 1))
+    assert np.array_equal(out["y_bits"], base["y_bits"])
+    assert np.array_equal(inv[base["topk_idx"]], out["topk_idx"])
+
+
+def test_batch_invariance():
+    cfg = _small(FMT_MXFP4, E=5, k=2)
+    lay = synth.make_layer(cfg, seed=7)
+    x = synth.make_tokens(cfg, 6, seed=7)
+    full = M.layer_forward(lay, x)
+    for t in (0, 3, 5):
+        one = M.layer_forward(lay, x[t:t + 1])
+        assert np.array_equal(one["y_bits"][0], full["y_bits"][t])
+        assert np.array_equal(one["topk_idx"][0], full["topk_idx"][t])
+    sub = M.layer_forward(lay, x, tokens=[5, 1])
+    assert np.array_equal(sub["y_bits"], full["y_bits"][[1, 5]])
+
+
+def test_nvfp4_act_quantizer_pins():
+    # on-grid block: values e2m1 * s with amax = 6 s -> exact round trip
+    s = 0.75                                          # e4m3 0.75 (exact), amax/6 = 0.75
+    codes = np.array([7, 1, 2, 3, 4, 5, 6, 0, 9, 10, 11, 12, 13, 14, 15, 8])
+    a = F.E2M1_TABLE[codes] * s
+    q, sc = M.nvfp4_quantize_act(a[None, :])
+    assert F.E4M3_TABLE[sc[0, 0]] == s
+    assert np.array_equal(M.nvfp4_dequantize_act(q, sc)[0], a)
+    # zero block -> zero scale, zero codes
+    q0, s0 = M.nvfp4_quantize_act(np.zeros((1, 16)))
+    assert s0[0, 0] == 0 and np.all(q0 == 0)
+    # brute force on random blocks: each value is the nearest E2M1 multiple of the block scale
+    rng = np.random.default_rng(9)
+    A = F.round_bf16(rng.standard_normal((64, 32)))
+    q, sc = M.nvfp4_quantize_act(A)
+    D = M.nvfp4_dequantize_act(q, sc)
+    for r in range(64):
+        for b in range(2):
+            blk = A[r, b * 16:(b + 1) * 16]
+            sv = F.E4M3_TABLE[sc[r, b]]
+            amax6 = float(np.float32(np.abs(blk).max() / 6.0))
+            assert sv == F.E4M3_TABLE[F.e4m3_encode_rne_sat(np.array([amax6]))[0]]
+            for i in range(16):
+                y = float(np.float32(blk[i] / sv))
+                cand = np.abs(min(abs(y), 6.0) - F.E2M1_GRID)
+                assert abs(abs(D[r, b * 16 + i]) / sv - F.E2M1_GRID[np.argmin(cand)]) == 0 or cand.min() == np.sort(cand)[1]
+
+
+# --------------------------------------------------- planted mistakes ----
+
+def _run_pin(fn, *args):
+    try:
+        fn(*args)
+        return True
+    except Exception:
+        return False
+
+
+def _swapped_nibbles(data):
+    d = np.asarray(data, dtype=np.uint8)
+    out = np.empty(d.shape[:-1] + (d.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = d >> 4
+    out[..., 1::2] = d & 0x0F
+    return out
+
+
+def _topk_ids_descending(l32, k):
+    ids = -np.arange(l32.shape[1])
+    return np.stack([np.lexsort((ids, -l32[t].astype(np.float64)))[:k] for t in range(l32.shape[0])]).astype(np.int32)
+
+
+def _unnormalised_weights(l32, idx):
+    sel = np.take_along_axis(l32.astype(np.float64), idx.astype(np.int64), axis=1)
+    return np.exp(sel - l32.astype(np.float64).max(axis=1, keepdims=True)).astype(np.float32)
+
+
+def _unstable_dispatch(idx, E):
+    cnt, off, pair = _ORIG["dispatch"](idx, E)
+    return cnt, off, np.concatenate([pair[off[e]:off[e + 1]][::-1] for e in range(E)]).astype(np.int32)
+
+
+_ORIG = {"dispatch": M.dispatch, "decode": F.decode, "swiglu": M.swiglu_mlp}
+
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    """Each plausible oracle mistake fails at least one pin (mistakes planted in the oracle, on the CPU)."""
+    import tests.test_oracle_formats as TF
+    import tests.test_oracle_router as TR
+
+    single = (test_single_expert_equals_plain_swiglu_mlp, FMT_NVFP4, 128, 64)
+    mistakes = {
+        "nibble order": (F, "unpack_nibbles", _swapped_nibbles, [(TF.test_nvfp4_layout_hand_built,), single]),
+        "silu sign": (M, "silu", lambda z: z / (1.0 + np.exp(z)), [single]),
+        "dropped tensor scale": (F, "decode", lambda fmt, d, s, ts, N, K: _ORIG["decode"](fmt, d, s, 1.0, N, K),
+                                 [(TF.test_nvfp4_layout_hand_built,)]),
+        "tie-break reversed": (M, "topk", _topk_ids_descending, [(TR.test_topk_order_descending_then_id,)]),
+        "unnormalised weights": (M, "topk_weights", _unnormalised_weights, [(TR.test_weights_identity_and_sum,)]),
+        "unstable dispatch": (M, "dispatch", _unstable_dispatch, [(TR.test_dispatch_matches_plain_loop,)]),
+        "gate/up swapped": (M, "swiglu_mlp", lambda Wg, Wu, Wd, X, act_quant=False: _ORIG["swiglu"](
+            Wu, Wg, Wd, X, act_quant), [single]),
+        "shared expert dropped": (M, "swiglu_mlp", lambda Wg, Wu, Wd, X, act_quant=False: (
+            lambda h, P: (h, P * (Wg.shape[0] != 128)))(*_ORIG["swiglu"](Wg, Wu, Wd, X, act_quant)),
+            [(test_shared_expert_adds_plain_mlp, FMT_FP8_B128)]),
+    }
+    for name, (mod, attr, bad, pins) in mistakes.items():
+        with monkeypatch.context() as mp:
+            mp.setattr(mod, attr, bad)
+            caught = [not _run_pin(*p) for p in pins]
+        assert any(caught), f"planted mistake not caught: {name}"

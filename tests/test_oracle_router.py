@@ -1,0 +1,133 @@
+"""Pins for the oracle's router (logits, top-k, weights) and dispatch index.
+
+Checked against exact rational arithmetic, brute force over all k-subsets,
+the closed-form softmax identity and plain loops.
+"""
+import itertools
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import formats as F
+from oracle import moe as M
+
+
+def _fl32_of_fraction(s: Fraction) -> np.float32:
+    """Correctly rounded binary32 of an exact rational (ties to even), by bisection on neighbours."""
+    f = np.float32(float(s))                      # within one fp32 ulp of s
+    for _ in range(3):
+        up = np.nextafter(f, np.float32(np.inf))
+        dn = np.nextafter(f, np.float32(-np.inf))
+        best = min((abs(Fraction(float(c)) - s), int(c.view(np.uint32)) & 1, c) for c in (dn, f, up))
+        f = best[2]
+    return np.float32(f)
+
+
+def _bf16_bits_random(rng, shape):
+    return np.asarray(
+        (np.float32(rng.standard_normal(shape)).view(np.uint32) >> 16), dtype=np.uint16)
+
+
+def test_logits_are_correctly_rounded_fp32():
+    rng = np.random.default_rng(5)
+    T, E, H = 4, 8, 96
+    x = _bf16_bits_random(rng, (T, H))
+    W = (rng.standard_normal((E, H)) * 0.02).astype(np.float32)
+    l32, _ = M.router_logits(x, W)
+    X = F.bf16_to_f64(x)
+    for t in range(T):
+        for e in range(E):
+            s = sum(Fraction(float(X[t, h])) * Fraction(float(W[e, h])) for h in range(H))
+            assert l32[t, e] == _fl32_of_fraction(s)
+
+
+def test_logits_exact_midpoint_cases():
+    # dot products landing exactly on, and just beside, an fp32 rounding midpoint
+    one = np.float32(1.0)
+    half_ulp = 2.0 ** -24
+    H = 4
+    cases = [
+        ([1.0, half_ulp, 0.0, 0.0], one),                          # exactly 1 + 2^-24: tie -> even (1.0)
+        ([1.0, half_ulp, 2.0 ** -60, 0.0], np.nextafter(one, np.float32(2))),   # just above the tie
+        ([1.0, half_ulp, -2.0 ** -60, 0.0], one),                  # just below the tie
+        ([1.0 + 2.0 ** -23, half_ulp, 0.0, 0.0], np.float32(1.0 + 2.0 ** -22)),  # tie from odd -> up
+    ]
+    for terms, expect in cases:
+        Wr = np.array([terms], dtype=np.float64)
+        assert np.all(Wr.astype(np.float32).astype(np.float64) == Wr)
+        x = np.full((1, H), 0x3F80, dtype=np.uint16)               # bf16 1.0
+        l32, near = M.router_logits(x, Wr.astype(np.float32))
+        assert l32[0, 0] == expect, (terms, l32[0, 0], expect)
+
+
+def test_logit_bias_is_fp32_add_after_rounding():
+    rng = np.random.default_rng(6)
+    x = _bf16_bits_random(rng, (3, 64))
+    W = (rng.standard_normal((5, 64)) * 0.02).astype(np.float32)
+    b = rng.standard_normal(5).astype(np.float32)
+    l0, _ = M.router_logits(x, W)
+    lb, _ = M.router_logits(x, W, b)
+    assert np.array_equal(lb, (l0 + b[None, :]).astype(np.float32))
+
+
+def _brute_topk(row, k):
+    best = None
+    for sub in itertools.combinations(range(len(row)), k):
+        key = sorted(((-float(row[e]), e) for e in sub))
+        if best is None or key < best:
+            best = key
+    return [e for _, e in best]
+
+
+@pytest.mark.parametrize("E,k", [(6, 1), (8, 2), (10, 3), (12, 4)])
+def test_topk_brute_force_with_ties(E, k):
+    rng = np.random.default_rng(E * 10 + k)
+    for trial in range(40):
+        # few distinct values -> many exact ties
+        row = rng.integers(-3, 3, size=E).astype(np.float32) * np.float32(0.5)
+        if trial % 4 == 0:
+            row = rng.standard_normal(E).astype(np.float32)
+        got = M.topk(row[None, :], k)[0]
+        assert list(got) == _brute_topk(row, k)
+
+
+def test_topk_order_descending_then_id():
+    row = np.array([[1.0, 3.0, 3.0, 2.0, 3.0]], dtype=np.float32)
+    assert list(M.topk(row, 4)[0]) == [1, 2, 4, 3]
+
+
+def test_weights_identity_and_sum():
+    rng = np.random.default_rng(7)
+    l32 = (rng.standard_normal((50, 64)) * 2).astype(np.float32)
+    idx = M.topk(l32, 8)
+    w = M.topk_weights(l32, idx)
+    w_full = M.topk_weights_full_softmax(l32, idx)
+    assert np.allclose(w.astype(np.float64), w_full, rtol=2 ** -23, atol=0)
+    assert np.all(np.abs(w.astype(np.float64).sum(axis=1) - 1.0) <= 8 * 2 ** -24)
+    assert np.all(np.diff(w, axis=1) <= 0)                         # ordered like the logits
+    assert np.all(M.topk_weights(l32, M.topk(l32, 1)) == 1.0)      # k = 1 -> weight 1
+
+
+def test_dispatch_matches_plain_loop():
+    rng = np.random.default_rng(8)
+    T, k, E = 37, 5, 23
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    cnt, off, pair = M.dispatch(idx, E)
+    ref_lists = [[] for _ in range(E)]
+    for t in range(T):
+        for j in range(k):
+            ref_lists[idx[t, j]].append(t * k + j)
+    assert list(cnt) == [len(l) for l in ref_lists]
+    assert off[0] == 0 and off[-1] == T * k
+    for e in range(E):
+        assert list(pair[off[e]:off[e + 1]]) == ref_lists[e]
+    assert sorted(pair.tolist()) == list(range(T * k))
+
+
+def test_dispatch_empty_experts_and_single_token():
+    idx = np.array([[3, 0]], dtype=np.int32)
+    cnt, off, pair = M.dispatch(idx, 6)
+    assert list(cnt) == [1, 0, 0, 1, 0, 0]
+    assert list(off) == [0, 1, 1, 1, 2, 2, 2]
+    assert list(pair) == [1, 0]
