@@ -1,0 +1,224 @@
+/*
+ * moe.h - C ABI of the quantized mixture-of-experts layer for GB300 (sm_103a).
+ *
+ * One MoE layer computed directly on block-quantized checkpoint weights, with
+ * no dequantized copy: router softmax + top-k, expert dispatch, gate/up
+ * projection with SwiGLU, down projection and the weighted combine, BF16
+ * activations and FP32 accumulation.
+ *
+ * Sources (the DGPP pages):
+ *  - DGPP README (GitHub mirror), intro bullets "Serves checkpoints as
+ *    published" (formats read by kernels written for each, no dequantized
+ *    copy) and "Exact" (the default chain computes what the checkpoint
+ *    specifies; reduced-precision levers are explicit and off by default).
+ *  - DGPP README, "Execution and performance" table: engine.prefill_bf16_partials
+ *    (per-expert partials summed in fp32 by default), engine.prefill_fold_scales
+ *    (per-group scale fma by default), engine.expert_tile_list (expert GEMM over
+ *    a compact list of routed segments' tiles), engine.expert_gemm_pair (gate
+ *    and up in one launch).
+ *  - "DGPP: a GB10-optimized C/CUDA inference engine" (NVIDIA Developer Forums),
+ *    post 1, quantisation table (NVFP4 / MXFP4 routed experts, int4 g64 routed
+ *    with int8 g64 shared experts, FP8 shared experts; activations stay BF16);
+ *    post 15 "Lossless bf12" (decode streams weights at the memory line rate;
+ *    weights rebuilt in registers).
+ *  - same thread, weekly update on page 5: NVFP4 W4A4 prefill is opt-in.
+ *
+ * Conventions
+ *  - Every pointer marked "device" is a CUDA device pointer owned by the
+ *    caller; descriptors (moe_layer, moe_options) live in host memory and are
+ *    read only during the call.  The library allocates nothing and keeps no
+ *    global state; it is safe to call concurrently on different streams with
+ *    different workspaces.
+ *  - All calls are asynchronous on `stream` and make no host reads of device
+ *    data, so they can be captured in a CUDA graph.  Arguments are validated
+ *    on the host before any launch; a failed validation launches nothing.
+ *  - Device pointers must be 16-byte aligned (MOE_ERR_MISALIGNED otherwise).
+ *  - Weight matrices W[N, K] are row-major with the reduction dimension K
+ *    innermost; experts are stacked contiguously: W_e = base + e * stride.
+ *    Gate and up are [I, H] per expert, down is [H, I].
+ *  - Activations x and outputs y are BF16 [T, H] row-major.
+ *  - Results are deterministic: no floating-point atomics; per-expert
+ *    partials are summed in FP32 in a fixed order.
+ */
+#ifndef QMOE_MOE_H
+#define QMOE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's cudaStream_t; NULL selects the legacy default stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,      /* null pointer, bad size, T out of range, unknown enum   */
+  MOE_ERR_UNSUPPORTED = -2,      /* valid but not implemented (shape or format combination) */
+  MOE_ERR_MISALIGNED = -3,       /* a device pointer is not 16-byte aligned                 */
+  MOE_ERR_WORKSPACE = -4,        /* workspace null or smaller than moe_workspace_size()     */
+  MOE_ERR_CUDA = -5,             /* a CUDA runtime call or launch failed                    */
+  MOE_ERR_DEVICE_TIMEOUT = -6,   /* a bounded device-side wait gave up (see moe_check)      */
+  MOE_ERR_DEVICE_BAD_INDEX = -7  /* a device-side index check failed (see moe_check)        */
+} moe_status;
+
+/* Weight formats (DGPP forum post 1, quantisation table). */
+typedef enum {
+  MOE_FMT_NONE = 0,
+  /* E2M1 codes, two per byte (low nibble = even k); E4M3 scale per 16
+   * elements, scales [N, K/16] u8; FP32 tensor scale per expert.
+   * W = e2m1 * e4m3 * tensor_scale. */
+  MOE_FMT_NVFP4 = 1,
+  /* E2M1 codes as NVFP4; E8M0 scale per 32 elements, scales [N, K/32] u8.
+   * W = e2m1 * 2^(scale - 127). */
+  MOE_FMT_MXFP4 = 2,
+  /* Symmetric int4, two's-complement nibbles (low nibble = even k), BF16 scale
+   * per 64 elements, scales [N, K/64] bf16.  W = q * s. */
+  MOE_FMT_INT4_G64 = 3,
+  /* Symmetric int8 [N, K], BF16 scale per 64 elements, scales [N, K/64] bf16. */
+  MOE_FMT_INT8_G64 = 4,
+  /* E4M3 codes [N, K], FP32 scale per 128x128 block, scales [N/128, K/128] f32. */
+  MOE_FMT_FP8_B128 = 5
+} moe_format;
+
+/* A stack of matrices W_e[N, K] (e = 0 .. count-1) in one format. */
+typedef struct {
+  const void* data;          /* device; codes of expert e at data + e * data_bytes(N, K)      */
+  const void* scales;        /* device; scales of expert e at scales + e * scale_bytes(N, K)  */
+  const float* tensor_scale; /* device [count] f32; NVFP4 only (ignored for other formats)    */
+} moe_qweight;
+
+/* One MoE layer.  Routed experts: E of them, top_k chosen per token. */
+typedef struct {
+  int32_t hidden;            /* H */
+  int32_t inter;             /* I, routed expert intermediate size */
+  int32_t n_experts;         /* E, 1 .. 1024 */
+  int32_t top_k;             /* k, 1 .. min(E, 16) */
+  int32_t fmt;               /* moe_format of the routed experts */
+  const float* router_w;     /* device [E, H] f32 */
+  const float* router_bias;  /* device [E] f32, added to the FP32 logits, or NULL */
+  moe_qweight gate;          /* [E] x [I, H] */
+  moe_qweight up;            /* [E] x [I, H] */
+  moe_qweight down;          /* [E] x [H, I] */
+  int32_t shared_fmt;        /* moe_format of the shared expert, MOE_FMT_NONE if absent */
+  int32_t shared_inter;      /* Is */
+  moe_qweight shared_gate;   /* [1] x [Is, H] */
+  moe_qweight shared_up;     /* [1] x [Is, H] */
+  moe_qweight shared_down;   /* [1] x [H, Is] */
+} moe_layer;
+
+typedef struct {
+  /* 0 (default): BF16 activations, the exact chain.  1: the NVFP4 W4A4
+   * lever (prefill only, NVFP4 routed experts): activations and SwiGLU
+   * outputs re-quantised to NVFP4 16-element blocks before the projections
+   * (DGPP forum, page 5 weekly update: W4A4 prefill is opt-in). */
+  int32_t act_quant;
+  int32_t reserved[7];       /* must be zero */
+} moe_options;
+
+/* Largest token count moe_decode_forward accepts. */
+#define MOE_DECODE_MAX_TOKENS 8
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(int32_t status);
+
+/*
+ * Bytes of device workspace needed by moe_route / moe_decode_forward /
+ * moe_prefill_forward for up to max_tokens tokens (0 if the layer or options
+ * are invalid).  The workspace must be 256-byte aligned and initialised once
+ * with moe_workspace_init before its first use; the library leaves it
+ * re-usable after every call.
+ */
+size_t moe_workspace_size(const moe_layer* layer, int32_t max_tokens, const moe_options* opts);
+
+/* Zero the workspace control block (stream-ordered).  Call once per workspace. */
+int32_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Router and dispatch only (DGPP README "Execution and performance",
+ * engine.expert_tile_list: routed segments per expert).
+ *   logits     l[t, e] = fl32( sum_h x[t, h] * router_w[e, h] ), the correctly
+ *              rounded FP32 dot product, then fl32(l + router_bias[e]) if a bias
+ *              is given.
+ *   topk_idx   [T, k] i32: experts by logit descending, ties to the lower id.
+ *   topk_w     [T, k] f32: exp(l_j - l_0) / sum_i exp(l_i - l_0) over the selected.
+ *   expert_cnt [E] i32 pairs per expert; expert_off [E+1] i32 exclusive scan.
+ *   pair_list  [T*k] i32: pair ids p = t*k + j grouped by expert, ascending p
+ *              within an expert (a stable counting sort).
+ * Any of the output pointers may be NULL (that output is not written).
+ * T: 1 .. max_tokens of the workspace.
+ */
+int32_t moe_route(const moe_layer* layer, const void* x /* device bf16 [T, H] */, int32_t T,
+                  int32_t* topk_idx, float* topk_w, int32_t* expert_cnt, int32_t* expert_off,
+                  int32_t* pair_list, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Whole layer for decode-sized batches, T = 1 .. MOE_DECODE_MAX_TOKENS:
+ *   y[t] = bf16( sum_j topk_w[t, j] * down_e( h_tj ) + shared(x_t) ),
+ *   h_tj = bf16( silu(gate_e x_t) * (up_e x_t) ),  e = topk_idx[t, j],
+ * with the shared expert (weight 1, no gate) added when present.  Routing
+ * outputs are left in the workspace (see moe_workspace_layout).
+ * opts may be NULL (defaults); act_quant must be 0 here.
+ */
+int32_t moe_decode_forward(const moe_layer* layer, const void* x /* device bf16 [T, H] */, int32_t T,
+                           void* y /* device bf16 [T, H] */, const moe_options* opts, void* ws, size_t ws_bytes,
+                           moe_stream_t stream);
+
+/*
+ * Whole layer for any T >= 1 (prefill), same result definition as
+ * moe_decode_forward; expert projections run as grouped GEMMs over a compact
+ * tile list of the routed segments.  opts->act_quant = 1 selects the NVFP4
+ * W4A4 lever (NVFP4 routed experts only).
+ */
+int32_t moe_prefill_forward(const moe_layer* layer, const void* x /* device bf16 [T, H] */, int32_t T,
+                            void* y /* device bf16 [T, H] */, const moe_options* opts, void* ws, size_t ws_bytes,
+                            moe_stream_t stream);
+
+/*
+ * Read and clear the device-side error flag of a workspace.  Synchronises
+ * `stream` (this is the one call that blocks).  Returns MOE_OK,
+ * MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BAD_INDEX.
+ */
+int32_t moe_check(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Byte offsets, within the workspace, of the routing results a forward call leaves there. */
+typedef struct {
+  size_t logits;      /* f32 [T, E] */
+  size_t topk_idx;    /* i32 [T, k] */
+  size_t topk_w;      /* f32 [T, k] */
+  size_t expert_cnt;  /* i32 [E] */
+  size_t expert_off;  /* i32 [E + 1] */
+  size_t pair_list;   /* i32 [T * k] */
+  size_t total;       /* workspace bytes for this max_tokens */
+} moe_ws_layout;
+
+int32_t moe_workspace_layout(const moe_layer* layer, int32_t max_tokens, const moe_options* opts,
+                             moe_ws_layout* out);
+
+/*
+ * Decode rows [row0, row0 + nrows) of expert `expert` of a weight stack to
+ * FP32 (format decode, the step every projection kernel performs in
+ * registers; exposed for bit-exact checking).  out[r, k] = fl32(exact value):
+ * e2m1 * e4m3 * ts (NVFP4), e2m1 * 2^(c-127) (MXFP4), q * s (int4/int8 g64),
+ * e4m3 * s (FP8 b128).  out: device f32 [nrows, K].
+ */
+int32_t moe_dequantize(int32_t fmt, const moe_qweight* w, int32_t N, int32_t K, int32_t expert, int32_t row0,
+                       int32_t nrows, float* out, moe_stream_t stream);
+
+/*
+ * NVFP4 activation quantizer of the W4A4 lever, per 16-element block of each
+ * row: s = e4m3_rne_sat( fl32(amax / 6) ), code = e2m1_rne_sat( fl32(a / s) ),
+ * tensor scale 1; a block whose scale rounds to zero gets zero codes.
+ *   x: device bf16 [rows, K]; codes: device u8 [rows, K/2] (low nibble = even k);
+ *   scales: device u8 [rows, K/16] (E4M3).  K a multiple of 16.
+ */
+int32_t moe_quantize_act_nvfp4(const void* x, int32_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
+                               moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMOE_MOE_H */

@@ -1,0 +1,361 @@
+// Host side of the C ABI (include/moe.h): argument validation, workspace
+// layout, tiling choices and kernel launches.  Nothing here allocates device
+// memory; every buffer belongs to the caller.
+#include <cstring>
+
+#include "kernels.cuh"
+
+using namespace qmoe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+bool valid_fmt(int f) { return f >= MOE_FMT_NVFP4 && f <= MOE_FMT_FP8_B128; }
+
+// Shape rules of the formats and of the kernels (16-byte units along K,
+// 128-row FP8 scale blocks).
+bool shape_ok(int fmt, int N, int K) {
+  if (N <= 0 || K <= 0 || N % 16 || K % 128) return false;
+  if (fmt == MOE_FMT_FP8_B128 && (N % 128 || K % 128)) return false;
+  return true;
+}
+
+struct Layout {
+  size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, rb_cnt, total;
+};
+
+Layout make_layout(const moe_layer* L, int maxT) {
+  Layout o;
+  size_t at = 0;
+  auto take = [&](size_t bytes) {
+    size_t p = at;
+    at = align_up(at + bytes);
+    return p;
+  };
+  const size_t T = (size_t)maxT, E = (size_t)L->n_experts, k = (size_t)L->top_k, H = (size_t)L->hidden,
+               I = (size_t)L->inter, Is = (size_t)(L->shared_fmt ? L->shared_inter : 0);
+  o.ctrl = take(sizeof(Ctrl));
+  o.logits = take(T * E * 4);
+  o.topk_idx = take(T * k * 4);
+  o.topk_w = take(T * k * 4);
+  o.cnt = take(E * 4);
+  o.off = take((E + 1) * 4);
+  o.pair = take(T * k * 4);
+  o.act = take(E * 4);
+  o.h = take(T * k * I * 2);
+  o.hs = take(T * Is * 2 + 16);
+  o.P = take(T * k * H * 4);
+  o.S = take(T * H * 4 + 16);
+  o.rb_cnt = take(H / 16 * 4);
+  o.total = at;
+  return o;
+}
+
+int32_t check_qweight(const moe_qweight& w, int fmt, int N, int K) {
+  if (!w.data || !w.scales) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w.data) || !aligned4(w.scales)) return MOE_ERR_MISALIGNED;
+  if (fmt == MOE_FMT_NVFP4) {
+    if (!w.tensor_scale) return MOE_ERR_INVALID_ARG;
+    if (!aligned4(w.tensor_scale)) return MOE_ERR_MISALIGNED;
+  }
+  if (!shape_ok(fmt, N, K)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int32_t check_layer(const moe_layer* L) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (L->hidden <= 0 || L->inter <= 0 || L->n_experts <= 0 || L->top_k <= 0) return MOE_ERR_INVALID_ARG;
+  if (L->n_experts > 1024 || L->top_k > 16 || L->top_k > L->n_experts) return MOE_ERR_UNSUPPORTED;
+  if (!valid_fmt(L->fmt)) return MOE_ERR_INVALID_ARG;
+  if (!L->router_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(L->router_w)) return MOE_ERR_MISALIGNED;
+  if (L->router_bias && !aligned4(L->router_bias)) return MOE_ERR_MISALIGNED;
+  const int H = L->hidden, I = L->inter;
+  int32_t st;
+  if ((st = check_qweight(L->gate, L->fmt, I, H)) != MOE_OK) return st;
+  if ((st = check_qweight(L->up, L->fmt, I, H)) != MOE_OK) return st;
+  if ((st = check_qweight(L->down, L->fmt, H, I)) != MOE_OK) return st;
+  if (L->shared_fmt != MOE_FMT_NONE) {
+    if (!valid_fmt(L->shared_fmt)) return MOE_ERR_INVALID_ARG;
+    const int Is = L->shared_inter;
+    if (Is <= 0) return MOE_ERR_INVALID_ARG;
+    if ((st = check_qweight(L->shared_gate, L->shared_fmt, Is, H)) != MOE_OK) return st;
+    if ((st = check_qweight(L->shared_up, L->shared_fmt, Is, H)) != MOE_OK) return st;
+    if ((st = check_qweight(L->shared_down, L->shared_fmt, H, Is)) != MOE_OK) return st;
+  }
+  return MOE_OK;
+}
+
+int32_t check_options(const moe_options* o) {
+  if (!o) return MOE_OK;
+  if (o->act_quant != 0 && o->act_quant != 1) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 7; ++i)
+    if (o->reserved[i] != 0) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+int32_t check_ws(const moe_layer* L, int maxT, void* ws, size_t ws_bytes) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < make_layout(L, maxT).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+QW qw(const moe_qweight& w, int fmt) {
+  QW q;
+  q.data = static_cast<const uint8_t*>(w.data);
+  q.scales = static_cast<const uint8_t*>(w.scales);
+  q.ts = fmt == MOE_FMT_NVFP4 ? w.tensor_scale : nullptr;
+  return q;
+}
+
+RouteBufs route_bufs(const Layout& lo, void* ws) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  RouteBufs r;
+  r.ctrl = reinterpret_cast<Ctrl*>(b + lo.ctrl);
+  r.logits = reinterpret_cast<float*>(b + lo.logits);
+  r.topk_idx = reinterpret_cast<int32_t*>(b + lo.topk_idx);
+  r.topk_w = reinterpret_cast<float*>(b + lo.topk_w);
+  r.cnt = reinterpret_cast<int32_t*>(b + lo.cnt);
+  r.off = reinterpret_cast<int32_t*>(b + lo.off);
+  r.pair = reinterpret_cast<int32_t*>(b + lo.pair);
+  r.act = reinterpret_cast<int32_t*>(b + lo.act);
+  return r;
+}
+
+// The largest token count a workspace of ws_bytes supports for this layer.
+int ws_max_tokens(const moe_layer* L, size_t ws_bytes) {
+  int lo = 0, hi = 1;
+  while (hi < (1 << 24) && make_layout(L, hi).total <= ws_bytes) { lo = hi; hi *= 2; }
+  while (hi - lo > 1) {
+    int mid = lo + (hi - lo) / 2;
+    if (make_layout(L, mid).total <= ws_bytes) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+int32_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Warp split (wk along K, wr along rows; wk * wr = 8) for matrices with
+// reduction length K and row counts that must divide into 16*wr-row tiles.
+bool choose_split(int K, int rowsA, int rowsB, int& wk, int& wr) {
+  const int cands[4] = {8, 4, 2, 1};
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int c : cands) {
+      const int r = 8 / c;
+      if (K % (c * 32)) continue;
+      if (rowsA % (16 * r) || (rowsB && rowsB % (16 * r))) continue;
+      if (pass == 0 && K / (c * 32) < 8) continue;  // prefer two or more 16-byte units per lane
+      wk = c;
+      wr = r;
+      return true;
+    }
+  }
+  return false;
+}
+
+int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* y, void* ws, size_t ws_bytes,
+                            cudaStream_t stream) {
+  const int maxT = ws_max_tokens(L, ws_bytes);
+  const Layout lo = make_layout(L, maxT);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  const int H = L->hidden, I = L->inter, Is = L->shared_fmt ? L->shared_inter : 0;
+
+  RouterArgs ra;
+  ra.H = H; ra.E = L->n_experts; ra.k = L->top_k; ra.T = T;
+  ra.x = static_cast<const uint16_t*>(x);
+  ra.w = L->router_w;
+  ra.bias = L->router_bias;
+  ra.rb = route_bufs(lo, ws);
+  std::memset(&ra.out, 0, sizeof(ra.out));
+
+  ExpertArgs ea;
+  std::memset(&ea, 0, sizeof(ea));
+  ea.H = H; ea.I = I; ea.E = L->n_experts; ea.k = L->top_k; ea.T = T;
+  ea.fmt = L->fmt; ea.sfmt = L->shared_fmt; ea.Is = Is;
+  ea.x = ra.x;
+  ea.gate = qw(L->gate, L->fmt); ea.up = qw(L->up, L->fmt); ea.down = qw(L->down, L->fmt);
+  if (L->shared_fmt) {
+    ea.sgate = qw(L->shared_gate, L->shared_fmt);
+    ea.sup = qw(L->shared_up, L->shared_fmt);
+    ea.sdown = qw(L->shared_down, L->shared_fmt);
+  }
+  ea.rb = ra.rb;
+  ea.h = reinterpret_cast<uint16_t*>(b + lo.h);
+  ea.hs = reinterpret_cast<uint16_t*>(b + lo.hs);
+  ea.P = reinterpret_cast<float*>(b + lo.P);
+  ea.S = reinterpret_cast<float*>(b + lo.S);
+  ea.rb_cnt = reinterpret_cast<uint32_t*>(b + lo.rb_cnt);
+  ea.y = static_cast<uint16_t*>(y);
+  if (!choose_split(H, I, Is, ea.wk_gu, ea.wr_gu)) return MOE_ERR_UNSUPPORTED;
+  const int Kd = Is ? (I < Is ? I : Is) : I;
+  if (!choose_split(Kd, H, 0, ea.wk_dn, ea.wr_dn)) return MOE_ERR_UNSUPPORTED;
+  if (I % (ea.wk_dn * 32) || (Is && Is % (ea.wk_dn * 32))) return MOE_ERR_UNSUPPORTED;
+  ea.xs_tok_stride = H + 16;
+  ea.xs_q_stride = 0;
+  const int Kmax = Is > I ? Is : I;
+  ea.hs_tok_stride = Kmax + 16;
+  ea.hs_q_stride = 0;
+
+  const size_t smem_gu = (size_t)(T + 1) * ea.xs_tok_stride * 2 + (size_t)(kExpertThreads / 32) * 2 * 32 * 4 * 4;
+  const size_t smem_dn = (size_t)9 * ea.hs_tok_stride * 2 + (size_t)(kExpertThreads / 32) * 32 * 4 * 4;
+  if (smem_gu > 220 * 1024 || smem_dn > 220 * 1024) return MOE_ERR_UNSUPPORTED;
+
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+  int smem_sm = 0;
+  cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  auto per_sm = [&](size_t smem) {
+    int n = (int)((size_t)smem_sm / (smem + 1024));
+    return n < 1 ? 1 : (n > 2 ? 2 : n);
+  };
+
+  cudaError_t err = launch_router_decode(ra, stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  err = launch_gateup_decode(ea, sms * per_sm(smem_gu), smem_gu, stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  err = launch_down_decode(ea, sms * per_sm(smem_dn), smem_dn, stream);
+  return cuda_status(err);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int32_t status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape or format combination not supported";
+    case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED: device pointer not aligned";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing or too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA runtime error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a bounded device-side wait gave up";
+    case MOE_ERR_DEVICE_BAD_INDEX: return "MOE_ERR_DEVICE_BAD_INDEX: device-side index check failed";
+    default: return "unknown moe_status";
+  }
+}
+
+size_t moe_workspace_size(const moe_layer* layer, int32_t max_tokens, const moe_options* opts) {
+  if (check_layer(layer) != MOE_OK || check_options(opts) != MOE_OK || max_tokens < 1) return 0;
+  return make_layout(layer, max_tokens).total;
+}
+
+int32_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws || ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_MISALIGNED;
+  // control block plus every counter section: zero the whole workspace once
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_workspace_layout(const moe_layer* layer, int32_t max_tokens, const moe_options* opts,
+                             moe_ws_layout* out) {
+  int32_t st = check_layer(layer);
+  if (st != MOE_OK) return st;
+  if ((st = check_options(opts)) != MOE_OK) return st;
+  if (!out || max_tokens < 1) return MOE_ERR_INVALID_ARG;
+  const Layout lo = make_layout(layer, max_tokens);
+  out->logits = lo.logits;
+  out->topk_idx = lo.topk_idx;
+  out->topk_w = lo.topk_w;
+  out->expert_cnt = lo.cnt;
+  out->expert_off = lo.off;
+  out->pair_list = lo.pair;
+  out->total = lo.total;
+  return MOE_OK;
+}
+
+int32_t moe_route(const moe_layer* layer, const void* x, int32_t T, int32_t* topk_idx, float* topk_w,
+                  int32_t* expert_cnt, int32_t* expert_off, int32_t* pair_list, void* ws, size_t ws_bytes,
+                  moe_stream_t stream) {
+  int32_t st = check_layer(layer);
+  if (st != MOE_OK) return st;
+  if (!x) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x)) return MOE_ERR_MISALIGNED;
+  if (T < 1) return MOE_ERR_INVALID_ARG;
+  if (T > MOE_DECODE_MAX_TOKENS) return MOE_ERR_UNSUPPORTED;
+  const void* outs[5] = {topk_idx, topk_w, expert_cnt, expert_off, pair_list};
+  for (const void* p : outs)
+    if (p && !aligned4(p)) return MOE_ERR_MISALIGNED;
+  if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
+  const int maxT = ws_max_tokens(layer, ws_bytes);
+  const Layout lo = make_layout(layer, maxT);
+  RouterArgs ra;
+  ra.H = layer->hidden; ra.E = layer->n_experts; ra.k = layer->top_k; ra.T = T;
+  ra.x = static_cast<const uint16_t*>(x);
+  ra.w = layer->router_w;
+  ra.bias = layer->router_bias;
+  ra.rb = route_bufs(lo, ws);
+  ra.out.topk_idx = topk_idx; ra.out.topk_w = topk_w; ra.out.cnt = expert_cnt; ra.out.off = expert_off;
+  ra.out.pair = pair_list;
+  if ((size_t)T * layer->hidden * 2 > 200 * 1024) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_router_decode(ra, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_decode_forward(const moe_layer* layer, const void* x, int32_t T, void* y, const moe_options* opts,
+                           void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int32_t st = check_layer(layer);
+  if (st != MOE_OK) return st;
+  if ((st = check_options(opts)) != MOE_OK) return st;
+  if (opts && opts->act_quant) return MOE_ERR_UNSUPPORTED;
+  if (!x || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return MOE_ERR_MISALIGNED;
+  if (T < 1) return MOE_ERR_INVALID_ARG;
+  if (T > MOE_DECODE_MAX_TOKENS) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
+  if ((size_t)T * layer->hidden * 2 > 200 * 1024) return MOE_ERR_UNSUPPORTED;
+  return decode_forward_impl(layer, x, T, y, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int32_t moe_prefill_forward(const moe_layer* layer, const void* x, int32_t T, void* y, const moe_options* opts,
+                            void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int32_t st = check_layer(layer);
+  if (st != MOE_OK) return st;
+  if ((st = check_options(opts)) != MOE_OK) return st;
+  if (!x || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return MOE_ERR_MISALIGNED;
+  if (T < 1) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
+  (void)stream;
+  return MOE_ERR_UNSUPPORTED;
+}
+
+int32_t moe_check(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws || ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  Ctrl c;
+  if (cudaMemcpy(&c, ws, sizeof(Ctrl), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (c.error == 0) return MOE_OK;
+  const uint32_t zero[2] = {0, 0};
+  if (cudaMemcpy(ws, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+  return (int32_t)c.error;
+}
+
+int32_t moe_dequantize(int32_t fmt, const moe_qweight* w, int32_t N, int32_t K, int32_t expert, int32_t row0,
+                       int32_t nrows, float* out, moe_stream_t stream) {
+  if (!w || !out || !valid_fmt(fmt)) return MOE_ERR_INVALID_ARG;
+  int32_t st = check_qweight(*w, fmt, N, K);
+  if (st != MOE_OK) return st;
+  if (!aligned16(out)) return MOE_ERR_MISALIGNED;
+  if (expert < 0 || row0 < 0 || nrows < 1 || row0 + nrows > N) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_dequantize(fmt, qw(*w, fmt), N, K, expert, row0, nrows, out,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_quantize_act_nvfp4(const void* x, int32_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
+                               moe_stream_t stream) {
+  if (!x || !codes || !scales || rows < 1 || K < 16 || K % 16) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(codes) & 7)) return MOE_ERR_MISALIGNED;
+  return cuda_status(launch_quantize_act_nvfp4(static_cast<const uint16_t*>(x), rows, K, codes, scales,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,127 @@
+"""Helpers shared by the GPU tests: build once, cache synthetic layers, run the
+C ABI on device buffers and bring results back as numpy arrays."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import torch
+
+import synth
+from quantized_moe_decode_router_gb300 import _binding as B
+from quantized_moe_decode_router_gb300 import build as qbuild
+from quantized_moe_decode_router_gb300.device import to_device
+
+
+@functools.lru_cache(maxsize=1)
+def lib():
+    qbuild.build()
+    return B.load()
+
+
+@functools.lru_cache(maxsize=6)
+def host_layer(name: str, seed: int = 0):
+    return synth.make_layer(synth.CONFIGS[name], seed)
+
+
+_dev_cache = {}
+
+
+def device_layer(name: str, seed: int = 0):
+    key = (name, seed)
+    if key not in _dev_cache:
+        if len(_dev_cache) >= 2:
+            _dev_cache.clear()
+            torch.cuda.empty_cache()
+        _dev_cache[key] = to_device(host_layer(name, seed))
+    return _dev_cache[key]
+
+
+def x_device(x_bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).cuda()
+
+
+def new_ws(layer, T: int, act_quant: int = 0) -> torch.Tensor:
+    n = B.workspace_size(layer, T, act_quant)
+    assert n > 0
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    B.workspace_init(ws)
+    return ws
+
+
+def ws_read(ws: torch.Tensor, off: int, dtype, count: int) -> np.ndarray:
+    nbytes = np.dtype(dtype).itemsize * count
+    return ws[off:off + nbytes].cpu().numpy().view(dtype).copy()
+
+
+def decode(layer, x_bits: np.ndarray, ws=None, prefill: bool = False, act_quant: int = 0):
+    """Run one forward call; returns (y bits uint16 [T, H], routing dict read from the workspace)."""
+    T, H = x_bits.shape
+    if ws is None:
+        ws = new_ws(layer, T, act_quant)
+    x = x_device(x_bits)
+    y = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+    if prefill:
+        B.moe_prefill_forward(layer, x, T, y, ws, act_quant=act_quant)
+    else:
+        B.moe_decode_forward(layer, x, T, y, ws, act_quant=act_quant)
+    torch.cuda.synchronize()
+    assert B.moe_check(ws) == 0
+    maxT = _ws_tokens(layer, ws)
+    lo = B.workspace_layout(layer, maxT, act_quant)
+    E, k = layer.n_experts, layer.top_k
+    routing = {
+        "logits": ws_read(ws, lo.logits, np.float32, T * E).reshape(T, E),
+        "topk_idx": ws_read(ws, lo.topk_idx, np.int32, T * k).reshape(T, k),
+        "topk_w": ws_read(ws, lo.topk_w, np.float32, T * k).reshape(T, k),
+        "expert_cnt": ws_read(ws, lo.expert_cnt, np.int32, E),
+        "expert_off": ws_read(ws, lo.expert_off, np.int32, E + 1),
+        "pair_list": ws_read(ws, lo.pair_list, np.int32, T * k),
+    }
+    return y.cpu().numpy().view(np.uint16), routing
+
+
+def _ws_tokens(layer, ws) -> int:
+    n = ws.numel()
+    lo, hi = 1, 1
+    while B.workspace_size(layer, hi * 2) <= n and hi < (1 << 22):
+        hi *= 2
+    lo = hi
+    hi = hi * 2
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if B.workspace_size(layer, mid) <= n:
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
+def route(layer, x_bits: np.ndarray):
+    T = x_bits.shape[0]
+    E, k = layer.n_experts, layer.top_k
+    ws = new_ws(layer, T)
+    x = x_device(x_bits)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    cnt = torch.empty(E, dtype=torch.int32, device="cuda")
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    pair = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    B.moe_route(layer, x, T, idx, w, cnt, off, pair, ws)
+    torch.cuda.synchronize()
+    lo = B.workspace_layout(layer, T)
+    logits = ws_read(ws, lo.logits, np.float32, T * E).reshape(T, E)
+    return {"logits": logits, "topk_idx": idx.cpu().numpy(), "topk_w": w.cpu().numpy(),
+            "expert_cnt": cnt.cpu().numpy(), "expert_off": off.cpu().numpy(), "pair_list": pair.cpu().numpy()}
+
+
+def assert_routing_matches(got: dict, ref: dict, near: np.ndarray):
+    """Bit-exact indices and dispatch; logits exact except oracle-flagged near-midpoint ones."""
+    lg, lr = got["logits"], ref["logits"]
+    diff = lg.view(np.uint32) != lr.view(np.uint32)
+    assert not np.any(diff & ~near), f"{int(np.sum(diff & ~near))} logits differ from the correctly rounded value"
+    np.testing.assert_array_equal(got["topk_idx"], ref["topk_idx"])
+    np.testing.assert_array_equal(got["expert_cnt"], ref["expert_cnt"])
+    np.testing.assert_array_equal(got["expert_off"], ref["expert_off"])
+    np.testing.assert_array_equal(got["pair_list"], ref["pair_list"])
+    np.testing.assert_allclose(got["topk_w"], ref["topk_w"], rtol=8 * 2.0 ** -24, atol=2.0 ** -30)
