@@ -143,15 +143,16 @@ int ws_max_tokens(const moe_layer* L, size_t ws_bytes) {
 int32_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // Warp split (wk along K, wr along rows; wk * wr = 8) for matrices with
-// reduction length K and row counts that must divide into 16*wr-row tiles.
-bool choose_split(int K, int rowsA, int rowsB, int& wk, int& wr) {
+// reduction length K, decode unit width unitK (the larger of the formats
+// involved) and row counts that must divide into 16*wr-row tiles.
+bool choose_split(int K, int unitK, int rowsA, int rowsB, int& wk, int& wr) {
   const int cands[4] = {8, 4, 2, 1};
   for (int pass = 0; pass < 2; ++pass) {
     for (int c : cands) {
       const int r = 8 / c;
-      if (K % (c * 32)) continue;
+      if (K % (c * unitK)) continue;
       if (rowsA % (16 * r) || (rowsB && rowsB % (16 * r))) continue;
-      if (pass == 0 && K / (c * 32) < 8) continue;  // prefer two or more 16-byte units per lane
+      if (pass == 0 && K / (c * unitK) < 2) continue;  // prefer two or more units per warp
       wk = c;
       wr = r;
       return true;
@@ -193,10 +194,12 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   ea.S = reinterpret_cast<float*>(b + lo.S);
   ea.rb_cnt = reinterpret_cast<uint32_t*>(b + lo.rb_cnt);
   ea.y = static_cast<uint16_t*>(y);
-  if (!choose_split(H, I, Is, ea.wk_gu, ea.wr_gu)) return MOE_ERR_UNSUPPORTED;
+  int uk = decode_unit_k(L->fmt);
+  if (Is && decode_unit_k(L->shared_fmt) > uk) uk = decode_unit_k(L->shared_fmt);
+  if (!choose_split(H, uk, I, Is, ea.wk_gu, ea.wr_gu)) return MOE_ERR_UNSUPPORTED;
   const int Kd = Is ? (I < Is ? I : Is) : I;
-  if (!choose_split(Kd, H, 0, ea.wk_dn, ea.wr_dn)) return MOE_ERR_UNSUPPORTED;
-  if (I % (ea.wk_dn * 32) || (Is && Is % (ea.wk_dn * 32))) return MOE_ERR_UNSUPPORTED;
+  if (!choose_split(Kd, uk, H, 0, ea.wk_dn, ea.wr_dn)) return MOE_ERR_UNSUPPORTED;
+  if (I % (ea.wk_dn * uk) || (Is && Is % (ea.wk_dn * uk))) return MOE_ERR_UNSUPPORTED;
   ea.xs_tok_stride = H + 16;
   ea.xs_q_stride = 0;
   const int Kmax = Is > I ? Is : I;

@@ -31,12 +31,22 @@ namespace {
 constexpr int kMaxT = MOE_DECODE_MAX_TOKENS;
 constexpr int kWarps = kExpertThreads / 32;
 
+// Per-format work unit.  The four lanes c = 0..3 of a row group always work
+// inside one unit of kUnitK consecutive columns, lane c on its chunk of
+// kChunkBytes bytes at byte offset c * kChunkBytes.  An m16n8k16 MMA reduces
+// over K across those four lanes, so a unit never spans two scale blocks
+// whose scale is applied after the MMA: MXFP4 units are one 32-element
+// block, int4/int8 units one 64-element group, FP8 units lie inside one
+// 128x128 block.  NVFP4 folds its 16-element block scales into the f16
+// weights before the MMA, so its units may span several blocks.
 template <int F> struct Fm;
-template <> struct Fm<MOE_FMT_NVFP4> { static constexpr int kBits = 4, kUnitK = 32; };
-template <> struct Fm<MOE_FMT_MXFP4> { static constexpr int kBits = 4, kUnitK = 32; };
-template <> struct Fm<MOE_FMT_INT4_G64> { static constexpr int kBits = 4, kUnitK = 32; };
-template <> struct Fm<MOE_FMT_INT8_G64> { static constexpr int kBits = 8, kUnitK = 16; };
-template <> struct Fm<MOE_FMT_FP8_B128> { static constexpr int kBits = 8, kUnitK = 16; };
+template <> struct Fm<MOE_FMT_NVFP4> { static constexpr int kBits = 4, kChunkBytes = 16, kPrefetch = 2; };
+template <> struct Fm<MOE_FMT_MXFP4> { static constexpr int kBits = 4, kChunkBytes = 4, kPrefetch = 8; };
+template <> struct Fm<MOE_FMT_INT4_G64> { static constexpr int kBits = 4, kChunkBytes = 8, kPrefetch = 4; };
+template <> struct Fm<MOE_FMT_INT8_G64> { static constexpr int kBits = 8, kChunkBytes = 16, kPrefetch = 2; };
+template <> struct Fm<MOE_FMT_FP8_B128> { static constexpr int kBits = 8, kChunkBytes = 16, kPrefetch = 2; };
+template <int F> constexpr int unit_k() { return 4 * Fm<F>::kChunkBytes * 8 / Fm<F>::kBits; }
+template <int F> constexpr int chunk_k() { return Fm<F>::kChunkBytes * 8 / Fm<F>::kBits; }
 
 // One expert matrix W[N, K] seen by a warp.
 struct Mat {
@@ -53,7 +63,7 @@ __device__ __forceinline__ Mat mat_of(const QW& w, int fmt, int e, int N, int K)
   return m;
 }
 
-// The raw scale bits a 16-byte unit of row R starting at column k needs.
+// The raw scale bits of row R that lane chunk starting at column k needs.
 template <int F>
 __device__ __forceinline__ uint32_t load_scale(const Mat& m, int R, int k) {
   if constexpr (F == MOE_FMT_NVFP4) return ldg_nc_u16(m.scales + (size_t)R * (m.K / 16) + k / 16);
@@ -72,21 +82,30 @@ __device__ __forceinline__ float unit_scale(uint32_t s) {
 
 template <int NM>
 struct Unit {
-  uint4 d[NM][2];      // rows r and r+8
+  uint4 d[NM][2];      // this lane's chunk of rows r and r+8 (only the first kChunkBytes used)
   uint32_t s[NM][2];
 };
 
 template <int F, int NM>
-__device__ __forceinline__ void load_unit(Unit<NM>& u, const Mat (&m)[NM], int R0, int k) {
-  constexpr int kB = Fm<F>::kBits;
+__device__ __forceinline__ void load_unit(Unit<NM>& u, const Mat (&m)[NM], int R0, int kc) {
+  constexpr int kB = Fm<F>::kBits, kC = Fm<F>::kChunkBytes;
 #pragma unroll
   for (int i = 0; i < NM; ++i) {
     const size_t rb = (size_t)m[i].K * kB / 8;
-    const uint8_t* p0 = m[i].data + (size_t)R0 * rb + (size_t)k * kB / 8;
-    u.d[i][0] = ldg_nc_v4(p0);
-    u.d[i][1] = ldg_nc_v4(p0 + 8 * rb);
-    u.s[i][0] = load_scale<F>(m[i], R0, k);
-    u.s[i][1] = load_scale<F>(m[i], R0 + 8, k);
+    const uint8_t* p0 = m[i].data + (size_t)R0 * rb + (size_t)kc * kB / 8;
+    if constexpr (kC == 16) {
+      u.d[i][0] = ldg_nc_v4(p0);
+      u.d[i][1] = ldg_nc_v4(p0 + 8 * rb);
+    } else if constexpr (kC == 8) {
+      const uint2 a = ldg_nc_v2(p0), b = ldg_nc_v2(p0 + 8 * rb);
+      u.d[i][0] = make_uint4(a.x, a.y, 0, 0);
+      u.d[i][1] = make_uint4(b.x, b.y, 0, 0);
+    } else {
+      u.d[i][0] = make_uint4(ldg_nc_u32(p0), 0, 0, 0);
+      u.d[i][1] = make_uint4(ldg_nc_u32(p0 + 8 * rb), 0, 0, 0);
+    }
+    u.s[i][0] = load_scale<F>(m[i], R0, kc);
+    u.s[i][1] = load_scale<F>(m[i], R0 + 8, kc);
   }
 }
 
@@ -94,11 +113,12 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// MMA over one 16-byte unit (per row) of NM matrices.  xl: this lane's
-// activations (f16) at the unit's first column.
+// MMA over one unit of NM matrices; xl: this lane's activations (f16) at its
+// chunk's first column.  Every lane of the warp executes every MMA.
 template <int F, int NM>
 __device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl, float (&acc)[NM][4]) {
-  if constexpr (F == MOE_FMT_NVFP4 || F == MOE_FMT_MXFP4 || F == MOE_FMT_INT4_G64) {
+  if constexpr (Fm<F>::kBits == 4) {
+    constexpr int kWords = Fm<F>::kChunkBytes / 4;  // 8 columns per word
     float d[NM][4];
     uint32_t s2[NM][2][2];
 #pragma unroll
@@ -114,7 +134,7 @@ __device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl
       }
     }
 #pragma unroll
-    for (int wd = 0; wd < 4; ++wd) {
+    for (int wd = 0; wd < kWords; ++wd) {
       const uint4 xv = *reinterpret_cast<const uint4*>(xl + wd * 8);  // x[k .. k+8) as f16 pairs
       uint32_t bA0, bA1, bB0, bB1;
       if constexpr (F == MOE_FMT_INT4_G64) {
@@ -164,7 +184,7 @@ __device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl
       }
     }
   } else {
-    // 8-bit codes: a unit is 16 columns = four words of four codes
+    // 8-bit codes: a 16-byte chunk is 16 columns = four words of four codes
     float d[NM][4];
 #pragma unroll
     for (int i = 0; i < NM; ++i)
@@ -198,34 +218,30 @@ __device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl
   }
 }
 
-// One warp: rows [row0, row0 + 16) of NM matrices over columns [kb, kb + Kw).
-// Lane (r = lane/4, c = lane%4) takes rows r and r+8 and the 16-byte units
-// c, c+4, c+8, ... of the range; the four lanes of a row read 64 contiguous
-// bytes per load instruction.  xrow: this lane's token row (f16) in shared
-// memory, indexed by absolute column.
-constexpr int kPrefetch = 2;
-
+// One warp: rows [row0, row0 + 16) of NM matrices over columns [kb, kb + Kw),
+// Kw a multiple of the unit.  Lane (r = lane/4, c = lane%4) takes rows r and
+// r+8 and chunk c of every unit; units stream through a register ring of
+// kPrefetch entries.  The trip count is the same for every lane (mma.sync
+// needs the whole warp).  xrow: this lane's token row (f16) in shared memory.
 template <int F, int NM>
 __device__ __forceinline__ void warp_tile(const Mat (&m)[NM], int row0, int kb, int Kw, const __half* xrow,
                                           float (&acc)[NM][4]) {
-  constexpr int UK = Fm<F>::kUnitK;
+  constexpr int UK = unit_k<F>(), CK = chunk_k<F>(), PF = Fm<F>::kPrefetch;
   const int lane = threadIdx.x & 31;
   const int R0 = row0 + (lane >> 2);
-  const int c = lane & 3;
-  const int nU = Kw / UK;                       // units in the warp's range
-  const int nL = (nU - c + 3) / 4;              // units of this lane
-  Unit<NM> buf[kPrefetch];
+  const int koff = kb + (lane & 3) * CK;
+  const int nU = Kw / UK;
+  Unit<NM> buf[PF];
 #pragma unroll
-  for (int p = 0; p < kPrefetch; ++p)
-    if (p < nL) load_unit<F, NM>(buf[p], m, R0, kb + (4 * p + c) * UK);
-  for (int i0 = 0; i0 < nL; i0 += kPrefetch) {
+  for (int p = 0; p < PF; ++p)
+    if (p < nU) load_unit<F, NM>(buf[p], m, R0, koff + p * UK);
+  for (int u0 = 0; u0 < nU; u0 += PF) {
 #pragma unroll
-    for (int p = 0; p < kPrefetch; ++p) {
-      const int i = i0 + p;
-      if (i < nL) {
-        const int k = kb + (4 * i + c) * UK;
-        compute_unit<F, NM>(buf[p], xrow + k, acc);
-        if (i + kPrefetch < nL) load_unit<F, NM>(buf[p], m, R0, kb + (4 * (i + kPrefetch) + c) * UK);
+    for (int p = 0; p < PF; ++p) {
+      const int u = u0 + p;
+      if (u < nU) {
+        compute_unit<F, NM>(buf[p], xrow + koff + u * UK, acc);
+        if (u + PF < nU) load_unit<F, NM>(buf[p], m, R0, koff + (u + PF) * UK);
       }
     }
   }

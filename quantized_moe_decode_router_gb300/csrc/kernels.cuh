@@ -94,14 +94,15 @@ __host__ __device__ inline size_t scale_bytes(int fmt, int N, int K) {
   }
 }
 
-// Scale-block length along K (the lane-quarter K range must be a multiple).
-__host__ __device__ inline int block_k(int fmt) {
+// Columns of one decode work unit (four lanes' chunks) in a format; a warp's
+// share of K must be a multiple of it.
+__host__ __device__ inline int decode_unit_k(int fmt) {
   switch (fmt) {
-    case MOE_FMT_NVFP4: return 32;   // one 16-byte unit holds two 16-element blocks
+    case MOE_FMT_NVFP4: return 128;
     case MOE_FMT_MXFP4: return 32;
     case MOE_FMT_INT4_G64: return 64;
     case MOE_FMT_INT8_G64: return 64;
-    case MOE_FMT_FP8_B128: return 128;
+    case MOE_FMT_FP8_B128: return 64;
     default: return 0;
   }
 }
