@@ -1,0 +1,376 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized MoE layer on GB300.
+
+One step = one MoE-layer forward at decode batch size (router + top-k,
+dispatch, gate/up + SwiGLU, down, combine) on the NVFP4 decode layer:
+hidden 2048, 512 routed experts, top-10, intermediate 512, FP8 block-128
+shared expert (intermediate 512).  The headline value is algorithmic weight
+bytes per second at batch 8 (the bytes of the router, the shared expert and
+every distinct routed expert the batch touches, each read once); per-batch
+results for 1, 4 and 8 tokens ride along.
+
+Synthetic inputs: N(0, 0.02) FP32 weights quantised per format, N(0, 1) BF16
+activations, seeded.  L2 is defeated by rotating R copies of the layer (each
+at its own addresses) so one rotation touches at least three times the L2
+size, and by a new token batch every step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the FP64 CPU oracle (the reference implementation of
+this build) on the same workload and metric.  With N > 1 (torchrun), every
+rank runs an independent replica (the layer does not shard across ranks in
+this build); value sums the ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer weight GB/s & tokens/s at batch 1/8; % of HBM (decode) / FP4 peak"
+WORKLOAD = "decode_nvfp4"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def _once(self):
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                  "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
+            if out.returncode == 0:
+                self.rows.append(out.stdout.strip())
+        except Exception:
+            pass
+
+    def start(self):
+        self._once()
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append(line.strip())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        self._once()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _bytes_per_call(host, cnt_rows):
+    """Algorithmic weight bytes of one call from its per-expert pair counts."""
+    per_expert = host.expert_bytes()
+    fixed = host.router_bytes() + host.shared_bytes()
+    return [fixed + int(np.count_nonzero(c)) * per_expert for c in cnt_rows]
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import quantized_moe_decode_router_gb300 as q
+    from quantized_moe_decode_router_gb300 import build as qbuild
+
+    qbuild.build()
+    q.load()
+    torch.cuda.set_device(local)
+    dev_name = torch.cuda.get_device_name(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cfg = synth.CONFIGS[args.workload]
+    t0 = time.time()
+    host = synth.make_layer(cfg, seed=rank)
+    gen_s = time.time() - t0
+    base = q.to_device(host, f"cuda:{local}")
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    batches = [int(b) for b in args.batches.split(",")]
+    Tmax = max(batches)
+    fixed = host.router_bytes() + host.shared_bytes()
+    min_call = fixed + min(cfg.k, cfg.E) * host.expert_bytes()
+    R = args.instances or max(2, -(-3 * l2 // min_call))
+    layers = [base]
+
+    def clone(qw):
+        return q.QWeight(qw.data.clone(), qw.scales.clone(),
+                         None if qw.tensor_scale is None else qw.tensor_scale.clone())
+    for _ in range(R - 1):
+        L = q.Layer(base.hidden, base.inter, base.n_experts, base.top_k, base.fmt, base.router_w.clone(),
+                    None if base.router_bias is None else base.router_bias.clone(), clone(base.gate),
+                    clone(base.up), clone(base.down), base.shared_fmt, base.shared_inter,
+                    clone(base.shared_gate) if base.shared_gate else None,
+                    clone(base.shared_up) if base.shared_up else None,
+                    clone(base.shared_down) if base.shared_down else None)
+        layers.append(L)
+    NB = args.token_batches
+    stream = torch.cuda.Stream()
+    results = {}
+    peak, peak_kind = _peaks()
+    clocks = None
+    roof = None
+    e2e = None
+    for T in batches:
+        xs = [torch.from_numpy(synth.make_tokens(cfg, T, seed=1000 + rank, batch=i).view(np.int16)).cuda()
+              for i in range(NB)]
+        ys = torch.zeros((T, cfg.H), dtype=torch.int16, device="cuda")
+        ws = torch.empty(q.workspace_size(base, Tmax), dtype=torch.uint8, device="cuda")
+        q.workspace_init(ws)
+        # per-batch routing (the library's own) -> distinct experts -> algorithmic bytes
+        cnt = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
+        cnts = []
+        for i in range(NB):
+            q.moe_route(base, xs[i], T, expert_cnt=cnt, ws=ws)
+            cnts.append(cnt.cpu().numpy().copy())
+        bytes_b = _bytes_per_call(host, cnts)
+        torch.cuda.synchronize()
+
+        def call(i, s=None):
+            q.moe_decode_forward(layers[i % R], xs[i % NB], T, ys, ws, stream=s)
+
+        # capture one graph of G calls (rotating instances and batches); replay it
+        G = min(512, -(-max(R, NB) // R) * R)   # a whole number of rotations, >= NB batches
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                call(i, stream)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(G):
+                    call(i, stream)
+        bytes_graph = sum(bytes_b[i % NB] for i in range(G))
+        steps = args.steps if T == batches[-1] else max(G, args.steps // 4)
+        reps = max(1, steps // G)
+        steps = reps * G
+        warm = max(1, args.warmup // G)
+        for _ in range(warm):
+            g.replay()
+        torch.cuda.synchronize()
+        headline = T == batches[-1]
+        sampler = ClockSampler(local) if headline else None
+        if sampler:
+            sampler.start()
+            time.sleep(0.3)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        ms = ev0.elapsed_time(ev1)
+        if sampler:
+            clocks = sampler.stop()
+        if dist:
+            t = torch.tensor([ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+            tb = torch.tensor([float(bytes_graph * reps)], device="cuda", dtype=torch.float64)
+            dist.all_reduce(tb)
+            total_bytes = float(tb.item())
+        else:
+            total_bytes = float(bytes_graph * reps)
+        us_call = ms * 1e3 / steps
+        gbs = total_bytes / (ms * 1e-3) / 1e9
+        toks = world * T * steps / (ms * 1e-3)
+        results[T] = {"us_per_layer": round(us_call, 3), "weight_GBps": round(gbs, 1),
+                      "tokens_per_s": round(toks, 1), "hbm_frac": round(gbs / world / peak, 4),
+                      "bytes_per_layer": int(np.mean(bytes_b)), "steps": steps}
+        # dominant kernel (gate/up): live CUDA-event timing of each kernel on the launch stream
+        if headline:
+            n = min(256, max(32, steps // 8))
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+            with torch.cuda.stream(stream):
+                for i in range(n):
+                    q.moe_decode_forward_timed(layers[i % R], xs[i % NB], T, ys, ws, evs[i], stream=stream)
+            torch.cuda.synchronize()
+            dur = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)] for i in range(n)])
+            avg = dur.mean(axis=0) * 1e3  # us per launch: router, gate/up, down
+            per_exp_gu = sum(m.nbytes() // m.E for m in (host.gate, host.up))
+            s_gu = (host.shared_gate.nbytes() + host.shared_up.nbytes()) if host.shared_gate else 0
+            gu_bytes = np.mean([int(np.count_nonzero(cnts[i % NB])) * per_exp_gu + s_gu for i in range(n)])
+            ach = gu_bytes / (avg[1] * 1e-6) / 1e9
+            roof = {"kernel": "gateup_decode_kernel", "bound": "hbm", "achieved": round(ach, 1),
+                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(ach / peak, 4),
+                    "traffic": None, "bytes_per_launch": int(gu_bytes),
+                    "kernel_us": {"router": round(avg[0], 3), "gateup": round(avg[1], 3), "down": round(avg[2], 3)}}
+            # end to end through the public API with host buffers (pinned), one call per step
+            ne = min(steps, args.e2e_steps)
+            xh = [torch.from_numpy(synth.make_tokens(cfg, T, seed=2000 + rank, batch=i).view(np.int16)).pin_memory()
+                  for i in range(min(NB, ne))]
+            yh = torch.empty((T, cfg.H), dtype=torch.int16).pin_memory()
+            xd = torch.empty((T, cfg.H), dtype=torch.int16, device="cuda")
+            for i in range(3):
+                xd.copy_(xh[i % len(xh)], non_blocking=True)
+                q.moe_decode_forward(layers[i % R], xd, T, ys, ws)
+                yh.copy_(ys, non_blocking=True)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for i in range(ne):
+                xd.copy_(xh[i % len(xh)], non_blocking=True)
+                q.moe_decode_forward(layers[i % R], xd, T, ys, ws)
+                yh.copy_(ys, non_blocking=True)
+            e1.record()
+            torch.cuda.synchronize()
+            ems = e0.elapsed_time(e1)
+            eb = sum(bytes_b[i % NB] for i in range(ne))
+            e2e = {"value": round(eb / (ems * 1e-3) / 1e9, 1), "unit": "GB/s", "steps": ne,
+                   "us_per_step": round(ems * 1e3 / ne, 2), "tokens_per_s": round(T * ne / (ems * 1e-3), 1),
+                   "h2d_bytes_per_step": T * cfg.H * 2, "d2h_bytes_per_step": T * cfg.H * 2}
+        del g
+        torch.cuda.synchronize()
+    st = q.moe_check(ws)
+    if st != 0:
+        raise RuntimeError(f"device-side error: {q.status_string(st)}")
+    Th = batches[-1]
+    head = results[Th]
+    out = {
+        "metric": METRIC, "value": head["weight_GBps"], "unit": "GB/s", "n_gpus": world,
+        "steps": head["steps"], "warmup": args.warmup, "ms_per_step": round(head["us_per_layer"] / 1e3, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) weights quantised NVFP4 / FP8 b128; N(0,1) bf16 tokens)",
+        "config": {"workload": f"{cfg.name}: NVFP4 MoE layer H={cfg.H} E={cfg.E} top-{cfg.k} I={cfg.I} "
+                               f"+ FP8 b128 shared expert I={cfg.shared_I}, batch {Th} tokens",
+                   "batch_tokens": Th, "instances_rotated": R,
+                   "l2": f"inputs larger than L2: {R} layer copies rotated, "
+                         f"{R * min_call / 1e6:.0f} MB touched per rotation vs L2 {l2 / 1e6:.0f} MB",
+                   "graph": f"CUDA graph of {G} layer calls replayed", "parallelism": "replicas" if world > 1 else "1 GPU",
+                   "gpu": dev_name, "layer_gen_s": round(gen_s, 1)},
+        "tokens_per_s": head["tokens_per_s"], "hbm_frac": head["hbm_frac"],
+        "batches": {str(T): r for T, r in results.items()},
+        "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": 3 * head["steps"],
+    }
+    return out
+
+
+def run_cpu_baseline(args, seconds_budget: float = 20.0):
+    """The oracle, as it stands, on a bounded sample of the workload (rank 0 only)."""
+    from oracle import moe as M
+    cfg = synth.CONFIGS[args.workload]
+    T = max(int(b) for b in args.batches.split(","))
+    host = synth.make_layer(cfg, seed=0)
+    n = 0
+    byts = 0
+    t0 = time.time()
+    while True:
+        x = synth.make_tokens(cfg, T, seed=3000, batch=n)
+        ref = M.layer_forward(host, x)
+        byts += host.router_bytes() + host.shared_bytes() + int(np.count_nonzero(ref["expert_cnt"])) * \
+            host.expert_bytes()
+        n += 1
+        if time.time() - t0 > seconds_budget or n >= args.cpu_batches:
+            break
+    dt = time.time() - t0
+    cores = len(os.sched_getaffinity(0))
+    return {"value": round(byts / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} layer calls of {T} tokens on {cfg.name} (FP64 numpy oracle, BLAS threads = {cores}, "
+                      f"decode single-threaded)", "seconds": round(dt, 2), "tokens_per_s": round(n * T / dt, 2)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4096)
+    ap.add_argument("--warmup", type=int, default=512)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--batches", default="1,4,8")
+    ap.add_argument("--instances", type=int, default=0)
+    ap.add_argument("--token-batches", type=int, default=64)
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-batches", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cb = run_cpu_baseline(args)
+        out = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": args.gpus,
+               "steps": args.cpu_batches, "warmup": 0, "ms_per_step": round(cb["seconds"] * 1e3 / max(1, args.cpu_batches), 3),
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+               "data": "synthetic", "config": {"workload": args.workload},
+               "cpu_baseline": cb,
+               "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(out))
+        return
+    out = run_ours(args, world, rank, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = run_cpu_baseline(args)
+    elif rank == 0:
+        out["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

@@ -177,6 +177,18 @@ int32_t moe_prefill_forward(const moe_layer* layer, const void* x /* device bf16
                             moe_stream_t stream);
 
 /*
+ * moe_decode_forward that also records four CUDA events on `stream`: before
+ * the router kernel, after it, after the gate/up kernel and after the down +
+ * combine kernel (events[i] is a cudaEvent_t; any entry may be NULL).  For
+ * per-kernel timing; the event records between launches stop the kernels
+ * from overlapping their prologues, so whole-layer timing should use
+ * moe_decode_forward.
+ */
+int32_t moe_decode_forward_timed(const moe_layer* layer, const void* x, int32_t T, void* y,
+                                 const moe_options* opts, void* ws, size_t ws_bytes, moe_stream_t stream,
+                                 void* const* events);
+
+/*
  * Read and clear the device-side error flag of a workspace.  Synchronises
  * `stream` (this is the one call that blocks).  Returns MOE_OK,
  * MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BAD_INDEX.

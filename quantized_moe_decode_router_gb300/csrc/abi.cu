@@ -162,7 +162,10 @@ bool choose_split(int K, int unitK, int rowsA, int rowsB, int& wk, int& wr) {
 }
 
 int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* y, void* ws, size_t ws_bytes,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, void* const* events) {
+  auto mark = [&](int i) {
+    if (events && events[i]) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream);
+  };
   const int maxT = ws_max_tokens(L, ws_bytes);
   const Layout lo = make_layout(L, maxT);
   uint8_t* b = static_cast<uint8_t*>(ws);
@@ -220,11 +223,15 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
     return n < 1 ? 1 : (n > 2 ? 2 : n);
   };
 
+  mark(0);
   cudaError_t err = launch_router_decode(ra, stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
+  mark(1);
   err = launch_gateup_decode(ea, sms * per_sm(smem_gu), smem_gu, stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
+  mark(2);
   err = launch_down_decode(ea, sms * per_sm(smem_dn), smem_dn, stream);
+  mark(3);
   return cuda_status(err);
 }
 
@@ -302,8 +309,9 @@ int32_t moe_route(const moe_layer* layer, const void* x, int32_t T, int32_t* top
   return cuda_status(launch_router_decode(ra, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int32_t moe_decode_forward(const moe_layer* layer, const void* x, int32_t T, void* y, const moe_options* opts,
-                           void* ws, size_t ws_bytes, moe_stream_t stream) {
+static int32_t decode_forward_checked(const moe_layer* layer, const void* x, int32_t T, void* y,
+                                      const moe_options* opts, void* ws, size_t ws_bytes, moe_stream_t stream,
+                                      void* const* events) {
   int32_t st = check_layer(layer);
   if (st != MOE_OK) return st;
   if ((st = check_options(opts)) != MOE_OK) return st;
@@ -314,7 +322,18 @@ int32_t moe_decode_forward(const moe_layer* layer, const void* x, int32_t T, voi
   if (T > MOE_DECODE_MAX_TOKENS) return MOE_ERR_UNSUPPORTED;
   if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
   if ((size_t)T * layer->hidden * 2 > 200 * 1024) return MOE_ERR_UNSUPPORTED;
-  return decode_forward_impl(layer, x, T, y, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+  return decode_forward_impl(layer, x, T, y, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), events);
+}
+
+int32_t moe_decode_forward(const moe_layer* layer, const void* x, int32_t T, void* y, const moe_options* opts,
+                           void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return decode_forward_checked(layer, x, T, y, opts, ws, ws_bytes, stream, nullptr);
+}
+
+int32_t moe_decode_forward_timed(const moe_layer* layer, const void* x, int32_t T, void* y,
+                                 const moe_options* opts, void* ws, size_t ws_bytes, moe_stream_t stream,
+                                 void* const* events) {
+  return decode_forward_checked(layer, x, T, y, opts, ws, ws_bytes, stream, events);
 }
 
 int32_t moe_prefill_forward(const moe_layer* layer, const void* x, int32_t T, void* y, const moe_options* opts,
