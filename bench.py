@@ -207,8 +207,9 @@ def run_ours(args, world, rank, local):
         reps = max(1, steps // G)
         steps = reps * G
         warm = max(1, args.warmup // G)
-        for _ in range(warm):
-            g.replay()
+        with torch.cuda.stream(stream):          # replay on the stream the timing events use
+            for _ in range(warm):
+                g.replay()
         torch.cuda.synchronize()
         headline = T == batches[-1]
         sampler = ClockSampler(local) if headline else None
@@ -219,10 +220,11 @@ def run_ours(args, world, rank, local):
             dist.barrier()
         torch.cuda.synchronize()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        ev1.record(stream)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            ev1.record(stream)
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
@@ -248,9 +250,16 @@ def run_ours(args, world, rank, local):
         if headline:
             n = min(256, max(32, steps // 8))
             evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
-            with torch.cuda.stream(stream):
+            for row in evs:          # create the CUDA events (torch creates them lazily on first record)
+                for e in row:
+                    e.record(stream)
+            torch.cuda.synchronize()
+            gt = torch.cuda.CUDAGraph()         # event-record nodes between the kernels, no host gaps
+            with torch.cuda.graph(gt, stream=stream):
                 for i in range(n):
                     q.moe_decode_forward_timed(layers[i % R], xs[i % NB], T, ys, ws, evs[i], stream=stream)
+            with torch.cuda.stream(stream):
+                gt.replay()
             torch.cuda.synchronize()
             dur = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)] for i in range(n)])
             avg = dur.mean(axis=0) * 1e3  # us per launch: router, gate/up, down

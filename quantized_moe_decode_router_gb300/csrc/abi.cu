@@ -164,7 +164,8 @@ bool choose_split(int K, int unitK, int rowsA, int rowsB, int& wk, int& wr) {
 int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* y, void* ws, size_t ws_bytes,
                             cudaStream_t stream, void* const* events) {
   auto mark = [&](int i) {
-    if (events && events[i]) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream);
+    // external records so that, inside a stream capture, they become event-record nodes
+    if (events && events[i]) cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), stream, cudaEventRecordExternal);
   };
   const int maxT = ws_max_tokens(L, ws_bytes);
   const Layout lo = make_layout(L, maxT);
