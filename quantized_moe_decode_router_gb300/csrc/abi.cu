@@ -27,7 +27,8 @@ bool shape_ok(int fmt, int N, int K) {
 }
 
 struct Layout {
-  size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, rb_cnt, total;
+  size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, rb_cnt, h_amax, hs_amax, gu_part, gu_cnt,
+      dn_part, dn_cnt, total;
 };
 
 Layout make_layout(const moe_layer* L, int maxT) {
@@ -53,6 +54,15 @@ Layout make_layout(const moe_layer* L, int maxT) {
   o.P = take(T * k * H * 4);
   o.S = take(T * H * 4 + 16);
   o.rb_cnt = take(H / 16 * 4);
+  o.h_amax = take(T * k * 4);
+  o.hs_amax = take(T * 4 + 16);
+  // block sums of tiles split along K (at most kMaxSplitBlocks entries)
+  const size_t act_max = T * k < E ? T * k : E;
+  const size_t gu_tiles = act_max * (I / 16) + Is / 16, dn_tiles = (act_max + 1) * (H / 16);
+  o.gu_part = take((size_t)kMaxSplitBlocks * 32 * 8 * 4);
+  o.gu_cnt = take(gu_tiles * 4);
+  o.dn_part = take((size_t)kMaxSplitBlocks * 32 * 4 * 4);
+  o.dn_cnt = take(dn_tiles * 4);
   o.total = at;
   return o;
 }
@@ -142,43 +152,56 @@ int ws_max_tokens(const moe_layer* L, size_t ws_bytes) {
 
 int32_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// Warp split (wk along K, wr along rows; wk * wr = 8) for matrices with
-// reduction length K, decode unit width unitK (the larger of the formats
-// involved) and row counts that must divide into 16*wr-row tiles.
-bool choose_split(int K, int unitK, int rowsA, int rowsB, int& wk, int& wr) {
-  const int cands[4] = {8, 4, 2, 1};
-  for (int pass = 0; pass < 2; ++pass) {
-    for (int c : cands) {
-      const int r = 8 / c;
-      if (K % (c * unitK)) continue;
-      if (rowsA % (16 * r) || (rowsB && rowsB % (16 * r))) continue;
-      if (pass == 0 && K / (c * unitK) < 2) continue;  // prefer two or more units per warp
-      wk = c;
-      wr = r;
-      return true;
-    }
+// K slices per 16-row tile: split while the tasks stay below ~2 per resident
+// warp, the slices divide the accumulation blocks of both formats and the
+// stored block sums fit the partial buffer.  The result of a tile does not
+// depend on the split (blocks are always added in block order).
+int choose_slices(int K_r, int fmt_r, long tiles_r, int K_s, int fmt_s, long tiles_s, int warps) {
+  const int Br = dec_blocks(fmt_r, K_r), Bs = fmt_s ? dec_blocks(fmt_s, K_s) : Br;
+  if (tiles_r * Br + tiles_s * Bs > kMaxSplitBlocks) return 1;
+  int S = 1;
+  while (Br % (2 * S) == 0 && Bs % (2 * S) == 0 && (tiles_r + tiles_s) * 2 * S <= 2L * warps) S *= 2;
+  return S;
+}
+
+cudaError_t launch_expert(int fmt, int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s) {
+  switch (fmt) {
+    case MOE_FMT_NVFP4: return launch_expert_nvfp4(sfmt, down, a, smem, s);
+    case MOE_FMT_MXFP4: return launch_expert_mxfp4(sfmt, down, a, smem, s);
+    case MOE_FMT_INT4_G64: return launch_expert_int4(sfmt, down, a, smem, s);
+    case MOE_FMT_INT8_G64: return launch_expert_int8(sfmt, down, a, smem, s);
+    case MOE_FMT_FP8_B128: return launch_expert_fp8(sfmt, down, a, smem, s);
+    default: return cudaErrorInvalidValue;
   }
-  return false;
+}
+
+RouterArgs router_args(const moe_layer* L, const Layout& lo, void* ws, const void* x, int T) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  RouterArgs ra;
+  std::memset(&ra, 0, sizeof(ra));
+  ra.H = L->hidden; ra.E = L->n_experts; ra.k = L->top_k; ra.T = T;
+  ra.wpr = router_warps_per_row(L->hidden);
+  ra.x = static_cast<const uint16_t*>(x);
+  ra.w = L->router_w;
+  ra.bias = L->router_bias;
+  ra.rb = route_bufs(lo, ws);
+  ra.h_amax = reinterpret_cast<uint32_t*>(b + lo.h_amax);
+  ra.hs_amax = reinterpret_cast<uint32_t*>(b + lo.hs_amax);
+  return ra;
 }
 
 int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* y, void* ws, size_t ws_bytes,
                             cudaStream_t stream, void* const* events) {
   auto mark = [&](int i) {
     // external records so that, inside a stream capture, they become event-record nodes
-    if (events && events[i]) cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), stream, cudaEventRecordExternal);
+    if (events && events[i])
+      cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), stream, cudaEventRecordExternal);
   };
   const int maxT = ws_max_tokens(L, ws_bytes);
   const Layout lo = make_layout(L, maxT);
   uint8_t* b = static_cast<uint8_t*>(ws);
   const int H = L->hidden, I = L->inter, Is = L->shared_fmt ? L->shared_inter : 0;
-
-  RouterArgs ra;
-  ra.H = H; ra.E = L->n_experts; ra.k = L->top_k; ra.T = T;
-  ra.x = static_cast<const uint16_t*>(x);
-  ra.w = L->router_w;
-  ra.bias = L->router_bias;
-  ra.rb = route_bufs(lo, ws);
-  std::memset(&ra.out, 0, sizeof(ra.out));
+  const RouterArgs ra = router_args(L, lo, ws, x, T);
 
   ExpertArgs ea;
   std::memset(&ea, 0, sizeof(ea));
@@ -194,44 +217,40 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   ea.rb = ra.rb;
   ea.h = reinterpret_cast<uint16_t*>(b + lo.h);
   ea.hs = reinterpret_cast<uint16_t*>(b + lo.hs);
+  ea.h_amax = ra.h_amax;
+  ea.hs_amax = ra.hs_amax;
   ea.P = reinterpret_cast<float*>(b + lo.P);
   ea.S = reinterpret_cast<float*>(b + lo.S);
   ea.rb_cnt = reinterpret_cast<uint32_t*>(b + lo.rb_cnt);
+  ea.gu_part = reinterpret_cast<float*>(b + lo.gu_part);
+  ea.gu_cnt = reinterpret_cast<uint32_t*>(b + lo.gu_cnt);
+  ea.dn_part = reinterpret_cast<float*>(b + lo.dn_part);
+  ea.dn_cnt = reinterpret_cast<uint32_t*>(b + lo.dn_cnt);
   ea.y = static_cast<uint16_t*>(y);
-  int uk = decode_unit_k(L->fmt);
-  if (Is && decode_unit_k(L->shared_fmt) > uk) uk = decode_unit_k(L->shared_fmt);
-  if (!choose_split(H, uk, I, Is, ea.wk_gu, ea.wr_gu)) return MOE_ERR_UNSUPPORTED;
-  const int Kd = Is ? (I < Is ? I : Is) : I;
-  if (!choose_split(Kd, uk, H, 0, ea.wk_dn, ea.wr_dn)) return MOE_ERR_UNSUPPORTED;
-  if (I % (ea.wk_dn * uk) || (Is && Is % (ea.wk_dn * uk))) return MOE_ERR_UNSUPPORTED;
-  ea.xs_tok_stride = H + 16;
-  ea.xs_q_stride = 0;
-  const int Kmax = Is > I ? Is : I;
-  ea.hs_tok_stride = Kmax + 16;
-  ea.hs_q_stride = 0;
-
-  const size_t smem_gu = (size_t)(T + 1) * ea.xs_tok_stride * 2 + (size_t)(kExpertThreads / 32) * 2 * 32 * 4 * 4;
-  const size_t smem_dn = (size_t)9 * ea.hs_tok_stride * 2 + (size_t)(kExpertThreads / 32) * 32 * 4 * 4;
-  if (smem_gu > 220 * 1024 || smem_dn > 220 * 1024) return MOE_ERR_UNSUPPORTED;
 
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
-  int smem_sm = 0;
-  cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-  auto per_sm = [&](size_t smem) {
-    int n = (int)((size_t)smem_sm / (smem + 1024));
-    return n < 1 ? 1 : (n > 2 ? 2 : n);
-  };
+  const int warps = sms * 16;  // resident warps the expert kernels aim for
+  const long act = (long)T * L->top_k < L->n_experts ? (long)T * L->top_k : L->n_experts;
+  ea.gu_slices = choose_slices(H, L->fmt, act * (I / 16), H, L->shared_fmt, Is / 16, warps);
+  ea.dn_slices = choose_slices(I, L->fmt, act * (H / 16), Is, L->shared_fmt, Is ? H / 16 : 0, warps);
+  ea.xs_tok_stride = H + 16;
+  const int Kmax = Is > I ? Is : I;
+  ea.hs_tok_stride = Kmax + 16;
+
+  const size_t smem_gu = (size_t)(T + 1) * ea.xs_tok_stride * 2;
+  const size_t smem_dn = (size_t)(MOE_DECODE_MAX_TOKENS + 1) * ea.hs_tok_stride * 2;
+  if (smem_gu > 200 * 1024 || smem_dn > 200 * 1024) return MOE_ERR_UNSUPPORTED;
 
   mark(0);
   cudaError_t err = launch_router_decode(ra, stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   mark(1);
-  err = launch_gateup_decode(ea, sms * per_sm(smem_gu), smem_gu, stream);
+  err = launch_expert(L->fmt, L->shared_fmt, false, ea, smem_gu, stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   mark(2);
-  err = launch_down_decode(ea, sms * per_sm(smem_dn), smem_dn, stream);
+  err = launch_expert(L->fmt, L->shared_fmt, true, ea, smem_dn, stream);
   mark(3);
   return cuda_status(err);
 }
@@ -298,12 +317,7 @@ int32_t moe_route(const moe_layer* layer, const void* x, int32_t T, int32_t* top
   if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
   const int maxT = ws_max_tokens(layer, ws_bytes);
   const Layout lo = make_layout(layer, maxT);
-  RouterArgs ra;
-  ra.H = layer->hidden; ra.E = layer->n_experts; ra.k = layer->top_k; ra.T = T;
-  ra.x = static_cast<const uint16_t*>(x);
-  ra.w = layer->router_w;
-  ra.bias = layer->router_bias;
-  ra.rb = route_bufs(lo, ws);
+  RouterArgs ra = router_args(layer, lo, ws, x, T);
   ra.out.topk_idx = topk_idx; ra.out.topk_w = topk_w; ra.out.cnt = expert_cnt; ra.out.off = expert_off;
   ra.out.pair = pair_list;
   if ((size_t)T * layer->hidden * 2 > 200 * 1024) return MOE_ERR_UNSUPPORTED;

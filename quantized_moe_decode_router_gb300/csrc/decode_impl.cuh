@@ -1,0 +1,715 @@
+// Decode-path expert projections (T <= 8 tokens), templated on the routed
+// and shared expert formats.  Included by one translation unit per routed
+// format (decode_<fmt>.cu).
+//
+//   gate/up: h[p, rows] = bf16( silu(g) * u ) for every pair p routed to an
+//            expert, gate and up in one pass (DGPP README "Execution and
+//            performance", engine.expert_gemm_pair).
+//   down:    P[p, rows] = W_down_e h_p (FP32 partials, DGPP README row
+//            engine.prefill_bf16_partials); the last contribution to a
+//            16-row block combines y = bf16( sum_j w_j P_j + S ).
+//
+// Work is split into independent warp tasks (expert, 16-row tile, K slice)
+// so that every warp streams its own weights without CTA barriers; K slices
+// of one tile are summed by the last slice to finish, in slice order
+// (deterministic, no floating-point atomics).  Weights stream from HBM with
+// 128-bit non-allocating loads and are decoded in registers (DGPP forum post
+// 15 "Lossless bf12": decode reads weights at the memory line rate,
+// rebuilding them in registers) into f16 MMA fragments; the tokens are the
+// N=8 side of m16n8k16, so one decode serves every token of the expert.
+//
+// Lane layout: lane (r = lane/4, c = lane%4) holds rows r and r+8 of the
+// tile and the 16-byte chunk c of every unit (4-bit formats: 128 columns per
+// unit, 32 per lane; 8-bit formats: 64 and 16).  An MMA reduces K across the
+// four lanes of a row group, so scales that differ between those lanes are
+// folded into the f16 weights before the MMA:
+//   NVFP4   e2m1 * e4m3 (at most 6 significant bits, f16-normal): exact.
+//   MXFP4   e2m1 * 2^(c - cmax), cmax the largest scale code of the four
+//           lanes; 2^(cmax-127) multiplies the FP32 partial.  Exact while
+//           c - cmax >= -20; otherwise the unit takes a 4-MMA path that
+//           applies each lane's scale in FP32.
+//   INT4    q * M * 2^(e - emax) with the BF16 scale s = M * 2^e (M an 8-bit
+//           integer): |q * M| <= 2040 fits f16's 11-bit significand; exact
+//           while e - emax >= -24, else the 4-MMA path.
+//   INT8, FP8: one scale per unit for all four lanes, applied to the FP32
+//           partial of the unit (the per-group FMA of the default chain,
+//           DGPP README row engine.prefill_fold_scales).
+// Activations enter as f16 scaled by a per-token (per-pair for h) power of
+// two, exact for every element above 2^-32 of the row's largest magnitude.
+#pragma once
+
+#include "kernels.cuh"
+
+namespace qmoe {
+namespace dec {
+
+constexpr int kMaxT = MOE_DECODE_MAX_TOKENS;
+constexpr int kWarps = kExpertThreads / 32;
+
+template <int F> struct Fm;
+template <> struct Fm<MOE_FMT_NVFP4> { static constexpr int kBits = 4; };
+template <> struct Fm<MOE_FMT_MXFP4> { static constexpr int kBits = 4; };
+template <> struct Fm<MOE_FMT_INT4_G64> { static constexpr int kBits = 4; };
+template <> struct Fm<MOE_FMT_INT8_G64> { static constexpr int kBits = 8; };
+template <> struct Fm<MOE_FMT_FP8_B128> { static constexpr int kBits = 8; };
+template <int F> constexpr int unit_k() { return Fm<F>::kBits == 4 ? 128 : 64; }
+template <int F> constexpr int chunk_k() { return unit_k<F>() / 4; }
+constexpr int kPrefetch = 2;
+
+struct Mat {
+  const uint8_t* data;
+  const uint8_t* scales;
+  int K;
+};
+
+__device__ __forceinline__ Mat mat_of(const QW& w, int fmt, int e, int N, int K) {
+  Mat m;
+  m.data = w.data + (size_t)e * data_bytes(fmt, N, K);
+  m.scales = w.scales + (size_t)e * scale_bytes(fmt, N, K);
+  m.K = K;
+  return m;
+}
+
+// Raw scale bits of row R for the lane chunk starting at column k.
+template <int F>
+__device__ __forceinline__ uint32_t load_scale(const Mat& m, int R, int k) {
+  if constexpr (F == MOE_FMT_NVFP4) return ldg_nc_u16(m.scales + (size_t)R * (m.K / 16) + k / 16);
+  else if constexpr (F == MOE_FMT_MXFP4) return ldg_nc_u8(m.scales + (size_t)R * (m.K / 32) + k / 32);
+  else if constexpr (F == MOE_FMT_INT4_G64 || F == MOE_FMT_INT8_G64)
+    return ldg_nc_u16(m.scales + ((size_t)R * (m.K / 64) + k / 64) * 2);
+  else return ldg_nc_u32(m.scales + ((size_t)(R / 128) * (m.K / 128) + k / 128) * 4);
+}
+
+template <int NM>
+struct Unit {
+  uint4 d[NM][2];  // rows r and r+8
+  uint32_t s[NM][2];
+};
+
+template <int F, int NM>
+__device__ __forceinline__ void load_unit(Unit<NM>& u, const Mat (&m)[NM], int R0, int kc) {
+  constexpr int kB = Fm<F>::kBits;
+#pragma unroll
+  for (int i = 0; i < NM; ++i) {
+    const size_t rb = (size_t)m[i].K * kB / 8;
+    const uint8_t* p0 = m[i].data + (size_t)R0 * rb + (size_t)kc * kB / 8;
+    u.d[i][0] = ldg_nc_v4(p0);
+    u.d[i][1] = ldg_nc_v4(p0 + 8 * rb);
+    u.s[i][0] = load_scale<F>(m[i], R0, kc);
+    u.s[i][1] = load_scale<F>(m[i], R0 + 8, kc);
+  }
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ int max4(int v) {
+  v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+  return max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+}
+
+__device__ __forceinline__ uint32_t f16x2_bcast(float v) {
+  __half2 h = __float2half2_rn(v);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Decoded (unscaled) f16 fragments of one 32-bit word of row r / r+8.
+template <int F>
+__device__ __forceinline__ void decode_word4(uint32_t w, uint32_t (&v)[4]) {
+  if constexpr (F == MOE_FMT_INT4_G64) int4x8_to_f16x2_paired(w, v);
+  else e2m1x8_to_f16x2(w, v);
+}
+
+// Per-lane scale folding of a 4-bit unit.  fac[i][r][b]: f16x2 factor for
+// row r (0 -> r, 1 -> r+8) and 16-element half b of the lane's chunk;
+// us[i][r]: FP32 unit scale applied after the MMA.  Returns false if the
+// fold would not be exact for some lane of the warp (-> 4-MMA path).
+template <int F, int NM>
+__device__ __forceinline__ bool fold4(const Unit<NM>& u, uint32_t (&fac)[NM][2][2], float (&us)[NM][2]) {
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < NM; ++i) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint32_t s = u.s[i][r];
+      if constexpr (F == MOE_FMT_NVFP4) {
+        fac[i][r][0] = e4m3_bcast_f16x2(s & 0xFF);
+        fac[i][r][1] = e4m3_bcast_f16x2(s >> 8);
+        us[i][r] = 1.f;
+      } else if constexpr (F == MOE_FMT_MXFP4) {
+        const int c = (int)(s & 0xFF);
+        const int cm = max4(c);
+        const int d = c - cm;
+        ok = ok && d >= -20 && cm != 255;
+        fac[i][r][0] = fac[i][r][1] = f16x2_bcast(exp2i(max(d, -20)));
+        us[i][r] = e8m0_to_float((uint32_t)cm);
+      } else {  // INT4_G64: bf16 scale = M * 2^e, M the integer significand
+        const uint32_t E8 = (s >> 7) & 0xFF;
+        const int M = (int)((s & 0x7F) | (E8 ? 0x80u : 0u));
+        const int e = (E8 ? (int)E8 : 1) - 134;
+        const int ev = M ? e : -100000;
+        const int em = max4(ev);
+        const int d = e - em;
+        ok = ok && E8 != 255 && (M == 0 || d >= -24);
+        const float f = (float)M * exp2i(max(d, -24));  // exact: an 8-bit integer times a power of two
+        fac[i][r][0] = fac[i][r][1] = f16x2_bcast((s & 0x8000) ? -f : f);
+        us[i][r] = ldexpf(1.0f, em < -1000 ? 0 : em);
+      }
+    }
+  }
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+template <int F>
+__device__ __forceinline__ float unscaled_scale(uint32_t s) {
+  if constexpr (F == MOE_FMT_MXFP4) return e8m0_to_float(s & 0xFF);
+  else if constexpr (F == MOE_FMT_INT4_G64 || F == MOE_FMT_INT8_G64) return __uint_as_float(s << 16);
+  else return __uint_as_float(s);
+}
+
+// B fragments (activations) of word wd of the lane's chunk.
+template <int F>
+__device__ __forceinline__ void b_frags(const uint4& xv, uint32_t& a0, uint32_t& a1, uint32_t& b0, uint32_t& b1) {
+  if constexpr (F == MOE_FMT_INT4_G64) {
+    a0 = prmt(xv.x, xv.z, 0x5410u);  // (x0, x4)
+    a1 = prmt(xv.x, xv.z, 0x7632u);  // (x1, x5)
+    b0 = prmt(xv.y, xv.w, 0x5410u);  // (x2, x6)
+    b1 = prmt(xv.y, xv.w, 0x7632u);  // (x3, x7)
+  } else {
+    a0 = xv.x; a1 = xv.y; b0 = xv.z; b1 = xv.w;
+  }
+}
+
+// One unit of NM matrices: MMA into acc.  xl: this lane's activations (f16)
+// at its chunk's first column.  Every lane executes every MMA.
+template <int F, int NM>
+__device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl, float (&acc)[NM][4]) {
+  if constexpr (Fm<F>::kBits == 4) {
+    uint32_t fac[NM][2][2];
+    float us[NM][2];
+    const bool fast = fold4<F, NM>(u, fac, us);
+    if (fast) {
+      float d[NM][4];
+#pragma unroll
+      for (int i = 0; i < NM; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d[i][j] = 0.f;
+#pragma unroll
+      for (int wd = 0; wd < 4; ++wd) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xl + wd * 8);
+        uint32_t bA0, bA1, bB0, bB1;
+        b_frags<F>(xv, bA0, bA1, bB0, bB1);
+#pragma unroll
+        for (int i = 0; i < NM; ++i) {
+          uint32_t v0[4], v1[4];
+          decode_word4<F>(word(u.d[i][0], wd), v0);
+          decode_word4<F>(word(u.d[i][1], wd), v1);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            v0[j] = hmul2_u32(v0[j], fac[i][0][wd >> 1]);
+            v1[j] = hmul2_u32(v1[j], fac[i][1][wd >> 1]);
+          }
+          const uint32_t aA[4] = {v0[0], v1[0], v0[1], v1[1]};
+          const uint32_t aB[4] = {v0[2], v1[2], v0[3], v1[3]};
+          float (&dst)[4] = (F == MOE_FMT_NVFP4) ? acc[i] : d[i];
+          mma_f16_16816(dst, aA, bA0, bA1);
+          mma_f16_16816(dst, aB, bB0, bB1);
+        }
+      }
+      if constexpr (F != MOE_FMT_NVFP4) {
+#pragma unroll
+        for (int i = 0; i < NM; ++i) {
+          acc[i][0] = __fmaf_rn(d[i][0], us[i][0], acc[i][0]);
+          acc[i][1] = __fmaf_rn(d[i][1], us[i][0], acc[i][1]);
+          acc[i][2] = __fmaf_rn(d[i][2], us[i][1], acc[i][2]);
+          acc[i][3] = __fmaf_rn(d[i][3], us[i][1], acc[i][3]);
+        }
+      }
+    } else if constexpr (F != MOE_FMT_NVFP4) {
+      // exact slow path: one MMA pass per lane column c', applying that lane's scale in FP32
+      const int lane = threadIdx.x & 31, c = lane & 3;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        float d[NM][4];
+#pragma unroll
+        for (int i = 0; i < NM; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) d[i][j] = 0.f;
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xl + wd * 8);
+          uint32_t bA0, bA1, bB0, bB1;
+          b_frags<F>(xv, bA0, bA1, bB0, bB1);
+#pragma unroll
+          for (int i = 0; i < NM; ++i) {
+            uint32_t v0[4], v1[4];
+            decode_word4<F>(c == cc ? word(u.d[i][0], wd) : 0u, v0);
+            decode_word4<F>(c == cc ? word(u.d[i][1], wd) : 0u, v1);
+            const uint32_t aA[4] = {v0[0], v1[0], v0[1], v1[1]};
+            const uint32_t aB[4] = {v0[2], v1[2], v0[3], v1[3]};
+            mma_f16_16816(d[i], aA, bA0, bA1);
+            mma_f16_16816(d[i], aB, bB0, bB1);
+          }
+        }
+        const int src = (lane & ~3) | cc;
+#pragma unroll
+        for (int i = 0; i < NM; ++i) {
+          const float sa = unscaled_scale<F>(__shfl_sync(0xFFFFFFFFu, u.s[i][0], src));
+          const float sb = unscaled_scale<F>(__shfl_sync(0xFFFFFFFFu, u.s[i][1], src));
+          acc[i][0] = __fmaf_rn(d[i][0], sa, acc[i][0]);
+          acc[i][1] = __fmaf_rn(d[i][1], sa, acc[i][1]);
+          acc[i][2] = __fmaf_rn(d[i][2], sb, acc[i][2]);
+          acc[i][3] = __fmaf_rn(d[i][3], sb, acc[i][3]);
+        }
+      }
+    }
+  } else {
+    // 8-bit codes: the four lanes' chunks are one scale block; four words of four codes
+    float d[NM][4];
+#pragma unroll
+    for (int i = 0; i < NM; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) d[i][j] = 0.f;
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+      const uint2 xv = *reinterpret_cast<const uint2*>(xl + wd * 4);
+#pragma unroll
+      for (int i = 0; i < NM; ++i) {
+        uint32_t lo0, hi0, lo1, hi1;
+        if constexpr (F == MOE_FMT_INT8_G64) {
+          int8x4_to_f16x2(word(u.d[i][0], wd), lo0, hi0);
+          int8x4_to_f16x2(word(u.d[i][1], wd), lo1, hi1);
+        } else {
+          e4m3x4_to_f16x2(word(u.d[i][0], wd), lo0, hi0);
+          e4m3x4_to_f16x2(word(u.d[i][1], wd), lo1, hi1);
+        }
+        const uint32_t a[4] = {lo0, lo1, hi0, hi1};
+        mma_f16_16816(d[i], a, xv.x, xv.y);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NM; ++i) {
+      const float sa = unscaled_scale<F>(u.s[i][0]), sb = unscaled_scale<F>(u.s[i][1]);
+      acc[i][0] = __fmaf_rn(d[i][0], sa, acc[i][0]);
+      acc[i][1] = __fmaf_rn(d[i][1], sa, acc[i][1]);
+      acc[i][2] = __fmaf_rn(d[i][2], sb, acc[i][2]);
+      acc[i][3] = __fmaf_rn(d[i][3], sb, acc[i][3]);
+    }
+  }
+}
+
+// One warp: rows [row0, row0 + 16) of NM matrices over columns [kb, kb + Kw)
+// (Kw a multiple of the block).  Units stream through a kPrefetch-deep
+// register ring; the trip count is warp-uniform.  The K range is summed as
+// blocks of `bu` units, each block from zero; block sums are either added to
+// acc in block order (bpart == nullptr) or stored to bpart[b] for the
+// tile's last slice to add in the same order.  The association of the sum
+// therefore depends only on K, never on how K is split between warps.
+template <int F, int NM>
+__device__ __forceinline__ void warp_tile(const Mat (&m)[NM], int row0, int kb, int Kw, int bu, const __half* xrow,
+                                          float (&acc)[NM][4], float* bpart) {
+  constexpr int UK = unit_k<F>(), CK = chunk_k<F>(), PF = kPrefetch;
+  const int lane = threadIdx.x & 31;
+  const int R0 = row0 + (lane >> 2);
+  const int koff = kb + (lane & 3) * CK;
+  const int nU = Kw / UK;
+  Unit<NM> buf[PF];
+  float blk[NM][4];
+#pragma unroll
+  for (int i = 0; i < NM; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) blk[i][j] = 0.f;
+#pragma unroll
+  for (int p = 0; p < PF; ++p)
+    if (p < nU) load_unit<F, NM>(buf[p], m, R0, koff + p * UK);
+  for (int u0 = 0; u0 < nU; u0 += PF) {
+#pragma unroll
+    for (int p = 0; p < PF; ++p) {
+      const int u = u0 + p;
+      if (u < nU) {
+        compute_unit<F, NM>(buf[p], xrow + koff + u * UK, blk);
+        if (u + PF < nU) load_unit<F, NM>(buf[p], m, R0, koff + (u + PF) * UK);
+        if ((u + 1) % bu == 0) {  // block complete
+          if (bpart) {
+            float* d = bpart + (size_t)(u / bu) * (32 * 4 * NM) + lane * 4 * NM;
+#pragma unroll
+            for (int i = 0; i < NM; ++i)
+              *reinterpret_cast<float4*>(d + 4 * i) = make_float4(blk[i][0], blk[i][1], blk[i][2], blk[i][3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < NM; ++i)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) acc[i][j] += blk[i][j];
+          }
+#pragma unroll
+          for (int i = 0; i < NM; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) blk[i][j] = 0.f;
+        }
+      }
+    }
+  }
+}
+
+// Largest-magnitude element -> exponent p with amax * 2^-p in [2^14, 2^15).
+__device__ __forceinline__ int scale_exponent_bits(uint32_t amax_bits) {
+  amax_bits &= 0x7FFFFFFFu;
+  if (amax_bits == 0 || amax_bits >= 0x7F800000u) return 0;
+  int e = (int)(amax_bits >> 23) - 127;
+  return max(-100, min(100, e - 14));
+}
+
+// Stage bf16 rows into shared memory as f16 scaled by 2^-p (p from the row's
+// amax, computed here when amax_bits is null).  Row `nrows` is zero-filled.
+static __device__ void stage_rows_f16(const uint16_t* const* src, const uint32_t* amax_bits, int nrows, int K, __half* dst,
+                               int stride, int* pexp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int r = warp; r < nrows; r += kWarps) {
+    const uint16_t* s = src[r];
+    uint32_t am;
+    if (amax_bits) {
+      am = amax_bits[r];
+    } else {
+      float amax = 0.f;
+      for (int k = lane * 8; k < K; k += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(s + k);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[j] & 0xFFFF)), fabsf(bf16_bits_to_float(w[j] >> 16))));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+      am = __float_as_uint(amax);
+    }
+    const int p = scale_exponent_bits(am);
+    if (lane == 0) pexp[r] = p;
+    const float inv = exp2i(-p);
+    __half* d = dst + (size_t)r * stride;
+    for (int k = lane * 8; k < K; k += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(s + k);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        __half2 hh = __floats2half2_rn(bf16_bits_to_float(w[j] & 0xFFFF) * inv, bf16_bits_to_float(w[j] >> 16) * inv);
+        o[j] = *reinterpret_cast<uint32_t*>(&hh);
+      }
+      *reinterpret_cast<uint4*>(d + k) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  __half* z = dst + (size_t)nrows * stride;
+  for (int k = tid * 8; k < K; k += kExpertThreads * 8) *reinterpret_cast<uint4*>(z + k) = make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// Tiles split into S > 1 slices: every slice has stored its block sums
+// (tile_part[b], b < nblk); the slice that arrives last adds all of them in
+// block order and returns true with the sum in acc.  S == 1: acc already
+// holds the sum, return true.
+template <int NM>
+__device__ __forceinline__ bool block_reduce(float (&acc)[NM][4], const float* tile_part, uint32_t* cnt, int S,
+                                             int nblk) {
+  const int lane = threadIdx.x & 31;
+  if (S == 1) return true;
+  __threadfence();
+  __syncwarp();
+  uint32_t prev = 0;
+  if (lane == 0) prev = atomicAdd(cnt, 1u);
+  prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+  if (prev != (uint32_t)S - 1) return false;
+  __threadfence();
+#pragma unroll
+  for (int i = 0; i < NM; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int bl = 0; bl < nblk; ++bl) {
+    const float* p = tile_part + (size_t)bl * (32 * 4 * NM) + lane * 4 * NM;
+#pragma unroll
+    for (int i = 0; i < NM; ++i) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(p + 4 * i));
+      acc[i][0] += v.x; acc[i][1] += v.y; acc[i][2] += v.z; acc[i][3] += v.w;
+    }
+  }
+  if (lane == 0) *cnt = 0;
+  return true;
+}
+
+// --------------------------------------------------------------- gate / up --
+
+template <int FR, int FS>
+__device__ __forceinline__ void gu_tile(int fmt_is_shared, const Mat (&m)[2], int row0, int kb, int Kw, int bu,
+                                        const __half* xrow, float (&acc)[2][4], float* bpart) {
+  if (fmt_is_shared) {
+    if constexpr (FS != 0) warp_tile<FS, 2>(m, row0, kb, Kw, bu, xrow, acc, bpart);
+  } else {
+    warp_tile<FR, 2>(m, row0, kb, Kw, bu, xrow, acc, bpart);
+  }
+}
+
+template <int FR, int FS>
+__global__ void __launch_bounds__(kExpertThreads, 2) gateup_kernel(ExpertArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int T = a.T, H = a.H, I = a.I, k = a.k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int xs_stride = a.xs_tok_stride;
+  __half* xs = reinterpret_cast<__half*>(smem);  // [T + 1][xs_stride]
+  __shared__ int s_pexp[kMaxT + 1];
+  __shared__ const uint16_t* s_src[kMaxT];
+
+  pdl_launch_dependents();
+  // the activations are an input of the call: stage them before waiting on the router
+  if (tid < T) s_src[tid] = a.x + (size_t)tid * H;
+  __syncthreads();
+  stage_rows_f16(s_src, nullptr, T, H, xs, xs_stride, s_pexp);
+  if (tid == 0) s_pexp[T] = 0;
+  __syncthreads();
+  pdl_wait();
+
+  const int n_active = *reinterpret_cast<volatile int*>(&a.rb.ctrl->n_active);
+  const int tpe = I / 16;
+  const int stiles = FS ? a.Is / 16 : 0;
+  const int n_tiles = n_active * tpe + stiles;
+  const int S = a.gu_slices;
+  const int n_tasks = n_tiles * S;
+  const int Kw = H / S;
+  const int Br = dec_blocks(FR, H), bur = dec_block_units(FR, H);
+  const int Bs = FS ? dec_blocks(FS, H) : 1, bus = FS ? dec_block_units(FS, H) : 1;
+  const int gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
+  const int r = lane >> 2, c = lane & 3;
+
+  for (int q = gw; q < n_tasks; q += nw) {
+    const int tile_id = q / S, slice = q - tile_id * S;
+    const bool shared_item = tile_id >= n_active * tpe;
+    int e = 0, tile, ncols, col_tok = T, col_pair[2] = {-1, -1}, col_tokc[2] = {T, T};
+    if (!shared_item) {
+      const int slot = tile_id / tpe;
+      tile = tile_id - slot * tpe;
+      e = a.rb.act[slot];
+      ncols = a.rb.cnt[e];
+      const int off = a.rb.off[e];
+      if (r < ncols) col_tok = a.rb.pair[off + r] / k;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int n = 2 * c + j;
+        if (n < ncols) {
+          col_pair[j] = a.rb.pair[off + n];
+          col_tokc[j] = col_pair[j] / k;
+        }
+      }
+    } else {
+      tile = tile_id - n_active * tpe;
+      ncols = T;
+      if (r < T) col_tok = r;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int n = 2 * c + j;
+        if (n < T) { col_pair[j] = n; col_tokc[j] = n; }
+      }
+    }
+    const int fmt = shared_item ? FS : FR;
+    const int N = shared_item ? a.Is : I;
+    const QW& qg = shared_item ? a.sgate : a.gate;
+    const QW& qu = shared_item ? a.sup : a.up;
+    const Mat m[2] = {mat_of(qg, fmt, e, N, H), mat_of(qu, fmt, e, N, H)};
+    const int row0 = tile * 16;
+    const int B = shared_item ? Bs : Br;
+    float* tile_part = a.gu_part + (shared_item ? (size_t)n_active * tpe * Br + (size_t)tile * Bs
+                                                : (size_t)tile_id * Br) * (32 * 8);
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    gu_tile<FR, FS>(shared_item, m, row0, slice * Kw, Kw, shared_item ? bus : bur, xs + (size_t)col_tok * xs_stride,
+                    acc, S > 1 ? tile_part + (size_t)slice * (B / S) * (32 * 8) : nullptr);
+    if (!block_reduce<2>(acc, tile_part, a.gu_cnt + tile_id, S, B)) continue;
+    const float tsg = (fmt == MOE_FMT_NVFP4) ? __ldg(qg.ts + e) : 1.f;
+    const float tsu = (fmt == MOE_FMT_NVFP4) ? __ldg(qu.ts + e) : 1.f;
+    uint32_t amax[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int cj = j & 1;
+      const int row = row0 + r + ((j & 2) ? 8 : 0);
+      const int out = col_pair[cj];
+      if (out >= 0) {
+        const float sc = exp2i(s_pexp[col_tokc[cj]]);
+        const float gv = acc[0][j] * sc * tsg, uv = acc[1][j] * sc * tsu;
+        const uint16_t hb = float_to_bf16_bits(silu_f(gv) * uv);
+        if (shared_item) a.hs[(size_t)out * a.Is + row] = hb;
+        else a.h[(size_t)out * I + row] = hb;
+        amax[cj] = max(amax[cj], (uint32_t)(hb & 0x7FFF) << 16);
+      }
+    }
+    // per-column max over the tile's 16 rows, then one atomic per column
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 4));
+      amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 8));
+      amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 16));
+      if (r == 0 && col_pair[j] >= 0)
+        atomicMax(shared_item ? &a.hs_amax[col_pair[j]] : &a.h_amax[col_pair[j]], amax[j]);
+    }
+  }
+}
+
+// -------------------------------------------------------- down + combine --
+
+template <int FR, int FS>
+__global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int T = a.T, H = a.H, I = a.I, k = a.k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int hs_stride = a.hs_tok_stride;
+  __half* hsm = reinterpret_cast<__half*>(smem);  // [kMaxT + 1][hs_stride]
+  __shared__ int s_pexp[kMaxT + 1];
+  __shared__ int s_col_out[kMaxT];
+  __shared__ const uint16_t* s_src[kMaxT];
+  __shared__ uint32_t s_amax[kMaxT];
+
+  pdl_launch_dependents();
+  pdl_wait();
+  const int n_active = *reinterpret_cast<volatile int*>(&a.rb.ctrl->n_active);
+  const int tpe = H / 16;
+  const int S = a.dn_slices;
+  const int Br = dec_blocks(FR, I), Bs = FS ? dec_blocks(FS, a.Is) : 1;
+  const int n_seg = n_active + (FS ? 1 : 0);      // expert segments, shared last
+  const int tasks_per_seg = tpe * S;
+  const int n_tasks = n_seg * tasks_per_seg;
+  const int needed = n_seg;
+  // contiguous task range per CTA; segments inside it are staged one at a time
+  const int q0 = (int)((long long)blockIdx.x * n_tasks / gridDim.x);
+  const int q1 = (int)((long long)(blockIdx.x + 1) * n_tasks / gridDim.x);
+  const int r = lane >> 2, c = lane & 3;
+
+  for (int seg = q0 / tasks_per_seg; seg * tasks_per_seg < q1; ++seg) {
+    const bool shared_item = seg >= n_active;
+    int e = 0, ncols;
+    __syncthreads();
+    if (!shared_item) {
+      e = a.rb.act[seg];
+      ncols = a.rb.cnt[e];
+      if (tid < kMaxT) {
+        if (tid < ncols) {
+          const int p = a.rb.pair[a.rb.off[e] + tid];
+          s_src[tid] = a.h + (size_t)p * I;
+          s_col_out[tid] = p;
+          s_amax[tid] = __ldcg(a.h_amax + p);
+        } else {
+          s_col_out[tid] = -1;
+        }
+      }
+    } else {
+      ncols = T;
+      if (tid < kMaxT) {
+        if (tid < T) {
+          s_src[tid] = a.hs + (size_t)tid * a.Is;
+          s_amax[tid] = __ldcg(a.hs_amax + tid);
+        }
+        s_col_out[tid] = tid < T ? tid : -1;
+      }
+    }
+    __syncthreads();
+    const int K = shared_item ? a.Is : I;
+    stage_rows_f16(s_src, s_amax, ncols, K, hsm, hs_stride, s_pexp);
+    __syncthreads();
+    const int fmt = shared_item ? FS : FR;
+    const QW& qd = shared_item ? a.sdown : a.down;
+    const Mat m[1] = {mat_of(qd, fmt, e, H, K)};
+    const int Kw = K / S;
+    const int B = dec_blocks(fmt, K), bu = dec_block_units(fmt, K);
+    const int t_lo = max(q0, seg * tasks_per_seg), t_hi = min(q1, (seg + 1) * tasks_per_seg);
+    const __half* xrow = hsm + (size_t)(r < ncols ? r : ncols) * hs_stride;
+    for (int q = t_lo + warp; q < t_hi; q += kWarps) {
+      const int local = q - seg * tasks_per_seg;
+      const int tile = local / S, slice = local - tile * S;
+      float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+      const int tile_id = seg * tpe + tile;
+      float* tile_part = a.dn_part + (shared_item ? (size_t)n_active * tpe * Br + (size_t)tile * Bs
+                                                  : (size_t)tile_id * Br) * (32 * 4);
+      float* bpart = S > 1 ? tile_part + (size_t)slice * (B / S) * (32 * 4) : nullptr;
+      if (shared_item) {
+        if constexpr (FS != 0) warp_tile<FS, 1>(m, tile * 16, slice * Kw, Kw, bu, xrow, acc, bpart);
+      } else {
+        warp_tile<FR, 1>(m, tile * 16, slice * Kw, Kw, bu, xrow, acc, bpart);
+      }
+      if (!block_reduce<1>(acc, tile_part, a.dn_cnt + tile_id, S, B)) continue;
+      const float ts = (fmt == MOE_FMT_NVFP4) ? __ldg(qd.ts + e) : 1.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int col = 2 * c + (j & 1);
+        const int row = tile * 16 + r + ((j & 2) ? 8 : 0);
+        const int out = s_col_out[col];
+        if (out >= 0) {
+          const float val = acc[0][j] * exp2i(s_pexp[col]) * ts;
+          if (shared_item) a.S[(size_t)out * H + row] = val;
+          else a.P[(size_t)out * H + row] = val;
+        }
+      }
+      // this expert's contribution to the 16-row block is complete; the last
+      // of the n_seg contributions combines the block in fixed order
+      __threadfence();
+      __syncwarp();
+      uint32_t prev = 0;
+      if (lane == 0) prev = atomicAdd(&a.rb_cnt[tile], 1u);
+      prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+      if (prev == (uint32_t)needed - 1) {
+        __threadfence();
+        for (int qq = lane; qq < T * 16; qq += 32) {
+          const int t = qq >> 4, row = tile * 16 + (qq & 15);
+          float y = 0.f;
+          for (int j = 0; j < k; ++j)
+            y = __fmaf_rn(__ldcg(a.rb.topk_w + t * k + j), __ldcg(a.P + (size_t)(t * k + j) * H + row), y);
+          if (FS) y = __fadd_rn(y, __ldcg(a.S + (size_t)t * H + row));
+          a.y[(size_t)t * H + row] = float_to_bf16_bits(y);
+        }
+        if (lane == 0) a.rb_cnt[tile] = 0;
+      }
+    }
+  }
+}
+
+template <int FR, int FS>
+cudaError_t launch_pdl_kernel(void (*kern)(ExpertArgs), const ExpertArgs& a, size_t smem, cudaStream_t s) {
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kExpertThreads, smem);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) per_sm = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms * per_sm);
+  cfg.blockDim = dim3(kExpertThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int FR>
+cudaError_t launch_expert_pair(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s) {
+  switch (sfmt) {
+#define QMOE_CASE(FS)                                                                              \
+  case FS:                                                                                         \
+    return down ? launch_pdl_kernel<FR, FS>(down_kernel<FR, FS>, a, smem, s)                       \
+                : launch_pdl_kernel<FR, FS>(gateup_kernel<FR, FS>, a, smem, s);
+    QMOE_CASE(0)
+    QMOE_CASE(MOE_FMT_NVFP4)
+    QMOE_CASE(MOE_FMT_MXFP4)
+    QMOE_CASE(MOE_FMT_INT4_G64)
+    QMOE_CASE(MOE_FMT_INT8_G64)
+    QMOE_CASE(MOE_FMT_FP8_B128)
+#undef QMOE_CASE
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dec
+}  // namespace qmoe

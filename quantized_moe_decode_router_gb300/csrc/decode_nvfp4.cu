@@ -1,0 +1,11 @@
+// Decode-path expert kernels with nvfp4 routed experts (one instance per shared
+// expert format); the kernels themselves are in decode_impl.cuh.
+#include "decode_impl.cuh"
+
+namespace qmoe {
+
+cudaError_t launch_expert_nvfp4(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s) {
+  return dec::launch_expert_pair<MOE_FMT_NVFP4>(sfmt, down, a, smem, s);
+}
+
+}  // namespace qmoe

@@ -35,11 +35,14 @@ struct RouteOut {
 
 struct RouterArgs {
   int H, E, k, T;
+  int wpr;            // warps per expert row (the row's columns are split between them)
   const uint16_t* x;  // bf16 [T, H]
   const float* w;     // [E, H]
   const float* bias;  // [E] or nullptr
   RouteBufs rb;
   RouteOut out;
+  uint32_t* h_amax;   // [T*k] per-pair max |h| (float bits), zeroed here
+  uint32_t* hs_amax;  // [T] per-token max |h| of the shared expert, zeroed here
 };
 
 // Decode-path expert kernels.
@@ -51,23 +54,35 @@ struct ExpertArgs {
   RouteBufs rb;
   uint16_t* h;        // bf16 [T*k, I]
   uint16_t* hs;       // bf16 [T, Is]
+  uint32_t* h_amax;   // [T*k] max |h| per pair (float bits, atomicMax)
+  uint32_t* hs_amax;  // [T]
   float* P;           // f32 [T*k, H] per-pair down partials
   float* S;           // f32 [T, H] shared expert output
-  uint32_t* rb_cnt;   // [H / (16 * wr_dn)] arrival counters of the combine
+  uint32_t* rb_cnt;   // [H / 16] arrival counters of the combine
   uint16_t* y;        // bf16 [T, H]
-  // warp split of a CTA's 8 warps: wk ways along K, wr ways along rows
-  int wk_gu, wr_gu, wk_dn, wr_dn;
-  // shared-memory layout of the staged activations (in halfs)
-  int xs_q_stride, xs_tok_stride;  // gate/up: x
-  int hs_q_stride, hs_tok_stride;  // down: h
+  int gu_slices, dn_slices;  // K slices per 16-row tile (1 = no split)
+  float* gu_part;     // block sums of split tiles, [tile blocks][32 lanes][8]
+  uint32_t* gu_cnt;   // [tiles] slice arrival counters
+  float* dn_part;     // [tile blocks][32 lanes][4]
+  uint32_t* dn_cnt;   // [tiles]
+  int xs_tok_stride;  // halfs per staged token row (gate/up)
+  int hs_tok_stride;  // halfs per staged hidden row (down)
 };
 
 constexpr int kExpertThreads = 256;  // 8 warps
 constexpr int kRouterThreads = 256;
+// Cap on stored block sums when tiles are split along K (bounds the partial buffers).
+constexpr int kMaxSplitBlocks = 16384;
 
+int router_warps_per_row(int H);
 cudaError_t launch_router_decode(const RouterArgs& a, cudaStream_t s);
-cudaError_t launch_gateup_decode(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s);
-cudaError_t launch_down_decode(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s);
+// Gate/up (down = false) or down + combine (down = true) for a routed format;
+// the shared format is selected at run time among the compiled instances.
+cudaError_t launch_expert_nvfp4(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
+cudaError_t launch_expert_mxfp4(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
+cudaError_t launch_expert_int4(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
+cudaError_t launch_expert_int8(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
+cudaError_t launch_expert_fp8(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
 
 // moe_dequantize / moe_quantize_act_nvfp4
 cudaError_t launch_dequantize(int fmt, QW w, int N, int K, int expert, int row0, int nrows, float* out,
@@ -98,13 +113,20 @@ __host__ __device__ inline size_t scale_bytes(int fmt, int N, int K) {
 // share of K must be a multiple of it.
 __host__ __device__ inline int decode_unit_k(int fmt) {
   switch (fmt) {
-    case MOE_FMT_NVFP4: return 128;
-    case MOE_FMT_MXFP4: return 32;
-    case MOE_FMT_INT4_G64: return 64;
-    case MOE_FMT_INT8_G64: return 64;
-    case MOE_FMT_FP8_B128: return 64;
+    case MOE_FMT_NVFP4: case MOE_FMT_MXFP4: case MOE_FMT_INT4_G64: return 128;  // 16 bytes per lane
+    case MOE_FMT_INT8_G64: case MOE_FMT_FP8_B128: return 64;
     default: return 0;
   }
+}
+
+// The decode kernels sum K as blocks of units (pairs of units when a row has
+// an even number of them): the block layout depends only on (format, K).
+__host__ __device__ inline int dec_block_units(int fmt, int K) {
+  const int u = K / decode_unit_k(fmt);
+  return (u % 2 == 0) ? 2 : 1;
+}
+__host__ __device__ inline int dec_blocks(int fmt, int K) {
+  return K / decode_unit_k(fmt) / dec_block_units(fmt, K);
 }
 
 }  // namespace qmoe
