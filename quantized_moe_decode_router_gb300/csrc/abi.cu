@@ -160,7 +160,7 @@ int choose_slices(int K_r, int fmt_r, long tiles_r, int K_s, int fmt_s, long til
   const int Br = dec_blocks(fmt_r, K_r), Bs = fmt_s ? dec_blocks(fmt_s, K_s) : Br;
   if (tiles_r * Br + tiles_s * Bs > kMaxSplitBlocks) return 1;
   int S = 1;
-  while (Br % (2 * S) == 0 && Bs % (2 * S) == 0 && (tiles_r + tiles_s) * 2 * S <= 2L * warps) S *= 2;
+  while (Br % (2 * S) == 0 && Bs % (2 * S) == 0 && (tiles_r + tiles_s) * 2 * S * 4 <= 5L * warps) S *= 2;
   return S;
 }
 
@@ -192,10 +192,14 @@ RouterArgs router_args(const moe_layer* L, const Layout& lo, void* ws, const voi
 
 int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* y, void* ws, size_t ws_bytes,
                             cudaStream_t stream, void* const* events) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (events) cudaStreamIsCapturing(stream, &cap);
   auto mark = [&](int i) {
-    // external records so that, inside a stream capture, they become event-record nodes
-    if (events && events[i])
-      cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), stream, cudaEventRecordExternal);
+    if (!events || !events[i]) return;
+    cudaEvent_t ev = static_cast<cudaEvent_t>(events[i]);
+    // inside a stream capture an external record becomes an event-record node
+    if (cap == cudaStreamCaptureStatusActive) cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
+    else cudaEventRecord(ev, stream);
   };
   const int maxT = ws_max_tokens(L, ws_bytes);
   const Layout lo = make_layout(L, maxT);
@@ -239,9 +243,11 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   const int Kmax = Is > I ? Is : I;
   ea.hs_tok_stride = Kmax + 16;
 
-  const size_t smem_gu = (size_t)(T + 1) * ea.xs_tok_stride * 2;
-  const size_t smem_dn = (size_t)(MOE_DECODE_MAX_TOKENS + 1) * ea.hs_tok_stride * 2;
-  if (smem_gu > 200 * 1024 || smem_dn > 200 * 1024) return MOE_ERR_UNSUPPORTED;
+  const size_t warps_cta = kExpertThreads / 32;
+  const size_t smem_gu = (size_t)(T + 1) * ea.xs_tok_stride * 2 + warps_cta * kStagesGU * dec_stage_bytes(2);
+  const size_t smem_dn =
+      (size_t)(MOE_DECODE_MAX_TOKENS + 1) * ea.hs_tok_stride * 2 + warps_cta * kStagesDN * dec_stage_bytes(1);
+  if (smem_gu > 227 * 1024 || smem_dn > 227 * 1024) return MOE_ERR_UNSUPPORTED;
 
   mark(0);
   cudaError_t err = launch_router_decode(ra, stream);

@@ -54,7 +54,6 @@ template <> struct Fm<MOE_FMT_INT8_G64> { static constexpr int kBits = 8; };
 template <> struct Fm<MOE_FMT_FP8_B128> { static constexpr int kBits = 8; };
 template <int F> constexpr int unit_k() { return Fm<F>::kBits == 4 ? 128 : 64; }
 template <int F> constexpr int chunk_k() { return unit_k<F>() / 4; }
-constexpr int kPrefetch = 2;
 
 struct Mat {
   const uint8_t* data;
@@ -70,14 +69,54 @@ __device__ __forceinline__ Mat mat_of(const QW& w, int fmt, int e, int N, int K)
   return m;
 }
 
-// Raw scale bits of row R for the lane chunk starting at column k.
+// Byte offset of the scale bits for column k inside one row's scales.
 template <int F>
-__device__ __forceinline__ uint32_t load_scale(const Mat& m, int R, int k) {
-  if constexpr (F == MOE_FMT_NVFP4) return ldg_nc_u16(m.scales + (size_t)R * (m.K / 16) + k / 16);
-  else if constexpr (F == MOE_FMT_MXFP4) return ldg_nc_u8(m.scales + (size_t)R * (m.K / 32) + k / 32);
-  else if constexpr (F == MOE_FMT_INT4_G64 || F == MOE_FMT_INT8_G64)
-    return ldg_nc_u16(m.scales + ((size_t)R * (m.K / 64) + k / 64) * 2);
-  else return ldg_nc_u32(m.scales + ((size_t)(R / 128) * (m.K / 128) + k / 128) * 4);
+__device__ __forceinline__ uint32_t scale_col(int k) {
+  if constexpr (F == MOE_FMT_NVFP4) return (uint32_t)k / 16;
+  else if constexpr (F == MOE_FMT_MXFP4) return (uint32_t)k / 32;
+  else if constexpr (F == MOE_FMT_INT4_G64 || F == MOE_FMT_INT8_G64) return (uint32_t)k / 64 * 2;
+  else return (uint32_t)k / 128 * 4;
+}
+
+// Start of row R's scales (FP8: of its 128-row block).
+template <int F>
+__device__ __forceinline__ const uint8_t* scale_row(const Mat& m, int R) {
+  if constexpr (F == MOE_FMT_NVFP4) return m.scales + (size_t)R * (m.K / 16);
+  else if constexpr (F == MOE_FMT_MXFP4) return m.scales + (size_t)R * (m.K / 32);
+  else if constexpr (F == MOE_FMT_INT4_G64 || F == MOE_FMT_INT8_G64) return m.scales + (size_t)R * (m.K / 64) * 2;
+  else return m.scales + (size_t)(R / 128) * (m.K / 128) * 4;
+}
+
+// The scale bits inside the aligned 32-bit word that holds them (byte offset lo2 = address & 3).
+template <int F>
+__device__ __forceinline__ uint32_t scale_bits(uint32_t w, uint32_t lo2) {
+  if constexpr (F == MOE_FMT_MXFP4) return (w >> (8 * lo2)) & 0xFFu;
+  else if constexpr (F == MOE_FMT_FP8_B128) return w;
+  else return (w >> (8 * lo2)) & 0xFFFFu;
+}
+
+// Per-task view of a warp's rows: data pointers at the lane's first chunk and
+// scale-row pointers; units advance the data by 64 bytes.
+template <int NM>
+struct Stream {
+  const uint8_t* d[NM][2];
+  const uint8_t* s[NM][2];
+};
+
+template <int F, int NM>
+__device__ __forceinline__ Stream<NM> make_stream(const Mat (&m)[NM], int R0, int koff) {
+  constexpr int kB = Fm<F>::kBits;
+  Stream<NM> st;
+#pragma unroll
+  for (int i = 0; i < NM; ++i) {
+    const size_t rb = (size_t)m[i].K * kB / 8;
+    const uint8_t* p0 = m[i].data + (size_t)R0 * rb + (size_t)koff * kB / 8;
+    st.d[i][0] = p0;
+    st.d[i][1] = p0 + 8 * rb;
+    st.s[i][0] = scale_row<F>(m[i], R0);
+    st.s[i][1] = scale_row<F>(m[i], R0 + 8);
+  }
+  return st;
 }
 
 template <int NM>
@@ -86,18 +125,39 @@ struct Unit {
   uint32_t s[NM][2];
 };
 
+// Warp-private shared-memory ring: one stage holds a unit of every lane,
+// data [NM][2 rows][32 lanes] x 16 B followed by scale words [NM][2][32] x 4 B.
+template <int NM>
+constexpr int stage_bytes() { return dec_stage_bytes(NM); }
+
 template <int F, int NM>
-__device__ __forceinline__ void load_unit(Unit<NM>& u, const Mat (&m)[NM], int R0, int kc) {
-  constexpr int kB = Fm<F>::kBits;
+__device__ __forceinline__ void issue_unit(uint8_t* stage, const Stream<NM>& st, int u, int kc) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t sc = scale_col<F>(kc);
 #pragma unroll
-  for (int i = 0; i < NM; ++i) {
-    const size_t rb = (size_t)m[i].K * kB / 8;
-    const uint8_t* p0 = m[i].data + (size_t)R0 * rb + (size_t)kc * kB / 8;
-    u.d[i][0] = ldg_nc_v4(p0);
-    u.d[i][1] = ldg_nc_v4(p0 + 8 * rb);
-    u.s[i][0] = load_scale<F>(m[i], R0, kc);
-    u.s[i][1] = load_scale<F>(m[i], R0 + 8, kc);
-  }
+  for (int i = 0; i < NM; ++i)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      cp_async16(stage + ((i * 2 + r) * 32 + lane) * 16, st.d[i][r] + (size_t)u * 64);
+      const uintptr_t sp = reinterpret_cast<uintptr_t>(st.s[i][r]) + sc;
+      cp_async4(stage + NM * 2 * 32 * 16 + ((i * 2 + r) * 32 + lane) * 4,
+                reinterpret_cast<const void*>(sp & ~(uintptr_t)3));
+    }
+}
+
+template <int F, int NM>
+__device__ __forceinline__ void read_unit(Unit<NM>& u, const uint8_t* stage, const Stream<NM>& st, int kc) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t sc = scale_col<F>(kc);
+#pragma unroll
+  for (int i = 0; i < NM; ++i)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      u.d[i][r] = *reinterpret_cast<const uint4*>(stage + ((i * 2 + r) * 32 + lane) * 16);
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(stage + NM * 2 * 32 * 16 + ((i * 2 + r) * 32 + lane) * 4);
+      const uint32_t lo2 = ((uint32_t)reinterpret_cast<uintptr_t>(st.s[i][r]) + sc) & 3u;
+      u.s[i][r] = scale_bits<F>(w, lo2);
+    }
 }
 
 __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
@@ -300,56 +360,65 @@ __device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl
 }
 
 // One warp: rows [row0, row0 + 16) of NM matrices over columns [kb, kb + Kw)
-// (Kw a multiple of the block).  Units stream through a kPrefetch-deep
-// register ring; the trip count is warp-uniform.  The K range is summed as
-// blocks of `bu` units, each block from zero; block sums are either added to
-// acc in block order (bpart == nullptr) or stored to bpart[b] for the
-// tile's last slice to add in the same order.  The association of the sum
-// therefore depends only on K, never on how K is split between warps.
-template <int F, int NM>
+// (Kw a multiple of the block).  Units stream from HBM into the warp's
+// private shared-memory ring of PF stages with cp.async (PF - 1 units in
+// flight while one is decoded), so the bytes in flight do not cost
+// registers.  Each lane copies and reads back only its own chunk, so the
+// per-thread cp.async groups are the only synchronisation needed.  The trip
+// count is warp-uniform (mma.sync needs the whole warp).  The K range is
+// summed as blocks of `bu` units, each block from zero; block sums are either
+// added to acc in block order (bpart == nullptr) or stored to bpart[b] for
+// the tile's last slice to add in the same order, so the association of the
+// sum depends only on K, never on how K is split between warps.
+template <int F, int NM, int PF>
 __device__ __forceinline__ void warp_tile(const Mat (&m)[NM], int row0, int kb, int Kw, int bu, const __half* xrow,
-                                          float (&acc)[NM][4], float* bpart) {
-  constexpr int UK = unit_k<F>(), CK = chunk_k<F>(), PF = kPrefetch;
+                                          float (&acc)[NM][4], float* bpart, uint8_t* ring) {
+  constexpr int UK = unit_k<F>(), CK = chunk_k<F>(), SB = stage_bytes<NM>();
   const int lane = threadIdx.x & 31;
   const int R0 = row0 + (lane >> 2);
   const int koff = kb + (lane & 3) * CK;
   const int nU = Kw / UK;
-  Unit<NM> buf[PF];
   float blk[NM][4];
 #pragma unroll
   for (int i = 0; i < NM; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) blk[i][j] = 0.f;
+  const Stream<NM> st = make_stream<F, NM>(m, R0, koff);
 #pragma unroll
-  for (int p = 0; p < PF; ++p)
-    if (p < nU) load_unit<F, NM>(buf[p], m, R0, koff + p * UK);
-  for (int u0 = 0; u0 < nU; u0 += PF) {
+  for (int p = 0; p < PF - 1; ++p) {
+    if (p < nU) issue_unit<F, NM>(ring + p * SB, st, p, koff + p * UK);
+    cp_async_commit();
+  }
+  int slot_issue = PF - 1, slot_read = 0;
+  for (int u = 0; u < nU; ++u) {
+    const int un = u + PF - 1;
+    if (un < nU) issue_unit<F, NM>(ring + slot_issue * SB, st, un, koff + un * UK);
+    cp_async_commit();
+    cp_async_wait<PF - 1>();  // unit u has landed
+    Unit<NM> cur;
+    read_unit<F, NM>(cur, ring + slot_read * SB, st, koff + u * UK);
+    slot_issue = (slot_issue + 1 == PF) ? 0 : slot_issue + 1;
+    slot_read = (slot_read + 1 == PF) ? 0 : slot_read + 1;
+    compute_unit<F, NM>(cur, xrow + koff + u * UK, blk);
+    if ((u + 1) % bu == 0) {  // block complete
+      if (bpart) {
+        float* d = bpart + (size_t)(u / bu) * (32 * 4 * NM) + lane * 4 * NM;
 #pragma unroll
-    for (int p = 0; p < PF; ++p) {
-      const int u = u0 + p;
-      if (u < nU) {
-        compute_unit<F, NM>(buf[p], xrow + koff + u * UK, blk);
-        if (u + PF < nU) load_unit<F, NM>(buf[p], m, R0, koff + (u + PF) * UK);
-        if ((u + 1) % bu == 0) {  // block complete
-          if (bpart) {
-            float* d = bpart + (size_t)(u / bu) * (32 * 4 * NM) + lane * 4 * NM;
+        for (int i = 0; i < NM; ++i)
+          *reinterpret_cast<float4*>(d + 4 * i) = make_float4(blk[i][0], blk[i][1], blk[i][2], blk[i][3]);
+      } else {
 #pragma unroll
-            for (int i = 0; i < NM; ++i)
-              *reinterpret_cast<float4*>(d + 4 * i) = make_float4(blk[i][0], blk[i][1], blk[i][2], blk[i][3]);
-          } else {
+        for (int i = 0; i < NM; ++i)
 #pragma unroll
-            for (int i = 0; i < NM; ++i)
-#pragma unroll
-              for (int j = 0; j < 4; ++j) acc[i][j] += blk[i][j];
-          }
-#pragma unroll
-          for (int i = 0; i < NM; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) blk[i][j] = 0.f;
-        }
+          for (int j = 0; j < 4; ++j) acc[i][j] += blk[i][j];
       }
+#pragma unroll
+      for (int i = 0; i < NM; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) blk[i][j] = 0.f;
     }
   }
+  cp_async_wait<0>();
 }
 
 // Largest-magnitude element -> exponent p with amax * 2^-p in [2^14, 2^15).
@@ -362,8 +431,11 @@ __device__ __forceinline__ int scale_exponent_bits(uint32_t amax_bits) {
 
 // Stage bf16 rows into shared memory as f16 scaled by 2^-p (p from the row's
 // amax, computed here when amax_bits is null).  Row `nrows` is zero-filled.
-static __device__ void stage_rows_f16(const uint16_t* const* src, const uint32_t* amax_bits, int nrows, int K, __half* dst,
-                               int stride, int* pexp) {
+// Loads are issued in batches of eight per lane so a row costs about one
+// memory round trip per 2048 elements.
+static __device__ void stage_rows_f16(const uint16_t* const* src, const uint32_t* amax_bits, int nrows, int K,
+                                      __half* dst, int stride, int* pexp) {
+  constexpr int kBatch = 8;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int r = warp; r < nrows; r += kWarps) {
     const uint16_t* s = src[r];
@@ -372,12 +444,20 @@ static __device__ void stage_rows_f16(const uint16_t* const* src, const uint32_t
       am = amax_bits[r];
     } else {
       float amax = 0.f;
-      for (int k = lane * 8; k < K; k += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(s + k);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (int k0 = 0; k0 < K; k0 += kBatch * 256) {
+        uint4 v[kBatch];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[j] & 0xFFFF)), fabsf(bf16_bits_to_float(w[j] >> 16))));
+        for (int j = 0; j < kBatch; ++j) {
+          const int k = k0 + j * 256 + lane * 8;
+          v[j] = (k < K) ? *reinterpret_cast<const uint4*>(s + k) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[q] & 0xFFFF)), fabsf(bf16_bits_to_float(w[q] >> 16))));
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
@@ -387,16 +467,28 @@ static __device__ void stage_rows_f16(const uint16_t* const* src, const uint32_t
     if (lane == 0) pexp[r] = p;
     const float inv = exp2i(-p);
     __half* d = dst + (size_t)r * stride;
-    for (int k = lane * 8; k < K; k += 256) {
-      const uint4 v = *reinterpret_cast<const uint4*>(s + k);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[4];
+    for (int k0 = 0; k0 < K; k0 += kBatch * 256) {
+      uint4 v[kBatch];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        __half2 hh = __floats2half2_rn(bf16_bits_to_float(w[j] & 0xFFFF) * inv, bf16_bits_to_float(w[j] >> 16) * inv);
-        o[j] = *reinterpret_cast<uint32_t*>(&hh);
+      for (int j = 0; j < kBatch; ++j) {
+        const int k = k0 + j * 256 + lane * 8;
+        v[j] = (k < K) ? *reinterpret_cast<const uint4*>(s + k) : make_uint4(0, 0, 0, 0);
       }
-      *reinterpret_cast<uint4*>(d + k) = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int k = k0 + j * 256 + lane * 8;
+        if (k < K) {
+          const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            __half2 hh = __floats2half2_rn(bf16_bits_to_float(w[q] & 0xFFFF) * inv,
+                                           bf16_bits_to_float(w[q] >> 16) * inv);
+            o[q] = *reinterpret_cast<uint32_t*>(&hh);
+          }
+          *reinterpret_cast<uint4*>(d + k) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
     }
   }
   __half* z = dst + (size_t)nrows * stride;
@@ -444,11 +536,11 @@ __device__ __forceinline__ bool block_reduce(float (&acc)[NM][4], const float* t
 
 template <int FR, int FS>
 __device__ __forceinline__ void gu_tile(int fmt_is_shared, const Mat (&m)[2], int row0, int kb, int Kw, int bu,
-                                        const __half* xrow, float (&acc)[2][4], float* bpart) {
+                                        const __half* xrow, float (&acc)[2][4], float* bpart, uint8_t* ring) {
   if (fmt_is_shared) {
-    if constexpr (FS != 0) warp_tile<FS, 2>(m, row0, kb, Kw, bu, xrow, acc, bpart);
+    if constexpr (FS != 0) warp_tile<FS, 2, kStagesGU>(m, row0, kb, Kw, bu, xrow, acc, bpart, ring);
   } else {
-    warp_tile<FR, 2>(m, row0, kb, Kw, bu, xrow, acc, bpart);
+    warp_tile<FR, 2, kStagesGU>(m, row0, kb, Kw, bu, xrow, acc, bpart, ring);
   }
 }
 
@@ -459,6 +551,7 @@ __global__ void __launch_bounds__(kExpertThreads, 2) gateup_kernel(ExpertArgs a)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int xs_stride = a.xs_tok_stride;
   __half* xs = reinterpret_cast<__half*>(smem);  // [T + 1][xs_stride]
+  uint8_t* ring = smem + (size_t)(T + 1) * xs_stride * 2 + (size_t)warp * kStagesGU * stage_bytes<2>();
   __shared__ int s_pexp[kMaxT + 1];
   __shared__ const uint16_t* s_src[kMaxT];
 
@@ -523,7 +616,7 @@ __global__ void __launch_bounds__(kExpertThreads, 2) gateup_kernel(ExpertArgs a)
                                                 : (size_t)tile_id * Br) * (32 * 8);
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     gu_tile<FR, FS>(shared_item, m, row0, slice * Kw, Kw, shared_item ? bus : bur, xs + (size_t)col_tok * xs_stride,
-                    acc, S > 1 ? tile_part + (size_t)slice * (B / S) * (32 * 8) : nullptr);
+                    acc, S > 1 ? tile_part + (size_t)slice * (B / S) * (32 * 8) : nullptr, ring);
     if (!block_reduce<2>(acc, tile_part, a.gu_cnt + tile_id, S, B)) continue;
     const float tsg = (fmt == MOE_FMT_NVFP4) ? __ldg(qg.ts + e) : 1.f;
     const float tsu = (fmt == MOE_FMT_NVFP4) ? __ldg(qu.ts + e) : 1.f;
@@ -563,6 +656,7 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int hs_stride = a.hs_tok_stride;
   __half* hsm = reinterpret_cast<__half*>(smem);  // [kMaxT + 1][hs_stride]
+  uint8_t* ring = smem + (size_t)(kMaxT + 1) * hs_stride * 2 + (size_t)warp * kStagesDN * stage_bytes<1>();
   __shared__ int s_pexp[kMaxT + 1];
   __shared__ int s_col_out[kMaxT];
   __shared__ const uint16_t* s_src[kMaxT];
@@ -630,9 +724,9 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
                                                   : (size_t)tile_id * Br) * (32 * 4);
       float* bpart = S > 1 ? tile_part + (size_t)slice * (B / S) * (32 * 4) : nullptr;
       if (shared_item) {
-        if constexpr (FS != 0) warp_tile<FS, 1>(m, tile * 16, slice * Kw, Kw, bu, xrow, acc, bpart);
+        if constexpr (FS != 0) warp_tile<FS, 1, kStagesDN>(m, tile * 16, slice * Kw, Kw, bu, xrow, acc, bpart, ring);
       } else {
-        warp_tile<FR, 1>(m, tile * 16, slice * Kw, Kw, bu, xrow, acc, bpart);
+        warp_tile<FR, 1, kStagesDN>(m, tile * 16, slice * Kw, Kw, bu, xrow, acc, bpart, ring);
       }
       if (!block_reduce<1>(acc, tile_part, a.dn_cnt + tile_id, S, B)) continue;
       const float ts = (fmt == MOE_FMT_NVFP4) ? __ldg(qd.ts + e) : 1.f;

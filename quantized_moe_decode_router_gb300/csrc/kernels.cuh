@@ -70,6 +70,10 @@ struct ExpertArgs {
 };
 
 constexpr int kExpertThreads = 256;  // 8 warps
+constexpr int kStagesGU = 3;         // cp.async ring stages per warp, gate/up (two matrices per unit)
+constexpr int kStagesDN = 4;         // cp.async ring stages per warp, down (one matrix per unit)
+// Bytes of one ring stage: NM matrices x 2 rows x 32 lanes x (16 B codes + 4 B scale word).
+constexpr int dec_stage_bytes(int nm) { return nm * 2 * 32 * (16 + 4); }
 constexpr int kRouterThreads = 256;
 // Cap on stored block sums when tiles are split along K (bounds the partial buffers).
 constexpr int kMaxSplitBlocks = 16384;

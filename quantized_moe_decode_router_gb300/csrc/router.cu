@@ -22,43 +22,71 @@ namespace {
 constexpr int kMaxT = MOE_DECODE_MAX_TOKENS;
 constexpr int kWarpsR = kRouterThreads / 32;
 
-// Larger logit first; equal logits -> smaller expert id first.  A NaN logit
-// ranks like -inf, so every untaken expert beats the empty state.
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  if (v != v) v = -__int_as_float(0x7F800000);
-  return (v > bv) || (v == bv && i < bi);
+// Selection key of a candidate: larger logit first, equal logits -> smaller
+// expert id first, as one unsigned 64-bit maximum.  The float is mapped to
+// an order-preserving unsigned integer (NaN ranks like -inf); the low half is
+// the complemented expert id.  0 marks a taken or absent entry: every real
+// candidate, even a -inf logit, has a larger key.
+__device__ __forceinline__ unsigned long long sel_key(float v, int e) {
+  uint32_t b = __float_as_uint(v);
+  if (v != v) b = 0xFF800000u;  // -inf
+  if (b == 0x80000000u) b = 0;  // -0 ties with +0
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (uint32_t)(~(uint32_t)e);
 }
 
-// One warp: top-k of one token.  E <= 1024: lane holds experts lane + 32 q.
+__device__ __forceinline__ float key_value(unsigned long long k) {
+  const uint32_t ord = (uint32_t)(k >> 32);
+  return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+}
+
+__device__ __forceinline__ int key_id(unsigned long long k) { return (int)(~(uint32_t)k); }
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+
+// Largest of the lane's NQ keys, as a tournament (depth log2 NQ).
+template <int NQ>
+__device__ __forceinline__ unsigned long long lane_max(const unsigned long long (&key)[NQ]) {
+  unsigned long long t[NQ / 2];
+#pragma unroll
+  for (int q = 0; q < NQ / 2; ++q) t[q] = umax64(key[2 * q], key[2 * q + 1]);
+#pragma unroll
+  for (int w = NQ / 4; w > 0; w >>= 1)
+#pragma unroll
+    for (int q = 0; q < w; ++q) t[q] = umax64(t[2 * q], t[2 * q + 1]);
+  return t[0];
+}
+
+// One warp: top-k of one token.  E <= 32 NQ: lane holds the keys of experts
+// lane + 32 q in registers; after each round only the lane whose candidate
+// won recomputes its maximum.
+template <int NQ>
 __device__ void topk_warp(const float* __restrict__ logits_row, int E, int k, int32_t* idx_out, float* w_out,
                           int32_t* idx_out2, float* w_out2) {
   const int lane = threadIdx.x & 31;
-  const float kNegInf = -__int_as_float(0x7F800000);
-  float v[32];
+  unsigned long long key[NQ];
 #pragma unroll
-  for (int q = 0; q < 32; ++q) {
+  for (int q = 0; q < NQ; ++q) {
     const int e = q * 32 + lane;
-    v[q] = (e < E) ? __ldcg(logits_row + e) : kNegInf;
-    if (v[q] != v[q]) v[q] = kNegInf;
+    key[q] = (e < E) ? sel_key(__ldcg(logits_row + e), e) : 0ull;
   }
-  uint32_t taken = 0;
+  unsigned long long mine = lane_max<NQ>(key);
   float sel_v0 = 0.f, sum = 0.f, my_ex = 0.f;
   int my_i = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = kNegInf;
-    int bi = 0x7FFFFFFF;
+    unsigned long long best = mine;
 #pragma unroll
-    for (int q = 0; q < 32; ++q) {
-      const int e = q * 32 + lane;
-      if (e < E && !((taken >> q) & 1u) && better(v[q], e, bv, bi)) { bv = v[q]; bi = e; }
-    }
+    for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+    const int bi = key_id(best);
+    if (best == mine) {  // this lane's candidate won: drop it, find the next one
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      for (int q = 0; q < NQ; ++q)
+        if (q == (bi >> 5)) key[q] = 0ull;
+      mine = lane_max<NQ>(key);
     }
-    if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const float bv = key_value(best);
     if (j == 0) sel_v0 = bv;
     // w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0); the sum runs in j order
     const float ex = expf(bv - sel_v0);
@@ -75,8 +103,7 @@ __device__ void topk_warp(const float* __restrict__ logits_row, int E, int k, in
 }
 
 // Logits of this CTA's expert rows; returns after writing them to global memory.
-__device__ void router_logits_cta(const RouterArgs& a, const uint16_t* xs, float (*s_hi)[kMaxT],
-                                  float (*s_lo)[kMaxT]) {
+__device__ void router_logits_cta(const RouterArgs& a, float (*s_hi)[kMaxT], float (*s_lo)[kMaxT]) {
   const int H = a.H, E = a.E, T = a.T, wpr = a.wpr;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rows_per_cta = kWarpsR / wpr;
@@ -88,14 +115,14 @@ __device__ void router_logits_cta(const RouterArgs& a, const uint16_t* xs, float
   for (int t = 0; t < kMaxT; ++t) { hi[t] = 0.f; lo[t] = 0.f; }
   if (e < E) {
     const float4* wrow = reinterpret_cast<const float4*>(a.w + (size_t)e * H + (size_t)part * Hw);
-    const uint16_t* xp = xs + (size_t)part * Hw;
+    const uint16_t* xp = a.x + (size_t)part * Hw;  // the tokens are small and stay in L1/L2
 #pragma unroll 2
     for (int h4 = lane; h4 < Hw / 4; h4 += 32) {
       const float4 wv = __ldg(wrow + h4);
 #pragma unroll
       for (int t = 0; t < kMaxT; ++t) {
         if (t < T) {
-          const uint2 xv = *reinterpret_cast<const uint2*>(xp + (size_t)t * H + h4 * 4);
+          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(xp + (size_t)t * H + h4 * 4));
           dot2_step(bf16_bits_to_float(xv.x & 0xFFFF), wv.x, hi[t], lo[t]);
           dot2_step(bf16_bits_to_float(xv.x >> 16), wv.y, hi[t], lo[t]);
           dot2_step(bf16_bits_to_float(xv.y & 0xFFFF), wv.z, hi[t], lo[t]);
@@ -131,8 +158,7 @@ __device__ void router_logits_cta(const RouterArgs& a, const uint16_t* xs, float
 }
 
 __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // bf16 [T][H]
+  extern __shared__ __align__(16) uint8_t smem[];  // dispatch scratch of the last CTA
   __shared__ float s_hi[kWarpsR][kMaxT], s_lo[kWarpsR][kMaxT];
   __shared__ int is_last;
   const int H = a.H, E = a.E, T = a.T, k = a.k;
@@ -140,14 +166,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArg
   // the expert kernel that follows may be scheduled now: it stages the
   // activations and then waits for this grid's results (griddepcontrol.wait)
   asm volatile("griddepcontrol.launch_dependents;");
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(a.x);
-    uint4* dst = reinterpret_cast<uint4*>(xs);
-    const int n16 = T * H / 8;
-    for (int i = tid; i < n16; i += blockDim.x) dst[i] = src[i];
-  }
-  __syncthreads();
-  router_logits_cta(a, xs, s_hi, s_lo);
+  router_logits_cta(a, s_hi, s_lo);
 
   // ---- last CTA: top-k and dispatch ----
   __syncthreads();
@@ -160,9 +179,16 @@ __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArg
   if (!is_last) return;
   __threadfence();
 
-  for (int t = warp; t < T; t += kWarpsR)
-    topk_warp(a.rb.logits + (size_t)t * E, E, k, a.rb.topk_idx + t * k, a.rb.topk_w + t * k,
-              a.out.topk_idx ? a.out.topk_idx + t * k : nullptr, a.out.topk_w ? a.out.topk_w + t * k : nullptr);
+  for (int t = warp; t < T; t += kWarpsR) {
+    const float* lr = a.rb.logits + (size_t)t * E;
+    int32_t* io = a.rb.topk_idx + t * k;
+    float* wo = a.rb.topk_w + t * k;
+    int32_t* io2 = a.out.topk_idx ? a.out.topk_idx + t * k : nullptr;
+    float* wo2 = a.out.topk_w ? a.out.topk_w + t * k : nullptr;
+    if (E <= 256) topk_warp<8>(lr, E, k, io, wo, io2, wo2);
+    else if (E <= 512) topk_warp<16>(lr, E, k, io, wo, io2, wo2);
+    else topk_warp<32>(lr, E, k, io, wo, io2, wo2);
+  }
   // the expert kernels accumulate per-pair maxima with atomicMax: start them at zero
   if (a.h_amax)
     for (int i = tid; i < T * k; i += blockDim.x) a.h_amax[i] = 0u;
@@ -183,29 +209,44 @@ __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArg
     atomicAdd(&s_cnt[ex], 1);
   }
   __syncthreads();
-  if (warp == 0) {
-    // exclusive scan over E counts, and the compacted list of active experts
-    int run = 0, run_act = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e2 = base + lane;
-      const int c = (e2 < E) ? s_cnt[e2] : 0;
-      int incl = c, act_incl = (c > 0);
+  {
+    // exclusive scan over the E counts and over the active flags, by the whole
+    // CTA: each thread owns up to four consecutive experts
+    __shared__ int s_wsum[kWarpsR][2];
+    const int per = (E + kRouterThreads - 1) / kRouterThreads;  // <= 4 for E <= 1024
+    const int e0 = tid * per;
+    int c4[4], tot = 0, act = 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        const int va = __shfl_up_sync(0xFFFFFFFFu, act_incl, o);
-        if (lane >= o) { incl += v; act_incl += va; }
-      }
-      if (e2 < E) {
-        s_off[e2] = run + incl - c;
-        a.rb.cnt[e2] = c;
-        if (a.out.cnt) a.out.cnt[e2] = c;
-        if (c > 0) a.rb.act[run_act + act_incl - 1] = e2;
-      }
-      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
-      run_act += __shfl_sync(0xFFFFFFFFu, act_incl, 31);
+    for (int q = 0; q < 4; ++q) {
+      const int e2 = e0 + q;
+      c4[q] = (q < per && e2 < E) ? s_cnt[e2] : 0;
+      tot += c4[q];
+      act += c4[q] > 0;
     }
-    if (lane == 0) {
+    int incl = tot, ainc = act;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      const int va = __shfl_up_sync(0xFFFFFFFFu, ainc, o);
+      if (lane >= o) { incl += v; ainc += va; }
+    }
+    if (lane == 31) { s_wsum[warp][0] = incl; s_wsum[warp][1] = ainc; }
+    __syncthreads();
+    int wbase = 0, abase = 0;
+    for (int w2 = 0; w2 < warp; ++w2) { wbase += s_wsum[w2][0]; abase += s_wsum[w2][1]; }
+    int run = wbase + incl - tot, run_act = abase + ainc - act;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e2 = e0 + q;
+      if (q < per && e2 < E) {
+        s_off[e2] = run;
+        a.rb.cnt[e2] = c4[q];
+        if (a.out.cnt) a.out.cnt[e2] = c4[q];
+        if (c4[q] > 0) a.rb.act[run_act++] = e2;
+        run += c4[q];
+      }
+    }
+    if (tid == kRouterThreads - 1) {
       s_off[E] = run;
       a.rb.ctrl->n_active = run_act;
     }
@@ -228,19 +269,17 @@ __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArg
 
 }  // namespace
 
-// Warps sharing one expert row: split H while each warp keeps >= 256 columns.
+// Warps sharing one expert row: split H while each warp keeps >= 512 columns.
 int router_warps_per_row(int H) {
   int w = 1;
-  while (w < kWarpsR && H % (4 * 32 * w * 2) == 0 && H / (w * 2) >= 256) w *= 2;
+  while (w < kWarpsR && H % (4 * 32 * w * 2) == 0 && H / (w * 2) >= 512) w *= 2;
   return w;
 }
 
 cudaError_t launch_router_decode(const RouterArgs& a, cudaStream_t s) {
   const int rows_per_cta = kWarpsR / a.wpr;
   const int grid = (a.E + rows_per_cta - 1) / rows_per_cta;
-  const size_t smem_x = (size_t)a.T * a.H * 2;
-  const size_t smem_d = (size_t)(2 * a.E + 1 + a.T * a.k) * 4;
-  const size_t smem = smem_x > smem_d ? smem_x : smem_d;
+  const size_t smem = (size_t)(2 * a.E + 1 + a.T * a.k) * 4;
   cudaError_t err = cudaFuncSetAttribute(router_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;
