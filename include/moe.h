@@ -189,6 +189,27 @@ int32_t moe_decode_forward_timed(const moe_layer* layer, const void* x, int32_t 
                                  void* const* events);
 
 /*
+ * moe_decode_forward without a caller-supplied workspace, for callers that
+ * cannot allocate device memory: code running inside a host framework that
+ * owns every device buffer and gives plugins no allocator, or a serving loop
+ * that forbids allocations once it has started.  (The DGPP pages have no
+ * counterpart; this is an interface convenience of this library.)
+ *  - The workspace is a fixed 32 MiB array in the library's device memory;
+ *    every GPU that loads the library holds it until the process exits.  A
+ *    layer and T whose moe_workspace_size exceeds 32 MiB are rejected with
+ *    MOE_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address and
+ *    zeroes it synchronously; make that first call before any stream capture.
+ *  - Every call shares the one array (the arrival counters it needs at zero
+ *    are cleared on `stream` at the start of each call), so calls that
+ *    overlap on the GPU, from any stream or thread, race: serialise them.
+ *  - The routing results stay in the array; they are not exposed.
+ * Other arguments, checks and results are those of moe_decode_forward.
+ */
+int32_t moe_decode_forward_noalloc(const moe_layer* layer, const void* x /* device bf16 [T, H] */, int32_t T,
+                                   void* y /* device bf16 [T, H] */, const moe_options* opts, moe_stream_t stream);
+
+/*
  * Read and clear the device-side error flag of a workspace.  Synchronises
  * `stream` (this is the one call that blocks).  Returns MOE_OK,
  * MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BAD_INDEX.

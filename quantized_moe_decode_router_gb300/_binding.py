@@ -68,6 +68,8 @@ _SIGNATURES = {
     "moe_decode_forward_timed": (ctypes.c_int32, [_P(moe_layer), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                                   _P(moe_options), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                                   ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_decode_forward_noalloc": (ctypes.c_int32, [_P(moe_layer), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                                    _P(moe_options), ctypes.c_void_p]),
     "moe_check": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_workspace_layout": (ctypes.c_int32, [_P(moe_layer), ctypes.c_int32, _P(moe_options), _P(moe_ws_layout)]),
     "moe_dequantize": (ctypes.c_int32, [ctypes.c_int32, _P(moe_qweight), ctypes.c_int32, ctypes.c_int32,
@@ -206,6 +208,14 @@ def moe_decode_forward_timed(layer: Layer, x, T: int, y, ws, events, stream=None
     st = load().moe_decode_forward_timed(ctypes.byref(lc), _ptr(x), T, _ptr(y), ctypes.byref(o), _ptr(ws),
                                          ws.numel() * ws.element_size(), _stream_handle(stream), arr)
     return _check(st, "moe_decode_forward_timed")
+
+
+def moe_decode_forward_noalloc(layer: Layer, x, T: int, y, stream=None, raise_on_error: bool = True) -> int:
+    """moe_decode_forward on the library's fixed device workspace (no caller workspace, no allocation)."""
+    lc, o = layer.c(), _opts(0)
+    st = load().moe_decode_forward_noalloc(ctypes.byref(lc), _ptr(x), T, _ptr(y), ctypes.byref(o),
+                                           _stream_handle(stream))
+    return _check(st, "moe_decode_forward_noalloc") if raise_on_error else st
 
 
 def moe_prefill_forward(layer: Layer, x, T: int, y, ws, stream=None, act_quant: int = 0,

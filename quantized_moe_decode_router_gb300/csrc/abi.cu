@@ -263,6 +263,19 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
 
 }  // namespace
 
+int32_t qmoe::clear_workspace_counters(const moe_layer* L, void* ws, size_t ws_bytes, cudaStream_t s) {
+  const Layout lo = make_layout(L, ws_max_tokens(L, ws_bytes));
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  const size_t H = (size_t)L->hidden;
+  const size_t sections[4][2] = {{lo.ctrl, sizeof(Ctrl)},
+                                 {lo.rb_cnt, H / 16 * 4},
+                                 {lo.gu_cnt, lo.dn_part - lo.gu_cnt},
+                                 {lo.dn_cnt, lo.total - lo.dn_cnt}};
+  for (const auto& sec : sections)
+    if (cudaMemsetAsync(b + sec[0], 0, sec[1], s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 extern "C" {
 
 const char* moe_status_string(int32_t status) {

@@ -79,6 +79,9 @@ constexpr int kRouterThreads = 256;
 constexpr int kMaxSplitBlocks = 16384;
 
 int router_warps_per_row(int H);
+// Zero the control block and every arrival counter of a workspace laid out
+// for this layer and workspace size (stream-ordered memsets, no allocation).
+int32_t clear_workspace_counters(const moe_layer* L, void* ws, size_t ws_bytes, cudaStream_t s);
 cudaError_t launch_router_decode(const RouterArgs& a, cudaStream_t s);
 // Gate/up (down = false) or down + combine (down = true) for a routed format;
 // the shared format is selected at run time among the compiled instances.
