@@ -28,7 +28,11 @@ bool shape_ok(int fmt, int N, int K) {
 
 struct Layout {
   size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, rb_cnt, h_amax, hs_amax, gu_part, gu_cnt,
-      dn_part, dn_cnt, total;
+      dn_part, dn_cnt;
+  // prefill path
+  size_t xs, xsig, xnorm, wnorm, hist, pos_of, tiles, h16, hsig;
+  int max_tiles;
+  size_t total;
 };
 
 Layout make_layout(const moe_layer* L, int maxT) {
@@ -63,6 +67,17 @@ Layout make_layout(const moe_layer* L, int maxT) {
   o.gu_cnt = take(gu_tiles * 4);
   o.dn_part = take((size_t)kMaxSplitBlocks * 32 * 4 * 4);
   o.dn_cnt = take(dn_tiles * 4);
+  const size_t nchunk = (T + kPfChunk - 1) / kPfChunk;
+  o.max_tiles = (int)(T * k / kPfTokTile + E + 1);
+  o.xs = take(T * H * 2);
+  o.xsig = take(T * 4);
+  o.xnorm = take(T * 4);
+  o.wnorm = take(E * 4);
+  o.hist = take(nchunk * E * 4);
+  o.pos_of = take(T * k * 4);
+  o.tiles = take((size_t)o.max_tiles * 8);
+  o.h16 = take(T * k * I * 2);
+  o.hsig = take(T * k * 4);
   o.total = at;
   return o;
 }
@@ -261,6 +276,47 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   return cuda_status(err);
 }
 
+PrefillArgs prefill_args(const moe_layer* L, const Layout& lo, void* ws, const void* x, int T, void* y) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  PrefillArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.H = L->hidden; a.I = L->inter; a.E = L->n_experts; a.k = L->top_k; a.T = T;
+  a.fmt = L->fmt;
+  a.x = static_cast<const uint16_t*>(x);
+  a.rw = L->router_w;
+  a.bias = L->router_bias;
+  a.gate = qw(L->gate, L->fmt); a.up = qw(L->up, L->fmt); a.down = qw(L->down, L->fmt);
+  a.rb = route_bufs(lo, ws);
+  a.xs = reinterpret_cast<uint16_t*>(b + lo.xs);
+  a.xsig = reinterpret_cast<int32_t*>(b + lo.xsig);
+  a.xnorm = reinterpret_cast<float*>(b + lo.xnorm);
+  a.wnorm = reinterpret_cast<float*>(b + lo.wnorm);
+  a.hist = reinterpret_cast<int32_t*>(b + lo.hist);
+  a.pos_of = reinterpret_cast<int32_t*>(b + lo.pos_of);
+  a.tiles = reinterpret_cast<int2*>(b + lo.tiles);
+  a.max_tiles = lo.max_tiles;
+  a.h = reinterpret_cast<uint16_t*>(b + lo.h);
+  a.h_amax = reinterpret_cast<uint32_t*>(b + lo.h_amax);
+  a.h16 = reinterpret_cast<uint16_t*>(b + lo.h16);
+  a.hsig = reinterpret_cast<int32_t*>(b + lo.hsig);
+  a.P = reinterpret_cast<float*>(b + lo.P);
+  a.y = static_cast<uint16_t*>(y);
+  return a;
+}
+
+int sm_count(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// Formats the prefill expert GEMMs implement so far.
+bool prefill_supported(const moe_layer* L) {
+  return L->fmt == MOE_FMT_NVFP4 && L->shared_fmt == MOE_FMT_NONE && L->hidden % 128 == 0 &&
+         L->inter % 128 == 0;
+}
+
 }  // namespace
 
 int32_t qmoe::clear_workspace_counters(const moe_layer* L, void* ws, size_t ws_bytes, cudaStream_t s) {
@@ -270,7 +326,7 @@ int32_t qmoe::clear_workspace_counters(const moe_layer* L, void* ws, size_t ws_b
   const size_t sections[4][2] = {{lo.ctrl, sizeof(Ctrl)},
                                  {lo.rb_cnt, H / 16 * 4},
                                  {lo.gu_cnt, lo.dn_part - lo.gu_cnt},
-                                 {lo.dn_cnt, lo.total - lo.dn_cnt}};
+                                 {lo.dn_cnt, lo.xs - lo.dn_cnt}};
   for (const auto& sec : sections)
     if (cudaMemsetAsync(b + sec[0], 0, sec[1], s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
@@ -329,13 +385,19 @@ int32_t moe_route(const moe_layer* layer, const void* x, int32_t T, int32_t* top
   if (!x) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x)) return MOE_ERR_MISALIGNED;
   if (T < 1) return MOE_ERR_INVALID_ARG;
-  if (T > MOE_DECODE_MAX_TOKENS) return MOE_ERR_UNSUPPORTED;
   const void* outs[5] = {topk_idx, topk_w, expert_cnt, expert_off, pair_list};
   for (const void* p : outs)
     if (p && !aligned4(p)) return MOE_ERR_MISALIGNED;
   if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
   const int maxT = ws_max_tokens(layer, ws_bytes);
   const Layout lo = make_layout(layer, maxT);
+  if (T > MOE_DECODE_MAX_TOKENS) {
+    PrefillArgs pa = prefill_args(layer, lo, ws, x, T, nullptr);
+    pa.out.topk_idx = topk_idx; pa.out.topk_w = topk_w; pa.out.cnt = expert_cnt; pa.out.off = expert_off;
+    pa.out.pair = pair_list;
+    pa.h_amax = nullptr;  // no expert pass follows
+    return cuda_status(launch_prefill_route(pa, reinterpret_cast<cudaStream_t>(stream)));
+  }
   RouterArgs ra = router_args(layer, lo, ws, x, T);
   ra.out.topk_idx = topk_idx; ra.out.topk_w = topk_w; ra.out.cnt = expert_cnt; ra.out.off = expert_off;
   ra.out.pair = pair_list;
@@ -379,8 +441,15 @@ int32_t moe_prefill_forward(const moe_layer* layer, const void* x, int32_t T, vo
   if (!aligned16(x) || !aligned16(y)) return MOE_ERR_MISALIGNED;
   if (T < 1) return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
-  (void)stream;
-  return MOE_ERR_UNSUPPORTED;
+  if ((opts && opts->act_quant) || !prefill_supported(layer)) return MOE_ERR_UNSUPPORTED;
+  int sms = 0;
+  if ((st = sm_count(&sms)) != MOE_OK) return st;
+  const Layout lo = make_layout(layer, ws_max_tokens(layer, ws_bytes));
+  const PrefillArgs pa = prefill_args(layer, lo, ws, x, T, y);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err = launch_prefill_route(pa, s);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_prefill_experts(pa, sms, s));
 }
 
 int32_t moe_check(void* ws, size_t ws_bytes, moe_stream_t stream) {

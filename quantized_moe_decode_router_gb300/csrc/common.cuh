@@ -25,7 +25,8 @@ struct Ctrl {
   uint32_t error_info;     // where it happened (kernel-specific)
   uint32_t router_arrive;  // CTAs of the router kernel that finished their logits
   int32_t n_active;        // experts with at least one routed pair
-  uint32_t pad[4];
+  int32_t n_tiles;         // prefill: token tiles in the GEMM tile list
+  uint32_t pad[3];
 };
 
 __device__ __forceinline__ void report_error(Ctrl* ctrl, uint32_t code, uint32_t info) {

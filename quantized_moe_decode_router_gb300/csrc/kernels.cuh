@@ -91,6 +91,48 @@ cudaError_t launch_expert_int4(int sfmt, bool down, const ExpertArgs& a, size_t 
 cudaError_t launch_expert_int8(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
 cudaError_t launch_expert_fp8(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
 
+// ---------------------------------------------------------------- prefill --
+// Any token count.  Routing: FP32 approximate logits with a rigorous error
+// bound, exact (correctly rounded) logits for the experts that can still
+// reach the top-k, then a chunked counting-sort dispatch.  Experts: grouped
+// GEMMs on tcgen05 over token tiles of one expert each.
+constexpr int kPfTokTile = 128;    // tokens per GEMM tile (MMA N)
+constexpr int kPfRowTile = 128;    // weight rows per GEMM tile (MMA M)
+constexpr int kPfChunk = 64;       // tokens per dispatch chunk
+constexpr int kPfGemmThreads = 320;  // 8 decode/epilogue warps + B loader warp + MMA warp
+
+struct PrefillArgs {
+  int H, I, E, k, T;
+  int fmt;
+  const uint16_t* x;    // bf16 [T, H]
+  const float* rw;      // router [E, H]
+  const float* bias;    // [E] or nullptr
+  QW gate, up, down;
+  RouteBufs rb;         // logits [T, E] (approximate, then exact for candidates), top-k, cnt, off, pair
+  RouteOut out;
+  uint16_t* xs;         // f16 [T, H]: x * 2^xsig[t]
+  int32_t* xsig;        // [T]
+  float* xnorm;         // [T] ||x_t||_2
+  float* wnorm;         // [E] ||Wr_e||_2
+  int32_t* hist;        // [nchunk, E]: per-chunk counts, then per-chunk bases
+  int32_t* pos_of;      // [T*k] sorted position of pair p
+  int2* tiles;          // [max tiles] (expert, first sorted position)
+  int max_tiles;
+  uint16_t* h;          // bf16 [T*k, I] in sorted order
+  uint32_t* h_amax;     // [T*k] max |h| (float bits) per sorted position
+  uint16_t* h16;        // f16 [T*k, I]: h * 2^hsig[pos]
+  int32_t* hsig;        // [T*k]
+  float* P;             // f32 [T*k, H] indexed by pair id
+  uint16_t* y;          // bf16 [T, H]
+};
+
+cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s);
+// Expert GEMMs + combine (after launch_prefill_route).
+cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s);
+cudaError_t launch_prefill_topk(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_gemm_nvfp4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
+size_t prefill_gemm_smem(bool down);
+
 // moe_dequantize / moe_quantize_act_nvfp4
 cudaError_t launch_dequantize(int fmt, QW w, int N, int K, int expert, int row0, int nrows, float* out,
                               cudaStream_t s);

@@ -267,6 +267,111 @@ __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArg
   if (tid == 0) a.rb.ctrl->router_arrive = 0;  // leave the counter at zero for the next call
 }
 
+// ---------------------------------------------------------------- prefill --
+// One warp per token.  The approximate logit a of expert e carries the bound
+// eps = gamma_H ||x_t|| ||Wr_e|| (sequential FMA sum of exact products,
+// Cauchy-Schwarz for sum |x w|), widened for the FP32 bias additions.  L is
+// the k-th largest lower bound a - eps; an expert whose upper bound a + eps
+// is below L has an exact logit below the k-th largest exact logit, so only
+// the others (at least k) get exact float-float logits.  The row of the
+// logits buffer then holds the exact logit of every candidate and -inf
+// elsewhere, and the decode path's top-k runs on it.
+template <int NQ>
+__device__ void prefill_topk_token(const PrefillArgs& a, int t) {
+  const int lane = threadIdx.x & 31;
+  const int E = a.E, H = a.H, k = a.k;
+  float* row = a.rb.logits + (size_t)t * E;
+  const float u = 5.9604645e-8f;  // 2^-24
+  const float gam = (float)H * u / (1.f - (float)H * u);
+  const float xn = a.xnorm[t];
+  float av[NQ], ev[NQ];
+  unsigned long long lo_key[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    const int e = q * 32 + lane;
+    av[q] = 0.f;
+    ev[q] = 0.f;
+    lo_key[q] = 0ull;
+    if (e < E) {
+      const float d = row[e];
+      const float b = a.bias ? __ldg(a.bias + e) : 0.f;
+      const float ab = __fadd_rn(d, b);
+      const float eps0 = gam * xn * a.wnorm[e] * 1.00390625f;
+      const float eps = eps0 + 4.7683716e-7f * (fabsf(d) + fabsf(b) + eps0) + 1e-30f;
+      av[q] = ab;
+      ev[q] = eps;
+      lo_key[q] = sel_key(ab - eps, e);
+    }
+  }
+  // k-th largest lower bound
+  unsigned long long mine = lane_max<NQ>(lo_key), kth = 0ull;
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = mine;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+    if (best == mine) {
+      const int bi = key_id(best);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q)
+        if (q == (bi >> 5)) lo_key[q] = 0ull;
+      mine = lane_max<NQ>(lo_key);
+    }
+    kth = best;
+  }
+  const float L = key_value(kth);
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    const int e_mine = q * 32 + lane;
+    const bool cand = e_mine < E && !(av[q] + ev[q] < L);
+    uint32_t bal = __ballot_sync(0xFFFFFFFFu, cand);
+    if (e_mine < E && !cand) row[e_mine] = __int_as_float(0xFF800000);  // -inf
+    while (bal) {
+      const int src = __ffs(bal) - 1;
+      bal &= bal - 1;
+      const int e = q * 32 + src;
+      // exact logit of expert e: float-float over H, lanes on consecutive float4 columns
+      const float4* wrow = reinterpret_cast<const float4*>(a.rw + (size_t)e * H);
+      const uint2* xp = reinterpret_cast<const uint2*>(a.x + (size_t)t * H);
+      float hi = 0.f, lo = 0.f;
+      for (int c = lane; c < H / 4; c += 32) {
+        const float4 wv = __ldg(wrow + c);
+        const uint2 xv = __ldg(xp + c);
+        dot2_step(bf16_bits_to_float(xv.x & 0xFFFF), wv.x, hi, lo);
+        dot2_step(bf16_bits_to_float(xv.x >> 16), wv.y, hi, lo);
+        dot2_step(bf16_bits_to_float(xv.y & 0xFFFF), wv.z, hi, lo);
+        dot2_step(bf16_bits_to_float(xv.y >> 16), wv.w, hi, lo);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float h2 = __shfl_xor_sync(0xFFFFFFFFu, hi, o);
+        const float l2 = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+        dot2_merge(hi, lo, h2, l2);
+      }
+      float lg = __fadd_rn(hi, lo);
+      if (a.bias) lg = __fadd_rn(lg, __ldg(a.bias + e));
+      const float aq = __shfl_sync(0xFFFFFFFFu, av[q], src), eq = __shfl_sync(0xFFFFFFFFu, ev[q], src);
+      if (lane == 0) {
+        row[e] = lg;
+        if (fabsf(lg - aq) > eq && lg == lg) report_error(a.rb.ctrl, MOE_ERR_DEVICE_BAD_INDEX, 0x200);
+      }
+    }
+  }
+  __syncwarp();
+  int32_t* io = a.rb.topk_idx + (size_t)t * k;
+  float* wo = a.rb.topk_w + (size_t)t * k;
+  int32_t* io2 = a.out.topk_idx ? a.out.topk_idx + (size_t)t * k : nullptr;
+  float* wo2 = a.out.topk_w ? a.out.topk_w + (size_t)t * k : nullptr;
+  topk_warp<NQ>(row, E, k, io, wo, io2, wo2);
+}
+
+__global__ void __launch_bounds__(kRouterThreads) prefill_topk_kernel(PrefillArgs a) {
+  const int t = blockIdx.x * kWarpsR + (threadIdx.x >> 5);
+  if (t >= a.T) return;
+  if (a.E <= 256) prefill_topk_token<8>(a, t);
+  else if (a.E <= 512) prefill_topk_token<16>(a, t);
+  else prefill_topk_token<32>(a, t);
+}
+
 }  // namespace
 
 // Warps sharing one expert row: split H while each warp keeps >= 512 columns.
@@ -284,6 +389,11 @@ cudaError_t launch_router_decode(const RouterArgs& a, cudaStream_t s) {
                                          (int)smem);
   if (err != cudaSuccess) return err;
   router_decode_kernel<<<grid, kRouterThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_topk(const PrefillArgs& a, cudaStream_t s) {
+  prefill_topk_kernel<<<(a.T + kWarpsR - 1) / kWarpsR, kRouterThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
