@@ -53,6 +53,17 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _bf16_peak():
+    """Dense bf16 tensor peak (TFLOP/s): the measured burst figure, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -321,6 +332,88 @@ def run_ours(args, world, rank, local):
     return out
 
 
+def run_prefill(args, local, peak_bf16, peak_kind):
+    """The prefill workload (NVFP4 layer, 4096 tokens, Zipf-skewed router): whole-layer time through
+    moe_prefill_forward, per-kernel event times, and the grouped GEMMs' tensor throughput."""
+    import torch
+    import quantized_moe_decode_router_gb300 as q
+    cfg = synth.CONFIGS["prefill_nvfp4"]
+    T = cfg.batches[0]
+    host = synth.make_layer(cfg, seed=0)
+    lay = q.to_device(host, f"cuda:{local}")
+    NB = 3
+    xs = [torch.from_numpy(synth.make_tokens(cfg, T, seed=4000, batch=i).view(np.int16)).cuda() for i in range(NB)]
+    y = torch.zeros((T, cfg.H), dtype=torch.int16, device="cuda")
+    ws = torch.empty(q.workspace_size(lay, T), dtype=torch.uint8, device="cuda")
+    q.workspace_init(ws)
+    cnt = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
+    touched = []
+    for i in range(NB):
+        q.moe_route(lay, xs[i], T, expert_cnt=cnt, ws=ws)
+        touched.append(int(np.count_nonzero(cnt.cpu().numpy())))
+    stream = torch.cuda.Stream()
+    G = 6
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            q.moe_prefill_forward(lay, xs[i % NB], T, y, ws, stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(G):
+                q.moe_prefill_forward(lay, xs[i % NB], T, y, ws, stream=stream)
+        for _ in range(2):
+            g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, args.prefill_steps // G)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * G)
+    # per-kernel times: event-record nodes between the launches
+    n = 6
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    gt = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gt, stream=stream):
+        for i in range(n):
+            q.moe_prefill_forward_timed(lay, xs[i % NB], T, y, ws, evs[i], stream=stream)
+    with torch.cuda.stream(stream):
+        gt.replay()
+    torch.cuda.synchronize()
+    dur = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(7)] for i in range(n)]).mean(axis=0) * 1e3
+    names = ["router_logits", "router_topk", "dispatch", "gateup_gemm", "h_convert", "down_gemm", "combine"]
+    st = q.moe_check(ws)
+    if st != 0:
+        raise RuntimeError(f"device-side error: {q.status_string(st)}")
+    pairs = T * cfg.k
+    flops = pairs * 6.0 * cfg.H * cfg.I
+    gemm_us = dur[3] + dur[5]
+    tflops = flops / (gemm_us * 1e-6) / 1e12
+    fp4_peak = peak_bf16 * 13.5 / 2.25
+    wbytes = host.router_bytes() + np.mean(touched) * host.expert_bytes()
+    return {
+        "workload": f"prefill_nvfp4: NVFP4 MoE layer H={cfg.H} E={cfg.E} top-{cfg.k} I={cfg.I}, {T} tokens, "
+                    f"Zipf router bias s={cfg.zipf_s}",
+        "us_per_layer": round(us, 1), "tokens_per_s": round(T / (us * 1e-6), 1),
+        "kernel_us": {k: round(float(v), 2) for k, v in zip(names, dur)},
+        "experts_touched": float(np.mean(touched)),
+        "gemm": {"path": "exact chain: tcgen05 kind::f16, NVFP4 decoded in shared memory",
+                 "flops_per_layer": flops, "achieved_tflops": round(tflops, 1),
+                 "frac_f16_peak": round(tflops / peak_bf16, 4), "f16_peak_tflops": peak_bf16,
+                 "frac_fp4_peak": round(tflops / fp4_peak, 4), "fp4_peak_tflops": round(fp4_peak, 1),
+                 "peak_kind": peak_kind},
+        "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
+        "graph": f"CUDA graph of {G} layer calls, {reps} replays",
+    }
+
+
 def run_cpu_baseline(args, seconds_budget: float = 20.0):
     """The oracle, as it stands, on a bounded sample of the workload (rank 0 only)."""
     from oracle import moe as M
@@ -358,6 +451,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-batches", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill workload's measurement")
+    ap.add_argument("--prefill-steps", type=int, default=60)
     args = ap.parse_args()
     world, rank, local = _dist()
     if args.impl == "reference":
@@ -373,6 +468,9 @@ def main():
         print(json.dumps(out))
         return
     out = run_ours(args, world, rank, local)
+    if world == 1 and not args.no_prefill:
+        pk, pkk = _bf16_peak()
+        out["prefill"] = run_prefill(args, local, pk, pkk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = run_cpu_baseline(args)
     elif rank == 0:

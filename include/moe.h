@@ -169,12 +169,31 @@ int32_t moe_decode_forward(const moe_layer* layer, const void* x /* device bf16 
 /*
  * Whole layer for any T >= 1 (prefill), same result definition as
  * moe_decode_forward; expert projections run as grouped GEMMs over a compact
- * tile list of the routed segments.  opts->act_quant = 1 selects the NVFP4
- * W4A4 lever (NVFP4 routed experts only).
+ * tile list of the routed segments (DGPP README "Execution and performance":
+ * engine.expert_tile_list, engine.expert_gemm_pair), with FP32 partials and
+ * a combine pass.  Supported so far: NVFP4 routed experts without a shared
+ * expert, hidden and inter multiples of 128; anything else returns
+ * MOE_ERR_UNSUPPORTED before any launch.  opts->act_quant must be 0 (the
+ * NVFP4 W4A4 lever is not available yet: MOE_ERR_UNSUPPORTED).  Routing
+ * outputs are left in the workspace; in its logits array only the experts the
+ * router recomputed exactly (every selected one among them) hold their FP32
+ * logit, the others hold -inf.
  */
 int32_t moe_prefill_forward(const moe_layer* layer, const void* x /* device bf16 [T, H] */, int32_t T,
                             void* y /* device bf16 [T, H] */, const moe_options* opts, void* ws, size_t ws_bytes,
                             moe_stream_t stream);
+
+/*
+ * moe_prefill_forward that also records up to eight CUDA events on `stream`
+ * (events[i] a cudaEvent_t or NULL): [0] before the first kernel, [1] after
+ * the approximate router logits, [2] after top-k, [3] after the dispatch
+ * index, [4] after the gate/up GEMM, [5] after the h conversion, [6] after
+ * the down GEMM, [7] after the combine.  Inside a stream capture the records
+ * become event-record nodes.  For per-kernel timing only.
+ */
+int32_t moe_prefill_forward_timed(const moe_layer* layer, const void* x, int32_t T, void* y,
+                                  const moe_options* opts, void* ws, size_t ws_bytes, moe_stream_t stream,
+                                  void* const* events);
 
 /*
  * moe_decode_forward that also records four CUDA events on `stream`: before

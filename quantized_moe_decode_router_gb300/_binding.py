@@ -68,6 +68,9 @@ _SIGNATURES = {
     "moe_decode_forward_timed": (ctypes.c_int32, [_P(moe_layer), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                                   _P(moe_options), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                                   ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_prefill_forward_timed": (ctypes.c_int32, [_P(moe_layer), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                                   _P(moe_options), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                                   ctypes.POINTER(ctypes.c_void_p)]),
     "moe_decode_forward_noalloc": (ctypes.c_int32, [_P(moe_layer), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                                     _P(moe_options), ctypes.c_void_p]),
     "moe_check": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -224,6 +227,15 @@ def moe_prefill_forward(layer: Layer, x, T: int, y, ws, stream=None, act_quant: 
     st = load().moe_prefill_forward(ctypes.byref(lc), _ptr(x), T, _ptr(y), ctypes.byref(o), _ptr(ws),
                                     0 if ws is None else ws.numel() * ws.element_size(), _stream_handle(stream))
     return _check(st, "moe_prefill_forward") if raise_on_error else st
+
+
+def moe_prefill_forward_timed(layer: Layer, x, T: int, y, ws, events, stream=None) -> int:
+    """moe_prefill_forward recording torch.cuda.Event objects (8, or None entries) between its kernels."""
+    lc, o = layer.c(), _opts(0)
+    arr = (ctypes.c_void_p * 8)(*[None if e is None else int(e.cuda_event) for e in events])
+    st = load().moe_prefill_forward_timed(ctypes.byref(lc), _ptr(x), T, _ptr(y), ctypes.byref(o), _ptr(ws),
+                                          ws.numel() * ws.element_size(), _stream_handle(stream), arr)
+    return _check(st, "moe_prefill_forward_timed")
 
 
 def moe_check(ws, stream=None) -> int:

@@ -432,8 +432,23 @@ int32_t moe_decode_forward_timed(const moe_layer* layer, const void* x, int32_t 
   return decode_forward_checked(layer, x, T, y, opts, ws, ws_bytes, stream, events);
 }
 
-int32_t moe_prefill_forward(const moe_layer* layer, const void* x, int32_t T, void* y, const moe_options* opts,
-                            void* ws, size_t ws_bytes, moe_stream_t stream) {
+struct MarkCtx {
+  void* const* events;
+  cudaStream_t stream;
+  bool capturing;
+};
+
+static void record_mark(void* ctx, int i) {
+  const MarkCtx* m = static_cast<const MarkCtx*>(ctx);
+  if (!m->events || !m->events[i]) return;
+  cudaEvent_t ev = static_cast<cudaEvent_t>(m->events[i]);
+  if (m->capturing) cudaEventRecordWithFlags(ev, m->stream, cudaEventRecordExternal);
+  else cudaEventRecord(ev, m->stream);
+}
+
+static int32_t prefill_forward_checked(const moe_layer* layer, const void* x, int32_t T, void* y,
+                                       const moe_options* opts, void* ws, size_t ws_bytes, moe_stream_t stream,
+                                       void* const* events) {
   int32_t st = check_layer(layer);
   if (st != MOE_OK) return st;
   if ((st = check_options(opts)) != MOE_OK) return st;
@@ -447,9 +462,28 @@ int32_t moe_prefill_forward(const moe_layer* layer, const void* x, int32_t T, vo
   const Layout lo = make_layout(layer, ws_max_tokens(layer, ws_bytes));
   const PrefillArgs pa = prefill_args(layer, lo, ws, x, T, y);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t err = launch_prefill_route(pa, s);
+  MarkCtx mc{events, s, false};
+  if (events) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cap);
+    mc.capturing = cap == cudaStreamCaptureStatusActive;
+  }
+  const Marks mk{events ? record_mark : nullptr, &mc};
+  mk(0);
+  cudaError_t err = launch_prefill_route(pa, s, mk);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_prefill_experts(pa, sms, s));
+  return cuda_status(launch_prefill_experts(pa, sms, s, mk));
+}
+
+int32_t moe_prefill_forward(const moe_layer* layer, const void* x, int32_t T, void* y, const moe_options* opts,
+                            void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return prefill_forward_checked(layer, x, T, y, opts, ws, ws_bytes, stream, nullptr);
+}
+
+int32_t moe_prefill_forward_timed(const moe_layer* layer, const void* x, int32_t T, void* y,
+                                  const moe_options* opts, void* ws, size_t ws_bytes, moe_stream_t stream,
+                                  void* const* events) {
+  return prefill_forward_checked(layer, x, T, y, opts, ws, ws_bytes, stream, events);
 }
 
 int32_t moe_check(void* ws, size_t ws_bytes, moe_stream_t stream) {

@@ -99,7 +99,7 @@ cudaError_t launch_expert_fp8(int sfmt, bool down, const ExpertArgs& a, size_t s
 constexpr int kPfTokTile = 128;    // tokens per GEMM tile (MMA N)
 constexpr int kPfRowTile = 128;    // weight rows per GEMM tile (MMA M)
 constexpr int kPfChunk = 64;       // tokens per dispatch chunk
-constexpr int kPfGemmThreads = 320;  // 8 decode/epilogue warps + B loader warp + MMA warp
+constexpr int kPfGemmThreads = 448;  // 8 decode warps, B loader, MMA, 4 epilogue warps
 
 struct PrefillArgs {
   int H, I, E, k, T;
@@ -126,9 +126,20 @@ struct PrefillArgs {
   uint16_t* y;          // bf16 [T, H]
 };
 
-cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s);
-// Expert GEMMs + combine (after launch_prefill_route).
-cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s);
+// Optional host callback between launches (event records of the timed entry
+// point): mark(ctx, i) after stage i.
+struct Marks {
+  void (*fn)(void*, int);
+  void* ctx;
+  void operator()(int i) const {
+    if (fn) fn(ctx, i);
+  }
+};
+// Router + dispatch; marks 1 (logits), 2 (top-k), 3 (dispatch).
+cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s, Marks mk = Marks{nullptr, nullptr});
+// Expert GEMMs + combine (after launch_prefill_route); marks 4 (gate/up),
+// 5 (h conversion), 6 (down), 7 (combine).
+cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s, Marks mk = Marks{nullptr, nullptr});
 cudaError_t launch_prefill_topk(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_gemm_nvfp4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
 size_t prefill_gemm_smem(bool down);

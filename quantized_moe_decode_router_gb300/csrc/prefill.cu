@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) pf_hist_kernel(PrefillArgs a) {
   for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
     const int e = a.rb.topk_idx[p];
     if ((unsigned)e < (unsigned)E) atomicAdd(&s_h[e], 1);
-    else report_error(a.rb.ctrl, MOE_ERR_DEVICE_BAD_INDEX, 0x100);
+    else report_error(a.rb.ctrl, (uint32_t)MOE_ERR_DEVICE_BAD_INDEX, 0x100);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) a.hist[(size_t)c * E + e] = s_h[e];
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kScanThreads) pf_scan_kernel(PrefillArgs a) {
       a.rb.off[E] = off + cnt;
       if (a.out.off) a.out.off[E] = off + cnt;
       const int nt = toff + ntile;
-      if (nt > a.max_tiles) report_error(a.rb.ctrl, MOE_ERR_DEVICE_BAD_INDEX, 0x101);
+      if (nt > a.max_tiles) report_error(a.rb.ctrl, (uint32_t)MOE_ERR_DEVICE_BAD_INDEX, 0x101);
       a.rb.ctrl->n_tiles = nt > a.max_tiles ? a.max_tiles : nt;
     }
   }
@@ -308,28 +308,35 @@ __global__ void __launch_bounds__(kThreads) pf_combine_kernel(PrefillArgs a) {
 
 }  // namespace
 
-cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s) {
+cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s, Marks mk) {
   const int wpb = kThreads / 32;
   pf_prep_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(a);
   pf_wnorm_kernel<<<(a.E + wpb - 1) / wpb, kThreads, 0, s>>>(a);
   pf_logits_kernel<<<dim3((a.E + kLE - 1) / kLE, (a.T + kLT - 1) / kLT), kThreads, 0, s>>>(a);
+  mk(1);
   cudaError_t err = launch_prefill_topk(a, s);
   if (err != cudaSuccess) return err;
+  mk(2);
   const int nchunk = (a.T + kPfChunk - 1) / kPfChunk;
   pf_hist_kernel<<<nchunk, kThreads, a.E * 4, s>>>(a);
   pf_scan_kernel<<<1, kScanThreads, 0, s>>>(a);
   pf_place_kernel<<<nchunk, 32, a.E * 4, s>>>(a);
+  mk(3);
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s) {
+cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s, Marks mk) {
   cudaError_t err = launch_prefill_gemm_nvfp4(false, a, sms, s);
   if (err != cudaSuccess) return err;
+  mk(4);
   const int wpb = kThreads / 32;
   pf_hconv_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  mk(5);
   if ((err = launch_prefill_gemm_nvfp4(true, a, sms, s)) != cudaSuccess) return err;
+  mk(6);
   pf_combine_kernel<<<a.T, kThreads, 0, s>>>(a);
+  mk(7);
   return cudaGetLastError();
 }
 

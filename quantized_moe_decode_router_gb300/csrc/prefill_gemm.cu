@@ -19,14 +19,20 @@
 // CTA roles (persistent grid, one CTA per SM):
 //   warps 0-7  decode the weight rows of each K step (cp.async ring of raw
 //              codes per thread, e2m1/e4m3 conversion to f16) into the
-//              stage's A tiles, then run the epilogue from TMEM;
-//   warp 8     copies the stage's token rows (B tile) with cp.async and
-//              signals their arrival through the stage's mbarrier;
+//              stage's A tiles;
+//   warp 8     loads the stage's token rows (B tile) with TMA into a
+//              128-byte-swizzled tile: four-row gathers of the scaled
+//              activations by token (gate/up), one 2-D box of the
+//              contiguous h rows (down); the stage's mbarrier counts bytes;
 //   warp 9     allocates TMEM and issues the MMAs from one thread;
-//              tcgen05.commit releases each stage and publishes each tile.
+//              tcgen05.commit releases each stage and publishes each tile;
+//   warps 10-13 the epilogue, from TMEM accumulators that are double
+//              buffered so the next tile's MMAs overlap it.
 // Every wait on an mbarrier is bounded; a wait that gives up records
 // MOE_ERR_DEVICE_TIMEOUT and the CTA winds down (draining its MMAs before
 // TMEM is released).
+#include <cuda.h>
+
 #include "kernels.cuh"
 #include "tc.cuh"
 
@@ -54,27 +60,26 @@ struct Cfg {
   static constexpr int STAGE_BYTES = NMAT * A_BYTES + B_BYTES;
   static constexpr int RAW_OFF = STAGES * STAGE_BYTES;
   static constexpr int SMEM = RAW_OFF + kRaw * kDec * kRawBytes + 1024;
-  static constexpr uint32_t TMEM_COLS = 256;
+  static constexpr uint32_t ACC_COLS = NMAT * NT;      // one accumulator set
+  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // double buffered
 };
 
-__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src),
-               "r"(valid ? 16 : 0));
-}
-
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
-}
+// Warp roles.
+constexpr int kWarpLoader = 8;
+constexpr int kWarpMma = 9;
+constexpr int kWarpEpi0 = 10;  // warps 10..13: epilogue, warp w reads TMEM lanes 32 * (w % 4)
+constexpr int kEpiThreads = 128;
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 template <bool DOWN>
-__global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs a) {
+__global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs a,
+                                                                    const __grid_constant__ CUtensorMap tmB) {
   using C = Cfg<DOWN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full_a[C::STAGES], full_b[C::STAGES], empty[C::STAGES];
-  __shared__ __align__(8) uint64_t acc_full, acc_empty, drain;
+  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], drain;
   __shared__ uint32_t tmem_slot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -89,22 +94,24 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
   if (tid == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
       tc::bar_init(&full_a[i], kDec);
-      tc::bar_init(&full_b[i], 32);
+      tc::bar_init(&full_b[i], 1);
       tc::bar_init(&empty[i], 1);
     }
-    tc::bar_init(&acc_full, 1);
-    tc::bar_init(&acc_empty, kDec);
+    for (int b = 0; b < 2; ++b) {
+      tc::bar_init(&acc_full[b], 1);
+      tc::bar_init(&acc_empty[b], kEpiThreads);
+    }
     tc::bar_init(&drain, 1);
     tc::bar_init_fence();
   }
-  if (warp == 9) tc::tmem_alloc(&tmem_slot, C::TMEM_COLS);
+  if (warp == kWarpMma) tc::tmem_alloc(&tmem_slot, C::TMEM_COLS);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
 
   if (warp < 8) {
-    // ------------------------------------------------ decode + epilogue --
+    // ----------------------------------------------------------- decode --
     const int d = tid;
     const int m = d / (BM * C::TPR);
     const int rr = (d % (BM * C::TPR)) / C::TPR;
@@ -113,10 +120,9 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
     uint8_t* raw = smem + C::RAW_OFF + d * kRawBytes;
     uint32_t g = 0;
     bool ok = true;
-    int item = 0;
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++item) {
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
       const int2 tile = a.tiles[it / RT];
-      const int rt = it % RT, e = tile.x, pos0 = tile.y;
+      const int rt = it % RT, e = tile.x;
       const int row = rt * BM + rr;
       const uint8_t* crow = W.data + (size_t)e * data_bytes(MOE_FMT_NVFP4, N, K) + (size_t)row * (K / 2);
       const uint8_t* srow = W.scales + (size_t)e * scale_bytes(MOE_FMT_NVFP4, N, K) + (size_t)row * (K / 16);
@@ -150,7 +156,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         }
         const int stage = g % C::STAGES;
         if (!tc::bar_wait(&empty[stage], ((g / C::STAGES) & 1) ^ 1, kWaitLimit)) {
-          report_error(ctrl, MOE_ERR_DEVICE_TIMEOUT, 0x300 | (DOWN ? 1 : 0));
+          report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x300 | (DOWN ? 1 : 0));
           ok = false;
           break;
         }
@@ -161,61 +167,9 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         tc::fence_proxy_async();
         tc::bar_arrive(&full_a[stage]);
       }
-      cp_async_wait<0>();
-      if (!ok) break;
-
-      // ---- epilogue: warp (q, half) reads TMEM lanes 32q.. and half of the columns
-      if (!tc::bar_wait(&acc_full, item & 1, kWaitLimit)) {
-        report_error(ctrl, MOE_ERR_DEVICE_TIMEOUT, 0x310 | (DOWN ? 1 : 0));
-        ok = false;
-        break;
-      }
-      tc::fence_after_sync();
-      const int q = warp & 3, half = warp >> 2;
-      const int n_valid = min(NT, a.rb.off[e + 1] - pos0);
-      const int orow = rt * BM + q * 32 + lane;
-      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-#pragma unroll 1
-      for (int cb = 0; cb < NT / 2; cb += 16) {
-        const int c0 = half * (NT / 2) + cb;
-        if (c0 >= n_valid) break;
-        if (!DOWN) {
-          uint32_t gv[16], uv[16];
-          tc::tmem_ld16(tq + c0, gv);
-          tc::tmem_ld16(tq + NT + c0, uv);
-          tc::tmem_ld_wait();
-          const float tsg = __ldg(a.gate.ts + e), tsu = __ldg(a.up.ts + e);
-#pragma unroll 4
-          for (int j = 0; j < 16; ++j) {
-            if (c0 + j >= n_valid) break;
-            const int pos = pos0 + c0 + j;
-            const int tok = a.rb.pair[pos] / k;
-            const float un = exp2i(-a.xsig[tok]);
-            const float gg = __uint_as_float(gv[j]) * (tsg * un);
-            const float uu = __uint_as_float(uv[j]) * (tsu * un);
-            const uint16_t hb = float_to_bf16_bits(silu(gg) * uu);
-            a.h[(size_t)pos * I + orow] = hb;
-            const uint32_t mag = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(hb & 0x7FFF) << 16);
-            if (lane == 0 && mag) atomicMax(&a.h_amax[pos], mag);
-          }
-        } else {
-          uint32_t dv[16];
-          tc::tmem_ld16(tq + c0, dv);
-          tc::tmem_ld_wait();
-          const float tsd = __ldg(a.down.ts + e);
-#pragma unroll 4
-          for (int j = 0; j < 16; ++j) {
-            if (c0 + j >= n_valid) break;
-            const int pos = pos0 + c0 + j;
-            const float un = exp2i(-a.hsig[pos]);
-            a.P[(size_t)a.rb.pair[pos] * H + orow] = __uint_as_float(dv[j]) * (tsd * un);
-          }
-        }
-      }
-      tc::fence_before_sync();
-      tc::bar_arrive(&acc_empty);
     }
-  } else if (warp == 8) {
+    cp_async_wait<0>();
+  } else if (warp == kWarpLoader) {
     // --------------------------------------------------------- B loader --
     uint32_t g = 0;
     bool ok = true;
@@ -223,36 +177,32 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
       const int2 tile = a.tiles[it / RT];
       const int e = tile.x, pos0 = tile.y;
       const int n_valid = min(NT, a.rb.off[e + 1] - pos0);
-      const uint16_t* src[NT / 32];
-      bool val[NT / 32];
+      // gate/up: this lane gathers tile rows 4*lane .. 4*lane+3 (rows past the
+      // tile's tokens repeat its last token: they only feed discarded columns)
+      int trow[4] = {0, 0, 0, 0};
+      if (!DOWN) {
 #pragma unroll
-      for (int i = 0; i < NT / 32; ++i) {
-        const int r = lane + 32 * i;
-        val[i] = r < n_valid;
-        const int pos = pos0 + (val[i] ? r : 0);
-        src[i] = DOWN ? a.h16 + (size_t)pos * I : a.xs + (size_t)(a.rb.pair[pos] / k) * H;
+        for (int i = 0; i < 4; ++i) trow[i] = a.rb.pair[pos0 + min(4 * lane + i, n_valid - 1)] / k;
       }
 #pragma unroll 1
       for (int s = 0; s < nsteps; ++s, ++g) {
         const int stage = g % C::STAGES;
         if (!tc::bar_wait(&empty[stage], ((g / C::STAGES) & 1) ^ 1, kWaitLimit)) {
-          report_error(ctrl, MOE_ERR_DEVICE_TIMEOUT, 0x320 | (DOWN ? 1 : 0));
+          report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x320 | (DOWN ? 1 : 0));
           ok = false;
           break;
         }
         uint8_t* B = smem + stage * C::STAGE_BYTES + C::NMAT * C::A_BYTES;
-#pragma unroll
-        for (int i = 0; i < NT / 32; ++i) {
-          if (!val[i]) continue;  // rows past the tile's tokens only feed discarded columns
-          const int r = lane + 32 * i;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) cp_async16_zfill(B + tc::chunk_off(r, c, KB), src[i] + s * BK + c * 8, true);
+        if (lane == 0) tc::bar_arrive_expect_tx(&full_b[stage], C::B_BYTES);
+        __syncwarp();
+        if (DOWN) {
+          if (lane == 0) tc::tma_load_2d(B, &tmB, s * BK, pos0, &full_b[stage]);
+        } else {
+          tc::tma_gather4(B + lane * 4 * KB, &tmB, s * BK, trow[0], trow[1], trow[2], trow[3], &full_b[stage]);
         }
-        cp_async_arrive_noinc(&full_b[stage]);
       }
     }
-    cp_async_wait<0>();
-  } else {
+  } else if (warp == kWarpMma) {
     // -------------------------------------------------------------- MMA --
     if (lane == 0) {
       uint32_t g = 0;
@@ -263,17 +213,19 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         const int n_valid = min(NT, a.rb.off[tile.x + 1] - tile.y);
         const int n_mma = (n_valid + 15) & ~15;
         const uint32_t idesc = tc::idesc_f16(BM, n_mma, 0);
-        if (!tc::bar_wait(&acc_empty, (item & 1) ^ 1, kWaitLimit)) {
-          report_error(ctrl, MOE_ERR_DEVICE_TIMEOUT, 0x330 | (DOWN ? 1 : 0));
+        const int buf = item & 1;
+        if (!tc::bar_wait(&acc_empty[buf], ((item >> 1) & 1) ^ 1, kWaitLimit)) {
+          report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x330 | (DOWN ? 1 : 0));
           break;
         }
         tc::fence_after_sync();
+        const uint32_t acc = tmem + buf * C::ACC_COLS;
 #pragma unroll 1
         for (int s = 0; s < nsteps; ++s, ++g) {
           const int stage = g % C::STAGES;
           const uint32_t par = (g / C::STAGES) & 1;
           if (!tc::bar_wait(&full_a[stage], par, kWaitLimit) || !tc::bar_wait(&full_b[stage], par, kWaitLimit)) {
-            report_error(ctrl, MOE_ERR_DEVICE_TIMEOUT, 0x340 | (DOWN ? 1 : 0));
+            report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x340 | (DOWN ? 1 : 0));
             ok = false;
             break;
           }
@@ -283,30 +235,130 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
           const uint32_t bB = base + C::NMAT * C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t db = tc::smem_desc(bB + kk * 256, 128, 1024);
+            const uint64_t db = tc::smem_desc_sw128(bB + kk * 32);
 #pragma unroll
             for (int mm = 0; mm < C::NMAT; ++mm) {
               const uint64_t da = tc::smem_desc(base + mm * C::A_BYTES + kk * 256, 128, 1024);
-              tc::mma_f16(tmem + mm * NT, da, db, idesc, (s | kk) != 0);
+              tc::mma_f16(acc + mm * NT, da, db, idesc, (s | kk) != 0);
             }
           }
           tc::commit(&empty[stage]);
         }
         if (!ok) break;
-        tc::commit(&acc_full);
+        tc::commit(&acc_full[buf]);
       }
       tc::commit(&drain);
       tc::bar_wait(&drain, 0, kWaitLimit);
     }
     __syncwarp();
+  } else {
+    // --------------------------------------------------------- epilogue --
+    // warp w handles TMEM lanes (= weight rows of the tile) 32 * (w % 4) ..
+    const int q = warp & 3;
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+    int item = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++item) {
+      const int2 tile = a.tiles[it / RT];
+      const int rt = it % RT, e = tile.x, pos0 = tile.y;
+      const int n_valid = min(NT, a.rb.off[e + 1] - pos0);
+      const int buf = item & 1;
+      if (!tc::bar_wait(&acc_full[buf], (item >> 1) & 1, kWaitLimit)) {
+        report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x310 | (DOWN ? 1 : 0));
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t acc = tq + buf * C::ACC_COLS;
+      const int orow = rt * BM + q * 32 + lane;
+#pragma unroll 1
+      for (int c0 = 0; c0 < n_valid; c0 += 32) {
+        // column data for columns c0 + lane, shared through shuffles
+        const int cv = min(c0 + lane, n_valid - 1);
+        const int pos_l = pos0 + cv;
+        const int pair_l = a.rb.pair[pos_l];
+        float un_l;
+        if (DOWN) un_l = exp2i(-a.hsig[pos_l]) * __ldg(a.down.ts + e);
+        else un_l = exp2i(-a.xsig[pair_l / k]);
+        const int ncol = min(32, n_valid - c0);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if (half * 16 >= ncol) break;
+          const int cb = c0 + half * 16;
+          if (!DOWN) {
+            uint32_t gv[16], uv[16];
+            tc::tmem_ld16(acc + cb, gv);
+            tc::tmem_ld16(acc + NT + cb, uv);
+            tc::tmem_ld_wait();
+            const float tsg = __ldg(a.gate.ts + e), tsu = __ldg(a.up.ts + e);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int jj = half * 16 + j;
+              const float un = __shfl_sync(0xFFFFFFFFu, un_l, jj);
+              if (jj >= ncol) break;
+              const float gg = __uint_as_float(gv[j]) * (tsg * un);
+              const float uu = __uint_as_float(uv[j]) * (tsu * un);
+              const uint16_t hb = float_to_bf16_bits(silu(gg) * uu);
+              const int pos = pos0 + c0 + jj;
+              a.h[(size_t)pos * I + orow] = hb;
+              const uint32_t mag = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(hb & 0x7FFF) << 16);
+              if (lane == 0 && mag) atomicMax(&a.h_amax[pos], mag);
+            }
+          } else {
+            uint32_t dv[16];
+            tc::tmem_ld16(acc + cb, dv);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int jj = half * 16 + j;
+              const float un = __shfl_sync(0xFFFFFFFFu, un_l, jj);
+              const int pr = __shfl_sync(0xFFFFFFFFu, pair_l, jj);
+              if (jj >= ncol) break;
+              a.P[(size_t)pr * H + orow] = __uint_as_float(dv[j]) * un;
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      tc::bar_arrive(&acc_empty[buf]);
+    }
   }
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// f16 matrix [rows, cols] (row-major), boxes of 64 columns x box_rows rows,
+// 128-byte swizzle, zero fill outside the matrix.
+bool f16_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -315,14 +367,17 @@ size_t prefill_gemm_smem(bool down) { return down ? Cfg<true>::SMEM : Cfg<false>
 
 cudaError_t launch_prefill_gemm_nvfp4(bool down, const PrefillArgs& a, int grid, cudaStream_t s) {
   cudaError_t err;
+  alignas(64) CUtensorMap tm;
   if (down) {
+    if (!f16_map(&tm, a.h16, (uint64_t)a.I, (uint64_t)a.T * a.k, NT)) return cudaErrorInvalidValue;
     err = cudaFuncSetAttribute(pf_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true>::SMEM);
     if (err != cudaSuccess) return err;
-    pf_gemm_kernel<true><<<grid, kPfGemmThreads, Cfg<true>::SMEM, s>>>(a);
+    pf_gemm_kernel<true><<<grid, kPfGemmThreads, Cfg<true>::SMEM, s>>>(a, tm);
   } else {
+    if (!f16_map(&tm, a.xs, (uint64_t)a.H, (uint64_t)a.T, 1)) return cudaErrorInvalidValue;
     err = cudaFuncSetAttribute(pf_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<false>::SMEM);
     if (err != cudaSuccess) return err;
-    pf_gemm_kernel<false><<<grid, kPfGemmThreads, Cfg<false>::SMEM, s>>>(a);
+    pf_gemm_kernel<false><<<grid, kPfGemmThreads, Cfg<false>::SMEM, s>>>(a, tm);
   }
   return cudaGetLastError();
 }

@@ -352,7 +352,7 @@ __device__ void prefill_topk_token(const PrefillArgs& a, int t) {
       const float aq = __shfl_sync(0xFFFFFFFFu, av[q], src), eq = __shfl_sync(0xFFFFFFFFu, ev[q], src);
       if (lane == 0) {
         row[e] = lg;
-        if (fabsf(lg - aq) > eq && lg == lg) report_error(a.rb.ctrl, MOE_ERR_DEVICE_BAD_INDEX, 0x200);
+        if (fabsf(lg - aq) > eq && lg == lg) report_error(a.rb.ctrl, (uint32_t)MOE_ERR_DEVICE_BAD_INDEX, 0x200);
       }
     }
   }

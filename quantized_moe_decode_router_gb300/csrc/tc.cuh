@@ -30,6 +30,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          (1ull << 46);
 }
 
+// Descriptor of a K-major tile written by TMA with 128-byte swizzle: rows of
+// 128 bytes, 8-row atoms of 1024 bytes (the stride byte offset); the start
+// address advances by 32 bytes per K step of 16 two-byte elements.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+
 // Instruction descriptor of kind::f16 with FP32 accumulation, both operands
 // K-major.  ab = 0: f16 operands; ab = 1: bf16 operands.
 __host__ __device__ __forceinline__ uint32_t idesc_f16(int M, int N, int ab) {
@@ -120,6 +128,31 @@ __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, uint64_
     if (global_ns() - t0 > limit_ns) return false;
   }
   return false;
+}
+
+// Expect `bytes` of TMA transactions on the barrier's current phase and arrive.
+__device__ __forceinline__ void bar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// TMA: 2-D tile load of the tensor map's box at (c0, c1).
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// TMA: four rows r0..r3 (any order) of the tensor map's one-row box at column c0.
+__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int c0, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // Writes by this thread through the generic proxy (st.shared, cp.async)
