@@ -30,7 +30,7 @@ struct Layout {
   size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, rb_cnt, h_amax, hs_amax, gu_part, gu_cnt,
       dn_part, dn_cnt;
   // prefill path
-  size_t xs, xsig, xnorm, wnorm, hist, pos_of, tiles, h16, hsig;
+  size_t xg, xsig, xnorm, wnorm, hist, pos_of, tiles, h16, hsig;
   int max_tiles;
   size_t total;
 };
@@ -69,7 +69,7 @@ Layout make_layout(const moe_layer* L, int maxT) {
   o.dn_cnt = take(dn_tiles * 4);
   const size_t nchunk = (T + kPfChunk - 1) / kPfChunk;
   o.max_tiles = (int)(T * k / kPfTokTile + E + 1);
-  o.xs = take(T * H * 2);
+  o.xg = take(T * k * H * 2);
   o.xsig = take(T * 4);
   o.xnorm = take(T * 4);
   o.wnorm = take(E * 4);
@@ -287,7 +287,7 @@ PrefillArgs prefill_args(const moe_layer* L, const Layout& lo, void* ws, const v
   a.bias = L->router_bias;
   a.gate = qw(L->gate, L->fmt); a.up = qw(L->up, L->fmt); a.down = qw(L->down, L->fmt);
   a.rb = route_bufs(lo, ws);
-  a.xs = reinterpret_cast<uint16_t*>(b + lo.xs);
+  a.xg = reinterpret_cast<uint16_t*>(b + lo.xg);
   a.xsig = reinterpret_cast<int32_t*>(b + lo.xsig);
   a.xnorm = reinterpret_cast<float*>(b + lo.xnorm);
   a.wnorm = reinterpret_cast<float*>(b + lo.wnorm);
@@ -326,7 +326,7 @@ int32_t qmoe::clear_workspace_counters(const moe_layer* L, void* ws, size_t ws_b
   const size_t sections[4][2] = {{lo.ctrl, sizeof(Ctrl)},
                                  {lo.rb_cnt, H / 16 * 4},
                                  {lo.gu_cnt, lo.dn_part - lo.gu_cnt},
-                                 {lo.dn_cnt, lo.xs - lo.dn_cnt}};
+                                 {lo.dn_cnt, lo.xg - lo.dn_cnt}};
   for (const auto& sec : sections)
     if (cudaMemsetAsync(b + sec[0], 0, sec[1], s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
@@ -396,6 +396,7 @@ int32_t moe_route(const moe_layer* layer, const void* x, int32_t T, int32_t* top
     pa.out.topk_idx = topk_idx; pa.out.topk_w = topk_w; pa.out.cnt = expert_cnt; pa.out.off = expert_off;
     pa.out.pair = pair_list;
     pa.h_amax = nullptr;  // no expert pass follows
+    pa.xg = nullptr;
     return cuda_status(launch_prefill_route(pa, reinterpret_cast<cudaStream_t>(stream)));
   }
   RouterArgs ra = router_args(layer, lo, ws, x, T);

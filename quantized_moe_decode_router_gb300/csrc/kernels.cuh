@@ -99,7 +99,7 @@ cudaError_t launch_expert_fp8(int sfmt, bool down, const ExpertArgs& a, size_t s
 constexpr int kPfTokTile = 128;    // tokens per GEMM tile (MMA N)
 constexpr int kPfRowTile = 128;    // weight rows per GEMM tile (MMA M)
 constexpr int kPfChunk = 64;       // tokens per dispatch chunk
-constexpr int kPfGemmThreads = 448;  // 8 decode warps, B loader, MMA, 4 epilogue warps
+constexpr int kPfGemmThreads = 576;  // 8 decode warps, B loader, MMA, 8 epilogue warps
 
 struct PrefillArgs {
   int H, I, E, k, T;
@@ -110,7 +110,7 @@ struct PrefillArgs {
   QW gate, up, down;
   RouteBufs rb;         // logits [T, E] (approximate, then exact for candidates), top-k, cnt, off, pair
   RouteOut out;
-  uint16_t* xs;         // f16 [T, H]: x * 2^xsig[t]
+  uint16_t* xg;         // f16 [T*k, H]: row pos = x[token of pos] * 2^xsig[token] (sorted order)
   int32_t* xsig;        // [T]
   float* xnorm;         // [T] ||x_t||_2
   float* wnorm;         // [E] ||Wr_e||_2
@@ -122,7 +122,7 @@ struct PrefillArgs {
   uint32_t* h_amax;     // [T*k] max |h| (float bits) per sorted position
   uint16_t* h16;        // f16 [T*k, I]: h * 2^hsig[pos]
   int32_t* hsig;        // [T*k]
-  float* P;             // f32 [T*k, H] indexed by pair id
+  float* P;             // f32 [T*k, H] in sorted order (row pos)
   uint16_t* y;          // bf16 [T, H]
 };
 
@@ -135,7 +135,8 @@ struct Marks {
     if (fn) fn(ctx, i);
   }
 };
-// Router + dispatch; marks 1 (logits), 2 (top-k), 3 (dispatch).
+// Router + dispatch (+ the sorted token copy when a.xg is set); marks 1
+// (logits), 2 (top-k), 3 (dispatch).
 cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s, Marks mk = Marks{nullptr, nullptr});
 // Expert GEMMs + combine (after launch_prefill_route); marks 4 (gate/up),
 // 5 (h conversion), 6 (down), 7 (combine).

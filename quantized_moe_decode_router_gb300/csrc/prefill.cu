@@ -45,7 +45,7 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// One warp per token: max |x|, ||x||_2, and the f16 copy x * 2^s.
+// One warp per token: max |x| (-> the f16 shift s) and ||x||_2.
 __global__ void __launch_bounds__(kThreads) pf_prep_kernel(PrefillArgs a) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
@@ -69,17 +69,6 @@ __global__ void __launch_bounds__(kThreads) pf_prep_kernel(PrefillArgs a) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
   const int sft = f16_shift(amax);
-  const float mul = exp2i(sft);
-  uint4* xo = reinterpret_cast<uint4*>(a.xs + (size_t)t * H);
-  for (int c = lane; c < H / 8; c += 32) {
-    const uint4 v = __ldg(xr + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      o[i] = pack_f16x2(bf16_bits_to_float(w[i] & 0xFFFF) * mul, bf16_bits_to_float(w[i] >> 16) * mul);
-    xo[c] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
   if (lane == 0) {
     a.xsig[t] = sft;
     a.xnorm[t] = sqrtf(ss);
@@ -264,6 +253,29 @@ __global__ void __launch_bounds__(32) pf_place_kernel(PrefillArgs a) {
   }
 }
 
+// One warp per sorted position: the GEMM operand row xg[pos] = f16( x[t] * 2^s_t ),
+// t the token of the pair placed at pos (a contiguous copy per expert segment,
+// so the gate/up GEMM loads its token tiles as plain 2-D boxes).
+__global__ void __launch_bounds__(kThreads) pf_gather_kernel(PrefillArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int pos = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  if (pos >= a.T * a.k) return;
+  const int H = a.H;
+  const int t = a.rb.pair[pos] / a.k;
+  const float mul = exp2i(a.xsig[t]);
+  const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
+  uint4* xo = reinterpret_cast<uint4*>(a.xg + (size_t)pos * H);
+  for (int c = lane; c < H / 8; c += 32) {
+    const uint4 v = __ldg(xr + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = pack_f16x2(bf16_bits_to_float(w[i] & 0xFFFF) * mul, bf16_bits_to_float(w[i] >> 16) * mul);
+    xo[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // One warp per sorted position: h (bf16) -> f16 * 2^s, s from the row's max |h|.
 __global__ void __launch_bounds__(kThreads) pf_hconv_kernel(PrefillArgs a) {
   const int lane = threadIdx.x & 31;
@@ -286,7 +298,7 @@ __global__ void __launch_bounds__(kThreads) pf_hconv_kernel(PrefillArgs a) {
   if (lane == 0) a.hsig[pos] = sft;
 }
 
-// y[t] = bf16( sum_j w[t, j] * P[t*k + j] ), j ascending.
+// y[t] = bf16( sum_j w[t, j] * P[pos_of[t*k + j]] ), j ascending.
 __global__ void __launch_bounds__(kThreads) pf_combine_kernel(PrefillArgs a) {
   const int t = blockIdx.x, H = a.H, k = a.k;
   const float* wt = a.rb.topk_w + (size_t)t * k;
@@ -294,7 +306,8 @@ __global__ void __launch_bounds__(kThreads) pf_combine_kernel(PrefillArgs a) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
       const float w = __ldg(wt + j);
-      const float4 p = __ldcs(reinterpret_cast<const float4*>(a.P + ((size_t)t * k + j) * H) + c);
+      const int pos = __ldg(a.pos_of + (size_t)t * k + j);
+      const float4 p = __ldcs(reinterpret_cast<const float4*>(a.P + (size_t)pos * H) + c);
       acc.x = fmaf(w, p.x, acc.x);
       acc.y = fmaf(w, p.y, acc.y);
       acc.z = fmaf(w, p.z, acc.z);
@@ -321,15 +334,16 @@ cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s, Marks mk)
   pf_hist_kernel<<<nchunk, kThreads, a.E * 4, s>>>(a);
   pf_scan_kernel<<<1, kScanThreads, 0, s>>>(a);
   pf_place_kernel<<<nchunk, 32, a.E * 4, s>>>(a);
+  if (a.xg) pf_gather_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
   mk(3);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s, Marks mk) {
+  const int wpb = kThreads / 32;
   cudaError_t err = launch_prefill_gemm_nvfp4(false, a, sms, s);
   if (err != cudaSuccess) return err;
   mk(4);
-  const int wpb = kThreads / 32;
   pf_hconv_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   mk(5);

@@ -4,8 +4,9 @@
 //            G = Wg x^T, U = Wu x^T (two TMEM accumulators), epilogue
 //            h = bf16( silu(ts_g G) * (ts_u U) ) per sorted position.
 //   down:    for a token tile and 128 rows of H, D = Wd h^T, epilogue
-//            P[pair] = ts_d D (FP32 partials, DGPP README "Execution and
-//            performance", engine.prefill_bf16_partials off by default).
+//            P[pos] = ts_d D (FP32 partials by sorted position, DGPP README
+//            "Execution and performance", engine.prefill_bf16_partials off
+//            by default).
 //
 // The MMA is kind::f16 with f16 operands.  Weights are decoded in shared
 // memory, never in HBM (DGPP README intro "no dequantized copy"): e2m1 * e4m3
@@ -20,14 +21,16 @@
 //   warps 0-7  decode the weight rows of each K step (cp.async ring of raw
 //              codes per thread, e2m1/e4m3 conversion to f16) into the
 //              stage's A tiles;
-//   warp 8     loads the stage's token rows (B tile) with TMA into a
-//              128-byte-swizzled tile: four-row gathers of the scaled
-//              activations by token (gate/up), one 2-D box of the
-//              contiguous h rows (down); the stage's mbarrier counts bytes;
+//   warp 8     loads the stage's token rows (B tile) with one 2-D TMA box
+//              (128-byte swizzle) of the position-sorted operand rows
+//              (scaled activations for gate/up, h for down); the stage's
+//              mbarrier counts the bytes;
 //   warp 9     allocates TMEM and issues the MMAs from one thread;
 //              tcgen05.commit releases each stage and publishes each tile;
-//   warps 10-13 the epilogue, from TMEM accumulators that are double
-//              buffered so the next tile's MMAs overlap it.
+//   warps 10-17 the epilogue, from TMEM accumulators that are double
+//              buffered so the next tile's MMAs overlap it; outputs are
+//              staged in shared memory and written with bulk copies (h and P
+//              rows in sorted-position order).
 // Every wait on an mbarrier is bounded; a wait that gives up records
 // MOE_ERR_DEVICE_TIMEOUT and the CTA winds down (draining its MMAs before
 // TMEM is released).
@@ -44,33 +47,41 @@ constexpr int BM = kPfRowTile;  // weight rows per tile (MMA M)
 constexpr int NT = kPfTokTile;  // tokens per tile (MMA N at most)
 constexpr int BK = 64;          // K per step (f16: 128 bytes per row)
 constexpr int KB = BK * 2;
-constexpr int kDec = 256;       // decode / epilogue threads
-constexpr int kRaw = 4;         // raw ring stages per decode thread
-constexpr int kRawBytes = 48;   // per thread per raw stage
+constexpr int kDec = 256;       // decode threads (8 warps)
 constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s of global timer per wait
 
 template <bool DOWN>
 struct Cfg {
   static constexpr int NMAT = DOWN ? 1 : 2;
-  static constexpr int STAGES = DOWN ? 4 : 3;
+  static constexpr int SA = 2;                  // decoded-weight (A) stages
+  static constexpr int SB = 4;                  // token-row (B) stages: TMA latency spans several steps
+  static constexpr int RAW = DOWN ? 6 : 5;      // raw-code ring stages (prefetch distance RAW - 1 steps)
   static constexpr int TPR = kDec / (NMAT * BM);  // decode threads per weight row
   static constexpr int KT = BK / TPR;             // columns per decode thread per step
   static constexpr int A_BYTES = BM * KB;
   static constexpr int B_BYTES = NT * KB;
-  static constexpr int STAGE_BYTES = NMAT * A_BYTES + B_BYTES;
-  static constexpr int RAW_OFF = STAGES * STAGE_BYTES;
-  static constexpr int SMEM = RAW_OFF + kRaw * kDec * kRawBytes + 1024;
+  static constexpr int A_STAGE = NMAT * A_BYTES;
+  static constexpr int B_OFF = SA * A_STAGE;
+  static constexpr int CODE_BYTES = KT / 2;                    // per thread per step
+  static constexpr int RAW_BYTES = CODE_BYTES + 16;            // codes, then the 4-byte scale word (padded)
+  static constexpr int RAW_OFF = B_OFF + SB * B_BYTES;
+  static constexpr int STG_OFF = RAW_OFF + RAW * kDec * RAW_BYTES;  // epilogue staging [NT cols][BM rows]
+  static constexpr int OUT_BYTES = DOWN ? 4 : 2;                      // f32 partials / bf16 h
+  static constexpr int SMEM = STG_OFF + NT * BM * OUT_BYTES + 1024;
   static constexpr uint32_t ACC_COLS = NMAT * NT;      // one accumulator set
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // double buffered
 };
 
 // Warp roles.
-constexpr int kWarpLoader = 8;
-constexpr int kWarpMma = 9;
-constexpr int kWarpEpi0 = 10;  // warps 10..13: epilogue, warp w reads TMEM lanes 32 * (w % 4)
-constexpr int kEpiThreads = 128;
+constexpr int kWarpLoader = kDec / 32;       // 16
+constexpr int kWarpMma = kWarpLoader + 1;    // 17
+constexpr int kWarpEpi0 = kWarpMma + 1;      // 10..17: epilogue, warp w reads TMEM lanes 32 * (w % 4)
+constexpr int kEpiWarps = 8;                 // two per TMEM lane quarter, each half of the columns
+constexpr int kEpiThreads = kEpiWarps * 32;
+static_assert(kWarpEpi0 * 32 + kEpiThreads == kPfGemmThreads, "warp roles");
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// SiLU in FP32 (z / (1 + e^-z)); the quotient to within 2 ulp.
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + expf(-z)); }
 
 template <bool DOWN>
 __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs a,
@@ -78,9 +89,10 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
   using C = Cfg<DOWN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_a[C::STAGES], full_b[C::STAGES], empty[C::STAGES];
+  __shared__ __align__(8) uint64_t full_a[C::SA], empty_a[C::SA], full_b[C::SB], empty_b[C::SB];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], drain;
   __shared__ uint32_t tmem_slot;
+  __shared__ uint32_t s_amax[NT];  // gate/up epilogue: max |h| per column of the tile
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H, I = a.I, k = a.k;
@@ -92,10 +104,13 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
   Ctrl* ctrl = a.rb.ctrl;
 
   if (tid == 0) {
-    for (int i = 0; i < C::STAGES; ++i) {
+    for (int i = 0; i < C::SA; ++i) {
       tc::bar_init(&full_a[i], kDec);
+      tc::bar_init(&empty_a[i], 1);
+    }
+    for (int i = 0; i < C::SB; ++i) {
       tc::bar_init(&full_b[i], 1);
-      tc::bar_init(&empty[i], 1);
+      tc::bar_init(&empty_b[i], 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::bar_init(&acc_full[b], 1);
@@ -105,19 +120,20 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
     tc::bar_init_fence();
   }
   if (warp == kWarpMma) tc::tmem_alloc(&tmem_slot, C::TMEM_COLS);
+  if (tid < NT) s_amax[tid] = 0u;
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
 
-  if (warp < 8) {
+  if (warp < kDec / 32) {
     // ----------------------------------------------------------- decode --
     const int d = tid;
     const int m = d / (BM * C::TPR);
     const int rr = (d % (BM * C::TPR)) / C::TPR;
     const int hh = d % C::TPR;
     const QW& W = DOWN ? a.down : (m == 0 ? a.gate : a.up);
-    uint8_t* raw = smem + C::RAW_OFF + d * kRawBytes;
+    uint8_t* raw = smem + C::RAW_OFF + d * C::RAW_BYTES;
     uint32_t g = 0;
     bool ok = true;
     for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
@@ -127,40 +143,47 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
       const uint8_t* crow = W.data + (size_t)e * data_bytes(MOE_FMT_NVFP4, N, K) + (size_t)row * (K / 2);
       const uint8_t* srow = W.scales + (size_t)e * scale_bytes(MOE_FMT_NVFP4, N, K) + (size_t)row * (K / 16);
       auto issue = [&](int s) {
-        uint8_t* dst = raw + (s % kRaw) * (kDec * kRawBytes);
+        uint8_t* dst = raw + (s % C::RAW) * (kDec * C::RAW_BYTES);
         const int k0 = s * BK + hh * C::KT;
         cp_async16(dst, crow + k0 / 2);
-        if (C::KT == 64) cp_async16(dst + 16, crow + k0 / 2 + 16);
-        cp_async4(dst + 32, srow + (s * BK) / 16);
+        if (C::CODE_BYTES == 32) cp_async16(dst + 16, crow + k0 / 2 + 16);
+        cp_async4(dst + C::CODE_BYTES, srow + (s * BK) / 16);
       };
 #pragma unroll 1
-      for (int j = 0; j < kRaw - 1; ++j) {
+      for (int j = 0; j < C::RAW - 1; ++j) {
         if (j < nsteps) issue(j);
         cp_async_commit();
       }
 #pragma unroll 1
       for (int s = 0; s < nsteps; ++s, ++g) {
-        if (s + kRaw - 1 < nsteps) issue(s + kRaw - 1);
+        if (s + C::RAW - 1 < nsteps) issue(s + C::RAW - 1);
         cp_async_commit();
-        cp_async_wait<kRaw - 1>();
-        const uint8_t* src = raw + (s % kRaw) * (kDec * kRawBytes);
-        const uint32_t sw = *reinterpret_cast<const uint32_t*>(src + 32);
+        cp_async_wait<C::RAW - 1>();
+        const uint8_t* src = raw + (s % C::RAW) * (kDec * C::RAW_BYTES);
+        // 16-byte shared loads: conflict-free at this thread stride
+        uint32_t cw[C::KT / 8];
+#pragma unroll
+        for (int c4 = 0; c4 < C::KT / 32; ++c4) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * c4);
+          cw[4 * c4] = v.x; cw[4 * c4 + 1] = v.y; cw[4 * c4 + 2] = v.z; cw[4 * c4 + 3] = v.w;
+        }
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(src + C::CODE_BYTES);
         uint4 out[C::KT / 8];
 #pragma unroll
         for (int c = 0; c < C::KT / 8; ++c) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(src + 4 * c);
+          const uint32_t w = cw[c];
           const uint32_t sc = e4m3_bcast_f16x2(sw >> (8 * (hh * (C::KT / 16) + c / 2)));
           uint32_t v[4];
           e2m1x8_to_f16x2(w, v);
           out[c] = make_uint4(hmul2_u32(v[0], sc), hmul2_u32(v[1], sc), hmul2_u32(v[2], sc), hmul2_u32(v[3], sc));
         }
-        const int stage = g % C::STAGES;
-        if (!tc::bar_wait(&empty[stage], ((g / C::STAGES) & 1) ^ 1, kWaitLimit)) {
+        const int stage = g % C::SA;
+        if (!tc::bar_wait(&empty_a[stage], ((g / C::SA) & 1) ^ 1, kWaitLimit)) {
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x300 | (DOWN ? 1 : 0));
           ok = false;
           break;
         }
-        uint8_t* A = smem + stage * C::STAGE_BYTES + m * C::A_BYTES;
+        uint8_t* A = smem + stage * C::A_STAGE + m * C::A_BYTES;
 #pragma unroll
         for (int c = 0; c < C::KT / 8; ++c)
           *reinterpret_cast<uint4*>(A + tc::chunk_off(rr, hh * (C::KT / 8) + c, KB)) = out[c];
@@ -177,29 +200,19 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
       const int2 tile = a.tiles[it / RT];
       const int e = tile.x, pos0 = tile.y;
       const int n_valid = min(NT, a.rb.off[e + 1] - pos0);
-      // gate/up: this lane gathers tile rows 4*lane .. 4*lane+3 (rows past the
-      // tile's tokens repeat its last token: they only feed discarded columns)
-      int trow[4] = {0, 0, 0, 0};
-      if (!DOWN) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) trow[i] = a.rb.pair[pos0 + min(4 * lane + i, n_valid - 1)] / k;
-      }
 #pragma unroll 1
       for (int s = 0; s < nsteps; ++s, ++g) {
-        const int stage = g % C::STAGES;
-        if (!tc::bar_wait(&empty[stage], ((g / C::STAGES) & 1) ^ 1, kWaitLimit)) {
+        const int stage = g % C::SB;
+        if (!tc::bar_wait(&empty_b[stage], ((g / C::SB) & 1) ^ 1, kWaitLimit)) {
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x320 | (DOWN ? 1 : 0));
           ok = false;
           break;
         }
-        uint8_t* B = smem + stage * C::STAGE_BYTES + C::NMAT * C::A_BYTES;
+        uint8_t* B = smem + C::B_OFF + stage * C::B_BYTES;
         if (lane == 0) tc::bar_arrive_expect_tx(&full_b[stage], C::B_BYTES);
         __syncwarp();
-        if (DOWN) {
-          if (lane == 0) tc::tma_load_2d(B, &tmB, s * BK, pos0, &full_b[stage]);
-        } else {
-          tc::tma_gather4(B + lane * 4 * KB, &tmB, s * BK, trow[0], trow[1], trow[2], trow[3], &full_b[stage]);
-        }
+        // rows past the tile's tokens (the next segment, or zero fill) only feed discarded columns
+        if (lane == 0) tc::tma_load_2d(B, &tmB, s * BK, pos0, &full_b[stage]);
       }
     }
   } else if (warp == kWarpMma) {
@@ -222,17 +235,17 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         const uint32_t acc = tmem + buf * C::ACC_COLS;
 #pragma unroll 1
         for (int s = 0; s < nsteps; ++s, ++g) {
-          const int stage = g % C::STAGES;
-          const uint32_t par = (g / C::STAGES) & 1;
-          if (!tc::bar_wait(&full_a[stage], par, kWaitLimit) || !tc::bar_wait(&full_b[stage], par, kWaitLimit)) {
+          const int sa = g % C::SA, sb = g % C::SB;
+          if (!tc::bar_wait(&full_a[sa], (g / C::SA) & 1, kWaitLimit) ||
+              !tc::bar_wait(&full_b[sb], (g / C::SB) & 1, kWaitLimit)) {
             report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x340 | (DOWN ? 1 : 0));
             ok = false;
             break;
           }
           tc::fence_after_sync();
           tc::fence_proxy_async();
-          const uint32_t base = tc::smem_u32(smem + stage * C::STAGE_BYTES);
-          const uint32_t bB = base + C::NMAT * C::A_BYTES;
+          const uint32_t base = tc::smem_u32(smem + sa * C::A_STAGE);
+          const uint32_t bB = tc::smem_u32(smem + C::B_OFF + sb * C::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t db = tc::smem_desc_sw128(bB + kk * 32);
@@ -242,7 +255,8 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
               tc::mma_f16(acc + mm * NT, da, db, idesc, (s | kk) != 0);
             }
           }
-          tc::commit(&empty[stage]);
+          tc::commit(&empty_a[sa]);
+          tc::commit(&empty_b[sb]);
         }
         if (!ok) break;
         tc::commit(&acc_full[buf]);
@@ -254,72 +268,92 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
   } else {
     // --------------------------------------------------------- epilogue --
     // warp w handles TMEM lanes (= weight rows of the tile) 32 * (w % 4) ..
-    const int q = warp & 3;
+    // and half of the columns; the tile is staged in shared memory as
+    // [column][row] and leaves with one bulk copy per column (a contiguous
+    // run of the output row).
+    const int ew = warp - kWarpEpi0;
+    const int q = warp & 3, chalf = ew >> 2;  // columns [64 * chalf, 64 * chalf + 64)
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+    uint8_t* stg = smem + C::STG_OFF;
     int item = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++item) {
       const int2 tile = a.tiles[it / RT];
       const int rt = it % RT, e = tile.x, pos0 = tile.y;
       const int n_valid = min(NT, a.rb.off[e + 1] - pos0);
       const int buf = item & 1;
+      // per-column scale factors of this warp's columns, fetched before the wait
+      float un_c[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int pos_l = pos0 + min(chalf * 64 + i * 32 + lane, n_valid - 1);
+        if (DOWN) un_c[i] = exp2i(-a.hsig[pos_l]) * __ldg(a.down.ts + e);
+        else un_c[i] = exp2i(-a.xsig[a.rb.pair[pos_l] / k]);
+      }
+      const float tsg = DOWN ? 0.f : __ldg(a.gate.ts + e), tsu = DOWN ? 0.f : __ldg(a.up.ts + e);
       if (!tc::bar_wait(&acc_full[buf], (item >> 1) & 1, kWaitLimit)) {
         report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x310 | (DOWN ? 1 : 0));
         break;
       }
       tc::fence_after_sync();
+      tc::named_sync(1, kEpiThreads);  // staging free: the previous tile's copies have read it
       const uint32_t acc = tq + buf * C::ACC_COLS;
-      const int orow = rt * BM + q * 32 + lane;
-#pragma unroll 1
-      for (int c0 = 0; c0 < n_valid; c0 += 32) {
-        // column data for columns c0 + lane, shared through shuffles
-        const int cv = min(c0 + lane, n_valid - 1);
-        const int pos_l = pos0 + cv;
-        const int pair_l = a.rb.pair[pos_l];
-        float un_l;
-        if (DOWN) un_l = exp2i(-a.hsig[pos_l]) * __ldg(a.down.ts + e);
-        else un_l = exp2i(-a.xsig[pair_l / k]);
+      const int row = q * 32 + lane;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int c0 = chalf * 64 + i * 32;
+        if (c0 >= n_valid) break;
         const int ncol = min(32, n_valid - c0);
+        if (!DOWN) {
+          uint32_t gv[32], uv[32];
+          tc::tmem_ld32(acc + c0, gv);
+          tc::tmem_ld32(acc + NT + c0, uv);
+          tc::tmem_ld_wait();
+          uint16_t* st16 = reinterpret_cast<uint16_t*>(stg) + (size_t)c0 * BM + row;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          if (half * 16 >= ncol) break;
-          const int cb = c0 + half * 16;
-          if (!DOWN) {
-            uint32_t gv[16], uv[16];
-            tc::tmem_ld16(acc + cb, gv);
-            tc::tmem_ld16(acc + NT + cb, uv);
-            tc::tmem_ld_wait();
-            const float tsg = __ldg(a.gate.ts + e), tsu = __ldg(a.up.ts + e);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int jj = half * 16 + j;
-              const float un = __shfl_sync(0xFFFFFFFFu, un_l, jj);
-              if (jj >= ncol) break;
+          for (int j = 0; j < 32; ++j) {
+            const float un = __shfl_sync(0xFFFFFFFFu, un_c[i], j);
+            if (j < ncol) {
               const float gg = __uint_as_float(gv[j]) * (tsg * un);
               const float uu = __uint_as_float(uv[j]) * (tsu * un);
               const uint16_t hb = float_to_bf16_bits(silu(gg) * uu);
-              const int pos = pos0 + c0 + jj;
-              a.h[(size_t)pos * I + orow] = hb;
+              st16[j * BM] = hb;
               const uint32_t mag = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(hb & 0x7FFF) << 16);
-              if (lane == 0 && mag) atomicMax(&a.h_amax[pos], mag);
+              if (lane == 0) atomicMax(&s_amax[c0 + j], mag);
             }
-          } else {
-            uint32_t dv[16];
-            tc::tmem_ld16(acc + cb, dv);
-            tc::tmem_ld_wait();
+          }
+        } else {
+          uint32_t dv[32];
+          tc::tmem_ld32(acc + c0, dv);
+          tc::tmem_ld_wait();
+          float* st32 = reinterpret_cast<float*>(stg) + (size_t)c0 * BM + row;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int jj = half * 16 + j;
-              const float un = __shfl_sync(0xFFFFFFFFu, un_l, jj);
-              const int pr = __shfl_sync(0xFFFFFFFFu, pair_l, jj);
-              if (jj >= ncol) break;
-              a.P[(size_t)pr * H + orow] = __uint_as_float(dv[j]) * un;
-            }
+          for (int j = 0; j < 32; ++j) {
+            const float un = __shfl_sync(0xFFFFFFFFu, un_c[i], j);
+            if (j < ncol) st32[j * BM] = __uint_as_float(dv[j]) * un;
           }
         }
       }
       tc::fence_before_sync();
-      tc::bar_arrive(&acc_empty[buf]);
+      tc::bar_arrive(&acc_empty[buf]);  // TMEM buffer free for the MMA of a later tile
+      tc::fence_proxy_async();          // staging writes -> bulk copy reads
+      tc::named_sync(1, kEpiThreads);
+      if (ew == 0) {
+        for (int c = lane; c < n_valid; c += 32) {
+          const int pos = pos0 + c;
+          if (DOWN) {
+            tc::bulk_store(a.P + (size_t)pos * H + rt * BM, stg + c * BM * 4, BM * 4);
+          } else {
+            tc::bulk_store(a.h + (size_t)pos * I + rt * BM, stg + c * BM * 2, BM * 2);
+            const uint32_t mg = s_amax[c];
+            s_amax[c] = 0u;  // cleared for the next tile (its writers start after the next barrier)
+            if (mg) atomicMax(&a.h_amax[pos], mg);
+          }
+        }
+        tc::bulk_commit();
+        tc::bulk_wait_read();
+      }
     }
+    if (ew == 0) tc::bulk_wait();
   }
 
   tc::fence_before_sync();
@@ -374,7 +408,7 @@ cudaError_t launch_prefill_gemm_nvfp4(bool down, const PrefillArgs& a, int grid,
     if (err != cudaSuccess) return err;
     pf_gemm_kernel<true><<<grid, kPfGemmThreads, Cfg<true>::SMEM, s>>>(a, tm);
   } else {
-    if (!f16_map(&tm, a.xs, (uint64_t)a.H, (uint64_t)a.T, 1)) return cudaErrorInvalidValue;
+    if (!f16_map(&tm, a.xg, (uint64_t)a.H, (uint64_t)a.T * a.k, NT)) return cudaErrorInvalidValue;
     err = cudaFuncSetAttribute(pf_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<false>::SMEM);
     if (err != cudaSuccess) return err;
     pf_gemm_kernel<false><<<grid, kPfGemmThreads, Cfg<false>::SMEM, s>>>(a, tm);
