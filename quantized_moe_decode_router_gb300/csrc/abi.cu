@@ -30,7 +30,7 @@ struct Layout {
   size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, rb_cnt, h_amax, hs_amax, gu_part, gu_cnt,
       dn_part, dn_cnt;
   // prefill path
-  size_t xg, xsig, xnorm, wnorm, hist, pos_of, tiles, h16, hsig;
+  size_t xg, xsig, xnorm, wnorm, hist, pos_of, tiles, h16, hsig, xq, xsf, xqg, xsfg, hq, hsf;
   int max_tiles;
   size_t total;
 };
@@ -78,6 +78,12 @@ Layout make_layout(const moe_layer* L, int maxT) {
   o.tiles = take((size_t)o.max_tiles * 8);
   o.h16 = take(T * k * I * 2);
   o.hsig = take(T * k * 4);
+  o.xq = take(T * H / 2);
+  o.xsf = take(T * H / 16);
+  o.xqg = take(T * k * H / 2);
+  o.xsfg = take(T * k * H / 16);
+  o.hq = take(T * k * I / 2);
+  o.hsf = take(T * k * I / 16);
   o.total = at;
   return o;
 }
@@ -195,7 +201,9 @@ RouterArgs router_args(const moe_layer* L, const Layout& lo, void* ws, const voi
   RouterArgs ra;
   std::memset(&ra, 0, sizeof(ra));
   ra.H = L->hidden; ra.E = L->n_experts; ra.k = L->top_k; ra.T = T;
-  ra.wpr = router_warps_per_row(L->hidden);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  ra.wpr = router_warps_per_row(L->hidden, L->n_experts, sms);
   ra.x = static_cast<const uint16_t*>(x);
   ra.w = L->router_w;
   ra.bias = L->router_bias;
@@ -301,6 +309,12 @@ PrefillArgs prefill_args(const moe_layer* L, const Layout& lo, void* ws, const v
   a.hsig = reinterpret_cast<int32_t*>(b + lo.hsig);
   a.P = reinterpret_cast<float*>(b + lo.P);
   a.y = static_cast<uint16_t*>(y);
+  a.xq = b + lo.xq;
+  a.xsf = b + lo.xsf;
+  a.xqg = b + lo.xqg;
+  a.xsfg = b + lo.xsfg;
+  a.hq = b + lo.hq;
+  a.hsf = b + lo.hsf;
   return a;
 }
 
@@ -311,10 +325,15 @@ int sm_count(int* sms) {
   return MOE_OK;
 }
 
-// Formats the prefill expert GEMMs implement so far.
-bool prefill_supported(const moe_layer* L) {
-  return L->fmt == MOE_FMT_NVFP4 && L->shared_fmt == MOE_FMT_NONE && L->hidden % 128 == 0 &&
-         L->inter % 128 == 0;
+// Formats the prefill expert GEMMs implement so far.  The W4A4 lever also
+// needs whole 256-column stages and 16-byte aligned scale rows.
+bool prefill_supported(const moe_layer* L, bool act_quant) {
+  if (!(L->fmt == MOE_FMT_NVFP4 && L->shared_fmt == MOE_FMT_NONE && L->hidden % 128 == 0 && L->inter % 128 == 0))
+    return false;
+  if (!act_quant) return true;
+  const auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  return L->hidden % 256 == 0 && L->inter % 256 == 0 && a16(L->gate.scales) && a16(L->up.scales) &&
+         a16(L->down.scales);
 }
 
 }  // namespace
@@ -457,11 +476,13 @@ static int32_t prefill_forward_checked(const moe_layer* layer, const void* x, in
   if (!aligned16(x) || !aligned16(y)) return MOE_ERR_MISALIGNED;
   if (T < 1) return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
-  if ((opts && opts->act_quant) || !prefill_supported(layer)) return MOE_ERR_UNSUPPORTED;
+  const bool aq = opts && opts->act_quant;
+  if (!prefill_supported(layer, aq)) return MOE_ERR_UNSUPPORTED;
   int sms = 0;
   if ((st = sm_count(&sms)) != MOE_OK) return st;
   const Layout lo = make_layout(layer, ws_max_tokens(layer, ws_bytes));
-  const PrefillArgs pa = prefill_args(layer, lo, ws, x, T, y);
+  PrefillArgs pa = prefill_args(layer, lo, ws, x, T, y);
+  pa.act_quant = aq ? 1 : 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   MarkCtx mc{events, s, false};
   if (events) {

@@ -68,20 +68,6 @@ __global__ void dequantize_kernel(int fmt, QW w, int N, int K, int expert, int r
   o[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-// f32 -> E4M3 code, round to nearest even, saturating to +-448.
-__device__ __forceinline__ uint32_t f32_to_e4m3_sat(float x) {
-  unsigned short r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(r) : "f"(x));
-  return r & 0xFF;
-}
-
-// Two f32 -> two E2M1 codes in one byte (lo -> low nibble), RNE, saturating to +-6.
-__device__ __forceinline__ uint32_t f32x2_to_e2m1x2_sat(float lo, float hi) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}" : "=r"(r) : "f"(hi), "f"(lo));
-  return r & 0xFF;
-}
-
 // One thread per 16-element block.
 __global__ void quantize_act_nvfp4_kernel(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales) {
   const int nb = K / 16;

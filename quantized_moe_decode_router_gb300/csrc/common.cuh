@@ -116,6 +116,20 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&out)[4]) 
       : "r"(w));
 }
 
+// f32 -> E4M3 code, round to nearest even, saturating to +-448.
+__device__ __forceinline__ uint32_t f32_to_e4m3_sat(float x) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(r) : "f"(x));
+  return r & 0xFF;
+}
+
+// Two f32 -> two E2M1 codes in one byte (lo -> low nibble), RNE, saturating to +-6.
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}" : "=r"(r) : "f"(hi), "f"(lo));
+  return r & 0xFF;
+}
+
 // Two E4M3 codes (low byte -> low half) -> f16x2, exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   uint32_t r;

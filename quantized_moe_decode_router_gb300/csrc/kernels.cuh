@@ -78,7 +78,7 @@ constexpr int kRouterThreads = 256;
 // Cap on stored block sums when tiles are split along K (bounds the partial buffers).
 constexpr int kMaxSplitBlocks = 16384;
 
-int router_warps_per_row(int H);
+int router_warps_per_row(int H, int E, int sms);
 // Zero the control block and every arrival counter of a workspace laid out
 // for this layer and workspace size (stream-ordered memsets, no allocation).
 int32_t clear_workspace_counters(const moe_layer* L, void* ws, size_t ws_bytes, cudaStream_t s);
@@ -124,6 +124,14 @@ struct PrefillArgs {
   int32_t* hsig;        // [T*k]
   float* P;             // f32 [T*k, H] in sorted order (row pos)
   uint16_t* y;          // bf16 [T, H]
+  // NVFP4 W4A4 lever (act_quant = 1)
+  int act_quant;
+  uint8_t* xq;          // [T, H/2] E2M1 codes of x (16-element blocks)
+  uint8_t* xsf;         // [T, H/16] E4M3 block scales of x
+  uint8_t* xqg;         // [T*k, H/2] codes in sorted order
+  uint8_t* xsfg;        // [T*k, H/16]
+  uint8_t* hq;          // [T*k, I/2] codes of h in sorted order
+  uint8_t* hsf;         // [T*k, I/16]
 };
 
 // Optional host callback between launches (event records of the timed entry
@@ -143,6 +151,7 @@ cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s, Marks mk 
 cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s, Marks mk = Marks{nullptr, nullptr});
 cudaError_t launch_prefill_topk(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_gemm_nvfp4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_prefill_gemm_w4a4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
 size_t prefill_gemm_smem(bool down);
 
 // moe_dequantize / moe_quantize_act_nvfp4

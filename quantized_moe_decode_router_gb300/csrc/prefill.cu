@@ -276,6 +276,22 @@ __global__ void __launch_bounds__(kThreads) pf_gather_kernel(PrefillArgs a) {
   }
 }
 
+// W4A4: one warp per sorted position copies the NVFP4 codes and block scales
+// of its token (16-byte chunks).
+__global__ void __launch_bounds__(kThreads) pf_gather_q_kernel(PrefillArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int pos = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  if (pos >= a.T * a.k) return;
+  const int H = a.H;
+  const int t = a.rb.pair[pos] / a.k;
+  const uint4* cs = reinterpret_cast<const uint4*>(a.xq + (size_t)t * (H / 2));
+  uint4* cd = reinterpret_cast<uint4*>(a.xqg + (size_t)pos * (H / 2));
+  for (int c = lane; c < H / 32; c += 32) cd[c] = cs[c];
+  const uint4* ss = reinterpret_cast<const uint4*>(a.xsf + (size_t)t * (H / 16));
+  uint4* sd = reinterpret_cast<uint4*>(a.xsfg + (size_t)pos * (H / 16));
+  for (int c = lane; c < H / 256; c += 32) sd[c] = ss[c];
+}
+
 // One warp per sorted position: h (bf16) -> f16 * 2^s, s from the row's max |h|.
 __global__ void __launch_bounds__(kThreads) pf_hconv_kernel(PrefillArgs a) {
   const int lane = threadIdx.x & 31;
@@ -334,14 +350,31 @@ cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s, Marks mk)
   pf_hist_kernel<<<nchunk, kThreads, a.E * 4, s>>>(a);
   pf_scan_kernel<<<1, kScanThreads, 0, s>>>(a);
   pf_place_kernel<<<nchunk, 32, a.E * 4, s>>>(a);
-  if (a.xg) pf_gather_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
+  if (a.act_quant) {
+    cudaError_t e2 = launch_quantize_act_nvfp4(a.x, a.T, a.H, a.xq, a.xsf, s);
+    if (e2 != cudaSuccess) return e2;
+    pf_gather_q_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
+  } else if (a.xg) {
+    pf_gather_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
+  }
   mk(3);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s, Marks mk) {
   const int wpb = kThreads / 32;
-  cudaError_t err = launch_prefill_gemm_nvfp4(false, a, sms, s);
+  cudaError_t err;
+  if (a.act_quant) {
+    if ((err = launch_prefill_gemm_w4a4(false, a, sms, s)) != cudaSuccess) return err;
+    mk(4);
+    mk(5);
+    if ((err = launch_prefill_gemm_w4a4(true, a, sms, s)) != cudaSuccess) return err;
+    mk(6);
+    pf_combine_kernel<<<a.T, kThreads, 0, s>>>(a);
+    mk(7);
+    return cudaGetLastError();
+  }
+  err = launch_prefill_gemm_nvfp4(false, a, sms, s);
   if (err != cudaSuccess) return err;
   mk(4);
   pf_hconv_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);

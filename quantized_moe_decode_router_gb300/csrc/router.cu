@@ -59,39 +59,65 @@ __device__ __forceinline__ unsigned long long lane_max(const unsigned long long 
   return t[0];
 }
 
+// Order-preserving unsigned image of a logit (larger logit -> larger key);
+// NaN ranks like -inf, -0 like +0.  Every real logit maps above 0, the key of
+// a taken or absent entry.
+__device__ __forceinline__ uint32_t ord_key(float v) {
+  uint32_t b = __float_as_uint(v);
+  if (v != v) b = 0xFF800000u;  // -inf
+  if (b == 0x80000000u) b = 0;  // -0 ties with +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float ord_value(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+// Largest key of the lane and its slot; equal keys -> the lower slot (lower expert id).
+template <int NQ>
+__device__ __forceinline__ void lane_best(const uint32_t (&key)[NQ], uint32_t& bk, int& bq) {
+  bk = key[0];
+  bq = 0;
+#pragma unroll
+  for (int q = 1; q < NQ; ++q)
+    if (key[q] > bk) { bk = key[q]; bq = q; }
+}
+
 // One warp: top-k of one token.  E <= 32 NQ: lane holds the keys of experts
-// lane + 32 q in registers; after each round only the lane whose candidate
-// won recomputes its maximum.
+// lane + 32 q in registers.  Each round takes the largest key over the warp
+// (one redux), then the lowest expert id among the lanes holding it (a
+// second redux): logit descending, ties to the lower id.  Only the winning
+// lane rescans its keys.
 template <int NQ>
 __device__ void topk_warp(const float* __restrict__ logits_row, int E, int k, int32_t* idx_out, float* w_out,
                           int32_t* idx_out2, float* w_out2) {
   const int lane = threadIdx.x & 31;
-  unsigned long long key[NQ];
+  uint32_t key[NQ];
 #pragma unroll
   for (int q = 0; q < NQ; ++q) {
     const int e = q * 32 + lane;
-    key[q] = (e < E) ? sel_key(__ldcg(logits_row + e), e) : 0ull;
+    key[q] = (e < E) ? ord_key(__ldcg(logits_row + e)) : 0u;
   }
-  unsigned long long mine = lane_max<NQ>(key);
+  uint32_t bk;
+  int bq;
+  lane_best<NQ>(key, bk, bq);
   float sel_v0 = 0.f, sum = 0.f, my_ex = 0.f;
   int my_i = 0;
   for (int j = 0; j < k; ++j) {
-    unsigned long long best = mine;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
-    const int bi = key_id(best);
-    if (best == mine) {  // this lane's candidate won: drop it, find the next one
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
+    const uint32_t id = __reduce_min_sync(0xFFFFFFFFu, bk == m ? (uint32_t)(bq * 32 + lane) : 0xFFFFFFFFu);
+    if ((int)(id & 31) == lane) {  // this lane's candidate won: drop it, find the next one
 #pragma unroll
       for (int q = 0; q < NQ; ++q)
-        if (q == (bi >> 5)) key[q] = 0ull;
-      mine = lane_max<NQ>(key);
+        if (q == bq) key[q] = 0u;
+      lane_best<NQ>(key, bk, bq);
     }
-    const float bv = key_value(best);
+    const float bv = ord_value(m);
     if (j == 0) sel_v0 = bv;
     // w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0); the sum runs in j order
     const float ex = expf(bv - sel_v0);
     sum += ex;
-    if (lane == j) { my_ex = ex; my_i = bi; }
+    if (lane == j) { my_ex = ex; my_i = (int)id; }
   }
   if (lane < k) {
     const float w = my_ex / sum;
@@ -256,13 +282,23 @@ __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArg
     a.rb.off[i] = s_off[i];
     if (a.out.off) a.out.off[i] = s_off[i];
   }
-  for (int p = tid; p < P; p += blockDim.x) {
-    const int ex = s_idx[p];
-    int rank = 0;
-    for (int q = 0; q < p; ++q) rank += (s_idx[q] == ex);
-    const int pos = s_off[ex] + rank;
-    a.rb.pair[pos] = p;
-    if (a.out.pair) a.out.pair[pos] = p;
+  __syncthreads();  // the offsets are out: s_off now serves as the running position
+  // pair positions: one warp walks the pairs in order, 32 at a time; equal
+  // experts within a batch are ranked by lane (match_any), s_off[e] advances
+  if (warp == 0) {
+    for (int b = 0; b < P; b += 32) {
+      const int p = b + lane;
+      const int ex = p < P ? s_idx[p] : -1 - lane;
+      const uint32_t peers = __match_any_sync(0xFFFFFFFFu, ex);
+      if (p < P) {
+        const int pos = s_off[ex] + __popc(peers & ((1u << lane) - 1u));
+        a.rb.pair[pos] = p;
+        if (a.out.pair) a.out.pair[pos] = p;
+      }
+      __syncwarp();
+      if (p < P && lane == 31 - __clz(peers)) s_off[ex] += __popc(peers);
+      __syncwarp();
+    }
   }
   if (tid == 0) a.rb.ctrl->router_arrive = 0;  // leave the counter at zero for the next call
 }
@@ -374,10 +410,14 @@ __global__ void __launch_bounds__(kRouterThreads) prefill_topk_kernel(PrefillArg
 
 }  // namespace
 
-// Warps sharing one expert row: split H while each warp keeps >= 512 columns.
-int router_warps_per_row(int H) {
+// Warps sharing one expert row: split H (up to all 8 warps of a CTA) while
+// every warp keeps at least 256 columns (two float4 per lane) and the grid
+// (E * w / 8 CTAs) still fits one wave of two CTAs per SM.
+int router_warps_per_row(int H, int E, int sms) {
   int w = 1;
-  while (w < kWarpsR && H % (4 * 32 * w * 2) == 0 && H / (w * 2) >= 512) w *= 2;
+  while (w < kWarpsR && H % (4 * 32 * w * 2) == 0 && H / (w * 2) >= 256 &&
+         (long)E * (w * 2) <= (long)kWarpsR * 2 * sms)
+    w *= 2;
   return w;
 }
 

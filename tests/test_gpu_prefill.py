@@ -139,3 +139,61 @@ def test_prefill_unsupported_format_is_reported():
     ws = G.new_ws(dl, 20)
     st = B.moe_prefill_forward(dl, x, 20, y, ws, raise_on_error=False)
     assert st == B.MOE_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------ W4A4 lever ----
+
+W4A4 = [
+    LayerConfig("w4_small", FMT_NVFP4, H=512, E=6, k=2, I=256),
+    LayerConfig("w4_skew", FMT_NVFP4, H=768, E=20, k=4, I=512, zipf_s=1.1),
+]
+
+
+def _check_w4a4(y_bits, ref_bits, tokens=None):
+    """W4A4 against the oracle's act_quant mode.  x is quantised identically on
+    both sides (same rule, same BF16 input); h is re-quantised from a BF16 value
+    that the GPU reaches with FP32 accumulation, so a rare h can land on the
+    other side of a BF16 or E2M1 rounding boundary.  Bar: every element within
+    max(2 BF16 ulp, 1e-3) except at most 0.1 %, and those within 2^-5 relative."""
+    y = F.bf16_to_f64(y_bits if tokens is None else y_bits[tokens])
+    r = F.bf16_to_f64(ref_bits)
+    ok = M.within_tolerance(y, r)
+    assert np.isfinite(y).all()
+    frac_bad = float((~ok).mean())
+    assert frac_bad <= 1e-3, f"{int((~ok).sum())} of {ok.size} outputs outside the 2-ulp bar"
+    loose = np.abs(y - r) <= np.maximum(2.0 ** -5 * np.abs(r), 1e-2)
+    assert loose.all(), f"{int((~loose).sum())} outputs outside the loose bar"
+
+
+@pytest.mark.parametrize("cfg", W4A4, ids=[c.name for c in W4A4])
+@pytest.mark.parametrize("T", [1, 37, 300])
+def test_prefill_w4a4_matches_oracle(cfg, T):
+    hl = synth.make_layer(cfg, seed=9)
+    dl = to_device(hl)
+    x = synth.make_tokens(cfg, T, seed=9, batch=T)
+    y, routing = G.decode(dl, x, prefill=True, act_quant=1)
+    ref = M.layer_forward(hl, x, act_quant=True)
+    _check_w4a4(y, ref["y_bits"])
+    assert_prefill_routing(routing, ref, ref["near_midpoint"])
+
+
+def test_prefill_w4a4_workload_sampled():
+    hl = G.host_layer("prefill_nvfp4")
+    dl = G.device_layer("prefill_nvfp4")
+    T, tokens = 4096, [0, 5, 2047, 4095]
+    x = synth.make_tokens(hl.cfg, T, seed=0, batch=T)
+    y, _ = G.decode(dl, x, prefill=True, act_quant=1)
+    ref = M.layer_forward(hl, x, act_quant=True, tokens=tokens)
+    _check_w4a4(y, ref["y_bits"], tokens)
+
+
+def test_prefill_w4a4_differs_from_exact_chain():
+    # the lever is a different computation: it must not silently run the exact chain
+    cfg = W4A4[0]
+    hl = synth.make_layer(cfg, seed=4)
+    dl = to_device(hl)
+    x = synth.make_tokens(cfg, 64, seed=4)
+    y_exact, _ = G.decode(dl, x, prefill=True)
+    y_w4, _ = G.decode(dl, x, prefill=True, act_quant=1)
+    assert not np.array_equal(y_exact, y_w4)
+    _check_y(y_exact, M.layer_forward(hl, x)["y_bits"])
