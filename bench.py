@@ -392,8 +392,47 @@ def run_prefill(args, local, peak_bf16, peak_kind):
     st = q.moe_check(ws)
     if st != 0:
         raise RuntimeError(f"device-side error: {q.status_string(st)}")
+    # the W4A4 lever (act_quant = 1): block-scaled FP4 GEMMs, same workload
+    ws4 = torch.empty(q.workspace_size(lay, T, 1), dtype=torch.uint8, device="cuda")
+    q.workspace_init(ws4)
+    g4 = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            q.moe_prefill_forward(lay, xs[i % NB], T, y, ws4, stream=stream, act_quant=1)
+        stream.synchronize()
+        with torch.cuda.graph(g4, stream=stream):
+            for i in range(G):
+                q.moe_prefill_forward(lay, xs[i % NB], T, y, ws4, stream=stream, act_quant=1)
+        for _ in range(2):
+            g4.replay()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g4.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us4 = e0.elapsed_time(e1) * 1e3 / (reps * G)
+    evs4 = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n)]
+    for row in evs4:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    gt4 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gt4, stream=stream):
+        for i in range(n):
+            q.moe_prefill_forward_timed(lay, xs[i % NB], T, y, ws4, evs4[i], stream=stream, act_quant=1)
+    with torch.cuda.stream(stream):
+        gt4.replay()
+    torch.cuda.synchronize()
+    dur4 = np.array([[evs4[i][j].elapsed_time(evs4[i][j + 1]) for j in range(7)] for i in range(n)]).mean(axis=0) * 1e3
+    st = q.moe_check(ws4)
+    if st != 0:
+        raise RuntimeError(f"device-side error (W4A4): {q.status_string(st)}")
     pairs = T * cfg.k
     flops = pairs * 6.0 * cfg.H * cfg.I
+    gemm4_us = dur4[3] + dur4[5]
+    tflops4 = flops / (gemm4_us * 1e-6) / 1e12
     gemm_us = dur[3] + dur[5]
     tflops = flops / (gemm_us * 1e-6) / 1e12
     fp4_peak = peak_bf16 * 13.5 / 2.25
@@ -411,6 +450,13 @@ def run_prefill(args, local, peak_bf16, peak_kind):
                  "peak_kind": peak_kind},
         "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
         "graph": f"CUDA graph of {G} layer calls, {reps} replays",
+        "w4a4": {"path": "NVFP4 activations (lever, act_quant=1): tcgen05 kind::mxf4nvf4 block-scaled GEMMs",
+                 "us_per_layer": round(us4, 1), "tokens_per_s": round(T / (us4 * 1e-6), 1),
+                 "kernel_us": {k: round(float(v), 2) for k, v in zip(
+                     ["router_logits", "router_topk", "dispatch_quantise", "gateup_gemm", "-", "down_gemm",
+                      "combine"], dur4) if k != "-"},
+                 "achieved_tflops": round(tflops4, 1), "frac_fp4_peak": round(tflops4 / fp4_peak, 4),
+                 "fp4_peak_tflops": round(fp4_peak, 1), "peak_kind": peak_kind},
     }
 
 

@@ -229,9 +229,9 @@ def moe_prefill_forward(layer: Layer, x, T: int, y, ws, stream=None, act_quant: 
     return _check(st, "moe_prefill_forward") if raise_on_error else st
 
 
-def moe_prefill_forward_timed(layer: Layer, x, T: int, y, ws, events, stream=None) -> int:
+def moe_prefill_forward_timed(layer: Layer, x, T: int, y, ws, events, stream=None, act_quant: int = 0) -> int:
     """moe_prefill_forward recording torch.cuda.Event objects (8, or None entries) between its kernels."""
-    lc, o = layer.c(), _opts(0)
+    lc, o = layer.c(), _opts(act_quant)
     arr = (ctypes.c_void_p * 8)(*[None if e is None else int(e.cuda_event) for e in events])
     st = load().moe_prefill_forward_timed(ctypes.byref(lc), _ptr(x), T, _ptr(y), ctypes.byref(o), _ptr(ws),
                                           ws.numel() * ws.element_size(), _stream_handle(stream), arr)

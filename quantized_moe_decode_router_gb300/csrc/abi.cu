@@ -304,7 +304,7 @@ PrefillArgs prefill_args(const moe_layer* L, const Layout& lo, void* ws, const v
   a.tiles = reinterpret_cast<int2*>(b + lo.tiles);
   a.max_tiles = lo.max_tiles;
   a.h = reinterpret_cast<uint16_t*>(b + lo.h);
-  a.h_amax = reinterpret_cast<uint32_t*>(b + lo.h_amax);
+  a.h_amax = nullptr;  // the h conversion finds each row's maximum itself
   a.h16 = reinterpret_cast<uint16_t*>(b + lo.h16);
   a.hsig = reinterpret_cast<int32_t*>(b + lo.hsig);
   a.P = reinterpret_cast<float*>(b + lo.P);
@@ -414,7 +414,6 @@ int32_t moe_route(const moe_layer* layer, const void* x, int32_t T, int32_t* top
     PrefillArgs pa = prefill_args(layer, lo, ws, x, T, nullptr);
     pa.out.topk_idx = topk_idx; pa.out.topk_w = topk_w; pa.out.cnt = expert_cnt; pa.out.off = expert_off;
     pa.out.pair = pair_list;
-    pa.h_amax = nullptr;  // no expert pass follows
     pa.xg = nullptr;
     return cuda_status(launch_prefill_route(pa, reinterpret_cast<cudaStream_t>(stream)));
   }

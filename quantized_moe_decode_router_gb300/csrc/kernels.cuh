@@ -119,7 +119,7 @@ struct PrefillArgs {
   int2* tiles;          // [max tiles] (expert, first sorted position)
   int max_tiles;
   uint16_t* h;          // bf16 [T*k, I] in sorted order
-  uint32_t* h_amax;     // [T*k] max |h| (float bits) per sorted position
+  uint32_t* h_amax;     // unused by the prefill path (nullptr)
   uint16_t* h16;        // f16 [T*k, I]: h * 2^hsig[pos]
   int32_t* hsig;        // [T*k]
   float* P;             // f32 [T*k, H] in sorted order (row pos)

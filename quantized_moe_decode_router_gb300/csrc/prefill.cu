@@ -292,15 +292,24 @@ __global__ void __launch_bounds__(kThreads) pf_gather_q_kernel(PrefillArgs a) {
   for (int c = lane; c < H / 256; c += 32) sd[c] = ss[c];
 }
 
-// One warp per sorted position: h (bf16) -> f16 * 2^s, s from the row's max |h|.
+// One warp per sorted position: h (bf16) -> f16 * 2^s, s from the row's max |h|
+// (found here: the row spans several gate/up tiles).
 __global__ void __launch_bounds__(kThreads) pf_hconv_kernel(PrefillArgs a) {
   const int lane = threadIdx.x & 31;
   const int pos = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
   if (pos >= a.T * a.k) return;
   const int I = a.I;
-  const int sft = f16_shift(a.h_amax[pos]);
-  const float mul = exp2i(sft);
   const uint4* hr = reinterpret_cast<const uint4*>(a.h + (size_t)pos * I);
+  uint32_t amax = 0;
+  for (int c = lane; c < I / 8; c += 32) {
+    const uint4 v = hr[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) amax = max(amax, max((w[i] & 0x7FFFu) << 16, (w[i] >> 16 & 0x7FFFu) << 16));
+  }
+  amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+  const int sft = f16_shift(amax);
+  const float mul = exp2i(sft);
   uint4* ho = reinterpret_cast<uint4*>(a.h16 + (size_t)pos * I);
   for (int c = lane; c < I / 8; c += 32) {
     const uint4 v = hr[c];

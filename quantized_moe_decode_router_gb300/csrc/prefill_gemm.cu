@@ -92,7 +92,6 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
   __shared__ __align__(8) uint64_t full_a[C::SA], empty_a[C::SA], full_b[C::SB], empty_b[C::SB];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], drain;
   __shared__ uint32_t tmem_slot;
-  __shared__ uint32_t s_amax[NT];  // gate/up epilogue: max |h| per column of the tile
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H, I = a.I, k = a.k;
@@ -120,7 +119,6 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
     tc::bar_init_fence();
   }
   if (warp == kWarpMma) tc::tmem_alloc(&tmem_slot, C::TMEM_COLS);
-  if (tid < NT) s_amax[tid] = 0u;
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -315,10 +313,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
             if (j < ncol) {
               const float gg = __uint_as_float(gv[j]) * (tsg * un);
               const float uu = __uint_as_float(uv[j]) * (tsu * un);
-              const uint16_t hb = float_to_bf16_bits(silu(gg) * uu);
-              st16[j * BM] = hb;
-              const uint32_t mag = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(hb & 0x7FFF) << 16);
-              if (lane == 0) atomicMax(&s_amax[c0 + j], mag);
+              st16[j * BM] = float_to_bf16_bits(silu(gg) * uu);
             }
           }
         } else {
@@ -344,9 +339,6 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
             tc::bulk_store(a.P + (size_t)pos * H + rt * BM, stg + c * BM * 4, BM * 4);
           } else {
             tc::bulk_store(a.h + (size_t)pos * I + rt * BM, stg + c * BM * 2, BM * 2);
-            const uint32_t mg = s_amax[c];
-            s_amax[c] = 0u;  // cleared for the next tile (its writers start after the next barrier)
-            if (mg) atomicMax(&a.h_amax[pos], mg);
           }
         }
         tc::bulk_commit();

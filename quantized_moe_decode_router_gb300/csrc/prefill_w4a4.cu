@@ -10,7 +10,8 @@
 //
 //   gate/up: G = Wg x^T, U = Wu x^T per (token tile, 128 rows of I);
 //            h = bf16( silu(ts_g G) * (ts_u U) ), re-quantised to NVFP4 per
-//            16 rows of I in the epilogue (the operand of the down GEMM).
+//            16 rows of I in the epilogue (the operand of the down GEMM): h is
+//            staged first so the TMEM accumulator is released early.
 //   down:    P[pos] = ts_d (Wd h^T), FP32 partials by sorted position.
 //
 // Operands: packed codes as 2-D TMA boxes of 128 rows x 128 bytes (256 K),
@@ -38,7 +39,7 @@ constexpr int BM = kPfRowTile;
 constexpr int NT = kPfTokTile;
 constexpr int KS = 256;        // K per stage
 constexpr int KSB = KS / 2;    // bytes of codes per row per stage
-constexpr int ST = 4;          // stages
+constexpr int ST = 3;          // stages
 constexpr uint64_t kWaitLimit = 2000000000ull;
 constexpr int kThreads = 512;
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSf0 = 4, kWarpEpi0 = 8;
@@ -51,7 +52,8 @@ struct Cw {
   static constexpr int B_BYTES = NT * KSB;
   static constexpr int STAGE = NMAT * A_BYTES + B_BYTES;
   static constexpr int STG_OFF = ST * STAGE;
-  static constexpr int STG_BYTES = DOWN ? NT * BM * 4 : NT * (BM / 2);
+  // down: P tile f32 [NT][BM]; gate/up: h tile bf16 [NT][BM], then its codes [NT][BM / 2]
+  static constexpr int STG_BYTES = DOWN ? NT * BM * 4 : NT * BM * 2 + NT * (BM / 2);
   static constexpr int SMEM = STG_OFF + STG_BYTES + 1024;
   static constexpr int ACC_BUFS = DOWN ? 2 : 1;
   static constexpr uint32_t ACC_COLS = NMAT * NT;
@@ -184,7 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
       bool ok = true;
       for (int s = 0; s < nst; ++s, ++g) {
         const int stage = g % ST;
-        uint32_t v[16];
+        // the scales do not depend on the slot: load them before waiting for it
+        uint32_t v[C::NMAT + 1][16];
+#pragma unroll
+        for (int m = 0; m < C::NMAT; ++m) {
+          const QW& W = DOWN ? a.down : (m == 0 ? a.gate : a.up);
+          load_scales(W.scales + (size_t)e * N * Kb, Kb, rt * BM, lane, N, s * 16, v[m]);
+        }
+        load_scales(sfb_base, Kb, pos0, lane, P, s * 16, v[C::NMAT]);
         if (!tc::bar_wait(&empty[stage], ((g / ST) & 1) ^ 1, kWaitLimit)) {
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x410 | (DOWN ? 1 : 0));
           ok = false;
@@ -193,14 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
         tc::fence_after_sync();
         const uint32_t col = tmem + lq + C::SF_BASE + stage * C::SF_STAGE;
 #pragma unroll
-        for (int m = 0; m < C::NMAT; ++m) {
-          const QW& W = DOWN ? a.down : (m == 0 ? a.gate : a.up);
-          const uint8_t* sb = W.scales + (size_t)e * N * Kb;
-          load_scales(sb, Kb, rt * BM, lane, N, s * 16, v);
-          tmem_st16(col + m * 16, v);
-        }
-        load_scales(sfb_base, Kb, pos0, lane, P, s * 16, v);
-        tmem_st16(col + C::NMAT * 16, v);
+        for (int m = 0; m <= C::NMAT; ++m) tmem_st16(col + m * 16, v[m]);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc::fence_before_sync();
         tc::bar_arrive(&sf_full[stage]);
@@ -282,31 +284,16 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
         if (c0 >= n_valid) break;
         const int ncol = min(32, n_valid - c0);
         if (!DOWN) {
+          // phase 1: h = bf16(silu(ts_g G) * (ts_u U)) into the staging tile [column][row]
           uint32_t gv[32], uv[32];
           tc::tmem_ld32(acc + c0, gv);
           tc::tmem_ld32(acc + NT + c0, uv);
           tc::tmem_ld_wait();
-#pragma unroll 4
-          for (int j = 0; j < 32; ++j) {
-            if (j >= ncol) break;
-            const float hv =
-                bf16_bits_to_float(float_to_bf16_bits(silu(__uint_as_float(gv[j]) * ts0) * (__uint_as_float(uv[j]) * ts1)));
-            // NVFP4 of h over 16 rows (lanes 0-15 / 16-31 of this warp): the
-            // activation quantiser's rule, scale e4m3(amax / 6), codes e2m1(h / s)
-            float amax = fabsf(hv);
+          uint16_t* st16 = reinterpret_cast<uint16_t*>(stg) + (size_t)c0 * BM + row;
 #pragma unroll
-            for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-            const uint32_t sc = f32_to_e4m3_sat(__fdiv_rn(amax, 6.0f));
-            const float s = e4m3_value(sc);
-            const float qv = s > 0.f ? __fdiv_rn(hv, s) : 0.f;
-            const float qn = __shfl_down_sync(0xFFFFFFFFu, qv, 1);
-            const int pos = pos0 + c0 + j;
-            if ((lane & 1) == 0) {
-              const uint32_t byte = s > 0.f ? f32x2_to_e2m1x2_sat(qv, qn) : 0u;
-              stg[(c0 + j) * (BM / 2) + row / 2] = (uint8_t)byte;
-            }
-            if ((lane & 15) == 0) a.hsf[(size_t)pos * (I / 16) + (rt * BM + row) / 16] = (uint8_t)sc;
-          }
+          for (int j = 0; j < 32; ++j)
+            if (j < ncol)
+              st16[j * BM] = float_to_bf16_bits(silu(__uint_as_float(gv[j]) * ts0) * (__uint_as_float(uv[j]) * ts1));
         } else {
           uint32_t dv[32];
           tc::tmem_ld32(acc + c0, dv);
@@ -318,14 +305,46 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
         }
       }
       tc::fence_before_sync();
-      tc::bar_arrive(&acc_empty[buf]);
-      tc::fence_proxy_async();
+      tc::bar_arrive(&acc_empty[buf]);  // TMEM buffer free for the MMA of a later tile
+      if (!DOWN) {
+        // phase 2: NVFP4 of h per (column, 16-row block), the activation quantiser's
+        // rule: scale e4m3(amax / 6), codes e2m1(h / scale)
+        tc::named_sync(1, kEpiThreads);
+        const uint16_t* hs = reinterpret_cast<const uint16_t*>(stg);
+        uint8_t* cs = stg + NT * BM * 2;
+        const int et = tid - kWarpEpi0 * 32;
+        for (int u = et; u < n_valid * (BM / 16); u += kEpiThreads) {
+          const int c = u / (BM / 16), b = u % (BM / 16);
+          const uint4* src = reinterpret_cast<const uint4*>(hs + (size_t)c * BM + b * 16);
+          const uint4 v0 = src[0], v1 = src[1];
+          const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          float hv[16];
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            hv[2 * i] = bf16_bits_to_float(w[i] & 0xFFFF);
+            hv[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+            amax = fmaxf(amax, fmaxf(fabsf(hv[2 * i]), fabsf(hv[2 * i + 1])));
+          }
+          const uint32_t sc = f32_to_e4m3_sat(__fdiv_rn(amax, 6.0f));
+          const float sv = e4m3_value(sc);
+          uint32_t out[2] = {0u, 0u};
+          if (sv > 0.f) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              out[i >> 2] |= f32x2_to_e2m1x2_sat(__fdiv_rn(hv[2 * i], sv), __fdiv_rn(hv[2 * i + 1], sv)) << (8 * (i & 3));
+          }
+          *reinterpret_cast<uint2*>(cs + c * (BM / 2) + b * 8) = make_uint2(out[0], out[1]);
+          a.hsf[(size_t)(pos0 + c) * (I / 16) + rt * (BM / 16) + b] = (uint8_t)sc;
+        }
+      }
+      tc::fence_proxy_async();  // staging writes -> bulk copy reads
       tc::named_sync(1, kEpiThreads);
       if (ew == 0) {
         for (int c = lane; c < n_valid; c += 32) {
           const int pos = pos0 + c;
           if (DOWN) tc::bulk_store(a.P + (size_t)pos * H + rt * BM, stg + c * BM * 4, BM * 4);
-          else tc::bulk_store(a.hq + (size_t)pos * (I / 2) + rt * (BM / 2), stg + c * (BM / 2), BM / 2);
+          else tc::bulk_store(a.hq + (size_t)pos * (I / 2) + rt * (BM / 2), stg + NT * BM * 2 + c * (BM / 2), BM / 2);
         }
         tc::bulk_commit();
         tc::bulk_wait_read();
