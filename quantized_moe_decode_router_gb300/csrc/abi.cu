@@ -30,7 +30,7 @@ struct Layout {
   size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, rb_cnt, h_amax, hs_amax, gu_part, gu_cnt,
       dn_part, dn_cnt;
   // prefill path
-  size_t xg, xsig, xnorm, wnorm, hist, pos_of, tiles, h16, hsig, xq, xsf, xqg, xsfg, hq, hsf;
+  size_t xg, xsig, xnorm, wnorm, hist, pos_of, tiles, h16, hsig, xq, xsf, xqg, xsfg, hq, hsf, rw_hi, rw_lo;
   int max_tiles;
   size_t total;
 };
@@ -84,6 +84,8 @@ Layout make_layout(const moe_layer* L, int maxT) {
   o.xsfg = take(T * k * H / 16);
   o.hq = take(T * k * I / 2);
   o.hsf = take(T * k * I / 16);
+  o.rw_hi = take(E * H * 2);
+  o.rw_lo = take(E * H * 2);
   o.total = at;
   return o;
 }
@@ -315,6 +317,9 @@ PrefillArgs prefill_args(const moe_layer* L, const Layout& lo, void* ws, const v
   a.xsfg = b + lo.xsfg;
   a.hq = b + lo.hq;
   a.hsf = b + lo.hsf;
+  a.rw_hi = reinterpret_cast<uint16_t*>(b + lo.rw_hi);
+  a.rw_lo = reinterpret_cast<uint16_t*>(b + lo.rw_lo);
+  a.logits_tc = prefill_logits_tc_ok(a) ? 1 : 0;
   return a;
 }
 

@@ -124,6 +124,10 @@ struct PrefillArgs {
   int32_t* hsig;        // [T*k]
   float* P;             // f32 [T*k, H] in sorted order (row pos)
   uint16_t* y;          // bf16 [T, H]
+  // approximate logits on tensor cores (bf16 split of the router matrix) instead of FP32 FMA
+  int logits_tc;
+  uint16_t* rw_hi;      // bf16 [E, H] = bf16(Wr)
+  uint16_t* rw_lo;      // bf16 [E, H] = bf16(Wr - hi)
   // NVFP4 W4A4 lever (act_quant = 1)
   int act_quant;
   uint8_t* xq;          // [T, H/2] E2M1 codes of x (16-element blocks)
@@ -150,6 +154,8 @@ cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s, Marks mk 
 // 5 (h conversion), 6 (down), 7 (combine).
 cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s, Marks mk = Marks{nullptr, nullptr});
 cudaError_t launch_prefill_topk(const PrefillArgs& a, cudaStream_t s);
+bool prefill_logits_tc_ok(const PrefillArgs& a);
+cudaError_t launch_prefill_logits_tc(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_gemm_nvfp4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill_gemm_w4a4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
 size_t prefill_gemm_smem(bool down);

@@ -350,7 +350,12 @@ cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s, Marks mk)
   const int wpb = kThreads / 32;
   pf_prep_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(a);
   pf_wnorm_kernel<<<(a.E + wpb - 1) / wpb, kThreads, 0, s>>>(a);
-  pf_logits_kernel<<<dim3((a.E + kLE - 1) / kLE, (a.T + kLT - 1) / kLT), kThreads, 0, s>>>(a);
+  if (a.logits_tc) {
+    cudaError_t e1 = launch_prefill_logits_tc(a, s);
+    if (e1 != cudaSuccess) return e1;
+  } else {
+    pf_logits_kernel<<<dim3((a.E + kLE - 1) / kLE, (a.T + kLT - 1) / kLT), kThreads, 0, s>>>(a);
+  }
   mk(1);
   cudaError_t err = launch_prefill_topk(a, s);
   if (err != cudaSuccess) return err;

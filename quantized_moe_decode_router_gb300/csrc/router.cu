@@ -332,7 +332,9 @@ __device__ void prefill_topk_token(const PrefillArgs& a, int t) {
       const float d = row[e];
       const float b = a.bias ? __ldg(a.bias + e) : 0.f;
       const float ab = __fadd_rn(d, b);
-      const float eps0 = gam * xn * a.wnorm[e] * 1.00390625f;
+      // tensor-core logits: twice the FMA-chain bound plus the bf16 split residual
+      const float g_e = a.logits_tc ? 2.f * gam + 7.62939453125e-06f : gam;
+      const float eps0 = g_e * xn * a.wnorm[e] * 1.00390625f;
       const float eps = eps0 + 4.7683716e-7f * (fabsf(d) + fabsf(b) + eps0) + 1e-30f;
       av[q] = ab;
       ev[q] = eps;
@@ -369,6 +371,7 @@ __device__ void prefill_topk_token(const PrefillArgs& a, int t) {
       const float4* wrow = reinterpret_cast<const float4*>(a.rw + (size_t)e * H);
       const uint2* xp = reinterpret_cast<const uint2*>(a.x + (size_t)t * H);
       float hi = 0.f, lo = 0.f;
+#pragma unroll 4
       for (int c = lane; c < H / 4; c += 32) {
         const float4 wv = __ldg(wrow + c);
         const uint2 xv = __ldg(xp + c);
@@ -400,7 +403,7 @@ __device__ void prefill_topk_token(const PrefillArgs& a, int t) {
   topk_warp<NQ>(row, E, k, io, wo, io2, wo2);
 }
 
-__global__ void __launch_bounds__(kRouterThreads) prefill_topk_kernel(PrefillArgs a) {
+__global__ void __launch_bounds__(kRouterThreads, 1) prefill_topk_kernel(PrefillArgs a) {
   const int t = blockIdx.x * kWarpsR + (threadIdx.x >> 5);
   if (t >= a.T) return;
   if (a.E <= 256) prefill_topk_token<8>(a, t);
