@@ -26,7 +26,8 @@ struct Ctrl {
   uint32_t router_arrive;  // CTAs of the router kernel that finished their logits
   int32_t n_active;        // experts with at least one routed pair
   int32_t n_tiles;         // prefill: token tiles in the GEMM tile list
-  uint32_t pad[3];
+  uint32_t gu_next;        // decode gate/up: next task to hand out (zeroed by the router)
+  uint32_t pad[2];
 };
 
 __device__ __forceinline__ void report_error(Ctrl* ctrl, uint32_t code, uint32_t info) {

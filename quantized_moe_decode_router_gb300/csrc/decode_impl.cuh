@@ -573,12 +573,20 @@ __global__ void __launch_bounds__(kExpertThreads, 2) gateup_kernel(ExpertArgs a)
   const int Kw = H / S;
   const int Br = dec_blocks(FR, H), bur = dec_block_units(FR, H);
   const int Bs = FS ? dec_blocks(FS, H) : 1, bus = FS ? dec_block_units(FS, H) : 1;
-  const int gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
   const int r = lane >> 2, c = lane & 3;
-
-  for (int q = gw; q < n_tasks; q += nw) {
-    const int tile_id = q / S, slice = q - tile_id * S;
-    const bool shared_item = tile_id >= n_active * tpe;
+  // every warp starts on task (its global warp id); later tasks are handed out
+  // one at a time from a global counter, so warps that finish early take more.
+  // The shared expert's (costlier) tasks come first.
+  const int n_shared_tasks = stiles * S;
+  const int nw = gridDim.x * kWarps;
+  uint32_t* next = &a.rb.ctrl->gu_next;
+  int qn = 0;
+  for (int q = blockIdx.x * kWarps + warp; q < n_tasks; q = __shfl_sync(0xFFFFFFFFu, qn, 0)) {
+    if (lane == 0) qn = nw + (int)atomicAdd(next, 1u);  // the next task, fetched while this one runs
+    const bool shared_item = q < n_shared_tasks;
+    const int qq = shared_item ? q : q - n_shared_tasks;
+    const int tile_id = shared_item ? n_active * tpe + qq / S : qq / S;
+    const int slice = qq % S;
     int e = 0, tile, ncols, col_tok = T, col_pair[2] = {-1, -1}, col_tokc[2] = {T, T};
     if (!shared_item) {
       const int slot = tile_id / tpe;
@@ -668,21 +676,33 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
   const int tpe = H / 16;
   const int S = a.dn_slices;
   const int Br = dec_blocks(FR, I), Bs = FS ? dec_blocks(FS, a.Is) : 1;
-  const int n_seg = n_active + (FS ? 1 : 0);      // expert segments, shared last
+  const int sh = FS ? 1 : 0;
+  const int n_seg = n_active + sh;                 // expert segments, the shared one first
   const int tasks_per_seg = tpe * S;
   const int n_tasks = n_seg * tasks_per_seg;
   const int needed = n_seg;
-  // contiguous task range per CTA; segments inside it are staged one at a time
-  const int q0 = (int)((long long)blockIdx.x * n_tasks / gridDim.x);
-  const int q1 = (int)((long long)(blockIdx.x + 1) * n_tasks / gridDim.x);
+  // contiguous task range per CTA, split by weight bytes (a shared-expert task
+  // can cost more than a routed one); segments are staged one at a time
+  const long long cr = (long long)(data_bytes(FR, H, I) + scale_bytes(FR, H, I)) / tasks_per_seg;
+  const long long cs = FS ? (long long)(data_bytes(FS, H, a.Is) + scale_bytes(FS, H, a.Is)) / tasks_per_seg : 0;
+  const long long ns = (long long)sh * tasks_per_seg;
+  const long long total = ns * cs + (long long)n_active * tasks_per_seg * cr;
+  auto task_at = [&](long long cost) -> int {
+    if (cost <= 0) return 0;
+    if (cost >= total) return n_tasks;
+    if (cost < ns * cs) return (int)((cost + cs - 1) / cs);
+    return (int)(ns + (cost - ns * cs + cr - 1) / cr);
+  };
+  const int q0 = task_at(total * blockIdx.x / gridDim.x);
+  const int q1 = task_at(total * (blockIdx.x + 1) / gridDim.x);
   const int r = lane >> 2, c = lane & 3;
 
   for (int seg = q0 / tasks_per_seg; seg * tasks_per_seg < q1; ++seg) {
-    const bool shared_item = seg >= n_active;
+    const bool shared_item = FS && seg == 0;
     int e = 0, ncols;
     __syncthreads();
     if (!shared_item) {
-      e = a.rb.act[seg];
+      e = a.rb.act[seg - sh];
       ncols = a.rb.cnt[e];
       if (tid < kMaxT) {
         if (tid < ncols) {
@@ -719,7 +739,7 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
       const int local = q - seg * tasks_per_seg;
       const int tile = local / S, slice = local - tile * S;
       float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-      const int tile_id = seg * tpe + tile;
+      const int tile_id = shared_item ? n_active * tpe + tile : (seg - sh) * tpe + tile;
       float* tile_part = a.dn_part + (shared_item ? (size_t)n_active * tpe * Br + (size_t)tile * Bs
                                                   : (size_t)tile_id * Br) * (32 * 4);
       float* bpart = S > 1 ? tile_part + (size_t)slice * (B / S) * (32 * 4) : nullptr;

@@ -101,7 +101,7 @@ __device__ void topk_warp(const float* __restrict__ logits_row, int E, int k, in
   uint32_t bk;
   int bq;
   lane_best<NQ>(key, bk, bq);
-  float sel_v0 = 0.f, sum = 0.f, my_ex = 0.f;
+  uint32_t my_key = 0u, key0 = 0u;
   int my_i = 0;
   for (int j = 0; j < k; ++j) {
     const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
@@ -112,13 +112,15 @@ __device__ void topk_warp(const float* __restrict__ logits_row, int E, int k, in
         if (q == bq) key[q] = 0u;
       lane_best<NQ>(key, bk, bq);
     }
-    const float bv = ord_value(m);
-    if (j == 0) sel_v0 = bv;
-    // w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0); the sum runs in j order
-    const float ex = expf(bv - sel_v0);
-    sum += ex;
-    if (lane == j) { my_ex = ex; my_i = (int)id; }
+    if (j == 0) key0 = m;
+    if (lane == j) { my_key = m; my_i = (int)id; }
   }
+  // w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0); lane j holds term j, the sum
+  // is a fixed butterfly over the warp (lanes >= k contribute 0)
+  const float my_ex = lane < k ? expf(ord_value(my_key) - ord_value(key0)) : 0.f;
+  float sum = my_ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
   if (lane < k) {
     const float w = my_ex / sum;
     idx_out[lane] = my_i;
@@ -129,7 +131,11 @@ __device__ void topk_warp(const float* __restrict__ logits_row, int E, int k, in
 }
 
 // Logits of this CTA's expert rows; returns after writing them to global memory.
-__device__ void router_logits_cta(const RouterArgs& a, float (*s_hi)[kMaxT], float (*s_lo)[kMaxT]) {
+// The tokens are staged once per CTA in shared memory (x_s, [T][H] bf16) and
+// every lane holds its router-weight chunk in registers before the
+// float-float loop, so the loop itself issues no global loads.
+__device__ void router_logits_cta(const RouterArgs& a, const uint16_t* x_s, float (*s_hi)[kMaxT],
+                                  float (*s_lo)[kMaxT]) {
   const int H = a.H, E = a.E, T = a.T, wpr = a.wpr;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rows_per_cta = kWarpsR / wpr;
@@ -141,18 +147,27 @@ __device__ void router_logits_cta(const RouterArgs& a, float (*s_hi)[kMaxT], flo
   for (int t = 0; t < kMaxT; ++t) { hi[t] = 0.f; lo[t] = 0.f; }
   if (e < E) {
     const float4* wrow = reinterpret_cast<const float4*>(a.w + (size_t)e * H + (size_t)part * Hw);
-    const uint16_t* xp = a.x + (size_t)part * Hw;  // the tokens are small and stay in L1/L2
-#pragma unroll 2
-    for (int h4 = lane; h4 < Hw / 4; h4 += 32) {
-      const float4 wv = __ldg(wrow + h4);
+    const uint16_t* xp = x_s + (size_t)part * Hw;
+    constexpr int kPre = 4;  // float4 chunks of the row held per lane at once
+    for (int base = lane; base < Hw / 4; base += 32 * kPre) {
+      float4 wv[kPre];
 #pragma unroll
-      for (int t = 0; t < kMaxT; ++t) {
-        if (t < T) {
-          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(xp + (size_t)t * H + h4 * 4));
-          dot2_step(bf16_bits_to_float(xv.x & 0xFFFF), wv.x, hi[t], lo[t]);
-          dot2_step(bf16_bits_to_float(xv.x >> 16), wv.y, hi[t], lo[t]);
-          dot2_step(bf16_bits_to_float(xv.y & 0xFFFF), wv.z, hi[t], lo[t]);
-          dot2_step(bf16_bits_to_float(xv.y >> 16), wv.w, hi[t], lo[t]);
+      for (int j = 0; j < kPre; ++j)
+        if (base + 32 * j < Hw / 4) wv[j] = __ldg(wrow + base + 32 * j);
+#pragma unroll
+      for (int j = 0; j < kPre; ++j) {
+        const int h4 = base + 32 * j;
+        if (h4 < Hw / 4) {
+#pragma unroll
+          for (int t = 0; t < kMaxT; ++t) {
+            if (t < T) {
+              const uint2 xv = *reinterpret_cast<const uint2*>(xp + (size_t)t * H + h4 * 4);
+              dot2_step(bf16_bits_to_float(xv.x & 0xFFFF), wv[j].x, hi[t], lo[t]);
+              dot2_step(bf16_bits_to_float(xv.x >> 16), wv[j].y, hi[t], lo[t]);
+              dot2_step(bf16_bits_to_float(xv.y & 0xFFFF), wv[j].z, hi[t], lo[t]);
+              dot2_step(bf16_bits_to_float(xv.y >> 16), wv[j].w, hi[t], lo[t]);
+            }
+          }
         }
       }
     }
@@ -192,7 +207,14 @@ __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArg
   // the expert kernel that follows may be scheduled now: it stages the
   // activations and then waits for this grid's results (griddepcontrol.wait)
   asm volatile("griddepcontrol.launch_dependents;");
-  router_logits_cta(a, s_hi, s_lo);
+  {
+    // stage the tokens (bf16 [T][H]) in shared memory
+    const uint4* xs = reinterpret_cast<const uint4*>(a.x);
+    uint4* xd = reinterpret_cast<uint4*>(smem);
+    for (int i = tid; i < T * H / 8; i += blockDim.x) xd[i] = __ldg(xs + i);
+  }
+  __syncthreads();
+  router_logits_cta(a, reinterpret_cast<const uint16_t*>(smem), s_hi, s_lo);
 
   // ---- last CTA: top-k and dispatch ----
   __syncthreads();
@@ -300,7 +322,10 @@ __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArg
       __syncwarp();
     }
   }
-  if (tid == 0) a.rb.ctrl->router_arrive = 0;  // leave the counter at zero for the next call
+  if (tid == 0) {
+    a.rb.ctrl->router_arrive = 0;  // leave the counter at zero for the next call
+    a.rb.ctrl->gu_next = 0;        // task counter of the gate/up kernel that follows
+  }
 }
 
 // ---------------------------------------------------------------- prefill --
@@ -427,7 +452,9 @@ int router_warps_per_row(int H, int E, int sms) {
 cudaError_t launch_router_decode(const RouterArgs& a, cudaStream_t s) {
   const int rows_per_cta = kWarpsR / a.wpr;
   const int grid = (a.E + rows_per_cta - 1) / rows_per_cta;
-  const size_t smem = (size_t)(2 * a.E + 1 + a.T * a.k) * 4;
+  // dispatch scratch of the last CTA, or the staged tokens before it (aliased)
+  const size_t disp = (size_t)(2 * a.E + 1 + a.T * a.k) * 4, xbytes = (size_t)a.T * a.H * 2;
+  const size_t smem = disp > xbytes ? disp : xbytes;
   cudaError_t err = cudaFuncSetAttribute(router_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;
