@@ -134,6 +134,19 @@ def _dist():
     return ws, rank, local
 
 
+def aggregate_ranks(ms: float, work: float, dist=None, device: str = "cpu"):
+    """Whole-job timing over replicas: the slowest rank's time and the sum of every rank's work
+    (a single process returns its own numbers)."""
+    if dist is None:
+        return ms, work
+    import torch
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    w = torch.tensor([work], device=device, dtype=torch.float64)
+    dist.all_reduce(w)
+    return float(t.item()), float(w.item())
+
+
 def _bytes_per_call(host, cnt_rows):
     """Algorithmic weight bytes of one call from its per-expert pair counts."""
     per_expert = host.expert_bytes()
@@ -242,15 +255,7 @@ def run_ours(args, world, rank, local):
         ms = ev0.elapsed_time(ev1)
         if sampler:
             clocks = sampler.stop()
-        if dist:
-            t = torch.tensor([ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-            tb = torch.tensor([float(bytes_graph * reps)], device="cuda", dtype=torch.float64)
-            dist.all_reduce(tb)
-            total_bytes = float(tb.item())
-        else:
-            total_bytes = float(bytes_graph * reps)
+        ms, total_bytes = aggregate_ranks(ms, float(bytes_graph * reps), dist, "cuda")
         us_call = ms * 1e3 / steps
         gbs = total_bytes / (ms * 1e-3) / 1e9
         toks = world * T * steps / (ms * 1e-3)
