@@ -262,8 +262,9 @@ def run_ours(args, world, rank, local):
         results[T] = {"us_per_layer": round(us_call, 3), "weight_GBps": round(gbs, 1),
                       "tokens_per_s": round(toks, 1), "hbm_frac": round(gbs / world / peak, 4),
                       "bytes_per_layer": int(np.mean(bytes_b)), "steps": steps}
-        # dominant kernel (gate/up): live CUDA-event timing of each kernel on the launch stream
-        if headline:
+        # per-kernel live CUDA-event timing on the launch stream (every batch size; the
+        # headline batch also gives the roofline of the dominant kernel, gate/up)
+        if True:
             n = min(256, max(32, steps // 8))
             evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
             for row in evs:          # create the CUDA events (torch creates them lazily on first record)
@@ -283,6 +284,8 @@ def run_ours(args, world, rank, local):
             s_gu = (host.shared_gate.nbytes() + host.shared_up.nbytes()) if host.shared_gate else 0
             gu_bytes = np.mean([int(np.count_nonzero(cnts[i % NB])) * per_exp_gu + s_gu for i in range(n)])
             ach = gu_bytes / (avg[1] * 1e-6) / 1e9
+            results[T]["kernel_us"] = {"router": round(avg[0], 3), "gateup": round(avg[1], 3), "down": round(avg[2], 3)}
+        if headline:
             roof = {"kernel": "gateup_decode_kernel", "bound": "hbm", "achieved": round(ach, 1),
                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(ach / peak, 4),
                     "traffic": None, "bytes_per_launch": int(gu_bytes),

@@ -270,8 +270,14 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
 
   const size_t warps_cta = kExpertThreads / 32;
   const size_t smem_gu = (size_t)(T + 1) * ea.xs_tok_stride * 2 + warps_cta * kStagesGU * dec_stage_bytes(2);
-  const size_t smem_dn =
-      (size_t)(MOE_DECODE_MAX_TOKENS + 1) * ea.hs_tok_stride * 2 + warps_cta * kStagesDN * dec_stage_bytes(1);
+  // the down kernel stages up to kMaxDnSegs expert segments of h at once, as
+  // many as keep two CTAs per SM
+  const size_t seg_bytes = (size_t)(MOE_DECODE_MAX_TOKENS + 1) * ea.hs_tok_stride * 2;
+  const size_t rings_dn = warps_cta * kStagesDN * dec_stage_bytes(1);
+  const size_t half_sm = 113 * 1024;
+  int segs = half_sm > rings_dn ? (int)((half_sm - rings_dn) / seg_bytes) : 1;
+  ea.dn_segs = segs < 1 ? 1 : (segs > kMaxDnSegs ? kMaxDnSegs : segs);
+  const size_t smem_dn = (size_t)ea.dn_segs * seg_bytes + rings_dn;
   if (smem_gu > 227 * 1024 || smem_dn > 227 * 1024) return MOE_ERR_UNSUPPORTED;
 
   mark(0);
@@ -282,6 +288,8 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   mark(2);
   err = launch_expert(L->fmt, L->shared_fmt, true, ea, smem_dn, stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  err = launch_combine_decode(ea, stream);
   mark(3);
   return cuda_status(err);
 }

@@ -2,7 +2,7 @@
 // exposed for bit-exact checking) and the NVFP4 activation quantizer of the
 // W4A4 lever (DGPP forum, weekly update on page 5: NVFP4 W4A4 prefill is
 // opt-in).
-#include "kernels.cuh"
+#include "decode_impl.cuh"
 
 namespace qmoe {
 
@@ -115,6 +115,21 @@ cudaError_t launch_quantize_act_nvfp4(const uint16_t* x, int rows, int K, uint8_
   const long long blocks = (n + threads - 1) / threads;
   quantize_act_nvfp4_kernel<<<(unsigned)blocks, threads, 0, s>>>(x, rows, K, codes, scales);
   return cudaGetLastError();
+}
+
+cudaError_t launch_combine_decode(const ExpertArgs& a, cudaStream_t s) {
+  const int n = a.T * (a.H / 4);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n + 255) / 256);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return a.sfmt ? cudaLaunchKernelEx(&cfg, dec::combine_kernel<1>, a) : cudaLaunchKernelEx(&cfg, dec::combine_kernel<0>, a);
 }
 
 }  // namespace qmoe

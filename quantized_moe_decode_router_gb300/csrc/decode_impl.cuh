@@ -663,10 +663,13 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
   const int T = a.T, H = a.H, I = a.I, k = a.k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int hs_stride = a.hs_tok_stride;
-  __half* hsm = reinterpret_cast<__half*>(smem);  // [kMaxT + 1][hs_stride]
-  uint8_t* ring = smem + (size_t)(kMaxT + 1) * hs_stride * 2 + (size_t)warp * kStagesDN * stage_bytes<1>();
-  __shared__ int s_pexp[kMaxT + 1];
-  __shared__ int s_col_out[kMaxT];
+  const int SG = a.dn_segs;  // segments staged at once
+  const size_t seg_halfs = (size_t)(kMaxT + 1) * hs_stride;
+  __half* hsm = reinterpret_cast<__half*>(smem);  // [SG][kMaxT + 1][hs_stride]
+  uint8_t* ring = smem + (size_t)SG * seg_halfs * 2 + (size_t)warp * kStagesDN * stage_bytes<1>();
+  __shared__ int s_pexp[kMaxDnSegs][kMaxT + 1];
+  __shared__ int s_col_out[kMaxDnSegs][kMaxT];
+  __shared__ int s_ncols[kMaxDnSegs];
   __shared__ const uint16_t* s_src[kMaxT];
   __shared__ uint32_t s_amax[kMaxT];
 
@@ -680,9 +683,8 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
   const int n_seg = n_active + sh;                 // expert segments, the shared one first
   const int tasks_per_seg = tpe * S;
   const int n_tasks = n_seg * tasks_per_seg;
-  const int needed = n_seg;
   // contiguous task range per CTA, split by weight bytes (a shared-expert task
-  // can cost more than a routed one); segments are staged one at a time
+  // can cost more than a routed one)
   const long long cr = (long long)(data_bytes(FR, H, I) + scale_bytes(FR, H, I)) / tasks_per_seg;
   const long long cs = FS ? (long long)(data_bytes(FS, H, a.Is) + scale_bytes(FS, H, a.Is)) / tasks_per_seg : 0;
   const long long ns = (long long)sh * tasks_per_seg;
@@ -696,46 +698,60 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
   const int q0 = task_at(total * blockIdx.x / gridDim.x);
   const int q1 = task_at(total * (blockIdx.x + 1) / gridDim.x);
   const int r = lane >> 2, c = lane & 3;
+  if (q0 >= q1) return;
 
-  for (int seg = q0 / tasks_per_seg; seg * tasks_per_seg < q1; ++seg) {
-    const bool shared_item = FS && seg == 0;
-    int e = 0, ncols;
-    __syncthreads();
-    if (!shared_item) {
-      e = a.rb.act[seg - sh];
-      ncols = a.rb.cnt[e];
-      if (tid < kMaxT) {
-        if (tid < ncols) {
-          const int p = a.rb.pair[a.rb.off[e] + tid];
-          s_src[tid] = a.h + (size_t)p * I;
-          s_col_out[tid] = p;
-          s_amax[tid] = __ldcg(a.h_amax + p);
-        } else {
-          s_col_out[tid] = -1;
+  // the segments of [q0, q1), staged SG at a time; inside a group the warps
+  // take the tasks in turn with no barrier between segments
+  const int seg_lo = q0 / tasks_per_seg, seg_hi = (q1 - 1) / tasks_per_seg;
+  for (int sg = seg_lo; sg <= seg_hi; sg += SG) {
+    const int sg_end = min(seg_hi + 1, sg + SG);
+    __syncthreads();  // the previous group's rows are no longer read
+    for (int seg = sg; seg < sg_end; ++seg) {
+      const int i = seg - sg;
+      const bool shared_item = FS && seg == 0;
+      int ncols;
+      if (!shared_item) {
+        const int e = a.rb.act[seg - sh];
+        ncols = a.rb.cnt[e];
+        if (tid < kMaxT) {
+          if (tid < ncols) {
+            const int p = a.rb.pair[a.rb.off[e] + tid];
+            s_src[tid] = a.h + (size_t)p * I;
+            s_col_out[i][tid] = p;
+            s_amax[tid] = __ldcg(a.h_amax + p);
+          } else {
+            s_col_out[i][tid] = -1;
+          }
+        }
+      } else {
+        ncols = T;
+        if (tid < kMaxT) {
+          if (tid < T) {
+            s_src[tid] = a.hs + (size_t)tid * a.Is;
+            s_amax[tid] = __ldcg(a.hs_amax + tid);
+          }
+          s_col_out[i][tid] = tid < T ? tid : -1;
         }
       }
-    } else {
-      ncols = T;
-      if (tid < kMaxT) {
-        if (tid < T) {
-          s_src[tid] = a.hs + (size_t)tid * a.Is;
-          s_amax[tid] = __ldcg(a.hs_amax + tid);
-        }
-        s_col_out[tid] = tid < T ? tid : -1;
-      }
+      if (tid == 0) s_ncols[i] = ncols;
+      __syncthreads();
+      stage_rows_f16(s_src, s_amax, ncols, shared_item ? a.Is : I, hsm + (size_t)i * seg_halfs, hs_stride,
+                     s_pexp[i]);
+      __syncthreads();  // s_src / s_amax are reused by the next segment
     }
-    __syncthreads();
-    const int K = shared_item ? a.Is : I;
-    stage_rows_f16(s_src, s_amax, ncols, K, hsm, hs_stride, s_pexp);
-    __syncthreads();
-    const int fmt = shared_item ? FS : FR;
-    const QW& qd = shared_item ? a.sdown : a.down;
-    const Mat m[1] = {mat_of(qd, fmt, e, H, K)};
-    const int Kw = K / S;
-    const int B = dec_blocks(fmt, K), bu = dec_block_units(fmt, K);
-    const int t_lo = max(q0, seg * tasks_per_seg), t_hi = min(q1, (seg + 1) * tasks_per_seg);
-    const __half* xrow = hsm + (size_t)(r < ncols ? r : ncols) * hs_stride;
+    const int t_lo = max(q0, sg * tasks_per_seg), t_hi = min(q1, sg_end * tasks_per_seg);
     for (int q = t_lo + warp; q < t_hi; q += kWarps) {
+      const int seg = q / tasks_per_seg, i = seg - sg;
+      const bool shared_item = FS && seg == 0;
+      const int e = shared_item ? 0 : a.rb.act[seg - sh];
+      const int ncols = s_ncols[i];
+      const int K = shared_item ? a.Is : I;
+      const int fmt = shared_item ? FS : FR;
+      const QW& qd = shared_item ? a.sdown : a.down;
+      const Mat m[1] = {mat_of(qd, fmt, e, H, K)};
+      const int Kw = K / S;
+      const int B = dec_blocks(fmt, K), bu = dec_block_units(fmt, K);
+      const __half* xrow = hsm + (size_t)i * seg_halfs + (size_t)(r < ncols ? r : ncols) * hs_stride;
       const int local = q - seg * tasks_per_seg;
       const int tile = local / S, slice = local - tile * S;
       float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
@@ -754,34 +770,46 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
       for (int j = 0; j < 4; ++j) {
         const int col = 2 * c + (j & 1);
         const int row = tile * 16 + r + ((j & 2) ? 8 : 0);
-        const int out = s_col_out[col];
+        const int out = s_col_out[i][col];
         if (out >= 0) {
-          const float val = acc[0][j] * exp2i(s_pexp[col]) * ts;
+          const float val = acc[0][j] * exp2i(s_pexp[i][col]) * ts;
           if (shared_item) a.S[(size_t)out * H + row] = val;
           else a.P[(size_t)out * H + row] = val;
         }
       }
-      // this expert's contribution to the 16-row block is complete; the last
-      // of the n_seg contributions combines the block in fixed order
-      __threadfence();
-      __syncwarp();
-      uint32_t prev = 0;
-      if (lane == 0) prev = atomicAdd(&a.rb_cnt[tile], 1u);
-      prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
-      if (prev == (uint32_t)needed - 1) {
-        __threadfence();
-        for (int qq = lane; qq < T * 16; qq += 32) {
-          const int t = qq >> 4, row = tile * 16 + (qq & 15);
-          float y = 0.f;
-          for (int j = 0; j < k; ++j)
-            y = __fmaf_rn(__ldcg(a.rb.topk_w + t * k + j), __ldcg(a.P + (size_t)(t * k + j) * H + row), y);
-          if (FS) y = __fadd_rn(y, __ldcg(a.S + (size_t)t * H + row));
-          a.y[(size_t)t * H + row] = float_to_bf16_bits(y);
-        }
-        if (lane == 0) a.rb_cnt[tile] = 0;
-      }
     }
   }
+}
+
+// y[t] = bf16( sum_j w[t, j] * P[t*k + j] (+ S[t]) ), j ascending, after the
+// down kernel (programmatic dependent launch; waits for its completion).
+template <int FS>
+__global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int H = a.H, k = a.k;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // (token, 4 columns)
+  if (i >= a.T * (H / 4)) return;
+  const int t = i / (H / 4), c4 = i - t * (H / 4);
+  float y[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < k; ++j) {
+    const float w = __ldcg(a.rb.topk_w + t * k + j);
+    const float4 p = __ldcg(reinterpret_cast<const float4*>(a.P + (size_t)(t * k + j) * H) + c4);
+    y[0] = __fmaf_rn(w, p.x, y[0]);
+    y[1] = __fmaf_rn(w, p.y, y[1]);
+    y[2] = __fmaf_rn(w, p.z, y[2]);
+    y[3] = __fmaf_rn(w, p.w, y[3]);
+  }
+  if (FS) {
+    const float4 sv = __ldcg(reinterpret_cast<const float4*>(a.S + (size_t)t * H) + c4);
+    y[0] = __fadd_rn(y[0], sv.x);
+    y[1] = __fadd_rn(y[1], sv.y);
+    y[2] = __fadd_rn(y[2], sv.z);
+    y[3] = __fadd_rn(y[3], sv.w);
+  }
+  const uint32_t lo = (uint32_t)float_to_bf16_bits(y[0]) | ((uint32_t)float_to_bf16_bits(y[1]) << 16);
+  const uint32_t hi = (uint32_t)float_to_bf16_bits(y[2]) | ((uint32_t)float_to_bf16_bits(y[3]) << 16);
+  reinterpret_cast<uint2*>(a.y + (size_t)t * H)[c4] = make_uint2(lo, hi);
 }
 
 template <int FR, int FS>

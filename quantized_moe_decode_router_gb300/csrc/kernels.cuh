@@ -67,7 +67,10 @@ struct ExpertArgs {
   uint32_t* dn_cnt;   // [tiles]
   int xs_tok_stride;  // halfs per staged token row (gate/up)
   int hs_tok_stride;  // halfs per staged hidden row (down)
+  int dn_segs;        // expert segments the down kernel stages at once (1 .. kMaxDnSegs)
 };
+
+constexpr int kMaxDnSegs = 4;
 
 constexpr int kExpertThreads = 256;  // 8 warps
 constexpr int kStagesGU = 3;         // cp.async ring stages per warp, gate/up (two matrices per unit)
@@ -159,6 +162,10 @@ cudaError_t launch_prefill_logits_tc(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_gemm_nvfp4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill_gemm_w4a4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
 size_t prefill_gemm_smem(bool down);
+
+// Decode combine y = bf16(sum_j w_j P_j (+ S)), launched after the down
+// kernel as a programmatic dependent of it.
+cudaError_t launch_combine_decode(const ExpertArgs& a, cudaStream_t s);
 
 // moe_dequantize / moe_quantize_act_nvfp4
 cudaError_t launch_dequantize(int fmt, QW w, int N, int K, int expert, int row0, int nrows, float* out,
