@@ -264,9 +264,26 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   const long act = (long)T * L->top_k < L->n_experts ? (long)T * L->top_k : L->n_experts;
   ea.gu_slices = choose_slices(H, L->fmt, act * (I / 16), H, L->shared_fmt, Is / 16, warps);
   ea.dn_slices = choose_slices(I, L->fmt, act * (H / 16), Is, L->shared_fmt, Is ? H / 16 : 0, warps);
-  ea.xs_tok_stride = H + 16;
+  // shared-expert tiles of gate/up: split K until a task carries no more bytes
+  // than a routed one (both formats' blocks permitting), so no task outlasts the rest
+  {
+    const int Sr = ea.gu_slices;
+    ea.gu_slices_s = Sr;
+    if (L->shared_fmt) {
+      const double br = (double)(data_bytes(L->fmt, I, H) + scale_bytes(L->fmt, I, H)) / I / Sr;
+      const double bs = (double)(data_bytes(L->shared_fmt, Is, H) + scale_bytes(L->shared_fmt, Is, H)) / Is;
+      const int Bs = dec_blocks(L->shared_fmt, H);
+      int Ss = 1;
+      while (bs / Ss > 1.15 * br && Bs % (2 * Ss) == 0) Ss *= 2;
+      const long blocks = (Sr > 1 ? act * (I / 16) * (long)dec_blocks(L->fmt, H) : 0) + (long)(Is / 16) * Bs;
+      ea.gu_slices_s = blocks <= kMaxSplitBlocks ? Ss : 1;
+    }
+  }
+  // token rows staged with a stride of 16 banks: the MMA operand loads of two
+  // rows in one quarter warp fall on disjoint banks
+  ea.xs_tok_stride = H + 32;
   const int Kmax = Is > I ? Is : I;
-  ea.hs_tok_stride = Kmax + 16;
+  ea.hs_tok_stride = Kmax + 32;
 
   const size_t warps_cta = kExpertThreads / 32;
   const size_t smem_gu = (size_t)(T + 1) * ea.xs_tok_stride * 2 + warps_cta * kStagesGU * dec_stage_bytes(2);

@@ -568,25 +568,26 @@ __global__ void __launch_bounds__(kExpertThreads, 2) gateup_kernel(ExpertArgs a)
   const int tpe = I / 16;
   const int stiles = FS ? a.Is / 16 : 0;
   const int n_tiles = n_active * tpe + stiles;
-  const int S = a.gu_slices;
-  const int n_tasks = n_tiles * S;
-  const int Kw = H / S;
+  const int S = a.gu_slices, Ss = FS ? a.gu_slices_s : 1;
+  const int n_tasks = (n_tiles - stiles) * S + stiles * Ss;
   const int Br = dec_blocks(FR, H), bur = dec_block_units(FR, H);
   const int Bs = FS ? dec_blocks(FS, H) : 1, bus = FS ? dec_block_units(FS, H) : 1;
   const int r = lane >> 2, c = lane & 3;
   // every warp starts on task (its global warp id); later tasks are handed out
   // one at a time from a global counter, so warps that finish early take more.
   // The shared expert's (costlier) tasks come first.
-  const int n_shared_tasks = stiles * S;
+  const int n_shared_tasks = stiles * Ss;
   const int nw = gridDim.x * kWarps;
   uint32_t* next = &a.rb.ctrl->gu_next;
   int qn = 0;
   for (int q = blockIdx.x * kWarps + warp; q < n_tasks; q = __shfl_sync(0xFFFFFFFFu, qn, 0)) {
     if (lane == 0) qn = nw + (int)atomicAdd(next, 1u);  // the next task, fetched while this one runs
     const bool shared_item = q < n_shared_tasks;
+    const int Si = shared_item ? Ss : S;  // K slices of this tile
     const int qq = shared_item ? q : q - n_shared_tasks;
-    const int tile_id = shared_item ? n_active * tpe + qq / S : qq / S;
-    const int slice = qq % S;
+    const int tile_id = shared_item ? n_active * tpe + qq / Si : qq / Si;
+    const int slice = qq % Si;
+    const int Kw = H / Si;
     int e = 0, tile, ncols, col_tok = T, col_pair[2] = {-1, -1}, col_tokc[2] = {T, T};
     if (!shared_item) {
       const int slot = tile_id / tpe;
@@ -620,12 +621,13 @@ __global__ void __launch_bounds__(kExpertThreads, 2) gateup_kernel(ExpertArgs a)
     const Mat m[2] = {mat_of(qg, fmt, e, N, H), mat_of(qu, fmt, e, N, H)};
     const int row0 = tile * 16;
     const int B = shared_item ? Bs : Br;
-    float* tile_part = a.gu_part + (shared_item ? (size_t)n_active * tpe * Br + (size_t)tile * Bs
+    // block sums of split tiles: routed tiles first (only when they are split), then shared ones
+    float* tile_part = a.gu_part + (shared_item ? (size_t)(S > 1 ? n_active * tpe * Br : 0) + (size_t)tile * Bs
                                                 : (size_t)tile_id * Br) * (32 * 8);
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     gu_tile<FR, FS>(shared_item, m, row0, slice * Kw, Kw, shared_item ? bus : bur, xs + (size_t)col_tok * xs_stride,
-                    acc, S > 1 ? tile_part + (size_t)slice * (B / S) * (32 * 8) : nullptr, ring);
-    if (!block_reduce<2>(acc, tile_part, a.gu_cnt + tile_id, S, B)) continue;
+                    acc, Si > 1 ? tile_part + (size_t)slice * (B / Si) * (32 * 8) : nullptr, ring);
+    if (!block_reduce<2>(acc, tile_part, a.gu_cnt + tile_id, Si, B)) continue;
     const float tsg = (fmt == MOE_FMT_NVFP4) ? __ldg(qg.ts + e) : 1.f;
     const float tsu = (fmt == MOE_FMT_NVFP4) ? __ldg(qu.ts + e) : 1.f;
     uint32_t amax[2] = {0u, 0u};

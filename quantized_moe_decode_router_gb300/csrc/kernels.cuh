@@ -61,6 +61,7 @@ struct ExpertArgs {
   uint32_t* rb_cnt;   // [H / 16] arrival counters of the combine
   uint16_t* y;        // bf16 [T, H]
   int gu_slices, dn_slices;  // K slices per 16-row tile (1 = no split)
+  int gu_slices_s;           // K slices per shared-expert tile of the gate/up kernel
   float* gu_part;     // block sums of split tiles, [tile blocks][32 lanes][8]
   uint32_t* gu_cnt;   // [tiles] slice arrival counters
   float* dn_part;     // [tile blocks][32 lanes][4]
