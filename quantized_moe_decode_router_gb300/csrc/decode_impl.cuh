@@ -421,6 +421,64 @@ __device__ __forceinline__ void warp_tile(const Mat (&m)[NM], int row0, int kb, 
   cp_async_wait<0>();
 }
 
+// ntile tiles of one matrix set, rows row0 + t * row_step (t < ntile), each
+// over the whole K range [0, Kw) with no split: one continuous cp.async
+// stream, so the next tile's first units are in flight while this tile
+// finishes.  Every block is summed from zero and added in block order, as in
+// warp_tile; epi(t, acc) runs when tile t is complete.
+template <int F, int NM, int PF, class Epi>
+__device__ __forceinline__ void warp_tiles(const Mat (&m)[NM], int row0, int row_step, int ntile, int Kw, int bu,
+                                           const __half* xrow, uint8_t* ring, Epi epi) {
+  constexpr int UK = unit_k<F>(), CK = chunk_k<F>(), SB = stage_bytes<NM>();
+  const int lane = threadIdx.x & 31;
+  const int R = lane >> 2;
+  const int koff = (lane & 3) * CK;
+  const int nU = Kw / UK;
+  const int total = ntile * nU;
+  float blk[NM][4], acc[NM][4];
+#pragma unroll
+  for (int i = 0; i < NM; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) { blk[i][j] = 0.f; acc[i][j] = 0.f; }
+  auto issue = [&](int g, int slot) {
+    const int t = g / nU, u = g - t * nU;
+    const Stream<NM> st = make_stream<F, NM>(m, row0 + t * row_step + R, koff);
+    issue_unit<F, NM>(ring + slot * SB, st, u, koff + u * UK);
+  };
+#pragma unroll
+  for (int p = 0; p < PF - 1; ++p) {
+    if (p < total) issue(p, p);
+    cp_async_commit();
+  }
+  int slot_issue = PF - 1, slot_read = 0;
+  for (int g = 0; g < total; ++g) {
+    const int gn = g + PF - 1;
+    if (gn < total) issue(gn, slot_issue);
+    cp_async_commit();
+    cp_async_wait<PF - 1>();  // unit g has landed
+    const int t = g / nU, u = g - t * nU;
+    Unit<NM> cur;
+    read_unit<F, NM>(cur, ring + slot_read * SB, make_stream<F, NM>(m, row0 + t * row_step + R, koff), koff + u * UK);
+    slot_issue = (slot_issue + 1 == PF) ? 0 : slot_issue + 1;
+    slot_read = (slot_read + 1 == PF) ? 0 : slot_read + 1;
+    compute_unit<F, NM>(cur, xrow + koff + u * UK, blk);
+    if ((u + 1) % bu == 0) {
+#pragma unroll
+      for (int i = 0; i < NM; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { acc[i][j] += blk[i][j]; blk[i][j] = 0.f; }
+    }
+    if (u == nU - 1) {
+      epi(t, acc);
+#pragma unroll
+      for (int i = 0; i < NM; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    }
+  }
+  cp_async_wait<0>();
+}
+
 // Largest-magnitude element -> exponent p with amax * 2^-p in [2^14, 2^15).
 __device__ __forceinline__ int scale_exponent_bits(uint32_t amax_bits) {
   amax_bits &= 0x7FFFFFFFu;
@@ -742,6 +800,48 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
       __syncthreads();  // s_src / s_amax are reused by the next segment
     }
     const int t_lo = max(q0, sg * tasks_per_seg), t_hi = min(q1, sg_end * tasks_per_seg);
+    if (S == 1) {
+      // this warp's tiles of each segment (every kWarps-th task) as one stream
+      for (int seg = sg; seg < sg_end; ++seg) {
+        const int a0 = max(t_lo, seg * tasks_per_seg), a1 = min(t_hi, (seg + 1) * tasks_per_seg);
+        if (a0 >= a1) continue;
+        const int qs = a0 + (((t_lo + warp - a0) % kWarps) + kWarps) % kWarps;
+        if (qs >= a1) continue;
+        const int ntile = (a1 - 1 - qs) / kWarps + 1;
+        const int i = seg - sg;
+        const bool shared_item = FS && seg == 0;
+        const int e = shared_item ? 0 : a.rb.act[seg - sh];
+        const int ncols = s_ncols[i];
+        const int K = shared_item ? a.Is : I;
+        const int fmt = shared_item ? FS : FR;
+        const QW& qd = shared_item ? a.sdown : a.down;
+        const Mat m[1] = {mat_of(qd, fmt, e, H, K)};
+        const int bu = dec_block_units(fmt, K);
+        const __half* xrow = hsm + (size_t)i * seg_halfs + (size_t)(r < ncols ? r : ncols) * hs_stride;
+        const int tile0 = qs - seg * tasks_per_seg;
+        const float ts = (fmt == MOE_FMT_NVFP4) ? __ldg(qd.ts + e) : 1.f;
+        auto epi = [&](int t, float (&acc)[1][4]) {
+          const int tile = tile0 + t * kWarps;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int col = 2 * c + (j & 1);
+            const int row = tile * 16 + r + ((j & 2) ? 8 : 0);
+            const int out = s_col_out[i][col];
+            if (out >= 0) {
+              const float val = acc[0][j] * exp2i(s_pexp[i][col]) * ts;
+              if (shared_item) a.S[(size_t)out * H + row] = val;
+              else a.P[(size_t)out * H + row] = val;
+            }
+          }
+        };
+        if (shared_item) {
+          if constexpr (FS != 0) warp_tiles<FS, 1, kStagesDN>(m, tile0 * 16, 16 * kWarps, ntile, K, bu, xrow, ring, epi);
+        } else {
+          warp_tiles<FR, 1, kStagesDN>(m, tile0 * 16, 16 * kWarps, ntile, K, bu, xrow, ring, epi);
+        }
+      }
+      continue;
+    }
     for (int q = t_lo + warp; q < t_hi; q += kWarps) {
       const int seg = q / tasks_per_seg, i = seg - sg;
       const bool shared_item = FS && seg == 0;
