@@ -440,10 +440,24 @@ __device__ __forceinline__ void warp_tiles(const Mat (&m)[NM], int row0, int row
   for (int i = 0; i < NM; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) { blk[i][j] = 0.f; acc[i][j] = 0.f; }
+  // the streams of tile t are those of tile 0 moved by t row steps (every
+  // format's code and scale addresses are linear in the row step used here)
+  const Stream<NM> st0 = make_stream<F, NM>(m, row0 + R, koff);
+  const Stream<NM> st1 = make_stream<F, NM>(m, row0 + row_step + R, koff);
+  auto stream_of = [&](int t) {
+    Stream<NM> st;
+#pragma unroll
+    for (int i = 0; i < NM; ++i)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        st.d[i][r] = st0.d[i][r] + (ptrdiff_t)t * (st1.d[i][r] - st0.d[i][r]);
+        st.s[i][r] = st0.s[i][r] + (ptrdiff_t)t * (st1.s[i][r] - st0.s[i][r]);
+      }
+    return st;
+  };
   auto issue = [&](int g, int slot) {
     const int t = g / nU, u = g - t * nU;
-    const Stream<NM> st = make_stream<F, NM>(m, row0 + t * row_step + R, koff);
-    issue_unit<F, NM>(ring + slot * SB, st, u, koff + u * UK);
+    issue_unit<F, NM>(ring + slot * SB, stream_of(t), u, koff + u * UK);
   };
 #pragma unroll
   for (int p = 0; p < PF - 1; ++p) {
@@ -458,7 +472,7 @@ __device__ __forceinline__ void warp_tiles(const Mat (&m)[NM], int row0, int row
     cp_async_wait<PF - 1>();  // unit g has landed
     const int t = g / nU, u = g - t * nU;
     Unit<NM> cur;
-    read_unit<F, NM>(cur, ring + slot_read * SB, make_stream<F, NM>(m, row0 + t * row_step + R, koff), koff + u * UK);
+    read_unit<F, NM>(cur, ring + slot_read * SB, stream_of(t), koff + u * UK);
     slot_issue = (slot_issue + 1 == PF) ? 0 : slot_issue + 1;
     slot_read = (slot_read + 1 == PF) ? 0 : slot_read + 1;
     compute_unit<F, NM>(cur, xrow + koff + u * UK, blk);
@@ -893,15 +907,24 @@ __global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;  // (token, 4 columns)
   if (i >= a.T * (H / 4)) return;
   const int t = i / (H / 4), c4 = i - t * (H / 4);
+  // all k partial rows are loaded before the j-ordered fma chain (k <= 16)
+  float wj[16];
+  float4 pj[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (j < k) {
+      wj[j] = __ldcg(a.rb.topk_w + t * k + j);
+      pj[j] = __ldcg(reinterpret_cast<const float4*>(a.P + (size_t)(t * k + j) * H) + c4);
+    }
   float y[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < k; ++j) {
-    const float w = __ldcg(a.rb.topk_w + t * k + j);
-    const float4 p = __ldcg(reinterpret_cast<const float4*>(a.P + (size_t)(t * k + j) * H) + c4);
-    y[0] = __fmaf_rn(w, p.x, y[0]);
-    y[1] = __fmaf_rn(w, p.y, y[1]);
-    y[2] = __fmaf_rn(w, p.z, y[2]);
-    y[3] = __fmaf_rn(w, p.w, y[3]);
-  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (j < k) {
+      y[0] = __fmaf_rn(wj[j], pj[j].x, y[0]);
+      y[1] = __fmaf_rn(wj[j], pj[j].y, y[1]);
+      y[2] = __fmaf_rn(wj[j], pj[j].z, y[2]);
+      y[3] = __fmaf_rn(wj[j], pj[j].w, y[3]);
+    }
   if (FS) {
     const float4 sv = __ldcg(reinterpret_cast<const float4*>(a.S + (size_t)t * H) + c4);
     y[0] = __fadd_rn(y[0], sv.x);
