@@ -73,14 +73,24 @@ __device__ __forceinline__ float ord_value(uint32_t o) {
   return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
-// Largest key of the lane and its slot; equal keys -> the lower slot (lower expert id).
+// Largest key of the lane and its slot; equal keys -> the lower slot (lower
+// expert id).  A tournament: depth log2(NQ) instead of a chain of NQ - 1.
 template <int NQ>
 __device__ __forceinline__ void lane_best(const uint32_t (&key)[NQ], uint32_t& bk, int& bq) {
-  bk = key[0];
-  bq = 0;
+  uint32_t k2[NQ];
+  int q2[NQ];
 #pragma unroll
-  for (int q = 1; q < NQ; ++q)
-    if (key[q] > bk) { bk = key[q]; bq = q; }
+  for (int q = 0; q < NQ; ++q) { k2[q] = key[q]; q2[q] = q; }
+#pragma unroll
+  for (int w = NQ / 2; w > 0; w >>= 1)
+#pragma unroll
+    for (int q = 0; q < w; ++q) {
+      const bool right = k2[2 * q + 1] > k2[2 * q];  // strictly larger: ties keep the lower slot
+      k2[q] = right ? k2[2 * q + 1] : k2[2 * q];
+      q2[q] = right ? q2[2 * q + 1] : q2[2 * q];
+    }
+  bk = k2[0];
+  bq = q2[0];
 }
 
 // One warp: top-k of one token.  E <= 32 NQ: lane holds the keys of experts
@@ -92,11 +102,23 @@ template <int NQ>
 __device__ void topk_warp(const float* __restrict__ logits_row, int E, int k, int32_t* idx_out, float* w_out,
                           int32_t* idx_out2, float* w_out2) {
   const int lane = threadIdx.x & 31;
+  // lane holds experts lane * NQ + q (q < NQ): consecutive logits, loaded as float4 when whole
   uint32_t key[NQ];
+  if (E == 32 * NQ) {
 #pragma unroll
-  for (int q = 0; q < NQ; ++q) {
-    const int e = q * 32 + lane;
-    key[q] = (e < E) ? ord_key(__ldcg(logits_row + e)) : 0u;
+    for (int q4 = 0; q4 < NQ / 4; ++q4) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(logits_row + lane * NQ) + q4);
+      key[4 * q4] = ord_key(v.x);
+      key[4 * q4 + 1] = ord_key(v.y);
+      key[4 * q4 + 2] = ord_key(v.z);
+      key[4 * q4 + 3] = ord_key(v.w);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const int e = lane * NQ + q;
+      key[q] = (e < E) ? ord_key(__ldcg(logits_row + e)) : 0u;
+    }
   }
   uint32_t bk;
   int bq;
@@ -105,8 +127,8 @@ __device__ void topk_warp(const float* __restrict__ logits_row, int E, int k, in
   int my_i = 0;
   for (int j = 0; j < k; ++j) {
     const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
-    const uint32_t id = __reduce_min_sync(0xFFFFFFFFu, bk == m ? (uint32_t)(bq * 32 + lane) : 0xFFFFFFFFu);
-    if ((int)(id & 31) == lane) {  // this lane's candidate won: drop it, find the next one
+    const uint32_t id = __reduce_min_sync(0xFFFFFFFFu, bk == m ? (uint32_t)(lane * NQ + bq) : 0xFFFFFFFFu);
+    if ((int)(id / NQ) == lane) {  // this lane's candidate won: drop it, find the next one
 #pragma unroll
       for (int q = 0; q < NQ; ++q)
         if (q == bq) key[q] = 0u;
