@@ -286,7 +286,8 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   ea.hs_tok_stride = Kmax + 32;
 
   const size_t warps_cta = kExpertThreads / 32;
-  const size_t smem_gu = (size_t)(T + 1) * ea.xs_tok_stride * 2 + warps_cta * kStagesGU * dec_stage_bytes(2);
+  const int gu_st = gu_stages(T <= kGuSmallT ? 3 : 2);
+  const size_t smem_gu = (size_t)T * ea.xs_tok_stride * 2 + warps_cta * gu_st * dec_stage_bytes(2);
   // the down kernel stages up to kMaxDnSegs expert segments of h at once, as
   // many as keep two CTAs per SM
   const size_t seg_bytes = (size_t)(MOE_DECODE_MAX_TOKENS + 1) * ea.hs_tok_stride * 2;

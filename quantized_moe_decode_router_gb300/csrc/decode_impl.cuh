@@ -606,24 +606,29 @@ __device__ __forceinline__ bool block_reduce(float (&acc)[NM][4], const float* t
 
 // --------------------------------------------------------------- gate / up --
 
-template <int FR, int FS>
+template <int FR, int FS, int PF>
 __device__ __forceinline__ void gu_tile(int fmt_is_shared, const Mat (&m)[2], int row0, int kb, int Kw, int bu,
                                         const __half* xrow, float (&acc)[2][4], float* bpart, uint8_t* ring) {
   if (fmt_is_shared) {
-    if constexpr (FS != 0) warp_tile<FS, 2, kStagesGU>(m, row0, kb, Kw, bu, xrow, acc, bpart, ring);
+    if constexpr (FS != 0) warp_tile<FS, 2, PF>(m, row0, kb, Kw, bu, xrow, acc, bpart, ring);
   } else {
-    warp_tile<FR, 2, kStagesGU>(m, row0, kb, Kw, bu, xrow, acc, bpart, ring);
+    warp_tile<FR, 2, PF>(m, row0, kb, Kw, bu, xrow, acc, bpart, ring);
   }
 }
 
-template <int FR, int FS>
-__global__ void __launch_bounds__(kExpertThreads, 2) gateup_kernel(ExpertArgs a) {
+// MINB CTAs per SM: 2 with three ring stages per warp (large batches: about
+// one task per warp, each streaming with more bytes in flight), 3 with two
+// (small batches: more warps in flight).
+template <int FR, int FS, int MINB>
+__global__ void __launch_bounds__(kExpertThreads, MINB) gateup_kernel(ExpertArgs a) {
+  constexpr int PF = gu_stages(MINB);
   extern __shared__ __align__(16) uint8_t smem[];
   const int T = a.T, H = a.H, I = a.I, k = a.k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int xs_stride = a.xs_tok_stride;
-  __half* xs = reinterpret_cast<__half*>(smem);  // [T + 1][xs_stride]
-  uint8_t* ring = smem + (size_t)(T + 1) * xs_stride * 2 + (size_t)warp * kStagesGU * stage_bytes<2>();
+  // [T][xs_stride]; columns without a token read row 0 (their results are discarded)
+  __half* xs = reinterpret_cast<__half*>(smem);
+  uint8_t* ring = smem + (size_t)T * xs_stride * 2 + (size_t)warp * PF * stage_bytes<2>();
   __shared__ int s_pexp[kMaxT + 1];
   __shared__ const uint16_t* s_src[kMaxT];
 
@@ -660,7 +665,7 @@ __global__ void __launch_bounds__(kExpertThreads, 2) gateup_kernel(ExpertArgs a)
     const int tile_id = shared_item ? n_active * tpe + qq / Si : qq / Si;
     const int slice = qq % Si;
     const int Kw = H / Si;
-    int e = 0, tile, ncols, col_tok = T, col_pair[2] = {-1, -1}, col_tokc[2] = {T, T};
+    int e = 0, tile, ncols, col_tok = 0, col_pair[2] = {-1, -1}, col_tokc[2] = {0, 0};
     if (!shared_item) {
       const int slot = tile_id / tpe;
       tile = tile_id - slot * tpe;
@@ -697,7 +702,7 @@ __global__ void __launch_bounds__(kExpertThreads, 2) gateup_kernel(ExpertArgs a)
     float* tile_part = a.gu_part + (shared_item ? (size_t)(S > 1 ? n_active * tpe * Br : 0) + (size_t)tile * Bs
                                                 : (size_t)tile_id * Br) * (32 * 8);
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    gu_tile<FR, FS>(shared_item, m, row0, slice * Kw, Kw, shared_item ? bus : bur, xs + (size_t)col_tok * xs_stride,
+    gu_tile<FR, FS, PF>(shared_item, m, row0, slice * Kw, Kw, shared_item ? bus : bur, xs + (size_t)col_tok * xs_stride,
                     acc, Si > 1 ? tile_part + (size_t)slice * (B / Si) * (32 * 8) : nullptr, ring);
     if (!block_reduce<2>(acc, tile_part, a.gu_cnt + tile_id, Si, B)) continue;
     const float tsg = (fmt == MOE_FMT_NVFP4) ? __ldg(qg.ts + e) : 1.f;
@@ -966,7 +971,8 @@ cudaError_t launch_expert_pair(int sfmt, bool down, const ExpertArgs& a, size_t 
 #define QMOE_CASE(FS)                                                                              \
   case FS:                                                                                         \
     return down ? launch_pdl_kernel<FR, FS>(down_kernel<FR, FS>, a, smem, s)                       \
-                : launch_pdl_kernel<FR, FS>(gateup_kernel<FR, FS>, a, smem, s);
+                : (a.T <= kGuSmallT ? launch_pdl_kernel<FR, FS>(gateup_kernel<FR, FS, 3>, a, smem, s)    \
+                                    : launch_pdl_kernel<FR, FS>(gateup_kernel<FR, FS, 2>, a, smem, s));
     QMOE_CASE(0)
     QMOE_CASE(MOE_FMT_NVFP4)
     QMOE_CASE(MOE_FMT_MXFP4)

@@ -74,7 +74,10 @@ struct ExpertArgs {
 constexpr int kMaxDnSegs = 4;
 
 constexpr int kExpertThreads = 256;  // 8 warps
-constexpr int kStagesGU = 3;         // cp.async ring stages per warp, gate/up (two matrices per unit)
+// Gate/up: batches of at most kGuSmallT tokens run 3 CTAs per SM with 2
+// cp.async ring stages per warp, larger ones 2 CTAs per SM with 3 stages.
+constexpr int kGuSmallT = 4;
+__host__ __device__ constexpr int gu_stages(int ctas_per_sm) { return ctas_per_sm >= 3 ? 2 : 3; }
 constexpr int kStagesDN = 4;         // cp.async ring stages per warp, down (one matrix per unit)
 // Bytes of one ring stage: NM matrices x 2 rows x 32 lanes x (16 B codes + 4 B scale word).
 constexpr int dec_stage_bytes(int nm) { return nm * 2 * 32 * (16 + 4); }
