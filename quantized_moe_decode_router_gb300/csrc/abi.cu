@@ -278,6 +278,17 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
       const long blocks = (Sr > 1 ? act * (I / 16) * (long)dec_blocks(L->fmt, H) : 0) + (long)(Is / 16) * Bs;
       ea.gu_slices_s = blocks <= kMaxSplitBlocks ? Ss : 1;
     }
+    // routed tiles beyond the first wave of tasks: up to 8 slices (the kernel
+    // decides how many tiles from the active-expert count); with unsplit head
+    // tiles only the tail's block sums are stored, after which come the shared ones
+    const int Br = dec_blocks(L->fmt, H);
+    int St = Sr;
+    while (St < 8 && Br % (2 * St) == 0) St *= 2;
+    ea.gu_slices_t = St;
+    const long shared_blocks =
+        L->shared_fmt && ea.gu_slices_s > 1 ? (long)(Is / 16) * dec_blocks(L->shared_fmt, H) : 0;
+    const long cap = Sr > 1 ? act * (I / 16) : (kMaxSplitBlocks - shared_blocks) / Br;
+    ea.gu_tail_cap = (int)(cap < 0 ? 0 : cap);
   }
   // token rows staged with a stride of 16 banks: the MMA operand loads of two
   // rows in one quarter warp fall on disjoint banks

@@ -644,26 +644,42 @@ __global__ void __launch_bounds__(kExpertThreads, MINB) gateup_kernel(ExpertArgs
   const int n_active = *reinterpret_cast<volatile int*>(&a.rb.ctrl->n_active);
   const int tpe = I / 16;
   const int stiles = FS ? a.Is / 16 : 0;
-  const int n_tiles = n_active * tpe + stiles;
-  const int S = a.gu_slices, Ss = FS ? a.gu_slices_s : 1;
-  const int n_tasks = (n_tiles - stiles) * S + stiles * Ss;
+  const int n_rtiles = n_active * tpe;
+  const int S = a.gu_slices, Ss = FS ? a.gu_slices_s : 1, St = a.gu_slices_t;
   const int Br = dec_blocks(FR, H), bur = dec_block_units(FR, H);
   const int Bs = FS ? dec_blocks(FS, H) : 1, bus = FS ? dec_block_units(FS, H) : 1;
   const int r = lane >> 2, c = lane & 3;
   // every warp starts on task (its global warp id); later tasks are handed out
   // one at a time from a global counter, so warps that finish early take more.
-  // The shared expert's (costlier) tasks come first.
+  // The shared expert's (costlier) tasks come first.  Routed tiles that do not
+  // fit in that first wave (the tail) are split into St > S slices, so the
+  // warps that finish the first wave share them in short pieces.
   const int n_shared_tasks = stiles * Ss;
   const int nw = gridDim.x * kWarps;
+  int n_tail = 0;
+  if (St > S) {
+    const long first = (long)n_shared_tasks + (long)n_rtiles * S;
+    if (first > nw) n_tail = (int)min((long)min(n_rtiles, a.gu_tail_cap), (first - nw + S - 1) / S);
+  }
+  const int n_head = n_rtiles - n_tail;
+  const int n_tasks = n_shared_tasks + n_head * S + n_tail * St;
+  // stored block sums: routed tiles (all when S > 1, else the tail only), then shared tiles
+  const size_t shared_part0 = (size_t)(S > 1 ? n_rtiles : n_tail) * Br;
   uint32_t* next = &a.rb.ctrl->gu_next;
   int qn = 0;
   for (int q = blockIdx.x * kWarps + warp; q < n_tasks; q = __shfl_sync(0xFFFFFFFFu, qn, 0)) {
     if (lane == 0) qn = nw + (int)atomicAdd(next, 1u);  // the next task, fetched while this one runs
     const bool shared_item = q < n_shared_tasks;
-    const int Si = shared_item ? Ss : S;  // K slices of this tile
-    const int qq = shared_item ? q : q - n_shared_tasks;
-    const int tile_id = shared_item ? n_active * tpe + qq / Si : qq / Si;
-    const int slice = qq % Si;
+    int Si, tile_id, slice;  // K slices of this tile, tile, slice
+    if (shared_item) {
+      Si = Ss; tile_id = n_rtiles + q / Ss; slice = q % Ss;
+    } else if (q - n_shared_tasks < n_head * S) {
+      const int qq = q - n_shared_tasks;
+      Si = S; tile_id = qq / S; slice = qq % S;
+    } else {
+      const int qt = q - n_shared_tasks - n_head * S;
+      Si = St; tile_id = n_head + qt / St; slice = qt % St;
+    }
     const int Kw = H / Si;
     int e = 0, tile, ncols, col_tok = 0, col_pair[2] = {-1, -1}, col_tokc[2] = {0, 0};
     if (!shared_item) {
@@ -682,7 +698,7 @@ __global__ void __launch_bounds__(kExpertThreads, MINB) gateup_kernel(ExpertArgs
         }
       }
     } else {
-      tile = tile_id - n_active * tpe;
+      tile = tile_id - n_rtiles;
       ncols = T;
       if (r < T) col_tok = r;
 #pragma unroll
@@ -698,9 +714,8 @@ __global__ void __launch_bounds__(kExpertThreads, MINB) gateup_kernel(ExpertArgs
     const Mat m[2] = {mat_of(qg, fmt, e, N, H), mat_of(qu, fmt, e, N, H)};
     const int row0 = tile * 16;
     const int B = shared_item ? Bs : Br;
-    // block sums of split tiles: routed tiles first (only when they are split), then shared ones
-    float* tile_part = a.gu_part + (shared_item ? (size_t)(S > 1 ? n_active * tpe * Br : 0) + (size_t)tile * Bs
-                                                : (size_t)tile_id * Br) * (32 * 8);
+    const int rslot = S > 1 ? tile_id : max(tile_id - n_head, 0);  // (unused for unsplit tiles)
+    float* tile_part = a.gu_part + (shared_item ? shared_part0 + (size_t)tile * Bs : (size_t)rslot * Br) * (32 * 8);
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     gu_tile<FR, FS, PF>(shared_item, m, row0, slice * Kw, Kw, shared_item ? bus : bur, xs + (size_t)col_tok * xs_stride,
                     acc, Si > 1 ? tile_part + (size_t)slice * (B / Si) * (32 * 8) : nullptr, ring);

@@ -62,6 +62,8 @@ struct ExpertArgs {
   uint16_t* y;        // bf16 [T, H]
   int gu_slices, dn_slices;  // K slices per 16-row tile (1 = no split)
   int gu_slices_s;           // K slices per shared-expert tile of the gate/up kernel
+  int gu_slices_t;           // K slices per routed gate/up tile beyond the first wave (>= gu_slices)
+  int gu_tail_cap;           // most routed tiles the block-sum buffer holds at gu_slices_t (gu_slices == 1)
   float* gu_part;     // block sums of split tiles, [tile blocks][32 lanes][8]
   uint32_t* gu_cnt;   // [tiles] slice arrival counters
   float* dn_part;     // [tile blocks][32 lanes][4]
@@ -208,12 +210,14 @@ __host__ __device__ inline int decode_unit_k(int fmt) {
 
 // The decode kernels sum K as blocks of units (pairs of units when a row has
 // an even number of them): the block layout depends only on (format, K).
+// Both are 0 for a format code that is not a weight format (0 = no shared expert).
 __host__ __device__ inline int dec_block_units(int fmt, int K) {
-  const int u = K / decode_unit_k(fmt);
-  return (u % 2 == 0) ? 2 : 1;
+  const int uk = decode_unit_k(fmt);
+  return (uk == 0 || (K / uk) % 2 == 0) ? 2 : 1;
 }
 __host__ __device__ inline int dec_blocks(int fmt, int K) {
-  return K / decode_unit_k(fmt) / dec_block_units(fmt, K);
+  const int uk = decode_unit_k(fmt);
+  return uk == 0 ? 0 : K / uk / dec_block_units(fmt, K);
 }
 
 }  // namespace qmoe
