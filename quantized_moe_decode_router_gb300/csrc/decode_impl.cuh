@@ -649,7 +649,8 @@ __global__ void __launch_bounds__(kExpertThreads, MINB) gateup_kernel(ExpertArgs
   const int Br = dec_blocks(FR, H), bur = dec_block_units(FR, H);
   const int Bs = FS ? dec_blocks(FS, H) : 1, bus = FS ? dec_block_units(FS, H) : 1;
   const int r = lane >> 2, c = lane & 3;
-  // every warp starts on task (its global warp id); later tasks are handed out
+  // every warp starts on task warp * grid + CTA, so consecutive tasks (the
+  // shared expert's first of all) land on different SMs; later tasks are handed out
   // one at a time from a global counter, so warps that finish early take more.
   // The shared expert's (costlier) tasks come first.  Routed tiles that do not
   // fit in that first wave (the tail) are split into St > S slices, so the
@@ -667,7 +668,7 @@ __global__ void __launch_bounds__(kExpertThreads, MINB) gateup_kernel(ExpertArgs
   const size_t shared_part0 = (size_t)(S > 1 ? n_rtiles : n_tail) * Br;
   uint32_t* next = &a.rb.ctrl->gu_next;
   int qn = 0;
-  for (int q = blockIdx.x * kWarps + warp; q < n_tasks; q = __shfl_sync(0xFFFFFFFFu, qn, 0)) {
+  for (int q = warp * gridDim.x + blockIdx.x; q < n_tasks; q = __shfl_sync(0xFFFFFFFFu, qn, 0)) {
     if (lane == 0) qn = nw + (int)atomicAdd(next, 1u);  // the next task, fetched while this one runs
     const bool shared_item = q < n_shared_tasks;
     int Si, tile_id, slice;  // K slices of this tile, tile, slice
