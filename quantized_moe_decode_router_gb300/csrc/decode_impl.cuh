@@ -400,9 +400,9 @@ __device__ __forceinline__ void warp_tile(const Mat (&m)[NM], int row0, int kb, 
     slot_issue = (slot_issue + 1 == PF) ? 0 : slot_issue + 1;
     slot_read = (slot_read + 1 == PF) ? 0 : slot_read + 1;
     compute_unit<F, NM>(cur, xrow + koff + u * UK, blk);
-    if ((u + 1) % bu == 0) {  // block complete
+    if (bu == 1 || (u & 1)) {  // block complete (bu is 1 or 2)
       if (bpart) {
-        float* d = bpart + (size_t)(u / bu) * (32 * 4 * NM) + lane * 4 * NM;
+        float* d = bpart + (size_t)(bu == 1 ? u : u >> 1) * (32 * 4 * NM) + lane * 4 * NM;
 #pragma unroll
         for (int i = 0; i < NM; ++i)
           *reinterpret_cast<float4*>(d + 4 * i) = make_float4(blk[i][0], blk[i][1], blk[i][2], blk[i][3]);
@@ -455,28 +455,29 @@ __device__ __forceinline__ void warp_tiles(const Mat (&m)[NM], int row0, int row
       }
     return st;
   };
-  auto issue = [&](int g, int slot) {
-    const int t = g / nU, u = g - t * nU;
-    issue_unit<F, NM>(ring + slot * SB, stream_of(t), u, koff + u * UK);
+  // (tile, unit) of the next unit to issue, kept as running counters
+  int ti = 0, ui = 0;
+  auto issue_next = [&](int slot) {
+    issue_unit<F, NM>(ring + slot * SB, stream_of(ti), ui, koff + ui * UK);
+    if (++ui == nU) { ui = 0; ++ti; }
   };
 #pragma unroll
   for (int p = 0; p < PF - 1; ++p) {
-    if (p < total) issue(p, p);
+    if (p < total) issue_next(p);
     cp_async_commit();
   }
   int slot_issue = PF - 1, slot_read = 0;
+  int t = 0, u = 0;  // the unit read in this iteration
   for (int g = 0; g < total; ++g) {
-    const int gn = g + PF - 1;
-    if (gn < total) issue(gn, slot_issue);
+    if (g + PF - 1 < total) issue_next(slot_issue);
     cp_async_commit();
     cp_async_wait<PF - 1>();  // unit g has landed
-    const int t = g / nU, u = g - t * nU;
     Unit<NM> cur;
     read_unit<F, NM>(cur, ring + slot_read * SB, stream_of(t), koff + u * UK);
     slot_issue = (slot_issue + 1 == PF) ? 0 : slot_issue + 1;
     slot_read = (slot_read + 1 == PF) ? 0 : slot_read + 1;
     compute_unit<F, NM>(cur, xrow + koff + u * UK, blk);
-    if ((u + 1) % bu == 0) {
+    if (bu == 1 || (u & 1)) {  // block complete (bu is 1 or 2)
 #pragma unroll
       for (int i = 0; i < NM; ++i)
 #pragma unroll
@@ -488,6 +489,10 @@ __device__ __forceinline__ void warp_tiles(const Mat (&m)[NM], int row0, int row
       for (int i = 0; i < NM; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+      u = 0;
+      ++t;
+    } else {
+      ++u;
     }
   }
   cp_async_wait<0>();
