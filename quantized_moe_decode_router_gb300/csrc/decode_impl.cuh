@@ -145,8 +145,22 @@ __device__ __forceinline__ void issue_unit(uint8_t* stage, const Stream<NM>& st,
     }
 }
 
+// Bit offset of the lane's scale bits inside their aligned 32-bit word.  For
+// 4-bit codes a unit advances the scale column by a multiple of 4 bytes (and
+// slices and row steps keep that alignment), so the offset of the first unit
+// (column koff) holds for every unit of the stream.
 template <int F, int NM>
-__device__ __forceinline__ void read_unit(Unit<NM>& u, const uint8_t* stage, const Stream<NM>& st, int kc) {
+__device__ __forceinline__ void scale_shifts(const Stream<NM>& st, int koff, uint32_t (&sh)[NM][2]) {
+#pragma unroll
+  for (int i = 0; i < NM; ++i)
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      sh[i][r] = 8u * (((uint32_t)reinterpret_cast<uintptr_t>(st.s[i][r]) + scale_col<F>(koff)) & 3u);
+}
+
+template <int F, int NM>
+__device__ __forceinline__ void read_unit(Unit<NM>& u, const uint8_t* stage, const Stream<NM>& st, int kc,
+                                          const uint32_t (&sh)[NM][2]) {
   const int lane = threadIdx.x & 31;
   const uint32_t sc = scale_col<F>(kc);
 #pragma unroll
@@ -155,8 +169,12 @@ __device__ __forceinline__ void read_unit(Unit<NM>& u, const uint8_t* stage, con
     for (int r = 0; r < 2; ++r) {
       u.d[i][r] = *reinterpret_cast<const uint4*>(stage + ((i * 2 + r) * 32 + lane) * 16);
       const uint32_t w = *reinterpret_cast<const uint32_t*>(stage + NM * 2 * 32 * 16 + ((i * 2 + r) * 32 + lane) * 4);
-      const uint32_t lo2 = ((uint32_t)reinterpret_cast<uintptr_t>(st.s[i][r]) + sc) & 3u;
-      u.s[i][r] = scale_bits<F>(w, lo2);
+      if constexpr (Fm<F>::kBits == 4) {
+        u.s[i][r] = (w >> sh[i][r]) & (F == MOE_FMT_MXFP4 ? 0xFFu : 0xFFFFu);
+      } else {
+        const uint32_t lo2 = ((uint32_t)reinterpret_cast<uintptr_t>(st.s[i][r]) + sc) & 3u;
+        u.s[i][r] = scale_bits<F>(w, lo2);
+      }
     }
 }
 
@@ -194,8 +212,10 @@ __device__ __forceinline__ bool fold4(const Unit<NM>& u, uint32_t (&fac)[NM][2][
     for (int r = 0; r < 2; ++r) {
       const uint32_t s = u.s[i][r];
       if constexpr (F == MOE_FMT_NVFP4) {
-        fac[i][r][0] = e4m3_bcast_f16x2(s & 0xFF);
-        fac[i][r][1] = e4m3_bcast_f16x2(s >> 8);
+        // both E4M3 scales in one conversion (byte 0 -> low half), each half then broadcast
+        const uint32_t f2 = e4m3x2_to_f16x2(s & 0xFFFFu);
+        fac[i][r][0] = prmt(f2, f2, 0x1010u);
+        fac[i][r][1] = prmt(f2, f2, 0x3232u);
         us[i][r] = 1.f;
       } else if constexpr (F == MOE_FMT_MXFP4) {
         const int c = (int)(s & 0xFF);
@@ -384,6 +404,8 @@ __device__ __forceinline__ void warp_tile(const Mat (&m)[NM], int row0, int kb, 
 #pragma unroll
     for (int j = 0; j < 4; ++j) blk[i][j] = 0.f;
   const Stream<NM> st = make_stream<F, NM>(m, R0, koff);
+  uint32_t sh[NM][2];
+  scale_shifts<F, NM>(st, koff, sh);
 #pragma unroll
   for (int p = 0; p < PF - 1; ++p) {
     if (p < nU) issue_unit<F, NM>(ring + p * SB, st, p, koff + p * UK);
@@ -396,7 +418,7 @@ __device__ __forceinline__ void warp_tile(const Mat (&m)[NM], int row0, int kb, 
     cp_async_commit();
     cp_async_wait<PF - 1>();  // unit u has landed
     Unit<NM> cur;
-    read_unit<F, NM>(cur, ring + slot_read * SB, st, koff + u * UK);
+    read_unit<F, NM>(cur, ring + slot_read * SB, st, koff + u * UK, sh);
     slot_issue = (slot_issue + 1 == PF) ? 0 : slot_issue + 1;
     slot_read = (slot_read + 1 == PF) ? 0 : slot_read + 1;
     compute_unit<F, NM>(cur, xrow + koff + u * UK, blk);
@@ -444,6 +466,8 @@ __device__ __forceinline__ void warp_tiles(const Mat (&m)[NM], int row0, int row
   // format's code and scale addresses are linear in the row step used here)
   const Stream<NM> st0 = make_stream<F, NM>(m, row0 + R, koff);
   const Stream<NM> st1 = make_stream<F, NM>(m, row0 + row_step + R, koff);
+  uint32_t sh[NM][2];  // the same for every tile: a row step moves the scales by a multiple of 4 bytes
+  scale_shifts<F, NM>(st0, koff, sh);
   auto stream_of = [&](int t) {
     Stream<NM> st;
 #pragma unroll
@@ -473,7 +497,7 @@ __device__ __forceinline__ void warp_tiles(const Mat (&m)[NM], int row0, int row
     cp_async_commit();
     cp_async_wait<PF - 1>();  // unit g has landed
     Unit<NM> cur;
-    read_unit<F, NM>(cur, ring + slot_read * SB, stream_of(t), koff + u * UK);
+    read_unit<F, NM>(cur, ring + slot_read * SB, stream_of(t), koff + u * UK, sh);
     slot_issue = (slot_issue + 1 == PF) ? 0 : slot_issue + 1;
     slot_read = (slot_read + 1 == PF) ? 0 : slot_read + 1;
     compute_unit<F, NM>(cur, xrow + koff + u * UK, blk);
