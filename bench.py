@@ -42,6 +42,10 @@ import synth  # noqa: E402
 METRIC = "MoE-layer weight GB/s & tokens/s at batch 1/8; % of HBM (decode) / FP4 peak"
 WORKLOAD = "decode_nvfp4"
 FALLBACK_HBM_GBS = 6800.0
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up launch at batch 8 on the
+# decode_nvfp4 workload, from one ncu capture of the current kernel (read 91.86 MB, write 2.36 MB);
+# None once the kernel changes, until the counters are taken again.
+GATEUP_TRAFFIC_BYTES = 94_224_128
 
 
 def _peaks():
@@ -288,7 +292,7 @@ def run_ours(args, world, rank, local):
         if headline:
             roof = {"kernel": "gateup_decode_kernel", "bound": "hbm", "achieved": round(ach, 1),
                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(ach / peak, 4),
-                    "traffic": None, "bytes_per_launch": int(gu_bytes),
+                    "traffic": GATEUP_TRAFFIC_BYTES, "bytes_per_launch": int(gu_bytes),
                     "kernel_us": {"router": round(avg[0], 3), "gateup": round(avg[1], 3), "down": round(avg[2], 3)}}
             # end to end through the public API with host buffers (pinned), one call per step
             ne = min(steps, args.e2e_steps)
