@@ -229,6 +229,37 @@ int32_t moe_decode_forward_noalloc(const moe_layer* layer, const void* x /* devi
                                    void* y /* device bf16 [T, H] */, const moe_options* opts, moe_stream_t stream);
 
 /*
+ * Launch plan of a decode call (moe_decode_forward) for a layer, T tokens and
+ * `num_sms` streaming multiprocessors: how each kernel splits the reduction
+ * dimension K of a 16-row weight tile between warps, and the shared memory
+ * it stages.  Host only: no device access, no launch; the layer's pointers
+ * are checked like moe_decode_forward's but never dereferenced.
+ *
+ * A K split changes no result: every tile is summed in fixed blocks added in
+ * block order whatever the split (DGPP README "Accuracy and correctness":
+ * deterministic, batch-invariant output).  Errors: MOE_ERR_INVALID_ARG (null
+ * out, T outside 1 .. MOE_DECODE_MAX_TOKENS, num_sms < 1, invalid layer),
+ * MOE_ERR_UNSUPPORTED (the layer's staging does not fit in shared memory).
+ */
+typedef struct {
+  int32_t gu_slices;        /* K slices of a routed gate/up tile in the first wave of tasks */
+  int32_t gu_slices_shared; /* K slices of a shared-expert gate/up tile */
+  int32_t gu_slices_tail;   /* K slices of a routed gate/up tile beyond the first wave */
+  int32_t gu_tail_cap;      /* most routed tiles split that way */
+  int32_t dn_slices;        /* K slices of a down tile */
+  int32_t dn_segs;          /* expert segments the down kernel stages at once */
+  int32_t gu_ctas_per_sm;   /* gate/up CTAs (of 8 warps) per SM */
+  int32_t reserved;
+  size_t gu_smem;           /* dynamic shared memory per gate/up CTA, bytes */
+  size_t dn_smem;           /* dynamic shared memory per down CTA, bytes */
+  size_t gu_split_blocks;   /* most K-block sums the gate/up kernel may store */
+  size_t dn_split_blocks;   /* most K-block sums the down kernel may store */
+  size_t split_block_capacity; /* K-block sums the workspace holds per kernel */
+} moe_decode_plan_info;
+
+int32_t moe_decode_plan(const moe_layer* layer, int32_t T, int32_t num_sms, moe_decode_plan_info* out);
+
+/*
  * Read and clear the device-side error flag of a workspace.  Synchronises
  * `stream` (this is the one call that blocks).  Returns MOE_OK,
  * MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BAD_INDEX.

@@ -52,6 +52,15 @@ class moe_ws_layout(ctypes.Structure):
                 ("total", ctypes.c_size_t)]
 
 
+class moe_decode_plan_info(ctypes.Structure):
+    _fields_ = [("gu_slices", ctypes.c_int32), ("gu_slices_shared", ctypes.c_int32),
+                ("gu_slices_tail", ctypes.c_int32), ("gu_tail_cap", ctypes.c_int32),
+                ("dn_slices", ctypes.c_int32), ("dn_segs", ctypes.c_int32), ("gu_ctas_per_sm", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("gu_smem", ctypes.c_size_t), ("dn_smem", ctypes.c_size_t),
+                ("gu_split_blocks", ctypes.c_size_t), ("dn_split_blocks", ctypes.c_size_t),
+                ("split_block_capacity", ctypes.c_size_t)]
+
+
 # (name, restype, argtypes) of every entry point declared in include/moe.h
 _P = ctypes.POINTER
 _SIGNATURES = {
@@ -74,6 +83,7 @@ _SIGNATURES = {
     "moe_decode_forward_noalloc": (ctypes.c_int32, [_P(moe_layer), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                                     _P(moe_options), ctypes.c_void_p]),
     "moe_check": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_decode_plan": (ctypes.c_int32, [_P(moe_layer), ctypes.c_int32, ctypes.c_int32, _P(moe_decode_plan_info)]),
     "moe_workspace_layout": (ctypes.c_int32, [_P(moe_layer), ctypes.c_int32, _P(moe_options), _P(moe_ws_layout)]),
     "moe_dequantize": (ctypes.c_int32, [ctypes.c_int32, _P(moe_qweight), ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
@@ -179,6 +189,13 @@ def workspace_layout(layer: Layer, max_tokens: int, act_quant: int = 0) -> moe_w
     lc, o, out = layer.c(), _opts(act_quant), moe_ws_layout()
     _check(load().moe_workspace_layout(ctypes.byref(lc), max_tokens, ctypes.byref(o), ctypes.byref(out)),
            "moe_workspace_layout")
+    return out
+
+
+def decode_plan(layer: Layer, T: int, num_sms: int) -> moe_decode_plan_info:
+    """Launch plan of a decode call (K splits, staged shared memory); host only."""
+    lc, out = layer.c(), moe_decode_plan_info()
+    _check(load().moe_decode_plan(ctypes.byref(lc), T, num_sms, ctypes.byref(out)), "moe_decode_plan")
     return out
 
 

@@ -215,6 +215,71 @@ RouterArgs router_args(const moe_layer* L, const Layout& lo, void* ws, const voi
   return ra;
 }
 
+
+// Launch plan of a decode call: K splits, staging strides and shared-memory
+// sizes, from the layer's shapes and formats and the SM count (host only).
+struct DecodePlan {
+  int gu_slices, gu_slices_s, gu_slices_t, gu_tail_cap, dn_slices, dn_segs;
+  int xs_tok_stride, hs_tok_stride;
+  size_t smem_gu, smem_dn;
+  long gu_blocks, dn_blocks;  // most K-block sums each kernel may store
+};
+
+int32_t plan_decode(const moe_layer* L, int T, int sms, DecodePlan* p) {
+  const int H = L->hidden, I = L->inter, Is = L->shared_fmt ? L->shared_inter : 0;
+  const int warps = sms * 16;  // resident warps the expert kernels aim for
+  const long act = (long)T * L->top_k < L->n_experts ? (long)T * L->top_k : L->n_experts;
+  const int Br = dec_blocks(L->fmt, H);
+  p->gu_slices = choose_slices(H, L->fmt, act * (I / 16), H, L->shared_fmt, Is / 16, warps);
+  p->dn_slices = choose_slices(I, L->fmt, act * (H / 16), Is, L->shared_fmt, Is ? H / 16 : 0, warps);
+  // shared-expert tiles of gate/up: split K until a task carries no more bytes
+  // than a routed one (both formats' blocks permitting), so no task outlasts the rest
+  const int Sr = p->gu_slices;
+  p->gu_slices_s = Sr;
+  long shared_blocks = 0;
+  if (L->shared_fmt) {
+    const double br = (double)(data_bytes(L->fmt, I, H) + scale_bytes(L->fmt, I, H)) / I / Sr;
+    const double bs = (double)(data_bytes(L->shared_fmt, Is, H) + scale_bytes(L->shared_fmt, Is, H)) / Is;
+    const int Bs = dec_blocks(L->shared_fmt, H);
+    int Ss = 1;
+    while (bs / Ss > 1.15 * br && Bs % (2 * Ss) == 0) Ss *= 2;
+    const long blocks = (Sr > 1 ? act * (I / 16) * (long)Br : 0) + (long)(Is / 16) * Bs;
+    p->gu_slices_s = blocks <= kMaxSplitBlocks ? Ss : 1;
+    if (p->gu_slices_s > 1) shared_blocks = (long)(Is / 16) * Bs;
+  }
+  // routed tiles beyond the first wave of tasks: up to 8 slices (the kernel
+  // decides how many tiles from the active-expert count); with unsplit head
+  // tiles only the tail's block sums are stored, after which come the shared ones
+  int St = Sr;
+  while (St < 8 && Br % (2 * St) == 0) St *= 2;
+  p->gu_slices_t = St;
+  const long cap = Sr > 1 ? act * (I / 16) : (kMaxSplitBlocks - shared_blocks) / Br;
+  p->gu_tail_cap = (int)(cap < 0 ? 0 : cap);
+  p->gu_blocks = (Sr > 1 ? act * (I / 16) : (St > Sr ? p->gu_tail_cap : 0)) * (long)Br + shared_blocks;
+  p->dn_blocks = p->dn_slices > 1 ? act * (H / 16) * (long)dec_blocks(L->fmt, I) +
+                                        (L->shared_fmt ? (long)(H / 16) * dec_blocks(L->shared_fmt, Is) : 0)
+                                  : 0;
+  // token rows staged with a stride of 16 banks: the MMA operand loads of two
+  // rows in one quarter warp fall on disjoint banks
+  p->xs_tok_stride = H + 32;
+  const int Kmax = Is > I ? Is : I;
+  p->hs_tok_stride = Kmax + 32;
+
+  const size_t warps_cta = kExpertThreads / 32;
+  const int gu_st = gu_stages(T <= kGuSmallT ? 3 : 2);
+  p->smem_gu = (size_t)T * p->xs_tok_stride * 2 + warps_cta * gu_st * dec_stage_bytes(2);
+  // the down kernel stages up to kMaxDnSegs expert segments of h at once, as
+  // many as keep two CTAs per SM
+  const size_t seg_bytes = (size_t)(MOE_DECODE_MAX_TOKENS + 1) * p->hs_tok_stride * 2;
+  const size_t rings_dn = warps_cta * kStagesDN * dec_stage_bytes(1);
+  const size_t half_sm = 113 * 1024;
+  const int segs = half_sm > rings_dn ? (int)((half_sm - rings_dn) / seg_bytes) : 1;
+  p->dn_segs = segs < 1 ? 1 : (segs > kMaxDnSegs ? kMaxDnSegs : segs);
+  p->smem_dn = (size_t)p->dn_segs * seg_bytes + rings_dn;
+  if (p->smem_gu > 227 * 1024 || p->smem_dn > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
 int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* y, void* ws, size_t ws_bytes,
                             cudaStream_t stream, void* const* events) {
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -260,54 +325,18 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
-  const int warps = sms * 16;  // resident warps the expert kernels aim for
-  const long act = (long)T * L->top_k < L->n_experts ? (long)T * L->top_k : L->n_experts;
-  ea.gu_slices = choose_slices(H, L->fmt, act * (I / 16), H, L->shared_fmt, Is / 16, warps);
-  ea.dn_slices = choose_slices(I, L->fmt, act * (H / 16), Is, L->shared_fmt, Is ? H / 16 : 0, warps);
-  // shared-expert tiles of gate/up: split K until a task carries no more bytes
-  // than a routed one (both formats' blocks permitting), so no task outlasts the rest
-  {
-    const int Sr = ea.gu_slices;
-    ea.gu_slices_s = Sr;
-    if (L->shared_fmt) {
-      const double br = (double)(data_bytes(L->fmt, I, H) + scale_bytes(L->fmt, I, H)) / I / Sr;
-      const double bs = (double)(data_bytes(L->shared_fmt, Is, H) + scale_bytes(L->shared_fmt, Is, H)) / Is;
-      const int Bs = dec_blocks(L->shared_fmt, H);
-      int Ss = 1;
-      while (bs / Ss > 1.15 * br && Bs % (2 * Ss) == 0) Ss *= 2;
-      const long blocks = (Sr > 1 ? act * (I / 16) * (long)dec_blocks(L->fmt, H) : 0) + (long)(Is / 16) * Bs;
-      ea.gu_slices_s = blocks <= kMaxSplitBlocks ? Ss : 1;
-    }
-    // routed tiles beyond the first wave of tasks: up to 8 slices (the kernel
-    // decides how many tiles from the active-expert count); with unsplit head
-    // tiles only the tail's block sums are stored, after which come the shared ones
-    const int Br = dec_blocks(L->fmt, H);
-    int St = Sr;
-    while (St < 8 && Br % (2 * St) == 0) St *= 2;
-    ea.gu_slices_t = St;
-    const long shared_blocks =
-        L->shared_fmt && ea.gu_slices_s > 1 ? (long)(Is / 16) * dec_blocks(L->shared_fmt, H) : 0;
-    const long cap = Sr > 1 ? act * (I / 16) : (kMaxSplitBlocks - shared_blocks) / Br;
-    ea.gu_tail_cap = (int)(cap < 0 ? 0 : cap);
-  }
-  // token rows staged with a stride of 16 banks: the MMA operand loads of two
-  // rows in one quarter warp fall on disjoint banks
-  ea.xs_tok_stride = H + 32;
-  const int Kmax = Is > I ? Is : I;
-  ea.hs_tok_stride = Kmax + 32;
-
-  const size_t warps_cta = kExpertThreads / 32;
-  const int gu_st = gu_stages(T <= kGuSmallT ? 3 : 2);
-  const size_t smem_gu = (size_t)T * ea.xs_tok_stride * 2 + warps_cta * gu_st * dec_stage_bytes(2);
-  // the down kernel stages up to kMaxDnSegs expert segments of h at once, as
-  // many as keep two CTAs per SM
-  const size_t seg_bytes = (size_t)(MOE_DECODE_MAX_TOKENS + 1) * ea.hs_tok_stride * 2;
-  const size_t rings_dn = warps_cta * kStagesDN * dec_stage_bytes(1);
-  const size_t half_sm = 113 * 1024;
-  int segs = half_sm > rings_dn ? (int)((half_sm - rings_dn) / seg_bytes) : 1;
-  ea.dn_segs = segs < 1 ? 1 : (segs > kMaxDnSegs ? kMaxDnSegs : segs);
-  const size_t smem_dn = (size_t)ea.dn_segs * seg_bytes + rings_dn;
-  if (smem_gu > 227 * 1024 || smem_dn > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+  DecodePlan pl;
+  const int32_t pst = plan_decode(L, T, sms, &pl);
+  if (pst != MOE_OK) return pst;
+  ea.gu_slices = pl.gu_slices;
+  ea.gu_slices_s = pl.gu_slices_s;
+  ea.gu_slices_t = pl.gu_slices_t;
+  ea.gu_tail_cap = pl.gu_tail_cap;
+  ea.dn_slices = pl.dn_slices;
+  ea.dn_segs = pl.dn_segs;
+  ea.xs_tok_stride = pl.xs_tok_stride;
+  ea.hs_tok_stride = pl.hs_tok_stride;
+  const size_t smem_gu = pl.smem_gu, smem_dn = pl.smem_dn;
 
   mark(0);
   cudaError_t err = launch_router_decode(ra, stream);
@@ -485,6 +514,29 @@ static int32_t decode_forward_checked(const moe_layer* layer, const void* x, int
 int32_t moe_decode_forward(const moe_layer* layer, const void* x, int32_t T, void* y, const moe_options* opts,
                            void* ws, size_t ws_bytes, moe_stream_t stream) {
   return decode_forward_checked(layer, x, T, y, opts, ws, ws_bytes, stream, nullptr);
+}
+
+int32_t moe_decode_plan(const moe_layer* layer, int32_t T, int32_t num_sms, moe_decode_plan_info* out) {
+  if (!out || T < 1 || T > MOE_DECODE_MAX_TOKENS || num_sms < 1) return MOE_ERR_INVALID_ARG;
+  const int32_t st = check_layer(layer);
+  if (st != MOE_OK) return st;
+  DecodePlan pl;
+  const int32_t pst = plan_decode(layer, T, num_sms, &pl);
+  if (pst != MOE_OK) return pst;
+  std::memset(out, 0, sizeof(*out));
+  out->gu_slices = pl.gu_slices;
+  out->gu_slices_shared = pl.gu_slices_s;
+  out->gu_slices_tail = pl.gu_slices_t;
+  out->gu_tail_cap = pl.gu_tail_cap;
+  out->dn_slices = pl.dn_slices;
+  out->dn_segs = pl.dn_segs;
+  out->gu_ctas_per_sm = T <= kGuSmallT ? 3 : 2;
+  out->gu_smem = pl.smem_gu;
+  out->dn_smem = pl.smem_dn;
+  out->gu_split_blocks = (size_t)pl.gu_blocks;
+  out->dn_split_blocks = (size_t)pl.dn_blocks;
+  out->split_block_capacity = kMaxSplitBlocks;
+  return MOE_OK;
 }
 
 int32_t moe_decode_forward_timed(const moe_layer* layer, const void* x, int32_t T, void* y,
