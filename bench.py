@@ -330,8 +330,7 @@ def run_ours(args, world, rank, local):
         "steps": head["steps"], "warmup": args.warmup, "ms_per_step": round(head["us_per_layer"] / 1e3, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) weights quantised NVFP4 / FP8 b128; N(0,1) bf16 tokens)",
-        "config": {"workload": f"{cfg.name}: NVFP4 MoE layer H={cfg.H} E={cfg.E} top-{cfg.k} I={cfg.I} "
-                               f"+ FP8 b128 shared expert I={cfg.shared_I}, batch {Th} tokens",
+        "config": {"workload": workload_name(cfg, Th),
                    "batch_tokens": Th, "instances_rotated": R,
                    "l2": f"inputs larger than L2: {R} layer copies rotated, "
                          f"{R * min_call / 1e6:.0f} MB touched per rotation vs L2 {l2 / 1e6:.0f} MB",
@@ -472,6 +471,86 @@ def run_prefill(args, local, peak_bf16, peak_kind):
     }
 
 
+def workload_name(cfg, T: int) -> str:
+    return (f"{cfg.name}: NVFP4 MoE layer H={cfg.H} E={cfg.E} top-{cfg.k} I={cfg.I} "
+            f"+ FP8 b128 shared expert I={cfg.shared_I}, batch {T} tokens")
+
+
+def run_reference(args):
+    """The oracle, as it stands, timed on the host cores.  One step is one piece
+    of a batch-T layer call, in layer order: the router (exact logits, top-k,
+    dispatch), the shared expert, then each routed expert segment (its gate, up
+    and down decoded to FP64, the SwiGLU MLP on its token rows, the weighted
+    add into the outputs); successive token batches follow one another, so K
+    steps cover whole layer calls in proportion.  value = weight bytes of the
+    timed pieces / time, the metric of the GPU arm."""
+    from oracle import formats as F
+    from oracle import moe as M
+    cfg = synth.CONFIGS[args.workload]
+    T = max(int(b) for b in args.batches.split(","))
+    host = synth.make_layer(cfg, seed=0)
+
+    def layer_pieces(batch):
+        x = synth.make_tokens(cfg, T, seed=3000, batch=batch)
+        X = F.bf16_to_f64(x)
+        st = {}
+
+        def router():
+            _, _, idx, w = M.route(x, host.router_w, host.router_b, cfg.k)
+            st["cnt"], st["off"], st["pair"] = M.dispatch(idx, cfg.E)
+            st["w"], st["y"] = w, np.zeros((T, cfg.H))
+            return host.router_bytes()
+        yield router
+        if host.shared_gate is not None:
+            def shared():
+                Wg, Wu, Wd = (F.decode_qmat(host.shared_gate, 0), F.decode_qmat(host.shared_up, 0),
+                              F.decode_qmat(host.shared_down, 0))
+                st["y"] += M.swiglu_mlp(Wg, Wu, Wd, X)[1]
+                return host.shared_bytes()
+            yield shared
+        for e in range(cfg.E):
+            if st["cnt"][e] == 0:
+                continue
+
+            def expert(e=e):
+                ps = [int(p) for p in st["pair"][st["off"][e]:st["off"][e + 1]]]
+                rows = np.array([p // cfg.k for p in ps])
+                Wg, Wu, Wd = F.decode_qmat(host.gate, e), F.decode_qmat(host.up, e), F.decode_qmat(host.down, e)
+                P = M.swiglu_mlp(Wg, Wu, Wd, X[rows])[1]
+                for i, p in enumerate(ps):
+                    t, j = divmod(p, cfg.k)
+                    st["y"][t] += float(st["w"][t, j]) * P[i]
+                return host.expert_bytes()
+            yield expert
+
+    def steps():
+        b = 0
+        while True:
+            yield from layer_pieces(b)
+            b += 1
+
+    it = steps()
+    for _ in range(args.warmup):
+        next(it)()
+    byts = 0
+    t0 = time.time()
+    for _ in range(args.steps):
+        byts += next(it)()
+    dt = time.time() - t0
+    cores = len(os.sched_getaffinity(0))
+    value = round(byts / dt / 1e9, 4)
+    sample = (f"{args.steps} pieces of batch-{T} layer calls on {cfg.name} (router, shared expert, routed expert "
+              f"segments in layer order; FP64 numpy oracle, BLAS threads = {cores})")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / max(1, args.steps), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, the GPU arm's layer and token recipe)",
+            "config": {"workload": workload_name(cfg, T), "batch_tokens": T, "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+                             "seconds": round(dt, 2)},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def run_cpu_baseline(args, seconds_budget: float = 20.0):
     """The oracle, as it stands, on a bounded sample of the workload (rank 0 only)."""
     from oracle import moe as M
@@ -516,14 +595,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        cb = run_cpu_baseline(args)
-        out = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": args.gpus,
-               "steps": args.cpu_batches, "warmup": 0, "ms_per_step": round(cb["seconds"] * 1e3 / max(1, args.cpu_batches), 3),
-               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-               "data": "synthetic", "config": {"workload": args.workload},
-               "cpu_baseline": cb,
-               "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(out))
+        print(json.dumps(run_reference(args)))
         return
     out = run_ours(args, world, rank, local)
     if world == 1 and not args.no_prefill:
