@@ -27,7 +27,7 @@ bool shape_ok(int fmt, int N, int K) {
 }
 
 struct Layout {
-  size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, rb_cnt, h_amax, hs_amax, gu_part, gu_cnt,
+  size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, h_amax, hs_amax, gu_part, gu_cnt,
       dn_part, dn_cnt;
   // prefill path
   size_t xg, xsig, xnorm, wnorm, hist, pos_of, tiles, h16, hsig, xq, xsf, xqg, xsfg, hq, hsf, rw_hi, rw_lo;
@@ -57,7 +57,6 @@ Layout make_layout(const moe_layer* L, int maxT) {
   o.hs = take(T * Is * 2 + 16);
   o.P = take(T * k * H * 4);
   o.S = take(T * H * 4 + 16);
-  o.rb_cnt = take(H / 16 * 4);
   o.h_amax = take(T * k * 4);
   o.hs_amax = take(T * 4 + 16);
   // block sums of tiles split along K (at most kMaxSplitBlocks entries)
@@ -315,7 +314,6 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   ea.hs_amax = ra.hs_amax;
   ea.P = reinterpret_cast<float*>(b + lo.P);
   ea.S = reinterpret_cast<float*>(b + lo.S);
-  ea.rb_cnt = reinterpret_cast<uint32_t*>(b + lo.rb_cnt);
   ea.gu_part = reinterpret_cast<float*>(b + lo.gu_part);
   ea.gu_cnt = reinterpret_cast<uint32_t*>(b + lo.gu_cnt);
   ea.dn_part = reinterpret_cast<float*>(b + lo.dn_part);
@@ -412,9 +410,7 @@ bool prefill_supported(const moe_layer* L, bool act_quant) {
 int32_t qmoe::clear_workspace_counters(const moe_layer* L, void* ws, size_t ws_bytes, cudaStream_t s) {
   const Layout lo = make_layout(L, ws_max_tokens(L, ws_bytes));
   uint8_t* b = static_cast<uint8_t*>(ws);
-  const size_t H = (size_t)L->hidden;
-  const size_t sections[4][2] = {{lo.ctrl, sizeof(Ctrl)},
-                                 {lo.rb_cnt, H / 16 * 4},
+  const size_t sections[3][2] = {{lo.ctrl, sizeof(Ctrl)},
                                  {lo.gu_cnt, lo.dn_part - lo.gu_cnt},
                                  {lo.dn_cnt, lo.xg - lo.dn_cnt}};
   for (const auto& sec : sections)

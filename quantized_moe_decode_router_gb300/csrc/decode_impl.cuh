@@ -6,14 +6,15 @@
 //            expert, gate and up in one pass (DGPP README "Execution and
 //            performance", engine.expert_gemm_pair).
 //   down:    P[p, rows] = W_down_e h_p (FP32 partials, DGPP README row
-//            engine.prefill_bf16_partials); the last contribution to a
-//            16-row block combines y = bf16( sum_j w_j P_j + S ).
+//            engine.prefill_bf16_partials), S for the shared expert.
+//   combine: y = bf16( sum_j w_j P_j + S ) in j order, chained after down.
 //
 // Work is split into independent warp tasks (expert, 16-row tile, K slice)
 // so that every warp streams its own weights without CTA barriers; K slices
 // of one tile are summed by the last slice to finish, in slice order
-// (deterministic, no floating-point atomics).  Weights stream from HBM with
-// 128-bit non-allocating loads and are decoded in registers (DGPP forum post
+// (deterministic, no floating-point atomics).  Weights stream from HBM in
+// 16-byte cp.async copies (L2 only) through a warp-private shared-memory ring
+// and are decoded in registers (DGPP forum post
 // 15 "Lossless bf12": decode reads weights at the memory line rate,
 // rebuilding them in registers) into f16 MMA fragments; the tokens are the
 // N=8 side of m16n8k16, so one decode serves every token of the expert.
@@ -779,7 +780,7 @@ __global__ void __launch_bounds__(kExpertThreads, MINB) gateup_kernel(ExpertArgs
   }
 }
 
-// -------------------------------------------------------- down + combine --
+// -------------------------------------------------------------------- down --
 
 template <int FR, int FS>
 __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {

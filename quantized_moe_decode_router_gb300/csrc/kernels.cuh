@@ -58,7 +58,6 @@ struct ExpertArgs {
   uint32_t* hs_amax;  // [T]
   float* P;           // f32 [T*k, H] per-pair down partials
   float* S;           // f32 [T, H] shared expert output
-  uint32_t* rb_cnt;   // [H / 16] arrival counters of the combine
   uint16_t* y;        // bf16 [T, H]
   int gu_slices, dn_slices;  // K slices per 16-row tile (1 = no split)
   int gu_slices_s;           // K slices per shared-expert tile of the gate/up kernel
@@ -92,7 +91,7 @@ int router_warps_per_row(int H, int E, int sms);
 // for this layer and workspace size (stream-ordered memsets, no allocation).
 int32_t clear_workspace_counters(const moe_layer* L, void* ws, size_t ws_bytes, cudaStream_t s);
 cudaError_t launch_router_decode(const RouterArgs& a, cudaStream_t s);
-// Gate/up (down = false) or down + combine (down = true) for a routed format;
+// Gate/up (down = false) or down (down = true) for a routed format;
 // the shared format is selected at run time among the compiled instances.
 cudaError_t launch_expert_nvfp4(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
 cudaError_t launch_expert_mxfp4(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
