@@ -46,6 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 # decode_nvfp4 workload, from one ncu capture of the current kernel (read 91.86 MB, write 2.36 MB);
 # None once the kernel changes, until the counters are taken again.
 GATEUP_TRAFFIC_BYTES = 94_224_128
+# kernels one decode layer call launches: router, gate/up, down, combine
+DECODE_KERNELS_PER_CALL = 4
 
 
 def _peaks():
@@ -338,7 +340,7 @@ def run_ours(args, world, rank, local):
                    "gpu": dev_name, "layer_gen_s": round(gen_s, 1)},
         "tokens_per_s": head["tokens_per_s"], "hbm_frac": head["hbm_frac"],
         "batches": {str(T): r for T, r in results.items()},
-        "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": 3 * head["steps"],
+        "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": DECODE_KERNELS_PER_CALL * head["steps"],
     }
     return out
 
