@@ -64,12 +64,13 @@ def router_logits(x_bits: np.ndarray, Wr: np.ndarray, bias: Optional[np.ndarray]
 
     Returns (logits f32 [T, E], near_midpoint bool [T, E]).  Each BF16 x FP32
     product is exact in FP64.  The FP64 BLAS dot carries at most
-    gamma_n * sum|x_h Wr_eh| error; where that bound cannot separate the FP64
-    result from an FP32 rounding midpoint, the logit is recomputed with an
-    exactly rounded sum (math.fsum, then exact rationals at a midpoint).
-    ``near_midpoint`` marks logits whose exact value lies within 2^-40
-    (relative) of an FP32 rounding midpoint: a compensated FP32 dot may round
-    those differently, so callers report them.
+    gamma_n * sum|x_h Wr_eh| error; every logit whose FP64 result lies within
+    that bound (plus 2^-40 relative) of an FP32 rounding midpoint is
+    recomputed from an exactly rounded sum (math.fsum, then exact rationals
+    at a midpoint), which settles both its rounding and its distance to the
+    midpoint.  ``near_midpoint`` then marks the logits whose exact value lies
+    within 2^-40 (relative) of an FP32 rounding midpoint: a compensated FP32
+    dot may round those differently, so callers report them.
     """
     X = F.bf16_to_f64(x_bits)
     W = np.asarray(Wr, dtype=np.float32).astype(np.float64)
@@ -79,22 +80,37 @@ def router_logits(x_bits: np.ndarray, Wr: np.ndarray, bias: Optional[np.ndarray]
     gamma = n * _U64 / (1.0 - n * _U64)
     bound = gamma * (np.abs(X) @ np.abs(W).T) * (1.0 + 1e-9) + 1e-300
     l32 = d.astype(np.float32)
-    f = l32.astype(np.float64)
-    up = np.nextafter(l32, np.float32(np.inf)).astype(np.float64)
-    dn = np.nextafter(l32, np.float32(-np.inf)).astype(np.float64)
-    mid_up, mid_dn = (f + up) / 2.0, (f + dn) / 2.0
-    safe = (d + bound < mid_up) & (d - bound > mid_dn)
-    for t, e in zip(*np.nonzero(~safe)):
+    # entries the FP64 result cannot settle: its rounding, or its distance to the nearer midpoint
+    uncertain = midpoint_distance(d, l32) <= 2.0 ** -40 * np.maximum(np.abs(d), 1e-300) + bound
+    d_exact = d.copy()
+    for t, e in zip(*np.nonzero(uncertain)):
         prods = [float(a) * float(b) for a, b in zip(X[t], W[e])]
+        d_exact[t, e] = math.fsum(prods)        # within 2^-53 relative of the exact sum
         l32[t, e] = _fl32_exact(prods)
-    f = l32.astype(np.float64)
-    up = np.nextafter(l32, np.float32(np.inf)).astype(np.float64)
-    dn = np.nextafter(l32, np.float32(-np.inf)).astype(np.float64)
-    dist = np.minimum(np.abs(d - (f + up) / 2.0), np.abs(d - (f + dn) / 2.0))
-    near = dist <= 2.0 ** -40 * np.maximum(np.abs(d), 1e-300) + bound
+    near = near_midpoint(d_exact, l32)
     if bias is not None:
         l32 = (l32 + np.asarray(bias, dtype=np.float32)[None, :]).astype(np.float32)
     return l32, near
+
+
+def midpoint_distance(d: np.ndarray, l32: np.ndarray) -> np.ndarray:
+    """Distance from d to the nearer of the two FP32 rounding midpoints around l32 (exact in FP64)."""
+    f = l32.astype(np.float64)
+    up = np.nextafter(l32, np.float32(np.inf)).astype(np.float64)
+    dn = np.nextafter(l32, np.float32(-np.inf)).astype(np.float64)
+    return np.minimum(np.abs(d - (f + up) / 2.0), np.abs(d - (f + dn) / 2.0))
+
+
+def near_midpoint(d_exact: np.ndarray, l32: np.ndarray) -> np.ndarray:
+    """Logits whose exact dot product lies within 2^-40 (relative) of an FP32 midpoint.
+
+    d_exact holds the dot products to within 2^-53 relative (the FP64 result
+    wherever it is provably farther from a midpoint) and l32 the correctly
+    rounded FP32 logits.  A compensated FP32 dot product (float-float, whose
+    error before its last rounding is of order 2^-44 relative) may round the
+    flagged ones the other way.
+    """
+    return midpoint_distance(d_exact, l32) <= 2.0 ** -40 * np.maximum(np.abs(d_exact), 1e-300)
 
 
 def topk(l32: np.ndarray, k: int) -> np.ndarray:

@@ -9,7 +9,10 @@
 * permuting expert ids permutes the routing and leaves y unchanged;
 * batch invariance: a token's output does not depend on the other tokens;
 * the W4A4 activation quantizer round-trips on-grid blocks and matches
-  brute force;
+  brute force, and an independent torch quantiser (float8_e4m3fn cast of
+  the block scale, round-half-even on the binade's quantum for E2M1);
+* the W4A4 mode of the layer: one expert, top-1, weight 1 equals the SwiGLU
+  MLP with x quantised, h rounded to BF16 and then quantised, in that order;
 * planted mistakes in the oracle are caught by these pins.
 """
 import numpy as np
@@ -173,7 +176,65 @@ def test_nvfp4_act_quantizer_pins():
             for i in range(16):
                 y = float(np.float32(blk[i] / sv))
                 cand = np.abs(min(abs(y), 6.0) - F.E2M1_GRID)
-                assert abs(abs(D[r, b * 16 + i]) / sv - F.E2M1_GRID[np.argmin(cand)]) == 0 or cand.min() == np.sort(cand)[1]
+                nearest = np.flatnonzero(cand == cand.min())       # one code, or two on a tie
+                pick = nearest[0] if len(nearest) == 1 else nearest[nearest % 2 == 0][0]   # tie: even code
+                assert abs(D[r, b * 16 + i]) / sv == F.E2M1_GRID[pick]
+
+
+def _torch_nvfp4_fake_quant(A: torch.Tensor) -> torch.Tensor:
+    """NVFP4 quantise-dequantise of BF16-valued rows in 16-element blocks, written independently of
+    the oracle: the block scale through torch's float8_e4m3fn cast of the FP32 quotient amax / 6, the
+    FP32 quotient a / s by torch's float32 division (the scale saturates at 448, where torch's cast
+    would give NaN), and the E2M1 code by round-half-even on the
+    binade's quantum (0.5 below 2, 1 below 4, 2 above) saturating at 6."""
+    n, K = A.shape
+    B = A.reshape(n, K // 16, 16)
+    amax = B.abs().amax(dim=-1)
+    s = torch.clamp(amax.to(torch.float32) / 6.0, max=448.0).to(torch.float8_e4m3fn).to(torch.float32)  # saturating
+    y = B.to(torch.float32) / s[..., None]
+    ay = y.abs().to(torch.float64)
+    quantum = torch.where(ay < 2, 0.5, torch.where(ay < 4, 1.0, 2.0))
+    v = torch.clamp(torch.round(ay / quantum) * quantum, max=6.0) * torch.sign(y).to(torch.float64)
+    v = torch.where(s[..., None] > 0, v, torch.zeros_like(v))
+    return (v * s[..., None].to(torch.float64)).reshape(n, K)
+
+
+def _torch_w4a4_mlp(Wg, Wu, Wd, X):
+    """The W4A4 lever's order: x quantised, gate and up, h = bf16(silu(g) * u), h quantised, down."""
+    Xq = _torch_nvfp4_fake_quant(X)
+    g = Xq @ Wg.T
+    u = Xq @ Wu.T
+    h = torch.from_numpy(F.round_bf16((torch.nn.functional.silu(g) * u).numpy()))
+    return _torch_nvfp4_fake_quant(h) @ Wd.T
+
+
+@pytest.mark.parametrize("fmt,H,I", [(FMT_NVFP4, 256, 128), (FMT_MXFP4, 256, 128)])
+def test_w4a4_single_expert_equals_quantised_swiglu_mlp(fmt, H, I):
+    # one expert, top-1, weight 1: the W4A4 mode is the SwiGLU MLP with x and h replaced by their
+    # NVFP4 quantise-dequantise (activations, page 5 weekly update: W4A4 prefill is opt-in)
+    cfg = _small(fmt, H=H, I=I)
+    lay = synth.make_layer(cfg, seed=8)
+    x = synth.make_tokens(cfg, 24, seed=8)
+    out = M.layer_forward(lay, x, act_quant=True)
+    X = torch.from_numpy(F.bf16_to_f64(x))
+    y_ref = _torch_w4a4_mlp(_torch_decode(lay.gate), _torch_decode(lay.up), _torch_decode(lay.down), X).numpy()
+    ok = M.within_tolerance(F.bf16_to_f64(out["y_bits"]), y_ref, ulps=1.0, abs_tol=1e-6)
+    assert ok.all(), np.abs(F.bf16_to_f64(out["y_bits"]) - y_ref).max()
+    # and the lever changes the result: the exact chain differs from it
+    exact = M.layer_forward(lay, x)
+    assert not np.array_equal(exact["y_bits"], out["y_bits"])
+
+
+def test_w4a4_fake_quant_matches_torch_on_hard_blocks():
+    # zero blocks, blocks at the E2M1 tie points and at saturation, huge and tiny binades
+    rng = np.random.default_rng(12)
+    A = F.round_bf16(rng.standard_normal((40, 64)) * np.exp(rng.uniform(-20, 20, (40, 1))))
+    A[0, :16] = 0.0
+    A[1, :16] = np.array([6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0] * 2) * np.array([1, -1] * 8)  # amax 6: s = 1
+    A[2, :16] = np.array([4.0, 5.0, 6.0, -6.0] * 4) * 3.0                  # s = 3: ties at 5 * 3
+    got = M.nvfp4_fake_quant(A)
+    ref = _torch_nvfp4_fake_quant(torch.from_numpy(A)).numpy()
+    assert np.array_equal(got, ref)
 
 
 # --------------------------------------------------- planted mistakes ----
@@ -209,7 +270,44 @@ def _unstable_dispatch(idx, E):
     return cnt, off, np.concatenate([pair[off[e]:off[e + 1]][::-1] for e in range(E)]).astype(np.int32)
 
 
-_ORIG = {"dispatch": M.dispatch, "decode": F.decode, "swiglu": M.swiglu_mlp}
+def _w4a4_variant(Wg, Wu, Wd, X, act_quant=False, quant_x=True, round_first=True, quant_h=True):
+    if act_quant and quant_x:
+        X = M.nvfp4_fake_quant(X)
+    g = X @ Wg.T
+    u = X @ Wu.T
+    raw = M.silu(g) * u
+    h = F.round_bf16(raw)
+    if act_quant and quant_h:
+        hq = M.nvfp4_fake_quant(h if round_first else raw)
+    else:
+        hq = h
+    return h, hq @ Wd.T
+
+
+def _w4a4_h_unrounded(Wg, Wu, Wd, X, act_quant=False):
+    return _w4a4_variant(Wg, Wu, Wd, X, act_quant, round_first=False)
+
+
+def _w4a4_x_unquantised(Wg, Wu, Wd, X, act_quant=False):
+    return _w4a4_variant(Wg, Wu, Wd, X, act_quant, quant_x=False)
+
+
+def _w4a4_h_unquantised(Wg, Wu, Wd, X, act_quant=False):
+    return _w4a4_variant(Wg, Wu, Wd, X, act_quant, quant_h=False)
+
+
+def _router_logits_bound_mask(x_bits, Wr, bias=None):
+    # the mask computed from the FP64 result and its error bound, without settling the uncertain ones
+    l32, _ = _ORIG["router_logits"](x_bits, Wr, bias)
+    X = F.bf16_to_f64(x_bits)
+    W = np.asarray(Wr, dtype=np.float32).astype(np.float64)
+    d = X @ W.T
+    bound = X.shape[1] * 2.0 ** -53 * (np.abs(X) @ np.abs(W).T)
+    l0 = d.astype(np.float32)
+    return l32, M.midpoint_distance(d, l0) <= 2.0 ** -40 * np.abs(d) + bound
+
+
+_ORIG = {"dispatch": M.dispatch, "decode": F.decode, "swiglu": M.swiglu_mlp, "router_logits": M.router_logits}
 
 
 def test_planted_mistakes_are_caught(monkeypatch):
@@ -218,6 +316,7 @@ def test_planted_mistakes_are_caught(monkeypatch):
     import tests.test_oracle_router as TR
 
     single = (test_single_expert_equals_plain_swiglu_mlp, FMT_NVFP4, 128, 64)
+    w4a4 = (test_w4a4_single_expert_equals_quantised_swiglu_mlp, FMT_NVFP4, 256, 128)
     mistakes = {
         "nibble order": (F, "unpack_nibbles", _swapped_nibbles, [(TF.test_nvfp4_layout_hand_built,), single]),
         "silu sign": (M, "silu", lambda z: z / (1.0 + np.exp(z)), [single]),
@@ -228,6 +327,16 @@ def test_planted_mistakes_are_caught(monkeypatch):
         "unstable dispatch": (M, "dispatch", _unstable_dispatch, [(TR.test_dispatch_matches_plain_loop,)]),
         "gate/up swapped": (M, "swiglu_mlp", lambda Wg, Wu, Wd, X, act_quant=False: _ORIG["swiglu"](
             Wu, Wg, Wd, X, act_quant), [single]),
+        "W4A4: h quantised before its BF16 rounding": (M, "swiglu_mlp", _w4a4_h_unrounded, [w4a4]),
+        "W4A4: x not quantised": (M, "swiglu_mlp", _w4a4_x_unquantised, [w4a4]),
+        "W4A4: h not re-quantised": (M, "swiglu_mlp", _w4a4_h_unquantised, [w4a4]),
+        "mask window 2^-4": (M, "near_midpoint", lambda d, l: M.midpoint_distance(d, l) <= 2.0 ** -4 * np.abs(d),
+                             [(TR.test_near_midpoint_mask_flags_only_the_window, 1.0),
+                              (TR.test_near_midpoint_mask_empty_at_the_decode_seeds,)]),
+        "mask never set": (M, "near_midpoint", lambda d, l: np.zeros(d.shape, dtype=bool),
+                           [(TR.test_near_midpoint_mask_flags_only_the_window, 1.0)]),
+        "mask widened by the FP64 error bound": (M, "router_logits", _router_logits_bound_mask,
+                                                 [(TR.test_near_midpoint_mask_empty_at_the_decode_seeds,)]),
         "shared expert dropped": (M, "swiglu_mlp", lambda Wg, Wu, Wd, X, act_quant=False: (
             lambda h, P: (h, P * (Wg.shape[0] != 128)))(*_ORIG["swiglu"](Wg, Wu, Wd, X, act_quant)),
             [(test_shared_expert_adds_plain_mlp, FMT_FP8_B128)]),

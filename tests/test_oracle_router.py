@@ -131,3 +131,52 @@ def test_dispatch_empty_experts_and_single_token():
     assert list(cnt) == [1, 0, 0, 1, 0, 0]
     assert list(off) == [0, 1, 1, 1, 2, 2, 2]
     assert list(pair) == [1, 0]
+
+
+# ------------------------------------------------------ near-midpoint mask ----
+
+def _midpoint_case(delta: float, scale: float = 1.0):
+    """One logit whose exact dot product is scale * (1 + 2^-24 + delta): the FP32
+    midpoint between scale and scale * (1 + 2^-23), moved by scale * delta."""
+    terms = np.array([[1.0, 2.0 ** -24, delta, 0.0]]) * scale
+    Wr = terms.astype(np.float32)
+    assert np.all(Wr.astype(np.float64) == terms)
+    x = np.full((1, 4), 0x3F80, dtype=np.uint16)                   # bf16 1.0
+    return M.router_logits(x, Wr)
+
+
+@pytest.mark.parametrize("scale", [1.0, 2.0 ** 10, 2.0 ** -20])
+def test_near_midpoint_mask_flags_only_the_window(scale):
+    # on the midpoint, and 2^-42 away on either side: flagged (inside 2^-40 relative)
+    for delta in (0.0, 2.0 ** -42, -2.0 ** -42):
+        _, near = _midpoint_case(delta, scale)
+        assert near[0, 0], (delta, scale)
+    # 2^-30 away on either side: not flagged
+    for delta in (2.0 ** -30, -2.0 ** -30):
+        _, near = _midpoint_case(delta, scale)
+        assert not near[0, 0], (delta, scale)
+
+
+def test_near_midpoint_mask_empty_at_the_decode_seeds():
+    # the decode workloads' router matrices and token batches, seeds 0-3: no logit lies within
+    # 2^-40 of an FP32 midpoint (about 2^-15 expected per logit), so the GPU logits must all be exact
+    import synth
+    for name in ("tiny_nvfp4", "decode_nvfp4", "decode_mxfp4", "decode_int4"):
+        cfg = synth.CONFIGS[name]
+        Wr = synth.normal_f32(synth.stream_key(0, synth.configs.KIND_ROUTER, 0, 0), cfg.E * cfg.H,
+                              synth.configs.WEIGHT_SIGMA).reshape(cfg.E, cfg.H)
+        for seed in range(4):
+            for T in cfg.batches:
+                x = synth.make_tokens(cfg, T, seed=seed, batch=T)
+                _, near = M.router_logits(x, Wr)
+                assert not near.any(), (name, seed, T, int(near.sum()))
+
+
+def test_near_midpoint_fraction_matches_its_width():
+    # random logits: the flagged fraction is about the window's share of an FP32 ulp (2 * 2^-40 / 2^-24
+    # on average); a mask 2^10 wider or narrower is far outside [1/8, 8] times that
+    rng = np.random.default_rng(11)
+    x = _bf16_bits_random(rng, (64, 256))
+    W = (rng.standard_normal((2048, 256)) * 0.02).astype(np.float32)
+    _, near = M.router_logits(x, W)
+    assert int(near.sum()) <= 32                                   # 131072 logits, about 4 expected
