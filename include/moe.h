@@ -27,8 +27,9 @@
  *  - Every pointer marked "device" is a CUDA device pointer owned by the
  *    caller; descriptors (moe_layer, moe_options) live in host memory and are
  *    read only during the call.  The library allocates nothing and keeps no
- *    global state; it is safe to call concurrently on different streams with
- *    different workspaces.
+ *    global state, with one exception: the fixed device array of
+ *    moe_decode_forward_noalloc (below).  It is safe to call concurrently on
+ *    different streams with different workspaces.
  *  - All calls are asynchronous on `stream` and make no host reads of device
  *    data, so they can be captured in a CUDA graph.  Arguments are validated
  *    on the host before any launch; a failed validation launches nothing.
@@ -121,7 +122,8 @@ typedef struct {
 /* Largest token count moe_decode_forward accepts. */
 #define MOE_DECODE_MAX_TOKENS 8
 
-/* Human-readable name of a status code (static string, never NULL). */
+/* Human-readable name of a status code (static string, never NULL).
+ * Interface convenience, no passage: the pages define no error reporting. */
 const char* moe_status_string(int32_t status);
 
 /*
@@ -129,11 +131,15 @@ const char* moe_status_string(int32_t status);
  * moe_prefill_forward for up to max_tokens tokens (0 if the layer or options
  * are invalid).  The workspace must be 256-byte aligned and initialised once
  * with moe_workspace_init before its first use; the library leaves it
- * re-usable after every call.
+ * re-usable after every call.  It holds the routing results, the per-expert
+ * activations h and the FP32 partials (DGPP README "Execution and
+ * performance", engine.prefill_bf16_partials: partials summed in FP32 by
+ * default), so that the caller owns every device buffer.
  */
 size_t moe_workspace_size(const moe_layer* layer, int32_t max_tokens, const moe_options* opts);
 
-/* Zero the workspace control block (stream-ordered).  Call once per workspace. */
+/* Zero the workspace control block (stream-ordered).  Call once per workspace.
+ * Interface convenience, no passage. */
 int32_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
@@ -158,9 +164,16 @@ int32_t moe_route(const moe_layer* layer, const void* x /* device bf16 [T, H] */
  * Whole layer for decode-sized batches, T = 1 .. MOE_DECODE_MAX_TOKENS:
  *   y[t] = bf16( sum_j topk_w[t, j] * down_e( h_tj ) + shared(x_t) ),
  *   h_tj = bf16( silu(gate_e x_t) * (up_e x_t) ),  e = topk_idx[t, j],
- * with the shared expert (weight 1, no gate) added when present.  Routing
- * outputs are left in the workspace (see moe_workspace_layout).
- * opts may be NULL (defaults); act_quant must be 0 here.
+ * with the shared expert (weight 1, no gate) added when present.  Weights are
+ * read in their checkpoint formats and decoded in registers (DGPP README
+ * intro bullet "Serves checkpoints as published": no dequantized copy; forum
+ * post 15 "Lossless bf12": decode streams the weights at the memory line
+ * rate); activations BF16, accumulation and partials FP32, h and y rounded
+ * to BF16 once (forum post 1, quantisation table: activations stay BF16;
+ * README "Execution and performance", engine.prefill_bf16_partials and
+ * engine.prefill_fold_scales off by default).  Routing outputs are left in
+ * the workspace (see moe_workspace_layout).  opts may be NULL (defaults);
+ * act_quant must be 0 here (MOE_ERR_UNSUPPORTED otherwise).
  */
 int32_t moe_decode_forward(const moe_layer* layer, const void* x /* device bf16 [T, H] */, int32_t T,
                            void* y /* device bf16 [T, H] */, const moe_options* opts, void* ws, size_t ws_bytes,
@@ -173,17 +186,21 @@ int32_t moe_decode_forward(const moe_layer* layer, const void* x /* device bf16 
  * engine.expert_tile_list, engine.expert_gemm_pair), with FP32 partials and
  * a combine pass.  Supported so far: NVFP4 routed experts without a shared
  * expert, hidden and inter multiples of 128; anything else returns
- * MOE_ERR_UNSUPPORTED before any launch.  opts->act_quant must be 0 (the
- * NVFP4 W4A4 lever is not available yet: MOE_ERR_UNSUPPORTED).  Routing
- * outputs are left in the workspace; in its logits array only the experts the
- * router recomputed exactly (every selected one among them) hold their FP32
- * logit, the others hold -inf.
+ * MOE_ERR_UNSUPPORTED before any launch.  opts->act_quant = 1 selects the
+ * NVFP4 W4A4 lever (DGPP forum, page 5 weekly update: NVFP4 W4A4 prefill is
+ * opt-in): x and h are quantised to NVFP4 16-element blocks (the rule of
+ * moe_quantize_act_nvfp4) and the projections run as block-scaled FP4
+ * GEMMs; it needs hidden and inter multiples of 256 and 16-byte aligned
+ * scale arrays.  Routing outputs are left in the workspace; in its logits
+ * array only the experts the router recomputed exactly (every selected one
+ * among them) hold their FP32 logit, the others hold -inf.
  */
 int32_t moe_prefill_forward(const moe_layer* layer, const void* x /* device bf16 [T, H] */, int32_t T,
                             void* y /* device bf16 [T, H] */, const moe_options* opts, void* ws, size_t ws_bytes,
                             moe_stream_t stream);
 
 /*
+ * Interface convenience for measurement, no passage:
  * moe_prefill_forward that also records up to eight CUDA events on `stream`
  * (events[i] a cudaEvent_t or NULL): [0] before the first kernel, [1] after
  * the approximate router logits, [2] after top-k, [3] after the dispatch
@@ -196,6 +213,7 @@ int32_t moe_prefill_forward_timed(const moe_layer* layer, const void* x, int32_t
                                   void* const* events);
 
 /*
+ * Interface convenience for measurement, no passage:
  * moe_decode_forward that also records four CUDA events on `stream`: before
  * the router kernel, after it, after the gate/up kernel and after the down +
  * combine kernel (events[i] is a cudaEvent_t; any entry may be NULL).  For
@@ -216,13 +234,18 @@ int32_t moe_decode_forward_timed(const moe_layer* layer, const void* x, int32_t 
  *  - The workspace is a fixed 32 MiB array in the library's device memory;
  *    every GPU that loads the library holds it until the process exits.  A
  *    layer and T whose moe_workspace_size exceeds 32 MiB are rejected with
- *    MOE_ERR_WORKSPACE before anything is launched.
- *  - The first call on a device looks up the array's device address and
- *    zeroes it synchronously; make that first call before any stream capture.
- *  - Every call shares the one array (the arrival counters it needs at zero
- *    are cleared on `stream` at the start of each call), so calls that
- *    overlap on the GPU, from any stream or thread, race: serialise them.
+ *    MOE_ERR_WORKSPACE.  Every argument check of moe_decode_forward runs
+ *    first: a rejected call touches neither the array nor the device.
+ *  - Every call clears, on `stream`, the counters of the array that must
+ *    start at zero.  The first call on a device also clears the array's
+ *    device-side error word; make that first call before any stream capture.
+ *  - Every call shares the one array, so calls that overlap on the GPU, from
+ *    any stream or thread, race: serialise them.
+ *  - A device-side error (see moe_check) stays in the array's error word
+ *    until moe_check(NULL, 0, stream) reads and clears it.
  *  - The routing results stay in the array; they are not exposed.
+ *  - After a device reset the array is looked up again and the next call
+ *    counts as the first on that device.
  * Other arguments, checks and results are those of moe_decode_forward.
  */
 int32_t moe_decode_forward_noalloc(const moe_layer* layer, const void* x /* device bf16 [T, H] */, int32_t T,
@@ -262,11 +285,18 @@ int32_t moe_decode_plan(const moe_layer* layer, int32_t T, int32_t num_sms, moe_
 /*
  * Read and clear the device-side error flag of a workspace.  Synchronises
  * `stream` (this is the one call that blocks).  Returns MOE_OK,
- * MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BAD_INDEX.
+ * MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BAD_INDEX (the first device-side
+ * error since the last read), MOE_ERR_WORKSPACE for a null or short ws,
+ * MOE_ERR_CUDA if the synchronisation or the copy fails.  ws = NULL with
+ * ws_bytes = 0 reads the fixed array of moe_decode_forward_noalloc on the
+ * current device (MOE_OK if no such call has run there).  Interface
+ * convenience, no passage: the pages define no error reporting; kernels
+ * never trap, so errors surface here.
  */
 int32_t moe_check(void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Byte offsets, within the workspace, of the routing results a forward call leaves there. */
+/* Byte offsets, within the workspace, of the routing results a forward call leaves there
+ * (interface convenience for inspection and testing, no passage). */
 typedef struct {
   size_t logits;      /* f32 [T, E] */
   size_t topk_idx;    /* i32 [T, k] */

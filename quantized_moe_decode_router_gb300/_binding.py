@@ -259,6 +259,11 @@ def moe_check(ws, stream=None) -> int:
     return int(load().moe_check(_ptr(ws), ws.numel() * ws.element_size(), _stream_handle(stream)))
 
 
+def moe_check_noalloc(stream=None) -> int:
+    """moe_check of the allocation-free entry point's fixed array on the current device."""
+    return int(load().moe_check(None, 0, _stream_handle(stream)))
+
+
 def moe_dequantize(fmt: int, w: QWeight, N: int, K: int, expert: int, row0: int, nrows: int, out,
                    stream=None) -> int:
     qc = w.c()

@@ -1,6 +1,7 @@
 // Host side of the C ABI (include/moe.h): argument validation, workspace
 // layout, tiling choices and kernel launches.  Nothing here allocates device
 // memory; every buffer belongs to the caller.
+#include <cstddef>
 #include <cstring>
 
 #include "kernels.cuh"
@@ -407,10 +408,13 @@ bool prefill_supported(const moe_layer* L, bool act_quant) {
 
 }  // namespace
 
-int32_t qmoe::clear_workspace_counters(const moe_layer* L, void* ws, size_t ws_bytes, cudaStream_t s) {
+int32_t qmoe::clear_workspace_counters(const moe_layer* L, void* ws, size_t ws_bytes, bool keep_error,
+                                       cudaStream_t s) {
   const Layout lo = make_layout(L, ws_max_tokens(L, ws_bytes));
   uint8_t* b = static_cast<uint8_t*>(ws);
-  const size_t sections[3][2] = {{lo.ctrl, sizeof(Ctrl)},
+  // the error word and its info come first in the control block
+  const size_t skip = keep_error ? offsetof(Ctrl, router_arrive) : 0;
+  const size_t sections[3][2] = {{lo.ctrl + skip, sizeof(Ctrl) - skip},
                                  {lo.gu_cnt, lo.dn_part - lo.gu_cnt},
                                  {lo.dn_cnt, lo.xg - lo.dn_cnt}};
   for (const auto& sec : sections)
@@ -491,9 +495,11 @@ int32_t moe_route(const moe_layer* layer, const void* x, int32_t T, int32_t* top
   return cuda_status(launch_router_decode(ra, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-static int32_t decode_forward_checked(const moe_layer* layer, const void* x, int32_t T, void* y,
-                                      const moe_options* opts, void* ws, size_t ws_bytes, moe_stream_t stream,
-                                      void* const* events) {
+}  // extern "C"
+
+// Host checks of a decode call's arguments other than the workspace (no device access).
+int32_t qmoe::check_decode_args(const moe_layer* layer, const void* x, int32_t T, const void* y,
+                                const moe_options* opts) {
   int32_t st = check_layer(layer);
   if (st != MOE_OK) return st;
   if ((st = check_options(opts)) != MOE_OK) return st;
@@ -502,8 +508,18 @@ static int32_t decode_forward_checked(const moe_layer* layer, const void* x, int
   if (!aligned16(x) || !aligned16(y)) return MOE_ERR_MISALIGNED;
   if (T < 1) return MOE_ERR_INVALID_ARG;
   if (T > MOE_DECODE_MAX_TOKENS) return MOE_ERR_UNSUPPORTED;
-  if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
   if ((size_t)T * layer->hidden * 2 > 200 * 1024) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+extern "C" {
+
+static int32_t decode_forward_checked(const moe_layer* layer, const void* x, int32_t T, void* y,
+                                      const moe_options* opts, void* ws, size_t ws_bytes, moe_stream_t stream,
+                                      void* const* events) {
+  int32_t st = qmoe::check_decode_args(layer, x, T, y, opts);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
   return decode_forward_impl(layer, x, T, y, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), events);
 }
 
@@ -598,8 +614,16 @@ int32_t moe_prefill_forward_timed(const moe_layer* layer, const void* x, int32_t
 }
 
 int32_t moe_check(void* ws, size_t ws_bytes, moe_stream_t stream) {
-  if (!ws || ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!ws && ws_bytes == 0) {
+    // the allocation-free entry point's array on the current device
+    void* p = nullptr;
+    const int32_t st = qmoe::noalloc_array_if_used(&p);
+    if (st != MOE_OK || !p) return st;
+    ws = p;
+    ws_bytes = sizeof(Ctrl);
+  }
+  if (!ws || ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   Ctrl c;
   if (cudaMemcpy(&c, ws, sizeof(Ctrl), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;

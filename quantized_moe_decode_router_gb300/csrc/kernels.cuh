@@ -88,8 +88,14 @@ constexpr int kMaxSplitBlocks = 16384;
 
 int router_warps_per_row(int H, int E, int sms);
 // Zero the control block and every arrival counter of a workspace laid out
-// for this layer and workspace size (stream-ordered memsets, no allocation).
-int32_t clear_workspace_counters(const moe_layer* L, void* ws, size_t ws_bytes, cudaStream_t s);
+// for this layer and workspace size (stream-ordered memsets, no allocation);
+// keep_error leaves the device-side error word and its info as they are.
+int32_t clear_workspace_counters(const moe_layer* L, void* ws, size_t ws_bytes, bool keep_error, cudaStream_t s);
+// Host checks of moe_decode_forward's arguments other than the workspace.
+int32_t check_decode_args(const moe_layer* layer, const void* x, int32_t T, const void* y, const moe_options* opts);
+// The allocation-free entry point's array on the current device, or nullptr
+// in *out if no call has used it on this device yet.
+int32_t noalloc_array_if_used(void** out);
 cudaError_t launch_router_decode(const RouterArgs& a, cudaStream_t s);
 // Gate/up (down = false) or down (down = true) for a routed format;
 // the shared format is selected at run time among the compiled instances.

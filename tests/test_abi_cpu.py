@@ -123,3 +123,27 @@ def test_invalid_calls_rejected_before_launch(lib):
         B.MOE_ERR_INVALID_ARG
     assert lib.moe_quantize_act_nvfp4(FAKE, 4, 100, FAKE, FAKE, None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_workspace_init(None, 1024, None) == B.MOE_ERR_WORKSPACE
+
+
+def test_noalloc_rejects_bad_calls_before_touching_the_device(lib):
+    # every host check of moe_decode_forward runs before the allocation-free entry point looks up its
+    # device array or clears anything: on a machine without a GPU a call that reached the device would
+    # return MOE_ERR_CUDA instead of these codes
+    L = _layer()
+    f = lib.moe_decode_forward_noalloc
+    assert f(ctypes.byref(L), FAKE, 1, None, None, None) == B.MOE_ERR_INVALID_ARG        # null y
+    assert f(ctypes.byref(L), None, 1, FAKE, None, None) == B.MOE_ERR_INVALID_ARG        # null x
+    assert f(ctypes.byref(L), FAKE, 1, FAKE + 4, None, None) == B.MOE_ERR_MISALIGNED
+    assert f(ctypes.byref(L), FAKE, 0, FAKE, None, None) == B.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(L), FAKE, 9, FAKE, None, None) == B.MOE_ERR_UNSUPPORTED        # as moe_decode_forward
+    o = B.moe_options(1, (ctypes.c_int32 * 7)())
+    assert f(ctypes.byref(L), FAKE, 1, FAKE, ctypes.byref(o), None) == B.MOE_ERR_UNSUPPORTED
+    assert f(None, FAKE, 1, FAKE, None, None) == B.MOE_ERR_INVALID_ARG
+    big = _layer(hidden=16384, inter=8192, n_experts=1024, top_k=16)
+    assert lib.moe_workspace_size(ctypes.byref(big), 4, None) > 32 << 20
+    assert f(ctypes.byref(big), FAKE, 4, FAKE, None, None) == B.MOE_ERR_WORKSPACE
+
+
+def test_check_reports_short_workspaces(lib):
+    assert lib.moe_check(None, 16, None) == B.MOE_ERR_WORKSPACE
+    assert lib.moe_check(FAKE, 4, None) == B.MOE_ERR_WORKSPACE
