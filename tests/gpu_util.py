@@ -37,6 +37,35 @@ def device_layer(name: str, seed: int = 0):
     return _dev_cache[key]
 
 
+def sparse_host_layer(name: str, seed: int, x_bits: np.ndarray):
+    """The layer of workload `name` at `seed` with only the routed experts these tokens
+    select filled in (the others all-zero codes and scales): the router, the shared
+    expert and every selected expert are the seed's own, so the outputs for these
+    tokens equal those of the full layer, at a fraction of the generation cost."""
+    import concurrent.futures as cf
+    from oracle import moe as M
+    cfg = synth.CONFIGS[name]
+    rw = synth.normal_f32(synth.stream_key(seed, synth.KIND_ROUTER, 0, 0), cfg.E * cfg.H,
+                          synth.configs.WEIGHT_SIGMA).reshape(cfg.E, cfg.H)
+    rb = synth.zipf_bias(cfg, seed) if cfg.zipf_s else None
+    _, _, idx, _ = M.route(x_bits, rw, rb, cfg.k)
+    touched = sorted(set(int(e) for e in idx.reshape(-1)))
+
+    def empty(N, K):
+        sshape, sdt = synth.scale_shape(cfg.fmt, N, K)
+        return synth.QMat(cfg.fmt, N, K, np.zeros((cfg.E,) + synth.data_shape(cfg.fmt, N, K), np.uint8),
+                          np.zeros((cfg.E,) + sshape, sdt), np.ones(cfg.E, np.float32))
+    gate, up, down = empty(cfg.I, cfg.H), empty(cfg.I, cfg.H), empty(cfg.H, cfg.I)
+    with cf.ThreadPoolExecutor(max_workers=16) as ex:
+        for e, mats in zip(touched, ex.map(lambda e: synth.make_expert(cfg, seed, e), touched)):
+            for dst, src in zip((gate, up, down), mats):
+                dst.data[e], dst.scales[e], dst.ts[e] = src.data[0], src.scales[0], src.ts[0]
+    full = synth.make_layer(cfg.with_(E=1, k=1), seed) if cfg.shared_fmt else None
+    return synth.HostLayer(cfg, seed, rw, rb, gate, up, down,
+                           full.shared_gate if full else None, full.shared_up if full else None,
+                           full.shared_down if full else None)
+
+
 def x_device(x_bits: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).cuda()
 
@@ -116,8 +145,12 @@ def route(layer, x_bits: np.ndarray):
 
 
 def assert_routing_matches(got: dict, ref: dict, near: np.ndarray):
-    """Bit-exact indices and dispatch; logits exact except oracle-flagged near-midpoint ones."""
+    """Bit-exact indices and dispatch; logits exact except oracle-flagged near-midpoint ones.
+    At decode sizes (a few thousand logits, about 2^-15 flagged per logit) none may be flagged,
+    so every logit is compared bit for bit."""
     lg, lr = got["logits"], ref["logits"]
+    if lg.size <= 8 * 1024:
+        assert not near.any(), f"{int(near.sum())} logits within 2^-40 of an FP32 midpoint at this seed"
     diff = lg.view(np.uint32) != lr.view(np.uint32)
     assert not np.any(diff & ~near), f"{int(np.sum(diff & ~near))} logits differ from the correctly rounded value"
     np.testing.assert_array_equal(got["topk_idx"], ref["topk_idx"])
