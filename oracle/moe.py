@@ -140,11 +140,26 @@ def topk_weights_full_softmax(l32: np.ndarray, idx: np.ndarray) -> np.ndarray:
     return sel / sel.sum(axis=1, keepdims=True)
 
 
-def route(x_bits, Wr, bias, k):
-    l32, near = router_logits(x_bits, Wr, bias)
-    idx = topk(l32, k)
-    w = topk_weights(l32, idx)
-    return l32, near, idx, w
+def route(x_bits, Wr, bias, k, bias_select: bool = False):
+    """Logits, top-k and weights.  The bias (if any) is added to the FP32 logits.
+    Default: the biased logits decide both the selection and the weights.  With
+    bias_select the bias steers the selection only and the weights come from the
+    unbiased logits of the selected experts (the variant where a per-expert
+    correction balances the load without changing the mixture weights).  Returns
+    (selection logits f32, near-midpoint flags, indices, weights)."""
+    l32, near = router_logits(x_bits, Wr, None)
+    lsel = l32 if bias is None else (l32 + np.asarray(bias, dtype=np.float32)[None, :]).astype(np.float32)
+    idx = topk(lsel, k)
+    w = topk_weights(l32 if bias_select else lsel, idx)
+    return lsel, near, idx, w
+
+
+def shared_gate(x_bits, w_gate) -> np.ndarray:
+    """Sigmoid gate of the shared expert per token: sigma(g_t), g_t the correctly
+    rounded FP32 dot product of the token with the gate vector [H] (the router's
+    logit rule), sigma(z) = 1 / (1 + e^-z) in FP64."""
+    g, _ = router_logits(x_bits, np.asarray(w_gate, dtype=np.float32)[None, :])
+    return 1.0 / (1.0 + np.exp(-g[:, 0].astype(np.float64)))
 
 
 # -------------------------------------------------------------- dispatch ----
@@ -228,19 +243,24 @@ def _decoded(qm, e):
     return F.decode_qmat(qm, e)
 
 
-def layer_forward(layer, x_bits: np.ndarray, act_quant: bool = False, tokens=None, expert_cache=None):
+def layer_forward(layer, x_bits: np.ndarray, act_quant: bool = False, tokens=None, expert_cache=None,
+                  bias_select: bool = False):
     """Full MoE layer on host-resident checkpoint data (a synth.HostLayer).
 
     tokens: optional subset of token rows whose outputs are wanted (routing is
     still computed for every token, so the dispatch index is complete).
     expert_cache: optional callable e -> (Wg, Wu, Wd) FP64, to regenerate
     experts lazily instead of reading them from ``layer``.
+    bias_select: the router bias steers the selection only (see ``route``).
+    A gate vector in ``layer.extra["shared_gate_w"]`` ([H] f32) scales the
+    shared expert by its sigmoid gate (``shared_gate``); without one the shared
+    expert enters with weight 1.
     Returns a dict of every intermediate the CUDA path exposes.
     """
     cfg = layer.cfg
     x_bits = np.asarray(x_bits, dtype=np.uint16)
     T = x_bits.shape[0]
-    l32, near, idx, w = route(x_bits, layer.router_w, layer.router_b, cfg.k)
+    l32, near, idx, w = route(x_bits, layer.router_w, layer.router_b, cfg.k, bias_select)
     cnt, off, pair = dispatch(idx, cfg.E)
     want = np.arange(T) if tokens is None else np.asarray(sorted(set(int(t) for t in tokens)))
     X = F.bf16_to_f64(x_bits)
@@ -266,6 +286,9 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: bool = False, tokens=Non
         Wg, Wu, Wd = (_decoded(layer.shared_gate, 0), _decoded(layer.shared_up, 0),
                       _decoded(layer.shared_down, 0))
         _, S = swiglu_mlp(Wg, Wu, Wd, X[want], act_quant)
+        gw = getattr(layer, "extra", {}).get("shared_gate_w")
+        if gw is not None:
+            S = S * shared_gate(x_bits[want], gw)[:, None]
     y = np.zeros((len(want), cfg.H))
     for i, t in enumerate(want):
         y[i] = acc[int(t)] + (S[i] if S is not None else 0.0)

@@ -105,6 +105,26 @@ def test_shared_expert_adds_plain_mlp(shared_fmt):
     assert np.allclose(with_shared["y_f64"] - without["y_f64"], S, rtol=1e-12, atol=1e-12)
 
 
+def test_sigmoid_gated_shared_expert():
+    # with a gate vector the shared expert enters scaled by sigmoid(x . w_gate), computed here with torch
+    # float64 (the dot of BF16 x FP32 values is exact in FP64, so its FP32 rounding is unambiguous)
+    cfg = _small(FMT_NVFP4, FMT_INT8_G64, E=4, k=2, H=128, I=128)
+    lay = synth.make_layer(cfg, seed=10)
+    x = synth.make_tokens(cfg, 5, seed=10)
+    base = M.layer_forward(lay, x)
+    gw = (np.random.default_rng(10).standard_normal(cfg.H) * 0.1).astype(np.float32)
+    lay_g = synth.HostLayer(cfg, lay.seed, lay.router_w, lay.router_b, lay.gate, lay.up, lay.down,
+                            lay.shared_gate, lay.shared_up, lay.shared_down, extra={"shared_gate_w": gw})
+    gated = M.layer_forward(lay_g, x)
+    X = torch.from_numpy(F.bf16_to_f64(x))
+    g = (X @ torch.from_numpy(gw.astype(np.float64))).to(torch.float32).to(torch.float64)
+    sig = torch.sigmoid(g).numpy()
+    S = _torch_mlp(_torch_decode(lay.shared_gate), _torch_decode(lay.shared_up), _torch_decode(lay.shared_down),
+                   X).numpy()
+    assert np.allclose(gated["y_f64"] - base["y_f64"], (sig[:, None] - 1.0) * S, rtol=1e-10, atol=1e-12)
+    assert np.array_equal(gated["topk_idx"], base["topk_idx"])
+
+
 def test_identical_experts_top2_equals_top1():
     cfg1 = _small(FMT_NVFP4, E=1, k=1)
     lay1 = synth.make_layer(cfg1, seed=5)
@@ -307,7 +327,12 @@ def _router_logits_bound_mask(x_bits, Wr, bias=None):
     return l32, M.midpoint_distance(d, l0) <= 2.0 ** -40 * np.abs(d) + bound
 
 
-_ORIG = {"dispatch": M.dispatch, "decode": F.decode, "swiglu": M.swiglu_mlp, "router_logits": M.router_logits}
+def _route_bias_always_weighs(x_bits, Wr, bias, k, bias_select=False):
+    return _ORIG["route"](x_bits, Wr, bias, k, False)
+
+
+_ORIG = {"dispatch": M.dispatch, "decode": F.decode, "swiglu": M.swiglu_mlp, "router_logits": M.router_logits,
+         "route": M.route, "shared_gate": M.shared_gate}
 
 
 def test_planted_mistakes_are_caught(monkeypatch):
@@ -337,6 +362,11 @@ def test_planted_mistakes_are_caught(monkeypatch):
                            [(TR.test_near_midpoint_mask_flags_only_the_window, 1.0)]),
         "mask widened by the FP64 error bound": (M, "router_logits", _router_logits_bound_mask,
                                                  [(TR.test_near_midpoint_mask_empty_at_the_decode_seeds,)]),
+        "bias weighs the mixture in bias_select mode": (M, "route", _route_bias_always_weighs,
+                                                        [(TR.test_bias_select_routes_by_biased_and_weighs_by_unbiased,
+                                                          8, 2)]),
+        "shared gate sign (sigmoid(-g))": (M, "shared_gate", lambda x, w: 1.0 - _ORIG["shared_gate"](x, w),
+                                           [(test_sigmoid_gated_shared_expert,)]),
         "shared expert dropped": (M, "swiglu_mlp", lambda Wg, Wu, Wd, X, act_quant=False: (
             lambda h, P: (h, P * (Wg.shape[0] != 128)))(*_ORIG["swiglu"](Wg, Wu, Wd, X, act_quant)),
             [(test_shared_expert_adds_plain_mlp, FMT_FP8_B128)]),

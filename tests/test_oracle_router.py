@@ -180,3 +180,26 @@ def test_near_midpoint_fraction_matches_its_width():
     W = (rng.standard_normal((2048, 256)) * 0.02).astype(np.float32)
     _, near = M.router_logits(x, W)
     assert int(near.sum()) <= 32                                   # 131072 logits, about 4 expected
+
+
+# ------------------------------------------------- bias for selection only ----
+
+@pytest.mark.parametrize("E,k", [(8, 2), (12, 4)])
+def test_bias_select_routes_by_biased_and_weighs_by_unbiased(E, k):
+    # selection: brute force over every k-subset of the biased FP32 logits; weights: a softmax over all
+    # unbiased logits renormalised over the selected experts (the shared denominator cancels)
+    rng = np.random.default_rng(40 + E)
+    x = _bf16_bits_random(rng, (6, 64))
+    W = (rng.standard_normal((E, 64)) * 0.05).astype(np.float32)
+    b = (rng.standard_normal(E) * 0.5).astype(np.float32)
+    lsel, _, idx, w = M.route(x, W, b, k, bias_select=True)
+    l0, _ = M.router_logits(x, W)
+    assert np.array_equal(lsel, (l0 + b[None, :]).astype(np.float32))
+    for t in range(x.shape[0]):
+        assert list(idx[t]) == _brute_topk(lsel[t], k)
+    p = np.exp(l0.astype(np.float64) - l0.max(axis=1, keepdims=True))
+    sel = np.take_along_axis(p, idx.astype(np.int64), axis=1)
+    assert np.allclose(w.astype(np.float64), sel / sel.sum(axis=1, keepdims=True), rtol=2 ** -23, atol=0)
+    # the default mode weighs by the biased logits: a different result whenever the bias is not constant
+    _, _, idx_d, w_d = M.route(x, W, b, k)
+    assert np.array_equal(idx_d, idx) and not np.allclose(w_d, w)
