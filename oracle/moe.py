@@ -244,7 +244,7 @@ def _decoded(qm, e):
 
 
 def layer_forward(layer, x_bits: np.ndarray, act_quant: bool = False, tokens=None, expert_cache=None,
-                  bias_select: bool = False):
+                  bias_select: bool = False, bf16_partials: bool = False):
     """Full MoE layer on host-resident checkpoint data (a synth.HostLayer).
 
     tokens: optional subset of token rows whose outputs are wanted (routing is
@@ -252,6 +252,10 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: bool = False, tokens=Non
     expert_cache: optional callable e -> (Wg, Wu, Wd) FP64, to regenerate
     experts lazily instead of reading them from ``layer``.
     bias_select: the router bias steers the selection only (see ``route``).
+    bf16_partials: every expert's down-projection output (the routed partials
+    and the shared expert's) is rounded to BF16 before the weighted sum (page
+    3 README "Execution and performance", engine.prefill_bf16_partials, a
+    lever off by default).
     A gate vector in ``layer.extra["shared_gate_w"]`` ([H] f32) scales the
     shared expert by its sigmoid gate (``shared_gate``); without one the shared
     expert enters with weight 1.
@@ -277,6 +281,8 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: bool = False, tokens=Non
             Wg, Wu, Wd = _decoded(layer.gate, e), _decoded(layer.up, e), _decoded(layer.down, e)
         rows = np.array([p // cfg.k for p in ps])
         h, P = swiglu_mlp(Wg, Wu, Wd, X[rows], act_quant)
+        if bf16_partials:
+            P = F.round_bf16(P)
         for i, p in enumerate(ps):
             t, j = divmod(p, cfg.k)
             acc[t] += float(w[t, j]) * P[i]
@@ -286,6 +292,8 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: bool = False, tokens=Non
         Wg, Wu, Wd = (_decoded(layer.shared_gate, 0), _decoded(layer.shared_up, 0),
                       _decoded(layer.shared_down, 0))
         _, S = swiglu_mlp(Wg, Wu, Wd, X[want], act_quant)
+        if bf16_partials:
+            S = F.round_bf16(S)
         gw = getattr(layer, "extra", {}).get("shared_gate_w")
         if gw is not None:
             S = S * shared_gate(x_bits[want], gw)[:, None]

@@ -125,6 +125,26 @@ def test_sigmoid_gated_shared_expert():
     assert np.array_equal(gated["topk_idx"], base["topk_idx"])
 
 
+def test_bf16_partials_round_each_expert_output():
+    # the lever: y = bf16( sum_j w_j bf16(P_j) + bf16(S) ), each P_j from an independent torch float64 MLP
+    cfg = _small(FMT_NVFP4, FMT_FP8_B128, E=5, k=3, H=128, I=128)
+    lay = synth.make_layer(cfg, seed=12)
+    x = synth.make_tokens(cfg, 6, seed=12)
+    out = M.layer_forward(lay, x, bf16_partials=True)
+    X = torch.from_numpy(F.bf16_to_f64(x))
+    S = _torch_mlp(_torch_decode(lay.shared_gate), _torch_decode(lay.shared_up), _torch_decode(lay.shared_down),
+                   X).numpy()
+    y = F.round_bf16(S)
+    for t in range(x.shape[0]):
+        for j in range(cfg.k):
+            e = int(out["topk_idx"][t, j])
+            P = _torch_mlp(_torch_decode(lay.gate, e), _torch_decode(lay.up, e), _torch_decode(lay.down, e),
+                           X[t:t + 1]).numpy()[0]
+            y[t] += float(out["topk_w"][t, j]) * F.round_bf16(P)
+    assert np.allclose(out["y_f64"], y, rtol=1e-12, atol=1e-14)
+    assert not np.array_equal(out["y_f64"], M.layer_forward(lay, x)["y_f64"])
+
+
 def test_identical_experts_top2_equals_top1():
     cfg1 = _small(FMT_NVFP4, E=1, k=1)
     lay1 = synth.make_layer(cfg1, seed=5)
@@ -332,7 +352,7 @@ def _route_bias_always_weighs(x_bits, Wr, bias, k, bias_select=False):
 
 
 _ORIG = {"dispatch": M.dispatch, "decode": F.decode, "swiglu": M.swiglu_mlp, "router_logits": M.router_logits,
-         "route": M.route, "shared_gate": M.shared_gate}
+         "route": M.route, "shared_gate": M.shared_gate, "layer_forward": M.layer_forward}
 
 
 def test_planted_mistakes_are_caught(monkeypatch):
@@ -367,6 +387,8 @@ def test_planted_mistakes_are_caught(monkeypatch):
                                                           8, 2)]),
         "shared gate sign (sigmoid(-g))": (M, "shared_gate", lambda x, w: 1.0 - _ORIG["shared_gate"](x, w),
                                            [(test_sigmoid_gated_shared_expert,)]),
+        "bf16 partials not rounded": (M, "layer_forward", lambda *a, **kw: _ORIG["layer_forward"](
+            *a, **{**kw, "bf16_partials": False}), [(test_bf16_partials_round_each_expert_output,)]),
         "shared expert dropped": (M, "swiglu_mlp", lambda Wg, Wu, Wd, X, act_quant=False: (
             lambda h, P: (h, P * (Wg.shape[0] != 128)))(*_ORIG["swiglu"](Wg, Wu, Wd, X, act_quant)),
             [(test_shared_expert_adds_plain_mlp, FMT_FP8_B128)]),
