@@ -43,11 +43,12 @@ METRIC = "MoE-layer weight GB/s & tokens/s at batch 1/8; % of HBM (decode) / FP4
 WORKLOAD = "decode_nvfp4"
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up launch at batch 8 on the
-# decode_nvfp4 workload, from one ncu capture of the current kernel (read 91.86 MB, write 2.36 MB);
-# None once the kernel changes, until the counters are taken again.
-GATEUP_TRAFFIC_BYTES = 94_224_128
-# kernels one decode layer call launches: router, gate/up, down, combine
-DECODE_KERNELS_PER_CALL = 4
+# decode_nvfp4 workload, from one ncu capture of the current kernel; None while the kernel has
+# changed since the counters were taken.
+GATEUP_TRAFFIC_BYTES = None
+# kernels one decode layer call launches: router (approximate logits, exact selection + dispatch),
+# gate/up, down, combine
+DECODE_KERNELS_PER_CALL = 5
 
 
 def _peaks():
@@ -160,6 +161,184 @@ def _bytes_per_call(host, cnt_rows):
     return [fixed + int(np.count_nonzero(c)) * per_expert for c in cnt_rows]
 
 
+def _clone_layer(q, base):
+    def clone(qw):
+        return q.QWeight(qw.data.clone(), qw.scales.clone(),
+                         None if qw.tensor_scale is None else qw.tensor_scale.clone())
+    return q.Layer(base.hidden, base.inter, base.n_experts, base.top_k, base.fmt, base.router_w.clone(),
+                   None if base.router_bias is None else base.router_bias.clone(), clone(base.gate),
+                   clone(base.up), clone(base.down), base.shared_fmt, base.shared_inter,
+                   clone(base.shared_gate) if base.shared_gate else None,
+                   clone(base.shared_up) if base.shared_up else None,
+                   clone(base.shared_down) if base.shared_down else None)
+
+
+def _median_replays(torch, graph, stream, n):
+    """Replay `graph` n times on `stream`, each bracketed by its own CUDA events; ms per replay."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def measure_decode(args, name, batches, world, rank, local, dist, peak, peak_kind, headline_T=None):
+    """One decode workload: per batch size, K consecutive layer calls (one CUDA graph, rotating
+    R layer copies and NB token batches) timed as one measurement, replayed at least 20 times;
+    the median replay gives the per-call time.  Per-kernel times come from a second graph with
+    event-record nodes between the kernels."""
+    import torch
+    import quantized_moe_decode_router_gb300 as q
+    cfg = synth.CONFIGS[name]
+    t0 = time.time()
+    host = synth.make_layer(cfg, seed=rank)
+    gen_s = time.time() - t0
+    base = q.to_device(host, f"cuda:{local}")
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    Tmax = max(batches)
+    fixed = host.router_bytes() + host.shared_bytes()
+    min_call = fixed + min(cfg.k, cfg.E) * host.expert_bytes()
+    layer_bytes = fixed + cfg.E * host.expert_bytes()
+    R = args.instances or max(2, min(-(-3 * l2 // min_call), int(args.mem_gb * 1e9 // layer_bytes)))
+    layers = [base] + [_clone_layer(q, base) for _ in range(R - 1)]
+    NB = args.token_batches
+    K = max(1, min(args.steps, 1024))
+    stream = torch.cuda.Stream()
+    per_exp_gu = sum(m.nbytes() // m.E for m in (host.gate, host.up))
+    per_exp_dn = host.down.nbytes() // host.down.E
+    s_gu = (host.shared_gate.nbytes() + host.shared_up.nbytes()) if host.shared_gate else 0
+    s_dn = host.shared_down.nbytes() if host.shared_gate else 0
+    results, extra = {}, {}
+    for T in batches:
+        xs = [torch.from_numpy(synth.make_tokens(cfg, T, seed=1000 + rank, batch=i).view(np.int16)).cuda()
+              for i in range(NB)]
+        ys = torch.zeros((T, cfg.H), dtype=torch.int16, device="cuda")
+        ws = torch.empty(q.workspace_size(base, Tmax), dtype=torch.uint8, device="cuda")
+        q.workspace_init(ws)
+        # the library's own routing of every token batch -> touched experts -> algorithmic bytes
+        cnt = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
+        cnts = []
+        for i in range(NB):
+            q.moe_route(base, xs[i], T, expert_cnt=cnt, ws=ws)
+            cnts.append(cnt.cpu().numpy().copy())
+        touched = [int(np.count_nonzero(c)) for c in cnts]
+        bytes_b = [fixed + n * host.expert_bytes() for n in touched]
+        torch.cuda.synchronize()
+
+        def call(i, s):
+            q.moe_decode_forward(layers[i % R], xs[i % NB], T, ys, ws, stream=s)
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                call(i, stream)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(K):
+                    call(i, stream)
+        bytes_graph = sum(bytes_b[i % NB] for i in range(K))
+        warm = max(3, -(-args.warmup // K))
+        _median_replays(torch, g, stream, warm)
+        reps = max(20, args.replays)
+        headline = T == headline_T
+        sampler = ClockSampler(local) if headline else None
+        if sampler:
+            sampler.start()
+            time.sleep(0.3)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ms_list = _median_replays(torch, g, stream, reps)
+        if dist:
+            dist.barrier()
+        if sampler:
+            extra["clocks"] = sampler.stop()
+        ms_med = statistics.median(ms_list)
+        ms_all, total_bytes = aggregate_ranks(ms_med, float(bytes_graph), dist, "cuda")
+        us_call = ms_all * 1e3 / K
+        gbs = total_bytes / (ms_all * 1e-3) / 1e9
+        res = {"us_per_layer": round(us_call, 3), "weight_GBps": round(gbs, 1),
+               "tokens_per_s": round(world * T * K / (ms_all * 1e-3), 1), "hbm_frac": round(gbs / world / peak, 4),
+               "bytes_per_layer": int(np.mean(bytes_b)), "experts_touched": round(float(np.mean(touched)), 1),
+               "steps": K, "replays": reps,
+               "us_per_layer_min_max": [round(min(ms_list) * 1e3 / K, 3), round(max(ms_list) * 1e3 / K, 3)]}
+        # per-kernel times: event-record nodes between the kernels of each call
+        n = 64
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+        for row in evs:          # create the CUDA events (torch creates them lazily on first record)
+            for e in row:
+                e.record(stream)
+        torch.cuda.synchronize()
+        gt = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gt, stream=stream):
+            for i in range(n):
+                q.moe_decode_forward_timed(layers[i % R], xs[i % NB], T, ys, ws, evs[i], stream=stream)
+        for _ in range(2):
+            with torch.cuda.stream(stream):
+                gt.replay()
+        torch.cuda.synchronize()
+        dur = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)] for i in range(n)])
+        avg = dur.mean(axis=0) * 1e3  # us per launch: router (both stages), gate/up, down + combine
+        gu_bytes = float(np.mean([touched[i % NB] * per_exp_gu + s_gu for i in range(n)]))
+        dn_bytes = float(np.mean([touched[i % NB] * per_exp_dn + s_dn for i in range(n)]))
+        rt_bytes = host.router_bytes()
+        res["kernel_us"] = {"router": round(avg[0], 3), "gateup": round(avg[1], 3), "down_combine": round(avg[2], 3)}
+        res["kernel_hbm_frac"] = {"router": round(rt_bytes / (avg[0] * 1e-6) / 1e9 / peak, 4),
+                                  "gateup": round(gu_bytes / (avg[1] * 1e-6) / 1e9 / peak, 4),
+                                  "down_combine": round(dn_bytes / (avg[2] * 1e-6) / 1e9 / peak, 4)}
+        results[T] = res
+        if headline:
+            ach = gu_bytes / (avg[1] * 1e-6) / 1e9
+            extra["roofline"] = {
+                "kernel": "gateup_kernel (decode gate/up + SwiGLU GEMV)", "bound": "hbm", "achieved": round(ach, 1),
+                "peak": peak, "peak_kind": f"{peak_kind} (HBM copy, burst)", "unit": "GB/s",
+                "frac": round(ach / peak, 4), "traffic": GATEUP_TRAFFIC_BYTES, "bytes_per_launch": int(gu_bytes),
+                "kernel_us": res["kernel_us"]}
+            # end to end through the public API with host buffers (pinned): K steps per measurement,
+            # each step copies its tokens in and its output back
+            xh = [torch.from_numpy(synth.make_tokens(cfg, T, seed=2000 + rank, batch=i).view(np.int16)).pin_memory()
+                  for i in range(NB)]
+            yh = torch.empty((T, cfg.H), dtype=torch.int16).pin_memory()
+            xd = torch.empty((T, cfg.H), dtype=torch.int16, device="cuda")
+
+            def e2e_steps(nsteps):
+                for i in range(nsteps):
+                    xd.copy_(xh[i % NB], non_blocking=True)
+                    q.moe_decode_forward(layers[i % R], xd, T, ys, ws)
+                    yh.copy_(ys, non_blocking=True)
+            e2e_steps(3)
+            torch.cuda.synchronize()
+            e_ms = []
+            for _ in range(5):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                e2e_steps(K)
+                e1.record()
+                torch.cuda.synchronize()
+                e_ms.append(e0.elapsed_time(e1))
+            ems = statistics.median(e_ms)
+            eb = sum(bytes_b[i % NB] for i in range(K))
+            extra["e2e"] = {"value": round(eb / (ems * 1e-3) / 1e9, 1), "unit": "GB/s", "steps": K,
+                            "us_per_step": round(ems * 1e3 / K, 2), "tokens_per_s": round(T * K / (ems * 1e-3), 1),
+                            "h2d_bytes_per_step": T * cfg.H * 2, "d2h_bytes_per_step": T * cfg.H * 2,
+                            "measurements": 5, "statistic": "median"}
+        del g, gt
+        torch.cuda.synchronize()
+    st = q.moe_check(ws)
+    if st != 0:
+        raise RuntimeError(f"device-side error: {q.status_string(st)}")
+    info = {"workload": workload_name(cfg), "instances_rotated": R,
+            "l2": f"inputs larger than L2: {R} layer copies rotated, at least {R * min_call / 1e6:.0f} MB "
+                  f"touched per rotation vs L2 {l2 / 1e6:.0f} MB",
+            "layer_gen_s": round(gen_s, 1), "batches": {str(T): r for T, r in results.items()}}
+    del layers, base
+    torch.cuda.empty_cache()
+    return info, extra
+
+
 def run_ours(args, world, rank, local):
     import torch
     import quantized_moe_decode_router_gb300 as q
@@ -173,174 +352,33 @@ def run_ours(args, world, rank, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    cfg = synth.CONFIGS[args.workload]
-    t0 = time.time()
-    host = synth.make_layer(cfg, seed=rank)
-    gen_s = time.time() - t0
-    base = q.to_device(host, f"cuda:{local}")
-    l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    batches = [int(b) for b in args.batches.split(",")]
-    Tmax = max(batches)
-    fixed = host.router_bytes() + host.shared_bytes()
-    min_call = fixed + min(cfg.k, cfg.E) * host.expert_bytes()
-    R = args.instances or max(2, -(-3 * l2 // min_call))
-    layers = [base]
-
-    def clone(qw):
-        return q.QWeight(qw.data.clone(), qw.scales.clone(),
-                         None if qw.tensor_scale is None else qw.tensor_scale.clone())
-    for _ in range(R - 1):
-        L = q.Layer(base.hidden, base.inter, base.n_experts, base.top_k, base.fmt, base.router_w.clone(),
-                    None if base.router_bias is None else base.router_bias.clone(), clone(base.gate),
-                    clone(base.up), clone(base.down), base.shared_fmt, base.shared_inter,
-                    clone(base.shared_gate) if base.shared_gate else None,
-                    clone(base.shared_up) if base.shared_up else None,
-                    clone(base.shared_down) if base.shared_down else None)
-        layers.append(L)
-    NB = args.token_batches
-    stream = torch.cuda.Stream()
-    results = {}
     peak, peak_kind = _peaks()
-    clocks = None
-    roof = None
-    e2e = None
-    for T in batches:
-        xs = [torch.from_numpy(synth.make_tokens(cfg, T, seed=1000 + rank, batch=i).view(np.int16)).cuda()
-              for i in range(NB)]
-        ys = torch.zeros((T, cfg.H), dtype=torch.int16, device="cuda")
-        ws = torch.empty(q.workspace_size(base, Tmax), dtype=torch.uint8, device="cuda")
-        q.workspace_init(ws)
-        # per-batch routing (the library's own) -> distinct experts -> algorithmic bytes
-        cnt = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
-        cnts = []
-        for i in range(NB):
-            q.moe_route(base, xs[i], T, expert_cnt=cnt, ws=ws)
-            cnts.append(cnt.cpu().numpy().copy())
-        bytes_b = _bytes_per_call(host, cnts)
-        torch.cuda.synchronize()
-
-        def call(i, s=None):
-            q.moe_decode_forward(layers[i % R], xs[i % NB], T, ys, ws, stream=s)
-
-        # capture one graph of G calls (rotating instances and batches); replay it
-        G = min(512, -(-max(R, NB) // R) * R)   # a whole number of rotations, >= NB batches
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            for i in range(3):
-                call(i, stream)
-            stream.synchronize()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(G):
-                    call(i, stream)
-        bytes_graph = sum(bytes_b[i % NB] for i in range(G))
-        steps = args.steps if T == batches[-1] else max(G, args.steps // 4)
-        reps = max(1, steps // G)
-        steps = reps * G
-        warm = max(1, args.warmup // G)
-        with torch.cuda.stream(stream):          # replay on the stream the timing events use
-            for _ in range(warm):
-                g.replay()
-        torch.cuda.synchronize()
-        headline = T == batches[-1]
-        sampler = ClockSampler(local) if headline else None
-        if sampler:
-            sampler.start()
-            time.sleep(0.3)
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            ev1.record(stream)
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        ms = ev0.elapsed_time(ev1)
-        if sampler:
-            clocks = sampler.stop()
-        ms, total_bytes = aggregate_ranks(ms, float(bytes_graph * reps), dist, "cuda")
-        us_call = ms * 1e3 / steps
-        gbs = total_bytes / (ms * 1e-3) / 1e9
-        toks = world * T * steps / (ms * 1e-3)
-        results[T] = {"us_per_layer": round(us_call, 3), "weight_GBps": round(gbs, 1),
-                      "tokens_per_s": round(toks, 1), "hbm_frac": round(gbs / world / peak, 4),
-                      "bytes_per_layer": int(np.mean(bytes_b)), "steps": steps}
-        # per-kernel live CUDA-event timing on the launch stream (every batch size; the
-        # headline batch also gives the roofline of the dominant kernel, gate/up)
-        if True:
-            n = min(256, max(32, steps // 8))
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
-            for row in evs:          # create the CUDA events (torch creates them lazily on first record)
-                for e in row:
-                    e.record(stream)
-            torch.cuda.synchronize()
-            gt = torch.cuda.CUDAGraph()         # event-record nodes between the kernels, no host gaps
-            with torch.cuda.graph(gt, stream=stream):
-                for i in range(n):
-                    q.moe_decode_forward_timed(layers[i % R], xs[i % NB], T, ys, ws, evs[i], stream=stream)
-            with torch.cuda.stream(stream):
-                gt.replay()
-            torch.cuda.synchronize()
-            dur = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)] for i in range(n)])
-            avg = dur.mean(axis=0) * 1e3  # us per launch: router, gate/up, down
-            per_exp_gu = sum(m.nbytes() // m.E for m in (host.gate, host.up))
-            s_gu = (host.shared_gate.nbytes() + host.shared_up.nbytes()) if host.shared_gate else 0
-            gu_bytes = np.mean([int(np.count_nonzero(cnts[i % NB])) * per_exp_gu + s_gu for i in range(n)])
-            ach = gu_bytes / (avg[1] * 1e-6) / 1e9
-            results[T]["kernel_us"] = {"router": round(avg[0], 3), "gateup": round(avg[1], 3), "down": round(avg[2], 3)}
-        if headline:
-            roof = {"kernel": "gateup_decode_kernel", "bound": "hbm", "achieved": round(ach, 1),
-                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(ach / peak, 4),
-                    "traffic": GATEUP_TRAFFIC_BYTES, "bytes_per_launch": int(gu_bytes),
-                    "kernel_us": {"router": round(avg[0], 3), "gateup": round(avg[1], 3), "down": round(avg[2], 3)}}
-            # end to end through the public API with host buffers (pinned), one call per step
-            ne = min(steps, args.e2e_steps)
-            xh = [torch.from_numpy(synth.make_tokens(cfg, T, seed=2000 + rank, batch=i).view(np.int16)).pin_memory()
-                  for i in range(min(NB, ne))]
-            yh = torch.empty((T, cfg.H), dtype=torch.int16).pin_memory()
-            xd = torch.empty((T, cfg.H), dtype=torch.int16, device="cuda")
-            for i in range(3):
-                xd.copy_(xh[i % len(xh)], non_blocking=True)
-                q.moe_decode_forward(layers[i % R], xd, T, ys, ws)
-                yh.copy_(ys, non_blocking=True)
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for i in range(ne):
-                xd.copy_(xh[i % len(xh)], non_blocking=True)
-                q.moe_decode_forward(layers[i % R], xd, T, ys, ws)
-                yh.copy_(ys, non_blocking=True)
-            e1.record()
-            torch.cuda.synchronize()
-            ems = e0.elapsed_time(e1)
-            eb = sum(bytes_b[i % NB] for i in range(ne))
-            e2e = {"value": round(eb / (ems * 1e-3) / 1e9, 1), "unit": "GB/s", "steps": ne,
-                   "us_per_step": round(ems * 1e3 / ne, 2), "tokens_per_s": round(T * ne / (ems * 1e-3), 1),
-                   "h2d_bytes_per_step": T * cfg.H * 2, "d2h_bytes_per_step": T * cfg.H * 2}
-        del g
-        torch.cuda.synchronize()
-    st = q.moe_check(ws)
-    if st != 0:
-        raise RuntimeError(f"device-side error: {q.status_string(st)}")
-    Th = batches[-1]
-    head = results[Th]
+    batches = [int(b) for b in args.batches.split(",")]
+    Th = max(batches)
+    head, extra = measure_decode(args, args.workload, batches, world, rank, local, dist, peak, peak_kind, Th)
+    others = {}
+    for name in [w for w in args.more_workloads.split(",") if w and w != args.workload]:
+        cfg = synth.CONFIGS[name]
+        others[name], _ = measure_decode(args, name, list(cfg.batches), world, rank, local, dist, peak, peak_kind)
+    hb = head["batches"][str(Th)]
     out = {
-        "metric": METRIC, "value": head["weight_GBps"], "unit": "GB/s", "n_gpus": world,
-        "steps": head["steps"], "warmup": args.warmup, "ms_per_step": round(head["us_per_layer"] / 1e3, 6),
+        "metric": METRIC, "value": hb["weight_GBps"], "unit": "GB/s", "n_gpus": world,
+        "steps": hb["steps"], "warmup": args.warmup, "ms_per_step": round(hb["us_per_layer"] / 1e3, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,0.02) weights quantised NVFP4 / FP8 b128; N(0,1) bf16 tokens)",
-        "config": {"workload": workload_name(cfg, Th),
-                   "batch_tokens": Th, "instances_rotated": R,
-                   "l2": f"inputs larger than L2: {R} layer copies rotated, "
-                         f"{R * min_call / 1e6:.0f} MB touched per rotation vs L2 {l2 / 1e6:.0f} MB",
-                   "graph": f"CUDA graph of {G} layer calls replayed", "parallelism": "replicas" if world > 1 else "1 GPU",
-                   "gpu": dev_name, "layer_gen_s": round(gen_s, 1)},
-        "tokens_per_s": head["tokens_per_s"], "hbm_frac": head["hbm_frac"],
-        "batches": {str(T): r for T, r in results.items()},
-        "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": DECODE_KERNELS_PER_CALL * head["steps"],
+        "data": f"synthetic ({DATA_DESC[args.workload]}; N(0,1) bf16 tokens; seeded)",
+        "config": {"workload": f"{head['workload']}, batch {Th} tokens", "batch_tokens": Th,
+                   "instances_rotated": head["instances_rotated"], "l2": head["l2"],
+                   "timing": f"one measurement = one CUDA graph of {hb['steps']} consecutive layer calls "
+                             f"(K = --steps); median of {hb['replays']} measurements",
+                   "parallelism": "replicas" if world > 1 else "1 GPU", "gpu": dev_name,
+                   "layer_gen_s": head["layer_gen_s"]},
+        "tokens_per_s": hb["tokens_per_s"], "hbm_frac": hb["hbm_frac"],
+        "batches": head["batches"],
+        "workloads": {name: {"workload": o["workload"], "data": DATA_DESC[name], "batches": o["batches"],
+                             "instances_rotated": o["instances_rotated"], "l2": o["l2"]}
+                      for name, o in others.items()},
+        "roofline": extra.get("roofline"), "clocks": extra.get("clocks"), "e2e": extra.get("e2e"),
+        "gpu_launches": DECODE_KERNELS_PER_CALL * hb["steps"],
     }
     return out
 
@@ -377,15 +415,9 @@ def run_prefill(args, local, peak_bf16, peak_kind):
         for _ in range(2):
             g.replay()
     torch.cuda.synchronize()
-    reps = max(1, args.prefill_steps // G)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / (reps * G)
+    reps = max(20, args.prefill_steps // G)
+    ms_list = _median_replays(torch, g, stream, reps)
+    us = statistics.median(ms_list) * 1e3 / G
     # per-kernel times: event-record nodes between the launches
     n = 6
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n)]
@@ -419,13 +451,8 @@ def run_prefill(args, local, peak_bf16, peak_kind):
         for _ in range(2):
             g4.replay()
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
-            g4.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    us4 = e0.elapsed_time(e1) * 1e3 / (reps * G)
+    ms4_list = _median_replays(torch, g4, stream, reps)
+    us4 = statistics.median(ms4_list) * 1e3 / G
     evs4 = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n)]
     for row in evs4:
         for e in row:
@@ -448,7 +475,8 @@ def run_prefill(args, local, peak_bf16, peak_kind):
     tflops4 = flops / (gemm4_us * 1e-6) / 1e12
     gemm_us = dur[3] + dur[5]
     tflops = flops / (gemm_us * 1e-6) / 1e12
-    fp4_peak = peak_bf16 * 13.5 / 2.25
+    fp4_peak = peak_bf16 * 13.5 / 2.25   # derived: the measured dense bf16 peak x the nominal FP4/bf16 ratio
+    fp4_kind = f"derived: {peak_kind} bf16 burst {peak_bf16} TFLOP/s x 13.5/2.25 (nominal dense FP4/bf16)"
     wbytes = host.router_bytes() + np.mean(touched) * host.expert_bytes()
     return {
         "workload": f"prefill_nvfp4: NVFP4 MoE layer H={cfg.H} E={cfg.E} top-{cfg.k} I={cfg.I}, {T} tokens, "
@@ -460,94 +488,73 @@ def run_prefill(args, local, peak_bf16, peak_kind):
                  "flops_per_layer": flops, "achieved_tflops": round(tflops, 1),
                  "frac_f16_peak": round(tflops / peak_bf16, 4), "f16_peak_tflops": peak_bf16,
                  "frac_fp4_peak": round(tflops / fp4_peak, 4), "fp4_peak_tflops": round(fp4_peak, 1),
-                 "peak_kind": peak_kind},
+                 "peak_kind": peak_kind, "fp4_peak_kind": fp4_kind},
         "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
-        "graph": f"CUDA graph of {G} layer calls, {reps} replays",
+        "graph": f"CUDA graph of {G} layer calls; median of {reps} replays",
         "w4a4": {"path": "NVFP4 activations (lever, act_quant=1): tcgen05 kind::mxf4nvf4 block-scaled GEMMs",
                  "us_per_layer": round(us4, 1), "tokens_per_s": round(T / (us4 * 1e-6), 1),
                  "kernel_us": {k: round(float(v), 2) for k, v in zip(
                      ["router_logits", "router_topk", "dispatch_quantise", "gateup_gemm", "-", "down_gemm",
                       "combine"], dur4) if k != "-"},
                  "achieved_tflops": round(tflops4, 1), "frac_fp4_peak": round(tflops4 / fp4_peak, 4),
-                 "fp4_peak_tflops": round(fp4_peak, 1), "peak_kind": peak_kind},
+                 "fp4_peak_tflops": round(fp4_peak, 1), "peak_kind": fp4_kind},
     }
 
 
-def workload_name(cfg, T: int) -> str:
-    return (f"{cfg.name}: NVFP4 MoE layer H={cfg.H} E={cfg.E} top-{cfg.k} I={cfg.I} "
-            f"+ FP8 b128 shared expert I={cfg.shared_I}, batch {T} tokens")
+FMT_TEXT = {1: "NVFP4", 2: "MXFP4", 3: "int4 g64", 4: "int8 g64", 5: "FP8 b128"}
+DATA_DESC = {
+    "tiny_nvfp4": "N(0,0.02) weights quantised NVFP4",
+    "decode_nvfp4": "N(0,0.02) weights quantised NVFP4 routed / FP8 b128 shared",
+    "decode_mxfp4": "N(0,0.02) weights quantised MXFP4",
+    "decode_int4": "N(0,0.02) weights quantised int4 g64 routed / int8 g64 shared",
+    "prefill_nvfp4": "N(0,0.02) weights quantised NVFP4, Zipf router bias s=1.1",
+}
 
 
-def run_reference(args):
-    """The oracle, as it stands, timed on the host cores.  One step is one piece
-    of a batch-T layer call, in layer order: the router (exact logits, top-k,
-    dispatch), the shared expert, then each routed expert segment (its gate, up
-    and down decoded to FP64, the SwiGLU MLP on its token rows, the weighted
-    add into the outputs); successive token batches follow one another, so K
-    steps cover whole layer calls in proportion.  value = weight bytes of the
-    timed pieces / time, the metric of the GPU arm."""
-    from oracle import formats as F
+def workload_name(cfg) -> str:
+    shared = (f" + {FMT_TEXT[cfg.shared_fmt]} shared expert I={cfg.shared_I}" if cfg.shared_fmt else "")
+    return f"{cfg.name}: {FMT_TEXT[cfg.fmt]} MoE layer H={cfg.H} E={cfg.E} top-{cfg.k} I={cfg.I}{shared}"
+
+
+def run_reference(args, seconds_budget: float = 180.0):
+    """The oracle, as it stands, timed on the host cores, on the GPU arm's headline
+    workload and metric: one step is one whole layer call on one batch of T tokens (the
+    router with exact logits, top-k and dispatch, the shared expert, every routed expert
+    segment, the weighted combine), successive steps on successive token batches.  W
+    untimed steps, then K timed ones, stopping early if the timed steps exceed
+    `seconds_budget` (the line reports the steps actually timed).  value = weight bytes
+    of the timed calls / time."""
     from oracle import moe as M
     cfg = synth.CONFIGS[args.workload]
     T = max(int(b) for b in args.batches.split(","))
     host = synth.make_layer(cfg, seed=0)
 
-    def layer_pieces(batch):
-        x = synth.make_tokens(cfg, T, seed=3000, batch=batch)
-        X = F.bf16_to_f64(x)
-        st = {}
+    def step(b):
+        x = synth.make_tokens(cfg, T, seed=3000, batch=b)
+        ref = M.layer_forward(host, x)
+        return host.router_bytes() + host.shared_bytes() + int(np.count_nonzero(ref["expert_cnt"])) * \
+            host.expert_bytes()
 
-        def router():
-            _, _, idx, w = M.route(x, host.router_w, host.router_b, cfg.k)
-            st["cnt"], st["off"], st["pair"] = M.dispatch(idx, cfg.E)
-            st["w"], st["y"] = w, np.zeros((T, cfg.H))
-            return host.router_bytes()
-        yield router
-        if host.shared_gate is not None:
-            def shared():
-                Wg, Wu, Wd = (F.decode_qmat(host.shared_gate, 0), F.decode_qmat(host.shared_up, 0),
-                              F.decode_qmat(host.shared_down, 0))
-                st["y"] += M.swiglu_mlp(Wg, Wu, Wd, X)[1]
-                return host.shared_bytes()
-            yield shared
-        for e in range(cfg.E):
-            if st["cnt"][e] == 0:
-                continue
-
-            def expert(e=e):
-                ps = [int(p) for p in st["pair"][st["off"][e]:st["off"][e + 1]]]
-                rows = np.array([p // cfg.k for p in ps])
-                Wg, Wu, Wd = F.decode_qmat(host.gate, e), F.decode_qmat(host.up, e), F.decode_qmat(host.down, e)
-                P = M.swiglu_mlp(Wg, Wu, Wd, X[rows])[1]
-                for i, p in enumerate(ps):
-                    t, j = divmod(p, cfg.k)
-                    st["y"][t] += float(st["w"][t, j]) * P[i]
-                return host.expert_bytes()
-            yield expert
-
-    def steps():
-        b = 0
-        while True:
-            yield from layer_pieces(b)
-            b += 1
-
-    it = steps()
-    for _ in range(args.warmup):
-        next(it)()
-    byts = 0
+    for b in range(args.warmup):
+        step(b)
+    byts, n = 0, 0
     t0 = time.time()
-    for _ in range(args.steps):
-        byts += next(it)()
+    for b in range(args.steps):
+        byts += step(args.warmup + b)
+        n += 1
+        if time.time() - t0 > seconds_budget:
+            break
     dt = time.time() - t0
     cores = len(os.sched_getaffinity(0))
     value = round(byts / dt / 1e9, 4)
-    sample = (f"{args.steps} pieces of batch-{T} layer calls on {cfg.name} (router, shared expert, routed expert "
-              f"segments in layer order; FP64 numpy oracle, BLAS threads = {cores})")
+    sample = (f"{n} whole layer calls of {T} tokens on {cfg.name} (FP64 numpy oracle, BLAS threads = {cores}; "
+              f"{args.warmup} untimed first)")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / max(1, args.steps), 3),
+            "steps": n, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / max(1, n), 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded, the GPU arm's layer and token recipe)",
-            "config": {"workload": workload_name(cfg, T), "batch_tokens": T, "parallelism": "host cores"},
+            "data": f"synthetic ({DATA_DESC[args.workload]}; N(0,1) bf16 tokens; seeded)",
+            "config": {"workload": f"{workload_name(cfg)}, batch {T} tokens", "batch_tokens": T,
+                       "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
                              "seconds": round(dt, 2)},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -580,14 +587,17 @@ def run_cpu_baseline(args, seconds_budget: float = 20.0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4096)
-    ap.add_argument("--warmup", type=int, default=512)
+    ap.add_argument("--steps", type=int, default=128, help="layer calls per timed measurement (K)")
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--replays", type=int, default=30, help="timed measurements per batch size (>= 20)")
+    ap.add_argument("--more-workloads", default="decode_mxfp4,decode_int4",
+                    help="further decode workloads measured at their own batch sizes")
+    ap.add_argument("--mem-gb", type=float, default=40.0, help="device memory budget for the rotated layer copies")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--batches", default="1,4,8")
     ap.add_argument("--instances", type=int, default=0)
     ap.add_argument("--token-batches", type=int, default=64)
-    ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-batches", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill workload's measurement")

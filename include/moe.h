@@ -81,7 +81,12 @@ typedef enum {
   /* Symmetric int8 [N, K], BF16 scale per 64 elements, scales [N, K/64] bf16. */
   MOE_FMT_INT8_G64 = 4,
   /* E4M3 codes [N, K], FP32 scale per 128x128 block, scales [N/128, K/128] f32. */
-  MOE_FMT_FP8_B128 = 5
+  MOE_FMT_FP8_B128 = 5,
+  /* The AutoRound / GPTQ int4 group-128 layout (DGPP README "Highlights":
+   * int4 group-128 experts served in their packed form): unsigned nibbles u
+   * (low nibble = even k) with zero point 8, FP16 scale per 128 elements,
+   * scales [N, K/128] f16.  W = (u - 8) * s. */
+  MOE_FMT_INT4_G128 = 6
 } moe_format;
 
 /* A stack of matrices W_e[N, K] (e = 0 .. count-1) in one format. */
@@ -108,6 +113,15 @@ typedef struct {
   moe_qweight shared_gate;   /* [1] x [Is, H] */
   moe_qweight shared_up;     /* [1] x [Is, H] */
   moe_qweight shared_down;   /* [1] x [H, Is] */
+  /* device [H] f32 or NULL.  When set, the shared expert's output is scaled
+   * per token by sigmoid(g_t), g_t the correctly rounded FP32 dot product of
+   * x_t with this vector (a gated shared expert); NULL: weight 1. */
+  const float* shared_expert_gate;
+  /* 0: router_bias shifts the logits that decide both the selection and the
+   * weights.  1: the bias steers the selection only and the weights come
+   * from the unbiased logits of the selected experts (a load-balancing
+   * correction that leaves the mixture weights as the router computes them). */
+  int32_t bias_select;
 } moe_layer;
 
 typedef struct {
@@ -116,7 +130,16 @@ typedef struct {
    * outputs re-quantised to NVFP4 16-element blocks before the projections
    * (DGPP forum, page 5 weekly update: W4A4 prefill is opt-in). */
   int32_t act_quant;
-  int32_t reserved[7];       /* must be zero */
+  /* 0 (default): FP32 per-expert partials.  1: the down projection's
+   * partials are rounded to BF16 before the weighted sum (DGPP README
+   * "Execution and performance", engine.prefill_bf16_partials, a lever that
+   * halves the partials' bytes and is not bitwise the default chain). */
+  int32_t bf16_partials;
+  /* 0 (default: 2 s): every bounded device-side wait of the prefill
+   * kernels gives up after this many microseconds and reports
+   * MOE_ERR_DEVICE_TIMEOUT through moe_check. */
+  int32_t wait_limit_us;
+  int32_t reserved[5];       /* must be zero */
 } moe_options;
 
 /* Largest token count moe_decode_forward accepts. */
@@ -147,7 +170,11 @@ int32_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
  * engine.expert_tile_list: routed segments per expert).
  *   logits     l[t, e] = fl32( sum_h x[t, h] * router_w[e, h] ), the correctly
  *              rounded FP32 dot product, then fl32(l + router_bias[e]) if a bias
- *              is given.
+ *              is given.  Selection and weights use these exact logits; the
+ *              router finds them with an FP32 pass and a rigorous error bound,
+ *              then recomputes exactly every expert that can still reach the
+ *              top-k, so in the workspace's logits array (moe_workspace_layout)
+ *              those experts hold l[t, e] and the others -inf.
  *   topk_idx   [T, k] i32: experts by logit descending, ties to the lower id.
  *   topk_w     [T, k] f32: exp(l_j - l_0) / sum_i exp(l_i - l_0) over the selected.
  *   expert_cnt [E] i32 pairs per expert; expert_off [E+1] i32 exclusive scan.
@@ -172,12 +199,30 @@ int32_t moe_route(const moe_layer* layer, const void* x /* device bf16 [T, H] */
  * to BF16 once (forum post 1, quantisation table: activations stay BF16;
  * README "Execution and performance", engine.prefill_bf16_partials and
  * engine.prefill_fold_scales off by default).  Routing outputs are left in
- * the workspace (see moe_workspace_layout).  opts may be NULL (defaults);
+ * the workspace (see moe_workspace_layout; logits as for moe_route).  opts may be NULL (defaults);
  * act_quant must be 0 here (MOE_ERR_UNSUPPORTED otherwise).
  */
 int32_t moe_decode_forward(const moe_layer* layer, const void* x /* device bf16 [T, H] */, int32_t T,
                            void* y /* device bf16 [T, H] */, const moe_options* opts, void* ws, size_t ws_bytes,
                            moe_stream_t stream);
+
+/*
+ * The expert half of moe_decode_forward on routing the caller computed: for
+ * T = 1 .. MOE_DECODE_MAX_TOKENS tokens and the caller's top-k choice
+ * (topk_idx device i32 [T, k], expert ids; topk_w device f32 [T, k], mixture
+ * weights), y[t] = bf16( sum_j topk_w[t, j] * down_e( h_tj ) + shared(x_t) )
+ * with the same expert kernels, dispatch (a stable counting sort of the pairs
+ * by expert; DGPP README "Execution and performance", engine.expert_tile_list)
+ * and rounding points.  This serves layers whose router is not the softmax
+ * top-k of moe_route (a sigmoid or group-limited router, or routing decided
+ * elsewhere); router_w and router_bias are not read.  An id outside
+ * [0, n_experts) is reported as MOE_ERR_DEVICE_BAD_INDEX through moe_check and
+ * its pair is left out (y is then undefined).  Other arguments, checks and
+ * results are those of moe_decode_forward.
+ */
+int32_t moe_experts_forward(const moe_layer* layer, const void* x /* device bf16 [T, H] */, int32_t T,
+                            const int32_t* topk_idx, const float* topk_w, void* y /* device bf16 [T, H] */,
+                            const moe_options* opts, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * Whole layer for any T >= 1 (prefill), same result definition as
@@ -305,6 +350,10 @@ typedef struct {
   size_t expert_off;  /* i32 [E + 1] */
   size_t pair_list;   /* i32 [T * k] */
   size_t total;       /* workspace bytes for this max_tokens */
+  /* moe_prefill_forward with act_quant = 1: the NVFP4 codes and E4M3 block scales of each
+   * pair's SwiGLU output h, by sorted position (position pos holds pair pair_list[pos]) */
+  size_t h_codes;     /* u8 [T * k, I / 2], low nibble = even column */
+  size_t h_scales;    /* u8 [T * k, I / 16] */
 } moe_ws_layout;
 
 int32_t moe_workspace_layout(const moe_layer* layer, int32_t max_tokens, const moe_options* opts,

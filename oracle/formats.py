@@ -28,7 +28,7 @@ from __future__ import annotations
 
 import numpy as np
 
-FMT_NVFP4, FMT_MXFP4, FMT_INT4_G64, FMT_INT8_G64, FMT_FP8_B128 = 1, 2, 3, 4, 5
+FMT_NVFP4, FMT_MXFP4, FMT_INT4_G64, FMT_INT8_G64, FMT_FP8_B128, FMT_INT4_G128 = 1, 2, 3, 4, 5, 6
 
 
 def e2m1_value(code: int) -> float:
@@ -130,6 +130,12 @@ def decode(fmt: int, data: np.ndarray, scales: np.ndarray, ts: float, N: int, K:
         q = np.asarray(data, dtype=np.uint8).reshape(N, K).view(np.int8).astype(np.float64)
         s = bf16_to_f64(np.asarray(scales, dtype=np.uint16).reshape(N, K // 64))
         return q * np.repeat(s, 64, axis=1)
+    if fmt == FMT_INT4_G128:
+        # AutoRound / GPTQ layout (page 2 README "Highlights": int4 group-128 experts served in their
+        # packed form): unsigned nibble u with zero point 8, q = u - 8; FP16 scale per 128 columns
+        q = unpack_nibbles(data).reshape(N, K).astype(np.float64) - 8.0
+        s = np.asarray(scales, dtype=np.uint16).reshape(N, K // 128).view(np.float16).astype(np.float64)
+        return q * np.repeat(s, 128, axis=1)
     if fmt == FMT_FP8_B128:
         q = E4M3_TABLE[np.asarray(data, dtype=np.uint8).reshape(N, K)]
         s = np.asarray(scales, dtype=np.float32).reshape(N // 128, K // 128).astype(np.float64)

@@ -244,7 +244,7 @@ def _decoded(qm, e):
 
 
 def layer_forward(layer, x_bits: np.ndarray, act_quant: bool = False, tokens=None, expert_cache=None,
-                  bias_select: bool = False, bf16_partials: bool = False):
+                  bias_select: bool = False, bf16_partials: bool = False, routing=None):
     """Full MoE layer on host-resident checkpoint data (a synth.HostLayer).
 
     tokens: optional subset of token rows whose outputs are wanted (routing is
@@ -259,12 +259,19 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: bool = False, tokens=Non
     A gate vector in ``layer.extra["shared_gate_w"]`` ([H] f32) scales the
     shared expert by its sigmoid gate (``shared_gate``); without one the shared
     expert enters with weight 1.
+    routing: optional (idx [T, k] i32, w [T, k] f32) chosen by the caller; the
+    router is then skipped and these pairs and weights are used as given.
     Returns a dict of every intermediate the CUDA path exposes.
     """
     cfg = layer.cfg
     x_bits = np.asarray(x_bits, dtype=np.uint16)
     T = x_bits.shape[0]
-    l32, near, idx, w = route(x_bits, layer.router_w, layer.router_b, cfg.k, bias_select)
+    if routing is None:
+        l32, near, idx, w = route(x_bits, layer.router_w, layer.router_b, cfg.k, bias_select)
+    else:
+        idx = np.asarray(routing[0], dtype=np.int32)
+        w = np.asarray(routing[1], dtype=np.float32)
+        l32, near = None, np.zeros((T, cfg.E), dtype=bool)
     cnt, off, pair = dispatch(idx, cfg.E)
     want = np.arange(T) if tokens is None else np.asarray(sorted(set(int(t) for t in tokens)))
     X = F.bf16_to_f64(x_bits)

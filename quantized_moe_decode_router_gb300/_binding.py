@@ -23,7 +23,8 @@ MOE_ERR_CUDA = -5
 MOE_ERR_DEVICE_TIMEOUT = -6
 MOE_ERR_DEVICE_BAD_INDEX = -7
 
-MOE_FMT_NONE, MOE_FMT_NVFP4, MOE_FMT_MXFP4, MOE_FMT_INT4_G64, MOE_FMT_INT8_G64, MOE_FMT_FP8_B128 = range(6)
+MOE_FMT_NONE, MOE_FMT_NVFP4, MOE_FMT_MXFP4, MOE_FMT_INT4_G64, MOE_FMT_INT8_G64, MOE_FMT_FP8_B128, MOE_FMT_INT4_G128 = \
+    range(7)
 MOE_DECODE_MAX_TOKENS = 8
 
 
@@ -39,17 +40,19 @@ class moe_layer(ctypes.Structure):
         ("gate", moe_qweight), ("up", moe_qweight), ("down", moe_qweight),
         ("shared_fmt", ctypes.c_int32), ("shared_inter", ctypes.c_int32),
         ("shared_gate", moe_qweight), ("shared_up", moe_qweight), ("shared_down", moe_qweight),
+        ("shared_expert_gate", ctypes.c_void_p), ("bias_select", ctypes.c_int32),
     ]
 
 
 class moe_options(ctypes.Structure):
-    _fields_ = [("act_quant", ctypes.c_int32), ("reserved", ctypes.c_int32 * 7)]
+    _fields_ = [("act_quant", ctypes.c_int32), ("bf16_partials", ctypes.c_int32), ("wait_limit_us", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 5)]
 
 
 class moe_ws_layout(ctypes.Structure):
     _fields_ = [("logits", ctypes.c_size_t), ("topk_idx", ctypes.c_size_t), ("topk_w", ctypes.c_size_t),
                 ("expert_cnt", ctypes.c_size_t), ("expert_off", ctypes.c_size_t), ("pair_list", ctypes.c_size_t),
-                ("total", ctypes.c_size_t)]
+                ("total", ctypes.c_size_t), ("h_codes", ctypes.c_size_t), ("h_scales", ctypes.c_size_t)]
 
 
 class moe_decode_plan_info(ctypes.Structure):
@@ -80,6 +83,9 @@ _SIGNATURES = {
     "moe_prefill_forward_timed": (ctypes.c_int32, [_P(moe_layer), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                                    _P(moe_options), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                                    ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_experts_forward": (ctypes.c_int32, [_P(moe_layer), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p, _P(moe_options), ctypes.c_void_p,
+                                             ctypes.c_size_t, ctypes.c_void_p]),
     "moe_decode_forward_noalloc": (ctypes.c_int32, [_P(moe_layer), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                                     _P(moe_options), ctypes.c_void_p]),
     "moe_check": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -166,6 +172,8 @@ class Layer:
     shared_gate: Optional[QWeight] = None
     shared_up: Optional[QWeight] = None
     shared_down: Optional[QWeight] = None
+    shared_expert_gate: object = None   # torch float32 [H] (device) or None
+    bias_select: int = 0                # 1: the router bias steers the selection only
 
     def c(self) -> moe_layer:
         z = moe_qweight(None, None, None)
@@ -173,11 +181,12 @@ class Layer:
                          _ptr(self.router_bias), self.gate.c(), self.up.c(), self.down.c(), self.shared_fmt,
                          self.shared_inter, self.shared_gate.c() if self.shared_gate else z,
                          self.shared_up.c() if self.shared_up else z,
-                         self.shared_down.c() if self.shared_down else z)
+                         self.shared_down.c() if self.shared_down else z, _ptr(self.shared_expert_gate),
+                         self.bias_select)
 
 
-def _opts(act_quant: int = 0):
-    return moe_options(act_quant, (ctypes.c_int32 * 7)())
+def _opts(act_quant: int = 0, bf16_partials: int = 0, wait_limit_us: int = 0):
+    return moe_options(act_quant, bf16_partials, wait_limit_us, (ctypes.c_int32 * 5)())
 
 
 def workspace_size(layer: Layer, max_tokens: int, act_quant: int = 0) -> int:
@@ -214,16 +223,26 @@ def moe_route(layer: Layer, x, T: int, topk_idx=None, topk_w=None, expert_cnt=No
 
 
 def moe_decode_forward(layer: Layer, x, T: int, y, ws, stream=None, act_quant: int = 0,
-                       raise_on_error: bool = True) -> int:
-    lc, o = layer.c(), _opts(act_quant)
+                       raise_on_error: bool = True, bf16_partials: int = 0) -> int:
+    lc, o = layer.c(), _opts(act_quant, bf16_partials)
     st = load().moe_decode_forward(ctypes.byref(lc), _ptr(x), T, _ptr(y), ctypes.byref(o), _ptr(ws),
                                    0 if ws is None else ws.numel() * ws.element_size(), _stream_handle(stream))
     return _check(st, "moe_decode_forward") if raise_on_error else st
 
 
-def moe_decode_forward_timed(layer: Layer, x, T: int, y, ws, events, stream=None) -> int:
+def moe_experts_forward(layer: Layer, x, T: int, topk_idx, topk_w, y, ws, stream=None, raise_on_error: bool = True,
+                        bf16_partials: int = 0) -> int:
+    """The expert half of the decode forward on caller routing (topk_idx i32 [T, k], topk_w f32 [T, k])."""
+    lc, o = layer.c(), _opts(0, bf16_partials)
+    st = load().moe_experts_forward(ctypes.byref(lc), _ptr(x), T, _ptr(topk_idx), _ptr(topk_w), _ptr(y),
+                                    ctypes.byref(o), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                    _stream_handle(stream))
+    return _check(st, "moe_experts_forward") if raise_on_error else st
+
+
+def moe_decode_forward_timed(layer: Layer, x, T: int, y, ws, events, stream=None, bf16_partials: int = 0) -> int:
     """moe_decode_forward recording torch.cuda.Event objects (4, or None entries) between its kernels."""
-    lc, o = layer.c(), _opts(0)
+    lc, o = layer.c(), _opts(0, bf16_partials)
     arr = (ctypes.c_void_p * 4)(*[None if e is None else int(e.cuda_event) for e in events])
     st = load().moe_decode_forward_timed(ctypes.byref(lc), _ptr(x), T, _ptr(y), ctypes.byref(o), _ptr(ws),
                                          ws.numel() * ws.element_size(), _stream_handle(stream), arr)
@@ -239,16 +258,17 @@ def moe_decode_forward_noalloc(layer: Layer, x, T: int, y, stream=None, raise_on
 
 
 def moe_prefill_forward(layer: Layer, x, T: int, y, ws, stream=None, act_quant: int = 0,
-                        raise_on_error: bool = True) -> int:
-    lc, o = layer.c(), _opts(act_quant)
+                        raise_on_error: bool = True, bf16_partials: int = 0, wait_limit_us: int = 0) -> int:
+    lc, o = layer.c(), _opts(act_quant, bf16_partials, wait_limit_us)
     st = load().moe_prefill_forward(ctypes.byref(lc), _ptr(x), T, _ptr(y), ctypes.byref(o), _ptr(ws),
                                     0 if ws is None else ws.numel() * ws.element_size(), _stream_handle(stream))
     return _check(st, "moe_prefill_forward") if raise_on_error else st
 
 
-def moe_prefill_forward_timed(layer: Layer, x, T: int, y, ws, events, stream=None, act_quant: int = 0) -> int:
+def moe_prefill_forward_timed(layer: Layer, x, T: int, y, ws, events, stream=None, act_quant: int = 0,
+                              bf16_partials: int = 0) -> int:
     """moe_prefill_forward recording torch.cuda.Event objects (8, or None entries) between its kernels."""
-    lc, o = layer.c(), _opts(act_quant)
+    lc, o = layer.c(), _opts(act_quant, bf16_partials)
     arr = (ctypes.c_void_p * 8)(*[None if e is None else int(e.cuda_event) for e in events])
     st = load().moe_prefill_forward_timed(ctypes.byref(lc), _ptr(x), T, _ptr(y), ctypes.byref(o), _ptr(ws),
                                           ws.numel() * ws.element_size(), _stream_handle(stream), arr)

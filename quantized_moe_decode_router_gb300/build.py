@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libqmoe.so")
 BUILD_DIR = os.path.join(os.path.dirname(PKG), "_build")
 SOURCES = ["abi.cu", "router.cu", "decode_nvfp4.cu", "decode_mxfp4.cu", "decode_int4.cu", "decode_int8.cu",
-           "decode_fp8.cu", "aux_kernels.cu", "noalloc.cu", "prefill.cu", "prefill_gemm.cu", "prefill_w4a4.cu", "prefill_router_tc.cu"]
+           "decode_fp8.cu", "decode_int4g128.cu", "aux_kernels.cu", "noalloc.cu", "prefill.cu", "prefill_gemm.cu", "prefill_w4a4.cu", "prefill_router_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

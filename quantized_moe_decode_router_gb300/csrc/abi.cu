@@ -17,7 +17,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-bool valid_fmt(int f) { return f >= MOE_FMT_NVFP4 && f <= MOE_FMT_FP8_B128; }
+bool valid_fmt(int f) { return f >= MOE_FMT_NVFP4 && f <= MOE_FMT_INT4_G128; }
 
 // Shape rules of the formats and of the kernels (16-byte units along K,
 // 128-row FP8 scale blocks).
@@ -28,7 +28,7 @@ bool shape_ok(int fmt, int N, int K) {
 }
 
 struct Layout {
-  size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, h_amax, hs_amax, gu_part, gu_cnt,
+  size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, approx, rwnorm, sgate, gu_part, gu_cnt,
       dn_part, dn_cnt;
   // prefill path
   size_t xg, xsig, xnorm, wnorm, hist, pos_of, tiles, h16, hsig, xq, xsf, xqg, xsfg, hq, hsf, rw_hi, rw_lo;
@@ -58,8 +58,9 @@ Layout make_layout(const moe_layer* L, int maxT) {
   o.hs = take(T * Is * 2 + 16);
   o.P = take(T * k * H * 4);
   o.S = take(T * H * 4 + 16);
-  o.h_amax = take(T * k * 4);
-  o.hs_amax = take(T * 4 + 16);
+  o.approx = take(T * E * 4);
+  o.rwnorm = take(E * 4);
+  o.sgate = take(T * 4);
   // block sums of tiles split along K (at most kMaxSplitBlocks entries)
   const size_t act_max = T * k < E ? T * k : E;
   const size_t gu_tiles = act_max * (I / 16) + Is / 16, dn_tiles = (act_max + 1) * (H / 16);
@@ -122,15 +123,27 @@ int32_t check_layer(const moe_layer* L) {
     if ((st = check_qweight(L->shared_up, L->shared_fmt, Is, H)) != MOE_OK) return st;
     if ((st = check_qweight(L->shared_down, L->shared_fmt, H, Is)) != MOE_OK) return st;
   }
+  if (L->shared_expert_gate) {
+    if (L->shared_fmt == MOE_FMT_NONE) return MOE_ERR_INVALID_ARG;  // a gate needs a shared expert
+    if (!aligned16(L->shared_expert_gate)) return MOE_ERR_MISALIGNED;
+  }
+  if (L->bias_select != 0 && L->bias_select != 1) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
 int32_t check_options(const moe_options* o) {
   if (!o) return MOE_OK;
   if (o->act_quant != 0 && o->act_quant != 1) return MOE_ERR_INVALID_ARG;
-  for (int i = 0; i < 7; ++i)
+  if (o->bf16_partials != 0 && o->bf16_partials != 1) return MOE_ERR_INVALID_ARG;
+  if (o->wait_limit_us < 0) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i)
     if (o->reserved[i] != 0) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
+}
+
+// Device-wait limit of the prefill kernels in nanoseconds (2 s unless the options set one).
+uint64_t wait_limit_ns(const moe_options* o) {
+  return (o && o->wait_limit_us > 0) ? (uint64_t)o->wait_limit_us * 1000ull : 2000000000ull;
 }
 
 int32_t check_ws(const moe_layer* L, int maxT, void* ws, size_t ws_bytes) {
@@ -194,6 +207,7 @@ cudaError_t launch_expert(int fmt, int sfmt, bool down, const ExpertArgs& a, siz
     case MOE_FMT_INT4_G64: return launch_expert_int4(sfmt, down, a, smem, s);
     case MOE_FMT_INT8_G64: return launch_expert_int8(sfmt, down, a, smem, s);
     case MOE_FMT_FP8_B128: return launch_expert_fp8(sfmt, down, a, smem, s);
+    case MOE_FMT_INT4_G128: return launch_expert_int4g128(sfmt, down, a, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -210,8 +224,11 @@ RouterArgs router_args(const moe_layer* L, const Layout& lo, void* ws, const voi
   ra.w = L->router_w;
   ra.bias = L->router_bias;
   ra.rb = route_bufs(lo, ws);
-  ra.h_amax = reinterpret_cast<uint32_t*>(b + lo.h_amax);
-  ra.hs_amax = reinterpret_cast<uint32_t*>(b + lo.hs_amax);
+  ra.approx = reinterpret_cast<float*>(b + lo.approx);
+  ra.rwnorm = reinterpret_cast<float*>(b + lo.rwnorm);
+  ra.bias_select = L->bias_select;
+  ra.sgate_w = L->shared_fmt ? L->shared_expert_gate : nullptr;
+  ra.sgate = reinterpret_cast<float*>(b + lo.sgate);
   return ra;
 }
 
@@ -280,8 +297,9 @@ int32_t plan_decode(const moe_layer* L, int T, int sms, DecodePlan* p) {
   return MOE_OK;
 }
 
-int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* y, void* ws, size_t ws_bytes,
-                            cudaStream_t stream, void* const* events) {
+int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* y, const moe_options* opts, void* ws,
+                            size_t ws_bytes, cudaStream_t stream, void* const* events,
+                            const int32_t* ext_idx = nullptr, const float* ext_w = nullptr) {
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (events) cudaStreamIsCapturing(stream, &cap);
   auto mark = [&](int i) {
@@ -311,8 +329,6 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   ea.rb = ra.rb;
   ea.h = reinterpret_cast<uint16_t*>(b + lo.h);
   ea.hs = reinterpret_cast<uint16_t*>(b + lo.hs);
-  ea.h_amax = ra.h_amax;
-  ea.hs_amax = ra.hs_amax;
   ea.P = reinterpret_cast<float*>(b + lo.P);
   ea.S = reinterpret_cast<float*>(b + lo.S);
   ea.gu_part = reinterpret_cast<float*>(b + lo.gu_part);
@@ -320,6 +336,8 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   ea.dn_part = reinterpret_cast<float*>(b + lo.dn_part);
   ea.dn_cnt = reinterpret_cast<uint32_t*>(b + lo.dn_cnt);
   ea.y = static_cast<uint16_t*>(y);
+  ea.shared_g = ra.sgate_w ? ra.sgate : nullptr;
+  ea.p_bf16 = (opts && opts->bf16_partials) ? 1 : 0;
 
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -338,7 +356,7 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   const size_t smem_gu = pl.smem_gu, smem_dn = pl.smem_dn;
 
   mark(0);
-  cudaError_t err = launch_router_decode(ra, stream);
+  cudaError_t err = ext_idx ? launch_dispatch_ext(ra, ext_idx, ext_w, stream) : launch_router_decode(ra, stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   mark(1);
   err = launch_expert(L->fmt, L->shared_fmt, false, ea, smem_gu, stream);
@@ -385,6 +403,9 @@ PrefillArgs prefill_args(const moe_layer* L, const Layout& lo, void* ws, const v
   a.rw_hi = reinterpret_cast<uint16_t*>(b + lo.rw_hi);
   a.rw_lo = reinterpret_cast<uint16_t*>(b + lo.rw_lo);
   a.logits_tc = prefill_logits_tc_ok(a) ? 1 : 0;
+  a.bias_select = L->bias_select;
+  a.unbiased = reinterpret_cast<float*>(b + lo.approx);
+  a.wait_ns = 2000000000ull;
   return a;
 }
 
@@ -464,6 +485,8 @@ int32_t moe_workspace_layout(const moe_layer* layer, int32_t max_tokens, const m
   out->expert_off = lo.off;
   out->pair_list = lo.pair;
   out->total = lo.total;
+  out->h_codes = lo.hq;
+  out->h_scales = lo.hsf;
   return MOE_OK;
 }
 
@@ -492,7 +515,10 @@ int32_t moe_route(const moe_layer* layer, const void* x, int32_t T, int32_t* top
   ra.out.topk_idx = topk_idx; ra.out.topk_w = topk_w; ra.out.cnt = expert_cnt; ra.out.off = expert_off;
   ra.out.pair = pair_list;
   if ((size_t)T * layer->hidden * 2 > 200 * 1024) return MOE_ERR_UNSUPPORTED;
-  return cuda_status(launch_router_decode(ra, reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t err = launch_router_decode(ra, s);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_route_dispatch(ra, s));
 }
 
 }  // extern "C"
@@ -520,12 +546,24 @@ static int32_t decode_forward_checked(const moe_layer* layer, const void* x, int
   int32_t st = qmoe::check_decode_args(layer, x, T, y, opts);
   if (st != MOE_OK) return st;
   if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
-  return decode_forward_impl(layer, x, T, y, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), events);
+  return decode_forward_impl(layer, x, T, y, opts, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), events);
 }
 
 int32_t moe_decode_forward(const moe_layer* layer, const void* x, int32_t T, void* y, const moe_options* opts,
                            void* ws, size_t ws_bytes, moe_stream_t stream) {
   return decode_forward_checked(layer, x, T, y, opts, ws, ws_bytes, stream, nullptr);
+}
+
+int32_t moe_experts_forward(const moe_layer* layer, const void* x, int32_t T, const int32_t* topk_idx,
+                            const float* topk_w, void* y, const moe_options* opts, void* ws, size_t ws_bytes,
+                            moe_stream_t stream) {
+  int32_t st = qmoe::check_decode_args(layer, x, T, y, opts);
+  if (st != MOE_OK) return st;
+  if (!topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned4(topk_idx) || !aligned4(topk_w)) return MOE_ERR_MISALIGNED;
+  if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
+  return decode_forward_impl(layer, x, T, y, opts, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                             topk_idx, topk_w);
 }
 
 int32_t moe_decode_plan(const moe_layer* layer, int32_t T, int32_t num_sms, moe_decode_plan_info* out) {
@@ -588,6 +626,8 @@ static int32_t prefill_forward_checked(const moe_layer* layer, const void* x, in
   const Layout lo = make_layout(layer, ws_max_tokens(layer, ws_bytes));
   PrefillArgs pa = prefill_args(layer, lo, ws, x, T, y);
   pa.act_quant = aq ? 1 : 0;
+  pa.wait_ns = wait_limit_ns(opts);
+  pa.p_bf16 = (opts && opts->bf16_partials) ? 1 : 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   MarkCtx mc{events, s, false};
   if (events) {

@@ -21,7 +21,7 @@ __global__ void dequantize_kernel(int fmt, QW w, int N, int K, int expert, int r
   const uint8_t* data = w.data + (size_t)expert * data_bytes(fmt, N, K);
   const uint8_t* sc = w.scales + (size_t)expert * scale_bytes(fmt, N, K);
   float v[8];
-  if (fmt == MOE_FMT_NVFP4 || fmt == MOE_FMT_MXFP4 || fmt == MOE_FMT_INT4_G64) {
+  if (fmt == MOE_FMT_NVFP4 || fmt == MOE_FMT_MXFP4 || fmt == MOE_FMT_INT4_G64 || fmt == MOE_FMT_INT4_G128) {
     const uint32_t wd = *reinterpret_cast<const uint32_t*>(data + (size_t)R * (K / 2) + k / 2);
     uint32_t f[4];
     if (fmt == MOE_FMT_INT4_G64) {
@@ -29,6 +29,12 @@ __global__ void dequantize_kernel(int fmt, QW w, int N, int K, int expert, int r
       for (int j = 0; j < 4; ++j) { v[j] = h2lo(f[j]); v[j + 4] = h2hi(f[j]); }
       const uint32_t sb = *reinterpret_cast<const uint16_t*>(sc + ((size_t)R * (K / 64) + k / 64) * 2);
       const float s = __uint_as_float(sb << 16);
+      for (int j = 0; j < 8; ++j) v[j] = v[j] * s;
+    } else if (fmt == MOE_FMT_INT4_G128) {
+      int4x8_to_f16x2_paired(wd ^ 0x88888888u, f);  // u - 8 (zero point 8)
+      for (int j = 0; j < 4; ++j) { v[j] = h2lo(f[j]); v[j + 4] = h2hi(f[j]); }
+      const uint16_t sb = *reinterpret_cast<const uint16_t*>(sc + ((size_t)R * (K / 128) + k / 128) * 2);
+      const float s = __half2float(__ushort_as_half(sb));
       for (int j = 0; j < 8; ++j) v[j] = v[j] * s;
     } else {
       e2m1x8_to_f16x2(wd, f);

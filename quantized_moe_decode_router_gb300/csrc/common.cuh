@@ -92,6 +92,26 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Hint: bring [p, p + bytes) into L2 (bulk prefetch, no completion to wait for).
+// p 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Prefetch the 16-byte aligned part of share `part` of `parts` equal shares of [base, base + len).
+__device__ __forceinline__ void prefetch_l2_share(const uint8_t* base, size_t len, int part, int parts) {
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(base);
+  uintptr_t lo = b0 + len * (size_t)part / (size_t)parts, hi = b0 + len * (size_t)(part + 1) / (size_t)parts;
+  lo = (lo + 15) & ~(uintptr_t)15;
+  hi &= ~(uintptr_t)15;
+  constexpr uintptr_t kMax = 1u << 20;  // one request at most 1 MiB
+  while (lo < hi) {
+    const uintptr_t n = hi - lo < kMax ? hi - lo : kMax;
+    prefetch_l2_bulk(reinterpret_cast<const void*>(lo), (uint32_t)n);
+    lo += n;
+  }
+}
+
 // 2^e as a float for e in [-126, 127].
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 

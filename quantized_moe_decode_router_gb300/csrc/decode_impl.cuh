@@ -53,7 +53,11 @@ template <> struct Fm<MOE_FMT_MXFP4> { static constexpr int kBits = 4; };
 template <> struct Fm<MOE_FMT_INT4_G64> { static constexpr int kBits = 4; };
 template <> struct Fm<MOE_FMT_INT8_G64> { static constexpr int kBits = 8; };
 template <> struct Fm<MOE_FMT_FP8_B128> { static constexpr int kBits = 8; };
+template <> struct Fm<MOE_FMT_INT4_G128> { static constexpr int kBits = 4; };
 template <int F> constexpr int unit_k() { return Fm<F>::kBits == 4 ? 128 : 64; }
+__device__ __forceinline__ int Fm_bits(int fmt) {
+  return (fmt == MOE_FMT_INT8_G64 || fmt == MOE_FMT_FP8_B128) ? 8 : 4;
+}
 template <int F> constexpr int chunk_k() { return unit_k<F>() / 4; }
 
 struct Mat {
@@ -76,6 +80,7 @@ __device__ __forceinline__ uint32_t scale_col(int k) {
   if constexpr (F == MOE_FMT_NVFP4) return (uint32_t)k / 16;
   else if constexpr (F == MOE_FMT_MXFP4) return (uint32_t)k / 32;
   else if constexpr (F == MOE_FMT_INT4_G64 || F == MOE_FMT_INT8_G64) return (uint32_t)k / 64 * 2;
+  else if constexpr (F == MOE_FMT_INT4_G128) return (uint32_t)k / 128 * 2;
   else return (uint32_t)k / 128 * 4;
 }
 
@@ -85,6 +90,7 @@ __device__ __forceinline__ const uint8_t* scale_row(const Mat& m, int R) {
   if constexpr (F == MOE_FMT_NVFP4) return m.scales + (size_t)R * (m.K / 16);
   else if constexpr (F == MOE_FMT_MXFP4) return m.scales + (size_t)R * (m.K / 32);
   else if constexpr (F == MOE_FMT_INT4_G64 || F == MOE_FMT_INT8_G64) return m.scales + (size_t)R * (m.K / 64) * 2;
+  else if constexpr (F == MOE_FMT_INT4_G128) return m.scales + (size_t)R * (m.K / 128) * 2;
   else return m.scales + (size_t)(R / 128) * (m.K / 128) * 4;
 }
 
@@ -170,7 +176,7 @@ __device__ __forceinline__ void read_unit(Unit<NM>& u, const uint8_t* stage, con
     for (int r = 0; r < 2; ++r) {
       u.d[i][r] = *reinterpret_cast<const uint4*>(stage + ((i * 2 + r) * 32 + lane) * 16);
       const uint32_t w = *reinterpret_cast<const uint32_t*>(stage + NM * 2 * 32 * 16 + ((i * 2 + r) * 32 + lane) * 4);
-      if constexpr (Fm<F>::kBits == 4) {
+      if constexpr (Fm<F>::kBits == 4 && F != MOE_FMT_INT4_G128) {
         u.s[i][r] = (w >> sh[i][r]) & (F == MOE_FMT_MXFP4 ? 0xFFu : 0xFFFFu);
       } else {
         const uint32_t lo2 = ((uint32_t)reinterpret_cast<uintptr_t>(st.s[i][r]) + sc) & 3u;
@@ -197,6 +203,7 @@ __device__ __forceinline__ uint32_t f16x2_bcast(float v) {
 template <int F>
 __device__ __forceinline__ void decode_word4(uint32_t w, uint32_t (&v)[4]) {
   if constexpr (F == MOE_FMT_INT4_G64) int4x8_to_f16x2_paired(w, v);
+  else if constexpr (F == MOE_FMT_INT4_G128) int4x8_to_f16x2_paired(w ^ 0x88888888u, v);  // u - 8: flip the top bit
   else e2m1x8_to_f16x2(w, v);
 }
 
@@ -245,6 +252,7 @@ __device__ __forceinline__ bool fold4(const Unit<NM>& u, uint32_t (&fac)[NM][2][
 template <int F>
 __device__ __forceinline__ float unscaled_scale(uint32_t s) {
   if constexpr (F == MOE_FMT_MXFP4) return e8m0_to_float(s & 0xFF);
+  else if constexpr (F == MOE_FMT_INT4_G128) return __half2float(__ushort_as_half((unsigned short)s));
   else if constexpr (F == MOE_FMT_INT4_G64 || F == MOE_FMT_INT8_G64) return __uint_as_float(s << 16);
   else return __uint_as_float(s);
 }
@@ -252,7 +260,7 @@ __device__ __forceinline__ float unscaled_scale(uint32_t s) {
 // B fragments (activations) of word wd of the lane's chunk.
 template <int F>
 __device__ __forceinline__ void b_frags(const uint4& xv, uint32_t& a0, uint32_t& a1, uint32_t& b0, uint32_t& b1) {
-  if constexpr (F == MOE_FMT_INT4_G64) {
+  if constexpr (F == MOE_FMT_INT4_G64 || F == MOE_FMT_INT4_G128) {
     a0 = prmt(xv.x, xv.z, 0x5410u);  // (x0, x4)
     a1 = prmt(xv.x, xv.z, 0x7632u);  // (x1, x5)
     b0 = prmt(xv.y, xv.w, 0x5410u);  // (x2, x6)
@@ -262,20 +270,60 @@ __device__ __forceinline__ void b_frags(const uint4& xv, uint32_t& a0, uint32_t&
   }
 }
 
-// One unit of NM matrices: MMA into acc.  xl: this lane's activations (f16)
+// One unit of NM matrices: MMA into acc (even words of the lane's chunk) and
+// acc2 (odd words): two independent accumulation chains, so consecutive MMAs
+// of a matrix do not wait for each other.  xl: this lane's activations (f16)
 // at its chunk's first column.  Every lane executes every MMA.
 template <int F, int NM>
-__device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl, float (&acc)[NM][4]) {
-  if constexpr (Fm<F>::kBits == 4) {
+__device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl, float (&acc)[NM][4],
+                                             float (&acc2)[NM][4]) {
+  if constexpr (F == MOE_FMT_INT4_G128) {
+    // one FP16 scale per row covers the whole 128-column unit for all four lanes: the integer codes
+    // go through the MMA unscaled (exact in f16) and the scale multiplies the FP32 partial
+    float d[NM][4], d2[NM][4];
+#pragma unroll
+    for (int i = 0; i < NM; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) { d[i][j] = 0.f; d2[i][j] = 0.f; }
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+      const uint4 xv = *reinterpret_cast<const uint4*>(xl + wd * 8);
+      uint32_t bA0, bA1, bB0, bB1;
+      b_frags<F>(xv, bA0, bA1, bB0, bB1);
+#pragma unroll
+      for (int i = 0; i < NM; ++i) {
+        uint32_t v0[4], v1[4];
+        decode_word4<F>(word(u.d[i][0], wd), v0);
+        decode_word4<F>(word(u.d[i][1], wd), v1);
+        const uint32_t aA[4] = {v0[0], v1[0], v0[1], v1[1]};
+        const uint32_t aB[4] = {v0[2], v1[2], v0[3], v1[3]};
+        float (&dst)[4] = (wd & 1) ? d2[i] : d[i];
+        mma_f16_16816(dst, aA, bA0, bA1);
+        mma_f16_16816(dst, aB, bB0, bB1);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NM; ++i) {
+      const float sa = unscaled_scale<F>(u.s[i][0]), sb = unscaled_scale<F>(u.s[i][1]);
+      acc[i][0] = __fmaf_rn(d[i][0], sa, acc[i][0]);
+      acc[i][1] = __fmaf_rn(d[i][1], sa, acc[i][1]);
+      acc[i][2] = __fmaf_rn(d[i][2], sb, acc[i][2]);
+      acc[i][3] = __fmaf_rn(d[i][3], sb, acc[i][3]);
+      acc2[i][0] = __fmaf_rn(d2[i][0], sa, acc2[i][0]);
+      acc2[i][1] = __fmaf_rn(d2[i][1], sa, acc2[i][1]);
+      acc2[i][2] = __fmaf_rn(d2[i][2], sb, acc2[i][2]);
+      acc2[i][3] = __fmaf_rn(d2[i][3], sb, acc2[i][3]);
+    }
+  } else if constexpr (Fm<F>::kBits == 4) {
     uint32_t fac[NM][2][2];
     float us[NM][2];
     const bool fast = fold4<F, NM>(u, fac, us);
     if (fast) {
-      float d[NM][4];
+      float d[NM][4], d2[NM][4];
 #pragma unroll
       for (int i = 0; i < NM; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) d[i][j] = 0.f;
+        for (int j = 0; j < 4; ++j) { d[i][j] = 0.f; d2[i][j] = 0.f; }
 #pragma unroll
       for (int wd = 0; wd < 4; ++wd) {
         const uint4 xv = *reinterpret_cast<const uint4*>(xl + wd * 8);
@@ -293,7 +341,7 @@ __device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl
           }
           const uint32_t aA[4] = {v0[0], v1[0], v0[1], v1[1]};
           const uint32_t aB[4] = {v0[2], v1[2], v0[3], v1[3]};
-          float (&dst)[4] = (F == MOE_FMT_NVFP4) ? acc[i] : d[i];
+          float (&dst)[4] = (F == MOE_FMT_NVFP4) ? ((wd & 1) ? acc2[i] : acc[i]) : ((wd & 1) ? d2[i] : d[i]);
           mma_f16_16816(dst, aA, bA0, bA1);
           mma_f16_16816(dst, aB, bB0, bB1);
         }
@@ -305,6 +353,10 @@ __device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl
           acc[i][1] = __fmaf_rn(d[i][1], us[i][0], acc[i][1]);
           acc[i][2] = __fmaf_rn(d[i][2], us[i][1], acc[i][2]);
           acc[i][3] = __fmaf_rn(d[i][3], us[i][1], acc[i][3]);
+          acc2[i][0] = __fmaf_rn(d2[i][0], us[i][0], acc2[i][0]);
+          acc2[i][1] = __fmaf_rn(d2[i][1], us[i][0], acc2[i][1]);
+          acc2[i][2] = __fmaf_rn(d2[i][2], us[i][1], acc2[i][2]);
+          acc2[i][3] = __fmaf_rn(d2[i][3], us[i][1], acc2[i][3]);
         }
       }
     } else if constexpr (F != MOE_FMT_NVFP4) {
@@ -347,11 +399,11 @@ __device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl
     }
   } else {
     // 8-bit codes: the four lanes' chunks are one scale block; four words of four codes
-    float d[NM][4];
+    float d[NM][4], d2[NM][4];
 #pragma unroll
     for (int i = 0; i < NM; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) d[i][j] = 0.f;
+      for (int j = 0; j < 4; ++j) { d[i][j] = 0.f; d2[i][j] = 0.f; }
 #pragma unroll
     for (int wd = 0; wd < 4; ++wd) {
       const uint2 xv = *reinterpret_cast<const uint2*>(xl + wd * 4);
@@ -366,7 +418,7 @@ __device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl
           e4m3x4_to_f16x2(word(u.d[i][1], wd), lo1, hi1);
         }
         const uint32_t a[4] = {lo0, lo1, hi0, hi1};
-        mma_f16_16816(d[i], a, xv.x, xv.y);
+        mma_f16_16816((wd & 1) ? d2[i] : d[i], a, xv.x, xv.y);
       }
     }
 #pragma unroll
@@ -376,6 +428,10 @@ __device__ __forceinline__ void compute_unit(const Unit<NM>& u, const __half* xl
       acc[i][1] = __fmaf_rn(d[i][1], sa, acc[i][1]);
       acc[i][2] = __fmaf_rn(d[i][2], sb, acc[i][2]);
       acc[i][3] = __fmaf_rn(d[i][3], sb, acc[i][3]);
+      acc2[i][0] = __fmaf_rn(d2[i][0], sa, acc2[i][0]);
+      acc2[i][1] = __fmaf_rn(d2[i][1], sa, acc2[i][1]);
+      acc2[i][2] = __fmaf_rn(d2[i][2], sb, acc2[i][2]);
+      acc2[i][3] = __fmaf_rn(d2[i][3], sb, acc2[i][3]);
     }
   }
 }
@@ -399,11 +455,11 @@ __device__ __forceinline__ void warp_tile(const Mat (&m)[NM], int row0, int kb, 
   const int R0 = row0 + (lane >> 2);
   const int koff = kb + (lane & 3) * CK;
   const int nU = Kw / UK;
-  float blk[NM][4];
+  float blk[NM][4], blk2[NM][4];
 #pragma unroll
   for (int i = 0; i < NM; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) blk[i][j] = 0.f;
+    for (int j = 0; j < 4; ++j) { blk[i][j] = 0.f; blk2[i][j] = 0.f; }
   const Stream<NM> st = make_stream<F, NM>(m, R0, koff);
   uint32_t sh[NM][2];
   scale_shifts<F, NM>(st, koff, sh);
@@ -422,23 +478,24 @@ __device__ __forceinline__ void warp_tile(const Mat (&m)[NM], int row0, int kb, 
     read_unit<F, NM>(cur, ring + slot_read * SB, st, koff + u * UK, sh);
     slot_issue = (slot_issue + 1 == PF) ? 0 : slot_issue + 1;
     slot_read = (slot_read + 1 == PF) ? 0 : slot_read + 1;
-    compute_unit<F, NM>(cur, xrow + koff + u * UK, blk);
-    if (bu == 1 || (u & 1)) {  // block complete (bu is 1 or 2)
+    compute_unit<F, NM>(cur, xrow + koff + u * UK, blk, blk2);
+    if (bu == 1 || (u & 1)) {  // block complete (bu is 1 or 2): its sum is blk + blk2
       if (bpart) {
         float* d = bpart + (size_t)(bu == 1 ? u : u >> 1) * (32 * 4 * NM) + lane * 4 * NM;
 #pragma unroll
         for (int i = 0; i < NM; ++i)
-          *reinterpret_cast<float4*>(d + 4 * i) = make_float4(blk[i][0], blk[i][1], blk[i][2], blk[i][3]);
+          *reinterpret_cast<float4*>(d + 4 * i) = make_float4(blk[i][0] + blk2[i][0], blk[i][1] + blk2[i][1],
+                                                              blk[i][2] + blk2[i][2], blk[i][3] + blk2[i][3]);
       } else {
 #pragma unroll
         for (int i = 0; i < NM; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] += blk[i][j];
+          for (int j = 0; j < 4; ++j) acc[i][j] += blk[i][j] + blk2[i][j];
       }
 #pragma unroll
       for (int i = 0; i < NM; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) blk[i][j] = 0.f;
+        for (int j = 0; j < 4; ++j) { blk[i][j] = 0.f; blk2[i][j] = 0.f; }
     }
   }
   cp_async_wait<0>();
@@ -458,11 +515,11 @@ __device__ __forceinline__ void warp_tiles(const Mat (&m)[NM], int row0, int row
   const int koff = (lane & 3) * CK;
   const int nU = Kw / UK;
   const int total = ntile * nU;
-  float blk[NM][4], acc[NM][4];
+  float blk[NM][4], blk2[NM][4], acc[NM][4];
 #pragma unroll
   for (int i = 0; i < NM; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) { blk[i][j] = 0.f; acc[i][j] = 0.f; }
+    for (int j = 0; j < 4; ++j) { blk[i][j] = 0.f; blk2[i][j] = 0.f; acc[i][j] = 0.f; }
   // the streams of tile t are those of tile 0 moved by t row steps (every
   // format's code and scale addresses are linear in the row step used here)
   const Stream<NM> st0 = make_stream<F, NM>(m, row0 + R, koff);
@@ -501,12 +558,12 @@ __device__ __forceinline__ void warp_tiles(const Mat (&m)[NM], int row0, int row
     read_unit<F, NM>(cur, ring + slot_read * SB, stream_of(t), koff + u * UK, sh);
     slot_issue = (slot_issue + 1 == PF) ? 0 : slot_issue + 1;
     slot_read = (slot_read + 1 == PF) ? 0 : slot_read + 1;
-    compute_unit<F, NM>(cur, xrow + koff + u * UK, blk);
-    if (bu == 1 || (u & 1)) {  // block complete (bu is 1 or 2)
+    compute_unit<F, NM>(cur, xrow + koff + u * UK, blk, blk2);
+    if (bu == 1 || (u & 1)) {  // block complete (bu is 1 or 2): its sum is blk + blk2
 #pragma unroll
       for (int i = 0; i < NM; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) { acc[i][j] += blk[i][j]; blk[i][j] = 0.f; }
+        for (int j = 0; j < 4; ++j) { acc[i][j] += blk[i][j] + blk2[i][j]; blk[i][j] = 0.f; blk2[i][j] = 0.f; }
     }
     if (u == nU - 1) {
       epi(t, acc);
@@ -634,6 +691,110 @@ __device__ __forceinline__ bool block_reduce(float (&acc)[NM][4], const float* t
   return true;
 }
 
+// ------------------------------------------------------------ local dispatch --
+// Every gate/up CTA builds the dispatch index of the call in shared memory
+// from the T * k top-k ids (at most 128 pairs): pairs sorted by (expert, pair
+// id) - the stable counting sort of the router's dispatch - the active experts
+// in ascending id, and each one's segment of the sorted list.  CTA 0 also
+// writes the index to the workspace (counts and offsets of every expert, the
+// pair list, the active list) for the down and combine kernels.  Ids outside
+// [0, E), or an expert named twice by one token (a top-k choice names distinct
+// experts), are reported as MOE_ERR_DEVICE_BAD_INDEX and their pairs left out.
+constexpr int kMaxPairs = kMaxT * 16;
+
+struct LocalDispatch {
+  int pe[kMaxPairs];        // expert of pair p (-1: left out)
+  int sorted[kMaxPairs];    // pair ids by (expert, pair id); the valid ones first
+  int act[kMaxPairs];       // active experts, ascending
+  int aoff[kMaxPairs + 1];  // segment of active expert i: sorted[aoff[i] .. aoff[i + 1])
+  int wcnt[kExpertThreads / 32];
+  int n_active, n_valid;
+};
+
+static __device__ void local_dispatch(const ExpertArgs& a, LocalDispatch& d, bool write_global) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = a.T * a.k, E = a.E, k = a.k;
+  if (tid < P) {
+    int e = __ldcg(a.rb.topk_idx + tid);
+    if ((unsigned)e >= (unsigned)E) {
+      report_error(a.rb.ctrl, (uint32_t)MOE_ERR_DEVICE_BAD_INDEX, 0x040);
+      e = -1;
+    }
+    d.pe[tid] = e;
+  }
+  __syncthreads();
+  bool dup = false;  // the same expert twice in one token: keep the first
+  if (tid < P && d.pe[tid] >= 0)
+    for (int q = tid / k * k; q < tid; ++q) dup = dup || d.pe[q] == d.pe[tid];
+  __syncthreads();
+  if (dup) {
+    report_error(a.rb.ctrl, (uint32_t)MOE_ERR_DEVICE_BAD_INDEX, 0x041);
+    d.pe[tid] = -1;
+  }
+  __syncthreads();
+  // rank of each pair under the key (expert, pair id), left-out pairs last
+  if (tid < P) {
+    const int ep = d.pe[tid] >= 0 ? d.pe[tid] : E;
+    const long kp = (long)ep * kMaxPairs + tid;
+    int rank = 0;
+    for (int q = 0; q < P; ++q) {
+      const int eq = d.pe[q] >= 0 ? d.pe[q] : E;
+      rank += ((long)eq * kMaxPairs + q) < kp;
+    }
+    d.sorted[rank] = tid;
+  }
+  __syncthreads();
+  // segment starts: the first sorted entry of each expert (ballots over the pair warps)
+  bool first = false;
+  int e = -1;
+  if (tid < P) {
+    e = d.pe[d.sorted[tid]];
+    first = e >= 0 && (tid == 0 || d.pe[d.sorted[tid - 1]] != e);
+  }
+  const uint32_t bal = __ballot_sync(0xFFFFFFFFu, first);
+  const uint32_t valid = __ballot_sync(0xFFFFFFFFu, tid < P && e >= 0);
+  if (lane == 0) d.wcnt[warp] = __popc(bal) | (__popc(valid) << 16);
+  __syncthreads();
+  int base = 0, nact = 0, nvalid = 0;
+  for (int w = 0; w < kExpertThreads / 32; ++w) {
+    if (w < warp) base += d.wcnt[w] & 0xFFFF;
+    nact += d.wcnt[w] & 0xFFFF;
+    nvalid += d.wcnt[w] >> 16;
+  }
+  if (first) {
+    const int slot = base + __popc(bal & ((1u << lane) - 1u));
+    d.act[slot] = e;
+    d.aoff[slot] = tid;
+  }
+  if (tid == 0) {
+    d.n_active = nact;
+    d.n_valid = nvalid;
+    d.aoff[nact] = nvalid;
+  }
+  __syncthreads();
+  if (!write_global) return;
+  for (int i = tid; i < d.n_valid; i += kExpertThreads) a.rb.pair[i] = d.sorted[i];
+  for (int i = tid; i < d.n_active; i += kExpertThreads) a.rb.act[i] = d.act[i];
+  // counts and offsets of every expert: binary search of the sorted valid pairs
+  for (int x = tid; x <= E; x += kExpertThreads) {
+    int lo = 0, hi = d.n_valid;  // first sorted position whose expert is >= x
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (d.pe[d.sorted[mid]] < x) lo = mid + 1; else hi = mid;
+    }
+    a.rb.off[x] = lo;
+    if (x < E) {
+      int lo2 = lo, hi2 = d.n_valid;  // first position whose expert is > x
+      while (lo2 < hi2) {
+        const int mid = (lo2 + hi2) >> 1;
+        if (d.pe[d.sorted[mid]] <= x) lo2 = mid + 1; else hi2 = mid;
+      }
+      a.rb.cnt[x] = lo2 - lo;
+    }
+  }
+  if (tid == 0) a.rb.ctrl->n_active = d.n_active;
+}
+
 // --------------------------------------------------------------- gate / up --
 
 template <int FR, int FS, int PF>
@@ -669,68 +830,63 @@ __global__ void __launch_bounds__(kExpertThreads, MINB) gateup_kernel(ExpertArgs
   stage_rows_f16(s_src, nullptr, T, H, xs, xs_stride, s_pexp);
   if (tid == 0) s_pexp[T] = 0;
   __syncthreads();
-  pdl_wait();
 
-  const int n_active = *reinterpret_cast<volatile int*>(&a.rb.ctrl->n_active);
   const int tpe = I / 16;
   const int stiles = FS ? a.Is / 16 : 0;
-  const int n_rtiles = n_active * tpe;
   const int S = a.gu_slices, Ss = FS ? a.gu_slices_s : 1, St = a.gu_slices_t;
   const int Br = dec_blocks(FR, H), bur = dec_block_units(FR, H);
   const int Bs = FS ? dec_blocks(FS, H) : 1, bus = FS ? dec_block_units(FS, H) : 1;
   const int r = lane >> 2, c = lane & 3;
-  // every warp starts on task warp * grid + CTA, so consecutive tasks (the
-  // shared expert's first of all) land on different SMs; later tasks are handed out
-  // one at a time from a global counter, so warps that finish early take more.
-  // The shared expert's (costlier) tasks come first.  Routed tiles that do not
-  // fit in that first wave (the tail) are split into St > S slices, so the
-  // warps that finish the first wave share them in short pieces.
+  // Tasks: the shared expert's tiles first (numbered 0 .. n_shared_tasks - 1,
+  // their split counters and block sums at the start of the buffers), then
+  // the routed tiles.  Every warp starts on task warp * grid + CTA, so
+  // consecutive tasks (the shared expert's first of all) land on different
+  // SMs; later tasks are handed out one at a time from a global counter, so
+  // warps that finish early take more.  The shared expert depends on the
+  // tokens only, so a warp whose first task is a shared one runs it before
+  // waiting for the router.  Routed tiles that do not fit in the first wave
+  // (the tail) are split into St > S slices, so the warps that finish the
+  // first wave share them in short pieces.
   const int n_shared_tasks = stiles * Ss;
   const int nw = gridDim.x * kWarps;
-  int n_tail = 0;
-  if (St > S) {
-    const long first = (long)n_shared_tasks + (long)n_rtiles * S;
-    if (first > nw) n_tail = (int)min((long)min(n_rtiles, a.gu_tail_cap), (first - nw + S - 1) / S);
-  }
-  const int n_head = n_rtiles - n_tail;
-  const int n_tasks = n_shared_tasks + n_head * S + n_tail * St;
-  // stored block sums: routed tiles (all when S > 1, else the tail only), then shared tiles
-  const size_t shared_part0 = (size_t)(S > 1 ? n_rtiles : n_tail) * Br;
+  const size_t shared_blocks = Ss > 1 ? (size_t)stiles * Bs : 0;  // block sums of the shared tiles
+  __shared__ LocalDispatch ld;
+  int n_rtiles = 0, n_tail = 0, n_head = 0, n_tasks = n_shared_tasks;
+  bool routed_known = false;
   uint32_t* next = &a.rb.ctrl->gu_next;
-  int qn = 0;
-  for (int q = warp * gridDim.x + blockIdx.x; q < n_tasks; q = __shfl_sync(0xFFFFFFFFu, qn, 0)) {
-    if (lane == 0) qn = nw + (int)atomicAdd(next, 1u);  // the next task, fetched while this one runs
+
+  // one task: shared tile q < n_shared_tasks, else a routed tile (after the local dispatch)
+  auto run_task = [&](int q) {
     const bool shared_item = q < n_shared_tasks;
-    int Si, tile_id, slice;  // K slices of this tile, tile, slice
+    int Si, tile_id, slice;  // K slices of this tile, tile (shared tiles first), slice
     if (shared_item) {
-      Si = Ss; tile_id = n_rtiles + q / Ss; slice = q % Ss;
+      Si = Ss; tile_id = q / Ss; slice = q % Ss;
     } else if (q - n_shared_tasks < n_head * S) {
       const int qq = q - n_shared_tasks;
-      Si = S; tile_id = qq / S; slice = qq % S;
+      Si = S; tile_id = stiles + qq / S; slice = qq % S;
     } else {
       const int qt = q - n_shared_tasks - n_head * S;
-      Si = St; tile_id = n_head + qt / St; slice = qt % St;
+      Si = St; tile_id = stiles + n_head + qt / St; slice = qt % St;
     }
     const int Kw = H / Si;
-    int e = 0, tile, ncols, col_tok = 0, col_pair[2] = {-1, -1}, col_tokc[2] = {0, 0};
+    int e = 0, tile, col_tok = 0, col_pair[2] = {-1, -1}, col_tokc[2] = {0, 0};
     if (!shared_item) {
-      const int slot = tile_id / tpe;
-      tile = tile_id - slot * tpe;
-      e = a.rb.act[slot];
-      ncols = a.rb.cnt[e];
-      const int off = a.rb.off[e];
-      if (r < ncols) col_tok = a.rb.pair[off + r] / k;
+      const int rt = tile_id - stiles;  // routed tile index
+      const int slot = rt / tpe;
+      tile = rt - slot * tpe;
+      e = ld.act[slot];
+      const int off = ld.aoff[slot], ncols = ld.aoff[slot + 1] - off;  // <= T: distinct experts per token
+      if (r < ncols) col_tok = ld.sorted[off + r] / k;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int n = 2 * c + j;
         if (n < ncols) {
-          col_pair[j] = a.rb.pair[off + n];
+          col_pair[j] = ld.sorted[off + n];
           col_tokc[j] = col_pair[j] / k;
         }
       }
     } else {
-      tile = tile_id - n_rtiles;
-      ncols = T;
+      tile = tile_id;
       if (r < T) col_tok = r;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -745,42 +901,95 @@ __global__ void __launch_bounds__(kExpertThreads, MINB) gateup_kernel(ExpertArgs
     const Mat m[2] = {mat_of(qg, fmt, e, N, H), mat_of(qu, fmt, e, N, H)};
     const int row0 = tile * 16;
     const int B = shared_item ? Bs : Br;
-    const int rslot = S > 1 ? tile_id : max(tile_id - n_head, 0);  // (unused for unsplit tiles)
-    float* tile_part = a.gu_part + (shared_item ? shared_part0 + (size_t)tile * Bs : (size_t)rslot * Br) * (32 * 8);
+    // block sums: shared tiles first, then the routed ones (all when S > 1, else the tail only)
+    float* tile_part;
+    if (shared_item) {
+      tile_part = a.gu_part + (size_t)tile * Bs * (32 * 8);
+    } else {
+      const int rt = tile_id - stiles;
+      const int rslot = S > 1 ? rt : max(rt - n_head, 0);  // (unused for unsplit tiles)
+      tile_part = a.gu_part + (shared_blocks + (size_t)rslot * Br) * (32 * 8);
+    }
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     gu_tile<FR, FS, PF>(shared_item, m, row0, slice * Kw, Kw, shared_item ? bus : bur, xs + (size_t)col_tok * xs_stride,
                     acc, Si > 1 ? tile_part + (size_t)slice * (B / Si) * (32 * 8) : nullptr, ring);
-    if (!block_reduce<2>(acc, tile_part, a.gu_cnt + tile_id, Si, B)) continue;
-    const float tsg = (fmt == MOE_FMT_NVFP4) ? __ldg(qg.ts + e) : 1.f;
-    const float tsu = (fmt == MOE_FMT_NVFP4) ? __ldg(qu.ts + e) : 1.f;
-    uint32_t amax[2] = {0u, 0u};
+    if (block_reduce<2>(acc, tile_part, a.gu_cnt + tile_id, Si, B)) {
+      const float tsg = (fmt == MOE_FMT_NVFP4) ? __ldg(qg.ts + e) : 1.f;
+      const float tsu = (fmt == MOE_FMT_NVFP4) ? __ldg(qu.ts + e) : 1.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int cj = j & 1;
-      const int row = row0 + r + ((j & 2) ? 8 : 0);
-      const int out = col_pair[cj];
-      if (out >= 0) {
-        const float sc = exp2i(s_pexp[col_tokc[cj]]);
-        const float gv = acc[0][j] * sc * tsg, uv = acc[1][j] * sc * tsu;
-        const uint16_t hb = float_to_bf16_bits(silu_f(gv) * uv);
-        if (shared_item) a.hs[(size_t)out * a.Is + row] = hb;
-        else a.h[(size_t)out * I + row] = hb;
-        amax[cj] = max(amax[cj], (uint32_t)(hb & 0x7FFF) << 16);
+      for (int j = 0; j < 4; ++j) {
+        const int cj = j & 1;
+        const int row = row0 + r + ((j & 2) ? 8 : 0);
+        const int out = col_pair[cj];
+        if (out >= 0) {
+          const float sc = exp2i(s_pexp[col_tokc[cj]]);
+          const float gv = acc[0][j] * sc * tsg, uv = acc[1][j] * sc * tsu;
+          const uint16_t hb = float_to_bf16_bits(silu_f(gv) * uv);
+          if (shared_item) a.hs[(size_t)out * a.Is + row] = hb;
+          else a.h[(size_t)out * I + row] = hb;
+        }
       }
     }
-    // per-column max over the tile's 16 rows, then one atomic per column
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 4));
-      amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 8));
-      amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 16));
-      if (r == 0 && col_pair[j] >= 0)
-        atomicMax(shared_item ? &a.hs_amax[col_pair[j]] : &a.h_amax[col_pair[j]], amax[j]);
+  };
+
+  // the shared expert depends on the tokens only: a warp whose first task is a shared one runs it
+  // before the router's results are needed
+  const int q0 = warp * gridDim.x + blockIdx.x;
+  const bool ran_first = q0 < n_shared_tasks;
+  if (ran_first) run_task(q0);
+  __syncthreads();
+  pdl_wait();
+  local_dispatch(a, ld, blockIdx.x == 0);
+  // every active expert's gate and up bytes are brought into L2 now, each CTA its share, so HBM
+  // streams from the start of the routed work and the warps' rings read from L2
+  if (tid < 32) {
+    const size_t db = data_bytes(FR, I, H), sb = scale_bytes(FR, I, H);
+    for (int i = lane; i < ld.n_active * 4; i += 32) {
+      const int slot = i >> 2, what = i & 3;
+      const QW& w = (what & 1) ? a.up : a.gate;
+      const size_t e = (size_t)ld.act[slot];
+      if (what < 2) prefetch_l2_share(w.data + e * db, db, blockIdx.x, gridDim.x);
+      else prefetch_l2_share(w.scales + e * sb, sb, blockIdx.x, gridDim.x);
     }
+  }
+  {
+    n_rtiles = ld.n_active * tpe;
+    if (St > S) {
+      const long first = (long)n_shared_tasks + (long)n_rtiles * S;
+      if (first > nw) n_tail = (int)min((long)min(n_rtiles, a.gu_tail_cap), (first - nw + S - 1) / S);
+    }
+    n_head = n_rtiles - n_tail;
+    n_tasks = n_shared_tasks + n_head * S + n_tail * St;
+    routed_known = true;
+  }
+  (void)routed_known;
+  // later tasks one at a time from the counter, each fetched while the previous one runs
+  int qn = 0;
+  int q = q0;
+  if (ran_first) {
+    if (lane == 0) qn = nw + (int)atomicAdd(next, 1u);
+    q = __shfl_sync(0xFFFFFFFFu, qn, 0);
+  }
+  while (q < n_tasks) {
+    if (lane == 0) qn = nw + (int)atomicAdd(next, 1u);
+    run_task(q);
+    q = __shfl_sync(0xFFFFFFFFu, qn, 0);
   }
 }
 
 // -------------------------------------------------------------------- down --
+
+// One element of a down projection's output: P[pair, row] (routed) or S[token, row]
+// (shared), FP32, or rounded to BF16 under the bf16-partials lever.
+__device__ __forceinline__ void store_partial(const ExpertArgs& a, bool shared_item, int out, int row, float v) {
+  const size_t i = (size_t)out * a.H + row;
+  if (a.p_bf16) {
+    uint16_t* d = reinterpret_cast<uint16_t*>(shared_item ? a.S : a.P);
+    d[i] = float_to_bf16_bits(v);
+  } else {
+    (shared_item ? a.S : a.P)[i] = v;
+  }
+}
 
 template <int FR, int FS>
 __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
@@ -796,10 +1005,11 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
   __shared__ int s_col_out[kMaxDnSegs][kMaxT];
   __shared__ int s_ncols[kMaxDnSegs];
   __shared__ const uint16_t* s_src[kMaxT];
-  __shared__ uint32_t s_amax[kMaxT];
 
   pdl_launch_dependents();
   pdl_wait();
+  // the gate/up kernel has finished: leave its task counter at zero for the next call
+  if (blockIdx.x == 0 && tid == 0) a.rb.ctrl->gu_next = 0;
   const int n_active = *reinterpret_cast<volatile int*>(&a.rb.ctrl->n_active);
   const int tpe = H / 16;
   const int S = a.dn_slices;
@@ -824,6 +1034,30 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
   const int q1 = task_at(total * (blockIdx.x + 1) / gridDim.x);
   const int r = lane >> 2, c = lane & 3;
   if (q0 >= q1) return;
+  // this CTA's weight bytes (one contiguous row range per segment) are brought into L2 before the
+  // hidden rows are staged; the warps' rings then read them from L2
+  if (tid < 32) {
+    const int seg_a = q0 / tasks_per_seg, seg_b = (q1 - 1) / tasks_per_seg;
+    for (int seg = seg_a + lane; seg <= seg_b; seg += 32) {
+      const bool shared_item = FS && seg == 0;
+      const int fmt = shared_item ? FS : FR;
+      const int K = shared_item ? a.Is : I;
+      const int e = shared_item ? 0 : a.rb.act[seg - sh];
+      if ((unsigned)e >= (unsigned)a.E) continue;
+      const QW& qd = shared_item ? a.sdown : a.down;
+      const int t_a = max(q0, seg * tasks_per_seg) - seg * tasks_per_seg;
+      const int t_b = min(q1, (seg + 1) * tasks_per_seg) - seg * tasks_per_seg;  // tasks [t_a, t_b)
+      const int tile_a = t_a / S, tile_b = (t_b + S - 1) / S;                    // row tiles they touch
+      const size_t rb = (size_t)K * Fm_bits(fmt) / 8;                            // bytes of one row
+      const uint8_t* d0 = qd.data + (size_t)e * data_bytes(fmt, H, K) + (size_t)tile_a * 16 * rb;
+      prefetch_l2_share(d0, (size_t)(tile_b - tile_a) * 16 * rb, 0, 1);
+      if (fmt != MOE_FMT_FP8_B128) {
+        const size_t sr = scale_bytes(fmt, H, K) / H;                            // scale bytes of one row
+        prefetch_l2_share(qd.scales + (size_t)e * scale_bytes(fmt, H, K) + (size_t)tile_a * 16 * sr,
+                          (size_t)(tile_b - tile_a) * 16 * sr, 0, 1);
+      }
+    }
+  }
 
   // the segments of [q0, q1), staged SG at a time; inside a group the warps
   // take the tasks in turn with no barrier between segments
@@ -837,13 +1071,12 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
       int ncols;
       if (!shared_item) {
         const int e = a.rb.act[seg - sh];
-        ncols = a.rb.cnt[e];
+        ncols = (unsigned)e < (unsigned)a.E ? min(a.rb.cnt[e], kMaxT) : 0;  // a bad id was reported by gate/up
         if (tid < kMaxT) {
           if (tid < ncols) {
             const int p = a.rb.pair[a.rb.off[e] + tid];
             s_src[tid] = a.h + (size_t)p * I;
             s_col_out[i][tid] = p;
-            s_amax[tid] = __ldcg(a.h_amax + p);
           } else {
             s_col_out[i][tid] = -1;
           }
@@ -851,16 +1084,14 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
       } else {
         ncols = T;
         if (tid < kMaxT) {
-          if (tid < T) {
-            s_src[tid] = a.hs + (size_t)tid * a.Is;
-            s_amax[tid] = __ldcg(a.hs_amax + tid);
-          }
+          if (tid < T) s_src[tid] = a.hs + (size_t)tid * a.Is;
           s_col_out[i][tid] = tid < T ? tid : -1;
         }
       }
       if (tid == 0) s_ncols[i] = ncols;
       __syncthreads();
-      stage_rows_f16(s_src, s_amax, ncols, shared_item ? a.Is : I, hsm + (size_t)i * seg_halfs, hs_stride,
+      // each staged row's largest magnitude is found here (the rows are h, just written to L2)
+      stage_rows_f16(s_src, nullptr, ncols, shared_item ? a.Is : I, hsm + (size_t)i * seg_halfs, hs_stride,
                      s_pexp[i]);
       __syncthreads();  // s_src / s_amax are reused by the next segment
     }
@@ -892,11 +1123,7 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
             const int col = 2 * c + (j & 1);
             const int row = tile * 16 + r + ((j & 2) ? 8 : 0);
             const int out = s_col_out[i][col];
-            if (out >= 0) {
-              const float val = acc[0][j] * exp2i(s_pexp[i][col]) * ts;
-              if (shared_item) a.S[(size_t)out * H + row] = val;
-              else a.P[(size_t)out * H + row] = val;
-            }
+            if (out >= 0) store_partial(a, shared_item, out, row, acc[0][j] * exp2i(s_pexp[i][col]) * ts);
           }
         };
         if (shared_item) {
@@ -938,18 +1165,22 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
         const int col = 2 * c + (j & 1);
         const int row = tile * 16 + r + ((j & 2) ? 8 : 0);
         const int out = s_col_out[i][col];
-        if (out >= 0) {
-          const float val = acc[0][j] * exp2i(s_pexp[i][col]) * ts;
-          if (shared_item) a.S[(size_t)out * H + row] = val;
-          else a.P[(size_t)out * H + row] = val;
-        }
+        if (out >= 0) store_partial(a, shared_item, out, row, acc[0][j] * exp2i(s_pexp[i][col]) * ts);
       }
     }
   }
 }
 
-// y[t] = bf16( sum_j w[t, j] * P[t*k + j] (+ S[t]) ), j ascending, after the
-// down kernel (programmatic dependent launch; waits for its completion).
+// y[t] = bf16( sum_j w[t, j] * P[t*k + j] (+ g_t S[t]) ), j ascending, after the
+// down kernel (programmatic dependent launch; waits for its completion).  g_t
+// is the shared expert's sigmoid gate when the layer has one, else 1.
+__device__ __forceinline__ float4 load_partial4(const float* base, size_t row, int H, int c4, int bf16) {
+  if (!bf16) return __ldcg(reinterpret_cast<const float4*>(base + row * H) + c4);
+  const uint2 v = __ldcg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + row * H) + c4);
+  return make_float4(bf16_bits_to_float(v.x & 0xFFFF), bf16_bits_to_float(v.x >> 16), bf16_bits_to_float(v.y & 0xFFFF),
+                     bf16_bits_to_float(v.y >> 16));
+}
+
 template <int FS>
 __global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
   pdl_launch_dependents();
@@ -965,7 +1196,7 @@ __global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
   for (int j = 0; j < 16; ++j)
     if (j < k) {
       wj[j] = __ldcg(a.rb.topk_w + t * k + j);
-      pj[j] = __ldcg(reinterpret_cast<const float4*>(a.P + (size_t)(t * k + j) * H) + c4);
+      pj[j] = load_partial4(a.P, (size_t)(t * k + j), H, c4, a.p_bf16);
     }
   float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -977,11 +1208,12 @@ __global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
       y[3] = __fmaf_rn(wj[j], pj[j].w, y[3]);
     }
   if (FS) {
-    const float4 sv = __ldcg(reinterpret_cast<const float4*>(a.S + (size_t)t * H) + c4);
-    y[0] = __fadd_rn(y[0], sv.x);
-    y[1] = __fadd_rn(y[1], sv.y);
-    y[2] = __fadd_rn(y[2], sv.z);
-    y[3] = __fadd_rn(y[3], sv.w);
+    const float4 sv = load_partial4(a.S, (size_t)t, H, c4, a.p_bf16);
+    const float g = a.shared_g ? __ldcg(a.shared_g + t) : 1.f;
+    y[0] = __fmaf_rn(g, sv.x, y[0]);
+    y[1] = __fmaf_rn(g, sv.y, y[1]);
+    y[2] = __fmaf_rn(g, sv.z, y[2]);
+    y[3] = __fmaf_rn(g, sv.w, y[3]);
   }
   const uint32_t lo = (uint32_t)float_to_bf16_bits(y[0]) | ((uint32_t)float_to_bf16_bits(y[1]) << 16);
   const uint32_t hi = (uint32_t)float_to_bf16_bits(y[2]) | ((uint32_t)float_to_bf16_bits(y[3]) << 16);
@@ -1025,6 +1257,7 @@ cudaError_t launch_expert_pair(int sfmt, bool down, const ExpertArgs& a, size_t 
     QMOE_CASE(MOE_FMT_INT4_G64)
     QMOE_CASE(MOE_FMT_INT8_G64)
     QMOE_CASE(MOE_FMT_FP8_B128)
+    QMOE_CASE(MOE_FMT_INT4_G128)
 #undef QMOE_CASE
     default: return cudaErrorInvalidValue;
   }

@@ -35,14 +35,17 @@ struct RouteOut {
 
 struct RouterArgs {
   int H, E, k, T;
-  int wpr;            // warps per expert row (the row's columns are split between them)
+  int wpr;            // warps per expert row of the approximate pass
+  int bias_select;    // 1: the bias steers the selection only, the weights use the unbiased logits
   const uint16_t* x;  // bf16 [T, H]
   const float* w;     // [E, H]
   const float* bias;  // [E] or nullptr
   RouteBufs rb;
   RouteOut out;
-  uint32_t* h_amax;   // [T*k] per-pair max |h| (float bits), zeroed here
-  uint32_t* hs_amax;  // [T] per-token max |h| of the shared expert, zeroed here
+  float* approx;      // [T, E] approximate logits (no bias)
+  float* rwnorm;      // [E] ||Wr_e||_2 (FP32)
+  const float* sgate_w;  // [H] gate vector of the shared expert, or nullptr
+  float* sgate;       // [T] sigmoid(x_t . sgate_w) (written when sgate_w is set)
 };
 
 // Decode-path expert kernels.
@@ -54,8 +57,6 @@ struct ExpertArgs {
   RouteBufs rb;
   uint16_t* h;        // bf16 [T*k, I]
   uint16_t* hs;       // bf16 [T, Is]
-  uint32_t* h_amax;   // [T*k] max |h| per pair (float bits, atomicMax)
-  uint32_t* hs_amax;  // [T]
   float* P;           // f32 [T*k, H] per-pair down partials
   float* S;           // f32 [T, H] shared expert output
   uint16_t* y;        // bf16 [T, H]
@@ -70,6 +71,8 @@ struct ExpertArgs {
   int xs_tok_stride;  // halfs per staged token row (gate/up)
   int hs_tok_stride;  // halfs per staged hidden row (down)
   int dn_segs;        // expert segments the down kernel stages at once (1 .. kMaxDnSegs)
+  const float* shared_g;  // [T] sigmoid gate of the shared expert per token, or nullptr (weight 1)
+  int p_bf16;         // 1: P and S are stored as BF16 (the bf16-partials lever)
 };
 
 constexpr int kMaxDnSegs = 4;
@@ -97,6 +100,11 @@ int32_t check_decode_args(const moe_layer* layer, const void* x, int32_t T, cons
 // in *out if no call has used it on this device yet.
 int32_t noalloc_array_if_used(void** out);
 cudaError_t launch_router_decode(const RouterArgs& a, cudaStream_t s);
+// Caller-supplied top-k indices and weights copied into the workspace (and the shared expert's gate);
+// the gate/up kernel builds the dispatch index from them.
+cudaError_t launch_dispatch_ext(const RouterArgs& a, const int32_t* idx, const float* w, cudaStream_t s);
+// moe_route: the dispatch index of the router's choices.
+cudaError_t launch_route_dispatch(const RouterArgs& a, cudaStream_t s);
 // Gate/up (down = false) or down (down = true) for a routed format;
 // the shared format is selected at run time among the compiled instances.
 cudaError_t launch_expert_nvfp4(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
@@ -104,6 +112,7 @@ cudaError_t launch_expert_mxfp4(int sfmt, bool down, const ExpertArgs& a, size_t
 cudaError_t launch_expert_int4(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
 cudaError_t launch_expert_int8(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
 cudaError_t launch_expert_fp8(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
+cudaError_t launch_expert_int4g128(int sfmt, bool down, const ExpertArgs& a, size_t smem, cudaStream_t s);
 
 // ---------------------------------------------------------------- prefill --
 // Any token count.  Routing: FP32 approximate logits with a rigorous error
@@ -142,6 +151,10 @@ struct PrefillArgs {
   int logits_tc;
   uint16_t* rw_hi;      // bf16 [E, H] = bf16(Wr)
   uint16_t* rw_lo;      // bf16 [E, H] = bf16(Wr - hi)
+  int bias_select;      // 1: the bias steers the selection only (weights from the unbiased logits)
+  float* unbiased;      // [T, E] unbiased exact logits of the recomputed experts (bias_select)
+  uint64_t wait_ns;     // limit of every bounded device wait (nanoseconds)
+  int p_bf16;           // 1: the down GEMM writes P as BF16 (the bf16-partials lever)
   // NVFP4 W4A4 lever (act_quant = 1)
   int act_quant;
   uint8_t* xq;          // [T, H/2] E2M1 codes of x (16-element blocks)
@@ -187,7 +200,7 @@ cudaError_t launch_quantize_act_nvfp4(const uint16_t* x, int rows, int K, uint8_
 // Bytes of one matrix's codes / scales in a format.
 __host__ __device__ inline size_t data_bytes(int fmt, int N, int K) {
   switch (fmt) {
-    case MOE_FMT_NVFP4: case MOE_FMT_MXFP4: case MOE_FMT_INT4_G64: return (size_t)N * K / 2;
+    case MOE_FMT_NVFP4: case MOE_FMT_MXFP4: case MOE_FMT_INT4_G64: case MOE_FMT_INT4_G128: return (size_t)N * K / 2;
     case MOE_FMT_INT8_G64: case MOE_FMT_FP8_B128: return (size_t)N * K;
     default: return 0;
   }
@@ -199,6 +212,7 @@ __host__ __device__ inline size_t scale_bytes(int fmt, int N, int K) {
     case MOE_FMT_MXFP4: return (size_t)N * (K / 32);
     case MOE_FMT_INT4_G64: case MOE_FMT_INT8_G64: return (size_t)N * (K / 64) * 2;
     case MOE_FMT_FP8_B128: return (size_t)(N / 128) * (K / 128) * 4;
+    case MOE_FMT_INT4_G128: return (size_t)N * (K / 128) * 2;
     default: return 0;
   }
 }
@@ -207,7 +221,8 @@ __host__ __device__ inline size_t scale_bytes(int fmt, int N, int K) {
 // share of K must be a multiple of it.
 __host__ __device__ inline int decode_unit_k(int fmt) {
   switch (fmt) {
-    case MOE_FMT_NVFP4: case MOE_FMT_MXFP4: case MOE_FMT_INT4_G64: return 128;  // 16 bytes per lane
+    case MOE_FMT_NVFP4: case MOE_FMT_MXFP4: case MOE_FMT_INT4_G64: case MOE_FMT_INT4_G128:
+      return 128;  // 16 bytes per lane
     case MOE_FMT_INT8_G64: case MOE_FMT_FP8_B128: return 64;
     default: return 0;
   }

@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(kThreads) pf_hconv_kernel(PrefillArgs a) {
   if (lane == 0) a.hsig[pos] = sft;
 }
 
-// y[t] = bf16( sum_j w[t, j] * P[pos_of[t*k + j]] ), j ascending.
+// y[t] = bf16( sum_j w[t, j] * P[pos_of[t*k + j]] ), j ascending (P in FP32, or in
+// BF16 under the bf16-partials lever).
 __global__ void __launch_bounds__(kThreads) pf_combine_kernel(PrefillArgs a) {
   const int t = blockIdx.x, H = a.H, k = a.k;
   const float* wt = a.rb.topk_w + (size_t)t * k;
@@ -332,7 +333,14 @@ __global__ void __launch_bounds__(kThreads) pf_combine_kernel(PrefillArgs a) {
     for (int j = 0; j < k; ++j) {
       const float w = __ldg(wt + j);
       const int pos = __ldg(a.pos_of + (size_t)t * k + j);
-      const float4 p = __ldcs(reinterpret_cast<const float4*>(a.P + (size_t)pos * H) + c);
+      float4 p;
+      if (a.p_bf16) {  // the bf16-partials lever: partials stored as BF16
+        const uint2 v = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(a.P) + (size_t)pos * H) + c);
+        p = make_float4(bf16_bits_to_float(v.x & 0xFFFF), bf16_bits_to_float(v.x >> 16), bf16_bits_to_float(v.y & 0xFFFF),
+                        bf16_bits_to_float(v.y >> 16));
+      } else {
+        p = __ldcs(reinterpret_cast<const float4*>(a.P + (size_t)pos * H) + c);
+      }
       acc.x = fmaf(w, p.x, acc.x);
       acc.y = fmaf(w, p.y, acc.y);
       acc.z = fmaf(w, p.z, acc.z);

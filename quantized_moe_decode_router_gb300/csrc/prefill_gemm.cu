@@ -48,7 +48,7 @@ constexpr int NT = kPfTokTile;  // tokens per tile (MMA N at most)
 constexpr int BK = 64;          // K per step (f16: 128 bytes per row)
 constexpr int KB = BK * 2;
 constexpr int kDec = 256;       // decode threads (8 warps)
-constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s of global timer per wait
+constexpr uint64_t kDrainLimit = 2000000000ull;  // 2 s: waits that drain copies and MMAs already issued
 
 template <bool DOWN>
 struct Cfg {
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
           out[c] = make_uint4(hmul2_u32(v[0], sc), hmul2_u32(v[1], sc), hmul2_u32(v[2], sc), hmul2_u32(v[3], sc));
         }
         const int stage = g % C::SA;
-        if (!tc::bar_wait(&empty_a[stage], ((g / C::SA) & 1) ^ 1, kWaitLimit)) {
+        if (!tc::bar_wait(&empty_a[stage], ((g / C::SA) & 1) ^ 1, a.wait_ns)) {
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x300 | (DOWN ? 1 : 0));
           ok = false;
           break;
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
 #pragma unroll 1
       for (int s = 0; s < nsteps; ++s, ++g) {
         const int stage = g % C::SB;
-        if (!tc::bar_wait(&empty_b[stage], ((g / C::SB) & 1) ^ 1, kWaitLimit)) {
+        if (!tc::bar_wait(&empty_b[stage], ((g / C::SB) & 1) ^ 1, a.wait_ns)) {
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x320 | (DOWN ? 1 : 0));
           ok = false;
           break;
@@ -213,6 +213,9 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         if (lane == 0) tc::tma_load_2d(B, &tmB, s * BK, pos0, &full_b[stage]);
       }
     }
+    // every load this warp issued has landed before the CTA can exit (the MMA warp may have stopped early)
+    if (lane == 0) tc::drain_loads(full_b, C::SB, g, kDrainLimit);
+    __syncwarp();
   } else if (warp == kWarpMma) {
     // -------------------------------------------------------------- MMA --
     if (lane == 0) {
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         const int n_mma = (n_valid + 15) & ~15;
         const uint32_t idesc = tc::idesc_f16(BM, n_mma, 0);
         const int buf = item & 1;
-        if (!tc::bar_wait(&acc_empty[buf], ((item >> 1) & 1) ^ 1, kWaitLimit)) {
+        if (!tc::bar_wait(&acc_empty[buf], ((item >> 1) & 1) ^ 1, a.wait_ns)) {
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x330 | (DOWN ? 1 : 0));
           break;
         }
@@ -234,8 +237,8 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
 #pragma unroll 1
         for (int s = 0; s < nsteps; ++s, ++g) {
           const int sa = g % C::SA, sb = g % C::SB;
-          if (!tc::bar_wait(&full_a[sa], (g / C::SA) & 1, kWaitLimit) ||
-              !tc::bar_wait(&full_b[sb], (g / C::SB) & 1, kWaitLimit)) {
+          if (!tc::bar_wait(&full_a[sa], (g / C::SA) & 1, a.wait_ns) ||
+              !tc::bar_wait(&full_b[sb], (g / C::SB) & 1, a.wait_ns)) {
             report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x340 | (DOWN ? 1 : 0));
             ok = false;
             break;
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         tc::commit(&acc_full[buf]);
       }
       tc::commit(&drain);
-      tc::bar_wait(&drain, 0, kWaitLimit);
+      tc::bar_wait(&drain, 0, kDrainLimit);
     }
     __syncwarp();
   } else {
@@ -288,12 +291,12 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         else un_c[i] = exp2i(-a.xsig[a.rb.pair[pos_l] / k]);
       }
       const float tsg = DOWN ? 0.f : __ldg(a.gate.ts + e), tsu = DOWN ? 0.f : __ldg(a.up.ts + e);
-      if (!tc::bar_wait(&acc_full[buf], (item >> 1) & 1, kWaitLimit)) {
-        report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x310 | (DOWN ? 1 : 0));
-        break;
-      }
+      const bool ready = tc::bar_wait(&acc_full[buf], (item >> 1) & 1, a.wait_ns);
+      if (!ready) report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x310 | (DOWN ? 1 : 0));
+      // all epilogue warps go on, or all stop; the barrier also frees the staging tile
+      // (the previous tile's copies have read it)
+      if (!tc::named_all(1, kEpiThreads, ready)) break;
       tc::fence_after_sync();
-      tc::named_sync(1, kEpiThreads);  // staging free: the previous tile's copies have read it
       const uint32_t acc = tq + buf * C::ACC_COLS;
       const int row = q * 32 + lane;
 #pragma unroll
@@ -321,10 +324,15 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
           tc::tmem_ld32(acc + c0, dv);
           tc::tmem_ld_wait();
           float* st32 = reinterpret_cast<float*>(stg) + (size_t)c0 * BM + row;
+          uint16_t* sb16 = reinterpret_cast<uint16_t*>(stg) + (size_t)c0 * BM + row;  // bf16-partials lever
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float un = __shfl_sync(0xFFFFFFFFu, un_c[i], j);
-            if (j < ncol) st32[j * BM] = __uint_as_float(dv[j]) * un;
+            if (j < ncol) {
+              const float v = __uint_as_float(dv[j]) * un;
+              if (a.p_bf16) sb16[j * BM] = float_to_bf16_bits(v);
+              else st32[j * BM] = v;
+            }
           }
         }
       }
@@ -335,7 +343,9 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
       if (ew == 0) {
         for (int c = lane; c < n_valid; c += 32) {
           const int pos = pos0 + c;
-          if (DOWN) {
+          if (DOWN && a.p_bf16) {
+            tc::bulk_store(reinterpret_cast<uint16_t*>(a.P) + (size_t)pos * H + rt * BM, stg + c * BM * 2, BM * 2);
+          } else if (DOWN) {
             tc::bulk_store(a.P + (size_t)pos * H + rt * BM, stg + c * BM * 4, BM * 4);
           } else {
             tc::bulk_store(a.h + (size_t)pos * I + rt * BM, stg + c * BM * 2, BM * 2);

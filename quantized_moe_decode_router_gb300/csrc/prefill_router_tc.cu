@@ -32,7 +32,7 @@ constexpr int STAGE_BYTES = 3 * TILE_BYTES;          // x, hi, lo
 constexpr int STG_OFF = NS * STAGE_BYTES;            // epilogue staging [TT][TE] f32
 constexpr int SMEM = STG_OFF + TT * TE * 4 + 1024;
 constexpr int kThreads = 256;                        // warp 0 TMA, warp 1 MMA, warps 4-7 epilogue
-constexpr uint64_t kWaitLimit = 2000000000ull;
+constexpr uint64_t kDrainLimit = 2000000000ull;  // 2 s: waits that drain copies and MMAs already issued
 
 // hi = bf16(w), lo = bf16(w - hi), element-wise over the router matrix.
 __global__ void __launch_bounds__(256) wsplit_kernel(const float* __restrict__ w, uint16_t* hi, uint16_t* lo, long n) {
@@ -78,9 +78,10 @@ __global__ void __launch_bounds__(kThreads, 1) logits_tc_kernel(PrefillArgs a, c
 
   if (warp == 0) {
     if (lane == 0) {
+      uint32_t issued = 0;
       for (int s = 0; s < nst; ++s) {
         const int st = s % NS;
-        if (!tc::bar_wait(&empty[st], ((s / NS) & 1) ^ 1, kWaitLimit)) {
+        if (!tc::bar_wait(&empty[st], ((s / NS) & 1) ^ 1, a.wait_ns)) {
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x500);
           break;
         }
@@ -89,7 +90,10 @@ __global__ void __launch_bounds__(kThreads, 1) logits_tc_kernel(PrefillArgs a, c
         tc::tma_load_2d(b, &tmX, s * BK, t0, &full[st]);
         tc::tma_load_2d(b + TILE_BYTES, &tmHi, s * BK, e0, &full[st]);
         tc::tma_load_2d(b + 2 * TILE_BYTES, &tmLo, s * BK, e0, &full[st]);
+        ++issued;
       }
+      // every load issued has landed before the CTA can exit (the MMA warp may have stopped early)
+      tc::drain_loads(full, NS, issued, kDrainLimit);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -98,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_tc_kernel(PrefillArgs a, c
       bool ok = true;
       for (int s = 0; s < nst; ++s) {
         const int st = s % NS;
-        if (!tc::bar_wait(&full[st], (s / NS) & 1, kWaitLimit)) {
+        if (!tc::bar_wait(&full[st], (s / NS) & 1, a.wait_ns)) {
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x510);
           ok = false;
           break;
@@ -115,14 +119,16 @@ __global__ void __launch_bounds__(kThreads, 1) logits_tc_kernel(PrefillArgs a, c
       }
       (void)ok;
       tc::commit(&done);  // also the drain: every MMA of this CTA completes before TMEM is freed
-      tc::bar_wait(&done, 0, kWaitLimit);
+      tc::bar_wait(&done, 0, kDrainLimit);
     }
     __syncwarp();
   } else if (warp >= 4) {
     // epilogue: lanes = tokens of the tile, columns = experts
     const int q = warp & 3;
     float* stg = reinterpret_cast<float*>(smem + STG_OFF);
-    if (tc::bar_wait(&done, 0, kWaitLimit)) {
+    // the four epilogue warps go on together or stop together (no warp left at the barrier below)
+    const bool ready = tc::bar_wait(&done, 0, kDrainLimit);
+    if (tc::named_all(2, 128, ready)) {
       tc::fence_after_sync();
       const int row = q * 32 + lane;
 #pragma unroll 1

@@ -40,7 +40,7 @@ constexpr int NT = kPfTokTile;
 constexpr int KS = 256;        // K per stage
 constexpr int KSB = KS / 2;    // bytes of codes per row per stage
 constexpr int ST = 3;          // stages
-constexpr uint64_t kWaitLimit = 2000000000ull;
+constexpr uint64_t kDrainLimit = 2000000000ull;  // 2 s: waits that drain copies and MMAs already issued
 constexpr int kThreads = 512;
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSf0 = 4, kWarpEpi0 = 8;
 constexpr int kEpiThreads = 256;
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
         bool ok = true;
         for (int s = 0; s < nst; ++s, ++g) {
           const int stage = g % ST;
-          if (!tc::bar_wait(&empty[stage], ((g / ST) & 1) ^ 1, kWaitLimit)) {
+          if (!tc::bar_wait(&empty[stage], ((g / ST) & 1) ^ 1, a.wait_ns)) {
             report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x400 | (DOWN ? 1 : 0));
             ok = false;
             break;
@@ -171,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
         }
         if (!ok) break;
       }
+      // every load issued has landed before the CTA can exit (the MMA warp may have stopped early)
+      tc::drain_loads(full, ST, g, kDrainLimit);
     }
     __syncwarp();
   } else if (warp >= kWarpSf0 && warp < kWarpSf0 + 4) {
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
           load_scales(W.scales + (size_t)e * N * Kb, Kb, rt * BM, lane, N, s * 16, v[m]);
         }
         load_scales(sfb_base, Kb, pos0, lane, P, s * 16, v[C::NMAT]);
-        if (!tc::bar_wait(&empty[stage], ((g / ST) & 1) ^ 1, kWaitLimit)) {
+        if (!tc::bar_wait(&empty[stage], ((g / ST) & 1) ^ 1, a.wait_ns)) {
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x410 | (DOWN ? 1 : 0));
           ok = false;
           break;
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
         const int n_valid = min(NT, a.rb.off[tile.x + 1] - tile.y);
         const uint32_t idesc = idesc_nvf4((n_valid + 15) & ~15);
         const int buf = DOWN ? (item & 1) : 0, use = DOWN ? (item >> 1) : item;
-        if (!tc::bar_wait(&acc_empty[buf], (use & 1) ^ 1, kWaitLimit)) {
+        if (!tc::bar_wait(&acc_empty[buf], (use & 1) ^ 1, a.wait_ns)) {
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x420 | (DOWN ? 1 : 0));
           break;
         }
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
         for (int s = 0; s < nst; ++s, ++g) {
           const int stage = g % ST;
           const uint32_t par = (g / ST) & 1;
-          if (!tc::bar_wait(&full[stage], par, kWaitLimit) || !tc::bar_wait(&sf_full[stage], par, kWaitLimit)) {
+          if (!tc::bar_wait(&full[stage], par, a.wait_ns) || !tc::bar_wait(&sf_full[stage], par, a.wait_ns)) {
             report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x430 | (DOWN ? 1 : 0));
             ok = false;
             break;
@@ -253,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
         tc::commit(&acc_full[buf]);
       }
       tc::commit(&drain);
-      tc::bar_wait(&drain, 0, kWaitLimit);
+      tc::bar_wait(&drain, 0, kDrainLimit);
     }
     __syncwarp();
   } else if (warp >= kWarpEpi0) {
@@ -270,12 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
       const int buf = DOWN ? (item & 1) : 0, use = DOWN ? (item >> 1) : item;
       const float ts0 = __ldg((DOWN ? a.down.ts : a.gate.ts) + e);
       const float ts1 = DOWN ? 0.f : __ldg(a.up.ts + e);
-      if (!tc::bar_wait(&acc_full[buf], use & 1, kWaitLimit)) {
-        report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x440 | (DOWN ? 1 : 0));
-        break;
-      }
+      const bool ready = tc::bar_wait(&acc_full[buf], use & 1, a.wait_ns);
+      if (!ready) report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x440 | (DOWN ? 1 : 0));
+      // all epilogue warps go on, or all stop; the barrier also frees the staging tile
+      if (!tc::named_all(1, kEpiThreads, ready)) break;
       tc::fence_after_sync();
-      tc::named_sync(1, kEpiThreads);  // staging free: the previous tile's copies have read it
       const uint32_t acc = tq + buf * C::ACC_COLS;
       const int row = q * 32 + lane;
 #pragma unroll
@@ -299,9 +300,14 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
           tc::tmem_ld32(acc + c0, dv);
           tc::tmem_ld_wait();
           float* st32 = reinterpret_cast<float*>(stg) + (size_t)c0 * BM + row;
+          uint16_t* sb16 = reinterpret_cast<uint16_t*>(stg) + (size_t)c0 * BM + row;  // bf16-partials lever
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j < ncol) st32[j * BM] = __uint_as_float(dv[j]) * ts0;
+            if (j < ncol) {
+              const float v = __uint_as_float(dv[j]) * ts0;
+              if (a.p_bf16) sb16[j * BM] = float_to_bf16_bits(v);
+              else st32[j * BM] = v;
+            }
         }
       }
       tc::fence_before_sync();
@@ -343,7 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
       if (ew == 0) {
         for (int c = lane; c < n_valid; c += 32) {
           const int pos = pos0 + c;
-          if (DOWN) tc::bulk_store(a.P + (size_t)pos * H + rt * BM, stg + c * BM * 4, BM * 4);
+          if (DOWN && a.p_bf16)
+            tc::bulk_store(reinterpret_cast<uint16_t*>(a.P) + (size_t)pos * H + rt * BM, stg + c * BM * 2, BM * 2);
+          else if (DOWN) tc::bulk_store(a.P + (size_t)pos * H + rt * BM, stg + c * BM * 4, BM * 4);
           else tc::bulk_store(a.hq + (size_t)pos * (I / 2) + rt * (BM / 2), stg + NT * BM * 2 + c * (BM / 2), BM / 2);
         }
         tc::bulk_commit();

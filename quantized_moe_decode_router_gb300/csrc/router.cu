@@ -1,14 +1,14 @@
 // Router and dispatch for decode-sized batches (T <= 8).
 //
-// Logits: each expert row is split over `wpr` warps; every lane accumulates
-// the exact products x[t, h] * Wr[e, h] of its columns into a float-float
-// pair (Dot2), the pairs are merged across lanes and then across the row's
-// warps in a fixed order, and one final rounding gives the FP32 logit: the
-// correctly rounded value unless the exact dot product lies within ~2^-44
-// (relative) of an FP32 rounding midpoint.  The last CTA to finish (arrival
-// counter, no spinning) computes softmax + top-k per token with the token's
-// logits held in registers, then the dispatch index: per-expert counts,
-// offsets, the pair list as a stable counting sort, and the active experts.
+// Stage 1 (every SM): approximate FP32 logits by FMA with a rigorous error
+// bound, and the router rows' norms.  Stage 2 (one CTA per token): the
+// experts that can still reach the top-k (upper bound not below the k-th
+// largest lower bound) get the correctly rounded FP32 logit, a float-float
+// (Dot2) dot product rounded once; top-k with the fixed tie rule runs on those
+// exact logits, and the last CTA to finish (arrival counter, no spinning)
+// builds the dispatch index: per-expert counts, offsets, the pair list as a
+// stable counting sort, and the active experts.  The result equals selecting
+// from exact logits of every expert.
 //
 // DGPP README "Execution and performance": engine.expert_tile_list (routed
 // segments per expert); the top-k tie rule (logit descending, lower expert
@@ -21,6 +21,8 @@ namespace {
 
 constexpr int kMaxT = MOE_DECODE_MAX_TOKENS;
 constexpr int kWarpsR = kRouterThreads / 32;
+constexpr int kSelThreads = 512;  // threads of the per-token selection and of the external dispatch
+constexpr int kSelWarps = kSelThreads / 32;
 
 // Selection key of a candidate: larger logit first, equal logits -> smaller
 // expert id first, as one unsigned 64-bit maximum.  The float is mapped to
@@ -100,7 +102,7 @@ __device__ __forceinline__ void lane_best(const uint32_t (&key)[NQ], uint32_t& b
 // lane rescans its keys.
 template <int NQ>
 __device__ void topk_warp(const float* __restrict__ logits_row, int E, int k, int32_t* idx_out, float* w_out,
-                          int32_t* idx_out2, float* w_out2) {
+                          int32_t* idx_out2, float* w_out2, const float* __restrict__ wrow = nullptr) {
   const int lane = threadIdx.x & 31;
   // lane holds experts lane * NQ + q (q < NQ): consecutive logits, loaded as float4 when whole
   uint32_t key[NQ];
@@ -138,8 +140,15 @@ __device__ void topk_warp(const float* __restrict__ logits_row, int E, int k, in
     if (lane == j) { my_key = m; my_i = (int)id; }
   }
   // w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0); lane j holds term j, the sum
-  // is a fixed butterfly over the warp (lanes >= k contribute 0)
-  const float my_ex = lane < k ? expf(ord_value(my_key) - ord_value(key0)) : 0.f;
+  // is a fixed butterfly over the warp (lanes >= k contribute 0).  With wrow
+  // the weights use wrow's logits of the selected experts (bias_select).
+  float lj = ord_value(my_key), l0 = ord_value(key0);
+  if (wrow) {
+    const int id0 = __shfl_sync(0xFFFFFFFFu, my_i, 0);
+    lj = lane < k ? __ldcg(wrow + my_i) : 0.f;
+    l0 = __ldcg(wrow + id0);
+  }
+  const float my_ex = lane < k ? expf(lj - l0) : 0.f;
   float sum = my_ex;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
@@ -152,138 +161,52 @@ __device__ void topk_warp(const float* __restrict__ logits_row, int E, int k, in
   }
 }
 
-// Logits of this CTA's expert rows; returns after writing them to global memory.
-// The tokens are staged once per CTA in shared memory (x_s, [T][H] bf16) and
-// every lane holds its router-weight chunk in registers before the
-// float-float loop, so the loop itself issues no global loads.
-__device__ void router_logits_cta(const RouterArgs& a, const uint16_t* x_s, float (*s_hi)[kMaxT],
-                                  float (*s_lo)[kMaxT]) {
-  const int H = a.H, E = a.E, T = a.T, wpr = a.wpr;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int rows_per_cta = kWarpsR / wpr;
-  const int e = blockIdx.x * rows_per_cta + warp / wpr;
-  const int part = warp % wpr;
-  const int Hw = H / wpr;
-  float hi[kMaxT], lo[kMaxT];
+// Bitonic sort of one 64-bit key per lane across the warp, descending: after
+// it lane j holds the (j+1)-th largest key.  15 compare-exchange steps of a
+// shuffle each, instead of one warp reduction per extracted element.
+__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long v) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int t = 0; t < kMaxT; ++t) { hi[t] = 0.f; lo[t] = 0.f; }
-  if (e < E) {
-    const float4* wrow = reinterpret_cast<const float4*>(a.w + (size_t)e * H + (size_t)part * Hw);
-    const uint16_t* xp = x_s + (size_t)part * Hw;
-    constexpr int kPre = 4;  // float4 chunks of the row held per lane at once
-    for (int base = lane; base < Hw / 4; base += 32 * kPre) {
-      float4 wv[kPre];
+  for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
-      for (int j = 0; j < kPre; ++j)
-        if (base + 32 * j < Hw / 4) wv[j] = __ldg(wrow + base + 32 * j);
-#pragma unroll
-      for (int j = 0; j < kPre; ++j) {
-        const int h4 = base + 32 * j;
-        if (h4 < Hw / 4) {
-#pragma unroll
-          for (int t = 0; t < kMaxT; ++t) {
-            if (t < T) {
-              const uint2 xv = *reinterpret_cast<const uint2*>(xp + (size_t)t * H + h4 * 4);
-              dot2_step(bf16_bits_to_float(xv.x & 0xFFFF), wv[j].x, hi[t], lo[t]);
-              dot2_step(bf16_bits_to_float(xv.x >> 16), wv[j].y, hi[t], lo[t]);
-              dot2_step(bf16_bits_to_float(xv.y & 0xFFFF), wv[j].z, hi[t], lo[t]);
-              dot2_step(bf16_bits_to_float(xv.y >> 16), wv[j].w, hi[t], lo[t]);
-            }
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < kMaxT; ++t) {
-      if (t < T) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float h2 = __shfl_xor_sync(0xFFFFFFFFu, hi[t], o);
-          const float l2 = __shfl_xor_sync(0xFFFFFFFFu, lo[t], o);
-          dot2_merge(hi[t], lo[t], h2, l2);
-        }
-      }
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int t = 0; t < kMaxT; ++t) { s_hi[warp][t] = hi[t]; s_lo[warp][t] = lo[t]; }
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, v, stride);
+      // descending overall: within a bitonic block of `size`, the lower lane keeps the larger key when
+      // the block sorts descending (bit `size` of the lane is 0), the smaller one otherwise
+      const bool lower = (lane & stride) == 0;
+      const bool desc = (lane & size) == 0;
+      const bool keep_max = lower == desc;
+      v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
     }
   }
-  __syncthreads();
-  // the first warp of each row merges the row's parts in order and rounds once
-  if (e < E && part == 0 && lane < T) {
-    float h = s_hi[warp][lane], l = s_lo[warp][lane];
-    for (int p = 1; p < wpr; ++p) dot2_merge(h, l, s_hi[warp + p][lane], s_lo[warp + p][lane]);
-    float lg = __fadd_rn(h, l);
-    if (a.bias) lg = __fadd_rn(lg, __ldg(a.bias + e));
-    a.rb.logits[(size_t)lane * E + e] = lg;
-  }
+  return v;
 }
 
-__global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];  // dispatch scratch of the last CTA
-  __shared__ float s_hi[kWarpsR][kMaxT], s_lo[kWarpsR][kMaxT];
-  __shared__ int is_last;
-  const int H = a.H, E = a.E, T = a.T, k = a.k;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // the expert kernel that follows may be scheduled now: it stages the
-  // activations and then waits for this grid's results (griddepcontrol.wait)
-  asm volatile("griddepcontrol.launch_dependents;");
-  {
-    // stage the tokens (bf16 [T][H]) in shared memory
-    const uint4* xs = reinterpret_cast<const uint4*>(a.x);
-    uint4* xd = reinterpret_cast<uint4*>(smem);
-    for (int i = tid; i < T * H / 8; i += blockDim.x) xd[i] = __ldg(xs + i);
-  }
+// Counting-sort dispatch of the T*k routed pairs (one CTA, any block size):
+// per-expert counts, offsets (exclusive scan over E), the pair list grouped by
+// expert in ascending pair id (a stable counting sort), and the active experts
+// in ascending id.  Expert ids outside [0, E) are reported and left out.
+// Scratch: s_cnt [E], s_off [E + 1], s_idx [T*k] in shared memory.
+__device__ void dispatch_cta(const RouteBufs& rb, const RouteOut& out, int E, int P, int32_t* s_cnt,
+                             int32_t* s_off, int32_t* s_idx) {
+  __shared__ int s_wsum[32][2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x, nwarp = nthr >> 5;
+  for (int i = tid; i < E; i += nthr) s_cnt[i] = 0;
   __syncthreads();
-  router_logits_cta(a, reinterpret_cast<const uint16_t*>(smem), s_hi, s_lo);
-
-  // ---- last CTA: top-k and dispatch ----
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const uint32_t prev = atomicAdd(&a.rb.ctrl->router_arrive, 1u);
-    is_last = (prev == gridDim.x - 1);
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-
-  for (int t = warp; t < T; t += kWarpsR) {
-    const float* lr = a.rb.logits + (size_t)t * E;
-    int32_t* io = a.rb.topk_idx + t * k;
-    float* wo = a.rb.topk_w + t * k;
-    int32_t* io2 = a.out.topk_idx ? a.out.topk_idx + t * k : nullptr;
-    float* wo2 = a.out.topk_w ? a.out.topk_w + t * k : nullptr;
-    if (E <= 256) topk_warp<8>(lr, E, k, io, wo, io2, wo2);
-    else if (E <= 512) topk_warp<16>(lr, E, k, io, wo, io2, wo2);
-    else topk_warp<32>(lr, E, k, io, wo, io2, wo2);
-  }
-  // the expert kernels accumulate per-pair maxima with atomicMax: start them at zero
-  if (a.h_amax)
-    for (int i = tid; i < T * k; i += blockDim.x) a.h_amax[i] = 0u;
-  if (a.hs_amax)
-    for (int i = tid; i < T; i += blockDim.x) a.hs_amax[i] = 0u;
-  __syncthreads();
-
-  // dispatch (counting sort, stable in the pair id p = t*k + j)
-  int32_t* s_cnt = reinterpret_cast<int32_t*>(smem);  // [E]
-  int32_t* s_off = s_cnt + E;                         // [E + 1]
-  int32_t* s_idx = s_off + E + 1;                     // [T*k]
-  const int P = T * k;
-  for (int i = tid; i < E; i += blockDim.x) s_cnt[i] = 0;
-  __syncthreads();
-  for (int p = tid; p < P; p += blockDim.x) {
-    const int ex = __ldcg(a.rb.topk_idx + p);
+  for (int p = tid; p < P; p += nthr) {
+    int ex = __ldcg(rb.topk_idx + p);
+    if ((unsigned)ex >= (unsigned)E) {
+      report_error(rb.ctrl, (uint32_t)MOE_ERR_DEVICE_BAD_INDEX, 0x010);
+      ex = -1;
+    } else {
+      atomicAdd(&s_cnt[ex], 1);
+    }
     s_idx[p] = ex;
-    atomicAdd(&s_cnt[ex], 1);
   }
   __syncthreads();
   {
-    // exclusive scan over the E counts and over the active flags, by the whole
-    // CTA: each thread owns up to four consecutive experts
-    __shared__ int s_wsum[kWarpsR][2];
-    const int per = (E + kRouterThreads - 1) / kRouterThreads;  // <= 4 for E <= 1024
+    // exclusive scan over the counts and over the active flags; each thread owns up to four experts
+    const int per = (E + nthr - 1) / nthr;  // <= 4 for E <= 1024 and >= 256 threads
     const int e0 = tid * per;
     int c4[4], tot = 0, act = 0;
 #pragma unroll
@@ -310,21 +233,22 @@ __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArg
       const int e2 = e0 + q;
       if (q < per && e2 < E) {
         s_off[e2] = run;
-        a.rb.cnt[e2] = c4[q];
-        if (a.out.cnt) a.out.cnt[e2] = c4[q];
-        if (c4[q] > 0) a.rb.act[run_act++] = e2;
+        rb.cnt[e2] = c4[q];
+        if (out.cnt) out.cnt[e2] = c4[q];
+        if (c4[q] > 0) rb.act[run_act++] = e2;
         run += c4[q];
       }
     }
-    if (tid == kRouterThreads - 1) {
+    if (tid == nthr - 1) {
       s_off[E] = run;
-      a.rb.ctrl->n_active = run_act;
+      rb.ctrl->n_active = run_act;
     }
+    (void)nwarp;
   }
   __syncthreads();
-  for (int i = tid; i <= E; i += blockDim.x) {
-    a.rb.off[i] = s_off[i];
-    if (a.out.off) a.out.off[i] = s_off[i];
+  for (int i = tid; i <= E; i += nthr) {
+    rb.off[i] = s_off[i];
+    if (out.off) out.off[i] = s_off[i];
   }
   __syncthreads();  // the offsets are out: s_off now serves as the running position
   // pair positions: one warp walks the pairs in order, 32 at a time; equal
@@ -332,22 +256,389 @@ __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArg
   if (warp == 0) {
     for (int b = 0; b < P; b += 32) {
       const int p = b + lane;
-      const int ex = p < P ? s_idx[p] : -1 - lane;
+      const int ex0 = p < P ? s_idx[p] : -1;
+      const int ex = ex0 >= 0 ? ex0 : -1 - lane;
       const uint32_t peers = __match_any_sync(0xFFFFFFFFu, ex);
-      if (p < P) {
+      if (ex >= 0) {
         const int pos = s_off[ex] + __popc(peers & ((1u << lane) - 1u));
-        a.rb.pair[pos] = p;
-        if (a.out.pair) a.out.pair[pos] = p;
+        rb.pair[pos] = p;
+        if (out.pair) out.pair[pos] = p;
       }
       __syncwarp();
-      if (p < P && lane == 31 - __clz(peers)) s_off[ex] += __popc(peers);
+      if (ex >= 0 && lane == 31 - __clz(peers)) s_off[ex] += __popc(peers);
       __syncwarp();
     }
   }
-  if (tid == 0) {
-    a.rb.ctrl->router_arrive = 0;  // leave the counter at zero for the next call
-    a.rb.ctrl->gu_next = 0;        // task counter of the gate/up kernel that follows
+}
+
+// ---- experts-only calls: the caller's routing -------------------------------
+// One CTA: copies the caller's top-k indices and weights into the workspace
+// and computes the shared expert's gate per token when the layer has one (one
+// warp per token, the exact float-float dot product).  The gate/up kernel
+// builds the dispatch index from the copied ids and reports any outside
+// [0, E) as MOE_ERR_DEVICE_BAD_INDEX.
+__global__ void __launch_bounds__(kSelThreads) dispatch_ext_kernel(RouterArgs a, const int32_t* idx_in,
+                                                                    const float* w_in) {
+  const int E = a.E, T = a.T, k = a.k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  asm volatile("griddepcontrol.launch_dependents;");
+  for (int p = tid; p < T * k; p += kSelThreads) {
+    a.rb.topk_idx[p] = __ldg(idx_in + p);
+    a.rb.topk_w[p] = __ldg(w_in + p);
   }
+  if (a.sgate_w) {
+    for (int t = warp; t < T; t += kSelWarps) {
+      const float4* wrow = reinterpret_cast<const float4*>(a.sgate_w);
+      const uint2* xp = reinterpret_cast<const uint2*>(a.x + (size_t)t * a.H);
+      float hi = 0.f, lo = 0.f;
+      for (int q = lane; q < a.H / 4; q += 32) {
+        const float4 wv = __ldg(wrow + q);
+        const uint2 xv = __ldg(xp + q);
+        dot2_step(bf16_bits_to_float(xv.x & 0xFFFF), wv.x, hi, lo);
+        dot2_step(bf16_bits_to_float(xv.x >> 16), wv.y, hi, lo);
+        dot2_step(bf16_bits_to_float(xv.y & 0xFFFF), wv.z, hi, lo);
+        dot2_step(bf16_bits_to_float(xv.y >> 16), wv.w, hi, lo);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float h2 = __shfl_xor_sync(0xFFFFFFFFu, hi, o);
+        const float l2 = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+        dot2_merge(hi, lo, h2, l2);
+      }
+      if (lane == 0) a.sgate[t] = 1.f / (1.f + expf(-__fadd_rn(hi, lo)));
+    }
+  }
+  (void)E;
+}
+
+// ---- decode router, stage 1: approximate logits on every SM -----------------
+// Each expert row is split over `wpr` warps; a lane owns 8-column chunks of
+// its warp's share and issues every weight load of the row before using any.
+// Per token: a = sum_h x[t, h] * Wr[e, h] by FMA (exact products, one rounding
+// per addition: |a - dot| <= gamma_H sum |x w| <= gamma_H ||x_t|| ||Wr_e||
+// whatever the order of the additions).  Per row: ||Wr_e||^2 by FMA.
+constexpr int kApproxChunks = 2;  // 8-column chunks a lane holds in flight at once
+
+__global__ void __launch_bounds__(kRouterThreads) router_approx_kernel(RouterArgs a) {
+  __shared__ float s_acc[kWarpsR][kMaxT + 1];
+  const int H = a.H, E = a.E, T = a.T, wpr = a.wpr;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // the selection kernel that follows may start now: it reads the tokens, then waits for this grid
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int rows_per_cta = kWarpsR / wpr;
+  const int e = blockIdx.x * rows_per_cta + warp / wpr;
+  const int part = warp % wpr;
+  const int Hw = H / wpr, nch = Hw / 8;
+  float acc[kMaxT], nrm = 0.f;
+#pragma unroll
+  for (int t = 0; t < kMaxT; ++t) acc[t] = 0.f;
+  if (e < E) {
+    const float* wrow = a.w + (size_t)e * H + (size_t)part * Hw;
+    const uint16_t* xp = a.x + (size_t)part * Hw;
+    for (int c0 = lane; c0 < nch; c0 += 32 * kApproxChunks) {
+      // every load of this batch (weights, and the tokens' matching columns, clamped to a
+      // valid token so no load waits behind a branch) is issued before any is used
+      float4 wv[kApproxChunks][2];
+      uint4 xv[kApproxChunks][kMaxT];
+#pragma unroll
+      for (int j = 0; j < kApproxChunks; ++j) {
+        const int c = min(c0 + 32 * j, nch - 1);
+        wv[j][0] = __ldg(reinterpret_cast<const float4*>(wrow + 8 * c));
+        wv[j][1] = __ldg(reinterpret_cast<const float4*>(wrow + 8 * c + 4));
+#pragma unroll
+        for (int t = 0; t < kMaxT; ++t)
+          xv[j][t] = __ldg(reinterpret_cast<const uint4*>(xp + (size_t)min(t, T - 1) * H + 8 * c));
+      }
+#pragma unroll
+      for (int j = 0; j < kApproxChunks; ++j) {
+        if (c0 + 32 * j < nch) {
+          const float w8[8] = {wv[j][0].x, wv[j][0].y, wv[j][0].z, wv[j][0].w,
+                               wv[j][1].x, wv[j][1].y, wv[j][1].z, wv[j][1].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) nrm = fmaf(w8[i], w8[i], nrm);
+#pragma unroll
+          for (int t = 0; t < kMaxT; ++t) {
+            if (t < T) {
+              const uint32_t xw[4] = {xv[j][t].x, xv[j][t].y, xv[j][t].z, xv[j][t].w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                acc[t] = fmaf(bf16_bits_to_float(xw[i] & 0xFFFF), w8[2 * i], acc[t]);
+                acc[t] = fmaf(bf16_bits_to_float(xw[i] >> 16), w8[2 * i + 1], acc[t]);
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t)
+      if (t < T) acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
+    nrm += __shfl_xor_sync(0xFFFFFFFFu, nrm, o);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t) s_acc[warp][t] = acc[t];
+    s_acc[warp][kMaxT] = nrm;
+  }
+  __syncthreads();
+  // the first warp of each row adds the row's parts and writes a[t, e] and ||Wr_e||
+  if (e < E && part == 0 && lane <= T) {
+    const int slot = lane < T ? lane : kMaxT;
+    float v = s_acc[warp][slot];
+    for (int p = 1; p < wpr; ++p) v += s_acc[warp + p][slot];
+    if (lane < T) a.approx[(size_t)lane * E + e] = v;
+    else a.rwnorm[e] = sqrtf(v);
+  }
+}
+
+// ---- decode router, stage 2: exact logits of the candidates, top-k ----------
+// One CTA per token, one thread per expert (two when E > 512).  eps_e bounds
+// |a_e + b_e - l_e| for the FP32 logit l_e (the approximation's
+// gamma_H ||x|| ||Wr_e||, widened by 2^-8 for the rounding of the norms, plus
+// the FP32 additions of the bias and of the final rounding).  Any L not above
+// the k-th largest lower bound a - eps is a valid threshold: an expert whose
+// upper bound a + eps is below L has an exact logit below k others.  Here L is
+// the k-th largest of the per-warp top-2 lower bounds (k distinct experts
+// reach it), which admits about k + 1 candidates.  The candidates get the
+// exact float-float logit (Dot2, correctly rounded, as every logit of the
+// prefill router), top-k with the fixed tie rule runs on them, and the last
+// CTA to finish builds the dispatch index.
+constexpr int kSelRowChunk = 16;  // float4 columns a lane holds in flight during the exact dot product
+
+// Dynamic shared memory of router_select_kernel: x_t (H bf16) and five E-entry rows (lower and
+// upper bounds, candidate ids, candidate logits, the unbiased ones).
+size_t select_smem_bytes(int H, int E) { return (size_t)H * 2 + (size_t)5 * E * 4; }
+
+// Selection key: larger value first, equal values -> lower id first (one 64-bit maximum).
+__device__ __forceinline__ unsigned long long cand_key(float v, int e) {
+  return ((unsigned long long)ord_key(v) << 32) | (uint32_t)(~(uint32_t)e);
+}
+
+__global__ void __launch_bounds__(kSelThreads) router_select_kernel(RouterArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int H = a.H, E = a.E, T = a.T, k = a.k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = blockIdx.x;
+  uint16_t* s_x = reinterpret_cast<uint16_t*>(smem);
+  float* s_lo = reinterpret_cast<float*>(smem + (size_t)H * 2);  // [E]
+  float* s_hi = s_lo + E;                                          // [E]
+  int32_t* s_cand = reinterpret_cast<int32_t*>(s_hi + E);          // [E] candidate expert ids
+  float* s_cval = reinterpret_cast<float*>(s_cand + E);            // [E] exact selection logits of candidates
+  float* s_cunb = s_cval + E;                                      // [E] exact logits used by the weights
+  __shared__ uint32_t s_top2[kSelWarps][2];
+  __shared__ float s_red[kSelWarps];
+  __shared__ float s_L;
+  __shared__ int s_ncand;
+  asm volatile("griddepcontrol.launch_dependents;");
+  // the token is an input of the call: stage it and find ||x_t|| before waiting for stage 1
+  float ss = 0.f;
+  for (int i = tid; i < H / 8; i += kSelThreads) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H) + i);
+    reinterpret_cast<uint4*>(s_x)[i] = v;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float lo = bf16_bits_to_float(w[q] & 0xFFFF), hi = bf16_bits_to_float(w[q] >> 16);
+      ss = fmaf(lo, lo, ss);
+      ss = fmaf(hi, hi, ss);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  if (lane == 0) s_red[warp] = ss;
+  if (tid == 0) s_ncand = 0;
+  float bias_v[2] = {0.f, 0.f};
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int e = tid + r * kSelThreads;
+    if (a.bias && e < E) bias_v[r] = __ldg(a.bias + e);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __syncthreads();
+  float xn2 = lane < kSelWarps ? s_red[lane] : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) xn2 += __shfl_xor_sync(0xFFFFFFFFu, xn2, o);
+  // the FP32 sum of H squares is within gamma_H of the true one: widen by 2^-10 before the root
+  const float xnorm = sqrtf(xn2 * 1.0009765625f);
+  const float u = 5.9604645e-8f;  // 2^-24
+  const float gam = (float)H * u / (1.f - (float)H * u);
+  // bounds of this thread's experts (coalesced loads of stage 1's results)
+  float lo_v[2], hi_v[2];
+  uint32_t key[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int e = tid + r * kSelThreads;
+    lo_v[r] = hi_v[r] = 0.f;
+    key[r] = 0u;
+    if (e < E) {
+      const float d = __ldcg(a.approx + (size_t)t * E + e);
+      const float wn = __ldcg(a.rwnorm + e);
+      const float b = bias_v[r];
+      const float ab = __fadd_rn(d, b);
+      const float eps0 = gam * xnorm * wn * 1.00390625f;
+      const float eps = eps0 + 4.7683716e-7f * (fabsf(d) + fabsf(b) + eps0) + 1e-30f;
+      lo_v[r] = ab - eps;
+      hi_v[r] = ab + eps;
+      s_lo[e] = lo_v[r];
+      s_hi[e] = hi_v[r];
+      key[r] = ord_key(lo_v[r]);
+    }
+  }
+  // the warp's two largest lower bounds
+  {
+    uint32_t best = max(key[0], key[1]);
+    const uint32_t m1 = __reduce_max_sync(0xFFFFFFFFu, best);
+    const uint32_t holders = __ballot_sync(0xFFFFFFFFu, best == m1);
+    if (lane == __ffs(holders) - 1) best = min(key[0], key[1]);  // drop one copy of the maximum
+    const uint32_t m2 = __reduce_max_sync(0xFFFFFFFFu, best);
+    if (lane == 0) { s_top2[warp][0] = m1; s_top2[warp][1] = m2; }
+  }
+  __syncthreads();
+  // L = the k-th largest of those 32 lower bounds (k <= 16 <= 32 distinct experts stand behind them)
+  if (warp == 0) {
+    const unsigned long long v = warp_sort_desc(s_top2[lane >> 1][lane & 1]);
+    const uint32_t m = (uint32_t)__shfl_sync(0xFFFFFFFFu, v, k - 1);  // the k-th largest
+    // fewer than k experts behind the 32 values (small E): every expert is a candidate
+    if (lane == 0) s_L = m ? ord_value(m) : __int_as_float(0xFF800000);
+  }
+  __syncthreads();
+  // candidates: upper bound not below L; the others hold -inf in the workspace row
+  const float L = s_L;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int e = tid + r * kSelThreads;
+    const bool cand = e < E && !(hi_v[r] < L);
+    if (e < E && !cand) a.rb.logits[(size_t)t * E + e] = __int_as_float(0xFF800000);
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, cand);
+    int base = 0;
+    if (lane == 0 && bal) base = atomicAdd(&s_ncand, __popc(bal));
+    base = __shfl_sync(0xFFFFFFFFu, base, 0);
+    if (cand) s_cand[base + __popc(bal & ((1u << lane) - 1u))] = e;
+  }
+  __syncthreads();
+  // exact logits of the candidates, one warp per candidate, lanes on consecutive float4 columns;
+  // each lane loads its columns in chunks of kSelRowChunk before the float-float loop.  One more
+  // row (c == nc) is the shared expert's gate vector when the layer has one.
+  const int nc = s_ncand;
+  const int nrows = nc + (a.sgate_w ? 1 : 0);
+  for (int c = warp; c < nrows; c += kSelWarps) {
+    const bool gate_row = c == nc;
+    const int e = gate_row ? 0 : s_cand[c];
+    const float4* wrow = reinterpret_cast<const float4*>(gate_row ? a.sgate_w : a.w + (size_t)e * H);
+    const uint2* xp = reinterpret_cast<const uint2*>(s_x);
+    float hi = 0.f, lo = 0.f;
+    for (int q0 = lane; q0 < H / 4; q0 += 32 * kSelRowChunk) {
+      float4 wv[kSelRowChunk];
+#pragma unroll
+      for (int j = 0; j < kSelRowChunk; ++j)
+        if (q0 + 32 * j < H / 4) wv[j] = __ldg(wrow + q0 + 32 * j);
+#pragma unroll
+      for (int j = 0; j < kSelRowChunk; ++j) {
+        const int q = q0 + 32 * j;
+        if (q < H / 4) {
+          const uint2 xv = xp[q];
+          dot2_step(bf16_bits_to_float(xv.x & 0xFFFF), wv[j].x, hi, lo);
+          dot2_step(bf16_bits_to_float(xv.x >> 16), wv[j].y, hi, lo);
+          dot2_step(bf16_bits_to_float(xv.y & 0xFFFF), wv[j].z, hi, lo);
+          dot2_step(bf16_bits_to_float(xv.y >> 16), wv[j].w, hi, lo);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float h2 = __shfl_xor_sync(0xFFFFFFFFu, hi, o);
+      const float l2 = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+      dot2_merge(hi, lo, h2, l2);
+    }
+    if (lane == 0 && gate_row) {
+      // sigmoid of the correctly rounded FP32 gate logit
+      a.sgate[t] = 1.f / (1.f + expf(-__fadd_rn(hi, lo)));
+    } else if (lane == 0) {
+      const float lg = __fadd_rn(hi, lo);
+      const float b = a.bias ? __ldg(a.bias + e) : 0.f;
+      const float lb = a.bias ? __fadd_rn(lg, b) : lg;
+      // the approximation's bound must hold for every exact logit (self-check of the bound)
+      if (lg == lg && (lb < s_lo[e] || lb > s_hi[e])) report_error(a.rb.ctrl, (uint32_t)MOE_ERR_DEVICE_BAD_INDEX, 0x020);
+      s_cval[c] = lb;
+      // bias_select: the bias decides the selection only; the weights use the unbiased logit
+      s_cunb[c] = a.bias_select ? lg : lb;
+      a.rb.logits[(size_t)t * E + e] = lb;
+    }
+  }
+  __syncthreads();
+  if (warp == 0 && nc <= 32) {
+    // top-k of the candidates (k <= nc <= 32): one key per lane (logit descending, id ascending),
+    // sorted across the warp; lane j then holds the j-th choice
+    const unsigned long long key = lane < nc ? cand_key(s_cval[lane], s_cand[lane]) : 0ull;
+    const unsigned long long sk = warp_sort_desc(key);
+    const int my_e = (int)(~(uint32_t)sk);
+    // the candidate slot of the chosen expert, for its (unbiased) weight logit
+    int slot = -1;
+    for (int c = 0; c < nc; ++c)
+      if (s_cand[c] == my_e) slot = c;
+    const int slot0 = __shfl_sync(0xFFFFFFFFu, slot, 0);
+    const float my_ex = lane < k ? expf(s_cunb[slot] - s_cunb[slot0]) : 0.f;
+    float sum = my_ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane < k) {
+      const float w = my_ex / sum;
+      a.rb.topk_idx[t * k + lane] = my_e;
+      a.rb.topk_w[t * k + lane] = w;
+      if (a.out.topk_idx) a.out.topk_idx[t * k + lane] = my_e;
+      if (a.out.topk_w) a.out.topk_w[t * k + lane] = w;
+    }
+  } else if (warp == 0) {
+    // more than 32 candidates (flat or tied logits): rounds of a warp maximum over
+    // (logit descending, id ascending); a lane holds candidates lane + 32 j
+    const int per = (nc + 31) / 32;
+    int my_c = -1, c0 = -1;
+    for (int j = 0; j < k; ++j) {
+      unsigned long long bkey = 0ull;
+      int bc = -1;
+      for (int q = 0; q < per; ++q) {
+        const int c = lane + 32 * q;
+        if (c < nc && s_cand[c] >= 0) {
+          const unsigned long long kk = cand_key(s_cval[c], s_cand[c]);
+          if (kk > bkey) { bkey = kk; bc = c; }
+        }
+      }
+      const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(bkey >> 32));
+      const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(bkey >> 32) == mhi ? (uint32_t)bkey : 0u);
+      const uint32_t win = __ballot_sync(0xFFFFFFFFu, bc >= 0 && (uint32_t)(bkey >> 32) == mhi && (uint32_t)bkey == mlo);
+      const int wl = __ffs(win) - 1;
+      const int wc = __shfl_sync(0xFFFFFFFFu, bc, wl);
+      if (lane == j) my_c = wc;
+      if (j == 0) c0 = wc;
+      if (lane == wl) s_cand[wc] = -1 - s_cand[wc];  // taken (ids stay recoverable)
+      __syncwarp();
+    }
+    const int my_e = lane < k ? -1 - s_cand[my_c] : 0;
+    const float my_ex = lane < k ? expf(s_cunb[my_c] - s_cunb[c0]) : 0.f;
+    float sum = my_ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane < k) {
+      const float w = my_ex / sum;
+      a.rb.topk_idx[t * k + lane] = my_e;
+      a.rb.topk_w[t * k + lane] = w;
+      if (a.out.topk_idx) a.out.topk_idx[t * k + lane] = my_e;
+      if (a.out.topk_w) a.out.topk_w[t * k + lane] = w;
+    }
+  }
+  // the dispatch index is built from these choices by the kernel that consumes them
+}
+
+// moe_route (T <= 8): the dispatch index of the selection kernel's choices (one CTA)
+__global__ void __launch_bounds__(kSelThreads) route_dispatch_kernel(RouterArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  int32_t* s_dcnt = reinterpret_cast<int32_t*>(smem);
+  int32_t* s_doff = s_dcnt + a.E;
+  int32_t* s_didx = s_doff + a.E + 1;
+  dispatch_cta(a.rb, a.out, a.E, a.T * a.k, s_dcnt, s_doff, s_didx);
 }
 
 // ---------------------------------------------------------------- prefill --
@@ -433,11 +724,12 @@ __device__ void prefill_topk_token(const PrefillArgs& a, int t) {
         const float l2 = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
         dot2_merge(hi, lo, h2, l2);
       }
-      float lg = __fadd_rn(hi, lo);
-      if (a.bias) lg = __fadd_rn(lg, __ldg(a.bias + e));
+      const float lu = __fadd_rn(hi, lo);
+      const float lg = a.bias ? __fadd_rn(lu, __ldg(a.bias + e)) : lu;
       const float aq = __shfl_sync(0xFFFFFFFFu, av[q], src), eq = __shfl_sync(0xFFFFFFFFu, ev[q], src);
       if (lane == 0) {
         row[e] = lg;
+        if (a.bias_select) a.unbiased[(size_t)t * E + e] = lu;
         if (fabsf(lg - aq) > eq && lg == lg) report_error(a.rb.ctrl, (uint32_t)MOE_ERR_DEVICE_BAD_INDEX, 0x200);
       }
     }
@@ -447,7 +739,8 @@ __device__ void prefill_topk_token(const PrefillArgs& a, int t) {
   float* wo = a.rb.topk_w + (size_t)t * k;
   int32_t* io2 = a.out.topk_idx ? a.out.topk_idx + (size_t)t * k : nullptr;
   float* wo2 = a.out.topk_w ? a.out.topk_w + (size_t)t * k : nullptr;
-  topk_warp<NQ>(row, E, k, io, wo, io2, wo2);
+  __syncwarp();
+  topk_warp<NQ>(row, E, k, io, wo, io2, wo2, a.bias_select ? a.unbiased + (size_t)t * E : nullptr);
 }
 
 __global__ void __launch_bounds__(kRouterThreads, 1) prefill_topk_kernel(PrefillArgs a) {
@@ -474,13 +767,35 @@ int router_warps_per_row(int H, int E, int sms) {
 cudaError_t launch_router_decode(const RouterArgs& a, cudaStream_t s) {
   const int rows_per_cta = kWarpsR / a.wpr;
   const int grid = (a.E + rows_per_cta - 1) / rows_per_cta;
-  // dispatch scratch of the last CTA, or the staged tokens before it (aliased)
-  const size_t disp = (size_t)(2 * a.E + 1 + a.T * a.k) * 4, xbytes = (size_t)a.T * a.H * 2;
-  const size_t smem = disp > xbytes ? disp : xbytes;
-  cudaError_t err = cudaFuncSetAttribute(router_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+  router_approx_kernel<<<grid, kRouterThreads, 0, s>>>(a);
+  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  router_decode_kernel<<<grid, kRouterThreads, smem, s>>>(a);
+  const size_t smem = select_smem_bytes(a.H, a.E);
+  if (smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(router_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.T);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, router_select_kernel, a);
+}
+
+cudaError_t launch_dispatch_ext(const RouterArgs& a, const int32_t* idx, const float* w, cudaStream_t s) {
+  dispatch_ext_kernel<<<1, kSelThreads, 0, s>>>(a, idx, w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_dispatch(const RouterArgs& a, cudaStream_t s) {
+  const size_t smem = ((size_t)2 * a.E + 1 + (size_t)a.T * a.k) * 4;
+  route_dispatch_kernel<<<1, kSelThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -185,6 +185,29 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier over `count` threads that also ANDs `pred` across them: every
+// participant gets the same answer, so a group of warps can agree to stop
+// (one warp's bounded wait gave up) without leaving the others at a barrier.
+__device__ __forceinline__ bool named_all(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// Waits (with the long limit) until the TMA loads behind the last `inflight`
+// phases of a ring of `stages` mbarriers have landed: load number i went to
+// barrier i % stages and completes its phase (i / stages) & 1.  A producer
+// that stopped early calls this before its CTA exits, so no copy still writes
+// shared memory after the CTA is gone.
+__device__ __forceinline__ void drain_loads(uint64_t* bars, int stages, uint32_t issued, uint64_t limit_ns) {
+  const uint32_t first = issued > (uint32_t)stages ? issued - (uint32_t)stages : 0u;
+  for (uint32_t i = first; i < issued; ++i) bar_wait(&bars[i % stages], (i / stages) & 1, limit_ns);
+}
+
 // Writes by this thread through the generic proxy (st.shared, cp.async)
 // become visible to the async proxy (tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

@@ -51,4 +51,8 @@ def to_device(host, device: Optional[str] = "cuda") -> Layer:
         lay.shared_gate = qweight_to_device(host.shared_gate, device)
         lay.shared_up = qweight_to_device(host.shared_up, device)
         lay.shared_down = qweight_to_device(host.shared_down, device)
+        gw = getattr(host, "extra", {}).get("shared_gate_w")
+        if gw is not None:
+            lay.shared_expert_gate = torch.from_numpy(np.ascontiguousarray(gw, dtype=np.float32)).to(device)
+    lay.bias_select = int(getattr(host, "extra", {}).get("bias_select", 0))
     return lay

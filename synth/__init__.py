@@ -22,13 +22,14 @@ from typing import Optional
 
 import numpy as np
 
-from .configs import (CONFIGS, FMT_FP8_B128, FMT_INT4_G64, FMT_INT8_G64, FMT_MXFP4, FMT_NVFP4, LayerConfig,
+from .configs import (CONFIGS, FMT_FP8_B128, FMT_INT4_G64, FMT_INT4_G128, FMT_INT8_G64, FMT_MXFP4, FMT_NVFP4,
+                      LayerConfig,
                       KIND_ROUTED, KIND_ROUTER, KIND_SHARED, KIND_TOKENS, KIND_ZIPF, WEIGHT_SIGMA)
 
 __all__ = [
     "CONFIGS", "LayerConfig", "QMat", "HostLayer", "make_layer", "make_tokens", "lib", "quantize",
     "normal_f32", "normal_bf16", "data_shape", "scale_shape", "FMT_NVFP4", "FMT_MXFP4", "FMT_INT4_G64",
-    "FMT_INT8_G64", "FMT_FP8_B128", "make_expert", "stream_key",
+    "FMT_INT8_G64", "FMT_FP8_B128", "FMT_INT4_G128", "make_expert", "stream_key",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -94,7 +95,7 @@ def normal_bf16(key: int, n: int, sigma: float, start: int = 0) -> np.ndarray:
 
 
 def data_shape(fmt: int, N: int, K: int) -> tuple:
-    if fmt in (FMT_NVFP4, FMT_MXFP4, FMT_INT4_G64):
+    if fmt in (FMT_NVFP4, FMT_MXFP4, FMT_INT4_G64, FMT_INT4_G128):
         return (N, K // 2)
     if fmt in (FMT_INT8_G64, FMT_FP8_B128):
         return (N, K)
@@ -111,6 +112,8 @@ def scale_shape(fmt: int, N: int, K: int) -> tuple:
         return (N, K // 64), np.uint16  # bf16 bit patterns
     if fmt == FMT_FP8_B128:
         return (N // 128, K // 128), np.float32
+    if fmt == FMT_INT4_G128:
+        return (N, K // 128), np.uint16  # f16 bit patterns
     raise ValueError(f"unknown format {fmt}")
 
 

@@ -17,9 +17,10 @@ FMT_MXFP4 = 2
 FMT_INT4_G64 = 3
 FMT_INT8_G64 = 4
 FMT_FP8_B128 = 5
+FMT_INT4_G128 = 6   # AutoRound / GPTQ layout: unsigned nibbles with zero point 8, FP16 scale per 128
 
 FMT_NAMES = {FMT_NVFP4: "nvfp4", FMT_MXFP4: "mxfp4", FMT_INT4_G64: "int4_g64", FMT_INT8_G64: "int8_g64",
-             FMT_FP8_B128: "fp8_b128"}
+             FMT_FP8_B128: "fp8_b128", FMT_INT4_G128: "int4_g128"}
 
 # Generator stream kinds (part of the stream key, see qmoe_synth.c).
 KIND_ROUTER = 1

@@ -41,7 +41,7 @@
 
 #define QS_GOLDEN 0x9E3779B97F4A7C15ull
 
-enum { QS_NVFP4 = 1, QS_MXFP4 = 2, QS_INT4_G64 = 3, QS_INT8_G64 = 4, QS_FP8_B128 = 5 };
+enum { QS_NVFP4 = 1, QS_MXFP4 = 2, QS_INT4_G64 = 3, QS_INT8_G64 = 4, QS_FP8_B128 = 5, QS_INT4_G128 = 6 };
 
 static inline uint64_t qs_mix(uint64_t z) {
   z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
@@ -237,6 +237,15 @@ static void qs_quant_mxfp4(const float* W, int N, int K, uint8_t* data, uint8_t*
   }
 }
 
+static double qs_f16_value(uint16_t b) {
+  const int e = (b >> 10) & 0x1F, m = b & 0x3FF;
+  double v;
+  if (e == 0) v = ldexp((double)m, -24);
+  else if (e == 31) v = m ? NAN : INFINITY;
+  else v = ldexp((double)(m | 0x400), e - 25);
+  return (b & 0x8000) ? -v : v;
+}
+
 static inline double qs_bf16_value(uint16_t b) {
   uint32_t u = (uint32_t)b << 16;
   float f;
@@ -277,6 +286,55 @@ static void qs_quant_int_g64(const float* W, int N, int K, int bits, uint8_t* da
   }
 }
 
+/* Nearest binary16 of a double (ties to even), as bits; overflow to infinity. */
+static uint16_t qs_f64_to_f16(double v) {
+  const uint16_t sign = signbit(v) ? 0x8000 : 0;
+  const double a = fabs(v);
+  if (isnan(v)) return 0x7E00;
+  if (a == 0.0) return sign;
+  if (a >= 65520.0) return (uint16_t)(sign | 0x7C00);
+  int ex;
+  frexp(a, &ex);
+  int E = ex - 1;                             /* 2^E <= a < 2^(E+1) */
+  if (E < -14) {                              /* subnormal: quantum 2^-24 */
+    const double q = nearbyint(ldexp(a, 24));
+    return (uint16_t)(sign | (uint16_t)q);    /* q == 1024 is the smallest normal, 0x0400 */
+  }
+  double q = nearbyint(ldexp(a, 10 - E));     /* 1024 .. 2048 */
+  if (q >= 2048.0) { q = 1024.0; ++E; }
+  if (E > 15) return (uint16_t)(sign | 0x7C00);
+  return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(q - 1024.0));
+}
+
+/* AutoRound / GPTQ-style int4 with group 128: s = f16(amax / 7) per 128
+ * columns, q = clamp(rne(x / s), -8, 7) stored as the unsigned nibble q + 8
+ * (zero point 8), low nibble = even k. */
+static void qs_quant_int4_g128(const float* W, int N, int K, uint8_t* data, uint16_t* sc) {
+  for (int n = 0; n < N; ++n) {
+    const float* row = W + (size_t)n * K;
+    for (int g = 0; g < K / 128; ++g) {
+      double agrp = 0.0;
+      for (int i = 0; i < 128; ++i) { double a = fabs((double)row[g * 128 + i]); if (a > agrp) agrp = a; }
+      const uint16_t sb = qs_f64_to_f16(agrp / 7.0);
+      sc[(size_t)n * (K / 128) + g] = sb;
+      const double s = qs_f16_value(sb);
+      for (int i = 0; i < 128; ++i) {
+        double q = 0.0;
+        if (s != 0.0) {
+          q = nearbyint((double)row[g * 128 + i] / s);
+          if (q > 7.0) q = 7.0;
+          if (q < -8.0) q = -8.0;
+        }
+        const uint8_t nib = (uint8_t)((int)q + 8);
+        const size_t k = (size_t)g * 128 + i;
+        uint8_t* p = data + (size_t)n * (K / 2) + k / 2;
+        if (k & 1) *p = (uint8_t)((*p & 0x0F) | (nib << 4));
+        else *p = (uint8_t)((*p & 0xF0) | nib);
+      }
+    }
+  }
+}
+
 static void qs_quant_fp8_b128(const float* W, int N, int K, uint8_t* data, float* sc) {
   for (int bn = 0; bn < N / 128; ++bn)
     for (int bk = 0; bk < K / 128; ++bk) {
@@ -304,13 +362,14 @@ int qs_quantize(int fmt, const float* W, int N, int K, void* data, void* scales,
     case QS_INT4_G64: if (K % 64) return -1; qs_quant_int_g64(W, N, K, 4, (uint8_t*)data, (uint16_t*)scales); *ts = 1.0f; return 0;
     case QS_INT8_G64: if (K % 64) return -1; qs_quant_int_g64(W, N, K, 8, (uint8_t*)data, (uint16_t*)scales); *ts = 1.0f; return 0;
     case QS_FP8_B128: if (K % 128 || N % 128) return -1; qs_quant_fp8_b128(W, N, K, (uint8_t*)data, (float*)scales); *ts = 1.0f; return 0;
+    case QS_INT4_G128: if (K % 128) return -1; qs_quant_int4_g128(W, N, K, (uint8_t*)data, (uint16_t*)scales); *ts = 1.0f; return 0;
     default: return -1;
   }
 }
 
 size_t qs_data_bytes(int fmt, int N, int K) {
   switch (fmt) {
-    case QS_NVFP4: case QS_MXFP4: case QS_INT4_G64: return (size_t)N * K / 2;
+    case QS_NVFP4: case QS_MXFP4: case QS_INT4_G64: case QS_INT4_G128: return (size_t)N * K / 2;
     case QS_INT8_G64: case QS_FP8_B128: return (size_t)N * K;
     default: return 0;
   }
@@ -322,6 +381,7 @@ size_t qs_scale_bytes(int fmt, int N, int K) {
     case QS_MXFP4: return (size_t)N * (K / 32);
     case QS_INT4_G64: case QS_INT8_G64: return (size_t)N * (K / 64) * 2;
     case QS_FP8_B128: return (size_t)(N / 128) * (K / 128) * 4;
+    case QS_INT4_G128: return (size_t)N * (K / 128) * 2;
     default: return 0;
   }
 }

@@ -107,6 +107,10 @@ def decode(layer, x_bits: np.ndarray, ws=None, prefill: bool = False, act_quant:
         "expert_off": ws_read(ws, lo.expert_off, np.int32, E + 1),
         "pair_list": ws_read(ws, lo.pair_list, np.int32, T * k),
     }
+    if act_quant:
+        I = layer.inter
+        routing["h_codes"] = ws_read(ws, lo.h_codes, np.uint8, T * k * I // 2).reshape(T * k, I // 2)
+        routing["h_scales"] = ws_read(ws, lo.h_scales, np.uint8, T * k * I // 16).reshape(T * k, I // 16)
     return y.cpu().numpy().view(np.uint16), routing
 
 
@@ -145,14 +149,20 @@ def route(layer, x_bits: np.ndarray):
 
 
 def assert_routing_matches(got: dict, ref: dict, near: np.ndarray):
-    """Bit-exact indices and dispatch; logits exact except oracle-flagged near-midpoint ones.
-    At decode sizes (a few thousand logits, about 2^-15 flagged per logit) none may be flagged,
-    so every logit is compared bit for bit."""
+    """Bit-exact indices and dispatch.  The router recomputes exactly every expert that
+    can still reach the top-k (the others hold -inf in the workspace's logits): those
+    logits are the correctly rounded value, except oracle-flagged near-midpoint ones, and
+    every selected expert is among them.  At decode sizes (a few thousand logits, about
+    2^-15 flagged per logit) none may be flagged, so every recomputed logit is compared
+    bit for bit."""
     lg, lr = got["logits"], ref["logits"]
     if lg.size <= 8 * 1024:
         assert not near.any(), f"{int(near.sum())} logits within 2^-40 of an FP32 midpoint at this seed"
-    diff = lg.view(np.uint32) != lr.view(np.uint32)
-    assert not np.any(diff & ~near), f"{int(np.sum(diff & ~near))} logits differ from the correctly rounded value"
+    recomputed = ~np.isneginf(lg)
+    diff = (lg.view(np.uint32) != lr.view(np.uint32)) & recomputed
+    assert not np.any(diff & ~near), f"{int(np.sum(diff & ~near))} recomputed logits differ from the correctly rounded value"
+    T, k = ref["topk_idx"].shape
+    assert np.all(recomputed[np.arange(T)[:, None], ref["topk_idx"]]), "a selected expert was not recomputed"
     np.testing.assert_array_equal(got["topk_idx"], ref["topk_idx"])
     np.testing.assert_array_equal(got["expert_cnt"], ref["expert_cnt"])
     np.testing.assert_array_equal(got["expert_off"], ref["expert_off"])

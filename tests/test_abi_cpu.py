@@ -102,10 +102,21 @@ def test_invalid_calls_rejected_before_launch(lib):
     assert f(ctypes.byref(L), FAKE, 1, FAKE, None, None, n, None) == B.MOE_ERR_WORKSPACE
     assert f(ctypes.byref(L), FAKE, 8, FAKE, None, FAKE, 1024, None) == B.MOE_ERR_WORKSPACE
     assert f(ctypes.byref(L), FAKE, 1, FAKE, None, FAKE + 16, n, None) == B.MOE_ERR_MISALIGNED
-    o = B.moe_options(1, (ctypes.c_int32 * 7)())
+    o = B._opts(act_quant=1)
     assert f(ctypes.byref(L), FAKE, 1, FAKE, ctypes.byref(o), FAKE, n, None) == B.MOE_ERR_UNSUPPORTED
-    o = B.moe_options(0, (ctypes.c_int32 * 7)(1, 0, 0, 0, 0, 0, 0))
+    o = B._opts()
+    o.reserved[0] = 1
     assert f(ctypes.byref(L), FAKE, 1, FAKE, ctypes.byref(o), FAKE, n, None) == B.MOE_ERR_INVALID_ARG
+    for bad in (dict(bf16_partials=2), dict(wait_limit_us=-1)):
+        o = B._opts(**bad)
+        assert f(ctypes.byref(L), FAKE, 1, FAKE, ctypes.byref(o), FAKE, n, None) == B.MOE_ERR_INVALID_ARG, bad
+    # a shared-expert gate without a shared expert, a bias mode outside 0/1
+    L4 = _layer()
+    L4.shared_expert_gate = FAKE
+    assert f(ctypes.byref(L4), FAKE, 1, FAKE, None, FAKE, n, None) == B.MOE_ERR_INVALID_ARG
+    L5 = _layer()
+    L5.bias_select = 2
+    assert f(ctypes.byref(L5), FAKE, 1, FAKE, None, FAKE, n, None) == B.MOE_ERR_INVALID_ARG
     # a missing NVFP4 tensor scale, a misaligned weight pointer
     L2 = _layer()
     L2.gate.tensor_scale = None
@@ -136,7 +147,7 @@ def test_noalloc_rejects_bad_calls_before_touching_the_device(lib):
     assert f(ctypes.byref(L), FAKE, 1, FAKE + 4, None, None) == B.MOE_ERR_MISALIGNED
     assert f(ctypes.byref(L), FAKE, 0, FAKE, None, None) == B.MOE_ERR_INVALID_ARG
     assert f(ctypes.byref(L), FAKE, 9, FAKE, None, None) == B.MOE_ERR_UNSUPPORTED        # as moe_decode_forward
-    o = B.moe_options(1, (ctypes.c_int32 * 7)())
+    o = B._opts(act_quant=1)
     assert f(ctypes.byref(L), FAKE, 1, FAKE, ctypes.byref(o), None) == B.MOE_ERR_UNSUPPORTED
     assert f(None, FAKE, 1, FAKE, None, None) == B.MOE_ERR_INVALID_ARG
     big = _layer(hidden=16384, inter=8192, n_experts=1024, top_k=16)

@@ -14,7 +14,8 @@ from oracle import formats as F
 from oracle import moe as M
 from quantized_moe_decode_router_gb300 import _binding as B
 from quantized_moe_decode_router_gb300.device import qweight_to_device, to_device
-from synth.configs import FMT_FP8_B128, FMT_INT4_G64, FMT_INT8_G64, FMT_MXFP4, FMT_NVFP4, LayerConfig
+from synth.configs import (FMT_FP8_B128, FMT_INT4_G64, FMT_INT4_G128, FMT_INT8_G64, FMT_MXFP4, FMT_NVFP4,
+                           LayerConfig)
 from tests import gpu_util as G
 
 pytestmark = pytest.mark.gpu
@@ -32,7 +33,7 @@ def _f32_bits(a):
 
 
 @pytest.mark.parametrize("fmt,N,K", [(FMT_NVFP4, 256, 512), (FMT_MXFP4, 256, 512), (FMT_INT4_G64, 256, 512),
-                                     (FMT_INT8_G64, 256, 512), (FMT_FP8_B128, 256, 512)])
+                                     (FMT_INT8_G64, 256, 512), (FMT_FP8_B128, 256, 512), (FMT_INT4_G128, 256, 512)])
 def test_dequantize_bit_exact(fmt, N, K):
     qm = synth.make_stack(fmt, 11, synth.KIND_ROUTED, 0, 0, 3, N, K)
     # adversarial codes: zero blocks, -0 nibbles, subnormal / NaN / signed scales, extreme exponents
@@ -46,6 +47,11 @@ def test_dequantize_bit_exact(fmt, N, K):
         qm.scales[1, :3, :] = np.array([0, 1, 254], dtype=np.uint8)[:, None] * np.ones((1, K // 32), np.uint8)
         qm.data[1, 2, :] = rng.integers(0, 256, K // 2).astype(np.uint8) & 0x33            # avoid fp32 overflow
         qm.scales[1, 3, 0] = 255                                                           # NaN
+    elif fmt == FMT_INT4_G128:
+        qm.scales[1, 0, :] = 0x8000                                                        # -0 scale
+        qm.scales[1, 1, :] = 0x0001                                                        # f16 subnormal
+        qm.scales[1, 2, :] = 0xC2F7                                                        # negative
+        qm.data[1, 3, :] = 0x08                                                            # codes 8 and 0: 0 and -8
     elif fmt in (FMT_INT4_G64, FMT_INT8_G64):
         qm.scales[1, 0, :] = 0x8000                                                        # -0 scale
         qm.scales[1, 1, :] = 0x0001                                                        # bf16 subnormal
@@ -218,6 +224,8 @@ SMALL = [
     LayerConfig("s_int8", FMT_INT8_G64, H=512, E=9, k=2, I=128, shared_fmt=FMT_NVFP4, shared_I=256),
     LayerConfig("s_fp8", FMT_FP8_B128, H=384, E=6, k=6, I=256, shared_fmt=FMT_MXFP4, shared_I=128),
     LayerConfig("s_nvfp4_k1", FMT_NVFP4, H=256, E=3, k=1, I=128),
+    LayerConfig("s_g128_int8", FMT_INT4_G128, H=768, E=10, k=3, I=256, shared_fmt=FMT_INT8_G64, shared_I=256),
+    LayerConfig("s_nvfp4_g128", FMT_NVFP4, H=512, E=8, k=2, I=128, shared_fmt=FMT_INT4_G128, shared_I=384),
 ]
 
 

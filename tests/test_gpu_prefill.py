@@ -149,20 +149,94 @@ W4A4 = [
 ]
 
 
-def _check_w4a4(y_bits, ref_bits, tokens=None):
-    """W4A4 against the oracle's act_quant mode.  x is quantised identically on
-    both sides (same rule, same BF16 input); h is re-quantised from a BF16 value
-    that the GPU reaches with FP32 accumulation, so a rare h can land on the
-    other side of a BF16 or E2M1 rounding boundary.  Bar: every element within
-    max(2 BF16 ulp, 1e-3) except at most 0.1 %, and those within 2^-5 relative."""
-    y = F.bf16_to_f64(y_bits if tokens is None else y_bits[tokens])
-    r = F.bf16_to_f64(ref_bits)
-    ok = M.within_tolerance(y, r)
+# Measured share of W4A4 outputs outside max(2 BF16 ulp, 1e-3) of the oracle's W4A4 mode (which
+# quantises the FP64 h): a few per mille, from the blocks the staged check below explains.
+W4A4_OUTLIER_CAP = 0.01
+
+
+def _bf16_neighbours(v):
+    """The BF16 values just below and just above each FP64 value (equal when v is a BF16 value)."""
+    b = F.f64_to_bf16_bits(v).astype(np.int64)
+    r = F.bf16_to_f64(b.astype(np.uint16))
+    lo = np.where(r <= v, r, F.bf16_to_f64(np.where(b & 0x8000, b + 1, b - 1).astype(np.uint16)))
+    hi = np.where(r >= v, r, F.bf16_to_f64(np.where(b & 0x8000, b - 1, b + 1).astype(np.uint16)))
+    return lo, hi
+
+
+def _check_w4a4(hl, x_bits, y_bits, routing, tokens=None):
+    """W4A4 parity in two exact stages.
+    (1) Down projection and combine: y equals, within max(2 BF16 ulp, 1e-3) everywhere, the oracle's
+        down projection and weighted combine applied to the GPU's own NVFP4 h (codes and scales read
+        from the workspace).
+    (2) Gate/up and the h quantiser: the GPU's h codes and scales equal the oracle's (the A9 rule
+        applied to bf16(silu(g) * u) of the quantised token, in FP64) on every 16-element block,
+        except blocks where some element's unrounded h lies within 2^-12 (relative) of a BF16
+        rounding midpoint and one choice of BF16 neighbours for those elements reproduces the GPU's
+        block exactly: the GPU reaches h with FP32 accumulation, so it may round such an h the
+        other way.  Any other difference fails.
+    Returns the share of outputs outside the 2-ulp bar of the oracle's own W4A4 result."""
+    cfg = hl.cfg
+    k, I, H = cfg.k, cfg.I, cfg.H
+    T = x_bits.shape[0]
+    want = np.arange(T) if tokens is None else np.asarray(sorted(tokens))
+    want_set = set(int(t) for t in want)
+    pair, off, w = routing["pair_list"], routing["expert_off"], routing["topk_w"]
+    codes = np.empty((T * k, I), dtype=np.uint8)
+    codes[:, 0::2] = routing["h_codes"] & 0xF
+    codes[:, 1::2] = routing["h_codes"] >> 4
+    sc = routing["h_scales"]
+    hq_gpu = M.nvfp4_dequantize_act(codes, sc)
+    Xq = M.nvfp4_fake_quant(F.bf16_to_f64(x_bits))
+    acc = {int(t): np.zeros(H) for t in want}
+    unexplained, mismatched, blocks = [], 0, 0
+    for e in range(cfg.E):
+        pos = [q for q in range(off[e], off[e + 1]) if int(pair[q]) // k in want_set]
+        if not pos:
+            continue
+        Wg, Wu, Wd = (F.decode_qmat(hl.gate, e), F.decode_qmat(hl.up, e), F.decode_qmat(hl.down, e))
+        rows = np.array([int(pair[q]) // k for q in pos])
+        h_pre = M.silu(Xq[rows] @ Wg.T) * (Xq[rows] @ Wu.T)
+        q_or, s_or = M.nvfp4_quantize_act(F.round_bf16(h_pre))
+        P = hq_gpu[pos] @ Wd.T
+        for i, q in enumerate(pos):
+            t, j = divmod(int(pair[q]), k)
+            acc[t] += float(w[t, j]) * P[i]
+            for b in range(I // 16):
+                blocks += 1
+                sl = slice(16 * b, 16 * b + 16)
+                if s_or[i, b] == sc[q, b] and np.array_equal(q_or[i, sl], codes[q, sl]):
+                    continue
+                mismatched += 1
+                hp = h_pre[i, sl]
+                lo, hi = _bf16_neighbours(hp)
+                near = np.abs(hp - (lo + hi) / 2) <= 2.0 ** -12 * np.abs(hp)
+                idx = np.flatnonzero(near & (lo != hi))
+                ok = False
+                if len(idx) <= 10:
+                    base = F.round_bf16(hp)
+                    for mask in range(1 << len(idx)):
+                        v = base.copy()
+                        for n, ii in enumerate(idx):
+                            v[ii] = hi[ii] if (mask >> n) & 1 else lo[ii]
+                        cq, cs = M.nvfp4_quantize_act(v[None, :])
+                        if cs[0, 0] == sc[q, b] and np.array_equal(cq[0], codes[q, sl]):
+                            ok = True
+                            break
+                if not ok:
+                    unexplained.append((q, b))
+    assert not unexplained, f"{len(unexplained)} of {blocks} h blocks differ beyond a BF16 rounding flip: {unexplained[:5]}"
+    assert mismatched <= 0.02 * blocks + 2, f"{mismatched} of {blocks} h blocks differ"
+    y = F.bf16_to_f64(y_bits if tokens is None else y_bits[want])
+    y_stage = np.stack([acc[int(t)] for t in want])
+    ok = M.within_tolerance(y, F.bf16_to_f64(F.f64_to_bf16_bits(y_stage)))
+    assert ok.all(), f"{int((~ok).sum())} of {ok.size} outputs differ from the down + combine of the GPU's h"
     assert np.isfinite(y).all()
-    frac_bad = float((~ok).mean())
-    assert frac_bad <= 1e-3, f"{int((~ok).sum())} of {ok.size} outputs outside the 2-ulp bar"
-    loose = np.abs(y - r) <= np.maximum(2.0 ** -5 * np.abs(r), 1e-2)
-    assert loose.all(), f"{int((~loose).sum())} outputs outside the loose bar"
+    ref = M.layer_forward(hl, x_bits, act_quant=True, tokens=tokens)
+    frac = float((~M.within_tolerance(y, F.bf16_to_f64(ref["y_bits"]))).mean())
+    print(f"W4A4: {mismatched} of {blocks} h blocks flipped by BF16 rounding; "
+          f"{frac:.2e} of outputs outside 2 ulp of the oracle's W4A4 result")
+    assert frac <= W4A4_OUTLIER_CAP, frac
+    return frac
 
 
 @pytest.mark.parametrize("cfg", W4A4, ids=[c.name for c in W4A4])
@@ -172,19 +246,19 @@ def test_prefill_w4a4_matches_oracle(cfg, T):
     dl = to_device(hl)
     x = synth.make_tokens(cfg, T, seed=9, batch=T)
     y, routing = G.decode(dl, x, prefill=True, act_quant=1)
+    _check_w4a4(hl, x, y, routing)
     ref = M.layer_forward(hl, x, act_quant=True)
-    _check_w4a4(y, ref["y_bits"])
     assert_prefill_routing(routing, ref, ref["near_midpoint"])
 
 
 def test_prefill_w4a4_workload_sampled():
     hl = G.host_layer("prefill_nvfp4")
     dl = G.device_layer("prefill_nvfp4")
-    T, tokens = 4096, [0, 5, 2047, 4095]
+    T = 4096
+    tokens = sorted(set([0, 1, 2047, 4095] + list(np.random.default_rng(1).choice(T, 60, replace=False))))
     x = synth.make_tokens(hl.cfg, T, seed=0, batch=T)
-    y, _ = G.decode(dl, x, prefill=True, act_quant=1)
-    ref = M.layer_forward(hl, x, act_quant=True, tokens=tokens)
-    _check_w4a4(y, ref["y_bits"], tokens)
+    y, routing = G.decode(dl, x, prefill=True, act_quant=1)
+    _check_w4a4(hl, x, y, routing, tokens)
 
 
 def test_prefill_w4a4_differs_from_exact_chain():

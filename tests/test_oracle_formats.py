@@ -137,6 +137,19 @@ def test_int4_int8_layout_hand_built():
     assert list(W8[0, :3]) == [-63.5, 63.5, -0.5]
 
 
+def test_int4_g128_layout_hand_built():
+    # unsigned nibbles with zero point 8: byte 0x80 -> k0 = 0 - 8, k1 = 8 - 8; byte 0xF7 -> k2 = -1, k3 = 7;
+    # FP16 scale 0x3C00 = 1.0 for the first 128 columns, 0xC000 = -2.0 for the next 128
+    data = np.full((1, 128), 0x88, dtype=np.uint8)
+    data[0, 0], data[0, 1] = 0x80, 0xF7
+    data[0, 64] = 0x9F                                    # k128 = 15 - 8 = 7, k129 = 9 - 8 = 1
+    sc = np.array([[0x3C00, 0xC000]], dtype=np.uint16)
+    W = F.decode(F.FMT_INT4_G128, data, sc, 1.0, 1, 256)
+    assert list(W[0, :4]) == [-8.0, 0.0, -1.0, 7.0]
+    assert list(W[0, 128:130]) == [-14.0, -2.0]
+    assert np.all(W[0, 4:128] == 0) and np.all(W[0, 130:] == 0)
+
+
 def test_fp8_b128_layout_hand_built():
     data = np.zeros((256, 128), dtype=np.uint8)
     data[0, 0] = 0x38                                     # 1.0
@@ -150,7 +163,8 @@ def test_fp8_b128_layout_hand_built():
 # ------------------------------------------- generator encoders (round trip) ----
 
 @pytest.mark.parametrize("fmt,N,K", [(F.FMT_NVFP4, 8, 64), (F.FMT_MXFP4, 8, 64), (F.FMT_INT4_G64, 8, 128),
-                                     (F.FMT_INT8_G64, 8, 128), (F.FMT_FP8_B128, 128, 256)])
+                                     (F.FMT_INT8_G64, 8, 128), (F.FMT_FP8_B128, 128, 256),
+                                     (F.FMT_INT4_G128, 8, 256)])
 def test_quantize_error_bound(fmt, N, K):
     rng = np.random.default_rng(fmt)
     W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
@@ -179,6 +193,14 @@ def test_quantize_error_bound(fmt, N, K):
         qmax = 7 if fmt == F.FMT_INT4_G64 else 127
         y = np.abs(Wd) / s
         ok = (np.abs(Wd - D) <= s / 2 * (1 + 1e-12)) | (y > qmax)
+        assert np.all(ok)
+    elif fmt == F.FMT_INT4_G128:
+        # FP16 scale = torch's float16 of amax / 7 per 128 columns; error within half a step or the clamp
+        amax = np.abs(Wd).reshape(N, K // 128, 128).max(-1)
+        ref = torch.from_numpy(amax / 7.0).to(torch.float16).numpy().view(np.uint16)
+        assert np.array_equal(scales, ref)
+        s = np.repeat(scales.view(np.float16).astype(np.float64), 128, axis=1)
+        ok = (np.abs(Wd - D) <= s / 2 * (1 + 1e-12)) | (np.abs(Wd) / s > 7)
         assert np.all(ok)
     else:
         s = np.repeat(np.repeat(scales.astype(np.float64), 128, 0), 128, 1)

@@ -22,7 +22,7 @@ import torch
 import synth
 from oracle import formats as F
 from oracle import moe as M
-from synth.configs import FMT_FP8_B128, FMT_INT4_G64, FMT_INT8_G64, FMT_MXFP4, FMT_NVFP4, LayerConfig
+from synth.configs import FMT_FP8_B128, FMT_INT4_G64, FMT_INT4_G128, FMT_INT8_G64, FMT_MXFP4, FMT_NVFP4, LayerConfig
 
 
 def _torch_e2m1(codes: np.ndarray) -> torch.Tensor:
@@ -36,7 +36,7 @@ def _torch_e2m1(codes: np.ndarray) -> torch.Tensor:
 def _torch_decode(qm, e=0) -> torch.Tensor:
     """Independent decoder (torch casts + explicit layout handling), float64 [N, K]."""
     N, K, d = qm.N, qm.K, qm.data[e]
-    if qm.fmt in (FMT_NVFP4, FMT_MXFP4, FMT_INT4_G64):
+    if qm.fmt in (FMT_NVFP4, FMT_MXFP4, FMT_INT4_G64, FMT_INT4_G128):
         lo, hi = d & 0xF, d >> 4
         codes = np.stack([lo, hi], axis=-1).reshape(N, K)
     if qm.fmt == FMT_NVFP4:
@@ -56,6 +56,10 @@ def _torch_decode(qm, e=0) -> torch.Tensor:
         q = torch.from_numpy(d.view(np.int8)).to(torch.float64)
         s = torch.from_numpy(qm.scales[e].view(np.int16)).view(torch.bfloat16).to(torch.float64)
         return q * s.repeat_interleave(64, dim=1)
+    if qm.fmt == FMT_INT4_G128:
+        q = torch.from_numpy(codes.astype(np.int16)).to(torch.float64) - 8.0
+        s = torch.from_numpy(qm.scales[e].view(np.int16)).view(torch.float16).to(torch.float64)
+        return q * s.repeat_interleave(128, dim=1)
     if qm.fmt == FMT_FP8_B128:
         q = torch.from_numpy(d).view(torch.float8_e4m3fn).to(torch.float64)
         s = torch.from_numpy(qm.scales[e]).to(torch.float64)
@@ -77,7 +81,7 @@ def _small(fmt, shared_fmt=0, E=1, k=1, H=128, I=64):
 
 
 @pytest.mark.parametrize("fmt,H,I", [(FMT_NVFP4, 128, 64), (FMT_MXFP4, 128, 64), (FMT_INT4_G64, 128, 128),
-                                     (FMT_INT8_G64, 128, 128)])
+                                     (FMT_INT8_G64, 128, 128), (FMT_INT4_G128, 256, 128)])
 def test_single_expert_equals_plain_swiglu_mlp(fmt, H, I):
     cfg = _small(fmt, H=H, I=I)
     lay = synth.make_layer(cfg, seed=3)
