@@ -383,13 +383,62 @@ def run_ours(args, world, rank, local):
     return out
 
 
-def run_prefill(args, local, peak_bf16, peak_kind):
-    """The prefill workload (NVFP4 layer, 4096 tokens, Zipf-skewed router): whole-layer time through
-    moe_prefill_forward, per-kernel event times, and the grouped GEMMs' tensor throughput."""
+PREFILL_EXTRA = {
+    # the MXFP4 and int4 g64 decode layers' routed experts at the prefill workload's token count
+    "prefill_mxfp4": lambda: synth.CONFIGS["decode_mxfp4"].with_(name="prefill_mxfp4", batches=(4096,)),
+    "prefill_int4": lambda: synth.CONFIGS["decode_int4"].with_(name="prefill_int4", shared_fmt=0, shared_I=0,
+                                                               batches=(4096,)),
+}
+
+
+def prefill_config(name: str):
+    return PREFILL_EXTRA[name]() if name in PREFILL_EXTRA else synth.CONFIGS[name]
+
+
+def _prefill_times(torch, q, lay, xs, T, y, ws, stream, act_quant, reps, G=6):
+    """Median whole-layer time (graph of G calls, `reps` replays) and per-stage event times."""
+    NB = len(xs)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            q.moe_prefill_forward(lay, xs[i % NB], T, y, ws, stream=stream, act_quant=act_quant)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(G):
+                q.moe_prefill_forward(lay, xs[i % NB], T, y, ws, stream=stream, act_quant=act_quant)
+        for _ in range(2):
+            g.replay()
+    torch.cuda.synchronize()
+    ms_list = _median_replays(torch, g, stream, reps)
+    us = statistics.median(ms_list) * 1e3 / G
+    # per-stage times: event-record nodes between the launches
+    n = 6
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    gt = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gt, stream=stream):
+        for i in range(n):
+            q.moe_prefill_forward_timed(lay, xs[i % NB], T, y, ws, evs[i], stream=stream, act_quant=act_quant)
+    with torch.cuda.stream(stream):
+        gt.replay()
+    torch.cuda.synchronize()
+    dur = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(7)] for i in range(n)]).mean(axis=0) * 1e3
+    st = q.moe_check(ws)
+    if st != 0:
+        raise RuntimeError(f"device-side error: {q.status_string(st)}")
+    return us, dur
+
+
+def run_prefill(args, local, peak_bf16, peak_kind, name="prefill_nvfp4", tokens=0, w4a4=True):
+    """One prefill workload: whole-layer time through moe_prefill_forward, per-stage event times and the
+    grouped GEMMs' tensor throughput, for the exact chain and (NVFP4 layers) the W4A4 lever."""
     import torch
     import quantized_moe_decode_router_gb300 as q
-    cfg = synth.CONFIGS["prefill_nvfp4"]
-    T = cfg.batches[0]
+    cfg = prefill_config(name)
+    T = tokens or cfg.batches[0]
     host = synth.make_layer(cfg, seed=0)
     lay = q.to_device(host, f"cuda:{local}")
     NB = 3
@@ -404,104 +453,50 @@ def run_prefill(args, local, peak_bf16, peak_kind):
         touched.append(int(np.count_nonzero(cnt.cpu().numpy())))
     stream = torch.cuda.Stream()
     G = 6
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            q.moe_prefill_forward(lay, xs[i % NB], T, y, ws, stream=stream)
-        stream.synchronize()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(G):
-                q.moe_prefill_forward(lay, xs[i % NB], T, y, ws, stream=stream)
-        for _ in range(2):
-            g.replay()
-    torch.cuda.synchronize()
     reps = max(20, args.prefill_steps // G)
-    ms_list = _median_replays(torch, g, stream, reps)
-    us = statistics.median(ms_list) * 1e3 / G
-    # per-kernel times: event-record nodes between the launches
-    n = 6
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n)]
-    for row in evs:
-        for e in row:
-            e.record(stream)
-    torch.cuda.synchronize()
-    gt = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gt, stream=stream):
-        for i in range(n):
-            q.moe_prefill_forward_timed(lay, xs[i % NB], T, y, ws, evs[i], stream=stream)
-    with torch.cuda.stream(stream):
-        gt.replay()
-    torch.cuda.synchronize()
-    dur = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(7)] for i in range(n)]).mean(axis=0) * 1e3
+    us, dur = _prefill_times(torch, q, lay, xs, T, y, ws, stream, 0, reps, G)
     names = ["router_logits", "router_topk", "dispatch", "gateup_gemm", "h_convert", "down_gemm", "combine"]
-    st = q.moe_check(ws)
-    if st != 0:
-        raise RuntimeError(f"device-side error: {q.status_string(st)}")
-    # the W4A4 lever (act_quant = 1): block-scaled FP4 GEMMs, same workload
-    ws4 = torch.empty(q.workspace_size(lay, T, 1), dtype=torch.uint8, device="cuda")
-    q.workspace_init(ws4)
-    g4 = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            q.moe_prefill_forward(lay, xs[i % NB], T, y, ws4, stream=stream, act_quant=1)
-        stream.synchronize()
-        with torch.cuda.graph(g4, stream=stream):
-            for i in range(G):
-                q.moe_prefill_forward(lay, xs[i % NB], T, y, ws4, stream=stream, act_quant=1)
-        for _ in range(2):
-            g4.replay()
-    torch.cuda.synchronize()
-    ms4_list = _median_replays(torch, g4, stream, reps)
-    us4 = statistics.median(ms4_list) * 1e3 / G
-    evs4 = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n)]
-    for row in evs4:
-        for e in row:
-            e.record(stream)
-    torch.cuda.synchronize()
-    gt4 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gt4, stream=stream):
-        for i in range(n):
-            q.moe_prefill_forward_timed(lay, xs[i % NB], T, y, ws4, evs4[i], stream=stream, act_quant=1)
-    with torch.cuda.stream(stream):
-        gt4.replay()
-    torch.cuda.synchronize()
-    dur4 = np.array([[evs4[i][j].elapsed_time(evs4[i][j + 1]) for j in range(7)] for i in range(n)]).mean(axis=0) * 1e3
-    st = q.moe_check(ws4)
-    if st != 0:
-        raise RuntimeError(f"device-side error (W4A4): {q.status_string(st)}")
     pairs = T * cfg.k
     flops = pairs * 6.0 * cfg.H * cfg.I
-    gemm4_us = dur4[3] + dur4[5]
-    tflops4 = flops / (gemm4_us * 1e-6) / 1e12
     gemm_us = dur[3] + dur[5]
     tflops = flops / (gemm_us * 1e-6) / 1e12
     fp4_peak = peak_bf16 * 13.5 / 2.25   # derived: the measured dense bf16 peak x the nominal FP4/bf16 ratio
     fp4_kind = f"derived: {peak_kind} bf16 burst {peak_bf16} TFLOP/s x 13.5/2.25 (nominal dense FP4/bf16)"
     wbytes = host.router_bytes() + np.mean(touched) * host.expert_bytes()
-    return {
-        "workload": f"prefill_nvfp4: NVFP4 MoE layer H={cfg.H} E={cfg.E} top-{cfg.k} I={cfg.I}, {T} tokens, "
-                    f"Zipf router bias s={cfg.zipf_s}",
+    zipf = f", Zipf router bias s={cfg.zipf_s}" if cfg.zipf_s else ""
+    out = {
+        "workload": f"{name}: {FMT_TEXT[cfg.fmt]} MoE layer H={cfg.H} E={cfg.E} top-{cfg.k} I={cfg.I}, "
+                    f"{T} tokens{zipf}",
         "us_per_layer": round(us, 1), "tokens_per_s": round(T / (us * 1e-6), 1),
         "kernel_us": {k: round(float(v), 2) for k, v in zip(names, dur)},
         "experts_touched": float(np.mean(touched)),
-        "gemm": {"path": "exact chain: tcgen05 kind::f16, NVFP4 decoded in shared memory",
+        "gemm": {"path": f"exact chain: tcgen05 kind::f16, {FMT_TEXT[cfg.fmt]} decoded in shared memory",
                  "flops_per_layer": flops, "achieved_tflops": round(tflops, 1),
                  "frac_f16_peak": round(tflops / peak_bf16, 4), "f16_peak_tflops": peak_bf16,
                  "frac_fp4_peak": round(tflops / fp4_peak, 4), "fp4_peak_tflops": round(fp4_peak, 1),
                  "peak_kind": peak_kind, "fp4_peak_kind": fp4_kind},
         "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
         "graph": f"CUDA graph of {G} layer calls; median of {reps} replays",
-        "w4a4": {"path": "NVFP4 activations (lever, act_quant=1): tcgen05 kind::mxf4nvf4 block-scaled GEMMs",
-                 "us_per_layer": round(us4, 1), "tokens_per_s": round(T / (us4 * 1e-6), 1),
-                 "kernel_us": {k: round(float(v), 2) for k, v in zip(
-                     ["router_logits", "router_topk", "dispatch_quantise", "gateup_gemm", "-", "down_gemm",
-                      "combine"], dur4) if k != "-"},
-                 "achieved_tflops": round(tflops4, 1), "frac_fp4_peak": round(tflops4 / fp4_peak, 4),
-                 "fp4_peak_tflops": round(fp4_peak, 1), "peak_kind": fp4_kind},
     }
+    if w4a4 and cfg.fmt == synth.configs.FMT_NVFP4:
+        # the W4A4 lever (act_quant = 1): block-scaled FP4 GEMMs, same workload
+        ws4 = torch.empty(q.workspace_size(lay, T, 1), dtype=torch.uint8, device="cuda")
+        q.workspace_init(ws4)
+        us4, dur4 = _prefill_times(torch, q, lay, xs, T, y, ws4, stream, 1, reps, G)
+        gemm4_us = dur4[3] + dur4[5]
+        tflops4 = flops / (gemm4_us * 1e-6) / 1e12
+        out["w4a4"] = {
+            "path": "NVFP4 activations (lever, act_quant=1): tcgen05 kind::mxf4nvf4 block-scaled GEMMs",
+            "us_per_layer": round(us4, 1), "tokens_per_s": round(T / (us4 * 1e-6), 1),
+            "kernel_us": {k: round(float(v), 2) for k, v in zip(
+                ["router_logits", "router_topk", "dispatch_quantise", "gateup_gemm", "-", "down_gemm",
+                 "combine"], dur4) if k != "-"},
+            "achieved_tflops": round(tflops4, 1), "frac_fp4_peak": round(tflops4 / fp4_peak, 4),
+            "fp4_peak_tflops": round(fp4_peak, 1), "peak_kind": fp4_kind}
+    return out
 
 
-FMT_TEXT = {1: "NVFP4", 2: "MXFP4", 3: "int4 g64", 4: "int8 g64", 5: "FP8 b128"}
+FMT_TEXT = {1: "NVFP4", 2: "MXFP4", 3: "int4 g64", 4: "int8 g64", 5: "FP8 b128", 6: "int4 g128"}
 DATA_DESC = {
     "tiny_nvfp4": "N(0,0.02) weights quantised NVFP4",
     "decode_nvfp4": "N(0,0.02) weights quantised NVFP4 routed / FP8 b128 shared",
@@ -602,6 +597,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill workload's measurement")
     ap.add_argument("--prefill-steps", type=int, default=60)
+    ap.add_argument("--more-prefill", default="prefill_mxfp4,prefill_int4",
+                    help="further prefill workloads (exact chain) measured beside prefill_nvfp4")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="measure only the prefill workload (e.g. at a small --prefill-tokens for a profiler)")
+    ap.add_argument("--prefill-tokens", type=int, default=0, help="token count of the prefill workloads (0: 4096)")
     args = ap.parse_args()
     world, rank, local = _dist()
     if args.impl == "reference":
@@ -609,10 +609,23 @@ def main():
             return
         print(json.dumps(run_reference(args)))
         return
+    if args.prefill_only:
+        pk, pkk = _bf16_peak()
+        res = {"prefill": run_prefill(args, local, pk, pkk, tokens=args.prefill_tokens)}
+        for name in filter(None, args.more_prefill.split(",")):
+            res[name] = run_prefill(args, local, pk, pkk, name, tokens=args.prefill_tokens, w4a4=False)
+        if rank == 0:
+            print(json.dumps(res))
+        return
     out = run_ours(args, world, rank, local)
     if world == 1 and not args.no_prefill:
         pk, pkk = _bf16_peak()
-        out["prefill"] = run_prefill(args, local, pk, pkk)
+        out["prefill"] = run_prefill(args, local, pk, pkk, tokens=args.prefill_tokens)
+        more = {}
+        for name in filter(None, args.more_prefill.split(",")):
+            more[name] = run_prefill(args, local, pk, pkk, name, tokens=args.prefill_tokens, w4a4=False)
+        if more:
+            out["prefill_more"] = more
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = run_cpu_baseline(args)
     elif rank == 0:

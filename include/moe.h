@@ -229,14 +229,19 @@ int32_t moe_experts_forward(const moe_layer* layer, const void* x /* device bf16
  * moe_decode_forward; expert projections run as grouped GEMMs over a compact
  * tile list of the routed segments (DGPP README "Execution and performance":
  * engine.expert_tile_list, engine.expert_gemm_pair), with FP32 partials and
- * a combine pass.  Supported so far: NVFP4 routed experts without a shared
- * expert, hidden and inter multiples of 128; anything else returns
- * MOE_ERR_UNSUPPORTED before any launch.  opts->act_quant = 1 selects the
+ * a combine pass.  Supported: NVFP4, MXFP4 or int4 g64 routed experts
+ * without a shared expert, hidden and inter multiples of 128; anything else
+ * (a shared expert, int8 / FP8 / int4 g128 routed experts) returns
+ * MOE_ERR_UNSUPPORTED before any launch.  MXFP4 and int4 g64 weights are
+ * folded into f16 relative to their row's largest block scale: exact while a
+ * row's block scales span at most 2^23 (MXFP4) / 2^24 (int4); blocks further
+ * below are rounded to f16's subnormal grid or dropped (weights under 2^-21
+ * times the row's largest block scale).  opts->act_quant = 1 selects the
  * NVFP4 W4A4 lever (DGPP forum, page 5 weekly update: NVFP4 W4A4 prefill is
- * opt-in): x and h are quantised to NVFP4 16-element blocks (the rule of
- * moe_quantize_act_nvfp4) and the projections run as block-scaled FP4
- * GEMMs; it needs hidden and inter multiples of 256 and 16-byte aligned
- * scale arrays.  Routing outputs are left in the workspace; in its logits
+ * opt-in; NVFP4 routed experts only): x and h are quantised to NVFP4
+ * 16-element blocks (the rule of moe_quantize_act_nvfp4) and the
+ * projections run as block-scaled FP4 GEMMs; it needs hidden and inter
+ * multiples of 256 and 16-byte aligned scale arrays.  Routing outputs are left in the workspace; in its logits
  * array only the experts the router recomputed exactly (every selected one
  * among them) hold their FP32 logit, the others hold -inf.
  */

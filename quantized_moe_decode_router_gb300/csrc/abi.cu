@@ -416,12 +416,14 @@ int sm_count(int* sms) {
   return MOE_OK;
 }
 
-// Formats the prefill expert GEMMs implement so far.  The W4A4 lever also
-// needs whole 256-column stages and 16-byte aligned scale rows.
+// Formats the prefill expert GEMMs implement: the exact chain for NVFP4, MXFP4
+// and int4 g64 routed experts; the W4A4 lever for NVFP4 only, with whole
+// 256-column stages and 16-byte aligned scale rows.
 bool prefill_supported(const moe_layer* L, bool act_quant) {
-  if (!(L->fmt == MOE_FMT_NVFP4 && L->shared_fmt == MOE_FMT_NONE && L->hidden % 128 == 0 && L->inter % 128 == 0))
-    return false;
+  const bool fmt_ok = L->fmt == MOE_FMT_NVFP4 || L->fmt == MOE_FMT_MXFP4 || L->fmt == MOE_FMT_INT4_G64;
+  if (!(fmt_ok && L->shared_fmt == MOE_FMT_NONE && L->hidden % 128 == 0 && L->inter % 128 == 0)) return false;
   if (!act_quant) return true;
+  if (L->fmt != MOE_FMT_NVFP4) return false;
   const auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   return L->hidden % 256 == 0 && L->inter % 256 == 0 && a16(L->gate.scales) && a16(L->up.scales) &&
          a16(L->down.scales);

@@ -183,7 +183,8 @@ cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s
 cudaError_t launch_prefill_topk(const PrefillArgs& a, cudaStream_t s);
 bool prefill_logits_tc_ok(const PrefillArgs& a);
 cudaError_t launch_prefill_logits_tc(const PrefillArgs& a, cudaStream_t s);
-cudaError_t launch_prefill_gemm_nvfp4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
+// The exact-chain grouped GEMMs for the layer's routed format (NVFP4, MXFP4 or int4 g64).
+cudaError_t launch_prefill_gemm(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill_gemm_w4a4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
 size_t prefill_gemm_smem(bool down);
 

@@ -396,13 +396,13 @@ cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s
     mk(7);
     return cudaGetLastError();
   }
-  err = launch_prefill_gemm_nvfp4(false, a, sms, s);
+  err = launch_prefill_gemm(false, a, sms, s);
   if (err != cudaSuccess) return err;
   mk(4);
   pf_hconv_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   mk(5);
-  if ((err = launch_prefill_gemm_nvfp4(true, a, sms, s)) != cudaSuccess) return err;
+  if ((err = launch_prefill_gemm(true, a, sms, s)) != cudaSuccess) return err;
   mk(6);
   pf_combine_kernel<<<a.T, kThreads, 0, s>>>(a);
   mk(7);

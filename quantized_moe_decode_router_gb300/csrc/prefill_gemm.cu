@@ -1,4 +1,4 @@
-// Prefill expert GEMMs on tcgen05 (exact chain, NVFP4 weights).
+// Prefill expert GEMMs on tcgen05 (exact chain; NVFP4, MXFP4 or int4 g64 weights).
 //
 //   gate/up: for a token tile of one expert and 128 rows of I,
 //            G = Wg x^T, U = Wu x^T (two TMEM accumulators), epilogue
@@ -9,9 +9,11 @@
 //            by default).
 //
 // The MMA is kind::f16 with f16 operands.  Weights are decoded in shared
-// memory, never in HBM (DGPP README intro "no dequantized copy"): e2m1 * e4m3
-// has at most 6 significant bits and lies in f16's normal range, so the
-// decoded operand is exact; the tensor scale multiplies the FP32
+// memory, never in HBM (DGPP README intro "no dequantized copy"): each code
+// times its block scale, taken relative to a per-row factor, is folded into
+// one f16 (exact for NVFP4; for MXFP4 and int4 g64 while the row's block
+// scales span at most 2^23 / 2^24, see the fold below); the row factor (the
+// NVFP4 tensor scale, else the row's largest block scale) multiplies the FP32
 // accumulator.  Tokens enter as f16 scaled by a power of two per token (per
 // sorted position for h), exact for every element above 2^-31 of the row's
 // largest magnitude; the epilogue undoes the scale.  Products are exact in
@@ -73,8 +75,8 @@ struct Cfg {
 };
 
 // Warp roles.
-constexpr int kWarpLoader = kDec / 32;       // 16
-constexpr int kWarpMma = kWarpLoader + 1;    // 17
+constexpr int kWarpLoader = kDec / 32;       // 8
+constexpr int kWarpMma = kWarpLoader + 1;    // 9
 constexpr int kWarpEpi0 = kWarpMma + 1;      // 10..17: epilogue, warp w reads TMEM lanes 32 * (w % 4)
 constexpr int kEpiWarps = 8;                 // two per TMEM lane quarter, each half of the columns
 constexpr int kEpiThreads = kEpiWarps * 32;
@@ -83,7 +85,109 @@ static_assert(kWarpEpi0 * 32 + kEpiThreads == kPfGemmThreads, "warp roles");
 // SiLU in FP32 (z / (1 + e^-z)); the quotient to within 2 ulp.
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + expf(-z)); }
 
-template <bool DOWN>
+// ---- 4-bit formats: the weights of a row folded exactly into f16 ----------
+// NVFP4: e2m1 * e4m3 (at most 6 significant bits, f16-normal), the row factor
+// is the tensor scale.  MXFP4: e2m1 * 2^(c - cref), cref the row's largest
+// scale code; the row factor 2^(cref - 127) goes to the epilogue.  int4 g64:
+// q * M * 2^(e - eref) with the BF16 scale written M * 2^e (M an 8-bit
+// integer, |q * M| <= 2040 fits f16's 11-bit significand), eref the row's
+// largest exponent; row factor 2^eref.  The fold is exact while a block's
+// scale lies within 2^-23 (MXFP4) / 2^-24 (int4) of the row's largest scale.
+// A block exactly 2^-24 below (MXFP4) has its products rounded to f16's
+// subnormal grid, and blocks further below are dropped: every weight so
+// changed is below 2^-21 times the row's largest block scale (MXFP4: 6 *
+// 2^-24; int4: 2040 * 2^-25 against a scale of at least 128 * 2^eref), an
+// error far inside the output tolerance.
+
+// Byte offset, within a row's scales, of the scales of K step s (BK = 64 columns).
+template <int F>
+__device__ __forceinline__ int step_scale_off(int s) {
+  if constexpr (F == MOE_FMT_NVFP4) return s * (BK / 16);
+  else return s * 2;  // MXFP4: two E8M0 codes; int4 g64: one BF16 scale
+}
+
+template <int F>
+__device__ __forceinline__ size_t row_scale_bytes(int K) {
+  if constexpr (F == MOE_FMT_NVFP4) return (size_t)K / 16;
+  else if constexpr (F == MOE_FMT_MXFP4) return (size_t)K / 32;
+  else return (size_t)K / 64 * 2;
+}
+
+// Reference exponent of a row (MXFP4: largest code; int4: largest scale exponent, -100000 if all zero).
+template <int F>
+__device__ __forceinline__ int row_ref(const uint8_t* srow, int K) {
+  if constexpr (F == MOE_FMT_NVFP4) {
+    return 0;
+  } else {
+    // a row's scales: K / 32 bytes (MXFP4) or K / 32 bytes of BF16 (int4 g64), a multiple of 4 bytes
+    // at a 4-byte aligned address for K a multiple of 128
+    const int nw = (int)(row_scale_bytes<F>(K) / 4);
+    int ref = F == MOE_FMT_MXFP4 ? 0 : -100000;
+#pragma unroll 4
+    for (int i = 0; i < nw; ++i) {
+      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(srow) + i);
+      if constexpr (F == MOE_FMT_MXFP4) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) ref = max(ref, (int)((w >> (8 * b)) & 0xFF));
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t sb = (w >> (16 * h)) & 0xFFFF;
+          const uint32_t E8 = (sb >> 7) & 0xFF;
+          if ((sb & 0x7FFF) != 0) ref = max(ref, (E8 ? (int)E8 : 1) - 134);
+        }
+      }
+    }
+    return ref;
+  }
+}
+
+// The row's factor applied to its FP32 accumulator.
+template <int F>
+__device__ __forceinline__ float row_factor(int ref, float ts) {
+  if constexpr (F == MOE_FMT_NVFP4) return ts;
+  else if constexpr (F == MOE_FMT_MXFP4) return e8m0_to_float((uint32_t)ref);
+  else return ref < -1000 ? 0.f : ldexpf(1.0f, ref);
+}
+
+// f16 of 2^d for d <= 0 (normal from -14, subnormal down to -24, 0 below).
+__device__ __forceinline__ uint32_t f16_pow2_bits(int d) {
+  return d >= -14 ? (uint32_t)(d + 15) << 10 : d >= -24 ? 1u << (d + 24) : 0u;
+}
+
+// Eight codes of one 32-bit word (k ascending) folded into four f16x2; sbits: the
+// scale bits covering them (NVFP4: one E4M3 byte, MXFP4: one E8M0 byte, int4: one BF16).
+template <int F>
+__device__ __forceinline__ uint4 fold_word(uint32_t w, uint32_t sbits, int ref) {
+  uint32_t v[4];
+  uint32_t fac;
+  if constexpr (F == MOE_FMT_INT4_G64) {
+    uint32_t p[4];
+    int4x8_to_f16x2_paired(w, p);                                    // (k0,k4) (k1,k5) (k2,k6) (k3,k7)
+    v[0] = prmt(p[0], p[1], 0x5410u);                                 // (k0,k1)
+    v[1] = prmt(p[2], p[3], 0x5410u);                                 // (k2,k3)
+    v[2] = prmt(p[0], p[1], 0x7632u);                                 // (k4,k5)
+    v[3] = prmt(p[2], p[3], 0x7632u);                                 // (k6,k7)
+    const uint32_t E8 = (sbits >> 7) & 0xFF;
+    const int M = (int)((sbits & 0x7F) | (E8 ? 0x80u : 0u));
+    const int d = (E8 ? (int)E8 : 1) - 134 - ref;
+    const float f = d >= -24 ? (float)M * ldexpf(1.0f, d) : 0.f;     // exact in f16: <= 8 bits, >= 2^-24
+    const __half hf = __float2half_rn((sbits & 0x8000) ? -f : f);
+    const uint32_t hb = (uint32_t)__half_as_ushort(hf);
+    fac = hb | (hb << 16);
+  } else {
+    e2m1x8_to_f16x2(w, v);
+    if constexpr (F == MOE_FMT_NVFP4) {
+      fac = e4m3_bcast_f16x2(sbits);
+    } else {
+      const uint32_t hb = f16_pow2_bits((int)(sbits & 0xFF) - ref);
+      fac = hb | (hb << 16);
+    }
+  }
+  return make_uint4(hmul2_u32(v[0], fac), hmul2_u32(v[1], fac), hmul2_u32(v[2], fac), hmul2_u32(v[3], fac));
+}
+
+template <int F, bool DOWN>
 __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs a,
                                                                     const __grid_constant__ CUtensorMap tmB) {
   using C = Cfg<DOWN>;
@@ -138,20 +242,23 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
       const int2 tile = a.tiles[it / RT];
       const int rt = it % RT, e = tile.x;
       const int row = rt * BM + rr;
-      const uint8_t* crow = W.data + (size_t)e * data_bytes(MOE_FMT_NVFP4, N, K) + (size_t)row * (K / 2);
-      const uint8_t* srow = W.scales + (size_t)e * scale_bytes(MOE_FMT_NVFP4, N, K) + (size_t)row * (K / 16);
+      const uint8_t* crow = W.data + (size_t)e * data_bytes(F, N, K) + (size_t)row * (K / 2);
+      const uint8_t* srow = W.scales + (size_t)e * scale_bytes(F, N, K) + (size_t)row * row_scale_bytes<F>(K);
       auto issue = [&](int s) {
         uint8_t* dst = raw + (s % C::RAW) * (kDec * C::RAW_BYTES);
         const int k0 = s * BK + hh * C::KT;
         cp_async16(dst, crow + k0 / 2);
         if (C::CODE_BYTES == 32) cp_async16(dst + 16, crow + k0 / 2 + 16);
-        cp_async4(dst + C::CODE_BYTES, srow + (s * BK) / 16);
+        // the aligned word holding the step's scales (their byte offset in it is taken at the read)
+        cp_async4(dst + C::CODE_BYTES,
+                  reinterpret_cast<const void*>(reinterpret_cast<uintptr_t>(srow + step_scale_off<F>(s)) & ~(uintptr_t)3));
       };
 #pragma unroll 1
       for (int j = 0; j < C::RAW - 1; ++j) {
         if (j < nsteps) issue(j);
         cp_async_commit();
       }
+      const int ref = row_ref<F>(srow, K);  // while the first steps are in flight
 #pragma unroll 1
       for (int s = 0; s < nsteps; ++s, ++g) {
         if (s + C::RAW - 1 < nsteps) issue(s + C::RAW - 1);
@@ -165,15 +272,17 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
           const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * c4);
           cw[4 * c4] = v.x; cw[4 * c4 + 1] = v.y; cw[4 * c4 + 2] = v.z; cw[4 * c4 + 3] = v.w;
         }
-        const uint32_t sw = *reinterpret_cast<const uint32_t*>(src + C::CODE_BYTES);
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(src + C::CODE_BYTES) >>
+                            (8 * ((uint32_t)reinterpret_cast<uintptr_t>(srow + step_scale_off<F>(s)) & 3u));
         uint4 out[C::KT / 8];
 #pragma unroll
         for (int c = 0; c < C::KT / 8; ++c) {
-          const uint32_t w = cw[c];
-          const uint32_t sc = e4m3_bcast_f16x2(sw >> (8 * (hh * (C::KT / 16) + c / 2)));
-          uint32_t v[4];
-          e2m1x8_to_f16x2(w, v);
-          out[c] = make_uint4(hmul2_u32(v[0], sc), hmul2_u32(v[1], sc), hmul2_u32(v[2], sc), hmul2_u32(v[3], sc));
+          const int col = hh * C::KT + c * 8;  // first column of word c within the step
+          uint32_t sbits;
+          if constexpr (F == MOE_FMT_NVFP4) sbits = (sw >> (8 * (col / 16))) & 0xFF;
+          else if constexpr (F == MOE_FMT_MXFP4) sbits = (sw >> (8 * (col / 32))) & 0xFF;
+          else sbits = sw & 0xFFFF;
+          out[c] = fold_word<F>(cw[c], sbits, ref);
         }
         const int stage = g % C::SA;
         if (!tc::bar_wait(&empty_a[stage], ((g / C::SA) & 1) ^ 1, a.wait_ns)) {
@@ -287,10 +396,19 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int pos_l = pos0 + min(chalf * 64 + i * 32 + lane, n_valid - 1);
-        if (DOWN) un_c[i] = exp2i(-a.hsig[pos_l]) * __ldg(a.down.ts + e);
+        if (DOWN) un_c[i] = exp2i(-a.hsig[pos_l]);
         else un_c[i] = exp2i(-a.xsig[a.rb.pair[pos_l] / k]);
       }
-      const float tsg = DOWN ? 0.f : __ldg(a.gate.ts + e), tsu = DOWN ? 0.f : __ldg(a.up.ts + e);
+      // the factor of this thread's row (TMEM lane) in each matrix: tensor scale or 2^reference
+      const int erow = rt * BM + q * 32 + lane;
+      float rf[2];
+#pragma unroll
+      for (int mm = 0; mm < C::NMAT; ++mm) {
+        const QW& Wm = DOWN ? a.down : (mm == 0 ? a.gate : a.up);
+        const uint8_t* sr = Wm.scales + (size_t)e * scale_bytes(F, N, K) + (size_t)erow * row_scale_bytes<F>(K);
+        rf[mm] = row_factor<F>(row_ref<F>(sr, K), F == MOE_FMT_NVFP4 ? __ldg(Wm.ts + e) : 1.f);
+      }
+      const float tsg = DOWN ? 0.f : rf[0], tsu = DOWN ? 0.f : rf[C::NMAT - 1];
       const bool ready = tc::bar_wait(&acc_full[buf], (item >> 1) & 1, a.wait_ns);
       if (!ready) report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x310 | (DOWN ? 1 : 0));
       // all epilogue warps go on, or all stop; the barrier also frees the staging tile
@@ -329,7 +447,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
           for (int j = 0; j < 32; ++j) {
             const float un = __shfl_sync(0xFFFFFFFFu, un_c[i], j);
             if (j < ncol) {
-              const float v = __uint_as_float(dv[j]) * un;
+              const float v = __uint_as_float(dv[j]) * (rf[0] * un);
               if (a.p_bf16) sb16[j * BM] = float_to_bf16_bits(v);
               else st32[j * BM] = v;
             }
@@ -401,21 +519,31 @@ bool f16_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uin
 
 size_t prefill_gemm_smem(bool down) { return down ? Cfg<true>::SMEM : Cfg<false>::SMEM; }
 
-cudaError_t launch_prefill_gemm_nvfp4(bool down, const PrefillArgs& a, int grid, cudaStream_t s) {
+template <int F>
+cudaError_t launch_pf_gemm(bool down, const PrefillArgs& a, int grid, cudaStream_t s) {
   cudaError_t err;
   alignas(64) CUtensorMap tm;
   if (down) {
     if (!f16_map(&tm, a.h16, (uint64_t)a.I, (uint64_t)a.T * a.k, NT)) return cudaErrorInvalidValue;
-    err = cudaFuncSetAttribute(pf_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true>::SMEM);
+    err = cudaFuncSetAttribute(pf_gemm_kernel<F, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true>::SMEM);
     if (err != cudaSuccess) return err;
-    pf_gemm_kernel<true><<<grid, kPfGemmThreads, Cfg<true>::SMEM, s>>>(a, tm);
+    pf_gemm_kernel<F, true><<<grid, kPfGemmThreads, Cfg<true>::SMEM, s>>>(a, tm);
   } else {
     if (!f16_map(&tm, a.xg, (uint64_t)a.H, (uint64_t)a.T * a.k, NT)) return cudaErrorInvalidValue;
-    err = cudaFuncSetAttribute(pf_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<false>::SMEM);
+    err = cudaFuncSetAttribute(pf_gemm_kernel<F, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<false>::SMEM);
     if (err != cudaSuccess) return err;
-    pf_gemm_kernel<false><<<grid, kPfGemmThreads, Cfg<false>::SMEM, s>>>(a, tm);
+    pf_gemm_kernel<F, false><<<grid, kPfGemmThreads, Cfg<false>::SMEM, s>>>(a, tm);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_gemm(bool down, const PrefillArgs& a, int grid, cudaStream_t s) {
+  switch (a.fmt) {
+    case MOE_FMT_NVFP4: return launch_pf_gemm<MOE_FMT_NVFP4>(down, a, grid, s);
+    case MOE_FMT_MXFP4: return launch_pf_gemm<MOE_FMT_MXFP4>(down, a, grid, s);
+    case MOE_FMT_INT4_G64: return launch_pf_gemm<MOE_FMT_INT4_G64>(down, a, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace qmoe

@@ -17,7 +17,7 @@ from oracle import formats as F
 from oracle import moe as M
 from quantized_moe_decode_router_gb300 import _binding as B
 from quantized_moe_decode_router_gb300.device import to_device
-from synth.configs import FMT_MXFP4, FMT_NVFP4, LayerConfig
+from synth.configs import FMT_INT4_G64, FMT_INT8_G64, FMT_MXFP4, FMT_NVFP4, LayerConfig
 from tests import gpu_util as G
 
 pytestmark = pytest.mark.gpu
@@ -92,6 +92,8 @@ SMALL = [
     LayerConfig("p_tiny", FMT_NVFP4, H=256, E=6, k=2, I=256),
     LayerConfig("p_rows3", FMT_NVFP4, H=384, E=5, k=3, I=384),
     LayerConfig("p_skew", FMT_NVFP4, H=512, E=24, k=4, I=128, zipf_s=1.1),
+    LayerConfig("p_mxfp4", FMT_MXFP4, H=640, E=7, k=2, I=256),
+    LayerConfig("p_int4", FMT_INT4_G64, H=384, E=9, k=3, I=384, zipf_s=1.1),
 ]
 
 
@@ -131,13 +133,71 @@ def test_prefill_deterministic_and_batch_invariant():
     assert np.array_equal(y_part, y1[100:160])
 
 
-def test_prefill_unsupported_format_is_reported():
-    cfg = LayerConfig("p_mx", FMT_MXFP4, H=256, E=4, k=2, I=128)
-    dl = to_device(synth.make_layer(cfg, seed=1))
+@pytest.mark.parametrize("name,T,tokens", [("decode_mxfp4", 512, [0, 255, 511]),
+                                           ("decode_int4", 384, [0, 200, 383])])
+def test_prefill_mxfp4_int4_workloads_sampled(name, T, tokens):
+    """The exact-chain GEMMs on the MXFP4 and int4 g64 layer shapes at full
+    size (the int4 layer without its int8 shared expert), sampled tokens."""
+    cfg = G.host_layer(name).cfg.with_(shared_fmt=0, shared_I=0, name=name + "_routed")
+    hl = synth.make_layer(cfg, seed=0)
+    dl = to_device(hl)
+    x = synth.make_tokens(cfg, T, seed=0, batch=T)
+    y, routing = G.decode(dl, x, prefill=True)
+    ref = M.layer_forward(hl, x, tokens=tokens)
+    _check_y(y, ref["y_bits"], tokens)
+    assert_prefill_routing(routing, ref, ref["near_midpoint"])
+
+
+def _spread_rows(qm, fmt, drops):
+    """Lower one scale block of every third row by each of `drops` powers of two
+    (MXFP4: E8M0 code; int4 g64: the BF16 scale's exponent)."""
+    qm = synth.QMat(qm.fmt, qm.N, qm.K, qm.data.copy(), qm.scales.copy(), qm.ts.copy())
+    rows = np.arange(0, qm.N, 3)
+    nblk = qm.scales.shape[2]
+    for j, drop in enumerate(drops):
+        blk = np.arange(j, nblk, 2 * len(drops))
+        sub = qm.scales[:, rows[:, None], blk[None, :]].astype(np.int32)
+        if fmt == FMT_MXFP4:
+            new = np.maximum(sub - drop, 1)
+        else:
+            ex = (sub >> 7) & 0xFF
+            new = (sub & 0x807F) | (np.maximum(ex - drop, 1) << 7)
+        qm.scales[:, rows[:, None], blk[None, :]] = new.astype(qm.scales.dtype)
+    return qm
+
+
+@pytest.mark.parametrize("fmt", [FMT_MXFP4, FMT_INT4_G64])
+def test_prefill_wide_scale_spreads(fmt):
+    """Blocks 2^-22, 2^-24 and 2^-30 below their row's largest scale: the first
+    fold exactly, the second exactly (int4) or rounded to f16's subnormal grid
+    (MXFP4), the third drop out; all stay inside the output tolerance."""
+    cfg = LayerConfig(f"p_spread_{fmt}", fmt, H=512, E=6, k=2, I=256)
+    hl = synth.make_layer(cfg, seed=4)
+    for attr in ("gate", "up", "down"):
+        setattr(hl, attr, _spread_rows(getattr(hl, attr), fmt, (22, 24, 30)))
+    dl = to_device(hl)
+    x = synth.make_tokens(cfg, 200, seed=4, batch=200)
+    y, routing = G.decode(dl, x, prefill=True)
+    ref = M.layer_forward(hl, x)
+    _check_y(y, ref["y_bits"])
+
+
+@pytest.mark.parametrize("case", ["int8_shared", "fp8_shared", "w4a4_mxfp4"])
+def test_prefill_unsupported_is_reported(case):
+    """Shared experts and the W4A4 lever on a format other than NVFP4 are not
+    implemented in prefill: the call reports MOE_ERR_UNSUPPORTED."""
+    if case == "int8_shared":
+        cfg = LayerConfig("p_u1", FMT_INT4_G64, H=256, E=4, k=2, I=128, shared_fmt=FMT_INT8_G64, shared_I=128)
+    elif case == "fp8_shared":
+        cfg = G.host_layer("decode_nvfp4").cfg
+    else:
+        cfg = LayerConfig("p_u3", FMT_MXFP4, H=256, E=4, k=2, I=128)
+    dl = to_device(synth.make_layer(cfg, seed=1)) if case != "fp8_shared" else G.device_layer("decode_nvfp4")
     x = G.x_device(synth.make_tokens(cfg, 20, seed=1))
     y = torch.zeros((20, cfg.H), dtype=torch.int16, device="cuda")
     ws = G.new_ws(dl, 20)
-    st = B.moe_prefill_forward(dl, x, 20, y, ws, raise_on_error=False)
+    st = B.moe_prefill_forward(dl, x, 20, y, ws, raise_on_error=False,
+                               act_quant=case == "w4a4_mxfp4")
     assert st == B.MOE_ERR_UNSUPPORTED
 
 
