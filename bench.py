@@ -384,10 +384,9 @@ def run_ours(args, world, rank, local):
 
 
 PREFILL_EXTRA = {
-    # the MXFP4 and int4 g64 decode layers' routed experts at the prefill workload's token count
+    # the MXFP4 and int4 g64 (+ int8 g64 shared) decode layers at the prefill workload's token count
     "prefill_mxfp4": lambda: synth.CONFIGS["decode_mxfp4"].with_(name="prefill_mxfp4", batches=(4096,)),
-    "prefill_int4": lambda: synth.CONFIGS["decode_int4"].with_(name="prefill_int4", shared_fmt=0, shared_I=0,
-                                                               batches=(4096,)),
+    "prefill_int4": lambda: synth.CONFIGS["decode_int4"].with_(name="prefill_int4", batches=(4096,)),
 }
 
 
@@ -464,8 +463,13 @@ def run_prefill(args, local, peak_bf16, peak_kind, name="prefill_nvfp4", tokens=
     fp4_kind = f"derived: {peak_kind} bf16 burst {peak_bf16} TFLOP/s x 13.5/2.25 (nominal dense FP4/bf16)"
     wbytes = host.router_bytes() + np.mean(touched) * host.expert_bytes()
     zipf = f", Zipf router bias s={cfg.zipf_s}" if cfg.zipf_s else ""
+    shared = f" + {FMT_TEXT[cfg.shared_fmt]} shared expert I={cfg.shared_I}" if cfg.shared_fmt else ""
+    if cfg.shared_fmt:
+        flops += T * 6.0 * cfg.H * cfg.shared_I
+        tflops = flops / (gemm_us * 1e-6) / 1e12
+        wbytes += host.shared_bytes()
     out = {
-        "workload": f"{name}: {FMT_TEXT[cfg.fmt]} MoE layer H={cfg.H} E={cfg.E} top-{cfg.k} I={cfg.I}, "
+        "workload": f"{name}: {FMT_TEXT[cfg.fmt]} MoE layer H={cfg.H} E={cfg.E} top-{cfg.k} I={cfg.I}{shared}, "
                     f"{T} tokens{zipf}",
         "us_per_layer": round(us, 1), "tokens_per_s": round(T / (us * 1e-6), 1),
         "kernel_us": {k: round(float(v), 2) for k, v in zip(names, dur)},
@@ -478,7 +482,7 @@ def run_prefill(args, local, peak_bf16, peak_kind, name="prefill_nvfp4", tokens=
         "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
         "graph": f"CUDA graph of {G} layer calls; median of {reps} replays",
     }
-    if w4a4 and cfg.fmt == synth.configs.FMT_NVFP4:
+    if w4a4 and cfg.fmt == synth.configs.FMT_NVFP4 and not cfg.shared_fmt:
         # the W4A4 lever (act_quant = 1): block-scaled FP4 GEMMs, same workload
         ws4 = torch.empty(q.workspace_size(lay, T, 1), dtype=torch.uint8, device="cuda")
         q.workspace_init(ws4)

@@ -32,6 +32,7 @@ struct Layout {
       dn_part, dn_cnt;
   // prefill path
   size_t xg, xsig, xnorm, wnorm, hist, pos_of, tiles, h16, hsig, xq, xsf, xqg, xsfg, hq, hsf, rw_hi, rw_lo;
+  size_t xs16, hs16, hssig;  // the shared expert's operands in prefill
   int max_tiles;
   size_t total;
 };
@@ -87,6 +88,9 @@ Layout make_layout(const moe_layer* L, int maxT) {
   o.hsf = take(T * k * I / 16);
   o.rw_hi = take(E * H * 2);
   o.rw_lo = take(E * H * 2);
+  o.xs16 = take(Is ? T * H * 2 : 0);
+  o.hs16 = take(T * Is * 2);
+  o.hssig = take(Is ? T * 4 : 0);
   o.total = at;
   return o;
 }
@@ -406,6 +410,20 @@ PrefillArgs prefill_args(const moe_layer* L, const Layout& lo, void* ws, const v
   a.bias_select = L->bias_select;
   a.unbiased = reinterpret_cast<float*>(b + lo.approx);
   a.wait_ns = 2000000000ull;
+  if (L->shared_fmt) {
+    a.sfmt = L->shared_fmt;
+    a.Is = L->shared_inter;
+    a.s_gate = qw(L->shared_gate, L->shared_fmt);
+    a.s_up = qw(L->shared_up, L->shared_fmt);
+    a.s_down = qw(L->shared_down, L->shared_fmt);
+    a.xs16 = reinterpret_cast<uint16_t*>(b + lo.xs16);
+    a.hs = reinterpret_cast<uint16_t*>(b + lo.hs);
+    a.hs16 = reinterpret_cast<uint16_t*>(b + lo.hs16);
+    a.hssig = reinterpret_cast<int32_t*>(b + lo.hssig);
+    a.S = reinterpret_cast<float*>(b + lo.S);
+    a.sgate_w = L->shared_expert_gate;
+    a.sgate = reinterpret_cast<float*>(b + lo.sgate);
+  }
   return a;
 }
 
@@ -416,14 +434,15 @@ int sm_count(int* sms) {
   return MOE_OK;
 }
 
-// Formats the prefill expert GEMMs implement: the exact chain for NVFP4, MXFP4
-// and int4 g64 routed experts; the W4A4 lever for NVFP4 only, with whole
+// Layers the prefill expert GEMMs implement: the exact chain for every routed
+// and shared format with hidden, inter and shared inter multiples of 128; the
+// W4A4 lever for NVFP4 routed experts without a shared expert, with whole
 // 256-column stages and 16-byte aligned scale rows.
 bool prefill_supported(const moe_layer* L, bool act_quant) {
-  const bool fmt_ok = L->fmt == MOE_FMT_NVFP4 || L->fmt == MOE_FMT_MXFP4 || L->fmt == MOE_FMT_INT4_G64;
-  if (!(fmt_ok && L->shared_fmt == MOE_FMT_NONE && L->hidden % 128 == 0 && L->inter % 128 == 0)) return false;
+  if (L->hidden % 128 != 0 || L->inter % 128 != 0) return false;
+  if (L->shared_fmt != MOE_FMT_NONE && L->shared_inter % 128 != 0) return false;
   if (!act_quant) return true;
-  if (L->fmt != MOE_FMT_NVFP4) return false;
+  if (L->fmt != MOE_FMT_NVFP4 || L->shared_fmt != MOE_FMT_NONE) return false;
   const auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   return L->hidden % 256 == 0 && L->inter % 256 == 0 && a16(L->gate.scales) && a16(L->up.scales) &&
          a16(L->down.scales);

@@ -163,6 +163,17 @@ struct PrefillArgs {
   uint8_t* xsfg;        // [T*k, H/16]
   uint8_t* hq;          // [T*k, I/2] codes of h in sorted order
   uint8_t* hsf;         // [T*k, I/16]
+  // the shared expert (dense over all T tokens), when the layer has one
+  int sfmt, Is;         // its format (0: none) and intermediate size
+  QW s_gate, s_up, s_down;
+  uint16_t* xs16;       // f16 [T, H]: x[t] * 2^xsig[t] in token order (B operand of the shared gate/up)
+  uint16_t* hs;         // bf16 [T, Is]
+  uint16_t* hs16;       // f16 [T, Is]: hs * 2^hssig[t]
+  int32_t* hssig;       // [T]
+  float* S;             // [T, H] shared expert output (f32, or bf16 under p_bf16)
+  const float* sgate_w; // [H] gate vector of a sigmoid-gated shared expert, or nullptr
+  float* sgate;         // [T] sigmoid(x_t . sgate_w)
+  int dense_T;          // > 0: this argument block is the shared expert's (tiles of NT consecutive tokens)
 };
 
 // Optional host callback between launches (event records of the timed entry
@@ -183,10 +194,10 @@ cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s
 cudaError_t launch_prefill_topk(const PrefillArgs& a, cudaStream_t s);
 bool prefill_logits_tc_ok(const PrefillArgs& a);
 cudaError_t launch_prefill_logits_tc(const PrefillArgs& a, cudaStream_t s);
-// The exact-chain grouped GEMMs for the layer's routed format (NVFP4, MXFP4 or int4 g64).
+// The exact-chain grouped GEMMs for a.fmt (any of the six weight formats); a.dense_T > 0 runs them
+// densely over tokens 0 .. dense_T - 1 of one weight set (the shared expert).
 cudaError_t launch_prefill_gemm(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill_gemm_w4a4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
-size_t prefill_gemm_smem(bool down);
 
 // Decode combine y = bf16(sum_j w_j P_j (+ S)), launched after the down
 // kernel as a programmatic dependent of it.

@@ -255,13 +255,14 @@ __global__ void __launch_bounds__(32) pf_place_kernel(PrefillArgs a) {
 
 // One warp per sorted position: the GEMM operand row xg[pos] = f16( x[t] * 2^s_t ),
 // t the token of the pair placed at pos (a contiguous copy per expert segment,
-// so the gate/up GEMM loads its token tiles as plain 2-D boxes).
+// so the gate/up GEMM loads its token tiles as plain 2-D boxes).  For the
+// shared expert's argument block (dense_T > 0) position = token.
 __global__ void __launch_bounds__(kThreads) pf_gather_kernel(PrefillArgs a) {
   const int lane = threadIdx.x & 31;
   const int pos = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
   if (pos >= a.T * a.k) return;
   const int H = a.H;
-  const int t = a.rb.pair[pos] / a.k;
+  const int t = a.dense_T ? pos : a.rb.pair[pos] / a.k;
   const float mul = exp2i(a.xsig[t]);
   const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
   uint4* xo = reinterpret_cast<uint4*>(a.xg + (size_t)pos * H);
@@ -323,8 +324,36 @@ __global__ void __launch_bounds__(kThreads) pf_hconv_kernel(PrefillArgs a) {
   if (lane == 0) a.hsig[pos] = sft;
 }
 
-// y[t] = bf16( sum_j w[t, j] * P[pos_of[t*k + j]] ), j ascending (P in FP32, or in
-// BF16 under the bf16-partials lever).
+// One warp per token: the sigmoid gate of a gated shared expert, from the
+// correctly rounded FP32 logit x_t . w_gate (float-float dot, one rounding).
+__global__ void __launch_bounds__(kThreads) pf_sgate_kernel(PrefillArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  if (t >= a.T) return;
+  const int H = a.H;
+  const uint2* xr = reinterpret_cast<const uint2*>(a.x + (size_t)t * H);
+  const float4* wr = reinterpret_cast<const float4*>(a.sgate_w);
+  float hi = 0.f, lo = 0.f;
+  for (int q = lane; q < H / 4; q += 32) {
+    const uint2 xv = __ldg(xr + q);
+    const float4 wv = __ldg(wr + q);
+    dot2_step(bf16_bits_to_float(xv.x & 0xFFFF), wv.x, hi, lo);
+    dot2_step(bf16_bits_to_float(xv.x >> 16), wv.y, hi, lo);
+    dot2_step(bf16_bits_to_float(xv.y & 0xFFFF), wv.z, hi, lo);
+    dot2_step(bf16_bits_to_float(xv.y >> 16), wv.w, hi, lo);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(0xFFFFFFFFu, hi, o);
+    const float l2 = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+    dot2_merge(hi, lo, h2, l2);
+  }
+  if (lane == 0) a.sgate[t] = 1.f / (1.f + expf(-__fadd_rn(hi, lo)));
+}
+
+// y[t] = bf16( sum_j w[t, j] * P[pos_of[t*k + j]] + g_t * S[t] ), j ascending, the
+// shared term last (g_t = 1 unless the shared expert is gated); P and S in FP32,
+// or in BF16 under the bf16-partials lever.
 __global__ void __launch_bounds__(kThreads) pf_combine_kernel(PrefillArgs a) {
   const int t = blockIdx.x, H = a.H, k = a.k;
   const float* wt = a.rb.topk_w + (size_t)t * k;
@@ -345,6 +374,21 @@ __global__ void __launch_bounds__(kThreads) pf_combine_kernel(PrefillArgs a) {
       acc.y = fmaf(w, p.y, acc.y);
       acc.z = fmaf(w, p.z, acc.z);
       acc.w = fmaf(w, p.w, acc.w);
+    }
+    if (a.S) {
+      const float g = a.sgate_w ? __ldg(a.sgate + t) : 1.f;
+      float4 sv;
+      if (a.p_bf16) {
+        const uint2 v = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(a.S) + (size_t)t * H) + c);
+        sv = make_float4(bf16_bits_to_float(v.x & 0xFFFF), bf16_bits_to_float(v.x >> 16), bf16_bits_to_float(v.y & 0xFFFF),
+                         bf16_bits_to_float(v.y >> 16));
+      } else {
+        sv = __ldcs(reinterpret_cast<const float4*>(a.S + (size_t)t * H) + c);
+      }
+      acc.x = fmaf(g, sv.x, acc.x);
+      acc.y = fmaf(g, sv.y, acc.y);
+      acc.z = fmaf(g, sv.z, acc.z);
+      acc.w = fmaf(g, sv.w, acc.w);
     }
     const uint32_t lo = (uint32_t)float_to_bf16_bits(acc.x) | ((uint32_t)float_to_bf16_bits(acc.y) << 16);
     const uint32_t hi = (uint32_t)float_to_bf16_bits(acc.z) | ((uint32_t)float_to_bf16_bits(acc.w) << 16);
@@ -396,13 +440,26 @@ cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s
     mk(7);
     return cudaGetLastError();
   }
+  // the shared expert: one weight set over all T tokens in token order (its own argument block)
+  PrefillArgs sa = a;
+  if (a.sfmt) {
+    sa.fmt = a.sfmt; sa.I = a.Is; sa.E = 1; sa.k = 1; sa.dense_T = a.T;
+    sa.gate = a.s_gate; sa.up = a.s_up; sa.down = a.s_down;
+    sa.xg = a.xs16; sa.h = a.hs; sa.h16 = a.hs16; sa.hsig = a.hssig; sa.P = a.S;
+    pf_gather_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(sa);
+    if (a.sgate_w) pf_sgate_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(a);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
   err = launch_prefill_gemm(false, a, sms, s);
   if (err != cudaSuccess) return err;
+  if (a.sfmt && (err = launch_prefill_gemm(false, sa, sms, s)) != cudaSuccess) return err;
   mk(4);
   pf_hconv_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
+  if (a.sfmt) pf_hconv_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(sa);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   mk(5);
   if ((err = launch_prefill_gemm(true, a, sms, s)) != cudaSuccess) return err;
+  if (a.sfmt && (err = launch_prefill_gemm(true, sa, sms, s)) != cudaSuccess) return err;
   mk(6);
   pf_combine_kernel<<<a.T, kThreads, 0, s>>>(a);
   mk(7);

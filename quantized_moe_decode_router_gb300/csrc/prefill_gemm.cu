@@ -52,26 +52,42 @@ constexpr int KB = BK * 2;
 constexpr int kDec = 256;       // decode threads (8 warps)
 constexpr uint64_t kDrainLimit = 2000000000ull;  // 2 s: waits that drain copies and MMAs already issued
 
-template <bool DOWN>
+// Formats whose block scale does not fold exactly into an f16 weight (an 8-bit
+// code or a 4-bit code times an 11-bit FP16 scale): their codes enter the MMA
+// as exact f16 integers / E4M3 values, each scale group's products accumulate
+// in a TMEM block of their own, and the epilogue adds scale x block to a
+// running FP32 sum (the group scale applied per group, in FP32).
+template <int F>
+constexpr bool promote_fmt() {
+  return F == MOE_FMT_INT8_G64 || F == MOE_FMT_FP8_B128 || F == MOE_FMT_INT4_G128;
+}
+
+template <int F, bool DOWN>
 struct Cfg {
+  static constexpr bool PROMOTE = promote_fmt<F>();
+  static constexpr int BITS = (F == MOE_FMT_INT8_G64 || F == MOE_FMT_FP8_B128) ? 8 : 4;
+  static constexpr int GS = F == MOE_FMT_INT8_G64 ? 1 : 2;  // K steps per scale group (promote formats)
   static constexpr int NMAT = DOWN ? 1 : 2;
   static constexpr int SA = 2;                  // decoded-weight (A) stages
   static constexpr int SB = 4;                  // token-row (B) stages: TMA latency spans several steps
-  static constexpr int RAW = DOWN ? 6 : 5;      // raw-code ring stages (prefetch distance RAW - 1 steps)
   static constexpr int TPR = kDec / (NMAT * BM);  // decode threads per weight row
   static constexpr int KT = BK / TPR;             // columns per decode thread per step
+  static constexpr int CODE_BYTES = KT * BITS / 8;               // per thread per step
+  static constexpr int RAW_BYTES = PROMOTE ? CODE_BYTES : CODE_BYTES + 16;  // fold: then the scale word (padded)
+  static constexpr int RAW = DOWN ? 6 : (BITS == 8 ? 4 : 5);    // raw-code ring stages (prefetch RAW - 1 steps)
   static constexpr int A_BYTES = BM * KB;
   static constexpr int B_BYTES = NT * KB;
   static constexpr int A_STAGE = NMAT * A_BYTES;
   static constexpr int B_OFF = SA * A_STAGE;
-  static constexpr int CODE_BYTES = KT / 2;                    // per thread per step
-  static constexpr int RAW_BYTES = CODE_BYTES + 16;            // codes, then the 4-byte scale word (padded)
   static constexpr int RAW_OFF = B_OFF + SB * B_BYTES;
   static constexpr int STG_OFF = RAW_OFF + RAW * kDec * RAW_BYTES;  // epilogue staging [NT cols][BM rows]
   static constexpr int OUT_BYTES = DOWN ? 4 : 2;                      // f32 partials / bf16 h
   static constexpr int SMEM = STG_OFF + NT * BM * OUT_BYTES + 1024;
   static constexpr uint32_t ACC_COLS = NMAT * NT;      // one accumulator set
-  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // double buffered
+  // fold: two accumulator sets (double buffered); promote: running sums, then the group block
+  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+  static_assert(CODE_BYTES % 16 == 0, "16-byte code copies");
 };
 
 // Warp roles.
@@ -187,10 +203,67 @@ __device__ __forceinline__ uint4 fold_word(uint32_t w, uint32_t sbits, int ref) 
   return make_uint4(hmul2_u32(v[0], fac), hmul2_u32(v[1], fac), hmul2_u32(v[2], fac), hmul2_u32(v[3], fac));
 }
 
+// Eight weights (k ascending) of a promote format as four f16x2 of the exact
+// code values (int8 / int4 g128 integers, E4M3 values); c: the group of eight
+// within the thread's code words.
+template <int F>
+__device__ __forceinline__ uint4 codes_to_f16(const uint32_t* cw, int c) {
+  uint32_t v[4];
+  if constexpr (F == MOE_FMT_INT8_G64) {
+    int8x4_to_f16x2(cw[2 * c], v[0], v[1]);
+    int8x4_to_f16x2(cw[2 * c + 1], v[2], v[3]);
+  } else if constexpr (F == MOE_FMT_FP8_B128) {
+    e4m3x4_to_f16x2(cw[2 * c], v[0], v[1]);
+    e4m3x4_to_f16x2(cw[2 * c + 1], v[2], v[3]);
+  } else {
+    uint32_t p[4];
+    int4x8_to_f16x2_paired(cw[c] ^ 0x88888888u, p);  // unsigned nibble u -> u - 8: flip the top bit
+    v[0] = prmt(p[0], p[1], 0x5410u);
+    v[1] = prmt(p[2], p[3], 0x5410u);
+    v[2] = prmt(p[0], p[1], 0x7632u);
+    v[3] = prmt(p[2], p[3], 0x7632u);
+  }
+  return make_uint4(v[0], v[1], v[2], v[3]);
+}
+
+// Scale of group g (GS K steps) for weight row `row` of expert e (FP8 b128: the
+// 128 x 128 block of row tile rt).
+template <int F>
+__device__ __forceinline__ float group_scale(const QW& W, int e, int N, int K, int row, int rt, int g) {
+  const uint8_t* sc = W.scales + (size_t)e * scale_bytes(F, N, K);
+  if constexpr (F == MOE_FMT_INT8_G64) {
+    return bf16_bits_to_float(__ldg(reinterpret_cast<const uint16_t*>(sc) + (size_t)row * (K / 64) + g));
+  } else if constexpr (F == MOE_FMT_FP8_B128) {
+    return __ldg(reinterpret_cast<const float*>(sc) + (size_t)rt * (K / 128) + g);
+  } else {
+    return __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(sc) + (size_t)row * (K / 128) + g)));
+  }
+}
+
+// The tile list: the dispatch's (expert, first sorted position) pairs, or, for
+// the shared expert (a.dense_T > 0), consecutive runs of NT tokens of one
+// weight set in token order.
+__device__ __forceinline__ int2 tile_at(const PrefillArgs& a, int i) {
+  return a.dense_T ? make_int2(0, i * NT) : a.tiles[i];
+}
+__device__ __forceinline__ int tile_valid(const PrefillArgs& a, int2 t) {
+  return min(NT, (a.dense_T ? a.dense_T : a.rb.off[t.x + 1]) - t.y);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),
+      "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 template <int F, bool DOWN>
 __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs a,
                                                                     const __grid_constant__ CUtensorMap tmB) {
-  using C = Cfg<DOWN>;
+  using C = Cfg<F, DOWN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full_a[C::SA], empty_a[C::SA], full_b[C::SB], empty_b[C::SB];
@@ -203,7 +276,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
   const int N = DOWN ? H : I;          // rows of one weight matrix
   const int RT = N / BM;               // row tiles per token tile
   const int nsteps = K / BK;
-  const int n_items = a.rb.ctrl->n_tiles * RT;
+  const int n_items = (a.dense_T ? (a.dense_T + NT - 1) / NT : a.rb.ctrl->n_tiles) * RT;
   Ctrl* ctrl = a.rb.ctrl;
 
   if (tid == 0) {
@@ -239,26 +312,30 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
     uint32_t g = 0;
     bool ok = true;
     for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      const int2 tile = a.tiles[it / RT];
+      const int2 tile = tile_at(a, it / RT);
       const int rt = it % RT, e = tile.x;
       const int row = rt * BM + rr;
-      const uint8_t* crow = W.data + (size_t)e * data_bytes(F, N, K) + (size_t)row * (K / 2);
-      const uint8_t* srow = W.scales + (size_t)e * scale_bytes(F, N, K) + (size_t)row * row_scale_bytes<F>(K);
+      const uint8_t* crow = W.data + (size_t)e * data_bytes(F, N, K) + (size_t)row * ((size_t)K * C::BITS / 8);
+      const uint8_t* srow =
+          C::PROMOTE ? nullptr : W.scales + (size_t)e * scale_bytes(F, N, K) + (size_t)row * row_scale_bytes<F>(K);
       auto issue = [&](int s) {
         uint8_t* dst = raw + (s % C::RAW) * (kDec * C::RAW_BYTES);
-        const int k0 = s * BK + hh * C::KT;
-        cp_async16(dst, crow + k0 / 2);
-        if (C::CODE_BYTES == 32) cp_async16(dst + 16, crow + k0 / 2 + 16);
-        // the aligned word holding the step's scales (their byte offset in it is taken at the read)
-        cp_async4(dst + C::CODE_BYTES,
-                  reinterpret_cast<const void*>(reinterpret_cast<uintptr_t>(srow + step_scale_off<F>(s)) & ~(uintptr_t)3));
+        const uint8_t* src = crow + (size_t)(s * BK + hh * C::KT) * C::BITS / 8;
+#pragma unroll
+        for (int j = 0; j < C::CODE_BYTES / 16; ++j) cp_async16(dst + 16 * j, src + 16 * j);
+        if constexpr (!C::PROMOTE) {
+          // the aligned word holding the step's scales (their byte offset in it is taken at the read)
+          cp_async4(dst + C::CODE_BYTES,
+                    reinterpret_cast<const void*>(reinterpret_cast<uintptr_t>(srow + step_scale_off<F>(s)) & ~(uintptr_t)3));
+        }
       };
 #pragma unroll 1
       for (int j = 0; j < C::RAW - 1; ++j) {
         if (j < nsteps) issue(j);
         cp_async_commit();
       }
-      const int ref = row_ref<F>(srow, K);  // while the first steps are in flight
+      int ref = 0;
+      if constexpr (!C::PROMOTE) ref = row_ref<F>(srow, K);  // while the first steps are in flight
 #pragma unroll 1
       for (int s = 0; s < nsteps; ++s, ++g) {
         if (s + C::RAW - 1 < nsteps) issue(s + C::RAW - 1);
@@ -266,23 +343,28 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         cp_async_wait<C::RAW - 1>();
         const uint8_t* src = raw + (s % C::RAW) * (kDec * C::RAW_BYTES);
         // 16-byte shared loads: conflict-free at this thread stride
-        uint32_t cw[C::KT / 8];
+        uint32_t cw[C::CODE_BYTES / 4];
 #pragma unroll
-        for (int c4 = 0; c4 < C::KT / 32; ++c4) {
+        for (int c4 = 0; c4 < C::CODE_BYTES / 16; ++c4) {
           const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * c4);
           cw[4 * c4] = v.x; cw[4 * c4 + 1] = v.y; cw[4 * c4 + 2] = v.z; cw[4 * c4 + 3] = v.w;
         }
-        const uint32_t sw = *reinterpret_cast<const uint32_t*>(src + C::CODE_BYTES) >>
-                            (8 * ((uint32_t)reinterpret_cast<uintptr_t>(srow + step_scale_off<F>(s)) & 3u));
         uint4 out[C::KT / 8];
+        if constexpr (C::PROMOTE) {
 #pragma unroll
-        for (int c = 0; c < C::KT / 8; ++c) {
-          const int col = hh * C::KT + c * 8;  // first column of word c within the step
-          uint32_t sbits;
-          if constexpr (F == MOE_FMT_NVFP4) sbits = (sw >> (8 * (col / 16))) & 0xFF;
-          else if constexpr (F == MOE_FMT_MXFP4) sbits = (sw >> (8 * (col / 32))) & 0xFF;
-          else sbits = sw & 0xFFFF;
-          out[c] = fold_word<F>(cw[c], sbits, ref);
+          for (int c = 0; c < C::KT / 8; ++c) out[c] = codes_to_f16<F>(cw, c);
+        } else {
+          const uint32_t sw = *reinterpret_cast<const uint32_t*>(src + C::CODE_BYTES) >>
+                              (8 * ((uint32_t)reinterpret_cast<uintptr_t>(srow + step_scale_off<F>(s)) & 3u));
+#pragma unroll
+          for (int c = 0; c < C::KT / 8; ++c) {
+            const int col = hh * C::KT + c * 8;  // first column of word c within the step
+            uint32_t sbits;
+            if constexpr (F == MOE_FMT_NVFP4) sbits = (sw >> (8 * (col / 16))) & 0xFF;
+            else if constexpr (F == MOE_FMT_MXFP4) sbits = (sw >> (8 * (col / 32))) & 0xFF;
+            else sbits = sw & 0xFFFF;
+            out[c] = fold_word<F>(cw[c], sbits, ref);
+          }
         }
         const int stage = g % C::SA;
         if (!tc::bar_wait(&empty_a[stage], ((g / C::SA) & 1) ^ 1, a.wait_ns)) {
@@ -304,9 +386,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
     uint32_t g = 0;
     bool ok = true;
     for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      const int2 tile = a.tiles[it / RT];
-      const int e = tile.x, pos0 = tile.y;
-      const int n_valid = min(NT, a.rb.off[e + 1] - pos0);
+      const int pos0 = tile_at(a, it / RT).y;
 #pragma unroll 1
       for (int s = 0; s < nsteps; ++s, ++g) {
         const int stage = g % C::SB;
@@ -328,48 +408,76 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
   } else if (warp == kWarpMma) {
     // -------------------------------------------------------------- MMA --
     if (lane == 0) {
-      uint32_t g = 0;
+      uint32_t g = 0, gg = 0;
       int item = 0;
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++item) {
-        const int2 tile = a.tiles[it / RT];
-        const int n_valid = min(NT, a.rb.off[tile.x + 1] - tile.y);
-        const int n_mma = (n_valid + 15) & ~15;
-        const uint32_t idesc = tc::idesc_f16(BM, n_mma, 0);
-        const int buf = item & 1;
-        if (!tc::bar_wait(&acc_empty[buf], ((item >> 1) & 1) ^ 1, a.wait_ns)) {
-          report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x330 | (DOWN ? 1 : 0));
-          break;
+      // one K step's MMAs into the accumulator set at `acc` (each matrix NT columns apart)
+      auto step = [&](int s, uint32_t acc, bool accumulate, uint32_t idesc) -> bool {
+        const int sa = g % C::SA, sb = g % C::SB;
+        if (!tc::bar_wait(&full_a[sa], (g / C::SA) & 1, a.wait_ns) ||
+            !tc::bar_wait(&full_b[sb], (g / C::SB) & 1, a.wait_ns)) {
+          report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x340 | (DOWN ? 1 : 0));
+          return false;
         }
         tc::fence_after_sync();
-        const uint32_t acc = tmem + buf * C::ACC_COLS;
+        tc::fence_proxy_async();
+        const uint32_t base = tc::smem_u32(smem + sa * C::A_STAGE);
+        const uint32_t bB = tc::smem_u32(smem + C::B_OFF + sb * C::B_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t db = tc::smem_desc_sw128(bB + kk * 32);
+#pragma unroll
+          for (int mm = 0; mm < C::NMAT; ++mm) {
+            const uint64_t da = tc::smem_desc(base + mm * C::A_BYTES + kk * 256, 128, 1024);
+            tc::mma_f16(acc + mm * NT, da, db, idesc, accumulate || kk != 0);
+          }
+        }
+        tc::commit(&empty_a[sa]);
+        tc::commit(&empty_b[sb]);
+        ++g;
+        (void)s;
+        return true;
+      };
+      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++item) {
+        const int n_valid = tile_valid(a, tile_at(a, it / RT));
+        const int n_mma = (n_valid + 15) & ~15;
+        const uint32_t idesc = tc::idesc_f16(BM, n_mma, 0);
+        if constexpr (C::PROMOTE) {
+          // each scale group into the block set; the epilogue empties it before the next group
+          const uint32_t blk = tmem + C::ACC_COLS;
 #pragma unroll 1
-        for (int s = 0; s < nsteps; ++s, ++g) {
-          const int sa = g % C::SA, sb = g % C::SB;
-          if (!tc::bar_wait(&full_a[sa], (g / C::SA) & 1, a.wait_ns) ||
-              !tc::bar_wait(&full_b[sb], (g / C::SB) & 1, a.wait_ns)) {
-            report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x340 | (DOWN ? 1 : 0));
-            ok = false;
+          for (int s0 = 0; ok && s0 < nsteps; s0 += C::GS, ++gg) {
+            if (!tc::bar_wait(&acc_empty[0], (gg & 1) ^ 1, a.wait_ns)) {
+              report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x330 | (DOWN ? 1 : 0));
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int j = 0; j < C::GS; ++j)
+              if (!step(s0 + j, blk, j != 0, idesc)) {
+                ok = false;
+                break;
+              }
+            if (ok) tc::commit(&acc_full[0]);
+          }
+        } else {
+          const int buf = item & 1;
+          if (!tc::bar_wait(&acc_empty[buf], ((item >> 1) & 1) ^ 1, a.wait_ns)) {
+            report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x330 | (DOWN ? 1 : 0));
             break;
           }
           tc::fence_after_sync();
-          tc::fence_proxy_async();
-          const uint32_t base = tc::smem_u32(smem + sa * C::A_STAGE);
-          const uint32_t bB = tc::smem_u32(smem + C::B_OFF + sb * C::B_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t db = tc::smem_desc_sw128(bB + kk * 32);
-#pragma unroll
-            for (int mm = 0; mm < C::NMAT; ++mm) {
-              const uint64_t da = tc::smem_desc(base + mm * C::A_BYTES + kk * 256, 128, 1024);
-              tc::mma_f16(acc + mm * NT, da, db, idesc, (s | kk) != 0);
+          const uint32_t acc = tmem + buf * C::ACC_COLS;
+#pragma unroll 1
+          for (int s = 0; s < nsteps; ++s)
+            if (!step(s, acc, s != 0, idesc)) {
+              ok = false;
+              break;
             }
-          }
-          tc::commit(&empty_a[sa]);
-          tc::commit(&empty_b[sb]);
+          if (!ok) break;
+          tc::commit(&acc_full[buf]);
         }
-        if (!ok) break;
-        tc::commit(&acc_full[buf]);
       }
       tc::commit(&drain);
       tc::bar_wait(&drain, 0, kDrainLimit);
@@ -385,77 +493,141 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
     const int q = warp & 3, chalf = ew >> 2;  // columns [64 * chalf, 64 * chalf + 64)
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
     uint8_t* stg = smem + C::STG_OFF;
+    const int row = q * 32 + lane;
     int item = 0;
+    uint32_t gg = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++item) {
-      const int2 tile = a.tiles[it / RT];
+      const int2 tile = tile_at(a, it / RT);
       const int rt = it % RT, e = tile.x, pos0 = tile.y;
-      const int n_valid = min(NT, a.rb.off[e + 1] - pos0);
-      const int buf = item & 1;
+      const int n_valid = tile_valid(a, tile);
       // per-column scale factors of this warp's columns, fetched before the wait
       float un_c[2];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int pos_l = pos0 + min(chalf * 64 + i * 32 + lane, n_valid - 1);
         if (DOWN) un_c[i] = exp2i(-a.hsig[pos_l]);
-        else un_c[i] = exp2i(-a.xsig[a.rb.pair[pos_l] / k]);
+        else un_c[i] = exp2i(-a.xsig[a.dense_T ? pos_l : a.rb.pair[pos_l] / k]);
       }
-      // the factor of this thread's row (TMEM lane) in each matrix: tensor scale or 2^reference
-      const int erow = rt * BM + q * 32 + lane;
-      float rf[2];
+      const int erow = rt * BM + row;
+      bool stop = false;
+      if constexpr (C::PROMOTE) {
+        // per scale group: running = scale * block (+ running), the running sums in TMEM
+        // columns [0, ACC_COLS), the group's block in [ACC_COLS, 2 ACC_COLS)
+        const int ngrp = nsteps / C::GS;
+#pragma unroll 1
+        for (int gi = 0; gi < ngrp; ++gi, ++gg) {
+          float sc[C::NMAT];
 #pragma unroll
-      for (int mm = 0; mm < C::NMAT; ++mm) {
-        const QW& Wm = DOWN ? a.down : (mm == 0 ? a.gate : a.up);
-        const uint8_t* sr = Wm.scales + (size_t)e * scale_bytes(F, N, K) + (size_t)erow * row_scale_bytes<F>(K);
-        rf[mm] = row_factor<F>(row_ref<F>(sr, K), F == MOE_FMT_NVFP4 ? __ldg(Wm.ts + e) : 1.f);
-      }
-      const float tsg = DOWN ? 0.f : rf[0], tsu = DOWN ? 0.f : rf[C::NMAT - 1];
-      const bool ready = tc::bar_wait(&acc_full[buf], (item >> 1) & 1, a.wait_ns);
-      if (!ready) report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x310 | (DOWN ? 1 : 0));
-      // all epilogue warps go on, or all stop; the barrier also frees the staging tile
-      // (the previous tile's copies have read it)
-      if (!tc::named_all(1, kEpiThreads, ready)) break;
-      tc::fence_after_sync();
-      const uint32_t acc = tq + buf * C::ACC_COLS;
-      const int row = q * 32 + lane;
+          for (int mm = 0; mm < C::NMAT; ++mm)
+            sc[mm] = group_scale<F>(DOWN ? a.down : (mm == 0 ? a.gate : a.up), e, N, K, erow, rt, gi);
+          const bool ready = tc::bar_wait(&acc_full[0], gg & 1, a.wait_ns);
+          if (!ready) report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x310 | (DOWN ? 1 : 0));
+          // all epilogue warps go on, or all stop; the barrier also frees the staging tile
+          if (!tc::named_all(1, kEpiThreads, ready)) {
+            stop = true;
+            break;
+          }
+          tc::fence_after_sync();
+          const bool last = gi == ngrp - 1;
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            const int c0 = chalf * 64 + ch * 16;
+            if (c0 >= n_valid) break;
+            float r[C::NMAT][16];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int c0 = chalf * 64 + i * 32;
-        if (c0 >= n_valid) break;
-        const int ncol = min(32, n_valid - c0);
-        if (!DOWN) {
-          uint32_t gv[32], uv[32];
-          tc::tmem_ld32(acc + c0, gv);
-          tc::tmem_ld32(acc + NT + c0, uv);
-          tc::tmem_ld_wait();
-          uint16_t* st16 = reinterpret_cast<uint16_t*>(stg) + (size_t)c0 * BM + row;
+            for (int mm = 0; mm < C::NMAT; ++mm) {
+              uint32_t bv[16], rv[16];
+              tc::tmem_ld16(tq + C::ACC_COLS + mm * NT + c0, bv);
+              if (gi > 0) tc::tmem_ld16(tq + mm * NT + c0, rv);
+              tc::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float un = __shfl_sync(0xFFFFFFFFu, un_c[i], j);
-            if (j < ncol) {
-              const float gg = __uint_as_float(gv[j]) * (tsg * un);
-              const float uu = __uint_as_float(uv[j]) * (tsu * un);
-              st16[j * BM] = float_to_bf16_bits(silu(gg) * uu);
+              for (int j = 0; j < 16; ++j)
+                r[mm][j] = gi > 0 ? fmaf(sc[mm], __uint_as_float(bv[j]), __uint_as_float(rv[j]))
+                                  : sc[mm] * __uint_as_float(bv[j]);
+              if (!last) tmem_st16(tq + mm * NT + c0, r[mm]);
+            }
+            if (last) {
+              const int ncol = min(16, n_valid - c0);
+              const float un_i = un_c[(ch * 16) / 32];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float un = __shfl_sync(0xFFFFFFFFu, un_i, (ch * 16) % 32 + j);
+                if (j < ncol) {
+                  if (!DOWN) {
+                    const float gv = r[0][j] * un, uv = r[C::NMAT - 1][j] * un;
+                    reinterpret_cast<uint16_t*>(stg)[(size_t)(c0 + j) * BM + row] = float_to_bf16_bits(silu(gv) * uv);
+                  } else if (a.p_bf16) {
+                    reinterpret_cast<uint16_t*>(stg)[(size_t)(c0 + j) * BM + row] = float_to_bf16_bits(r[0][j] * un);
+                  } else {
+                    reinterpret_cast<float*>(stg)[(size_t)(c0 + j) * BM + row] = r[0][j] * un;
+                  }
+                }
+              }
             }
           }
-        } else {
-          uint32_t dv[32];
-          tc::tmem_ld32(acc + c0, dv);
-          tc::tmem_ld_wait();
-          float* st32 = reinterpret_cast<float*>(stg) + (size_t)c0 * BM + row;
-          uint16_t* sb16 = reinterpret_cast<uint16_t*>(stg) + (size_t)c0 * BM + row;  // bf16-partials lever
+          if (!last) tmem_st_wait();
+          tc::fence_before_sync();
+          tc::bar_arrive(&acc_empty[0]);  // the block set is free for the next group's MMAs
+        }
+        if (stop) break;
+      } else {
+        // the factor of this thread's row (TMEM lane) in each matrix: tensor scale or 2^reference
+        float rf[2];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float un = __shfl_sync(0xFFFFFFFFu, un_c[i], j);
-            if (j < ncol) {
-              const float v = __uint_as_float(dv[j]) * (rf[0] * un);
-              if (a.p_bf16) sb16[j * BM] = float_to_bf16_bits(v);
-              else st32[j * BM] = v;
+        for (int mm = 0; mm < C::NMAT; ++mm) {
+          const QW& Wm = DOWN ? a.down : (mm == 0 ? a.gate : a.up);
+          const uint8_t* sr = Wm.scales + (size_t)e * scale_bytes(F, N, K) + (size_t)erow * row_scale_bytes<F>(K);
+          rf[mm] = row_factor<F>(row_ref<F>(sr, K), F == MOE_FMT_NVFP4 ? __ldg(Wm.ts + e) : 1.f);
+        }
+        const float tsg = DOWN ? 0.f : rf[0], tsu = DOWN ? 0.f : rf[C::NMAT - 1];
+        const int buf = item & 1;
+        const bool ready = tc::bar_wait(&acc_full[buf], (item >> 1) & 1, a.wait_ns);
+        if (!ready) report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x310 | (DOWN ? 1 : 0));
+        // all epilogue warps go on, or all stop; the barrier also frees the staging tile
+        // (the previous tile's copies have read it)
+        if (!tc::named_all(1, kEpiThreads, ready)) break;
+        tc::fence_after_sync();
+        const uint32_t acc = tq + buf * C::ACC_COLS;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int c0 = chalf * 64 + i * 32;
+          if (c0 >= n_valid) break;
+          const int ncol = min(32, n_valid - c0);
+          if (!DOWN) {
+            uint32_t gv[32], uv[32];
+            tc::tmem_ld32(acc + c0, gv);
+            tc::tmem_ld32(acc + NT + c0, uv);
+            tc::tmem_ld_wait();
+            uint16_t* st16 = reinterpret_cast<uint16_t*>(stg) + (size_t)c0 * BM + row;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float un = __shfl_sync(0xFFFFFFFFu, un_c[i], j);
+              if (j < ncol) {
+                const float gg2 = __uint_as_float(gv[j]) * (tsg * un);
+                const float uu = __uint_as_float(uv[j]) * (tsu * un);
+                st16[j * BM] = float_to_bf16_bits(silu(gg2) * uu);
+              }
+            }
+          } else {
+            uint32_t dv[32];
+            tc::tmem_ld32(acc + c0, dv);
+            tc::tmem_ld_wait();
+            float* st32 = reinterpret_cast<float*>(stg) + (size_t)c0 * BM + row;
+            uint16_t* sb16 = reinterpret_cast<uint16_t*>(stg) + (size_t)c0 * BM + row;  // bf16-partials lever
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float un = __shfl_sync(0xFFFFFFFFu, un_c[i], j);
+              if (j < ncol) {
+                const float v = __uint_as_float(dv[j]) * (rf[0] * un);
+                if (a.p_bf16) sb16[j * BM] = float_to_bf16_bits(v);
+                else st32[j * BM] = v;
+              }
             }
           }
         }
+        tc::fence_before_sync();
+        tc::bar_arrive(&acc_empty[buf]);  // TMEM buffer free for the MMA of a later tile
       }
-      tc::fence_before_sync();
-      tc::bar_arrive(&acc_empty[buf]);  // TMEM buffer free for the MMA of a later tile
       tc::fence_proxy_async();          // staging writes -> bulk copy reads
       tc::named_sync(1, kEpiThreads);
       if (ew == 0) {
@@ -517,22 +689,22 @@ bool f16_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uin
 
 }  // namespace
 
-size_t prefill_gemm_smem(bool down) { return down ? Cfg<true>::SMEM : Cfg<false>::SMEM; }
-
 template <int F>
 cudaError_t launch_pf_gemm(bool down, const PrefillArgs& a, int grid, cudaStream_t s) {
   cudaError_t err;
   alignas(64) CUtensorMap tm;
   if (down) {
     if (!f16_map(&tm, a.h16, (uint64_t)a.I, (uint64_t)a.T * a.k, NT)) return cudaErrorInvalidValue;
-    err = cudaFuncSetAttribute(pf_gemm_kernel<F, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true>::SMEM);
+    err = cudaFuncSetAttribute(pf_gemm_kernel<F, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<F, true>::SMEM);
     if (err != cudaSuccess) return err;
-    pf_gemm_kernel<F, true><<<grid, kPfGemmThreads, Cfg<true>::SMEM, s>>>(a, tm);
+    pf_gemm_kernel<F, true><<<grid, kPfGemmThreads, Cfg<F, true>::SMEM, s>>>(a, tm);
   } else {
     if (!f16_map(&tm, a.xg, (uint64_t)a.H, (uint64_t)a.T * a.k, NT)) return cudaErrorInvalidValue;
-    err = cudaFuncSetAttribute(pf_gemm_kernel<F, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<false>::SMEM);
+    err = cudaFuncSetAttribute(pf_gemm_kernel<F, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<F, false>::SMEM);
     if (err != cudaSuccess) return err;
-    pf_gemm_kernel<F, false><<<grid, kPfGemmThreads, Cfg<false>::SMEM, s>>>(a, tm);
+    pf_gemm_kernel<F, false><<<grid, kPfGemmThreads, Cfg<F, false>::SMEM, s>>>(a, tm);
   }
   return cudaGetLastError();
 }
@@ -542,6 +714,9 @@ cudaError_t launch_prefill_gemm(bool down, const PrefillArgs& a, int grid, cudaS
     case MOE_FMT_NVFP4: return launch_pf_gemm<MOE_FMT_NVFP4>(down, a, grid, s);
     case MOE_FMT_MXFP4: return launch_pf_gemm<MOE_FMT_MXFP4>(down, a, grid, s);
     case MOE_FMT_INT4_G64: return launch_pf_gemm<MOE_FMT_INT4_G64>(down, a, grid, s);
+    case MOE_FMT_INT8_G64: return launch_pf_gemm<MOE_FMT_INT8_G64>(down, a, grid, s);
+    case MOE_FMT_FP8_B128: return launch_pf_gemm<MOE_FMT_FP8_B128>(down, a, grid, s);
+    case MOE_FMT_INT4_G128: return launch_pf_gemm<MOE_FMT_INT4_G128>(down, a, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -17,7 +17,8 @@ from oracle import formats as F
 from oracle import moe as M
 from quantized_moe_decode_router_gb300 import _binding as B
 from quantized_moe_decode_router_gb300.device import to_device
-from synth.configs import FMT_INT4_G64, FMT_INT8_G64, FMT_MXFP4, FMT_NVFP4, LayerConfig
+from synth.configs import (FMT_FP8_B128, FMT_INT4_G64, FMT_INT4_G128, FMT_INT8_G64, FMT_MXFP4, FMT_NVFP4,
+                           LayerConfig)
 from tests import gpu_util as G
 
 pytestmark = pytest.mark.gpu
@@ -94,6 +95,14 @@ SMALL = [
     LayerConfig("p_skew", FMT_NVFP4, H=512, E=24, k=4, I=128, zipf_s=1.1),
     LayerConfig("p_mxfp4", FMT_MXFP4, H=640, E=7, k=2, I=256),
     LayerConfig("p_int4", FMT_INT4_G64, H=384, E=9, k=3, I=384, zipf_s=1.1),
+    # shared experts of every format (dense over all tokens), and the formats whose scale is applied
+    # per group in FP32 (int8 g64, FP8 b128, int4 g128) as routed experts
+    LayerConfig("p_nvfp4_fp8", FMT_NVFP4, H=512, E=8, k=2, I=256, shared_fmt=FMT_FP8_B128, shared_I=384),
+    LayerConfig("p_int4_int8", FMT_INT4_G64, H=384, E=6, k=3, I=256, shared_fmt=FMT_INT8_G64, shared_I=256),
+    LayerConfig("p_int8_nvfp4", FMT_INT8_G64, H=256, E=5, k=2, I=128, shared_fmt=FMT_NVFP4, shared_I=256),
+    LayerConfig("p_fp8_mxfp4", FMT_FP8_B128, H=384, E=6, k=2, I=256, shared_fmt=FMT_MXFP4, shared_I=128),
+    LayerConfig("p_g128", FMT_INT4_G128, H=512, E=7, k=3, I=256, shared_fmt=FMT_INT4_G128, shared_I=256),
+    LayerConfig("p_mx_int4", FMT_MXFP4, H=256, E=4, k=2, I=128, shared_fmt=FMT_INT4_G64, shared_I=128),
 ]
 
 
@@ -134,13 +143,14 @@ def test_prefill_deterministic_and_batch_invariant():
 
 
 @pytest.mark.parametrize("name,T,tokens", [("decode_mxfp4", 512, [0, 255, 511]),
-                                           ("decode_int4", 384, [0, 200, 383])])
-def test_prefill_mxfp4_int4_workloads_sampled(name, T, tokens):
-    """The exact-chain GEMMs on the MXFP4 and int4 g64 layer shapes at full
-    size (the int4 layer without its int8 shared expert), sampled tokens."""
-    cfg = G.host_layer(name).cfg.with_(shared_fmt=0, shared_I=0, name=name + "_routed")
-    hl = synth.make_layer(cfg, seed=0)
-    dl = to_device(hl)
+                                           ("decode_int4", 384, [0, 200, 383]),
+                                           ("decode_nvfp4", 1024, [0, 511, 1023])])
+def test_prefill_decode_layers_at_full_size_sampled(name, T, tokens):
+    """Prefill of the MXFP4, int4 g64 (+ int8 g64 shared) and NVFP4 (+ FP8 b128
+    shared) decode layers at full size, sampled tokens."""
+    hl = G.host_layer(name)
+    dl = G.device_layer(name)
+    cfg = hl.cfg
     x = synth.make_tokens(cfg, T, seed=0, batch=T)
     y, routing = G.decode(dl, x, prefill=True)
     ref = M.layer_forward(hl, x, tokens=tokens)
@@ -182,22 +192,21 @@ def test_prefill_wide_scale_spreads(fmt):
     _check_y(y, ref["y_bits"])
 
 
-@pytest.mark.parametrize("case", ["int8_shared", "fp8_shared", "w4a4_mxfp4"])
+@pytest.mark.parametrize("case", ["w4a4_shared", "w4a4_mxfp4", "w4a4_int8"])
 def test_prefill_unsupported_is_reported(case):
-    """Shared experts and the W4A4 lever on a format other than NVFP4 are not
-    implemented in prefill: the call reports MOE_ERR_UNSUPPORTED."""
-    if case == "int8_shared":
-        cfg = LayerConfig("p_u1", FMT_INT4_G64, H=256, E=4, k=2, I=128, shared_fmt=FMT_INT8_G64, shared_I=128)
-    elif case == "fp8_shared":
-        cfg = G.host_layer("decode_nvfp4").cfg
+    """The W4A4 lever is implemented for NVFP4 routed experts without a shared
+    expert only: other layers report MOE_ERR_UNSUPPORTED before any launch."""
+    if case == "w4a4_shared":
+        cfg = LayerConfig("p_u1", FMT_NVFP4, H=256, E=4, k=2, I=256, shared_fmt=FMT_FP8_B128, shared_I=128)
+    elif case == "w4a4_mxfp4":
+        cfg = LayerConfig("p_u2", FMT_MXFP4, H=256, E=4, k=2, I=256)
     else:
-        cfg = LayerConfig("p_u3", FMT_MXFP4, H=256, E=4, k=2, I=128)
-    dl = to_device(synth.make_layer(cfg, seed=1)) if case != "fp8_shared" else G.device_layer("decode_nvfp4")
+        cfg = LayerConfig("p_u3", FMT_INT8_G64, H=256, E=4, k=2, I=256)
+    dl = to_device(synth.make_layer(cfg, seed=1))
     x = G.x_device(synth.make_tokens(cfg, 20, seed=1))
     y = torch.zeros((20, cfg.H), dtype=torch.int16, device="cuda")
-    ws = G.new_ws(dl, 20)
-    st = B.moe_prefill_forward(dl, x, 20, y, ws, raise_on_error=False,
-                               act_quant=case == "w4a4_mxfp4")
+    ws = G.new_ws(dl, 20, 1)
+    st = B.moe_prefill_forward(dl, x, 20, y, ws, raise_on_error=False, act_quant=1)
     assert st == B.MOE_ERR_UNSUPPORTED
 
 

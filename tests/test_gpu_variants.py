@@ -150,6 +150,18 @@ def test_decode_sigmoid_gated_shared_expert(shared_fmt, T):
     assert np.array_equal(y2, y)
 
 
+@pytest.mark.parametrize("shared_fmt", [FMT_FP8_B128, FMT_NVFP4])
+def test_prefill_sigmoid_gated_shared_expert(shared_fmt):
+    cfg = LayerConfig("psg", FMT_NVFP4, H=512, E=16, k=4, I=256, shared_fmt=shared_fmt, shared_I=256)
+    hl = synth.make_layer(cfg, seed=29)
+    hl.extra["shared_gate_w"] = (np.random.default_rng(29).standard_normal(cfg.H) * 0.1).astype(np.float32)
+    dl = to_device(hl)
+    T = 150
+    x = synth.make_tokens(cfg, T, seed=29, batch=T)
+    y, _ = G.decode(dl, x, prefill=True)
+    _check_y(y, M.layer_forward(hl, x)["y_bits"])
+
+
 # --------------------------------------------------------------- bf16 partials ----
 
 @pytest.mark.parametrize("name,T", [("decode_nvfp4", 8), ("tiny_nvfp4", 1)])
@@ -165,9 +177,10 @@ def test_decode_bf16_partials(name, T):
     _check_y(y.cpu().numpy().view(np.uint16), M.layer_forward(hl, x, bf16_partials=True)["y_bits"])
 
 
-@pytest.mark.parametrize("T", [17, 300])
-def test_prefill_bf16_partials(T):
-    cfg = LayerConfig("pbf", FMT_NVFP4, H=512, E=24, k=4, I=256, zipf_s=1.1)
+@pytest.mark.parametrize("T,shared_fmt", [(17, 0), (300, 0), (200, FMT_INT8_G64)])
+def test_prefill_bf16_partials(T, shared_fmt):
+    cfg = LayerConfig("pbf", FMT_NVFP4, H=512, E=24, k=4, I=256, zipf_s=1.1, shared_fmt=shared_fmt,
+                      shared_I=256 if shared_fmt else 0)
     hl = synth.make_layer(cfg, seed=27)
     dl = to_device(hl)
     x = synth.make_tokens(cfg, T, seed=27, batch=T)
@@ -182,10 +195,12 @@ def test_prefill_bf16_partials(T):
 
 # --------------------------------------------------------- bounded device waits ----
 
-def test_prefill_wait_limit_runs_out_and_is_reported():
+@pytest.mark.parametrize("fmt", [FMT_NVFP4, FMT_INT8_G64])
+def test_prefill_wait_limit_runs_out_and_is_reported(fmt):
     # a 1 us limit on every pipeline wait of the prefill GEMMs: the first wait that needs HBM data
     # gives up, each CTA drains what it issued and returns, and moe_check reports the timeout
-    cfg = LayerConfig("waits", FMT_NVFP4, H=512, E=24, k=4, I=256)
+    # (int8 g64: the per-group accumulation's waits)
+    cfg = LayerConfig("waits", fmt, H=512, E=24, k=4, I=256)
     hl = synth.make_layer(cfg, seed=28)
     dl = to_device(hl)
     T = 300
