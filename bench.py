@@ -46,9 +46,9 @@ FALLBACK_HBM_GBS = 6800.0
 # decode_nvfp4 workload, from one ncu capture of the current kernel; None while the kernel has
 # changed since the counters were taken.
 GATEUP_TRAFFIC_BYTES = None
-# kernels one decode layer call launches: router (approximate logits, exact selection + dispatch),
-# gate/up, down, combine
-DECODE_KERNELS_PER_CALL = 5
+# kernels one decode layer call launches: router stage 1 (approximate logits), router stage 2
+# (exact selection), gate/up, down (with the combine fused)
+DECODE_KERNELS_PER_CALL = 4
 
 
 def _peaks():

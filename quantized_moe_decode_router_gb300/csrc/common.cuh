@@ -112,6 +112,14 @@ __device__ __forceinline__ void prefetch_l2_share(const uint8_t* base, size_t le
   }
 }
 
+// Named barrier `id` over n threads (a multiple of 32): wait for all, or arrive only.
+__device__ __forceinline__ void bar_sync_n(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive_n(uint32_t id, uint32_t n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // 2^e as a float for e in [-126, 127].
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 

@@ -692,14 +692,16 @@ __device__ __forceinline__ bool block_reduce(float (&acc)[NM][4], const float* t
 }
 
 // ------------------------------------------------------------ local dispatch --
-// Every gate/up CTA builds the dispatch index of the call in shared memory
-// from the T * k top-k ids (at most 128 pairs): pairs sorted by (expert, pair
-// id) - the stable counting sort of the router's dispatch - the active experts
-// in ascending id, and each one's segment of the sorted list.  CTA 0 also
-// writes the index to the workspace (counts and offsets of every expert, the
-// pair list, the active list) for the down and combine kernels.  Ids outside
-// [0, E), or an expert named twice by one token (a top-k choice names distinct
-// experts), are reported as MOE_ERR_DEVICE_BAD_INDEX and their pairs left out.
+// Every gate/up and down CTA builds the dispatch index of the call in shared
+// memory from the T * k top-k ids (at most 128 pairs): pairs sorted by
+// (expert, pair id) - the stable counting sort of the router's dispatch - the
+// active experts in ascending id, and each one's segment of the sorted list.
+// A group of nthr >= 128 threads does it (tid: the index in the group),
+// synchronised on named barrier `bar`.  Gate/up CTA 0 also writes the index
+// to the workspace (counts and offsets of every expert, the pair list, the
+// active list): the routing outputs of the call.  Ids outside [0, E), or an
+// expert named twice by one token (a top-k choice names distinct experts),
+// are reported as MOE_ERR_DEVICE_BAD_INDEX and their pairs left out.
 constexpr int kMaxPairs = kMaxT * 16;
 
 struct LocalDispatch {
@@ -711,8 +713,9 @@ struct LocalDispatch {
   int n_active, n_valid;
 };
 
-static __device__ void local_dispatch(const ExpertArgs& a, LocalDispatch& d, bool write_global) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+static __device__ void local_dispatch(const ExpertArgs& a, LocalDispatch& d, bool write_global, int tid, int nthr,
+                                      uint32_t bar) {
+  const int lane = tid & 31, warp = tid >> 5;
   const int P = a.T * a.k, E = a.E, k = a.k;
   if (tid < P) {
     int e = __ldcg(a.rb.topk_idx + tid);
@@ -722,16 +725,16 @@ static __device__ void local_dispatch(const ExpertArgs& a, LocalDispatch& d, boo
     }
     d.pe[tid] = e;
   }
-  __syncthreads();
+  bar_sync_n(bar, nthr);
   bool dup = false;  // the same expert twice in one token: keep the first
   if (tid < P && d.pe[tid] >= 0)
     for (int q = tid / k * k; q < tid; ++q) dup = dup || d.pe[q] == d.pe[tid];
-  __syncthreads();
+  bar_sync_n(bar, nthr);
   if (dup) {
     report_error(a.rb.ctrl, (uint32_t)MOE_ERR_DEVICE_BAD_INDEX, 0x041);
     d.pe[tid] = -1;
   }
-  __syncthreads();
+  bar_sync_n(bar, nthr);
   // rank of each pair under the key (expert, pair id), left-out pairs last
   if (tid < P) {
     const int ep = d.pe[tid] >= 0 ? d.pe[tid] : E;
@@ -743,7 +746,7 @@ static __device__ void local_dispatch(const ExpertArgs& a, LocalDispatch& d, boo
     }
     d.sorted[rank] = tid;
   }
-  __syncthreads();
+  bar_sync_n(bar, nthr);
   // segment starts: the first sorted entry of each expert (ballots over the pair warps)
   bool first = false;
   int e = -1;
@@ -754,9 +757,9 @@ static __device__ void local_dispatch(const ExpertArgs& a, LocalDispatch& d, boo
   const uint32_t bal = __ballot_sync(0xFFFFFFFFu, first);
   const uint32_t valid = __ballot_sync(0xFFFFFFFFu, tid < P && e >= 0);
   if (lane == 0) d.wcnt[warp] = __popc(bal) | (__popc(valid) << 16);
-  __syncthreads();
+  bar_sync_n(bar, nthr);
   int base = 0, nact = 0, nvalid = 0;
-  for (int w = 0; w < kExpertThreads / 32; ++w) {
+  for (int w = 0; w < nthr / 32; ++w) {
     if (w < warp) base += d.wcnt[w] & 0xFFFF;
     nact += d.wcnt[w] & 0xFFFF;
     nvalid += d.wcnt[w] >> 16;
@@ -771,12 +774,12 @@ static __device__ void local_dispatch(const ExpertArgs& a, LocalDispatch& d, boo
     d.n_valid = nvalid;
     d.aoff[nact] = nvalid;
   }
-  __syncthreads();
+  bar_sync_n(bar, nthr);
   if (!write_global) return;
-  for (int i = tid; i < d.n_valid; i += kExpertThreads) a.rb.pair[i] = d.sorted[i];
-  for (int i = tid; i < d.n_active; i += kExpertThreads) a.rb.act[i] = d.act[i];
+  for (int i = tid; i < d.n_valid; i += nthr) a.rb.pair[i] = d.sorted[i];
+  for (int i = tid; i < d.n_active; i += nthr) a.rb.act[i] = d.act[i];
   // counts and offsets of every expert: binary search of the sorted valid pairs
-  for (int x = tid; x <= E; x += kExpertThreads) {
+  for (int x = tid; x <= E; x += nthr) {
     int lo = 0, hi = d.n_valid;  // first sorted position whose expert is >= x
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
@@ -823,7 +826,6 @@ __global__ void __launch_bounds__(kExpertThreads, MINB) gateup_kernel(ExpertArgs
   __shared__ int s_pexp[kMaxT + 1];
   __shared__ const uint16_t* s_src[kMaxT];
 
-  pdl_launch_dependents();
   // the activations are an input of the call: stage them before waiting on the router
   if (tid < T) s_src[tid] = a.x + (size_t)tid * H;
   __syncthreads();
@@ -932,25 +934,27 @@ __global__ void __launch_bounds__(kExpertThreads, MINB) gateup_kernel(ExpertArgs
     }
   };
 
-  // the shared expert depends on the tokens only: a warp whose first task is a shared one runs it
-  // before the router's results are needed
+  // The shared expert depends on the tokens only: warps [0, ws) of this CTA start on a shared task
+  // (q0 < n_shared_tasks) and run it before the router's results are needed, while the other warps
+  // (at least four) wait for the router and build the dispatch; the shared-task warps then take it
+  // over a named barrier, so a routed task never waits for a shared one.
   const int q0 = warp * gridDim.x + blockIdx.x;
-  const bool ran_first = q0 < n_shared_tasks;
-  if (ran_first) run_task(q0);
-  __syncthreads();
-  pdl_wait();
-  local_dispatch(a, ld, blockIdx.x == 0);
-  // every active expert's gate and up bytes are brought into L2 now, each CTA its share, so HBM
-  // streams from the start of the routed work and the warps' rings read from L2
-  if (tid < 32) {
-    const size_t db = data_bytes(FR, I, H), sb = scale_bytes(FR, I, H);
-    for (int i = lane; i < ld.n_active * 4; i += 32) {
-      const int slot = i >> 2, what = i & 3;
-      const QW& w = (what & 1) ? a.up : a.gate;
-      const size_t e = (size_t)ld.act[slot];
-      if (what < 2) prefetch_l2_share(w.data + e * db, db, blockIdx.x, gridDim.x);
-      else prefetch_l2_share(w.scales + e * sb, sb, blockIdx.x, gridDim.x);
-    }
+  const int ws = n_shared_tasks > (int)blockIdx.x
+                     ? min(kWarps, (n_shared_tasks - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x)
+                     : 0;
+  const bool early = ws <= kWarps - 4;
+  const bool ran_first = early && warp < ws;
+  if (ran_first) {
+    run_task(q0);
+    pdl_wait();
+    bar_sync_n(2, kExpertThreads);  // the dispatch is built
+  } else {
+    pdl_wait();
+    const int g0 = early ? 32 * ws : 0;
+    local_dispatch(a, ld, blockIdx.x == 0, tid - g0, kExpertThreads - g0, 1);
+    // the down kernel may start now: the router has completed, so its prologue can read the top-k ids
+    pdl_launch_dependents();
+    if (early && ws > 0) bar_arrive_n(2, kExpertThreads);
   }
   {
     n_rtiles = ld.n_active * tpe;
@@ -991,6 +995,57 @@ __device__ __forceinline__ void store_partial(const ExpertArgs& a, bool shared_i
   }
 }
 
+// The combine, fused into the down kernel: every (segment, 16-row slab of H)
+// piece of the down projection, once its rows of P (or S) are stored, counts
+// itself in y_cnt[slab]; the warp that brings the count to n_seg forms the
+// slab's rows of y for every token, y[t] = bf16( sum_j w[t, j] * P[t*k + j]
+// (+ g_t S[t]) ), j ascending with the shared term last (g_t the shared
+// expert's sigmoid gate when the layer has one, else 1).  Called by a whole
+// warp.
+__device__ __forceinline__ float4 load_partial4(const float* base, size_t row, int H, int c4, int bf16) {
+  if (!bf16) return __ldcg(reinterpret_cast<const float4*>(base + row * H) + c4);
+  const uint2 v = __ldcg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + row * H) + c4);
+  return make_float4(bf16_bits_to_float(v.x & 0xFFFF), bf16_bits_to_float(v.x >> 16), bf16_bits_to_float(v.y & 0xFFFF),
+                     bf16_bits_to_float(v.y >> 16));
+}
+
+template <int FS>
+__device__ __forceinline__ void slab_done(const ExpertArgs& a, int slab, int n_seg) {
+  const int lane = threadIdx.x & 31;
+  __threadfence();  // this warp's partial rows, before the count
+  __syncwarp();
+  uint32_t prev = 0;
+  if (lane == 0) prev = atomicAdd(a.y_cnt + slab, 1u);
+  prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+  if (prev + 1 != (uint32_t)n_seg) return;
+  __threadfence();  // every other piece's rows, after the count
+  const int H = a.H, k = a.k;
+  // lane = (token, 4 consecutive columns of the slab): T * 4 <= 32 items
+  if (lane < a.T * 4) {
+    const int t = lane >> 2, c4 = slab * 4 + (lane & 3);
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      const float w = __ldcg(a.rb.topk_w + t * k + j);
+      const float4 p = load_partial4(a.P, (size_t)(t * k + j), H, c4, a.p_bf16);
+      y[0] = __fmaf_rn(w, p.x, y[0]);
+      y[1] = __fmaf_rn(w, p.y, y[1]);
+      y[2] = __fmaf_rn(w, p.z, y[2]);
+      y[3] = __fmaf_rn(w, p.w, y[3]);
+    }
+    if (FS) {
+      const float4 sv = load_partial4(a.S, (size_t)t, H, c4, a.p_bf16);
+      const float g = a.shared_g ? __ldcg(a.shared_g + t) : 1.f;
+      y[0] = __fmaf_rn(g, sv.x, y[0]);
+      y[1] = __fmaf_rn(g, sv.y, y[1]);
+      y[2] = __fmaf_rn(g, sv.z, y[2]);
+      y[3] = __fmaf_rn(g, sv.w, y[3]);
+    }
+    const uint32_t lo = (uint32_t)float_to_bf16_bits(y[0]) | ((uint32_t)float_to_bf16_bits(y[1]) << 16);
+    const uint32_t hi = (uint32_t)float_to_bf16_bits(y[2]) | ((uint32_t)float_to_bf16_bits(y[3]) << 16);
+    reinterpret_cast<uint2*>(a.y + (size_t)t * H)[c4] = make_uint2(lo, hi);
+  }
+}
+
 template <int FR, int FS>
 __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -1006,11 +1061,13 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
   __shared__ int s_ncols[kMaxDnSegs];
   __shared__ const uint16_t* s_src[kMaxT];
 
+  __shared__ LocalDispatch ld;
   pdl_launch_dependents();
-  pdl_wait();
-  // the gate/up kernel has finished: leave its task counter at zero for the next call
-  if (blockIdx.x == 0 && tid == 0) a.rb.ctrl->gu_next = 0;
-  const int n_active = *reinterpret_cast<volatile int*>(&a.rb.ctrl->n_active);
+  // The gate/up kernel let this grid start only after its own wait on the router, so the top-k
+  // ids are complete: the dispatch, the task range and the L2 prefetch of this CTA's weights run
+  // before the wait for gate/up's h.
+  local_dispatch(a, ld, false, tid, kExpertThreads, 1);
+  const int n_active = ld.n_active;
   const int tpe = H / 16;
   const int S = a.dn_slices;
   const int Br = dec_blocks(FR, I), Bs = FS ? dec_blocks(FS, a.Is) : 1;
@@ -1033,17 +1090,15 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
   const int q0 = task_at(total * blockIdx.x / gridDim.x);
   const int q1 = task_at(total * (blockIdx.x + 1) / gridDim.x);
   const int r = lane >> 2, c = lane & 3;
-  if (q0 >= q1) return;
-  // this CTA's weight bytes (one contiguous row range per segment) are brought into L2 before the
-  // hidden rows are staged; the warps' rings then read them from L2
-  if (tid < 32) {
+  // this CTA's weight bytes (one contiguous row range per segment) are brought into L2 while
+  // gate/up runs; the warps' rings then read them from L2
+  if (q0 < q1 && tid < 32) {
     const int seg_a = q0 / tasks_per_seg, seg_b = (q1 - 1) / tasks_per_seg;
     for (int seg = seg_a + lane; seg <= seg_b; seg += 32) {
       const bool shared_item = FS && seg == 0;
       const int fmt = shared_item ? FS : FR;
       const int K = shared_item ? a.Is : I;
-      const int e = shared_item ? 0 : a.rb.act[seg - sh];
-      if ((unsigned)e >= (unsigned)a.E) continue;
+      const int e = shared_item ? 0 : ld.act[seg - sh];
       const QW& qd = shared_item ? a.sdown : a.down;
       const int t_a = max(q0, seg * tasks_per_seg) - seg * tasks_per_seg;
       const int t_b = min(q1, (seg + 1) * tasks_per_seg) - seg * tasks_per_seg;  // tasks [t_a, t_b)
@@ -1059,6 +1114,11 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
     }
   }
 
+  pdl_wait();
+  // the gate/up kernel has finished: leave its task counter at zero for the next call
+  if (blockIdx.x == 0 && tid == 0) a.rb.ctrl->gu_next = 0;
+  if (q0 >= q1) return;
+
   // the segments of [q0, q1), staged SG at a time; inside a group the warps
   // take the tasks in turn with no barrier between segments
   const int seg_lo = q0 / tasks_per_seg, seg_hi = (q1 - 1) / tasks_per_seg;
@@ -1070,11 +1130,11 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
       const bool shared_item = FS && seg == 0;
       int ncols;
       if (!shared_item) {
-        const int e = a.rb.act[seg - sh];
-        ncols = (unsigned)e < (unsigned)a.E ? min(a.rb.cnt[e], kMaxT) : 0;  // a bad id was reported by gate/up
+        const int slot = seg - sh;
+        ncols = min(ld.aoff[slot + 1] - ld.aoff[slot], kMaxT);
         if (tid < kMaxT) {
           if (tid < ncols) {
-            const int p = a.rb.pair[a.rb.off[e] + tid];
+            const int p = ld.sorted[ld.aoff[slot] + tid];
             s_src[tid] = a.h + (size_t)p * I;
             s_col_out[i][tid] = p;
           } else {
@@ -1106,7 +1166,7 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
         const int ntile = (a1 - 1 - qs) / kWarps + 1;
         const int i = seg - sg;
         const bool shared_item = FS && seg == 0;
-        const int e = shared_item ? 0 : a.rb.act[seg - sh];
+        const int e = shared_item ? 0 : ld.act[seg - sh];
         const int ncols = s_ncols[i];
         const int K = shared_item ? a.Is : I;
         const int fmt = shared_item ? FS : FR;
@@ -1125,6 +1185,7 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
             const int out = s_col_out[i][col];
             if (out >= 0) store_partial(a, shared_item, out, row, acc[0][j] * exp2i(s_pexp[i][col]) * ts);
           }
+          slab_done<FS>(a, tile, n_seg);
         };
         if (shared_item) {
           if constexpr (FS != 0) warp_tiles<FS, 1, kStagesDN>(m, tile0 * 16, 16 * kWarps, ntile, K, bu, xrow, ring, epi);
@@ -1137,7 +1198,7 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
     for (int q = t_lo + warp; q < t_hi; q += kWarps) {
       const int seg = q / tasks_per_seg, i = seg - sg;
       const bool shared_item = FS && seg == 0;
-      const int e = shared_item ? 0 : a.rb.act[seg - sh];
+      const int e = shared_item ? 0 : ld.act[seg - sh];
       const int ncols = s_ncols[i];
       const int K = shared_item ? a.Is : I;
       const int fmt = shared_item ? FS : FR;
@@ -1167,57 +1228,9 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
         const int out = s_col_out[i][col];
         if (out >= 0) store_partial(a, shared_item, out, row, acc[0][j] * exp2i(s_pexp[i][col]) * ts);
       }
+      slab_done<FS>(a, tile, n_seg);
     }
   }
-}
-
-// y[t] = bf16( sum_j w[t, j] * P[t*k + j] (+ g_t S[t]) ), j ascending, after the
-// down kernel (programmatic dependent launch; waits for its completion).  g_t
-// is the shared expert's sigmoid gate when the layer has one, else 1.
-__device__ __forceinline__ float4 load_partial4(const float* base, size_t row, int H, int c4, int bf16) {
-  if (!bf16) return __ldcg(reinterpret_cast<const float4*>(base + row * H) + c4);
-  const uint2 v = __ldcg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + row * H) + c4);
-  return make_float4(bf16_bits_to_float(v.x & 0xFFFF), bf16_bits_to_float(v.x >> 16), bf16_bits_to_float(v.y & 0xFFFF),
-                     bf16_bits_to_float(v.y >> 16));
-}
-
-template <int FS>
-__global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const int H = a.H, k = a.k;
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // (token, 4 columns)
-  if (i >= a.T * (H / 4)) return;
-  const int t = i / (H / 4), c4 = i - t * (H / 4);
-  // all k partial rows are loaded before the j-ordered fma chain (k <= 16)
-  float wj[16];
-  float4 pj[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if (j < k) {
-      wj[j] = __ldcg(a.rb.topk_w + t * k + j);
-      pj[j] = load_partial4(a.P, (size_t)(t * k + j), H, c4, a.p_bf16);
-    }
-  float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if (j < k) {
-      y[0] = __fmaf_rn(wj[j], pj[j].x, y[0]);
-      y[1] = __fmaf_rn(wj[j], pj[j].y, y[1]);
-      y[2] = __fmaf_rn(wj[j], pj[j].z, y[2]);
-      y[3] = __fmaf_rn(wj[j], pj[j].w, y[3]);
-    }
-  if (FS) {
-    const float4 sv = load_partial4(a.S, (size_t)t, H, c4, a.p_bf16);
-    const float g = a.shared_g ? __ldcg(a.shared_g + t) : 1.f;
-    y[0] = __fmaf_rn(g, sv.x, y[0]);
-    y[1] = __fmaf_rn(g, sv.y, y[1]);
-    y[2] = __fmaf_rn(g, sv.z, y[2]);
-    y[3] = __fmaf_rn(g, sv.w, y[3]);
-  }
-  const uint32_t lo = (uint32_t)float_to_bf16_bits(y[0]) | ((uint32_t)float_to_bf16_bits(y[1]) << 16);
-  const uint32_t hi = (uint32_t)float_to_bf16_bits(y[2]) | ((uint32_t)float_to_bf16_bits(y[3]) << 16);
-  reinterpret_cast<uint2*>(a.y + (size_t)t * H)[c4] = make_uint2(lo, hi);
 }
 
 template <int FR, int FS>

@@ -73,6 +73,7 @@ struct ExpertArgs {
   int dn_segs;        // expert segments the down kernel stages at once (1 .. kMaxDnSegs)
   const float* shared_g;  // [T] sigmoid gate of the shared expert per token, or nullptr (weight 1)
   int p_bf16;         // 1: P and S are stored as BF16 (the bf16-partials lever)
+  uint32_t* y_cnt;    // [H/16] (segment, 16-row slab) pieces of the down projection finished per slab
 };
 
 constexpr int kMaxDnSegs = 4;
@@ -199,9 +200,6 @@ cudaError_t launch_prefill_logits_tc(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_gemm(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill_gemm_w4a4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
 
-// Decode combine y = bf16(sum_j w_j P_j (+ S)), launched after the down
-// kernel as a programmatic dependent of it.
-cudaError_t launch_combine_decode(const ExpertArgs& a, cudaStream_t s);
 
 // moe_dequantize / moe_quantize_act_nvfp4
 cudaError_t launch_dequantize(int fmt, QW w, int N, int K, int expert, int row0, int nrows, float* out,
