@@ -28,7 +28,7 @@ bool shape_ok(int fmt, int N, int K) {
 }
 
 struct Layout {
-  size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, approx, rwnorm, sgate, gu_part, gu_cnt,
+  size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, approx, sgate, gu_part, gu_cnt,
       dn_part, dn_cnt, y_cnt;
   // prefill path
   size_t xg, xsig, xnorm, wnorm, hist, pos_of, tiles, h16, hsig, xq, xsf, xqg, xsfg, hq, hsf, rw_hi, rw_lo;
@@ -60,7 +60,6 @@ Layout make_layout(const moe_layer* L, int maxT) {
   o.P = take(T * k * H * 4);
   o.S = take(T * H * 4 + 16);
   o.approx = take(T * E * 4);
-  o.rwnorm = take(E * 4);
   o.sgate = take(T * 4);
   // block sums of tiles split along K (at most kMaxSplitBlocks entries)
   const size_t act_max = T * k < E ? T * k : E;
@@ -69,7 +68,7 @@ Layout make_layout(const moe_layer* L, int maxT) {
   o.gu_cnt = take(gu_tiles * 4);
   o.dn_part = take((size_t)kMaxSplitBlocks * 32 * 4 * 4);
   o.dn_cnt = take(dn_tiles * 4);
-  o.y_cnt = take(H / 16 * 4);  // cleared with the split counters
+  o.y_cnt = take(H / 16 * 4);  // reset by the warp that completes each slab, like the split counters
   const size_t nchunk = (T + kPfChunk - 1) / kPfChunk;
   o.max_tiles = (int)(T * k / kPfTokTile + E + 1);
   o.xg = take(T * k * H * 2);
@@ -230,7 +229,6 @@ RouterArgs router_args(const moe_layer* L, const Layout& lo, void* ws, const voi
   ra.bias = L->router_bias;
   ra.rb = route_bufs(lo, ws);
   ra.approx = reinterpret_cast<float*>(b + lo.approx);
-  ra.rwnorm = reinterpret_cast<float*>(b + lo.rwnorm);
   ra.bias_select = L->bias_select;
   ra.sgate_w = L->shared_fmt ? L->shared_expert_gate : nullptr;
   ra.sgate = reinterpret_cast<float*>(b + lo.sgate);

@@ -1000,8 +1000,9 @@ __device__ __forceinline__ void store_partial(const ExpertArgs& a, bool shared_i
 // itself in y_cnt[slab]; the warp that brings the count to n_seg forms the
 // slab's rows of y for every token, y[t] = bf16( sum_j w[t, j] * P[t*k + j]
 // (+ g_t S[t]) ), j ascending with the shared term last (g_t the shared
-// expert's sigmoid gate when the layer has one, else 1).  Called by a whole
-// warp.
+// expert's sigmoid gate when the layer has one, else 1), and sets the count
+// back to zero for the next call (as the split counters do).  Called by a
+// whole warp.
 __device__ __forceinline__ float4 load_partial4(const float* base, size_t row, int H, int c4, int bf16) {
   if (!bf16) return __ldcg(reinterpret_cast<const float4*>(base + row * H) + c4);
   const uint2 v = __ldcg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + row * H) + c4);
@@ -1019,6 +1020,7 @@ __device__ __forceinline__ void slab_done(const ExpertArgs& a, int slab, int n_s
   prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
   if (prev + 1 != (uint32_t)n_seg) return;
   __threadfence();  // every other piece's rows, after the count
+  if (lane == 0) a.y_cnt[slab] = 0u;  // the count starts from zero in the next call
   const int H = a.H, k = a.k;
   // lane = (token, 4 consecutive columns of the slab): T * 4 <= 32 items
   if (lane < a.T * 4) {

@@ -42,8 +42,7 @@ struct RouterArgs {
   const float* bias;  // [E] or nullptr
   RouteBufs rb;
   RouteOut out;
-  float* approx;      // [T, E] approximate logits (no bias)
-  float* rwnorm;      // [E] ||Wr_e||_2 (FP32)
+  float* approx;      // [T, E] unbiased exact logits (written under bias_select)
   const float* sgate_w;  // [H] gate vector of the shared expert, or nullptr
   float* sgate;       // [T] sigmoid(x_t . sgate_w) (written when sgate_w is set)
 };

@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kMaxT = MOE_DECODE_MAX_TOKENS;
 constexpr int kWarpsR = kRouterThreads / 32;
-constexpr int kSelThreads = 512;  // threads of the per-token selection and of the external dispatch
+constexpr int kSelThreads = 512;  // threads of the one-CTA dispatch kernels (moe_route, caller routing)
 constexpr int kSelWarps = kSelThreads / 32;
 
 // Selection key of a candidate: larger logit first, equal logits -> smaller
@@ -311,37 +311,126 @@ __global__ void __launch_bounds__(kSelThreads) dispatch_ext_kernel(RouterArgs a,
   (void)E;
 }
 
-// ---- decode router, stage 1: approximate logits on every SM -----------------
-// Each expert row is split over `wpr` warps; a lane owns 8-column chunks of
-// its warp's share and issues every weight load of the row before using any.
-// Per token: a = sum_h x[t, h] * Wr[e, h] by FMA (exact products, one rounding
-// per addition: |a - dot| <= gamma_H sum |x w| <= gamma_H ||x_t|| ||Wr_e||
-// whatever the order of the additions).  Per row: ||Wr_e||^2 by FMA.
-constexpr int kApproxChunks = 2;  // 8-column chunks a lane holds in flight at once
+// ---- decode router: exact logits of every expert on every SM, then top-k ----
+// Each expert row (and, as row E, the shared expert's gate vector) is split
+// over `wpr` warps; a lane owns 8-column chunks of its warp's share, issues
+// every weight load of the batch before using any, and accumulates each
+// token's dot product as a float-float pair (Dot2: the product split exactly
+// by FMA, the sum by TwoSum).  The pairs are merged across lanes and then
+// across the row's warps in a fixed order and rounded once: the correctly
+// rounded FP32 logit unless the exact sum lies within about 2^-44 (relative)
+// of a rounding midpoint.  The CTA that finishes last (arrival counter, no
+// spin) runs every token's top-k, one warp per token.
+constexpr int kLogitChunks = 2;  // 8-column chunks a lane holds in flight at once
 
-__global__ void __launch_bounds__(kRouterThreads) router_approx_kernel(RouterArgs a) {
-  __shared__ float s_acc[kWarpsR][kMaxT + 1];
+// One warp: the top k of token t's E exact logits (logit descending, expert id
+// ascending) and their renormalised softmax weights (from the unbiased logits
+// under bias_select).  Lane l holds experts l + 32 q.  L = the k-th largest of
+// the 32 lane maxima is at most the k-th largest key, so the keys >= L (at
+// least k) contain the top k; up to 32 of them are sorted by one warp bitonic
+// sort, more (flat or tied logits) are taken by k rounds of warp maxima.
+__device__ void decode_topk_warp(const RouterArgs& a, int t, unsigned long long* s_c) {
+  constexpr int NQ = 1024 / 32;  // n_experts <= 1024
+  const int lane = threadIdx.x & 31, E = a.E, k = a.k;
+  const float* row = a.rb.logits + (size_t)t * E;
+  uint32_t ord[NQ];
+  unsigned long long best = 0ull;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    const int e = lane + 32 * q;
+    ord[q] = e < E ? ord_key(__ldcg(row + e)) : 0u;
+    const unsigned long long key = ord[q] ? (((unsigned long long)ord[q] << 32) | (uint32_t)~(uint32_t)e) : 0ull;
+    best = key > best ? key : best;
+  }
+  const unsigned long long L = __shfl_sync(0xFFFFFFFFu, warp_sort_desc(best), k - 1);
+  int n = 0;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    const unsigned long long key = (((unsigned long long)ord[q] << 32) | (uint32_t)~(uint32_t)(lane + 32 * q));
+    n += (ord[q] != 0u && key >= L) ? 1 : 0;
+  }
+  int base = n;  // inclusive scan of the candidate counts over the lanes
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, base, o);
+    if (lane >= o) base += v;
+  }
+  const int total = __shfl_sync(0xFFFFFFFFu, base, 31);
+  base -= n;
+  unsigned long long my_key = 0ull;
+  if (total <= 32) {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const unsigned long long key = (((unsigned long long)ord[q] << 32) | (uint32_t)~(uint32_t)(lane + 32 * q));
+      if (ord[q] != 0u && key >= L) s_c[base++] = key;
+    }
+    __syncwarp();
+    my_key = warp_sort_desc(lane < total ? s_c[lane] : 0ull);  // lane j: the (j+1)-th largest
+    __syncwarp();
+  } else {
+    for (int j = 0; j < k; ++j) {
+      unsigned long long b = 0ull;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        const unsigned long long key = ord[q] ? (((unsigned long long)ord[q] << 32) | (uint32_t)~(uint32_t)(lane + 32 * q)) : 0ull;
+        b = key > b ? key : b;
+      }
+      const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(b >> 32));
+      const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(b >> 32) == mhi ? (uint32_t)b : 0u);
+      const unsigned long long m = ((unsigned long long)mhi << 32) | mlo;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q)  // keys are unique (the low half names the expert)
+        if (ord[q] && (((unsigned long long)ord[q] << 32) | (uint32_t)~(uint32_t)(lane + 32 * q)) == m) ord[q] = 0u;
+      if (lane == j) my_key = m;
+    }
+  }
+  const int my_e = (int)~(uint32_t)my_key;
+  const int e0 = __shfl_sync(0xFFFFFFFFu, my_e, 0);
+  float lj = ord_value((uint32_t)(my_key >> 32));
+  float l0 = __shfl_sync(0xFFFFFFFFu, lj, 0);
+  if (a.bias_select) {  // the bias steered the choice only: the weights use the unbiased logits
+    lj = lane < k ? __ldcg(a.approx + (size_t)t * E + my_e) : 0.f;
+    l0 = __ldcg(a.approx + (size_t)t * E + e0);
+  }
+  const float my_ex = lane < k ? expf(lj - l0) : 0.f;
+  float sum = my_ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  if (lane < k) {
+    const float w = my_ex / sum;
+    a.rb.topk_idx[t * k + lane] = my_e;
+    a.rb.topk_w[t * k + lane] = w;
+    if (a.out.topk_idx) a.out.topk_idx[t * k + lane] = my_e;
+    if (a.out.topk_w) a.out.topk_w[t * k + lane] = w;
+  }
+}
+
+__global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArgs a) {
+  __shared__ float s_hi[kWarpsR][kMaxT], s_lo[kWarpsR][kMaxT];
+  __shared__ unsigned long long s_c[kWarpsR][32];
+  __shared__ int s_last;
   const int H = a.H, E = a.E, T = a.T, wpr = a.wpr;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // the selection kernel that follows may start now: it reads the tokens, then waits for this grid
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the gate/up kernel may start now: it stages the tokens and runs shared-expert work, then waits
   asm volatile("griddepcontrol.launch_dependents;");
+  const int rows = E + (a.sgate_w ? 1 : 0);
   const int rows_per_cta = kWarpsR / wpr;
   const int e = blockIdx.x * rows_per_cta + warp / wpr;
   const int part = warp % wpr;
   const int Hw = H / wpr, nch = Hw / 8;
-  float acc[kMaxT], nrm = 0.f;
+  float hi[kMaxT], lo[kMaxT];
 #pragma unroll
-  for (int t = 0; t < kMaxT; ++t) acc[t] = 0.f;
-  if (e < E) {
-    const float* wrow = a.w + (size_t)e * H + (size_t)part * Hw;
+  for (int t = 0; t < kMaxT; ++t) { hi[t] = 0.f; lo[t] = 0.f; }
+  if (e < rows) {
+    const float* wrow = (e < E ? a.w + (size_t)e * H : a.sgate_w) + (size_t)part * Hw;
     const uint16_t* xp = a.x + (size_t)part * Hw;
-    for (int c0 = lane; c0 < nch; c0 += 32 * kApproxChunks) {
+    for (int c0 = lane; c0 < nch; c0 += 32 * kLogitChunks) {
       // every load of this batch (weights, and the tokens' matching columns, clamped to a
       // valid token so no load waits behind a branch) is issued before any is used
-      float4 wv[kApproxChunks][2];
-      uint4 xv[kApproxChunks][kMaxT];
+      float4 wv[kLogitChunks][2];
+      uint4 xv[kLogitChunks][kMaxT];
 #pragma unroll
-      for (int j = 0; j < kApproxChunks; ++j) {
+      for (int j = 0; j < kLogitChunks; ++j) {
         const int c = min(c0 + 32 * j, nch - 1);
         wv[j][0] = __ldg(reinterpret_cast<const float4*>(wrow + 8 * c));
         wv[j][1] = __ldg(reinterpret_cast<const float4*>(wrow + 8 * c + 4));
@@ -350,20 +439,18 @@ __global__ void __launch_bounds__(kRouterThreads) router_approx_kernel(RouterArg
           xv[j][t] = __ldg(reinterpret_cast<const uint4*>(xp + (size_t)min(t, T - 1) * H + 8 * c));
       }
 #pragma unroll
-      for (int j = 0; j < kApproxChunks; ++j) {
+      for (int j = 0; j < kLogitChunks; ++j) {
         if (c0 + 32 * j < nch) {
           const float w8[8] = {wv[j][0].x, wv[j][0].y, wv[j][0].z, wv[j][0].w,
                                wv[j][1].x, wv[j][1].y, wv[j][1].z, wv[j][1].w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) nrm = fmaf(w8[i], w8[i], nrm);
 #pragma unroll
           for (int t = 0; t < kMaxT; ++t) {
             if (t < T) {
               const uint32_t xw[4] = {xv[j][t].x, xv[j][t].y, xv[j][t].z, xv[j][t].w};
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                acc[t] = fmaf(bf16_bits_to_float(xw[i] & 0xFFFF), w8[2 * i], acc[t]);
-                acc[t] = fmaf(bf16_bits_to_float(xw[i] >> 16), w8[2 * i + 1], acc[t]);
+                dot2_step(bf16_bits_to_float(xw[i] & 0xFFFF), w8[2 * i], hi[t], lo[t]);
+                dot2_step(bf16_bits_to_float(xw[i] >> 16), w8[2 * i + 1], hi[t], lo[t]);
               }
             }
           }
@@ -375,264 +462,42 @@ __global__ void __launch_bounds__(kRouterThreads) router_approx_kernel(RouterArg
   for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
     for (int t = 0; t < kMaxT; ++t)
-      if (t < T) acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
-    nrm += __shfl_xor_sync(0xFFFFFFFFu, nrm, o);
+      if (t < T) {
+        const float h2 = __shfl_xor_sync(0xFFFFFFFFu, hi[t], o);
+        const float l2 = __shfl_xor_sync(0xFFFFFFFFu, lo[t], o);
+        dot2_merge(hi[t], lo[t], h2, l2);
+      }
   }
   if (lane == 0) {
 #pragma unroll
-    for (int t = 0; t < kMaxT; ++t) s_acc[warp][t] = acc[t];
-    s_acc[warp][kMaxT] = nrm;
+    for (int t = 0; t < kMaxT; ++t) { s_hi[warp][t] = hi[t]; s_lo[warp][t] = lo[t]; }
   }
   __syncthreads();
-  // the first warp of each row adds the row's parts and writes a[t, e] and ||Wr_e||
-  if (e < E && part == 0 && lane <= T) {
-    const int slot = lane < T ? lane : kMaxT;
-    float v = s_acc[warp][slot];
-    for (int p = 1; p < wpr; ++p) v += s_acc[warp + p][slot];
-    if (lane < T) a.approx[(size_t)lane * E + e] = v;
-    else a.rwnorm[e] = sqrtf(v);
+  // the first warp of each row merges the row's parts in order and rounds once
+  if (e < rows && part == 0 && lane < T) {
+    float h = s_hi[warp][lane], l = s_lo[warp][lane];
+    for (int p = 1; p < wpr; ++p) dot2_merge(h, l, s_hi[warp + p][lane], s_lo[warp + p][lane]);
+    const float lg = __fadd_rn(h, l);
+    if (e == E) {
+      a.sgate[lane] = 1.f / (1.f + expf(-lg));  // the shared expert's sigmoid gate
+    } else {
+      const float lb = a.bias ? __fadd_rn(lg, __ldg(a.bias + e)) : lg;
+      a.rb.logits[(size_t)lane * E + e] = lb;
+      if (a.bias_select) a.approx[(size_t)lane * E + e] = lg;
+    }
   }
+  // the last CTA to finish runs the top-k of every token
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&a.rb.ctrl->router_arrive, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid == 0) a.rb.ctrl->router_arrive = 0u;  // the count starts from zero in the next call
+  for (int t = warp; t < T; t += kWarpsR) decode_topk_warp(a, t, s_c[warp]);
 }
 
-// ---- decode router, stage 2: exact logits of the candidates, top-k ----------
-// One CTA per token, one thread per expert (two when E > 512).  eps_e bounds
-// |a_e + b_e - l_e| for the FP32 logit l_e (the approximation's
-// gamma_H ||x|| ||Wr_e||, widened by 2^-8 for the rounding of the norms, plus
-// the FP32 additions of the bias and of the final rounding).  Any L not above
-// the k-th largest lower bound a - eps is a valid threshold: an expert whose
-// upper bound a + eps is below L has an exact logit below k others.  Here L is
-// the k-th largest of the per-warp top-2 lower bounds (k distinct experts
-// reach it), which admits about k + 1 candidates.  The candidates get the
-// exact float-float logit (Dot2, correctly rounded, as every logit of the
-// prefill router), top-k with the fixed tie rule runs on them, and the last
-// CTA to finish builds the dispatch index.
-constexpr int kSelRowChunk = 16;  // float4 columns a lane holds in flight during the exact dot product
-
-// Dynamic shared memory of router_select_kernel: x_t (H bf16) and five E-entry rows (lower and
-// upper bounds, candidate ids, candidate logits, the unbiased ones).
-size_t select_smem_bytes(int H, int E) { return (size_t)H * 2 + (size_t)5 * E * 4; }
-
-// Selection key: larger value first, equal values -> lower id first (one 64-bit maximum).
-__device__ __forceinline__ unsigned long long cand_key(float v, int e) {
-  return ((unsigned long long)ord_key(v) << 32) | (uint32_t)(~(uint32_t)e);
-}
-
-__global__ void __launch_bounds__(kSelThreads) router_select_kernel(RouterArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int H = a.H, E = a.E, T = a.T, k = a.k;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int t = blockIdx.x;
-  uint16_t* s_x = reinterpret_cast<uint16_t*>(smem);
-  float* s_lo = reinterpret_cast<float*>(smem + (size_t)H * 2);  // [E]
-  float* s_hi = s_lo + E;                                          // [E]
-  int32_t* s_cand = reinterpret_cast<int32_t*>(s_hi + E);          // [E] candidate expert ids
-  float* s_cval = reinterpret_cast<float*>(s_cand + E);            // [E] exact selection logits of candidates
-  float* s_cunb = s_cval + E;                                      // [E] exact logits used by the weights
-  __shared__ uint32_t s_top2[kSelWarps][2];
-  __shared__ float s_red[kSelWarps];
-  __shared__ float s_L;
-  __shared__ int s_ncand;
-  asm volatile("griddepcontrol.launch_dependents;");
-  // the token is an input of the call: stage it and find ||x_t|| before waiting for stage 1
-  float ss = 0.f;
-  for (int i = tid; i < H / 8; i += kSelThreads) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H) + i);
-    reinterpret_cast<uint4*>(s_x)[i] = v;
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float lo = bf16_bits_to_float(w[q] & 0xFFFF), hi = bf16_bits_to_float(w[q] >> 16);
-      ss = fmaf(lo, lo, ss);
-      ss = fmaf(hi, hi, ss);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-  if (lane == 0) s_red[warp] = ss;
-  if (tid == 0) s_ncand = 0;
-  float bias_v[2] = {0.f, 0.f};
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int e = tid + r * kSelThreads;
-    if (a.bias && e < E) bias_v[r] = __ldg(a.bias + e);
-  }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  __syncthreads();
-  float xn2 = lane < kSelWarps ? s_red[lane] : 0.f;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) xn2 += __shfl_xor_sync(0xFFFFFFFFu, xn2, o);
-  // the FP32 sum of H squares is within gamma_H of the true one: widen by 2^-10 before the root
-  const float xnorm = sqrtf(xn2 * 1.0009765625f);
-  const float u = 5.9604645e-8f;  // 2^-24
-  const float gam = (float)H * u / (1.f - (float)H * u);
-  // bounds of this thread's experts (coalesced loads of stage 1's results)
-  float lo_v[2], hi_v[2];
-  uint32_t key[2];
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int e = tid + r * kSelThreads;
-    lo_v[r] = hi_v[r] = 0.f;
-    key[r] = 0u;
-    if (e < E) {
-      const float d = __ldcg(a.approx + (size_t)t * E + e);
-      const float wn = __ldcg(a.rwnorm + e);
-      const float b = bias_v[r];
-      const float ab = __fadd_rn(d, b);
-      const float eps0 = gam * xnorm * wn * 1.00390625f;
-      const float eps = eps0 + 4.7683716e-7f * (fabsf(d) + fabsf(b) + eps0) + 1e-30f;
-      lo_v[r] = ab - eps;
-      hi_v[r] = ab + eps;
-      s_lo[e] = lo_v[r];
-      s_hi[e] = hi_v[r];
-      key[r] = ord_key(lo_v[r]);
-    }
-  }
-  // the warp's two largest lower bounds
-  {
-    uint32_t best = max(key[0], key[1]);
-    const uint32_t m1 = __reduce_max_sync(0xFFFFFFFFu, best);
-    const uint32_t holders = __ballot_sync(0xFFFFFFFFu, best == m1);
-    if (lane == __ffs(holders) - 1) best = min(key[0], key[1]);  // drop one copy of the maximum
-    const uint32_t m2 = __reduce_max_sync(0xFFFFFFFFu, best);
-    if (lane == 0) { s_top2[warp][0] = m1; s_top2[warp][1] = m2; }
-  }
-  __syncthreads();
-  // L = the k-th largest of those 32 lower bounds (k <= 16 <= 32 distinct experts stand behind them)
-  if (warp == 0) {
-    const unsigned long long v = warp_sort_desc(s_top2[lane >> 1][lane & 1]);
-    const uint32_t m = (uint32_t)__shfl_sync(0xFFFFFFFFu, v, k - 1);  // the k-th largest
-    // fewer than k experts behind the 32 values (small E): every expert is a candidate
-    if (lane == 0) s_L = m ? ord_value(m) : __int_as_float(0xFF800000);
-  }
-  __syncthreads();
-  // candidates: upper bound not below L; the others hold -inf in the workspace row
-  const float L = s_L;
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int e = tid + r * kSelThreads;
-    const bool cand = e < E && !(hi_v[r] < L);
-    if (e < E && !cand) a.rb.logits[(size_t)t * E + e] = __int_as_float(0xFF800000);
-    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, cand);
-    int base = 0;
-    if (lane == 0 && bal) base = atomicAdd(&s_ncand, __popc(bal));
-    base = __shfl_sync(0xFFFFFFFFu, base, 0);
-    if (cand) s_cand[base + __popc(bal & ((1u << lane) - 1u))] = e;
-  }
-  __syncthreads();
-  // exact logits of the candidates, one warp per candidate, lanes on consecutive float4 columns;
-  // each lane loads its columns in chunks of kSelRowChunk before the float-float loop.  One more
-  // row (c == nc) is the shared expert's gate vector when the layer has one.
-  const int nc = s_ncand;
-  const int nrows = nc + (a.sgate_w ? 1 : 0);
-  for (int c = warp; c < nrows; c += kSelWarps) {
-    const bool gate_row = c == nc;
-    const int e = gate_row ? 0 : s_cand[c];
-    const float4* wrow = reinterpret_cast<const float4*>(gate_row ? a.sgate_w : a.w + (size_t)e * H);
-    const uint2* xp = reinterpret_cast<const uint2*>(s_x);
-    float hi = 0.f, lo = 0.f;
-    for (int q0 = lane; q0 < H / 4; q0 += 32 * kSelRowChunk) {
-      float4 wv[kSelRowChunk];
-#pragma unroll
-      for (int j = 0; j < kSelRowChunk; ++j)
-        if (q0 + 32 * j < H / 4) wv[j] = __ldg(wrow + q0 + 32 * j);
-#pragma unroll
-      for (int j = 0; j < kSelRowChunk; ++j) {
-        const int q = q0 + 32 * j;
-        if (q < H / 4) {
-          const uint2 xv = xp[q];
-          dot2_step(bf16_bits_to_float(xv.x & 0xFFFF), wv[j].x, hi, lo);
-          dot2_step(bf16_bits_to_float(xv.x >> 16), wv[j].y, hi, lo);
-          dot2_step(bf16_bits_to_float(xv.y & 0xFFFF), wv[j].z, hi, lo);
-          dot2_step(bf16_bits_to_float(xv.y >> 16), wv[j].w, hi, lo);
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float h2 = __shfl_xor_sync(0xFFFFFFFFu, hi, o);
-      const float l2 = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
-      dot2_merge(hi, lo, h2, l2);
-    }
-    if (lane == 0 && gate_row) {
-      // sigmoid of the correctly rounded FP32 gate logit
-      a.sgate[t] = 1.f / (1.f + expf(-__fadd_rn(hi, lo)));
-    } else if (lane == 0) {
-      const float lg = __fadd_rn(hi, lo);
-      const float b = a.bias ? __ldg(a.bias + e) : 0.f;
-      const float lb = a.bias ? __fadd_rn(lg, b) : lg;
-      // the approximation's bound must hold for every exact logit (self-check of the bound)
-      if (lg == lg && (lb < s_lo[e] || lb > s_hi[e])) report_error(a.rb.ctrl, (uint32_t)MOE_ERR_DEVICE_BAD_INDEX, 0x020);
-      s_cval[c] = lb;
-      // bias_select: the bias decides the selection only; the weights use the unbiased logit
-      s_cunb[c] = a.bias_select ? lg : lb;
-      a.rb.logits[(size_t)t * E + e] = lb;
-    }
-  }
-  __syncthreads();
-  if (warp == 0 && nc <= 32) {
-    // top-k of the candidates (k <= nc <= 32): one key per lane (logit descending, id ascending),
-    // sorted across the warp; lane j then holds the j-th choice
-    const unsigned long long key = lane < nc ? cand_key(s_cval[lane], s_cand[lane]) : 0ull;
-    const unsigned long long sk = warp_sort_desc(key);
-    const int my_e = (int)(~(uint32_t)sk);
-    // the candidate slot of the chosen expert, for its (unbiased) weight logit
-    int slot = -1;
-    for (int c = 0; c < nc; ++c)
-      if (s_cand[c] == my_e) slot = c;
-    const int slot0 = __shfl_sync(0xFFFFFFFFu, slot, 0);
-    const float my_ex = lane < k ? expf(s_cunb[slot] - s_cunb[slot0]) : 0.f;
-    float sum = my_ex;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-    if (lane < k) {
-      const float w = my_ex / sum;
-      a.rb.topk_idx[t * k + lane] = my_e;
-      a.rb.topk_w[t * k + lane] = w;
-      if (a.out.topk_idx) a.out.topk_idx[t * k + lane] = my_e;
-      if (a.out.topk_w) a.out.topk_w[t * k + lane] = w;
-    }
-  } else if (warp == 0) {
-    // more than 32 candidates (flat or tied logits): rounds of a warp maximum over
-    // (logit descending, id ascending); a lane holds candidates lane + 32 j
-    const int per = (nc + 31) / 32;
-    int my_c = -1, c0 = -1;
-    for (int j = 0; j < k; ++j) {
-      unsigned long long bkey = 0ull;
-      int bc = -1;
-      for (int q = 0; q < per; ++q) {
-        const int c = lane + 32 * q;
-        if (c < nc && s_cand[c] >= 0) {
-          const unsigned long long kk = cand_key(s_cval[c], s_cand[c]);
-          if (kk > bkey) { bkey = kk; bc = c; }
-        }
-      }
-      const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(bkey >> 32));
-      const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(bkey >> 32) == mhi ? (uint32_t)bkey : 0u);
-      const uint32_t win = __ballot_sync(0xFFFFFFFFu, bc >= 0 && (uint32_t)(bkey >> 32) == mhi && (uint32_t)bkey == mlo);
-      const int wl = __ffs(win) - 1;
-      const int wc = __shfl_sync(0xFFFFFFFFu, bc, wl);
-      if (lane == j) my_c = wc;
-      if (j == 0) c0 = wc;
-      if (lane == wl) s_cand[wc] = -1 - s_cand[wc];  // taken (ids stay recoverable)
-      __syncwarp();
-    }
-    const int my_e = lane < k ? -1 - s_cand[my_c] : 0;
-    const float my_ex = lane < k ? expf(s_cunb[my_c] - s_cunb[c0]) : 0.f;
-    float sum = my_ex;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-    if (lane < k) {
-      const float w = my_ex / sum;
-      a.rb.topk_idx[t * k + lane] = my_e;
-      a.rb.topk_w[t * k + lane] = w;
-      if (a.out.topk_idx) a.out.topk_idx[t * k + lane] = my_e;
-      if (a.out.topk_w) a.out.topk_w[t * k + lane] = w;
-    }
-  }
-  // the dispatch index is built from these choices by the kernel that consumes them
-}
-
-// moe_route (T <= 8): the dispatch index of the selection kernel's choices (one CTA)
+// moe_route (T <= 8): the dispatch index of the router's choices (one CTA)
 __global__ void __launch_bounds__(kSelThreads) route_dispatch_kernel(RouterArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   int32_t* s_dcnt = reinterpret_cast<int32_t*>(smem);
@@ -766,26 +631,9 @@ int router_warps_per_row(int H, int E, int sms) {
 
 cudaError_t launch_router_decode(const RouterArgs& a, cudaStream_t s) {
   const int rows_per_cta = kWarpsR / a.wpr;
-  const int grid = (a.E + rows_per_cta - 1) / rows_per_cta;
-  router_approx_kernel<<<grid, kRouterThreads, 0, s>>>(a);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  const size_t smem = select_smem_bytes(a.H, a.E);
-  if (smem > 48 * 1024) {
-    err = cudaFuncSetAttribute(router_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.T);
-  cfg.blockDim = dim3(kSelThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, router_select_kernel, a);
+  const int rows = a.E + (a.sgate_w ? 1 : 0);
+  router_decode_kernel<<<(rows + rows_per_cta - 1) / rows_per_cta, kRouterThreads, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch_ext(const RouterArgs& a, const int32_t* idx, const float* w, cudaStream_t s) {
