@@ -46,8 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 # decode_nvfp4 workload, from one ncu capture of the current kernel; None while the kernel has
 # changed since the counters were taken.
 GATEUP_TRAFFIC_BYTES = None
-# kernels one decode layer call launches: router stage 1 (approximate logits), router stage 2
-# (exact selection), gate/up, down (with the combine fused)
+# kernels one decode layer call launches: router logits (exact, every SM), top-k selection (one CTA
+# per token), gate/up, down (with the combine fused)
 DECODE_KERNELS_PER_CALL = 4
 
 

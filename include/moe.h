@@ -170,11 +170,13 @@ int32_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
  * engine.expert_tile_list: routed segments per expert).
  *   logits     l[t, e] = fl32( sum_h x[t, h] * router_w[e, h] ), the correctly
  *              rounded FP32 dot product, then fl32(l + router_bias[e]) if a bias
- *              is given.  Selection and weights use these exact logits; the
- *              router finds them with an FP32 pass and a rigorous error bound,
- *              then recomputes exactly every expert that can still reach the
- *              top-k, so in the workspace's logits array (moe_workspace_layout)
- *              those experts hold l[t, e] and the others -inf.
+ *              is given.  Selection and weights use these exact logits.  For
+ *              T <= MOE_DECODE_MAX_TOKENS every expert's logit is computed
+ *              exactly and the workspace's logits array (moe_workspace_layout)
+ *              holds all of them; for larger T the router finds them with an
+ *              FP32 pass and a rigorous error bound, then recomputes exactly
+ *              every expert that can still reach the top-k, so those experts
+ *              hold l[t, e] and the others -inf.
  *   topk_idx   [T, k] i32: experts by logit descending, ties to the lower id.
  *   topk_w     [T, k] f32: exp(l_j - l_0) / sum_i exp(l_i - l_0) over the selected.
  *   expert_cnt [E] i32 pairs per expert; expert_off [E+1] i32 exclusive scan.

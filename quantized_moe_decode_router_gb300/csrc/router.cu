@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kMaxT = MOE_DECODE_MAX_TOKENS;
 constexpr int kWarpsR = kRouterThreads / 32;
-constexpr int kSelThreads = 512;  // threads of the one-CTA dispatch kernels (moe_route, caller routing)
+constexpr int kSelThreads = 512;  // threads of the per-token selection and of the one-CTA dispatch kernels
 constexpr int kSelWarps = kSelThreads / 32;
 
 // Selection key of a candidate: larger logit first, equal logits -> smaller
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kSelThreads) dispatch_ext_kernel(RouterArgs a,
   (void)E;
 }
 
-// ---- decode router: exact logits of every expert on every SM, then top-k ----
+// ---- decode router, stage 1: exact logits of every expert on every SM -------
 // Each expert row (and, as row E, the shared expert's gate vector) is split
 // over `wpr` warps; a lane owns 8-column chunks of its warp's share, issues
 // every weight load of the batch before using any, and accumulates each
@@ -319,99 +319,14 @@ __global__ void __launch_bounds__(kSelThreads) dispatch_ext_kernel(RouterArgs a,
 // by FMA, the sum by TwoSum).  The pairs are merged across lanes and then
 // across the row's warps in a fixed order and rounded once: the correctly
 // rounded FP32 logit unless the exact sum lies within about 2^-44 (relative)
-// of a rounding midpoint.  The CTA that finishes last (arrival counter, no
-// spin) runs every token's top-k, one warp per token.
+// of a rounding midpoint.
 constexpr int kLogitChunks = 2;  // 8-column chunks a lane holds in flight at once
-
-// One warp: the top k of token t's E exact logits (logit descending, expert id
-// ascending) and their renormalised softmax weights (from the unbiased logits
-// under bias_select).  Lane l holds experts l + 32 q.  L = the k-th largest of
-// the 32 lane maxima is at most the k-th largest key, so the keys >= L (at
-// least k) contain the top k; up to 32 of them are sorted by one warp bitonic
-// sort, more (flat or tied logits) are taken by k rounds of warp maxima.
-__device__ void decode_topk_warp(const RouterArgs& a, int t, unsigned long long* s_c) {
-  constexpr int NQ = 1024 / 32;  // n_experts <= 1024
-  const int lane = threadIdx.x & 31, E = a.E, k = a.k;
-  const float* row = a.rb.logits + (size_t)t * E;
-  uint32_t ord[NQ];
-  unsigned long long best = 0ull;
-#pragma unroll
-  for (int q = 0; q < NQ; ++q) {
-    const int e = lane + 32 * q;
-    ord[q] = e < E ? ord_key(__ldcg(row + e)) : 0u;
-    const unsigned long long key = ord[q] ? (((unsigned long long)ord[q] << 32) | (uint32_t)~(uint32_t)e) : 0ull;
-    best = key > best ? key : best;
-  }
-  const unsigned long long L = __shfl_sync(0xFFFFFFFFu, warp_sort_desc(best), k - 1);
-  int n = 0;
-#pragma unroll
-  for (int q = 0; q < NQ; ++q) {
-    const unsigned long long key = (((unsigned long long)ord[q] << 32) | (uint32_t)~(uint32_t)(lane + 32 * q));
-    n += (ord[q] != 0u && key >= L) ? 1 : 0;
-  }
-  int base = n;  // inclusive scan of the candidate counts over the lanes
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xFFFFFFFFu, base, o);
-    if (lane >= o) base += v;
-  }
-  const int total = __shfl_sync(0xFFFFFFFFu, base, 31);
-  base -= n;
-  unsigned long long my_key = 0ull;
-  if (total <= 32) {
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-      const unsigned long long key = (((unsigned long long)ord[q] << 32) | (uint32_t)~(uint32_t)(lane + 32 * q));
-      if (ord[q] != 0u && key >= L) s_c[base++] = key;
-    }
-    __syncwarp();
-    my_key = warp_sort_desc(lane < total ? s_c[lane] : 0ull);  // lane j: the (j+1)-th largest
-    __syncwarp();
-  } else {
-    for (int j = 0; j < k; ++j) {
-      unsigned long long b = 0ull;
-#pragma unroll
-      for (int q = 0; q < NQ; ++q) {
-        const unsigned long long key = ord[q] ? (((unsigned long long)ord[q] << 32) | (uint32_t)~(uint32_t)(lane + 32 * q)) : 0ull;
-        b = key > b ? key : b;
-      }
-      const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(b >> 32));
-      const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(b >> 32) == mhi ? (uint32_t)b : 0u);
-      const unsigned long long m = ((unsigned long long)mhi << 32) | mlo;
-#pragma unroll
-      for (int q = 0; q < NQ; ++q)  // keys are unique (the low half names the expert)
-        if (ord[q] && (((unsigned long long)ord[q] << 32) | (uint32_t)~(uint32_t)(lane + 32 * q)) == m) ord[q] = 0u;
-      if (lane == j) my_key = m;
-    }
-  }
-  const int my_e = (int)~(uint32_t)my_key;
-  const int e0 = __shfl_sync(0xFFFFFFFFu, my_e, 0);
-  float lj = ord_value((uint32_t)(my_key >> 32));
-  float l0 = __shfl_sync(0xFFFFFFFFu, lj, 0);
-  if (a.bias_select) {  // the bias steered the choice only: the weights use the unbiased logits
-    lj = lane < k ? __ldcg(a.approx + (size_t)t * E + my_e) : 0.f;
-    l0 = __ldcg(a.approx + (size_t)t * E + e0);
-  }
-  const float my_ex = lane < k ? expf(lj - l0) : 0.f;
-  float sum = my_ex;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-  if (lane < k) {
-    const float w = my_ex / sum;
-    a.rb.topk_idx[t * k + lane] = my_e;
-    a.rb.topk_w[t * k + lane] = w;
-    if (a.out.topk_idx) a.out.topk_idx[t * k + lane] = my_e;
-    if (a.out.topk_w) a.out.topk_w[t * k + lane] = w;
-  }
-}
 
 __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArgs a) {
   __shared__ float s_hi[kWarpsR][kMaxT], s_lo[kWarpsR][kMaxT];
-  __shared__ unsigned long long s_c[kWarpsR][32];
-  __shared__ int s_last;
   const int H = a.H, E = a.E, T = a.T, wpr = a.wpr;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // the gate/up kernel may start now: it stages the tokens and runs shared-expert work, then waits
+  // the selection kernel may start now (it waits for these logits)
   asm volatile("griddepcontrol.launch_dependents;");
   const int rows = E + (a.sgate_w ? 1 : 0);
   const int rows_per_cta = kWarpsR / wpr;
@@ -486,16 +401,105 @@ __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(RouterArg
       if (a.bias_select) a.approx[(size_t)lane * E + e] = lg;
     }
   }
-  // the last CTA to finish runs the top-k of every token
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&a.rb.ctrl->router_arrive, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (tid == 0) a.rb.ctrl->router_arrive = 0u;  // the count starts from zero in the next call
-  for (int t = warp; t < T; t += kWarpsR) decode_topk_warp(a, t, s_c[warp]);
 }
+
+// ---- decode router, stage 2: top-k of each token (one CTA per token) --------
+// One thread per expert (two when E > 512), keys (logit descending, expert id
+// ascending) from the exact logits of stage 1.  L = the k-th largest of the
+// per-warp top-2 keys is at most the k-th largest key, so the keys >= L (at
+// least k, typically a dozen) contain the top k; up to 32 of them are sorted
+// by one warp bitonic sort, more (flat or tied logits) are taken by rounds of
+// warp maxima.  The weights are the renormalised softmax of the chosen logits
+// (the unbiased ones under bias_select).
+__global__ void __launch_bounds__(kSelThreads) router_select_kernel(RouterArgs a) {
+  __shared__ unsigned long long s_top2[kSelWarps][2];
+  __shared__ unsigned long long s_cand[2 * kSelThreads];
+  __shared__ unsigned long long s_L;
+  __shared__ int s_ncand;
+  const int E = a.E, k = a.k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = blockIdx.x;
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (tid == 0) s_ncand = 0;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  unsigned long long key[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int e = tid + r * kSelThreads;
+    key[r] = e < E ? (((unsigned long long)ord_key(__ldcg(a.rb.logits + (size_t)t * E + e)) << 32) |
+                      (uint32_t)~(uint32_t)e)
+                   : 0ull;
+  }
+  {  // the warp's two largest keys
+    unsigned long long best = key[0] > key[1] ? key[0] : key[1];
+    const unsigned long long other = key[0] > key[1] ? key[1] : key[0];
+    const uint32_t h1 = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(best >> 32));
+    const uint32_t l1 = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(best >> 32) == h1 ? (uint32_t)best : 0u);
+    const unsigned long long m1 = ((unsigned long long)h1 << 32) | l1;
+    if (best == m1) best = other;  // keys are unique: the holder drops its maximum
+    const uint32_t h2 = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(best >> 32));
+    const uint32_t l2 = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(best >> 32) == h2 ? (uint32_t)best : 0u);
+    if (lane == 0) { s_top2[warp][0] = m1; s_top2[warp][1] = ((unsigned long long)h2 << 32) | l2; }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long v = warp_sort_desc(lane < 2 * kSelWarps ? s_top2[lane >> 1][lane & 1] : 0ull);
+    const unsigned long long L = __shfl_sync(0xFFFFFFFFu, v, k - 1);
+    if (lane == 0) s_L = L;
+  }
+  __syncthreads();
+  const unsigned long long L = s_L;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const bool cand = key[r] != 0ull && key[r] >= L;
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, cand);
+    int base = 0;
+    if (lane == 0 && bal) base = atomicAdd(&s_ncand, __popc(bal));
+    base = __shfl_sync(0xFFFFFFFFu, base, 0);
+    if (cand) s_cand[base + __popc(bal & ((1u << lane) - 1u))] = key[r];
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  const int nc = s_ncand;
+  unsigned long long my_key = 0ull;
+  if (nc <= 32) {
+    my_key = warp_sort_desc(lane < nc ? s_cand[lane] : 0ull);  // lane j: the (j+1)-th largest
+  } else {
+    // flat or tied logits: rounds of the warp maximum; a lane holds candidates lane + 32 q
+    for (int j = 0; j < k; ++j) {
+      unsigned long long b = 0ull;
+      int bc = -1;
+      for (int c = lane; c < nc; c += 32)
+        if (s_cand[c] > b) { b = s_cand[c]; bc = c; }
+      const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(b >> 32));
+      const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(b >> 32) == mhi ? (uint32_t)b : 0u);
+      const unsigned long long m = ((unsigned long long)mhi << 32) | mlo;
+      if (bc >= 0 && b == m) s_cand[bc] = 0ull;  // keys are unique: one lane holds the maximum
+      __syncwarp();
+      if (lane == j) my_key = m;
+    }
+  }
+  const int my_e = (int)~(uint32_t)my_key;
+  const int e0 = __shfl_sync(0xFFFFFFFFu, my_e, 0);
+  float lj = ord_value((uint32_t)(my_key >> 32));
+  float l0 = __shfl_sync(0xFFFFFFFFu, lj, 0);
+  if (a.bias_select) {  // the bias steered the choice only: the weights use the unbiased logits
+    lj = lane < k ? __ldcg(a.approx + (size_t)t * E + my_e) : 0.f;
+    l0 = __ldcg(a.approx + (size_t)t * E + e0);
+  }
+  const float my_ex = lane < k ? expf(lj - l0) : 0.f;
+  float sum = my_ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  if (lane < k) {
+    const float w = my_ex / sum;
+    a.rb.topk_idx[t * k + lane] = my_e;
+    a.rb.topk_w[t * k + lane] = w;
+    if (a.out.topk_idx) a.out.topk_idx[t * k + lane] = my_e;
+    if (a.out.topk_w) a.out.topk_w[t * k + lane] = w;
+  }
+}
+
 
 // moe_route (T <= 8): the dispatch index of the router's choices (one CTA)
 __global__ void __launch_bounds__(kSelThreads) route_dispatch_kernel(RouterArgs a) {
@@ -633,7 +637,18 @@ cudaError_t launch_router_decode(const RouterArgs& a, cudaStream_t s) {
   const int rows_per_cta = kWarpsR / a.wpr;
   const int rows = a.E + (a.sgate_w ? 1 : 0);
   router_decode_kernel<<<(rows + rows_per_cta - 1) / rows_per_cta, kRouterThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.T);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, router_select_kernel, a);
 }
 
 cudaError_t launch_dispatch_ext(const RouterArgs& a, const int32_t* idx, const float* w, cudaStream_t s) {
