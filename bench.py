@@ -45,10 +45,10 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up launch at batch 8 on the
 # decode_nvfp4 workload, from one ncu capture of the current kernel; None while the kernel has
 # changed since the counters were taken.
-GATEUP_TRAFFIC_BYTES = None
+GATEUP_TRAFFIC_BYTES = 93324800  # 90.69 MB read + 2.63 MB written in the full-section capture of gate/up
 # kernels one decode layer call launches: router logits (exact, every SM), top-k selection (one CTA
-# per token), gate/up, down (with the combine fused)
-DECODE_KERNELS_PER_CALL = 4
+# per token), gate/up, down, combine
+DECODE_KERNELS_PER_CALL = 5
 
 
 def _peaks():
@@ -463,6 +463,21 @@ def run_prefill(args, local, peak_bf16, peak_kind, name="prefill_nvfp4", tokens=
     fp4_kind = f"derived: {peak_kind} bf16 burst {peak_bf16} TFLOP/s x 13.5/2.25 (nominal dense FP4/bf16)"
     wbytes = host.router_bytes() + np.mean(touched) * host.expert_bytes()
     zipf = f", Zipf router bias s={cfg.zipf_s}" if cfg.zipf_s else ""
+    # the GEMMs' own HBM roofline: at about T*k/E tokens per expert each weight byte feeds few FLOP, so
+    # the weight stream bounds them (weight bytes of the touched experts / the GEMM's event time)
+    gu_bytes = np.mean(touched) * sum(m.nbytes() // m.E for m in (host.gate, host.up))
+    dn_bytes = np.mean(touched) * (host.down.nbytes() // host.down.E)
+    if cfg.shared_fmt:
+        gu_bytes += host.shared_gate.nbytes() + host.shared_up.nbytes()
+        dn_bytes += host.shared_down.nbytes()
+    hbm = _peaks()[0]
+    gemm_hbm = {"gateup_GBps": round(gu_bytes / (dur[3] * 1e-6) / 1e9, 1),
+                "down_GBps": round(dn_bytes / (dur[5] * 1e-6) / 1e9, 1),
+                "gateup_frac_hbm": round(gu_bytes / (dur[3] * 1e-6) / 1e9 / hbm, 4),
+                "down_frac_hbm": round(dn_bytes / (dur[5] * 1e-6) / 1e9 / hbm, 4),
+                "weight_bytes_gateup": int(gu_bytes), "weight_bytes_down": int(dn_bytes),
+                "flop_per_weight_byte": round(flops / (gu_bytes + dn_bytes), 1),
+                "hbm_bound_tflops": round(flops / (gu_bytes + dn_bytes) * hbm / 1e3, 1)}
     shared = f" + {FMT_TEXT[cfg.shared_fmt]} shared expert I={cfg.shared_I}" if cfg.shared_fmt else ""
     if cfg.shared_fmt:
         flops += T * 6.0 * cfg.H * cfg.shared_I
@@ -478,7 +493,7 @@ def run_prefill(args, local, peak_bf16, peak_kind, name="prefill_nvfp4", tokens=
                  "flops_per_layer": flops, "achieved_tflops": round(tflops, 1),
                  "frac_f16_peak": round(tflops / peak_bf16, 4), "f16_peak_tflops": peak_bf16,
                  "frac_fp4_peak": round(tflops / fp4_peak, 4), "fp4_peak_tflops": round(fp4_peak, 1),
-                 "peak_kind": peak_kind, "fp4_peak_kind": fp4_kind},
+                 "peak_kind": peak_kind, "fp4_peak_kind": fp4_kind, "hbm": gemm_hbm},
         "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
         "graph": f"CUDA graph of {G} layer calls; median of {reps} replays",
     }
@@ -496,7 +511,11 @@ def run_prefill(args, local, peak_bf16, peak_kind, name="prefill_nvfp4", tokens=
                 ["router_logits", "router_topk", "dispatch_quantise", "gateup_gemm", "-", "down_gemm",
                  "combine"], dur4) if k != "-"},
             "achieved_tflops": round(tflops4, 1), "frac_fp4_peak": round(tflops4 / fp4_peak, 4),
-            "fp4_peak_tflops": round(fp4_peak, 1), "peak_kind": fp4_kind}
+            "fp4_peak_tflops": round(fp4_peak, 1), "peak_kind": fp4_kind,
+            "hbm": {"gateup_GBps": round(gu_bytes / (dur4[3] * 1e-6) / 1e9, 1),
+                    "down_GBps": round(dn_bytes / (dur4[5] * 1e-6) / 1e9, 1),
+                    "gateup_frac_hbm": round(gu_bytes / (dur4[3] * 1e-6) / 1e9 / hbm, 4),
+                    "down_frac_hbm": round(dn_bytes / (dur4[5] * 1e-6) / 1e9 / hbm, 4)}}
     return out
 
 

@@ -29,7 +29,7 @@ bool shape_ok(int fmt, int N, int K) {
 
 struct Layout {
   size_t ctrl, logits, topk_idx, topk_w, cnt, off, pair, act, h, hs, P, S, approx, sgate, gu_part, gu_cnt,
-      dn_part, dn_cnt, y_cnt;
+      dn_part, dn_cnt;
   // prefill path
   size_t xg, xsig, xnorm, wnorm, hist, pos_of, tiles, h16, hsig, xq, xsf, xqg, xsfg, hq, hsf, rw_hi, rw_lo;
   size_t xs16, hs16, hssig;  // the shared expert's operands in prefill
@@ -68,7 +68,6 @@ Layout make_layout(const moe_layer* L, int maxT) {
   o.gu_cnt = take(gu_tiles * 4);
   o.dn_part = take((size_t)kMaxSplitBlocks * 32 * 4 * 4);
   o.dn_cnt = take(dn_tiles * 4);
-  o.y_cnt = take(H / 16 * 4);  // reset by the warp that completes each slab, like the split counters
   const size_t nchunk = (T + kPfChunk - 1) / kPfChunk;
   o.max_tiles = (int)(T * k / kPfTokTile + E + 1);
   o.xg = take(T * k * H * 2);
@@ -338,7 +337,6 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   ea.gu_cnt = reinterpret_cast<uint32_t*>(b + lo.gu_cnt);
   ea.dn_part = reinterpret_cast<float*>(b + lo.dn_part);
   ea.dn_cnt = reinterpret_cast<uint32_t*>(b + lo.dn_cnt);
-  ea.y_cnt = reinterpret_cast<uint32_t*>(b + lo.y_cnt);
   ea.y = static_cast<uint16_t*>(y);
   ea.shared_g = ra.sgate_w ? ra.sgate : nullptr;
   ea.p_bf16 = (opts && opts->bf16_partials) ? 1 : 0;
@@ -366,8 +364,9 @@ int32_t decode_forward_impl(const moe_layer* L, const void* x, int32_t T, void* 
   err = launch_expert(L->fmt, L->shared_fmt, false, ea, smem_gu, stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   mark(2);
-  // the down kernel also forms y: the warp finishing the last piece of a 16-row slab combines it
   err = launch_expert(L->fmt, L->shared_fmt, true, ea, smem_dn, stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  err = launch_combine_decode(ea, stream);
   mark(3);
   return cuda_status(err);
 }

@@ -123,4 +123,19 @@ cudaError_t launch_quantize_act_nvfp4(const uint16_t* x, int rows, int K, uint8_
   return cudaGetLastError();
 }
 
+cudaError_t launch_combine_decode(const ExpertArgs& a, cudaStream_t s) {
+  const int n = a.T * (a.H / 4);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n + 255) / 256);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return a.sfmt ? cudaLaunchKernelEx(&cfg, dec::combine_kernel<1>, a) : cudaLaunchKernelEx(&cfg, dec::combine_kernel<0>, a);
+}
+
 }  // namespace qmoe

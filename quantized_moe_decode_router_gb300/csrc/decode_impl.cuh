@@ -995,59 +995,6 @@ __device__ __forceinline__ void store_partial(const ExpertArgs& a, bool shared_i
   }
 }
 
-// The combine, fused into the down kernel: every (segment, 16-row slab of H)
-// piece of the down projection, once its rows of P (or S) are stored, counts
-// itself in y_cnt[slab]; the warp that brings the count to n_seg forms the
-// slab's rows of y for every token, y[t] = bf16( sum_j w[t, j] * P[t*k + j]
-// (+ g_t S[t]) ), j ascending with the shared term last (g_t the shared
-// expert's sigmoid gate when the layer has one, else 1), and sets the count
-// back to zero for the next call (as the split counters do).  Called by a
-// whole warp.
-__device__ __forceinline__ float4 load_partial4(const float* base, size_t row, int H, int c4, int bf16) {
-  if (!bf16) return __ldcg(reinterpret_cast<const float4*>(base + row * H) + c4);
-  const uint2 v = __ldcg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + row * H) + c4);
-  return make_float4(bf16_bits_to_float(v.x & 0xFFFF), bf16_bits_to_float(v.x >> 16), bf16_bits_to_float(v.y & 0xFFFF),
-                     bf16_bits_to_float(v.y >> 16));
-}
-
-template <int FS>
-__device__ __forceinline__ void slab_done(const ExpertArgs& a, int slab, int n_seg) {
-  const int lane = threadIdx.x & 31;
-  __threadfence();  // this warp's partial rows, before the count
-  __syncwarp();
-  uint32_t prev = 0;
-  if (lane == 0) prev = atomicAdd(a.y_cnt + slab, 1u);
-  prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
-  if (prev + 1 != (uint32_t)n_seg) return;
-  __threadfence();  // every other piece's rows, after the count
-  if (lane == 0) a.y_cnt[slab] = 0u;  // the count starts from zero in the next call
-  const int H = a.H, k = a.k;
-  // lane = (token, 4 consecutive columns of the slab): T * 4 <= 32 items
-  if (lane < a.T * 4) {
-    const int t = lane >> 2, c4 = slab * 4 + (lane & 3);
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const float w = __ldcg(a.rb.topk_w + t * k + j);
-      const float4 p = load_partial4(a.P, (size_t)(t * k + j), H, c4, a.p_bf16);
-      y[0] = __fmaf_rn(w, p.x, y[0]);
-      y[1] = __fmaf_rn(w, p.y, y[1]);
-      y[2] = __fmaf_rn(w, p.z, y[2]);
-      y[3] = __fmaf_rn(w, p.w, y[3]);
-    }
-    if (FS) {
-      const float4 sv = load_partial4(a.S, (size_t)t, H, c4, a.p_bf16);
-      const float g = a.shared_g ? __ldcg(a.shared_g + t) : 1.f;
-      y[0] = __fmaf_rn(g, sv.x, y[0]);
-      y[1] = __fmaf_rn(g, sv.y, y[1]);
-      y[2] = __fmaf_rn(g, sv.z, y[2]);
-      y[3] = __fmaf_rn(g, sv.w, y[3]);
-    }
-    const uint32_t lo = (uint32_t)float_to_bf16_bits(y[0]) | ((uint32_t)float_to_bf16_bits(y[1]) << 16);
-    const uint32_t hi = (uint32_t)float_to_bf16_bits(y[2]) | ((uint32_t)float_to_bf16_bits(y[3]) << 16);
-    reinterpret_cast<uint2*>(a.y + (size_t)t * H)[c4] = make_uint2(lo, hi);
-  }
-}
-
 template <int FR, int FS>
 __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -1187,7 +1134,6 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
             const int out = s_col_out[i][col];
             if (out >= 0) store_partial(a, shared_item, out, row, acc[0][j] * exp2i(s_pexp[i][col]) * ts);
           }
-          slab_done<FS>(a, tile, n_seg);
         };
         if (shared_item) {
           if constexpr (FS != 0) warp_tiles<FS, 1, kStagesDN>(m, tile0 * 16, 16 * kWarps, ntile, K, bu, xrow, ring, epi);
@@ -1230,9 +1176,57 @@ __global__ void __launch_bounds__(kExpertThreads, 2) down_kernel(ExpertArgs a) {
         const int out = s_col_out[i][col];
         if (out >= 0) store_partial(a, shared_item, out, row, acc[0][j] * exp2i(s_pexp[i][col]) * ts);
       }
-      slab_done<FS>(a, tile, n_seg);
     }
   }
+}
+
+// y[t] = bf16( sum_j w[t, j] * P[t*k + j] (+ g_t S[t]) ), j ascending, after the
+// down kernel (programmatic dependent launch; waits for its completion).  g_t
+// is the shared expert's sigmoid gate when the layer has one, else 1.
+__device__ __forceinline__ float4 load_partial4(const float* base, size_t row, int H, int c4, int bf16) {
+  if (!bf16) return __ldcg(reinterpret_cast<const float4*>(base + row * H) + c4);
+  const uint2 v = __ldcg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + row * H) + c4);
+  return make_float4(bf16_bits_to_float(v.x & 0xFFFF), bf16_bits_to_float(v.x >> 16), bf16_bits_to_float(v.y & 0xFFFF),
+                     bf16_bits_to_float(v.y >> 16));
+}
+
+template <int FS>
+__global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int H = a.H, k = a.k;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // (token, 4 columns)
+  if (i >= a.T * (H / 4)) return;
+  const int t = i / (H / 4), c4 = i - t * (H / 4);
+  // all k partial rows are loaded before the j-ordered fma chain (k <= 16)
+  float wj[16];
+  float4 pj[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (j < k) {
+      wj[j] = __ldcg(a.rb.topk_w + t * k + j);
+      pj[j] = load_partial4(a.P, (size_t)(t * k + j), H, c4, a.p_bf16);
+    }
+  float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (j < k) {
+      y[0] = __fmaf_rn(wj[j], pj[j].x, y[0]);
+      y[1] = __fmaf_rn(wj[j], pj[j].y, y[1]);
+      y[2] = __fmaf_rn(wj[j], pj[j].z, y[2]);
+      y[3] = __fmaf_rn(wj[j], pj[j].w, y[3]);
+    }
+  if (FS) {
+    const float4 sv = load_partial4(a.S, (size_t)t, H, c4, a.p_bf16);
+    const float g = a.shared_g ? __ldcg(a.shared_g + t) : 1.f;
+    y[0] = __fmaf_rn(g, sv.x, y[0]);
+    y[1] = __fmaf_rn(g, sv.y, y[1]);
+    y[2] = __fmaf_rn(g, sv.z, y[2]);
+    y[3] = __fmaf_rn(g, sv.w, y[3]);
+  }
+  const uint32_t lo = (uint32_t)float_to_bf16_bits(y[0]) | ((uint32_t)float_to_bf16_bits(y[1]) << 16);
+  const uint32_t hi = (uint32_t)float_to_bf16_bits(y[2]) | ((uint32_t)float_to_bf16_bits(y[3]) << 16);
+  reinterpret_cast<uint2*>(a.y + (size_t)t * H)[c4] = make_uint2(lo, hi);
 }
 
 template <int FR, int FS>

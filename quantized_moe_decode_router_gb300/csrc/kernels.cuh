@@ -72,7 +72,6 @@ struct ExpertArgs {
   int dn_segs;        // expert segments the down kernel stages at once (1 .. kMaxDnSegs)
   const float* shared_g;  // [T] sigmoid gate of the shared expert per token, or nullptr (weight 1)
   int p_bf16;         // 1: P and S are stored as BF16 (the bf16-partials lever)
-  uint32_t* y_cnt;    // [H/16] (segment, 16-row slab) pieces of the down projection finished per slab
 };
 
 constexpr int kMaxDnSegs = 4;
@@ -198,6 +197,10 @@ cudaError_t launch_prefill_logits_tc(const PrefillArgs& a, cudaStream_t s);
 // densely over tokens 0 .. dense_T - 1 of one weight set (the shared expert).
 cudaError_t launch_prefill_gemm(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill_gemm_w4a4(bool down, const PrefillArgs& a, int grid, cudaStream_t s);
+
+// Decode combine y = bf16(sum_j w_j P_j (+ g S)), launched after the down
+// kernel as a programmatic dependent of it.
+cudaError_t launch_combine_decode(const ExpertArgs& a, cudaStream_t s);
 
 
 // moe_dequantize / moe_quantize_act_nvfp4
