@@ -21,8 +21,9 @@
 //
 // CTA roles (persistent grid, one CTA per SM):
 //   warps 0-7  decode the weight rows of each K step (cp.async ring of raw
-//              codes per thread, e2m1/e4m3 conversion to f16) into the
-//              stage's A tiles;
+//              codes per thread, conversion to f16) into the stage's A
+//              tiles, stored in the 128-byte swizzled K-major layout (the
+//              layout of the TMA-loaded B tiles; conflict-free both ways);
 //   warp 8     loads the stage's token rows (B tile) with one 2-D TMA box
 //              (128-byte swizzle) of the position-sorted operand rows
 //              (scaled activations for gate/up, h for down); the stage's
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         uint8_t* A = smem + stage * C::A_STAGE + m * C::A_BYTES;
 #pragma unroll
         for (int c = 0; c < C::KT / 8; ++c)
-          *reinterpret_cast<uint4*>(A + tc::chunk_off(rr, hh * (C::KT / 8) + c, KB)) = out[c];
+          *reinterpret_cast<uint4*>(A + tc::sw128_off(rr, hh * (C::KT / 8) + c)) = out[c];
         tc::fence_proxy_async();
         tc::bar_arrive(&full_a[stage]);
       }
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
           const uint64_t db = tc::smem_desc_sw128(bB + kk * 32);
 #pragma unroll
           for (int mm = 0; mm < C::NMAT; ++mm) {
-            const uint64_t da = tc::smem_desc(base + mm * C::A_BYTES + kk * 256, 128, 1024);
+            const uint64_t da = tc::smem_desc_sw128(base + mm * C::A_BYTES + kk * 32);
             tc::mma_f16(acc + mm * NT, da, db, idesc, accumulate || kk != 0);
           }
         }

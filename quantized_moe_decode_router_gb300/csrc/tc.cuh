@@ -18,9 +18,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// Byte offset of the 16-byte chunk c of row r in a tile with KB bytes per row.
-__host__ __device__ __forceinline__ uint32_t chunk_off(int r, int c, int KB) {
-  return (uint32_t)(((r >> 3) * (KB >> 4) + c) * 128 + (r & 7) * 16);
+// Byte offset of the 16-byte chunk c (c < 8) of row r in a K-major tile of
+// 128-byte rows with the 128-byte swizzle (the layout TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B): chunk c of row r sits at chunk c ^ (r mod 8).
+// Rows 8 apart fall on the same banks, so the tensor core reads an 8-row atom
+// without conflicts; a quarter warp storing one chunk of 8 consecutive rows
+// hits 8 distinct bank groups.
+__host__ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
 // Shared-memory matrix descriptor (no swizzle): start address, leading-
