@@ -420,8 +420,8 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x340 | (DOWN ? 1 : 0));
           return false;
         }
+        // the decode warps fenced their generic-proxy stores before arriving; TMA writes are async-proxy
         tc::fence_after_sync();
-        tc::fence_proxy_async();
         const uint32_t base = tc::smem_u32(smem + sa * C::A_STAGE);
         const uint32_t bB = tc::smem_u32(smem + C::B_OFF + sb * C::B_BYTES);
 #pragma unroll
