@@ -185,20 +185,28 @@ def silu(z: np.ndarray) -> np.ndarray:
         return z / (1.0 + np.exp(-z))
 
 
+def act_fake_quant(a: np.ndarray, act_quant: int) -> np.ndarray:
+    """The W4A4 lever's activation quantiser: act_quant 1 (or True) = NVFP4
+    16-element blocks, 2 = MXFP4 32-element blocks; 0 = none."""
+    if not act_quant:
+        return a
+    return mxfp4_fake_quant(a) if int(act_quant) == 2 else nvfp4_fake_quant(a)
+
+
 def swiglu_mlp(Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray, X: np.ndarray,
-               act_quant: bool = False) -> tuple:
+               act_quant: int = 0) -> tuple:
     """One SwiGLU expert on token rows X [n, H] (FP64 values).
 
     Returns (h, P): h = bf16(silu(X Wg^T) * (X Wu^T)) [n, I] as FP64 values,
     P = h Wd^T [n, H] in FP64.  With act_quant the token rows and h are
-    replaced by their NVFP4-quantised values before each projection.
+    replaced by their quantised values (NVFP4 for 1, MXFP4 for 2) before each
+    projection.
     """
-    if act_quant:
-        X = nvfp4_fake_quant(X)
+    X = act_fake_quant(X, act_quant)
     g = X @ Wg.T
     u = X @ Wu.T
     h = F.round_bf16(silu(g) * u)
-    hq = nvfp4_fake_quant(h) if act_quant else h
+    hq = act_fake_quant(h, act_quant)
     P = hq @ Wd.T
     return h, P
 
@@ -237,13 +245,44 @@ def nvfp4_fake_quant(a: np.ndarray) -> np.ndarray:
     return nvfp4_dequantize_act(*nvfp4_quantize_act(a))
 
 
+def mxfp4_quantize_act(a: np.ndarray):
+    """MXFP4 quantisation of activation rows in 32-element blocks (the MXFP4
+    checkpoint rule, reading Q3): the block exponent e is the smallest integer
+    with 6 * 2^e >= amax (amax = 0 -> e = 0), its E8M0 code e + 127 clamped to
+    [0, 254]; code = e2m1_rne_sat( a / 2^e ) (the division by a power of two is
+    exact).  Returns (codes [.., K] u8 0..15, scale codes [.., K/32] u8).
+    """
+    a = np.asarray(a, dtype=np.float64)
+    *lead, K = a.shape
+    blk = a.reshape(*lead, K // 32, 32)
+    amax = np.abs(blk).max(axis=-1)
+    # log2(amax / 6) lies in [p - 3.585, p - 2.585) for amax = f 2^p, f in [0.5, 1): e is p - 3 or p - 2
+    _, p = np.frexp(np.where(amax > 0, amax, 1.0))
+    e = np.where(6.0 * np.ldexp(1.0, p - 3) >= amax, p - 3, p - 2)
+    e = np.where(amax > 0, e, 0)
+    s_code = np.clip(e + 127, 0, 254)
+    s = np.ldexp(1.0, s_code - 127)
+    codes = F.e2m1_encode_rne(blk / s[..., None])
+    return codes.reshape(*lead, K).astype(np.uint8), s_code.astype(np.uint8)
+
+
+def mxfp4_dequantize_act(codes: np.ndarray, s_code: np.ndarray) -> np.ndarray:
+    *lead, K = codes.shape
+    v = F.E2M1_TABLE[codes].reshape(*lead, K // 32, 32) * np.ldexp(1.0, s_code.astype(np.int64) - 127)[..., None]
+    return v.reshape(*lead, K)
+
+
+def mxfp4_fake_quant(a: np.ndarray) -> np.ndarray:
+    return mxfp4_dequantize_act(*mxfp4_quantize_act(a))
+
+
 # ------------------------------------------------------------------ layer ----
 
 def _decoded(qm, e):
     return F.decode_qmat(qm, e)
 
 
-def layer_forward(layer, x_bits: np.ndarray, act_quant: bool = False, tokens=None, expert_cache=None,
+def layer_forward(layer, x_bits: np.ndarray, act_quant: int = 0, tokens=None, expert_cache=None,
                   bias_select: bool = False, bf16_partials: bool = False, routing=None):
     """Full MoE layer on host-resident checkpoint data (a synth.HostLayer).
 
@@ -261,6 +300,8 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: bool = False, tokens=Non
     expert enters with weight 1.
     routing: optional (idx [T, k] i32, w [T, k] f32) chosen by the caller; the
     router is then skipped and these pairs and weights are used as given.
+    act_quant: the W4A4 lever's activation quantisation (1 or True: NVFP4, 2:
+    MXFP4), applied to the token rows and to h before each projection.
     Returns a dict of every intermediate the CUDA path exposes.
     """
     cfg = layer.cfg

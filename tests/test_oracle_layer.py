@@ -225,6 +225,64 @@ def test_nvfp4_act_quantizer_pins():
                 assert abs(D[r, b * 16 + i]) / sv == F.E2M1_GRID[pick]
 
 
+def test_mxfp4_act_quantizer_pins():
+    # on-grid block: values e2m1 * 2^e with amax = 6 * 2^e -> exact round trip, scale code e + 127
+    codes = np.array([7, 1, 2, 3, 4, 5, 6, 0, 9, 10, 11, 12, 13, 14, 15, 8] * 2)
+    for e in (-9, -1, 0, 3):
+        a = F.E2M1_TABLE[codes] * 2.0 ** e
+        q, sc = M.mxfp4_quantize_act(a[None, :])
+        assert sc[0, 0] == e + 127
+        assert np.array_equal(M.mxfp4_dequantize_act(q, sc)[0], a)
+    # zero block -> scale code 127 (2^0), zero codes
+    q0, s0 = M.mxfp4_quantize_act(np.zeros((1, 32)))
+    assert s0[0, 0] == 127 and np.all(q0 == 0)
+    # brute force: e is the smallest integer with 6 * 2^e >= amax (boundaries included), each value the
+    # nearest E2M1 multiple of 2^e (ties to the even code)
+    rng = np.random.default_rng(21)
+    A = F.round_bf16(rng.standard_normal((48, 64)) * np.exp(rng.uniform(-12, 12, (48, 1))))
+    A[0, :32] = F.round_bf16(np.linspace(-6.0, 6.0, 32) * 2.0 ** -4)     # amax exactly 6 * 2^-4
+    A[1, :32] = A[0, :32] * (1 + 2.0 ** -7)                               # just above: the next exponent
+    q, sc = M.mxfp4_quantize_act(A)
+    D = M.mxfp4_dequantize_act(q, sc)
+    for r in range(48):
+        for b in range(2):
+            blk = A[r, b * 32:(b + 1) * 32]
+            amax = np.abs(blk).max()
+            e = next(e for e in range(-140, 140) if 6.0 * 2.0 ** e >= amax) if amax > 0 else 0
+            assert sc[r, b] == e + 127
+            for i in range(32):
+                y = blk[i] / 2.0 ** e
+                cand = np.abs(min(abs(y), 6.0) - F.E2M1_GRID)
+                nearest = np.flatnonzero(cand == cand.min())
+                pick = nearest[0] if len(nearest) == 1 else nearest[nearest % 2 == 0][0]
+                assert abs(D[r, b * 32 + i]) / 2.0 ** e == F.E2M1_GRID[pick]
+    assert sc[0, 0] == 123 and sc[1, 0] == 124
+    # the synthetic checkpoints' MXFP4 encoder (plain C, the same rule for weights) agrees on every
+    # code and scale of the same rows
+    data, scales, _ = synth.quantize(FMT_MXFP4, A.astype(np.float32))
+    codes_c = F.unpack_nibbles(data)
+    assert np.array_equal(scales, sc)
+    assert np.array_equal(codes_c & 7, q & 7)                               # magnitudes
+    nz = (codes_c & 7) != 0
+    assert np.array_equal((codes_c & 8)[nz], (q & 8)[nz])                  # signs of the non-zero codes
+
+
+def _torch_mxfp4_fake_quant(A: torch.Tensor) -> torch.Tensor:
+    """MXFP4 quantise-dequantise of BF16-valued rows in 32-element blocks, written independently of
+    the oracle: the exponent as ceil(log2(amax / 6)) in float64 (exact at the powers of two), the
+    E2M1 code by round-half-even on the binade's quantum, saturating at 6."""
+    n, K = A.shape
+    B = A.reshape(n, K // 32, 32).to(torch.float64)
+    amax = B.abs().amax(dim=-1)
+    e = torch.where(amax > 0, torch.ceil(torch.log2(amax / 6.0)), torch.zeros_like(amax))
+    s = torch.pow(2.0, e)
+    y = B / s[..., None]
+    ay = y.abs()
+    quantum = torch.where(ay < 2, 0.5, torch.where(ay < 4, 1.0, 2.0))
+    v = torch.clamp(torch.round(ay / quantum) * quantum, max=6.0) * torch.sign(y)
+    return (v * s[..., None]).reshape(n, K)
+
+
 def _torch_nvfp4_fake_quant(A: torch.Tensor) -> torch.Tensor:
     """NVFP4 quantise-dequantise of BF16-valued rows in 16-element blocks, written independently of
     the oracle: the block scale through torch's float8_e4m3fn cast of the FP32 quotient amax / 6, the
@@ -243,30 +301,45 @@ def _torch_nvfp4_fake_quant(A: torch.Tensor) -> torch.Tensor:
     return (v * s[..., None].to(torch.float64)).reshape(n, K)
 
 
-def _torch_w4a4_mlp(Wg, Wu, Wd, X):
+def _torch_w4a4_mlp(Wg, Wu, Wd, X, quant=None):
     """The W4A4 lever's order: x quantised, gate and up, h = bf16(silu(g) * u), h quantised, down."""
-    Xq = _torch_nvfp4_fake_quant(X)
+    quant = quant or _torch_nvfp4_fake_quant
+    Xq = quant(X)
     g = Xq @ Wg.T
     u = Xq @ Wu.T
     h = torch.from_numpy(F.round_bf16((torch.nn.functional.silu(g) * u).numpy()))
-    return _torch_nvfp4_fake_quant(h) @ Wd.T
+    return quant(h) @ Wd.T
 
 
-@pytest.mark.parametrize("fmt,H,I", [(FMT_NVFP4, 256, 128), (FMT_MXFP4, 256, 128)])
-def test_w4a4_single_expert_equals_quantised_swiglu_mlp(fmt, H, I):
+@pytest.mark.parametrize("fmt,H,I,aq", [(FMT_NVFP4, 256, 128, 1), (FMT_MXFP4, 256, 128, 1),
+                                        (FMT_MXFP4, 256, 128, 2)])
+def test_w4a4_single_expert_equals_quantised_swiglu_mlp(fmt, H, I, aq):
     # one expert, top-1, weight 1: the W4A4 mode is the SwiGLU MLP with x and h replaced by their
-    # NVFP4 quantise-dequantise (activations, page 5 weekly update: W4A4 prefill is opt-in)
+    # NVFP4 (aq 1) or MXFP4 (aq 2) quantise-dequantise (activations, page 5 weekly update: W4A4
+    # prefill is opt-in)
     cfg = _small(fmt, H=H, I=I)
     lay = synth.make_layer(cfg, seed=8)
     x = synth.make_tokens(cfg, 24, seed=8)
-    out = M.layer_forward(lay, x, act_quant=True)
+    out = M.layer_forward(lay, x, act_quant=aq)
     X = torch.from_numpy(F.bf16_to_f64(x))
-    y_ref = _torch_w4a4_mlp(_torch_decode(lay.gate), _torch_decode(lay.up), _torch_decode(lay.down), X).numpy()
+    y_ref = _torch_w4a4_mlp(_torch_decode(lay.gate), _torch_decode(lay.up), _torch_decode(lay.down), X,
+                            _torch_mxfp4_fake_quant if aq == 2 else None).numpy()
     ok = M.within_tolerance(F.bf16_to_f64(out["y_bits"]), y_ref, ulps=1.0, abs_tol=1e-6)
     assert ok.all(), np.abs(F.bf16_to_f64(out["y_bits"]) - y_ref).max()
     # and the lever changes the result: the exact chain differs from it
     exact = M.layer_forward(lay, x)
     assert not np.array_equal(exact["y_bits"], out["y_bits"])
+
+
+def test_mxfp4_fake_quant_matches_torch_on_hard_blocks():
+    rng = np.random.default_rng(13)
+    A = F.round_bf16(rng.standard_normal((40, 64)) * np.exp(rng.uniform(-30, 30, (40, 1))))
+    A[0, :32] = 0.0
+    A[1, :32] = np.array([6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0] * 4) * np.array([1, -1] * 16)  # 2^0, ties
+    A[2, :32] = np.array([4.0, 5.0, 6.0, -6.0] * 8) * 8.0                   # 2^3: ties at 5 * 8
+    got = M.mxfp4_fake_quant(A)
+    ref = _torch_mxfp4_fake_quant(torch.from_numpy(A)).numpy()
+    assert np.array_equal(got, ref)
 
 
 def test_w4a4_fake_quant_matches_torch_on_hard_blocks():
@@ -355,8 +428,22 @@ def _route_bias_always_weighs(x_bits, Wr, bias, k, bias_select=False):
     return _ORIG["route"](x_bits, Wr, bias, k, False)
 
 
+def _mxfp4_exponent_low(a):
+    """floor(log2(amax / 6)) instead of the ceiling: values above 6 * 2^e saturate."""
+    a = np.asarray(a, dtype=np.float64)
+    *lead, K = a.shape
+    blk = a.reshape(*lead, K // 32, 32)
+    amax = np.abs(blk).max(axis=-1)
+    _, p = np.frexp(np.where(amax > 0, amax, 1.0))
+    e = np.where(amax > 0, p - 3, 0)
+    s_code = np.clip(e + 127, 0, 254)
+    codes = F.e2m1_encode_rne(blk / np.ldexp(1.0, s_code - 127)[..., None])
+    return codes.reshape(*lead, K).astype(np.uint8), s_code.astype(np.uint8)
+
+
 _ORIG = {"dispatch": M.dispatch, "decode": F.decode, "swiglu": M.swiglu_mlp, "router_logits": M.router_logits,
-         "route": M.route, "shared_gate": M.shared_gate, "layer_forward": M.layer_forward}
+         "route": M.route, "shared_gate": M.shared_gate, "layer_forward": M.layer_forward,
+         "act_fake_quant": M.act_fake_quant}
 
 
 def test_planted_mistakes_are_caught(monkeypatch):
@@ -365,7 +452,8 @@ def test_planted_mistakes_are_caught(monkeypatch):
     import tests.test_oracle_router as TR
 
     single = (test_single_expert_equals_plain_swiglu_mlp, FMT_NVFP4, 128, 64)
-    w4a4 = (test_w4a4_single_expert_equals_quantised_swiglu_mlp, FMT_NVFP4, 256, 128)
+    w4a4 = (test_w4a4_single_expert_equals_quantised_swiglu_mlp, FMT_NVFP4, 256, 128, 1)
+    w4a4_mx = (test_w4a4_single_expert_equals_quantised_swiglu_mlp, FMT_MXFP4, 256, 128, 2)
     mistakes = {
         "nibble order": (F, "unpack_nibbles", _swapped_nibbles, [(TF.test_nvfp4_layout_hand_built,), single]),
         "silu sign": (M, "silu", lambda z: z / (1.0 + np.exp(z)), [single]),
@@ -379,6 +467,10 @@ def test_planted_mistakes_are_caught(monkeypatch):
         "W4A4: h quantised before its BF16 rounding": (M, "swiglu_mlp", _w4a4_h_unrounded, [w4a4]),
         "W4A4: x not quantised": (M, "swiglu_mlp", _w4a4_x_unquantised, [w4a4]),
         "W4A4: h not re-quantised": (M, "swiglu_mlp", _w4a4_h_unquantised, [w4a4]),
+        "MXFP4 activations: exponent one too small": (M, "mxfp4_quantize_act", _mxfp4_exponent_low,
+                                                      [(test_mxfp4_act_quantizer_pins,)]),
+        "MXFP4 W4A4 quantised as NVFP4": (M, "act_fake_quant", lambda a, aq: _ORIG["act_fake_quant"](
+            a, 1 if aq else 0), [w4a4_mx]),
         "mask window 2^-4": (M, "near_midpoint", lambda d, l: M.midpoint_distance(d, l) <= 2.0 ** -4 * np.abs(d),
                              [(TR.test_near_midpoint_mask_flags_only_the_window, 1.0),
                               (TR.test_near_midpoint_mask_empty_at_the_decode_seeds,)]),
