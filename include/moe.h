@@ -128,7 +128,9 @@ typedef struct {
   /* 0 (default): BF16 activations, the exact chain.  1: the NVFP4 W4A4
    * lever (prefill only, NVFP4 routed experts): activations and SwiGLU
    * outputs re-quantised to NVFP4 16-element blocks before the projections
-   * (DGPP forum, page 5 weekly update: W4A4 prefill is opt-in). */
+   * (DGPP forum, page 5 weekly update: W4A4 prefill is opt-in).  2: the same
+   * lever for MXFP4 routed experts, with MXFP4 activations (32-element
+   * blocks, E8M0 scales; the rule of moe_quantize_act_mxfp4). */
   int32_t act_quant;
   /* 0 (default): FP32 per-expert partials.  1: the down projection's
    * partials are rounded to BF16 before the weighted sum (DGPP README
@@ -231,18 +233,20 @@ int32_t moe_experts_forward(const moe_layer* layer, const void* x /* device bf16
  * moe_decode_forward; expert projections run as grouped GEMMs over a compact
  * tile list of the routed segments (DGPP README "Execution and performance":
  * engine.expert_tile_list, engine.expert_gemm_pair), with FP32 partials and
- * a combine pass.  Supported: NVFP4, MXFP4 or int4 g64 routed experts
- * without a shared expert, hidden and inter multiples of 128; anything else
- * (a shared expert, int8 / FP8 / int4 g128 routed experts) returns
- * MOE_ERR_UNSUPPORTED before any launch.  MXFP4 and int4 g64 weights are
- * folded into f16 relative to their row's largest block scale: exact while a
- * row's block scales span at most 2^23 (MXFP4) / 2^24 (int4); blocks further
- * below are rounded to f16's subnormal grid or dropped (weights under 2^-21
- * times the row's largest block scale).  opts->act_quant = 1 selects the
- * NVFP4 W4A4 lever (DGPP forum, page 5 weekly update: NVFP4 W4A4 prefill is
- * opt-in; NVFP4 routed experts only): x and h are quantised to NVFP4
- * 16-element blocks (the rule of moe_quantize_act_nvfp4) and the
- * projections run as block-scaled FP4 GEMMs; it needs hidden and inter
+ * a combine pass.  Supported: every routed and shared format, hidden, inter
+ * and shared inter multiples of 128 (other shapes return MOE_ERR_UNSUPPORTED
+ * before any launch); a shared expert runs as a dense GEMM over all T tokens.
+ * MXFP4 and int4 g64 weights are folded into f16 relative to their row's
+ * largest block scale: exact while a row's block scales span at most 2^23
+ * (MXFP4) / 2^24 (int4); blocks further below are rounded to f16's subnormal
+ * grid or dropped (weights under 2^-21 times the row's largest block scale).
+ * int8 g64, FP8 b128 and int4 g128 weights enter the MMA unscaled and each
+ * scale group is applied in FP32.  opts->act_quant selects the W4A4 lever
+ * (DGPP forum, page 5 weekly update: W4A4 prefill is opt-in): 1 for NVFP4
+ * routed experts (x and h quantised to NVFP4 16-element blocks, the rule of
+ * moe_quantize_act_nvfp4), 2 for MXFP4 routed experts (MXFP4 32-element
+ * blocks, the rule of moe_quantize_act_mxfp4); the projections then run as
+ * block-scaled FP4 GEMMs.  It needs no shared expert, hidden and inter
  * multiples of 256 and 16-byte aligned scale arrays.  Routing outputs are left in the workspace; in its logits
  * array only the experts the router recomputed exactly (every selected one
  * among them) hold their FP32 logit, the others hold -inf.
@@ -357,10 +361,11 @@ typedef struct {
   size_t expert_off;  /* i32 [E + 1] */
   size_t pair_list;   /* i32 [T * k] */
   size_t total;       /* workspace bytes for this max_tokens */
-  /* moe_prefill_forward with act_quant = 1: the NVFP4 codes and E4M3 block scales of each
-   * pair's SwiGLU output h, by sorted position (position pos holds pair pair_list[pos]) */
+  /* moe_prefill_forward with act_quant = 1 (2): the NVFP4 (MXFP4) codes and E4M3 (E8M0) block
+   * scales of each pair's SwiGLU output h, by sorted position (position pos holds pair
+   * pair_list[pos]) */
   size_t h_codes;     /* u8 [T * k, I / 2], low nibble = even column */
-  size_t h_scales;    /* u8 [T * k, I / 16] */
+  size_t h_scales;    /* u8 [T * k, I / 16] (act_quant 1) or [T * k, I / 32] (act_quant 2) */
 } moe_ws_layout;
 
 int32_t moe_workspace_layout(const moe_layer* layer, int32_t max_tokens, const moe_options* opts,
@@ -384,6 +389,19 @@ int32_t moe_dequantize(int32_t fmt, const moe_qweight* w, int32_t N, int32_t K, 
  *   scales: device u8 [rows, K/16] (E4M3).  K a multiple of 16.
  */
 int32_t moe_quantize_act_nvfp4(const void* x, int32_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
+                               moe_stream_t stream);
+
+/*
+ * MXFP4 activation quantizer of the W4A4 lever (act_quant = 2), per
+ * 32-element block of each row: the block exponent e is the smallest integer
+ * with 6 * 2^e >= amax (e = 0 for an all-zero block), its E8M0 scale code
+ * e + 127 clamped to [0, 254]; code = e2m1_rne_sat( a / 2^e ) (the rule of
+ * the MXFP4 checkpoints' scales, DGPP forum post 1 quantisation table and the
+ * MXFP4 config's scale = 2^ceil(log2(amax / 6))).
+ *   x: device bf16 [rows, K]; codes: device u8 [rows, K/2] (low nibble = even k);
+ *   scales: device u8 [rows, K/32] (E8M0).  K a multiple of 32.
+ */
+int32_t moe_quantize_act_mxfp4(const void* x, int32_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
                                moe_stream_t stream);
 
 #ifdef __cplusplus

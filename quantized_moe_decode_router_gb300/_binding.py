@@ -96,6 +96,8 @@ _SIGNATURES = {
                                         ctypes.c_void_p]),
     "moe_quantize_act_nvfp4": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                                                 ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_quantize_act_mxfp4": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                                ctypes.c_void_p, ctypes.c_void_p]),
 }
 
 _lib = None
@@ -294,3 +296,8 @@ def moe_dequantize(fmt: int, w: QWeight, N: int, K: int, expert: int, row0: int,
 def moe_quantize_act_nvfp4(x, rows: int, K: int, codes, scales, stream=None) -> int:
     return _check(load().moe_quantize_act_nvfp4(_ptr(x), rows, K, _ptr(codes), _ptr(scales),
                                                 _stream_handle(stream)), "moe_quantize_act_nvfp4")
+
+
+def moe_quantize_act_mxfp4(x, rows: int, K: int, codes, scales, stream=None) -> int:
+    return _check(load().moe_quantize_act_mxfp4(_ptr(x), rows, K, _ptr(codes), _ptr(scales),
+                                                _stream_handle(stream)), "moe_quantize_act_mxfp4")

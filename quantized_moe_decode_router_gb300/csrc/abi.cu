@@ -136,7 +136,7 @@ int32_t check_layer(const moe_layer* L) {
 
 int32_t check_options(const moe_options* o) {
   if (!o) return MOE_OK;
-  if (o->act_quant != 0 && o->act_quant != 1) return MOE_ERR_INVALID_ARG;
+  if (o->act_quant < 0 || o->act_quant > 2) return MOE_ERR_INVALID_ARG;
   if (o->bf16_partials != 0 && o->bf16_partials != 1) return MOE_ERR_INVALID_ARG;
   if (o->wait_limit_us < 0) return MOE_ERR_INVALID_ARG;
   for (int i = 0; i < 5; ++i)
@@ -436,11 +436,12 @@ int sm_count(int* sms) {
 // and shared format with hidden, inter and shared inter multiples of 128; the
 // W4A4 lever for NVFP4 routed experts without a shared expert, with whole
 // 256-column stages and 16-byte aligned scale rows.
-bool prefill_supported(const moe_layer* L, bool act_quant) {
+bool prefill_supported(const moe_layer* L, int act_quant) {
   if (L->hidden % 128 != 0 || L->inter % 128 != 0) return false;
   if (L->shared_fmt != MOE_FMT_NONE && L->shared_inter % 128 != 0) return false;
   if (!act_quant) return true;
-  if (L->fmt != MOE_FMT_NVFP4 || L->shared_fmt != MOE_FMT_NONE) return false;
+  // the W4A4 lever: NVFP4 activations on NVFP4 weights, MXFP4 activations on MXFP4 weights
+  if (L->fmt != (act_quant == 2 ? MOE_FMT_MXFP4 : MOE_FMT_NVFP4) || L->shared_fmt != MOE_FMT_NONE) return false;
   const auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   return L->hidden % 256 == 0 && L->inter % 256 == 0 && a16(L->gate.scales) && a16(L->up.scales) &&
          a16(L->down.scales);
@@ -638,13 +639,13 @@ static int32_t prefill_forward_checked(const moe_layer* layer, const void* x, in
   if (!aligned16(x) || !aligned16(y)) return MOE_ERR_MISALIGNED;
   if (T < 1) return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(layer, T, ws, ws_bytes)) != MOE_OK) return st;
-  const bool aq = opts && opts->act_quant;
+  const int aq = opts ? opts->act_quant : 0;
   if (!prefill_supported(layer, aq)) return MOE_ERR_UNSUPPORTED;
   int sms = 0;
   if ((st = sm_count(&sms)) != MOE_OK) return st;
   const Layout lo = make_layout(layer, ws_max_tokens(layer, ws_bytes));
   PrefillArgs pa = prefill_args(layer, lo, ws, x, T, y);
-  pa.act_quant = aq ? 1 : 0;
+  pa.act_quant = aq;
   pa.wait_ns = wait_limit_ns(opts);
   pa.p_bf16 = (opts && opts->bf16_partials) ? 1 : 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -708,6 +709,14 @@ int32_t moe_quantize_act_nvfp4(const void* x, int32_t rows, int32_t K, uint8_t* 
   if (!x || !codes || !scales || rows < 1 || K < 16 || K % 16) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || (reinterpret_cast<uintptr_t>(codes) & 7)) return MOE_ERR_MISALIGNED;
   return cuda_status(launch_quantize_act_nvfp4(static_cast<const uint16_t*>(x), rows, K, codes, scales,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_quantize_act_mxfp4(const void* x, int32_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
+                               moe_stream_t stream) {
+  if (!x || !codes || !scales || rows < 1 || K < 32 || K % 32) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes)) return MOE_ERR_MISALIGNED;
+  return cuda_status(launch_quantize_act_mxfp4(static_cast<const uint16_t*>(x), rows, K, codes, scales,
                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 

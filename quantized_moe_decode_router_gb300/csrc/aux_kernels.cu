@@ -103,7 +103,48 @@ __global__ void quantize_act_nvfp4_kernel(const uint16_t* x, int rows, int K, ui
   scales[(size_t)r * nb + b] = (uint8_t)sc;
 }
 
+// MXFP4 activations, one thread per 32-element block: e = the smallest integer with 6 * 2^e >= amax
+// (from amax = f 2^p, f in [0.5, 1): e is p - 3 or p - 2, decided by one exact comparison), scale
+// code e + 127 clamped to [0, 254], codes e2m1_rne_sat(a * 2^-e) (exact scaling by a power of two).
+__global__ void quantize_act_mxfp4_kernel(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales) {
+  const int nb = K / 32;
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= (long long)rows * nb) return;
+  const int r = (int)(gid / nb), b = (int)(gid - (long long)r * nb);
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)r * K + b * 32);
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = src[i];
+    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[j] & 0xFFFF)), fabsf(bf16_bits_to_float(w[j] >> 16))));
+  const int sc = mxfp4_act_scale_code(amax);
+  const float inv = exp2i(127 - sc);  // 2^-e
+  uint32_t out[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t byte = f32x2_to_e2m1x2_sat(bf16_bits_to_float(w[j] & 0xFFFF) * inv,
+                                              bf16_bits_to_float(w[j] >> 16) * inv);
+    out[j >> 2] |= byte << (8 * (j & 3));
+  }
+  *reinterpret_cast<uint4*>(codes + (size_t)r * (K / 2) + b * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+  scales[(size_t)r * nb + b] = (uint8_t)sc;
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_act_mxfp4(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales,
+                                      cudaStream_t s) {
+  const long long n = (long long)rows * (K / 32);
+  const int threads = 256;
+  const long long blocks = (n + threads - 1) / threads;
+  quantize_act_mxfp4_kernel<<<(unsigned)blocks, threads, 0, s>>>(x, rows, K, codes, scales);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dequantize(int fmt, QW w, int N, int K, int expert, int row0, int nrows, float* out,
                               cudaStream_t s) {

@@ -120,6 +120,18 @@ __device__ __forceinline__ void bar_arrive_n(uint32_t id, uint32_t n) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// E8M0 scale code of an MXFP4 activation block with largest magnitude amax:
+// e = the smallest integer with 6 * 2^e >= amax (0 for amax = 0), code e + 127
+// clamped to [0, 254].  amax = f 2^p with f in [0.5, 1) puts log2(amax / 6) in
+// [p - 3.585, p - 2.585), so e is p - 3 or p - 2; the comparison is exact.
+__device__ __forceinline__ int mxfp4_act_scale_code(float amax) {
+  if (!(amax > 0.f)) return 127;
+  int p;
+  frexpf(amax, &p);
+  const int e = (6.0f * ldexpf(1.0f, p - 3) >= amax) ? p - 3 : p - 2;
+  return min(max(e + 127, 0), 254);
+}
+
 // 2^e as a float for e in [-126, 127].
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 

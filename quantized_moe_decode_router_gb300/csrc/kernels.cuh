@@ -208,6 +208,8 @@ cudaError_t launch_dequantize(int fmt, QW w, int N, int K, int expert, int row0,
                               cudaStream_t s);
 cudaError_t launch_quantize_act_nvfp4(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales,
                                       cudaStream_t s);
+cudaError_t launch_quantize_act_mxfp4(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales,
+                                      cudaStream_t s);
 
 // Bytes of one matrix's codes / scales in a format.
 __host__ __device__ inline size_t data_bytes(int fmt, int N, int K) {

@@ -277,8 +277,9 @@ __global__ void __launch_bounds__(kThreads) pf_gather_kernel(PrefillArgs a) {
   }
 }
 
-// W4A4: one warp per sorted position copies the NVFP4 codes and block scales
-// of its token (16-byte chunks).
+// W4A4: one warp per sorted position copies the FP4 codes and block scales of
+// its token (16-byte chunks for the codes, 8-byte chunks for the scales:
+// H / 16 of them for NVFP4, H / 32 for MXFP4).
 __global__ void __launch_bounds__(kThreads) pf_gather_q_kernel(PrefillArgs a) {
   const int lane = threadIdx.x & 31;
   const int pos = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
@@ -288,9 +289,10 @@ __global__ void __launch_bounds__(kThreads) pf_gather_q_kernel(PrefillArgs a) {
   const uint4* cs = reinterpret_cast<const uint4*>(a.xq + (size_t)t * (H / 2));
   uint4* cd = reinterpret_cast<uint4*>(a.xqg + (size_t)pos * (H / 2));
   for (int c = lane; c < H / 32; c += 32) cd[c] = cs[c];
-  const uint4* ss = reinterpret_cast<const uint4*>(a.xsf + (size_t)t * (H / 16));
-  uint4* sd = reinterpret_cast<uint4*>(a.xsfg + (size_t)pos * (H / 16));
-  for (int c = lane; c < H / 256; c += 32) sd[c] = ss[c];
+  const int sb = a.act_quant == 2 ? H / 32 : H / 16;  // scale bytes per row
+  const uint2* ss = reinterpret_cast<const uint2*>(a.xsf + (size_t)t * sb);
+  uint2* sd = reinterpret_cast<uint2*>(a.xsfg + (size_t)pos * sb);
+  for (int c = lane; c < sb / 8; c += 32) sd[c] = ss[c];
 }
 
 // One warp per sorted position: h (bf16) -> f16 * 2^s, s from the row's max |h|
@@ -417,7 +419,8 @@ cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s, Marks mk)
   pf_scan_kernel<<<1, kScanThreads, 0, s>>>(a);
   pf_place_kernel<<<nchunk, 32, a.E * 4, s>>>(a);
   if (a.act_quant) {
-    cudaError_t e2 = launch_quantize_act_nvfp4(a.x, a.T, a.H, a.xq, a.xsf, s);
+    cudaError_t e2 = a.act_quant == 2 ? launch_quantize_act_mxfp4(a.x, a.T, a.H, a.xq, a.xsf, s)
+                                      : launch_quantize_act_nvfp4(a.x, a.T, a.H, a.xq, a.xsf, s);
     if (e2 != cudaSuccess) return e2;
     pf_gather_q_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
   } else if (a.xg) {

@@ -1,4 +1,5 @@
-// Prefill expert GEMMs, NVFP4 W4A4 lever (block-scaled FP4 tensor cores).
+// Prefill expert GEMMs, W4A4 lever (block-scaled FP4 tensor cores): NVFP4
+// weights with NVFP4 activations, or MXFP4 weights with MXFP4 activations.
 //
 // The activation lever of the DGPP README ("Highlights", the W4A4 lever; the
 // levers are explicit and off by default): the token rows x and h are
@@ -6,7 +7,9 @@
 // and both operands of each projection are FP4.  tcgen05.mma
 // kind::mxf4nvf4 (scale_vec::4X) multiplies the packed E2M1 codes and
 // applies the two UE4M3 block scales in hardware; the weights' FP32 tensor
-// scale multiplies the FP32 accumulator in the epilogue.
+// scale multiplies the FP32 accumulator in the epilogue.  For MXFP4 weights
+// the activations are MXFP4 (32-element blocks, E8M0 scale) and the MMA is the
+// same kind with scale_vec::2X and UE8M0 scales.
 //
 //   gate/up: G = Wg x^T, U = Wu x^T per (token tile, 128 rows of I);
 //            h = bf16( silu(ts_g G) * (ts_u U) ), re-quantised to NVFP4 per
@@ -15,9 +18,10 @@
 //   down:    P[pos] = ts_d (Wd h^T), FP32 partials by sorted position.
 //
 // Operands: packed codes as 2-D TMA boxes of 128 rows x 128 bytes (256 K),
-// 128-byte swizzle, four stages.  Block scales go to TMEM: for every K=64
+// 128-byte swizzle, three stages.  Block scales go to TMEM: for every K=64
 // MMA, 4 columns per operand, where lane l of every quadrant, column c,
-// holds the four scale bytes of row (l mod 32) + 32 c.
+// holds the scale bytes of row (l mod 32) + 32 c for that MMA's K range:
+// four UE4M3 bytes (NVFP4), or two UE8M0 bytes in the low half (MXFP4).
 //
 // CTA roles (persistent grid, one CTA per SM):
 //   warp 0       TMA producer (weights and token codes);
@@ -62,19 +66,29 @@ struct Cw {
   static_assert(SF_BASE + ST * SF_STAGE <= 512, "TMEM columns");
 };
 
-// Instruction descriptor of kind::mxf4nvf4: E2M1 A and B, UE4M3 scales,
-// K-major operands, M = 128.
-__device__ __forceinline__ uint32_t idesc_nvf4(int N) {
-  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// Instruction descriptor of kind::mxf4nvf4: E2M1 A and B, K-major operands,
+// M = 128; bit 23 selects UE8M0 scales (MXFP4) instead of UE4M3 (NVFP4).
+template <bool MX>
+__device__ __forceinline__ uint32_t idesc_f4(int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (MX ? (1u << 23) : 0u) | ((uint32_t)(BM >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_nvf4(uint32_t d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa,
-                                         uint32_t sfb, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-          d),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate));
+template <bool MX>
+__device__ __forceinline__ void mma_f4(uint32_t d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+  if constexpr (MX) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+            "r"(d),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate));
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+            "r"(d),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate));
+  }
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
@@ -92,23 +106,34 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return __low2float(*reinterpret_cast<const __half2*>(&h));
 }
 
-// Block scales of rows row0 + lane + 32 c (c < 4) for one 256-K stage:
-// 16 bytes per row, word kk = the four scales of MMA kk -> v[4 kk + c].
+// Block scales of rows row0 + lane + 32 c (c < 4) for one 256-K stage, word kk
+// = the scales of MMA kk -> v[4 kk + c].  NVFP4: 16 bytes per row, four per
+// word; MXFP4: 8 bytes per row, two per word (low half).
+template <bool MX>
 __device__ __forceinline__ void load_scales(const uint8_t* base, size_t row_stride, int row0, int lane, int row_lim,
                                             int stage_off, uint32_t (&v)[16]) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int r = row0 + lane + 32 * c;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (r < row_lim) w = __ldg(reinterpret_cast<const uint4*>(base + (size_t)r * row_stride + stage_off));
-    v[c] = w.x;
-    v[4 + c] = w.y;
-    v[8 + c] = w.z;
-    v[12 + c] = w.w;
+    if constexpr (MX) {
+      uint2 w = make_uint2(0, 0);
+      if (r < row_lim) w = __ldg(reinterpret_cast<const uint2*>(base + (size_t)r * row_stride + stage_off));
+      v[c] = w.x & 0xFFFFu;
+      v[4 + c] = w.x >> 16;
+      v[8 + c] = w.y & 0xFFFFu;
+      v[12 + c] = w.y >> 16;
+    } else {
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (r < row_lim) w = __ldg(reinterpret_cast<const uint4*>(base + (size_t)r * row_stride + stage_off));
+      v[c] = w.x;
+      v[4 + c] = w.y;
+      v[8 + c] = w.z;
+      v[12 + c] = w.w;
+    }
   }
 }
 
-template <bool DOWN>
+template <bool DOWN, bool MX>
 __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, const __grid_constant__ CUtensorMap tmA0,
                                                               const __grid_constant__ CUtensorMap tmA1,
                                                               const __grid_constant__ CUtensorMap tmB) {
@@ -179,7 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
     // ---------------------------------------------------- scale writers --
     const int q = warp & 3;
     const uint32_t lq = (uint32_t)(q * 32) << 16;
-    const int Kb = K / 16;  // scale bytes per row
+    const int Kb = K / (MX ? 32 : 16);  // scale bytes per row
+    constexpr int kStageSf = KS / (MX ? 32 : 16);  // scale bytes per row per stage
     const uint8_t* sfb_base = DOWN ? a.hsf : a.xsfg;
     uint32_t g = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -193,9 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
 #pragma unroll
         for (int m = 0; m < C::NMAT; ++m) {
           const QW& W = DOWN ? a.down : (m == 0 ? a.gate : a.up);
-          load_scales(W.scales + (size_t)e * N * Kb, Kb, rt * BM, lane, N, s * 16, v[m]);
+          load_scales<MX>(W.scales + (size_t)e * N * Kb, Kb, rt * BM, lane, N, s * kStageSf, v[m]);
         }
-        load_scales(sfb_base, Kb, pos0, lane, P, s * 16, v[C::NMAT]);
+        load_scales<MX>(sfb_base, Kb, pos0, lane, P, s * kStageSf, v[C::NMAT]);
         if (!tc::bar_wait(&empty[stage], ((g / ST) & 1) ^ 1, a.wait_ns)) {
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x410 | (DOWN ? 1 : 0));
           ok = false;
@@ -220,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
       for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++item) {
         const int2 tile = a.tiles[it / RT];
         const int n_valid = min(NT, a.rb.off[tile.x + 1] - tile.y);
-        const uint32_t idesc = idesc_nvf4((n_valid + 15) & ~15);
+        const uint32_t idesc = idesc_f4<MX>((n_valid + 15) & ~15);
         const int buf = DOWN ? (item & 1) : 0, use = DOWN ? (item >> 1) : item;
         if (!tc::bar_wait(&acc_empty[buf], (use & 1) ^ 1, a.wait_ns)) {
           report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x420 | (DOWN ? 1 : 0));
@@ -246,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
 #pragma unroll
             for (int m = 0; m < C::NMAT; ++m) {
               const uint64_t da = tc::smem_desc_sw128(base + m * C::A_BYTES + kk * 32);
-              mma_nvf4(acc + m * NT, da, db, idesc, sf + m * 16 + kk * 4, sf + C::NMAT * 16 + kk * 4, (s | kk) != 0);
+              mma_f4<MX>(acc + m * NT, da, db, idesc, sf + m * 16 + kk * 4, sf + C::NMAT * 16 + kk * 4, (s | kk) != 0);
             }
           }
           tc::commit(&empty[stage]);
@@ -270,8 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
       const int rt = it % RT, e = tile.x, pos0 = tile.y;
       const int n_valid = min(NT, a.rb.off[e + 1] - pos0);
       const int buf = DOWN ? (item & 1) : 0, use = DOWN ? (item >> 1) : item;
-      const float ts0 = __ldg((DOWN ? a.down.ts : a.gate.ts) + e);
-      const float ts1 = DOWN ? 0.f : __ldg(a.up.ts + e);
+      // the NVFP4 tensor scales (MXFP4 has none)
+      const float ts0 = MX ? 1.f : __ldg((DOWN ? a.down.ts : a.gate.ts) + e);
+      const float ts1 = (DOWN || MX) ? 1.f : __ldg(a.up.ts + e);
       const bool ready = tc::bar_wait(&acc_full[buf], use & 1, a.wait_ns);
       if (!ready) report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x440 | (DOWN ? 1 : 0));
       // all epilogue warps go on, or all stop; the barrier also frees the staging tile
@@ -312,7 +339,37 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
       }
       tc::fence_before_sync();
       tc::bar_arrive(&acc_empty[buf]);  // TMEM buffer free for the MMA of a later tile
-      if (!DOWN) {
+      if (!DOWN && MX) {
+        // phase 2: MXFP4 of h per (column, 32-row block), the MXFP4 activation rule: the
+        // smallest e with 6 * 2^e >= amax, codes e2m1(h * 2^-e)
+        tc::named_sync(1, kEpiThreads);
+        const uint16_t* hs = reinterpret_cast<const uint16_t*>(stg);
+        uint8_t* cs = stg + NT * BM * 2;
+        const int et = tid - kWarpEpi0 * 32;
+        for (int u = et; u < n_valid * (BM / 32); u += kEpiThreads) {
+          const int c = u / (BM / 32), b = u % (BM / 32);
+          const uint4* src = reinterpret_cast<const uint4*>(hs + (size_t)c * BM + b * 32);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 v = src[i];
+            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+          }
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[i] & 0xFFFF)), fabsf(bf16_bits_to_float(w[i] >> 16))));
+          const int sc = mxfp4_act_scale_code(amax);
+          const float inv = exp2i(127 - sc);
+          uint32_t out[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            out[i >> 2] |= f32x2_to_e2m1x2_sat(bf16_bits_to_float(w[i] & 0xFFFF) * inv,
+                                               bf16_bits_to_float(w[i] >> 16) * inv) << (8 * (i & 3));
+          *reinterpret_cast<uint4*>(cs + c * (BM / 2) + b * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+          a.hsf[(size_t)(pos0 + c) * (I / 32) + rt * (BM / 32) + b] = (uint8_t)sc;
+        }
+      } else if (!DOWN) {
         // phase 2: NVFP4 of h per (column, 16-row block), the activation quantiser's
         // rule: scale e4m3(amax / 6), codes e2m1(h / scale)
         tc::named_sync(1, kEpiThreads);
@@ -402,7 +459,8 @@ bool u8_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
 
 }  // namespace
 
-cudaError_t launch_prefill_gemm_w4a4(bool down, const PrefillArgs& a, int grid, cudaStream_t s) {
+template <bool MX>
+cudaError_t launch_w4a4(bool down, const PrefillArgs& a, int grid, cudaStream_t s) {
   alignas(64) CUtensorMap tA0, tA1, tB;
   const uint64_t P = (uint64_t)a.T * a.k;
   cudaError_t err;
@@ -411,19 +469,25 @@ cudaError_t launch_prefill_gemm_w4a4(bool down, const PrefillArgs& a, int grid, 
         !u8_map(&tB, a.hq, (uint64_t)a.I / 2, P))
       return cudaErrorInvalidValue;
     tA1 = tA0;
-    err = cudaFuncSetAttribute(pf_w4a4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cw<true>::SMEM);
+    err = cudaFuncSetAttribute(pf_w4a4_kernel<true, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cw<true>::SMEM);
     if (err != cudaSuccess) return err;
-    pf_w4a4_kernel<true><<<grid, kThreads, Cw<true>::SMEM, s>>>(a, tA0, tA1, tB);
+    pf_w4a4_kernel<true, MX><<<grid, kThreads, Cw<true>::SMEM, s>>>(a, tA0, tA1, tB);
   } else {
     if (!u8_map(&tA0, a.gate.data, (uint64_t)a.H / 2, (uint64_t)a.E * a.I) ||
         !u8_map(&tA1, a.up.data, (uint64_t)a.H / 2, (uint64_t)a.E * a.I) ||
         !u8_map(&tB, a.xqg, (uint64_t)a.H / 2, P))
       return cudaErrorInvalidValue;
-    err = cudaFuncSetAttribute(pf_w4a4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cw<false>::SMEM);
+    err = cudaFuncSetAttribute(pf_w4a4_kernel<false, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cw<false>::SMEM);
     if (err != cudaSuccess) return err;
-    pf_w4a4_kernel<false><<<grid, kThreads, Cw<false>::SMEM, s>>>(a, tA0, tA1, tB);
+    pf_w4a4_kernel<false, MX><<<grid, kThreads, Cw<false>::SMEM, s>>>(a, tA0, tA1, tB);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_gemm_w4a4(bool down, const PrefillArgs& a, int grid, cudaStream_t s) {
+  return a.act_quant == 2 ? launch_w4a4<true>(down, a, grid, s) : launch_w4a4<false>(down, a, grid, s);
 }
 
 }  // namespace qmoe

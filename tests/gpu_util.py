@@ -110,7 +110,8 @@ def decode(layer, x_bits: np.ndarray, ws=None, prefill: bool = False, act_quant:
     if act_quant:
         I = layer.inter
         routing["h_codes"] = ws_read(ws, lo.h_codes, np.uint8, T * k * I // 2).reshape(T * k, I // 2)
-        routing["h_scales"] = ws_read(ws, lo.h_scales, np.uint8, T * k * I // 16).reshape(T * k, I // 16)
+        blk = 32 if act_quant == 2 else 16   # MXFP4 / NVFP4 block scales of h
+        routing["h_scales"] = ws_read(ws, lo.h_scales, np.uint8, T * k * I // blk).reshape(T * k, I // blk)
     return y.cpu().numpy().view(np.uint16), routing
 
 

@@ -100,6 +100,27 @@ def test_quantize_act_nvfp4_bit_exact():
     np.testing.assert_array_equal(codes.cpu().numpy(), packed)
 
 
+def test_quantize_act_mxfp4_bit_exact():
+    rng = np.random.default_rng(22)
+    rows, K = 37, 512
+    a = rng.standard_normal((rows, K)) * np.exp(rng.uniform(-30, 30, (rows, 1)))
+    a[0, :32] = 0.0                                  # zero block -> scale code 127, zero codes
+    a[1, :32] = np.linspace(-6.0, 6.0, 32) * 2.0 ** -4    # amax exactly 6 * 2^-4: exponent -4
+    a[2, :32] = a[1, :32] * (1 + 2.0 ** -7)          # just above: exponent -3
+    a[3, 32:64] = -0.0
+    a[4, :32] = 1e-40                                # below FP32's normal range
+    bits = F.f64_to_bf16_bits(a)
+    x = G.x_device(bits)
+    codes = torch.empty((rows, K // 2), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((rows, K // 32), dtype=torch.uint8, device="cuda")
+    B.moe_quantize_act_mxfp4(x, rows, K, codes, sc)
+    torch.cuda.synchronize()
+    q_ref, s_ref = M.mxfp4_quantize_act(F.bf16_to_f64(bits))
+    packed = (q_ref[:, 0::2] | (q_ref[:, 1::2] << 4)).astype(np.uint8)
+    np.testing.assert_array_equal(sc.cpu().numpy(), s_ref)
+    np.testing.assert_array_equal(codes.cpu().numpy(), packed)
+
+
 # ------------------------------------------------------------------ routing ----
 
 DECODE_CASES = [("tiny_nvfp4", 1), ("decode_nvfp4", 1), ("decode_nvfp4", 4), ("decode_nvfp4", 8),

@@ -194,8 +194,9 @@ def test_prefill_wide_scale_spreads(fmt):
 
 @pytest.mark.parametrize("case", ["w4a4_shared", "w4a4_mxfp4", "w4a4_int8"])
 def test_prefill_unsupported_is_reported(case):
-    """The W4A4 lever is implemented for NVFP4 routed experts without a shared
-    expert only: other layers report MOE_ERR_UNSUPPORTED before any launch."""
+    """The W4A4 lever is implemented for NVFP4 (act_quant 1) and MXFP4 (act_quant 2)
+    routed experts without a shared expert, each on its own format: other
+    layers report MOE_ERR_UNSUPPORTED before any launch."""
     if case == "w4a4_shared":
         cfg = LayerConfig("p_u1", FMT_NVFP4, H=256, E=4, k=2, I=256, shared_fmt=FMT_FP8_B128, shared_I=128)
     elif case == "w4a4_mxfp4":
@@ -208,6 +209,10 @@ def test_prefill_unsupported_is_reported(case):
     ws = G.new_ws(dl, 20, 1)
     st = B.moe_prefill_forward(dl, x, 20, y, ws, raise_on_error=False, act_quant=1)
     assert st == B.MOE_ERR_UNSUPPORTED
+    if cfg.fmt == FMT_MXFP4:   # MXFP4 activations on MXFP4 weights is supported; not on the others
+        return
+    st = B.moe_prefill_forward(dl, x, 20, y, ws, raise_on_error=False, act_quant=2)
+    assert st == B.MOE_ERR_UNSUPPORTED
 
 
 # ------------------------------------------------------------ W4A4 lever ----
@@ -215,7 +220,15 @@ def test_prefill_unsupported_is_reported(case):
 W4A4 = [
     LayerConfig("w4_small", FMT_NVFP4, H=512, E=6, k=2, I=256),
     LayerConfig("w4_skew", FMT_NVFP4, H=768, E=20, k=4, I=512, zipf_s=1.1),
+    # MXFP4 weights with MXFP4 activations (act_quant 2)
+    LayerConfig("w4_mx_small", FMT_MXFP4, H=512, E=6, k=2, I=256),
+    LayerConfig("w4_mx_skew", FMT_MXFP4, H=768, E=20, k=4, I=512, zipf_s=1.1),
 ]
+
+
+def _aq(cfg):
+    """The W4A4 lever's activation format for a layer: 2 (MXFP4) for MXFP4 weights, else 1 (NVFP4)."""
+    return 2 if cfg.fmt == FMT_MXFP4 else 1
 
 
 # Measured share of W4A4 outputs outside max(2 BF16 ulp, 1e-3) of the oracle's W4A4 mode (which
@@ -232,13 +245,14 @@ def _bf16_neighbours(v):
     return lo, hi
 
 
-def _check_w4a4(hl, x_bits, y_bits, routing, tokens=None):
-    """W4A4 parity in two exact stages.
+def _check_w4a4(hl, x_bits, y_bits, routing, tokens=None, aq=1):
+    """W4A4 parity in two exact stages (aq 1: NVFP4 activations in 16-element blocks; aq 2: MXFP4
+    activations in 32-element blocks).
     (1) Down projection and combine: y equals, within max(2 BF16 ulp, 1e-3) everywhere, the oracle's
-        down projection and weighted combine applied to the GPU's own NVFP4 h (codes and scales read
+        down projection and weighted combine applied to the GPU's own FP4 h (codes and scales read
         from the workspace).
-    (2) Gate/up and the h quantiser: the GPU's h codes and scales equal the oracle's (the A9 rule
-        applied to bf16(silu(g) * u) of the quantised token, in FP64) on every 16-element block,
+    (2) Gate/up and the h quantiser: the GPU's h codes and scales equal the oracle's (the activation
+        rule applied to bf16(silu(g) * u) of the quantised token, in FP64) on every block,
         except blocks where some element's unrounded h lies within 2^-12 (relative) of a BF16
         rounding midpoint and one choice of BF16 neighbours for those elements reproduces the GPU's
         block exactly: the GPU reaches h with FP32 accumulation, so it may round such an h the
@@ -254,8 +268,11 @@ def _check_w4a4(hl, x_bits, y_bits, routing, tokens=None):
     codes[:, 0::2] = routing["h_codes"] & 0xF
     codes[:, 1::2] = routing["h_codes"] >> 4
     sc = routing["h_scales"]
-    hq_gpu = M.nvfp4_dequantize_act(codes, sc)
-    Xq = M.nvfp4_fake_quant(F.bf16_to_f64(x_bits))
+    quantize = M.mxfp4_quantize_act if aq == 2 else M.nvfp4_quantize_act
+    dequantize = M.mxfp4_dequantize_act if aq == 2 else M.nvfp4_dequantize_act
+    nb = 32 if aq == 2 else 16
+    hq_gpu = dequantize(codes, sc)
+    Xq = M.act_fake_quant(F.bf16_to_f64(x_bits), aq)
     acc = {int(t): np.zeros(H) for t in want}
     unexplained, mismatched, blocks = [], 0, 0
     for e in range(cfg.E):
@@ -265,14 +282,14 @@ def _check_w4a4(hl, x_bits, y_bits, routing, tokens=None):
         Wg, Wu, Wd = (F.decode_qmat(hl.gate, e), F.decode_qmat(hl.up, e), F.decode_qmat(hl.down, e))
         rows = np.array([int(pair[q]) // k for q in pos])
         h_pre = M.silu(Xq[rows] @ Wg.T) * (Xq[rows] @ Wu.T)
-        q_or, s_or = M.nvfp4_quantize_act(F.round_bf16(h_pre))
+        q_or, s_or = quantize(F.round_bf16(h_pre))
         P = hq_gpu[pos] @ Wd.T
         for i, q in enumerate(pos):
             t, j = divmod(int(pair[q]), k)
             acc[t] += float(w[t, j]) * P[i]
-            for b in range(I // 16):
+            for b in range(I // nb):
                 blocks += 1
-                sl = slice(16 * b, 16 * b + 16)
+                sl = slice(nb * b, nb * b + nb)
                 if s_or[i, b] == sc[q, b] and np.array_equal(q_or[i, sl], codes[q, sl]):
                     continue
                 mismatched += 1
@@ -287,7 +304,7 @@ def _check_w4a4(hl, x_bits, y_bits, routing, tokens=None):
                         v = base.copy()
                         for n, ii in enumerate(idx):
                             v[ii] = hi[ii] if (mask >> n) & 1 else lo[ii]
-                        cq, cs = M.nvfp4_quantize_act(v[None, :])
+                        cq, cs = quantize(v[None, :])
                         if cs[0, 0] == sc[q, b] and np.array_equal(cq[0], codes[q, sl]):
                             ok = True
                             break
@@ -300,9 +317,9 @@ def _check_w4a4(hl, x_bits, y_bits, routing, tokens=None):
     ok = M.within_tolerance(y, F.bf16_to_f64(F.f64_to_bf16_bits(y_stage)))
     assert ok.all(), f"{int((~ok).sum())} of {ok.size} outputs differ from the down + combine of the GPU's h"
     assert np.isfinite(y).all()
-    ref = M.layer_forward(hl, x_bits, act_quant=True, tokens=tokens)
+    ref = M.layer_forward(hl, x_bits, act_quant=aq, tokens=tokens)
     frac = float((~M.within_tolerance(y, F.bf16_to_f64(ref["y_bits"]))).mean())
-    print(f"W4A4: {mismatched} of {blocks} h blocks flipped by BF16 rounding; "
+    print(f"W4A4 (act_quant {aq}): {mismatched} of {blocks} h blocks flipped by BF16 rounding; "
           f"{frac:.2e} of outputs outside 2 ulp of the oracle's W4A4 result")
     assert frac <= W4A4_OUTLIER_CAP, frac
     return frac
@@ -314,10 +331,22 @@ def test_prefill_w4a4_matches_oracle(cfg, T):
     hl = synth.make_layer(cfg, seed=9)
     dl = to_device(hl)
     x = synth.make_tokens(cfg, T, seed=9, batch=T)
-    y, routing = G.decode(dl, x, prefill=True, act_quant=1)
-    _check_w4a4(hl, x, y, routing)
-    ref = M.layer_forward(hl, x, act_quant=True)
+    y, routing = G.decode(dl, x, prefill=True, act_quant=_aq(cfg))
+    _check_w4a4(hl, x, y, routing, aq=_aq(cfg))
+    ref = M.layer_forward(hl, x, act_quant=_aq(cfg))
     assert_prefill_routing(routing, ref, ref["near_midpoint"])
+
+
+def test_prefill_w4a4_mxfp4_workload_sampled():
+    # the MXFP4 layer's shapes (H=4096, I=2048) with fewer experts, so that the layer stays small
+    cfg = G.host_layer("decode_mxfp4").cfg.with_(name="w4_mx_wide", E=32)
+    hl = synth.make_layer(cfg, seed=3)
+    dl = to_device(hl)
+    T = 512
+    tokens = [0, 1, 255, 511]
+    x = synth.make_tokens(cfg, T, seed=3, batch=T)
+    y, routing = G.decode(dl, x, prefill=True, act_quant=2)
+    _check_w4a4(hl, x, y, routing, tokens, aq=2)
 
 
 def test_prefill_w4a4_workload_sampled():
