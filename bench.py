@@ -497,15 +497,17 @@ def run_prefill(args, local, peak_bf16, peak_kind, name="prefill_nvfp4", tokens=
         "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
         "graph": f"CUDA graph of {G} layer calls; median of {reps} replays",
     }
-    if w4a4 and cfg.fmt == synth.configs.FMT_NVFP4 and not cfg.shared_fmt:
-        # the W4A4 lever (act_quant = 1): block-scaled FP4 GEMMs, same workload
-        ws4 = torch.empty(q.workspace_size(lay, T, 1), dtype=torch.uint8, device="cuda")
+    aq = {synth.configs.FMT_NVFP4: 1, synth.configs.FMT_MXFP4: 2}.get(cfg.fmt, 0)
+    if w4a4 and aq and not cfg.shared_fmt:
+        # the W4A4 lever (act_quant 1: NVFP4 activations, 2: MXFP4 activations): block-scaled FP4 GEMMs
+        ws4 = torch.empty(q.workspace_size(lay, T, aq), dtype=torch.uint8, device="cuda")
         q.workspace_init(ws4)
-        us4, dur4 = _prefill_times(torch, q, lay, xs, T, y, ws4, stream, 1, reps, G)
+        us4, dur4 = _prefill_times(torch, q, lay, xs, T, y, ws4, stream, aq, reps, G)
         gemm4_us = dur4[3] + dur4[5]
         tflops4 = flops / (gemm4_us * 1e-6) / 1e12
         out["w4a4"] = {
-            "path": "NVFP4 activations (lever, act_quant=1): tcgen05 kind::mxf4nvf4 block-scaled GEMMs",
+            "path": (f"{FMT_TEXT[cfg.fmt]} activations (lever, act_quant={aq}): tcgen05 kind::mxf4nvf4 "
+                     f"block-scaled GEMMs ({'UE8M0, scale_vec::2X' if aq == 2 else 'UE4M3, scale_vec::4X'})"),
             "us_per_layer": round(us4, 1), "tokens_per_s": round(T / (us4 * 1e-6), 1),
             "kernel_us": {k: round(float(v), 2) for k, v in zip(
                 ["router_logits", "router_topk", "dispatch_quantise", "gateup_gemm", "-", "down_gemm",
@@ -636,7 +638,7 @@ def main():
         pk, pkk = _bf16_peak()
         res = {"prefill": run_prefill(args, local, pk, pkk, tokens=args.prefill_tokens)}
         for name in filter(None, args.more_prefill.split(",")):
-            res[name] = run_prefill(args, local, pk, pkk, name, tokens=args.prefill_tokens, w4a4=False)
+            res[name] = run_prefill(args, local, pk, pkk, name, tokens=args.prefill_tokens)
         if rank == 0:
             print(json.dumps(res))
         return
@@ -646,7 +648,7 @@ def main():
         out["prefill"] = run_prefill(args, local, pk, pkk, tokens=args.prefill_tokens)
         more = {}
         for name in filter(None, args.more_prefill.split(",")):
-            more[name] = run_prefill(args, local, pk, pkk, name, tokens=args.prefill_tokens, w4a4=False)
+            more[name] = run_prefill(args, local, pk, pkk, name, tokens=args.prefill_tokens)
         if more:
             out["prefill_more"] = more
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
