@@ -24,6 +24,10 @@ page 4 forum post 1 quantisation table "Activations stay BF16"):
   rounding of the hidden activation to BF16, down projection in FP64, and the
   weighted combine with the FP32 routing weights plus the shared expert,
   rounded once to BF16 (``moe.layer_forward``);
+* optionally the fold-scales lever (page 3 README "Execution and performance"
+  table, row ``engine.prefill_fold_scales``): int8 g64, FP8 b128 and int4
+  g128 weights enter as bf16(fl32(code * scale)) with one accumulator
+  (``formats.fold_scales_weights``);
 * optionally the NVFP4 W4A4 lever (page 2/3 highlights and page 5 weekly
   update: NVFP4 W4A4 prefill is opt-in): activations and hidden states
   re-quantised to NVFP4 16-element blocks before the projections

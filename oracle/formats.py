@@ -148,6 +148,34 @@ def decode_qmat(qm, e: int = 0) -> np.ndarray:
     return decode(qm.fmt, qm.data[e], qm.scales[e], float(qm.ts[e]), qm.N, qm.K)
 
 
+# Formats whose group scale the fold-scales lever folds into BF16 weights.
+FOLD_LEVER_FORMATS = (FMT_INT8_G64, FMT_FP8_B128, FMT_INT4_G128)
+
+
+def fold_scales_weights(fmt: int, W: np.ndarray) -> np.ndarray:
+    """The fold-scales lever's weight values from the exact decode W = code * scale.
+
+    DGPP README "Execution and performance" table, row engine.prefill_fold_scales:
+    each group's scale is folded into the BF16 weight values, and one FP32
+    accumulator runs across K (Marlin's form, no per-group FMA).  Reading:
+    the product is taken in FP32, as a kernel computes code * scale, and is
+    then rounded to BF16 (nearest, ties to even).  For int8 g64 and int4 g128
+    the FP32 product is exact (at most 8 + 11 significant bits); for FP8 b128
+    (E4M3 times an FP32 scale) it is the FP32 rounding of the exact product.
+    The other formats (NVFP4, MXFP4, int4 g64) already reach the exact
+    chain's MMA with their scales folded exactly, so the lever leaves them as
+    decoded.
+    """
+    if fmt not in FOLD_LEVER_FORMATS:
+        return W
+    return round_bf16(np.asarray(W, dtype=np.float64).astype(np.float32).astype(np.float64))
+
+
+def decode_qmat_fold(qm, e: int = 0) -> np.ndarray:
+    """Expert e of a synth.QMat stack as the fold-scales lever's weights."""
+    return fold_scales_weights(qm.fmt, decode_qmat(qm, e))
+
+
 # ---- encoders used by the W4A4 activation quantizer (the layer's own arithmetic) ----
 
 E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])

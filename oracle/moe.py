@@ -278,12 +278,13 @@ def mxfp4_fake_quant(a: np.ndarray) -> np.ndarray:
 
 # ------------------------------------------------------------------ layer ----
 
-def _decoded(qm, e):
-    return F.decode_qmat(qm, e)
+def _decoded(qm, e, fold_scales: bool = False):
+    return F.decode_qmat_fold(qm, e) if fold_scales else F.decode_qmat(qm, e)
 
 
 def layer_forward(layer, x_bits: np.ndarray, act_quant: int = 0, tokens=None, expert_cache=None,
-                  bias_select: bool = False, bf16_partials: bool = False, routing=None):
+                  bias_select: bool = False, bf16_partials: bool = False, routing=None,
+                  fold_scales: bool = False):
     """Full MoE layer on host-resident checkpoint data (a synth.HostLayer).
 
     tokens: optional subset of token rows whose outputs are wanted (routing is
@@ -302,6 +303,10 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: int = 0, tokens=None, ex
     router is then skipped and these pairs and weights are used as given.
     act_quant: the W4A4 lever's activation quantisation (1 or True: NVFP4, 2:
     MXFP4), applied to the token rows and to h before each projection.
+    fold_scales: the fold-scales lever (``formats.fold_scales_weights``):
+    int8 g64, FP8 b128 and int4 g128 weights, routed and shared, enter as
+    bf16(fl32(code * scale)); the rest of the chain is unchanged.  An
+    ``expert_cache`` must then supply the folded weights itself.
     Returns a dict of every intermediate the CUDA path exposes.
     """
     cfg = layer.cfg
@@ -326,7 +331,8 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: int = 0, tokens=None, ex
         if expert_cache is not None:
             Wg, Wu, Wd = expert_cache(e)
         else:
-            Wg, Wu, Wd = _decoded(layer.gate, e), _decoded(layer.up, e), _decoded(layer.down, e)
+            Wg, Wu, Wd = (_decoded(layer.gate, e, fold_scales), _decoded(layer.up, e, fold_scales),
+                          _decoded(layer.down, e, fold_scales))
         rows = np.array([p // cfg.k for p in ps])
         h, P = swiglu_mlp(Wg, Wu, Wd, X[rows], act_quant)
         if bf16_partials:
@@ -337,8 +343,8 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: int = 0, tokens=None, ex
             h_out[p] = h[i]
     S = None
     if layer.shared_gate is not None:
-        Wg, Wu, Wd = (_decoded(layer.shared_gate, 0), _decoded(layer.shared_up, 0),
-                      _decoded(layer.shared_down, 0))
+        Wg, Wu, Wd = (_decoded(layer.shared_gate, 0, fold_scales), _decoded(layer.shared_up, 0, fold_scales),
+                      _decoded(layer.shared_down, 0, fold_scales))
         _, S = swiglu_mlp(Wg, Wu, Wd, X[want], act_quant)
         if bf16_partials:
             S = F.round_bf16(S)

@@ -295,3 +295,125 @@ def test_oracle_e4m3_encoder_matches_torch():
     ref = torch.from_numpy(v[inr]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(codes[inr], ref)
     assert np.all(codes[~inr] == 0x7E)                    # saturation
+
+
+# ------------------------------------------------------ fold-scales lever ----
+
+def _round_frac(x: Fraction, bits: int) -> Fraction:
+    """Nearest binary value with `bits` significant bits to x (ties to even), normal range."""
+    if x == 0:
+        return x
+    a = abs(x)
+    e = 0
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    while Fraction(2) ** e > a:
+        e -= 1
+    step = Fraction(2) ** (e - bits + 1)
+    lo = (a // step) * step
+    hi = lo + step
+    if a - lo < hi - a:
+        r = lo
+    elif hi - a < a - lo:
+        r = hi
+    else:
+        r = lo if (lo / step) % 2 == 0 else hi
+    return r if x > 0 else -r
+
+
+def _fold_ref(code: float, scale: float) -> float:
+    """bf16(fl32(code * scale)) by exact rational rounding: 24 significant bits, then 8."""
+    return float(_round_frac(_round_frac(Fraction(code) * Fraction(scale), 24), 8))
+
+
+def _double_rounding_fp8_cases():
+    """(E4M3 value, FP32 scale) pairs whose FP32 product lands on a BF16 midpoint that the exact
+    product is not on: rounding through FP32 and rounding directly disagree there."""
+    out = []
+    for j in range(128):
+        m = Fraction(1) + Fraction(j, 128) + Fraction(1, 256)          # a BF16 midpoint in [1, 2)
+        for c in (1.125, 1.25, 1.375, 1.625, 1.75, 1.875):
+            s0 = float(np.float32(float(m / Fraction(c))))
+            for k in range(-3, 4):
+                s = float(np.nextafter(np.float32(s0), np.float32(np.inf if k > 0 else -np.inf))) if k else s0
+                for _ in range(abs(k) - 1):
+                    s = float(np.nextafter(np.float32(s), np.float32(np.inf if k > 0 else -np.inf)))
+                p = Fraction(c) * Fraction(s)
+                if _round_frac(p, 8) != _round_frac(_round_frac(p, 24), 8):
+                    out.append((c, s))
+    return out
+
+
+def _fold_cases():
+    rng = np.random.default_rng(11)
+    f32 = (rng.standard_normal(40) * 0.02).astype(np.float32)
+    bf16_scales = [float(v) for v in torch.from_numpy(f32).to(torch.bfloat16).to(torch.float64).numpy()]
+    bf16_scales += [2.0 ** -7, 1.0078125, -3.0 * 2.0 ** -9]
+    fp16_scales = [float(v) for v in (rng.standard_normal(40) * 0.01).astype(np.float16)] + [2.0 ** -10]
+    fp32_scales = [float(v) for v in (rng.standard_normal(20) * 1e-3).astype(np.float32)] + [2.0 ** -8]
+    cases = []
+    for s in bf16_scales:
+        cases += [(F.FMT_INT8_G64, float(q), s) for q in range(-128, 128)]
+    for s in fp16_scales:
+        cases += [(F.FMT_INT4_G128, float(q), s) for q in range(-8, 8)]
+    e4m3 = [float(v) for v in F.E4M3_TABLE if np.isfinite(v)]
+    for s in fp32_scales:
+        cases += [(F.FMT_FP8_B128, q, s) for q in e4m3]
+    cases += [(F.FMT_FP8_B128, c, s) for c, s in _double_rounding_fp8_cases()]
+    return cases
+
+
+_FOLD_CASES = None
+
+
+def _fold_mismatches(fold_fn) -> int:
+    global _FOLD_CASES
+    if _FOLD_CASES is None:
+        _FOLD_CASES = _fold_cases()
+    bad = 0
+    for fmt, c, s in _FOLD_CASES:
+        got = float(fold_fn(fmt, np.array([c * s]))[0])  # c * s is exact in FP64 for every format here
+        bad += got != _fold_ref(c, s)
+    return bad
+
+
+def test_fold_scales_weights_exact_rationals():
+    # every code of int8 g64 / int4 g128 / FP8 b128 times sampled scales of the format's scale type,
+    # plus constructed FP8 cases where rounding through FP32 and rounding directly disagree
+    assert len(_double_rounding_fp8_cases()) > 0
+    assert _fold_mismatches(F.fold_scales_weights) == 0
+
+
+def test_fold_scales_hand_example_and_identity_cases():
+    # q = 3 times the BF16 scale 1 + 2^-7: 3.0234375 = 1.1000001|1 x 2^1 rounds up to 3.03125
+    assert F.fold_scales_weights(F.FMT_INT8_G64, np.array([3 * 1.0078125]))[0] == 3.03125
+    # power-of-two scales: an int8 code has at most 7 significant bits, so the fold is exact
+    q = np.arange(-128, 128, dtype=np.float64)
+    assert np.array_equal(F.fold_scales_weights(F.FMT_INT8_G64, q * 2.0 ** -7), q * 2.0 ** -7)
+    # formats the exact chain already folds exactly are left as decoded
+    W = np.array([0.1234567, -3.3e-5, 7.0])
+    for fmt in (F.FMT_NVFP4, F.FMT_MXFP4, F.FMT_INT4_G64):
+        assert np.array_equal(F.fold_scales_weights(fmt, W), W)
+
+
+def _fold_truncating(fmt, W):
+    if fmt not in F.FOLD_LEVER_FORMATS:
+        return W
+    b = np.asarray(W, dtype=np.float64).astype(np.float32).view(np.uint32) & np.uint32(0xFFFF0000)
+    return b.view(np.float32).astype(np.float64)
+
+
+def _fold_direct(fmt, W):
+    return F.round_bf16(W) if fmt in F.FOLD_LEVER_FORMATS else W
+
+
+def _fold_to_f16(fmt, W):
+    # wrong: the folded weight rounded to FP16 (the exact chain's operand type) instead of BF16
+    if fmt not in F.FOLD_LEVER_FORMATS:
+        return W
+    return np.asarray(W, dtype=np.float64).astype(np.float32).astype(np.float16).astype(np.float64)
+
+
+@pytest.mark.parametrize("planted", [_fold_truncating, _fold_direct, _fold_to_f16])
+def test_fold_scales_pin_catches_planted_mistakes(planted):
+    assert _fold_mismatches(planted) > 0

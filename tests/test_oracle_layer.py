@@ -149,6 +149,33 @@ def test_bf16_partials_round_each_expert_output():
     assert not np.array_equal(out["y_f64"], M.layer_forward(lay, x)["y_f64"])
 
 
+@pytest.mark.parametrize("fmt,shared_fmt,H,I", [(FMT_INT8_G64, FMT_FP8_B128, 128, 128),
+                                                (FMT_INT4_G128, FMT_INT8_G64, 256, 128)])
+def test_fold_scales_lever_equals_mlp_on_bf16_weights(fmt, shared_fmt, H, I):
+    # the lever: every int8 g64 / FP8 b128 / int4 g128 weight enters as bf16(fp32(code x scale)); here
+    # the folded weights come from torch's fp64 -> fp32 -> bf16 casts of an independent torch decode
+    cfg = _small(fmt, shared_fmt, E=1, k=1, H=H, I=I)
+    lay = synth.make_layer(cfg, seed=14)
+    x = synth.make_tokens(cfg, 5, seed=14)
+    out = M.layer_forward(lay, x, fold_scales=True)
+    fold = lambda W: W.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    X = torch.from_numpy(F.bf16_to_f64(x))
+    y_ref = (_torch_mlp(fold(_torch_decode(lay.gate)), fold(_torch_decode(lay.up)), fold(_torch_decode(lay.down)), X)
+             + _torch_mlp(fold(_torch_decode(lay.shared_gate)), fold(_torch_decode(lay.shared_up)),
+                          fold(_torch_decode(lay.shared_down)), X)).numpy()
+    ok = M.within_tolerance(F.bf16_to_f64(out["y_bits"]), y_ref, ulps=1.0, abs_tol=1e-6)
+    assert ok.all(), np.abs(F.bf16_to_f64(out["y_bits"]) - y_ref).max()
+    assert not np.array_equal(out["y_f64"], M.layer_forward(lay, x)["y_f64"])   # not the exact chain
+
+
+def test_fold_scales_lever_leaves_exactly_folded_formats():
+    # NVFP4 routed experts: the lever changes nothing (their scales already fold exactly)
+    cfg = _small(FMT_NVFP4, E=4, k=2, H=128, I=64)
+    lay = synth.make_layer(cfg, seed=15)
+    x = synth.make_tokens(cfg, 4, seed=15)
+    assert np.array_equal(M.layer_forward(lay, x, fold_scales=True)["y_f64"], M.layer_forward(lay, x)["y_f64"])
+
+
 def test_identical_experts_top2_equals_top1():
     cfg1 = _small(FMT_NVFP4, E=1, k=1)
     lay1 = synth.make_layer(cfg1, seed=5)
