@@ -141,7 +141,17 @@ typedef struct {
    * kernels gives up after this many microseconds and reports
    * MOE_ERR_DEVICE_TIMEOUT through moe_check. */
   int32_t wait_limit_us;
-  int32_t reserved[5];       /* must be zero */
+  /* 0 (default): the exact chain.  1: the fold-scales lever (prefill only;
+   * DGPP README "Execution and performance", engine.prefill_fold_scales):
+   * int8 g64, FP8 b128 and int4 g128 weights, routed or shared, enter the
+   * grouped GEMMs as BF16 values bf16(fl32(code * group scale)) against
+   * plain BF16 activations, with one FP32 accumulator across K instead of
+   * one per scale group.  Not bitwise the default chain.  NVFP4, MXFP4 and
+   * int4 g64 weights already reach the MMA with their scales folded exactly
+   * and are unchanged by it.  The decode entry points return
+   * MOE_ERR_UNSUPPORTED when it is set. */
+  int32_t fold_scales;
+  int32_t reserved[4];       /* must be zero */
 } moe_options;
 
 /* Largest token count moe_decode_forward accepts. */

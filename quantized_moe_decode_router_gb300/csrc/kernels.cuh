@@ -132,7 +132,8 @@ struct PrefillArgs {
   QW gate, up, down;
   RouteBufs rb;         // logits [T, E] (approximate, then exact for candidates), top-k, cnt, off, pair
   RouteOut out;
-  uint16_t* xg;         // f16 [T*k, H]: row pos = x[token of pos] * 2^xsig[token] (sorted order)
+  uint16_t* xg;         // f16 [T*k, H]: row pos = x[token of pos] * 2^xsig[token] (sorted order);
+                        // under the fold-scales lever the BF16 row x[token of pos] itself
   int32_t* xsig;        // [T]
   float* xnorm;         // [T] ||x_t||_2
   float* wnorm;         // [E] ||Wr_e||_2
@@ -154,6 +155,7 @@ struct PrefillArgs {
   float* unbiased;      // [T, E] unbiased exact logits of the recomputed experts (bias_select)
   uint64_t wait_ns;     // limit of every bounded device wait (nanoseconds)
   int p_bf16;           // 1: the down GEMM writes P as BF16 (the bf16-partials lever)
+  int fold_scales;      // 1: the fold-scales lever (int8 g64 / FP8 b128 / int4 g128 blocks, see fold_lever)
   // NVFP4 W4A4 lever (act_quant = 1)
   int act_quant;
   uint8_t* xq;          // [T, H/2] E2M1 codes of x (16-element blocks)
@@ -174,6 +176,14 @@ struct PrefillArgs {
   float* sgate;         // [T] sigmoid(x_t . sgate_w)
   int dense_T;          // > 0: this argument block is the shared expert's (tiles of NT consecutive tokens)
 };
+
+// The fold-scales lever applies to this argument block (routed or shared):
+// int8 g64, FP8 b128 and int4 g128 weights enter the GEMMs as bf16(code x
+// group scale) with plain BF16 tokens and one FP32 accumulator.
+__host__ __device__ inline bool fold_lever(const PrefillArgs& a) {
+  return a.fold_scales != 0 &&
+         (a.fmt == MOE_FMT_INT8_G64 || a.fmt == MOE_FMT_FP8_B128 || a.fmt == MOE_FMT_INT4_G128);
+}
 
 // Optional host callback between launches (event records of the timed entry
 // point): mark(ctx, i) after stage i.

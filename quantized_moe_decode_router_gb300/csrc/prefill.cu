@@ -263,9 +263,14 @@ __global__ void __launch_bounds__(kThreads) pf_gather_kernel(PrefillArgs a) {
   if (pos >= a.T * a.k) return;
   const int H = a.H;
   const int t = a.dense_T ? pos : a.rb.pair[pos] / a.k;
-  const float mul = exp2i(a.xsig[t]);
   const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
   uint4* xo = reinterpret_cast<uint4*>(a.xg + (size_t)pos * H);
+  if (fold_lever(a)) {
+    // the fold-scales lever's B operand: the BF16 row as it is
+    for (int c = lane; c < H / 8; c += 32) xo[c] = __ldg(xr + c);
+    return;
+  }
+  const float mul = exp2i(a.xsig[t]);
   for (int c = lane; c < H / 8; c += 32) {
     const uint4 v = __ldg(xr + c);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -457,8 +462,9 @@ cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s
   if (err != cudaSuccess) return err;
   if (a.sfmt && (err = launch_prefill_gemm(false, sa, sms, s)) != cudaSuccess) return err;
   mk(4);
-  pf_hconv_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
-  if (a.sfmt) pf_hconv_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(sa);
+  // h -> f16 with a power-of-two row scale (the down GEMM's B); the fold-scales lever reads h as it is
+  if (!fold_lever(a)) pf_hconv_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
+  if (a.sfmt && !fold_lever(sa)) pf_hconv_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(sa);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   mk(5);
   if ((err = launch_prefill_gemm(true, a, sms, s)) != cudaSuccess) return err;

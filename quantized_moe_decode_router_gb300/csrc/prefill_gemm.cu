@@ -64,9 +64,13 @@ constexpr bool promote_fmt() {
   return F == MOE_FMT_INT8_G64 || F == MOE_FMT_FP8_B128 || F == MOE_FMT_INT4_G128;
 }
 
-template <int F, bool DOWN>
+// FS: the fold-scales lever on a promote format: each code times its group
+// scale is rounded to one BF16 weight (FP32 product, then BF16), the tokens
+// enter as plain BF16, one FP32 accumulator runs across K.
+template <int F, bool DOWN, bool FS = false>
 struct Cfg {
-  static constexpr bool PROMOTE = promote_fmt<F>();
+  static_assert(!FS || promote_fmt<F>(), "the fold-scales lever applies to the promote formats");
+  static constexpr bool PROMOTE = promote_fmt<F>() && !FS;
   static constexpr int BITS = (F == MOE_FMT_INT8_G64 || F == MOE_FMT_FP8_B128) ? 8 : 4;
   static constexpr int GS = F == MOE_FMT_INT8_G64 ? 1 : 2;  // K steps per scale group (promote formats)
   static constexpr int NMAT = DOWN ? 1 : 2;
@@ -75,7 +79,8 @@ struct Cfg {
   static constexpr int TPR = kDec / (NMAT * BM);  // decode threads per weight row
   static constexpr int KT = BK / TPR;             // columns per decode thread per step
   static constexpr int CODE_BYTES = KT * BITS / 8;               // per thread per step
-  static constexpr int RAW_BYTES = PROMOTE ? CODE_BYTES : CODE_BYTES + 16;  // fold: then the scale word (padded)
+  // fold: the codes, then the step's scale word (padded); promote and FS: the codes only
+  static constexpr int RAW_BYTES = (PROMOTE || FS) ? CODE_BYTES : CODE_BYTES + 16;
   static constexpr int RAW = DOWN ? 6 : (BITS == 8 ? 4 : 5);    // raw-code ring stages (prefetch RAW - 1 steps)
   static constexpr int A_BYTES = BM * KB;
   static constexpr int B_BYTES = NT * KB;
@@ -228,6 +233,23 @@ __device__ __forceinline__ uint4 codes_to_f16(const uint32_t* cw, int c) {
   return make_uint4(v[0], v[1], v[2], v[3]);
 }
 
+// The fold-scales lever: eight weights (k ascending) of a promote format as
+// four bf16x2, each bf16(fl32(code * sc)) (the FP32 product, then BF16
+// nearest-even).
+template <int F>
+__device__ __forceinline__ uint4 fold_lever_word(const uint32_t* cw, int c, float sc) {
+  const uint4 q = codes_to_f16<F>(cw, c);  // exact code values
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+    o[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Scale of group g (GS K steps) for weight row `row` of expert e (FP8 b128: the
 // 128 x 128 block of row tile rt).
 template <int F>
@@ -262,10 +284,10 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-template <int F, bool DOWN>
+template <int F, bool DOWN, bool FS>
 __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs a,
                                                                     const __grid_constant__ CUtensorMap tmB) {
-  using C = Cfg<F, DOWN>;
+  using C = Cfg<F, DOWN, FS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full_a[C::SA], empty_a[C::SA], full_b[C::SB], empty_b[C::SB];
@@ -318,14 +340,15 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
       const int rt = it % RT, e = tile.x;
       const int row = rt * BM + rr;
       const uint8_t* crow = W.data + (size_t)e * data_bytes(F, N, K) + (size_t)row * ((size_t)K * C::BITS / 8);
-      const uint8_t* srow =
-          C::PROMOTE ? nullptr : W.scales + (size_t)e * scale_bytes(F, N, K) + (size_t)row * row_scale_bytes<F>(K);
+      const uint8_t* srow = (C::PROMOTE || FS) ? nullptr
+                                               : W.scales + (size_t)e * scale_bytes(F, N, K) +
+                                                     (size_t)row * row_scale_bytes<F>(K);
       auto issue = [&](int s) {
         uint8_t* dst = raw + (s % C::RAW) * (kDec * C::RAW_BYTES);
         const uint8_t* src = crow + (size_t)(s * BK + hh * C::KT) * C::BITS / 8;
 #pragma unroll
         for (int j = 0; j < C::CODE_BYTES / 16; ++j) cp_async16(dst + 16 * j, src + 16 * j);
-        if constexpr (!C::PROMOTE) {
+        if constexpr (!C::PROMOTE && !FS) {
           // the aligned word holding the step's scales (their byte offset in it is taken at the read)
           cp_async4(dst + C::CODE_BYTES,
                     reinterpret_cast<const void*>(reinterpret_cast<uintptr_t>(srow + step_scale_off<F>(s)) & ~(uintptr_t)3));
@@ -337,7 +360,10 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         cp_async_commit();
       }
       int ref = 0;
-      if constexpr (!C::PROMOTE) ref = row_ref<F>(srow, K);  // while the first steps are in flight
+      if constexpr (!C::PROMOTE && !FS) ref = row_ref<F>(srow, K);  // while the first steps are in flight
+      // FS: the group scale of the next step, loaded one step ahead
+      float sc_next = 0.f;
+      if constexpr (FS) sc_next = group_scale<F>(W, e, N, K, row, rt, 0);
 #pragma unroll 1
       for (int s = 0; s < nsteps; ++s, ++g) {
         if (s + C::RAW - 1 < nsteps) issue(s + C::RAW - 1);
@@ -352,7 +378,12 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
           cw[4 * c4] = v.x; cw[4 * c4 + 1] = v.y; cw[4 * c4 + 2] = v.z; cw[4 * c4 + 3] = v.w;
         }
         uint4 out[C::KT / 8];
-        if constexpr (C::PROMOTE) {
+        if constexpr (FS) {
+          const float sc = sc_next;
+          if (s + 1 < nsteps) sc_next = group_scale<F>(W, e, N, K, row, rt, (s + 1) / C::GS);
+#pragma unroll
+          for (int c = 0; c < C::KT / 8; ++c) out[c] = fold_lever_word<F>(cw, c, sc);
+        } else if constexpr (C::PROMOTE) {
 #pragma unroll
           for (int c = 0; c < C::KT / 8; ++c) out[c] = codes_to_f16<F>(cw, c);
         } else {
@@ -453,7 +484,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
     for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++item) {
       const int n_valid = tile_valid(a, tile_at(a, it / RT));
       const int n_mma = (n_valid + 15) & ~15;
-      const uint32_t idesc = tc::idesc_f16(BM, n_mma, 0);
+      const uint32_t idesc = tc::idesc_f16(BM, n_mma, FS ? 1 : 0);  // FS: bf16 operands
       if constexpr (C::PROMOTE) {
         // each scale group into the block set; the epilogue empties it before the next group
         const uint32_t blk = tmem + C::ACC_COLS;
@@ -510,7 +541,8 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int pos_l = pos0 + min(chalf * 64 + i * 32 + lane, n_valid - 1);
-        if (DOWN) un_c[i] = exp2i(-a.hsig[pos_l]);
+        if (FS) un_c[i] = 1.f;  // plain BF16 tokens
+        else if (DOWN) un_c[i] = exp2i(-a.hsig[pos_l]);
         else un_c[i] = exp2i(-a.xsig[a.dense_T ? pos_l : a.rb.pair[pos_l] / k]);
       }
       const int erow = rt * BM + row;
@@ -580,9 +612,14 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         float rf[2];
 #pragma unroll
         for (int mm = 0; mm < C::NMAT; ++mm) {
-          const QW& Wm = DOWN ? a.down : (mm == 0 ? a.gate : a.up);
-          const uint8_t* sr = Wm.scales + (size_t)e * scale_bytes(F, N, K) + (size_t)erow * row_scale_bytes<F>(K);
-          rf[mm] = row_factor<F>(row_ref<F>(sr, K), F == MOE_FMT_NVFP4 ? __ldg(Wm.ts + e) : 1.f);
+          if constexpr (FS) {
+            rf[mm] = 1.f;  // the scales are in the BF16 weights
+          } else {
+            const QW& Wm = DOWN ? a.down : (mm == 0 ? a.gate : a.up);
+            const uint8_t* sr =
+                Wm.scales + (size_t)e * scale_bytes(F, N, K) + (size_t)erow * row_scale_bytes<F>(K);
+            rf[mm] = row_factor<F>(row_ref<F>(sr, K), F == MOE_FMT_NVFP4 ? __ldg(Wm.ts + e) : 1.f);
+          }
         }
         const float tsg = DOWN ? 0.f : rf[0], tsu = DOWN ? 0.f : rf[C::NMAT - 1];
         const int buf = item & 1;
@@ -694,34 +731,41 @@ bool f16_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uin
 
 }  // namespace
 
-template <int F>
+// FS: the fold-scales lever (B operands: plain BF16 x rows and h rows).
+template <int F, bool FS>
 cudaError_t launch_pf_gemm(bool down, const PrefillArgs& a, int grid, cudaStream_t s) {
   cudaError_t err;
   alignas(64) CUtensorMap tm;
   if (down) {
-    if (!f16_map(&tm, a.h16, (uint64_t)a.I, (uint64_t)a.T * a.k, NT)) return cudaErrorInvalidValue;
-    err = cudaFuncSetAttribute(pf_gemm_kernel<F, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<F, true>::SMEM);
+    if (!f16_map(&tm, FS ? a.h : a.h16, (uint64_t)a.I, (uint64_t)a.T * a.k, NT)) return cudaErrorInvalidValue;
+    err = cudaFuncSetAttribute(pf_gemm_kernel<F, true, FS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<F, true, FS>::SMEM);
     if (err != cudaSuccess) return err;
-    pf_gemm_kernel<F, true><<<grid, kPfGemmThreads, Cfg<F, true>::SMEM, s>>>(a, tm);
+    pf_gemm_kernel<F, true, FS><<<grid, kPfGemmThreads, Cfg<F, true, FS>::SMEM, s>>>(a, tm);
   } else {
     if (!f16_map(&tm, a.xg, (uint64_t)a.H, (uint64_t)a.T * a.k, NT)) return cudaErrorInvalidValue;
-    err = cudaFuncSetAttribute(pf_gemm_kernel<F, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<F, false>::SMEM);
+    err = cudaFuncSetAttribute(pf_gemm_kernel<F, false, FS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<F, false, FS>::SMEM);
     if (err != cudaSuccess) return err;
-    pf_gemm_kernel<F, false><<<grid, kPfGemmThreads, Cfg<F, false>::SMEM, s>>>(a, tm);
+    pf_gemm_kernel<F, false, FS><<<grid, kPfGemmThreads, Cfg<F, false, FS>::SMEM, s>>>(a, tm);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_gemm(bool down, const PrefillArgs& a, int grid, cudaStream_t s) {
   switch (a.fmt) {
-    case MOE_FMT_NVFP4: return launch_pf_gemm<MOE_FMT_NVFP4>(down, a, grid, s);
-    case MOE_FMT_MXFP4: return launch_pf_gemm<MOE_FMT_MXFP4>(down, a, grid, s);
-    case MOE_FMT_INT4_G64: return launch_pf_gemm<MOE_FMT_INT4_G64>(down, a, grid, s);
-    case MOE_FMT_INT8_G64: return launch_pf_gemm<MOE_FMT_INT8_G64>(down, a, grid, s);
-    case MOE_FMT_FP8_B128: return launch_pf_gemm<MOE_FMT_FP8_B128>(down, a, grid, s);
-    case MOE_FMT_INT4_G128: return launch_pf_gemm<MOE_FMT_INT4_G128>(down, a, grid, s);
+    case MOE_FMT_NVFP4: return launch_pf_gemm<MOE_FMT_NVFP4, false>(down, a, grid, s);
+    case MOE_FMT_MXFP4: return launch_pf_gemm<MOE_FMT_MXFP4, false>(down, a, grid, s);
+    case MOE_FMT_INT4_G64: return launch_pf_gemm<MOE_FMT_INT4_G64, false>(down, a, grid, s);
+    case MOE_FMT_INT8_G64:
+      return fold_lever(a) ? launch_pf_gemm<MOE_FMT_INT8_G64, true>(down, a, grid, s)
+                           : launch_pf_gemm<MOE_FMT_INT8_G64, false>(down, a, grid, s);
+    case MOE_FMT_FP8_B128:
+      return fold_lever(a) ? launch_pf_gemm<MOE_FMT_FP8_B128, true>(down, a, grid, s)
+                           : launch_pf_gemm<MOE_FMT_FP8_B128, false>(down, a, grid, s);
+    case MOE_FMT_INT4_G128:
+      return fold_lever(a) ? launch_pf_gemm<MOE_FMT_INT4_G128, true>(down, a, grid, s)
+                           : launch_pf_gemm<MOE_FMT_INT4_G128, false>(down, a, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

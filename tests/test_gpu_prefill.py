@@ -118,6 +118,54 @@ def test_prefill_small_shapes(cfg, T):
     assert_prefill_routing(routing, ref, ref["near_midpoint"])
 
 
+# the fold-scales lever: layers with int8 g64 / FP8 b128 / int4 g128 experts, routed or shared
+FOLD = [c for c in SMALL if {c.fmt, c.shared_fmt} & {FMT_INT8_G64, FMT_FP8_B128, FMT_INT4_G128}]
+
+
+@pytest.mark.parametrize("cfg", FOLD, ids=[c.name for c in FOLD])
+@pytest.mark.parametrize("T", [1, 17, 300])
+def test_prefill_fold_scales_matches_oracle(cfg, T):
+    hl = synth.make_layer(cfg, seed=9)
+    dl = to_device(hl)
+    x = synth.make_tokens(cfg, T, seed=9, batch=T)
+    y, routing = G.decode(dl, x, prefill=True, fold_scales=1)
+    ref = M.layer_forward(hl, x, fold_scales=True)
+    _check_y(y, ref["y_bits"])
+    assert_prefill_routing(routing, ref, ref["near_midpoint"])
+
+
+def test_prefill_fold_scales_is_a_lever():
+    # on int8 routed experts the lever changes the output (not bitwise the exact chain) ...
+    cfg = next(c for c in SMALL if c.name == "p_int8_nvfp4")
+    hl = synth.make_layer(cfg, seed=10)
+    dl = to_device(hl)
+    x = synth.make_tokens(cfg, 300, seed=10, batch=3)
+    y_fold, _ = G.decode(dl, x, prefill=True, fold_scales=1)
+    y_exact, _ = G.decode(dl, x, prefill=True)
+    assert not np.array_equal(y_fold, y_exact)
+    _check_y(y_exact, M.layer_forward(hl, x)["y_bits"])
+    # ... and leaves a layer of exactly folded formats (NVFP4 routed, no shared expert) bit for bit
+    cfg2 = SMALL[2]
+    hl2 = synth.make_layer(cfg2, seed=10)
+    dl2 = to_device(hl2)
+    x2 = synth.make_tokens(cfg2, 300, seed=10, batch=4)
+    assert np.array_equal(G.decode(dl2, x2, prefill=True, fold_scales=1)[0], G.decode(dl2, x2, prefill=True)[0])
+
+
+@pytest.mark.parametrize("name,T,tokens", [("decode_int4", 384, [0, 200, 383]),
+                                           ("decode_nvfp4", 1024, [0, 511, 1023])])
+def test_prefill_fold_scales_full_size_sampled(name, T, tokens):
+    """The lever on the int4 g64 layer's int8 g64 shared expert and the NVFP4 layer's FP8 b128 shared
+    expert at full size, sampled tokens."""
+    hl = G.host_layer(name)
+    dl = G.device_layer(name)
+    x = synth.make_tokens(hl.cfg, T, seed=1, batch=T)
+    y, routing = G.decode(dl, x, prefill=True, fold_scales=1)
+    ref = M.layer_forward(hl, x, tokens=tokens, fold_scales=True)
+    _check_y(y, ref["y_bits"], tokens)
+    assert_prefill_routing(routing, ref, ref["near_midpoint"])
+
+
 @pytest.mark.parametrize("T,tokens", [(256, [0, 37, 255]), (4096, [0, 1, 2047, 4095])])
 def test_prefill_workload_matches_oracle(T, tokens):
     hl = G.host_layer("prefill_nvfp4")
