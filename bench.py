@@ -387,6 +387,9 @@ PREFILL_EXTRA = {
     # the MXFP4 and int4 g64 (+ int8 g64 shared) decode layers at the prefill workload's token count
     "prefill_mxfp4": lambda: synth.CONFIGS["decode_mxfp4"].with_(name="prefill_mxfp4", batches=(4096,)),
     "prefill_int4": lambda: synth.CONFIGS["decode_int4"].with_(name="prefill_int4", batches=(4096,)),
+    # the prefill workload's shape with AutoRound int4 g128 routed experts (the fold-scales lever's case)
+    "prefill_int4g128": lambda: synth.CONFIGS["prefill_nvfp4"].with_(name="prefill_int4g128",
+                                                                     fmt=synth.configs.FMT_INT4_G128),
 }
 
 
@@ -394,17 +397,19 @@ def prefill_config(name: str):
     return PREFILL_EXTRA[name]() if name in PREFILL_EXTRA else synth.CONFIGS[name]
 
 
-def _prefill_times(torch, q, lay, xs, T, y, ws, stream, act_quant, reps, G=6):
+def _prefill_times(torch, q, lay, xs, T, y, ws, stream, act_quant, reps, G=6, fold_scales=0):
     """Median whole-layer time (graph of G calls, `reps` replays) and per-stage event times."""
     NB = len(xs)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         for i in range(3):
-            q.moe_prefill_forward(lay, xs[i % NB], T, y, ws, stream=stream, act_quant=act_quant)
+            q.moe_prefill_forward(lay, xs[i % NB], T, y, ws, stream=stream, act_quant=act_quant,
+                                  fold_scales=fold_scales)
         stream.synchronize()
         with torch.cuda.graph(g, stream=stream):
             for i in range(G):
-                q.moe_prefill_forward(lay, xs[i % NB], T, y, ws, stream=stream, act_quant=act_quant)
+                q.moe_prefill_forward(lay, xs[i % NB], T, y, ws, stream=stream, act_quant=act_quant,
+                                  fold_scales=fold_scales)
         for _ in range(2):
             g.replay()
     torch.cuda.synchronize()
@@ -420,7 +425,8 @@ def _prefill_times(torch, q, lay, xs, T, y, ws, stream, act_quant, reps, G=6):
     gt = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gt, stream=stream):
         for i in range(n):
-            q.moe_prefill_forward_timed(lay, xs[i % NB], T, y, ws, evs[i], stream=stream, act_quant=act_quant)
+            q.moe_prefill_forward_timed(lay, xs[i % NB], T, y, ws, evs[i], stream=stream, act_quant=act_quant,
+                                        fold_scales=fold_scales)
     with torch.cuda.stream(stream):
         gt.replay()
     torch.cuda.synchronize()
@@ -433,7 +439,8 @@ def _prefill_times(torch, q, lay, xs, T, y, ws, stream, act_quant, reps, G=6):
 
 def run_prefill(args, local, peak_bf16, peak_kind, name="prefill_nvfp4", tokens=0, w4a4=True):
     """One prefill workload: whole-layer time through moe_prefill_forward, per-stage event times and the
-    grouped GEMMs' tensor throughput, for the exact chain and (NVFP4 layers) the W4A4 lever."""
+    grouped GEMMs' tensor throughput, for the exact chain, the W4A4 lever (NVFP4 and MXFP4 layers) and the
+    fold-scales lever (layers with int8 g64, FP8 b128 or int4 g128 experts)."""
     import torch
     import quantized_moe_decode_router_gb300 as q
     cfg = prefill_config(name)
@@ -518,6 +525,19 @@ def run_prefill(args, local, peak_bf16, peak_kind, name="prefill_nvfp4", tokens=
                     "down_GBps": round(dn_bytes / (dur4[5] * 1e-6) / 1e9, 1),
                     "gateup_frac_hbm": round(gu_bytes / (dur4[3] * 1e-6) / 1e9 / hbm, 4),
                     "down_frac_hbm": round(dn_bytes / (dur4[5] * 1e-6) / 1e9 / hbm, 4)}}
+    fold_fmts = (synth.configs.FMT_INT8_G64, synth.configs.FMT_FP8_B128, synth.configs.FMT_INT4_G128)
+    on = [w for w, f in (("routed", cfg.fmt), ("shared", cfg.shared_fmt)) if f in fold_fmts]
+    if on:
+        # the fold-scales lever: group scales folded into BF16 weights, one FP32 accumulator
+        usf, durf = _prefill_times(torch, q, lay, xs, T, y, ws, stream, 0, reps, G, fold_scales=1)
+        tflf = flops / ((durf[3] + durf[5]) * 1e-6) / 1e12
+        out["fold_scales"] = {
+            "path": (f"fold-scales lever (fold_scales=1) on the {' and '.join(on)} experts: bf16(code x group "
+                     f"scale) weights against BF16 tokens, one FP32 accumulator, tcgen05 kind::f16 bf16 operands"),
+            "us_per_layer": round(usf, 1), "tokens_per_s": round(T / (usf * 1e-6), 1),
+            "kernel_us": {k: round(float(v), 2) for k, v in zip(names, durf)},
+            "achieved_tflops": round(tflf, 1), "frac_f16_peak": round(tflf / peak_bf16, 4),
+            "vs_exact_chain": round(us / usf, 3)}
     return out
 
 
@@ -528,6 +548,7 @@ DATA_DESC = {
     "decode_mxfp4": "N(0,0.02) weights quantised MXFP4",
     "decode_int4": "N(0,0.02) weights quantised int4 g64 routed / int8 g64 shared",
     "prefill_nvfp4": "N(0,0.02) weights quantised NVFP4, Zipf router bias s=1.1",
+    "prefill_int4g128": "N(0,0.02) weights quantised int4 g128 (AutoRound layout), Zipf router bias s=1.1",
 }
 
 
@@ -622,8 +643,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill workload's measurement")
     ap.add_argument("--prefill-steps", type=int, default=60)
-    ap.add_argument("--more-prefill", default="prefill_mxfp4,prefill_int4",
-                    help="further prefill workloads (exact chain) measured beside prefill_nvfp4")
+    ap.add_argument("--more-prefill", default="prefill_mxfp4,prefill_int4,prefill_int4g128",
+                    help="further prefill workloads measured beside prefill_nvfp4 (the exact chain and the levers "
+                         "that apply to their formats)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="measure only the prefill workload (e.g. at a small --prefill-tokens for a profiler)")
     ap.add_argument("--prefill-tokens", type=int, default=0, help="token count of the prefill workloads (0: 4096)")

@@ -158,7 +158,28 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Bounded wait for the phase with the given parity to complete: gives up
 // (returns false) after `limit_ns` nanoseconds of the global timer or 2^26
 // polls, whichever comes first.
+// try_wait whose suspension of the thread is bounded by hint_ns nanoseconds.
+__device__ __forceinline__ bool bar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, "
+      "p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns < 1000000ull) {
+    // a short limit (under 1 ms): no single try_wait may keep the thread suspended past it
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < (1u << 26); ++i) {
+      if (bar_try_wait_hint(bar, parity, (uint32_t)limit_ns)) return true;
+      if (global_ns() - t0 > limit_ns) return false;
+    }
+    return false;
+  }
   if (bar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < (1u << 26); ++i) {
