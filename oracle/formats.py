@@ -198,7 +198,11 @@ def e2m1_encode_rne(y: np.ndarray) -> np.ndarray:
 
 
 def e4m3_encode_rne_sat(y: np.ndarray) -> np.ndarray:
-    """Nearest E4M3 code (ties to even mantissa), saturating at +-448."""
+    """Nearest E4M3 code (ties to even mantissa), saturating at +-448.
+
+    The sign bit is the sign bit of y (IEEE signbit), so a negative value that
+    rounds to zero is the -0 code 0x80, as in the IEEE conversions.
+    """
     y = np.asarray(y, dtype=np.float64)
     pos = E4M3_TABLE[:127]                             # codes 0..126: 0 .. 448, increasing
     a = np.minimum(np.abs(y), 448.0)
@@ -208,4 +212,4 @@ def e4m3_encode_rne_sat(y: np.ndarray) -> np.ndarray:
     pick_hi = (hi - a < a - lo) | ((hi - a == a - lo) & (idx % 2 == 0))
     code = np.where(a == hi, idx, np.where(pick_hi, idx, idx - 1)).astype(np.uint8)
     code = np.where(a == 0.0, 0, code).astype(np.uint8)
-    return np.where((y < 0) & (code != 0), code | 0x80, code).astype(np.uint8)
+    return np.where(np.signbit(y), code | 0x80, code).astype(np.uint8)

@@ -185,11 +185,19 @@ def silu(z: np.ndarray) -> np.ndarray:
         return z / (1.0 + np.exp(-z))
 
 
+# activation quantisers of the levers: the W4A4 lever's NVFP4 (1) and MXFP4 (2) blocks, and the
+# FP8-activation lever's per-token 1x128 E4M3 blocks (3, applied to FP8 b128 experts only)
+ACT_FP8 = 3
+
+
 def act_fake_quant(a: np.ndarray, act_quant: int) -> np.ndarray:
-    """The W4A4 lever's activation quantiser: act_quant 1 (or True) = NVFP4
-    16-element blocks, 2 = MXFP4 32-element blocks; 0 = none."""
+    """The levers' activation quantiser: act_quant 1 (or True) = NVFP4
+    16-element blocks, 2 = MXFP4 32-element blocks, 3 = E4M3 128-element
+    blocks (``fp8_quantize_act``); 0 = none."""
     if not act_quant:
         return a
+    if int(act_quant) == ACT_FP8:
+        return fp8_fake_quant(a)
     return mxfp4_fake_quant(a) if int(act_quant) == 2 else nvfp4_fake_quant(a)
 
 
@@ -199,8 +207,8 @@ def swiglu_mlp(Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray, X: np.ndarray,
 
     Returns (h, P): h = bf16(silu(X Wg^T) * (X Wu^T)) [n, I] as FP64 values,
     P = h Wd^T [n, H] in FP64.  With act_quant the token rows and h are
-    replaced by their quantised values (NVFP4 for 1, MXFP4 for 2) before each
-    projection.
+    replaced by their quantised values (NVFP4 for 1, MXFP4 for 2, E4M3 1x128
+    blocks for 3) before each projection.
     """
     X = act_fake_quant(X, act_quant)
     g = X @ Wg.T
@@ -276,6 +284,43 @@ def mxfp4_fake_quant(a: np.ndarray) -> np.ndarray:
     return mxfp4_dequantize_act(*mxfp4_quantize_act(a))
 
 
+# ---------------------------------------------- FP8 activation lever ----
+
+E4M3_MAX = 448.0
+
+
+def fp8_quantize_act(a: np.ndarray):
+    """Per-token 1x128 E4M3 quantisation of activation rows.
+
+    DGPP README "Execution and performance" table, row engine.prefill_fp8_gemm:
+    FP8 projections run on the fp8 tensor cores from per-token 1x128 e4m3
+    activations against the checkpoint's 128x128 weight scales.  Reading: per
+    128-element block of a row, the FP32 scale s = fl32(amax / 448) (448 the
+    largest finite E4M3 value; amax = 0 gives s = 0 and zero codes) and
+    code = e4m3_rne_sat( fl32(a / s) ), both quotients IEEE FP32 divisions as
+    a kernel computes them.  Returns (codes [.., K] u8, scales [.., K/128] f32).
+    """
+    a = np.asarray(a, dtype=np.float64)
+    *lead, K = a.shape
+    blk = a.reshape(*lead, K // 128, 128)
+    amax = np.abs(blk).max(axis=-1)
+    s = (amax.astype(np.float32) / np.float32(E4M3_MAX)).astype(np.float32)   # amax: BF16 values, exact in FP32
+    pos = s > 0
+    q = (blk.astype(np.float32) / np.where(pos, s, np.float32(1.0))[..., None]).astype(np.float64)
+    codes = np.where(pos[..., None], F.e4m3_encode_rne_sat(q), 0)   # a zero block: +0 codes
+    return codes.reshape(*lead, K).astype(np.uint8), s
+
+
+def fp8_dequantize_act(codes: np.ndarray, s: np.ndarray) -> np.ndarray:
+    *lead, K = codes.shape
+    v = F.E4M3_TABLE[codes].reshape(*lead, K // 128, 128) * np.asarray(s, dtype=np.float64)[..., None]
+    return v.reshape(*lead, K)
+
+
+def fp8_fake_quant(a: np.ndarray) -> np.ndarray:
+    return fp8_dequantize_act(*fp8_quantize_act(a))
+
+
 # ------------------------------------------------------------------ layer ----
 
 def _decoded(qm, e, fold_scales: bool = False):
@@ -284,7 +329,7 @@ def _decoded(qm, e, fold_scales: bool = False):
 
 def layer_forward(layer, x_bits: np.ndarray, act_quant: int = 0, tokens=None, expert_cache=None,
                   bias_select: bool = False, bf16_partials: bool = False, routing=None,
-                  fold_scales: bool = False):
+                  fold_scales: bool = False, fp8_act: bool = False):
     """Full MoE layer on host-resident checkpoint data (a synth.HostLayer).
 
     tokens: optional subset of token rows whose outputs are wanted (routing is
@@ -307,6 +352,10 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: int = 0, tokens=None, ex
     int8 g64, FP8 b128 and int4 g128 weights, routed and shared, enter as
     bf16(fl32(code * scale)); the rest of the chain is unchanged.  An
     ``expert_cache`` must then supply the folded weights itself.
+    fp8_act: the FP8-activation lever (``fp8_quantize_act``): FP8 b128 experts,
+    routed or shared, see their token rows and h (after its BF16 rounding) as
+    per-token 1x128 E4M3 blocks; their weights stay exact (the lever takes
+    precedence over fold_scales for them).  Other experts are unchanged.
     Returns a dict of every intermediate the CUDA path exposes.
     """
     cfg = layer.cfg
@@ -319,6 +368,10 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: int = 0, tokens=None, ex
         w = np.asarray(routing[1], dtype=np.float32)
         l32, near = None, np.zeros((T, cfg.E), dtype=bool)
     cnt, off, pair = dispatch(idx, cfg.E)
+    fp8_r = bool(fp8_act) and cfg.fmt == F.FMT_FP8_B128
+    fp8_s = bool(fp8_act) and cfg.shared_fmt == F.FMT_FP8_B128
+    aq_r = ACT_FP8 if fp8_r else act_quant
+    aq_s = ACT_FP8 if fp8_s else act_quant
     want = np.arange(T) if tokens is None else np.asarray(sorted(set(int(t) for t in tokens)))
     X = F.bf16_to_f64(x_bits)
     acc = {int(t): np.zeros(cfg.H) for t in want}
@@ -331,10 +384,10 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: int = 0, tokens=None, ex
         if expert_cache is not None:
             Wg, Wu, Wd = expert_cache(e)
         else:
-            Wg, Wu, Wd = (_decoded(layer.gate, e, fold_scales), _decoded(layer.up, e, fold_scales),
-                          _decoded(layer.down, e, fold_scales))
+            fr = fold_scales and not fp8_r
+            Wg, Wu, Wd = _decoded(layer.gate, e, fr), _decoded(layer.up, e, fr), _decoded(layer.down, e, fr)
         rows = np.array([p // cfg.k for p in ps])
-        h, P = swiglu_mlp(Wg, Wu, Wd, X[rows], act_quant)
+        h, P = swiglu_mlp(Wg, Wu, Wd, X[rows], aq_r)
         if bf16_partials:
             P = F.round_bf16(P)
         for i, p in enumerate(ps):
@@ -343,9 +396,10 @@ def layer_forward(layer, x_bits: np.ndarray, act_quant: int = 0, tokens=None, ex
             h_out[p] = h[i]
     S = None
     if layer.shared_gate is not None:
-        Wg, Wu, Wd = (_decoded(layer.shared_gate, 0, fold_scales), _decoded(layer.shared_up, 0, fold_scales),
-                      _decoded(layer.shared_down, 0, fold_scales))
-        _, S = swiglu_mlp(Wg, Wu, Wd, X[want], act_quant)
+        fs = fold_scales and not fp8_s
+        Wg, Wu, Wd = (_decoded(layer.shared_gate, 0, fs), _decoded(layer.shared_up, 0, fs),
+                      _decoded(layer.shared_down, 0, fs))
+        _, S = swiglu_mlp(Wg, Wu, Wd, X[want], aq_s)
         if bf16_partials:
             S = F.round_bf16(S)
         gw = getattr(layer, "extra", {}).get("shared_gate_w")

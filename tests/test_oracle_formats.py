@@ -295,6 +295,11 @@ def test_oracle_e4m3_encoder_matches_torch():
     ref = torch.from_numpy(v[inr]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(codes[inr], ref)
     assert np.all(codes[~inr] == 0x7E)                    # saturation
+    # negative values, including ones that round to -0 (code 0x80)
+    w = -np.concatenate([v[inr][:5000], 2.0 ** rng.uniform(-14, -9, 2000).astype(np.float32)])
+    ref_n = torch.from_numpy(w).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(F.e4m3_encode_rne_sat(w.astype(np.float64)), ref_n)
+    assert np.any(ref_n == 0x80)
 
 
 # ------------------------------------------------------ fold-scales lever ----

@@ -294,6 +294,118 @@ def test_mxfp4_act_quantizer_pins():
     assert np.array_equal((codes_c & 8)[nz], (q & 8)[nz])                  # signs of the non-zero codes
 
 
+def _torch_fp8_quant(A: torch.Tensor):
+    """Per-token 1x128 E4M3 codes and FP32 scales, written with torch float32 arithmetic and torch's own
+    float -> float8_e4m3fn cast (an independent E4M3 encoder): s = amax / 448, code = e4m3(a / s)."""
+    *lead, K = A.shape
+    a32 = A.to(torch.float32).reshape(*lead, K // 128, 128)
+    s = a32.abs().amax(dim=-1) / 448.0
+    q = a32 / torch.where(s > 0, s, torch.ones_like(s))[..., None]
+    codes = q.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    codes = torch.where((s > 0)[..., None], codes, torch.zeros_like(codes))
+    return codes.reshape(*lead, K), s
+
+
+def _fp8_pin_failures(quant=None) -> int:
+    """Mismatches of the oracle's FP8 activation quantiser against the torch version, over random BF16
+    rows at many magnitudes and hand-made blocks (zeros, one non-zero, values on the E4M3 grid, tiny
+    values that land on E4M3 subnormal codes)."""
+    quant = quant or M.fp8_quantize_act
+    rng = np.random.default_rng(33)
+    A = F.round_bf16(rng.standard_normal((40, 384)) * np.exp(rng.uniform(-20, 20, (40, 1))))
+    A[0, :128] = 0.0
+    A[1, :128] = 0.0
+    A[1, 77] = -3.5
+    A[2, :128] = F.round_bf16(F.E4M3_TABLE[np.arange(128) % 126] * 2.0 ** -3)   # every magnitude on the grid
+    A[3, :128] = F.round_bf16(rng.standard_normal(128) * 1e-3)
+    A[3, 5] = 40.0                                                                # small codes, subnormals
+    codes, s = quant(A)
+    tc, ts = _torch_fp8_quant(torch.from_numpy(A))
+    bad = int(np.sum(codes != tc.numpy())) + int(np.sum(s.view(np.uint32) != ts.numpy().view(np.uint32)))
+    return bad
+
+
+def test_fp8_act_quantizer_pins():
+    assert _fp8_pin_failures() == 0
+    rng = np.random.default_rng(34)
+    A = F.round_bf16(rng.standard_normal((16, 256)) * np.exp(rng.uniform(-8, 8, (16, 1))))
+    codes, s = M.fp8_quantize_act(A)
+    D = M.fp8_dequantize_act(codes, s)
+    blk = lambda v: v.reshape(16, 2, 128)
+    # each block's largest magnitude takes the largest code (+-448), so it comes back to 448 s
+    assert np.array_equal(np.abs(blk(D)).max(axis=-1), 448.0 * s.astype(np.float64))
+    # every value within half an E4M3 step: 2^-4 relative, or 2^-10 s on the subnormal grid
+    assert np.all(np.abs(D - A) <= np.maximum(2.0 ** -4 * np.abs(A), np.repeat(s, 128, axis=1) * 2.0 ** -10))
+    # zero block: zero scale and codes
+    c0, s0 = M.fp8_quantize_act(np.zeros((1, 128)))
+    assert s0[0, 0] == 0 and np.all(c0 == 0)
+
+
+def _fp8_scale_240(a):
+    # wrong: the E4M3 "fnuz" maximum 240 instead of 448
+    return _fp8_scaled(a, 240.0)
+
+
+def _fp8_scaled(a, top):
+    a = np.asarray(a, dtype=np.float64)
+    *lead, K = a.shape
+    blk = a.reshape(*lead, K // 128, 128)
+    s = (np.abs(blk).max(axis=-1).astype(np.float32) / np.float32(top)).astype(np.float32)
+    q = (blk.astype(np.float32) / np.where(s > 0, s, 1)[..., None]).astype(np.float64)
+    return np.where((s > 0)[..., None], F.e4m3_encode_rne_sat(q), 0).reshape(*lead, K).astype(np.uint8), s
+
+
+def _fp8_truncating(a):
+    _, s = _ORIG["fp8"](a)
+    a = np.asarray(a, dtype=np.float64)
+    *lead, K = a.shape
+    q = (a.reshape(*lead, K // 128, 128).astype(np.float32) / np.where(s > 0, s, 1)[..., None]).astype(np.float64)
+    # wrong: round toward zero on the E4M3 grid
+    mag = np.abs(q).reshape(-1)
+    grid = F.E4M3_TABLE[:127]
+    idx = np.clip(np.searchsorted(grid, mag, side="right") - 1, 0, 126)
+    tc = np.where(q.reshape(-1) < 0, idx | 0x80, idx).astype(np.uint8)
+    tc = np.where(idx == 0, 0, tc)
+    return np.where((s > 0)[..., None], tc.reshape(q.shape), 0).reshape(*lead, K).astype(np.uint8), s
+
+
+def _torch_fp8_fake(A: torch.Tensor) -> torch.Tensor:
+    codes, s = _torch_fp8_quant(A)
+    v = codes.view(torch.float8_e4m3fn).to(torch.float64).reshape(*A.shape[:-1], A.shape[-1] // 128, 128)
+    return (v * s.to(torch.float64)[..., None]).reshape(A.shape)
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_fp8_act_lever_equals_quantised_mlp(shared):
+    # an FP8 b128 expert (routed, or the shared expert beside an NVFP4 routed one) under the lever: x and
+    # h (after its BF16 rounding) quantised by the torch E4M3 version, exact weights
+    fmt, sfmt = (FMT_NVFP4, FMT_FP8_B128) if shared else (FMT_FP8_B128, 0)
+    cfg = _small(fmt, sfmt, E=1, k=1, H=256, I=128)
+    lay = synth.make_layer(cfg, seed=16)
+    x = synth.make_tokens(cfg, 5, seed=16)
+    out = M.layer_forward(lay, x, fp8_act=True)
+    X = torch.from_numpy(F.bf16_to_f64(x))
+
+    def mlp_fp8(Wg, Wu, Wd):
+        Xq = _torch_fp8_fake(X)
+        h = (torch.nn.functional.silu(Xq @ Wg.T) * (Xq @ Wu.T)).to(torch.float32).to(torch.bfloat16)
+        return _torch_fp8_fake(h.to(torch.float64)) @ Wd.T
+
+    if shared:
+        y_ref = (_torch_mlp(_torch_decode(lay.gate), _torch_decode(lay.up), _torch_decode(lay.down), X)
+                 + mlp_fp8(_torch_decode(lay.shared_gate), _torch_decode(lay.shared_up), _torch_decode(lay.shared_down)))
+    else:
+        y_ref = mlp_fp8(_torch_decode(lay.gate), _torch_decode(lay.up), _torch_decode(lay.down))
+    ok = M.within_tolerance(F.bf16_to_f64(out["y_bits"]), y_ref.numpy(), ulps=1.0, abs_tol=1e-6)
+    assert ok.all(), np.abs(F.bf16_to_f64(out["y_bits"]) - y_ref.numpy()).max()
+    assert not np.array_equal(out["y_f64"], M.layer_forward(lay, x)["y_f64"])
+    # NVFP4 experts are untouched by the lever
+    if shared:
+        lay_ns = synth.HostLayer(cfg.with_(shared_fmt=0, shared_I=0), lay.seed, lay.router_w, lay.router_b,
+                                 lay.gate, lay.up, lay.down)
+        assert np.array_equal(M.layer_forward(lay_ns, x, fp8_act=True)["y_f64"], M.layer_forward(lay_ns, x)["y_f64"])
+
+
 def _torch_mxfp4_fake_quant(A: torch.Tensor) -> torch.Tensor:
     """MXFP4 quantise-dequantise of BF16-valued rows in 32-element blocks, written independently of
     the oracle: the exponent as ceil(log2(amax / 6)) in float64 (exact at the powers of two), the
@@ -470,7 +582,7 @@ def _mxfp4_exponent_low(a):
 
 _ORIG = {"dispatch": M.dispatch, "decode": F.decode, "swiglu": M.swiglu_mlp, "router_logits": M.router_logits,
          "route": M.route, "shared_gate": M.shared_gate, "layer_forward": M.layer_forward,
-         "act_fake_quant": M.act_fake_quant}
+         "act_fake_quant": M.act_fake_quant, "fp8": M.fp8_quantize_act}
 
 
 def test_planted_mistakes_are_caught(monkeypatch):
@@ -512,6 +624,12 @@ def test_planted_mistakes_are_caught(monkeypatch):
                                            [(test_sigmoid_gated_shared_expert,)]),
         "bf16 partials not rounded": (M, "layer_forward", lambda *a, **kw: _ORIG["layer_forward"](
             *a, **{**kw, "bf16_partials": False}), [(test_bf16_partials_round_each_expert_output,)]),
+        "FP8 activations: scale from 240 (E4M3 fnuz) instead of 448": (
+            M, "fp8_quantize_act", _fp8_scale_240, [(test_fp8_act_quantizer_pins,)]),
+        "FP8 activations: truncated instead of nearest-even": (
+            M, "fp8_quantize_act", _fp8_truncating, [(test_fp8_act_quantizer_pins,)]),
+        "FP8 lever: h not re-quantised": (M, "act_fake_quant", lambda a, aq: _ORIG["act_fake_quant"](
+            a, aq) if aq != M.ACT_FP8 or a.shape[-1] != 128 else a, [(test_fp8_act_lever_equals_quantised_mlp, False)]),
         "shared expert dropped": (M, "swiglu_mlp", lambda Wg, Wu, Wd, X, act_quant=False: (
             lambda h, P: (h, P * (Wg.shape[0] != 128)))(*_ORIG["swiglu"](Wg, Wu, Wd, X, act_quant)),
             [(test_shared_expert_adds_plain_mlp, FMT_FP8_B128)]),
