@@ -151,7 +151,18 @@ typedef struct {
    * and are unchanged by it.  The decode entry points return
    * MOE_ERR_UNSUPPORTED when it is set. */
   int32_t fold_scales;
-  int32_t reserved[4];       /* must be zero */
+  /* 0 (default): the exact chain.  1: the FP8-activation lever (prefill
+   * only; DGPP README "Execution and performance", engine.prefill_fp8_gemm):
+   * FP8 b128 experts, routed or shared, meet per-token 1x128 E4M3
+   * activations on FP8 tensor cores: x, and h after its BF16 rounding, are
+   * quantised per 128-element block with scale fl32(amax / 448) and codes
+   * e4m3_rne_sat(fl32(v / scale)), and each 128-K group's products are scaled
+   * by weight scale x activation scale in FP32.  Not bitwise the default
+   * chain.  For FP8 b128 experts it takes precedence over fold_scales; other
+   * formats are unchanged by it.  The decode entry points return
+   * MOE_ERR_UNSUPPORTED when it is set. */
+  int32_t fp8_act;
+  int32_t reserved[3];       /* must be zero */
 } moe_options;
 
 /* Largest token count moe_decode_forward accepts. */

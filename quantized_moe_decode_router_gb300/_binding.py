@@ -46,7 +46,7 @@ class moe_layer(ctypes.Structure):
 
 class moe_options(ctypes.Structure):
     _fields_ = [("act_quant", ctypes.c_int32), ("bf16_partials", ctypes.c_int32), ("wait_limit_us", ctypes.c_int32),
-                ("fold_scales", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+                ("fold_scales", ctypes.c_int32), ("fp8_act", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 class moe_ws_layout(ctypes.Structure):
@@ -187,8 +187,9 @@ class Layer:
                          self.bias_select)
 
 
-def _opts(act_quant: int = 0, bf16_partials: int = 0, wait_limit_us: int = 0, fold_scales: int = 0):
-    return moe_options(act_quant, bf16_partials, wait_limit_us, fold_scales, (ctypes.c_int32 * 4)())
+def _opts(act_quant: int = 0, bf16_partials: int = 0, wait_limit_us: int = 0, fold_scales: int = 0,
+          fp8_act: int = 0):
+    return moe_options(act_quant, bf16_partials, wait_limit_us, fold_scales, fp8_act, (ctypes.c_int32 * 3)())
 
 
 def workspace_size(layer: Layer, max_tokens: int, act_quant: int = 0) -> int:
@@ -225,8 +226,9 @@ def moe_route(layer: Layer, x, T: int, topk_idx=None, topk_w=None, expert_cnt=No
 
 
 def moe_decode_forward(layer: Layer, x, T: int, y, ws, stream=None, act_quant: int = 0,
-                       raise_on_error: bool = True, bf16_partials: int = 0, fold_scales: int = 0) -> int:
-    lc, o = layer.c(), _opts(act_quant, bf16_partials, 0, fold_scales)
+                       raise_on_error: bool = True, bf16_partials: int = 0, fold_scales: int = 0,
+                       fp8_act: int = 0) -> int:
+    lc, o = layer.c(), _opts(act_quant, bf16_partials, 0, fold_scales, fp8_act)
     st = load().moe_decode_forward(ctypes.byref(lc), _ptr(x), T, _ptr(y), ctypes.byref(o), _ptr(ws),
                                    0 if ws is None else ws.numel() * ws.element_size(), _stream_handle(stream))
     return _check(st, "moe_decode_forward") if raise_on_error else st
@@ -261,17 +263,17 @@ def moe_decode_forward_noalloc(layer: Layer, x, T: int, y, stream=None, raise_on
 
 def moe_prefill_forward(layer: Layer, x, T: int, y, ws, stream=None, act_quant: int = 0,
                         raise_on_error: bool = True, bf16_partials: int = 0, wait_limit_us: int = 0,
-                        fold_scales: int = 0) -> int:
-    lc, o = layer.c(), _opts(act_quant, bf16_partials, wait_limit_us, fold_scales)
+                        fold_scales: int = 0, fp8_act: int = 0) -> int:
+    lc, o = layer.c(), _opts(act_quant, bf16_partials, wait_limit_us, fold_scales, fp8_act)
     st = load().moe_prefill_forward(ctypes.byref(lc), _ptr(x), T, _ptr(y), ctypes.byref(o), _ptr(ws),
                                     0 if ws is None else ws.numel() * ws.element_size(), _stream_handle(stream))
     return _check(st, "moe_prefill_forward") if raise_on_error else st
 
 
 def moe_prefill_forward_timed(layer: Layer, x, T: int, y, ws, events, stream=None, act_quant: int = 0,
-                              bf16_partials: int = 0, fold_scales: int = 0) -> int:
+                              bf16_partials: int = 0, fold_scales: int = 0, fp8_act: int = 0) -> int:
     """moe_prefill_forward recording torch.cuda.Event objects (8, or None entries) between its kernels."""
-    lc, o = layer.c(), _opts(act_quant, bf16_partials, 0, fold_scales)
+    lc, o = layer.c(), _opts(act_quant, bf16_partials, 0, fold_scales, fp8_act)
     arr = (ctypes.c_void_p * 8)(*[None if e is None else int(e.cuda_event) for e in events])
     st = load().moe_prefill_forward_timed(ctypes.byref(lc), _ptr(x), T, _ptr(y), ctypes.byref(o), _ptr(ws),
                                           ws.numel() * ws.element_size(), _stream_handle(stream), arr)

@@ -140,7 +140,8 @@ int32_t check_options(const moe_options* o) {
   if (o->bf16_partials != 0 && o->bf16_partials != 1) return MOE_ERR_INVALID_ARG;
   if (o->wait_limit_us < 0) return MOE_ERR_INVALID_ARG;
   if (o->fold_scales != 0 && o->fold_scales != 1) return MOE_ERR_INVALID_ARG;
-  for (int i = 0; i < 4; ++i)
+  if (o->fp8_act != 0 && o->fp8_act != 1) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i)
     if (o->reserved[i] != 0) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
@@ -550,7 +551,7 @@ int32_t qmoe::check_decode_args(const moe_layer* layer, const void* x, int32_t T
   int32_t st = check_layer(layer);
   if (st != MOE_OK) return st;
   if ((st = check_options(opts)) != MOE_OK) return st;
-  if (opts && (opts->act_quant || opts->fold_scales)) return MOE_ERR_UNSUPPORTED;  // prefill-only levers
+  if (opts && (opts->act_quant || opts->fold_scales || opts->fp8_act)) return MOE_ERR_UNSUPPORTED;  // prefill levers
   if (!x || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y)) return MOE_ERR_MISALIGNED;
   if (T < 1) return MOE_ERR_INVALID_ARG;
@@ -650,6 +651,7 @@ static int32_t prefill_forward_checked(const moe_layer* layer, const void* x, in
   pa.wait_ns = wait_limit_ns(opts);
   pa.p_bf16 = (opts && opts->bf16_partials) ? 1 : 0;
   pa.fold_scales = (opts && opts->fold_scales) ? 1 : 0;
+  pa.fp8_act = (opts && opts->fp8_act) ? 1 : 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   MarkCtx mc{events, s, false};
   if (events) {

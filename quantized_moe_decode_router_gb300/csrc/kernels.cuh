@@ -156,6 +156,8 @@ struct PrefillArgs {
   uint64_t wait_ns;     // limit of every bounded device wait (nanoseconds)
   int p_bf16;           // 1: the down GEMM writes P as BF16 (the bf16-partials lever)
   int fold_scales;      // 1: the fold-scales lever (int8 g64 / FP8 b128 / int4 g128 blocks, see fold_lever)
+  int fp8_act;          // 1: the FP8-activation lever (FP8 b128 blocks, see fp8_lever)
+  const float* asc;     // FP8-activation lever: the B operand's per-row 1x128 scales (set per GEMM launch)
   // NVFP4 W4A4 lever (act_quant = 1)
   int act_quant;
   uint8_t* xq;          // [T, H/2] E2M1 codes of x (16-element blocks)
@@ -177,12 +179,27 @@ struct PrefillArgs {
   int dense_T;          // > 0: this argument block is the shared expert's (tiles of NT consecutive tokens)
 };
 
+// The FP8-activation lever applies to this argument block (routed or shared):
+// FP8 b128 weights meet per-token 1x128 E4M3 activations (x, then h) on
+// kind::f8f6f4 MMAs, with the weight and activation block scales applied per
+// 128-K group in FP32.  It takes precedence over the fold-scales lever.
+__host__ __device__ inline bool fp8_lever(const PrefillArgs& a) {
+  return a.fp8_act != 0 && a.fmt == MOE_FMT_FP8_B128;
+}
+
 // The fold-scales lever applies to this argument block (routed or shared):
 // int8 g64, FP8 b128 and int4 g128 weights enter the GEMMs as bf16(code x
 // group scale) with plain BF16 tokens and one FP32 accumulator.
 __host__ __device__ inline bool fold_lever(const PrefillArgs& a) {
-  return a.fold_scales != 0 &&
+  return a.fold_scales != 0 && !fp8_lever(a) &&
          (a.fmt == MOE_FMT_INT8_G64 || a.fmt == MOE_FMT_FP8_B128 || a.fmt == MOE_FMT_INT4_G128);
+}
+
+// FP8-activation lever: the E4M3 codes of a B operand occupy the first rows x K
+// bytes of its f16 buffer (xg / h16), the FP32 block scales [rows, K/128]
+// follow them (K is a multiple of 128, so they stay 16-byte aligned).
+__host__ __device__ inline float* fp8_scales_after(void* codes, size_t rows, int K) {
+  return reinterpret_cast<float*>(static_cast<uint8_t*>(codes) + rows * (size_t)K);
 }
 
 // Optional host callback between launches (event records of the timed entry

@@ -17,6 +17,8 @@
 // The scan also emits the GEMM tile list: consecutive runs of at most
 // kPfTokTile sorted positions of one expert (DGPP README "Execution and
 // performance", engine.expert_tile_list).
+#include <cuda_fp8.h>
+
 #include "kernels.cuh"
 
 namespace qmoe {
@@ -257,6 +259,60 @@ __global__ void __launch_bounds__(32) pf_place_kernel(PrefillArgs a) {
 // t the token of the pair placed at pos (a contiguous copy per expert segment,
 // so the gate/up GEMM loads its token tiles as plain 2-D boxes).  For the
 // shared expert's argument block (dense_T > 0) position = token.
+// Per-token 1x128 E4M3 quantisation of one BF16 row (the FP8-activation
+// lever): per 128-element block s = amax / 448 and code = e4m3_rne_sat(v / s),
+// both IEEE FP32 divisions (a negative value that rounds to zero keeps its
+// sign: code 0x80); a zero block has scale 0 and +0 codes.  One warp, four
+// elements per lane and block.
+__device__ void quant_row_fp8(const uint16_t* src, int K, uint8_t* codes, float* scales, int lane) {
+  for (int b = 0; b < K / 128; ++b) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src + b * 128) + lane);
+    const float v[4] = {bf16_bits_to_float(w.x & 0xFFFF), bf16_bits_to_float(w.x >> 16),
+                        bf16_bits_to_float(w.y & 0xFFFF), bf16_bits_to_float(w.y >> 16)};
+    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const float sc = __fdiv_rn(m, 448.0f);
+    uint32_t out = 0;
+    if (sc > 0.f) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float q = __fdiv_rn(v[i], sc);
+        uint32_t c = (uint32_t)__nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3) & 0xFFu;
+        c |= (__float_as_uint(q) >> 24) & 0x80u;  // the sign, also of a value that rounds to zero
+        out |= c << (8 * i);
+      }
+    }
+    reinterpret_cast<uint32_t*>(codes + b * 128)[lane] = out;
+    if (lane == 0) scales[b] = sc;
+  }
+}
+
+// The FP8-activation lever's token operand: one warp per sorted position (or
+// token, dense) quantises the token's BF16 row into E4M3 codes and scales.
+__global__ void __launch_bounds__(kThreads) pf_gather_fp8_kernel(PrefillArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int pos = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  const int rows = a.T * a.k;
+  if (pos >= rows) return;
+  const int t = a.dense_T ? pos : a.rb.pair[pos] / a.k;
+  uint8_t* codes = reinterpret_cast<uint8_t*>(a.xg);
+  quant_row_fp8(a.x + (size_t)t * a.H, a.H, codes + (size_t)pos * a.H,
+                fp8_scales_after(codes, rows, a.H) + (size_t)pos * (a.H / 128), lane);
+}
+
+// The FP8-activation lever's h operand: each h row (BF16, after the gate/up
+// epilogue) quantised into E4M3 codes and scales in the h16 buffer.
+__global__ void __launch_bounds__(kThreads) pf_hquant_fp8_kernel(PrefillArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int pos = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  const int rows = a.T * a.k;
+  if (pos >= rows) return;
+  uint8_t* codes = reinterpret_cast<uint8_t*>(a.h16);
+  quant_row_fp8(a.h + (size_t)pos * a.I, a.I, codes + (size_t)pos * a.I,
+                fp8_scales_after(codes, rows, a.I) + (size_t)pos * (a.I / 128), lane);
+}
+
 __global__ void __launch_bounds__(kThreads) pf_gather_kernel(PrefillArgs a) {
   const int lane = threadIdx.x & 31;
   const int pos = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
@@ -429,7 +485,8 @@ cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s, Marks mk)
     if (e2 != cudaSuccess) return e2;
     pf_gather_q_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
   } else if (a.xg) {
-    pf_gather_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
+    if (fp8_lever(a)) pf_gather_fp8_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
+    else pf_gather_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
   }
   mk(3);
   return cudaGetLastError();
@@ -454,7 +511,8 @@ cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s
     sa.fmt = a.sfmt; sa.I = a.Is; sa.E = 1; sa.k = 1; sa.dense_T = a.T;
     sa.gate = a.s_gate; sa.up = a.s_up; sa.down = a.s_down;
     sa.xg = a.xs16; sa.h = a.hs; sa.h16 = a.hs16; sa.hsig = a.hssig; sa.P = a.S;
-    pf_gather_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(sa);
+    if (fp8_lever(sa)) pf_gather_fp8_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(sa);
+    else pf_gather_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(sa);
     if (a.sgate_w) pf_sgate_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
@@ -462,9 +520,12 @@ cudaError_t launch_prefill_experts(const PrefillArgs& a, int sms, cudaStream_t s
   if (err != cudaSuccess) return err;
   if (a.sfmt && (err = launch_prefill_gemm(false, sa, sms, s)) != cudaSuccess) return err;
   mk(4);
-  // h -> f16 with a power-of-two row scale (the down GEMM's B); the fold-scales lever reads h as it is
-  if (!fold_lever(a)) pf_hconv_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
-  if (a.sfmt && !fold_lever(sa)) pf_hconv_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(sa);
+  // h -> f16 with a power-of-two row scale (the down GEMM's B); the fold-scales lever reads h as it is,
+  // the FP8-activation lever quantises it to E4M3 blocks
+  if (fp8_lever(a)) pf_hquant_fp8_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
+  else if (!fold_lever(a)) pf_hconv_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
+  if (a.sfmt && fp8_lever(sa)) pf_hquant_fp8_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(sa);
+  else if (a.sfmt && !fold_lever(sa)) pf_hconv_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(sa);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   mk(5);
   if ((err = launch_prefill_gemm(true, a, sms, s)) != cudaSuccess) return err;

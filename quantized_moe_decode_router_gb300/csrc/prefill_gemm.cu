@@ -64,24 +64,31 @@ constexpr bool promote_fmt() {
   return F == MOE_FMT_INT8_G64 || F == MOE_FMT_FP8_B128 || F == MOE_FMT_INT4_G128;
 }
 
-// FS: the fold-scales lever on a promote format: each code times its group
-// scale is rounded to one BF16 weight (FP32 product, then BF16), the tokens
-// enter as plain BF16, one FP32 accumulator runs across K.
-template <int F, bool DOWN, bool FS = false>
+// LV selects a lever.  1, fold scales (promote formats): each code times its
+// group scale is rounded to one BF16 weight (FP32 product, then BF16), the
+// tokens enter as plain BF16, one FP32 accumulator runs across K.  2, FP8
+// activations (FP8 b128): the E4M3 weight codes and per-token 1x128 E4M3
+// activation codes meet on kind::f8f6f4 MMAs (K = 128 per step, one step per
+// scale group), the weight and activation scales applied per group in FP32.
+template <int F, bool DOWN, int LV = 0>
 struct Cfg {
+  static constexpr bool FS = LV == 1;
+  static constexpr bool F8 = LV == 2;
   static_assert(!FS || promote_fmt<F>(), "the fold-scales lever applies to the promote formats");
+  static_assert(!F8 || F == MOE_FMT_FP8_B128, "the FP8-activation lever applies to FP8 b128 weights");
   static constexpr bool PROMOTE = promote_fmt<F>() && !FS;
   static constexpr int BITS = (F == MOE_FMT_INT8_G64 || F == MOE_FMT_FP8_B128) ? 8 : 4;
-  static constexpr int GS = F == MOE_FMT_INT8_G64 ? 1 : 2;  // K steps per scale group (promote formats)
+  static constexpr int KSTEP = F8 ? 128 : BK;   // K per step (128 bytes of an A row either way)
+  static constexpr int GS = (F8 || F == MOE_FMT_INT8_G64) ? 1 : 2;  // K steps per scale group (promote)
   static constexpr int NMAT = DOWN ? 1 : 2;
-  static constexpr int SA = 2;                  // decoded-weight (A) stages
+  static constexpr int SA = F8 ? 4 : 2;         // A stages (F8: copied straight in, no raw ring)
   static constexpr int SB = 4;                  // token-row (B) stages: TMA latency spans several steps
   static constexpr int TPR = kDec / (NMAT * BM);  // decode threads per weight row
-  static constexpr int KT = BK / TPR;             // columns per decode thread per step
+  static constexpr int KT = KSTEP / TPR;          // columns per decode thread per step
   static constexpr int CODE_BYTES = KT * BITS / 8;               // per thread per step
   // fold: the codes, then the step's scale word (padded); promote and FS: the codes only
   static constexpr int RAW_BYTES = (PROMOTE || FS) ? CODE_BYTES : CODE_BYTES + 16;
-  static constexpr int RAW = DOWN ? 6 : (BITS == 8 ? 4 : 5);    // raw-code ring stages (prefetch RAW - 1 steps)
+  static constexpr int RAW = F8 ? 0 : (DOWN ? 6 : (BITS == 8 ? 4 : 5));  // raw-code ring stages (prefetch RAW - 1)
   static constexpr int A_BYTES = BM * KB;
   static constexpr int B_BYTES = NT * KB;
   static constexpr int A_STAGE = NMAT * A_BYTES;
@@ -284,10 +291,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-template <int F, bool DOWN, bool FS>
+template <int F, bool DOWN, int LV>
 __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs a,
                                                                     const __grid_constant__ CUtensorMap tmB) {
-  using C = Cfg<F, DOWN, FS>;
+  using C = Cfg<F, DOWN, LV>;
+  constexpr bool FS = C::FS, F8 = C::F8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full_a[C::SA], empty_a[C::SA], full_b[C::SB], empty_b[C::SB];
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
   const int K = DOWN ? I : H;          // reduction length
   const int N = DOWN ? H : I;          // rows of one weight matrix
   const int RT = N / BM;               // row tiles per token tile
-  const int nsteps = K / BK;
+  const int nsteps = K / C::KSTEP;
   const int n_items = (a.dense_T ? (a.dense_T + NT - 1) / NT : a.rb.ctrl->n_tiles) * RT;
   Ctrl* ctrl = a.rb.ctrl;
 
@@ -335,6 +343,44 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
     uint8_t* raw = smem + C::RAW_OFF + d * C::RAW_BYTES;
     uint32_t g = 0;
     bool ok = true;
+    if constexpr (F8) {
+      // FP8-activation lever: the E4M3 weight codes are the MMA's A operand as stored.  Each thread
+      // copies its row's step (128 bytes for gate/up, 64 for down) straight into the swizzled A
+      // stage and arrives two steps later, once those copies have landed.
+      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+        const int2 tile = tile_at(a, it / RT);
+        const int rt = it % RT, e = tile.x;
+        const int row = rt * BM + rr;
+        const uint8_t* crow = W.data + (size_t)e * data_bytes(F, N, K) + (size_t)row * (size_t)K;
+        const uint32_t g0 = g;
+#pragma unroll 1
+        for (int s = 0; s < nsteps; ++s, ++g) {
+          const int stage = g % C::SA;
+          if (!tc::bar_wait(&empty_a[stage], ((g / C::SA) & 1) ^ 1, a.wait_ns)) {
+            report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x300 | (DOWN ? 1 : 0));
+            ok = false;
+            break;
+          }
+          uint8_t* A = smem + stage * C::A_STAGE + m * C::A_BYTES;
+          const uint8_t* src = crow + (size_t)s * C::KSTEP + hh * C::KT;
+#pragma unroll
+          for (int j = 0; j < C::CODE_BYTES / 16; ++j)
+            cp_async16(A + tc::sw128_off(rr, hh * (C::CODE_BYTES / 16) + j), src + 16 * j);
+          cp_async_commit();
+          if (s >= 2) {
+            cp_async_wait<2>();
+            tc::fence_proxy_async();
+            tc::bar_arrive(&full_a[(g - 2) % C::SA]);
+          }
+        }
+        if (!ok) break;
+        // the item's last (up to two) steps
+        cp_async_wait<0>();
+        tc::fence_proxy_async();
+        for (int s = nsteps > 2 ? nsteps - 2 : 0; s < nsteps; ++s) tc::bar_arrive(&full_a[(g0 + s) % C::SA]);
+      }
+    }
+    if constexpr (!F8)
     for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
       const int2 tile = tile_at(a, it / RT);
       const int rt = it % RT, e = tile.x;
@@ -432,7 +478,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         if (lane == 0) tc::bar_arrive_expect_tx(&full_b[stage], C::B_BYTES);
         __syncwarp();
         // rows past the tile's tokens (the next segment, or zero fill) only feed discarded columns
-        if (lane == 0) tc::tma_load_2d(B, &tmB, s * BK, pos0, &full_b[stage]);
+        if (lane == 0) tc::tma_load_2d(B, &tmB, s * C::KSTEP, pos0, &full_b[stage]);
       }
     }
     // every load this warp issued has landed before the CTA can exit (the MMA warp may have stopped early)
@@ -464,7 +510,8 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
 #pragma unroll
         for (int mm = 0; mm < C::NMAT; ++mm) {
           const uint64_t da = tc::smem_desc_sw128(base + mm * C::A_BYTES + kk * 32);
-          tc::mma_f16_elect(acc + mm * NT, da, db, idesc, accumulate || kk != 0);
+          if constexpr (F8) tc::mma_e4m3_elect(acc + mm * NT, da, db, idesc, accumulate || kk != 0);
+          else tc::mma_f16_elect(acc + mm * NT, da, db, idesc, accumulate || kk != 0);
         }
       }
       tc::commit_elect(&empty_a[sa]);
@@ -484,7 +531,8 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
     for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++item) {
       const int n_valid = tile_valid(a, tile_at(a, it / RT));
       const int n_mma = (n_valid + 15) & ~15;
-      const uint32_t idesc = tc::idesc_f16(BM, n_mma, FS ? 1 : 0);  // FS: bf16 operands
+      // FS: bf16 operands; F8: E4M3 A and B (format code 0 of kind::f8f6f4, the bits of f16 in kind::f16)
+      const uint32_t idesc = tc::idesc_f16(BM, n_mma, FS ? 1 : 0);
       if constexpr (C::PROMOTE) {
         // each scale group into the block set; the epilogue empties it before the next group
         const uint32_t blk = tmem + C::ACC_COLS;
@@ -541,7 +589,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int pos_l = pos0 + min(chalf * 64 + i * 32 + lane, n_valid - 1);
-        if (FS) un_c[i] = 1.f;  // plain BF16 tokens
+        if (FS || F8) un_c[i] = 1.f;  // plain BF16 tokens / activation scales applied per group
         else if (DOWN) un_c[i] = exp2i(-a.hsig[pos_l]);
         else un_c[i] = exp2i(-a.xsig[a.dense_T ? pos_l : a.rb.pair[pos_l] / k]);
       }
@@ -571,6 +619,17 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
             const int c0 = chalf * 64 + ch * 16;
             if (c0 >= n_valid) break;
             float r[C::NMAT][16];
+            // F8: the group's activation scale of each of the chunk's columns (lane j < 16 loads column
+            // c0 + j), so the group's factor is weight scale x activation scale
+            float fa[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) fa[j] = 1.f;
+            if constexpr (F8) {
+              const int cj = c0 + (lane & 15);
+              const float asl = cj < n_valid ? __ldg(a.asc + (size_t)(pos0 + cj) * (K / 128) + gi) : 0.f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) fa[j] = __shfl_sync(0xFFFFFFFFu, asl, j);
+            }
 #pragma unroll
             for (int mm = 0; mm < C::NMAT; ++mm) {
               uint32_t bv[16], rv[16];
@@ -578,9 +637,11 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
               if (gi > 0) tc::tmem_ld16(tq + mm * NT + c0, rv);
               tc::tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                r[mm][j] = gi > 0 ? fmaf(sc[mm], __uint_as_float(bv[j]), __uint_as_float(rv[j]))
-                                  : sc[mm] * __uint_as_float(bv[j]);
+              for (int j = 0; j < 16; ++j) {
+                const float f = F8 ? sc[mm] * fa[j] : sc[mm];
+                r[mm][j] = gi > 0 ? fmaf(f, __uint_as_float(bv[j]), __uint_as_float(rv[j]))
+                                  : f * __uint_as_float(bv[j]);
+              }
               if (!last) tmem_st16(tq + mm * NT + c0, r[mm]);
             }
             if (last) {
@@ -731,41 +792,65 @@ bool f16_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uin
 
 }  // namespace
 
-// FS: the fold-scales lever (B operands: plain BF16 x rows and h rows).
-template <int F, bool FS>
+// E4M3 codes [rows, cols] (row-major bytes), boxes of 128 bytes x box_rows rows,
+// 128-byte swizzle, zero fill outside the matrix (the FP8-activation lever's B).
+bool u8_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {128u, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// LV: the lever (0 none, 1 fold scales: B is plain BF16 x rows and h rows; 2 FP8 activations: B is the
+// E4M3 codes of x and h, their block scales in the argument block's asc).
+template <int F, int LV>
 cudaError_t launch_pf_gemm(bool down, const PrefillArgs& a, int grid, cudaStream_t s) {
   cudaError_t err;
   alignas(64) CUtensorMap tm;
+  PrefillArgs b = a;
+  const uint64_t rows = (uint64_t)a.T * a.k;
+  const int K = down ? a.I : a.H;
+  void* src = down ? (LV == 1 ? (void*)a.h : (void*)a.h16) : (void*)a.xg;
+  if (LV == 2) {
+    if (!u8_map(&tm, src, (uint64_t)K, rows, NT)) return cudaErrorInvalidValue;
+    b.asc = fp8_scales_after(src, rows, K);
+  } else if (!f16_map(&tm, src, (uint64_t)K, rows, NT)) {
+    return cudaErrorInvalidValue;
+  }
   if (down) {
-    if (!f16_map(&tm, FS ? a.h : a.h16, (uint64_t)a.I, (uint64_t)a.T * a.k, NT)) return cudaErrorInvalidValue;
-    err = cudaFuncSetAttribute(pf_gemm_kernel<F, true, FS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<F, true, FS>::SMEM);
+    err = cudaFuncSetAttribute(pf_gemm_kernel<F, true, LV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<F, true, LV>::SMEM);
     if (err != cudaSuccess) return err;
-    pf_gemm_kernel<F, true, FS><<<grid, kPfGemmThreads, Cfg<F, true, FS>::SMEM, s>>>(a, tm);
+    pf_gemm_kernel<F, true, LV><<<grid, kPfGemmThreads, Cfg<F, true, LV>::SMEM, s>>>(b, tm);
   } else {
-    if (!f16_map(&tm, a.xg, (uint64_t)a.H, (uint64_t)a.T * a.k, NT)) return cudaErrorInvalidValue;
-    err = cudaFuncSetAttribute(pf_gemm_kernel<F, false, FS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<F, false, FS>::SMEM);
+    err = cudaFuncSetAttribute(pf_gemm_kernel<F, false, LV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<F, false, LV>::SMEM);
     if (err != cudaSuccess) return err;
-    pf_gemm_kernel<F, false, FS><<<grid, kPfGemmThreads, Cfg<F, false, FS>::SMEM, s>>>(a, tm);
+    pf_gemm_kernel<F, false, LV><<<grid, kPfGemmThreads, Cfg<F, false, LV>::SMEM, s>>>(b, tm);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_gemm(bool down, const PrefillArgs& a, int grid, cudaStream_t s) {
   switch (a.fmt) {
-    case MOE_FMT_NVFP4: return launch_pf_gemm<MOE_FMT_NVFP4, false>(down, a, grid, s);
-    case MOE_FMT_MXFP4: return launch_pf_gemm<MOE_FMT_MXFP4, false>(down, a, grid, s);
-    case MOE_FMT_INT4_G64: return launch_pf_gemm<MOE_FMT_INT4_G64, false>(down, a, grid, s);
+    case MOE_FMT_NVFP4: return launch_pf_gemm<MOE_FMT_NVFP4, 0>(down, a, grid, s);
+    case MOE_FMT_MXFP4: return launch_pf_gemm<MOE_FMT_MXFP4, 0>(down, a, grid, s);
+    case MOE_FMT_INT4_G64: return launch_pf_gemm<MOE_FMT_INT4_G64, 0>(down, a, grid, s);
     case MOE_FMT_INT8_G64:
-      return fold_lever(a) ? launch_pf_gemm<MOE_FMT_INT8_G64, true>(down, a, grid, s)
-                           : launch_pf_gemm<MOE_FMT_INT8_G64, false>(down, a, grid, s);
+      return fold_lever(a) ? launch_pf_gemm<MOE_FMT_INT8_G64, 1>(down, a, grid, s)
+                           : launch_pf_gemm<MOE_FMT_INT8_G64, 0>(down, a, grid, s);
     case MOE_FMT_FP8_B128:
-      return fold_lever(a) ? launch_pf_gemm<MOE_FMT_FP8_B128, true>(down, a, grid, s)
-                           : launch_pf_gemm<MOE_FMT_FP8_B128, false>(down, a, grid, s);
+      return fp8_lever(a)    ? launch_pf_gemm<MOE_FMT_FP8_B128, 2>(down, a, grid, s)
+             : fold_lever(a) ? launch_pf_gemm<MOE_FMT_FP8_B128, 1>(down, a, grid, s)
+                             : launch_pf_gemm<MOE_FMT_FP8_B128, 0>(down, a, grid, s);
     case MOE_FMT_INT4_G128:
-      return fold_lever(a) ? launch_pf_gemm<MOE_FMT_INT4_G128, true>(down, a, grid, s)
-                           : launch_pf_gemm<MOE_FMT_INT4_G128, false>(down, a, grid, s);
+      return fold_lever(a) ? launch_pf_gemm<MOE_FMT_INT4_G128, 1>(down, a, grid, s)
+                           : launch_pf_gemm<MOE_FMT_INT4_G128, 0>(down, a, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

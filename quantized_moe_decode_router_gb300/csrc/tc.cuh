@@ -96,6 +96,16 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
       smem_u32(bar)));
 }
 
+// kind::f8f6f4 with E4M3 A and B (instruction descriptor formats 0), K = 32
+// per MMA, FP32 accumulation; issued like mma_f16_elect.
+__device__ __forceinline__ void mma_e4m3_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
 // commit from the lane that mma_f16_elect elects (a converged warp).
 __device__ __forceinline__ void commit_elect(uint64_t* bar) {
   asm volatile(

@@ -83,7 +83,8 @@ def ws_read(ws: torch.Tensor, off: int, dtype, count: int) -> np.ndarray:
     return ws[off:off + nbytes].cpu().numpy().view(dtype).copy()
 
 
-def decode(layer, x_bits: np.ndarray, ws=None, prefill: bool = False, act_quant: int = 0, fold_scales: int = 0):
+def decode(layer, x_bits: np.ndarray, ws=None, prefill: bool = False, act_quant: int = 0, fold_scales: int = 0,
+           fp8_act: int = 0):
     """Run one forward call; returns (y bits uint16 [T, H], routing dict read from the workspace)."""
     T, H = x_bits.shape
     if ws is None:
@@ -91,7 +92,7 @@ def decode(layer, x_bits: np.ndarray, ws=None, prefill: bool = False, act_quant:
     x = x_device(x_bits)
     y = torch.zeros((T, H), dtype=torch.int16, device="cuda")
     if prefill:
-        B.moe_prefill_forward(layer, x, T, y, ws, act_quant=act_quant, fold_scales=fold_scales)
+        B.moe_prefill_forward(layer, x, T, y, ws, act_quant=act_quant, fold_scales=fold_scales, fp8_act=fp8_act)
     else:
         B.moe_decode_forward(layer, x, T, y, ws, act_quant=act_quant)
     torch.cuda.synchronize()

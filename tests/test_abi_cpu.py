@@ -106,10 +106,12 @@ def test_invalid_calls_rejected_before_launch(lib):
     assert f(ctypes.byref(L), FAKE, 1, FAKE, ctypes.byref(o), FAKE, n, None) == B.MOE_ERR_UNSUPPORTED
     o = B._opts(fold_scales=1)   # a prefill-only lever: refused by the decode entry points, never ignored
     assert f(ctypes.byref(L), FAKE, 1, FAKE, ctypes.byref(o), FAKE, n, None) == B.MOE_ERR_UNSUPPORTED
+    o = B._opts(fp8_act=1)
+    assert f(ctypes.byref(L), FAKE, 1, FAKE, ctypes.byref(o), FAKE, n, None) == B.MOE_ERR_UNSUPPORTED
     o = B._opts()
     o.reserved[0] = 1
     assert f(ctypes.byref(L), FAKE, 1, FAKE, ctypes.byref(o), FAKE, n, None) == B.MOE_ERR_INVALID_ARG
-    for bad in (dict(bf16_partials=2), dict(wait_limit_us=-1), dict(fold_scales=2)):
+    for bad in (dict(bf16_partials=2), dict(wait_limit_us=-1), dict(fold_scales=2), dict(fp8_act=-1)):
         o = B._opts(**bad)
         assert f(ctypes.byref(L), FAKE, 1, FAKE, ctypes.byref(o), FAKE, n, None) == B.MOE_ERR_INVALID_ARG, bad
     # a shared-expert gate without a shared expert, a bias mode outside 0/1

@@ -166,6 +166,55 @@ def test_prefill_fold_scales_full_size_sampled(name, T, tokens):
     assert_prefill_routing(routing, ref, ref["near_midpoint"])
 
 
+# the FP8-activation lever: layers with an FP8 b128 expert, routed or shared
+FP8A = [c for c in SMALL if FMT_FP8_B128 in (c.fmt, c.shared_fmt)]
+
+
+@pytest.mark.parametrize("cfg", FP8A, ids=[c.name for c in FP8A])
+@pytest.mark.parametrize("T", [1, 17, 300])
+def test_prefill_fp8_act_matches_oracle(cfg, T):
+    hl = synth.make_layer(cfg, seed=11)
+    dl = to_device(hl)
+    x = synth.make_tokens(cfg, T, seed=11, batch=T)
+    y, routing = G.decode(dl, x, prefill=True, fp8_act=1)
+    ref = M.layer_forward(hl, x, fp8_act=True)
+    _check_y(y, ref["y_bits"])
+    assert_prefill_routing(routing, ref, ref["near_midpoint"])
+
+
+def test_prefill_fp8_act_is_a_lever_and_composes_with_fold_scales():
+    cfg = next(c for c in SMALL if c.name == "p_fp8_mxfp4")
+    hl = synth.make_layer(cfg, seed=12)
+    dl = to_device(hl)
+    x = synth.make_tokens(cfg, 300, seed=12, batch=5)
+    y_f8, _ = G.decode(dl, x, prefill=True, fp8_act=1)
+    y_exact, _ = G.decode(dl, x, prefill=True)
+    assert not np.array_equal(y_f8, y_exact)
+    # both levers: the FP8 b128 routed experts take the FP8-activation path (precedence), so the output
+    # equals the FP8-activation lever alone
+    y_both, _ = G.decode(dl, x, prefill=True, fp8_act=1, fold_scales=1)
+    assert np.array_equal(y_both, y_f8)
+    _check_y(y_both, M.layer_forward(hl, x, fp8_act=True, fold_scales=True)["y_bits"])
+    # an NVFP4 layer without an FP8 expert is left bit for bit
+    cfg2 = SMALL[2]
+    hl2 = synth.make_layer(cfg2, seed=12)
+    dl2 = to_device(hl2)
+    x2 = synth.make_tokens(cfg2, 300, seed=12, batch=6)
+    assert np.array_equal(G.decode(dl2, x2, prefill=True, fp8_act=1)[0], G.decode(dl2, x2, prefill=True)[0])
+
+
+def test_prefill_fp8_act_full_size_sampled():
+    """The lever on the NVFP4 decode layer's FP8 b128 shared expert at full size, sampled tokens."""
+    hl = G.host_layer("decode_nvfp4")
+    dl = G.device_layer("decode_nvfp4")
+    T, tokens = 1024, [0, 511, 1023]
+    x = synth.make_tokens(hl.cfg, T, seed=2, batch=T)
+    y, routing = G.decode(dl, x, prefill=True, fp8_act=1)
+    ref = M.layer_forward(hl, x, tokens=tokens, fp8_act=True)
+    _check_y(y, ref["y_bits"], tokens)
+    assert_prefill_routing(routing, ref, ref["near_midpoint"])
+
+
 @pytest.mark.parametrize("T,tokens", [(256, [0, 37, 255]), (4096, [0, 1, 2047, 4095])])
 def test_prefill_workload_matches_oracle(T, tokens):
     hl = G.host_layer("prefill_nvfp4")
