@@ -390,6 +390,8 @@ PREFILL_EXTRA = {
     # the prefill workload's shape with AutoRound int4 g128 routed experts (the fold-scales lever's case)
     "prefill_int4g128": lambda: synth.CONFIGS["prefill_nvfp4"].with_(name="prefill_int4g128",
                                                                      fmt=synth.configs.FMT_INT4_G128),
+    # the prefill workload's shape with FP8 b128 routed experts (the FP8-activation lever's case)
+    "prefill_fp8": lambda: synth.CONFIGS["prefill_nvfp4"].with_(name="prefill_fp8", fmt=synth.configs.FMT_FP8_B128),
 }
 
 
@@ -397,19 +399,19 @@ def prefill_config(name: str):
     return PREFILL_EXTRA[name]() if name in PREFILL_EXTRA else synth.CONFIGS[name]
 
 
-def _prefill_times(torch, q, lay, xs, T, y, ws, stream, act_quant, reps, G=6, fold_scales=0):
+def _prefill_times(torch, q, lay, xs, T, y, ws, stream, act_quant, reps, G=6, fold_scales=0, fp8_act=0):
     """Median whole-layer time (graph of G calls, `reps` replays) and per-stage event times."""
     NB = len(xs)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         for i in range(3):
             q.moe_prefill_forward(lay, xs[i % NB], T, y, ws, stream=stream, act_quant=act_quant,
-                                  fold_scales=fold_scales)
+                                  fold_scales=fold_scales, fp8_act=fp8_act)
         stream.synchronize()
         with torch.cuda.graph(g, stream=stream):
             for i in range(G):
                 q.moe_prefill_forward(lay, xs[i % NB], T, y, ws, stream=stream, act_quant=act_quant,
-                                  fold_scales=fold_scales)
+                                  fold_scales=fold_scales, fp8_act=fp8_act)
         for _ in range(2):
             g.replay()
     torch.cuda.synchronize()
@@ -426,7 +428,7 @@ def _prefill_times(torch, q, lay, xs, T, y, ws, stream, act_quant, reps, G=6, fo
     with torch.cuda.graph(gt, stream=stream):
         for i in range(n):
             q.moe_prefill_forward_timed(lay, xs[i % NB], T, y, ws, evs[i], stream=stream, act_quant=act_quant,
-                                        fold_scales=fold_scales)
+                                        fold_scales=fold_scales, fp8_act=fp8_act)
     with torch.cuda.stream(stream):
         gt.replay()
     torch.cuda.synchronize()
@@ -439,8 +441,9 @@ def _prefill_times(torch, q, lay, xs, T, y, ws, stream, act_quant, reps, G=6, fo
 
 def run_prefill(args, local, peak_bf16, peak_kind, name="prefill_nvfp4", tokens=0, w4a4=True):
     """One prefill workload: whole-layer time through moe_prefill_forward, per-stage event times and the
-    grouped GEMMs' tensor throughput, for the exact chain, the W4A4 lever (NVFP4 and MXFP4 layers) and the
-    fold-scales lever (layers with int8 g64, FP8 b128 or int4 g128 experts)."""
+    grouped GEMMs' tensor throughput, for the exact chain, the W4A4 lever (NVFP4 and MXFP4 layers), the
+    fold-scales lever (layers with int8 g64, FP8 b128 or int4 g128 experts) and the FP8-activation lever
+    (layers with FP8 b128 experts)."""
     import torch
     import quantized_moe_decode_router_gb300 as q
     cfg = prefill_config(name)
@@ -538,6 +541,23 @@ def run_prefill(args, local, peak_bf16, peak_kind, name="prefill_nvfp4", tokens=
             "kernel_us": {k: round(float(v), 2) for k, v in zip(names, durf)},
             "achieved_tflops": round(tflf, 1), "frac_f16_peak": round(tflf / peak_bf16, 4),
             "vs_exact_chain": round(us / usf, 3)}
+    on8 = [w for w, f in (("routed", cfg.fmt), ("shared", cfg.shared_fmt)) if f == synth.configs.FMT_FP8_B128]
+    if on8:
+        # the FP8-activation lever: E4M3 x E4M3 MMAs, weight and activation block scales per 128-K group
+        us8, dur8 = _prefill_times(torch, q, lay, xs, T, y, ws, stream, 0, reps, G, fp8_act=1)
+        tfl8 = flops / ((dur8[3] + dur8[5]) * 1e-6) / 1e12
+        fp8_peak = peak_bf16 * 4.5 / 2.25   # derived: the measured dense bf16 peak x the nominal FP8/bf16 ratio
+        out["fp8_act"] = {
+            "path": (f"FP8-activation lever (fp8_act=1) on the {' and '.join(on8)} experts: per-token 1x128 E4M3 "
+                     f"activations, tcgen05 kind::f8f6f4 E4M3 x E4M3, scales per 128-K group in FP32"),
+            "us_per_layer": round(us8, 1), "tokens_per_s": round(T / (us8 * 1e-6), 1),
+            "kernel_us": {k: round(float(v), 2) for k, v in zip(
+                ["router_logits", "router_topk", "dispatch_quantise", "gateup_gemm", "h_quantise", "down_gemm",
+                 "combine"], dur8)},
+            "achieved_tflops": round(tfl8, 1), "frac_fp8_peak": round(tfl8 / fp8_peak, 4),
+            "fp8_peak_tflops": round(fp8_peak, 1),
+            "fp8_peak_kind": f"derived: {peak_kind} bf16 burst {peak_bf16} TFLOP/s x 4.5/2.25 (nominal dense FP8/bf16)",
+            "vs_exact_chain": round(us / us8, 3)}
     return out
 
 
@@ -549,6 +569,7 @@ DATA_DESC = {
     "decode_int4": "N(0,0.02) weights quantised int4 g64 routed / int8 g64 shared",
     "prefill_nvfp4": "N(0,0.02) weights quantised NVFP4, Zipf router bias s=1.1",
     "prefill_int4g128": "N(0,0.02) weights quantised int4 g128 (AutoRound layout), Zipf router bias s=1.1",
+    "prefill_fp8": "N(0,0.02) weights quantised FP8 b128, Zipf router bias s=1.1",
 }
 
 
@@ -643,7 +664,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill workload's measurement")
     ap.add_argument("--prefill-steps", type=int, default=60)
-    ap.add_argument("--more-prefill", default="prefill_mxfp4,prefill_int4,prefill_int4g128",
+    ap.add_argument("--more-prefill", default="prefill_mxfp4,prefill_int4,prefill_int4g128,prefill_fp8",
                     help="further prefill workloads measured beside prefill_nvfp4 (the exact chain and the levers "
                          "that apply to their formats)")
     ap.add_argument("--prefill-only", action="store_true",

@@ -263,8 +263,10 @@ __global__ void __launch_bounds__(32) pf_place_kernel(PrefillArgs a) {
 // lever): per 128-element block s = amax / 448 and code = e4m3_rne_sat(v / s),
 // both IEEE FP32 divisions (a negative value that rounds to zero keeps its
 // sign: code 0x80); a zero block has scale 0 and +0 codes.  One warp, four
-// elements per lane and block.
-__device__ void quant_row_fp8(const uint16_t* src, int K, uint8_t* codes, float* scales, int lane) {
+// elements per lane and block.  The result goes to ndst rows of the code and
+// scale arrays: row r = the value of `dst` in lane r (ndst <= 32).
+__device__ void quant_row_fp8(const uint16_t* src, int K, uint8_t* codes, float* scales, int dst, int ndst,
+                              int lane) {
   for (int b = 0; b < K / 128; ++b) {
     const uint2 w = __ldg(reinterpret_cast<const uint2*>(src + b * 128) + lane);
     const float v[4] = {bf16_bits_to_float(w.x & 0xFFFF), bf16_bits_to_float(w.x >> 16),
@@ -283,22 +285,26 @@ __device__ void quant_row_fp8(const uint16_t* src, int K, uint8_t* codes, float*
         out |= c << (8 * i);
       }
     }
-    reinterpret_cast<uint32_t*>(codes + b * 128)[lane] = out;
-    if (lane == 0) scales[b] = sc;
+    for (int r = 0; r < ndst; ++r) {
+      const int row = __shfl_sync(0xFFFFFFFFu, dst, r);
+      reinterpret_cast<uint32_t*>(codes + (size_t)row * K + b * 128)[lane] = out;
+      if (lane == 0) scales[(size_t)row * (K / 128) + b] = sc;
+    }
   }
 }
 
-// The FP8-activation lever's token operand: one warp per sorted position (or
-// token, dense) quantises the token's BF16 row into E4M3 codes and scales.
+// The FP8-activation lever's token operand: one warp per token quantises its
+// BF16 row once into E4M3 codes and scales and writes them to each of the
+// token's sorted positions (dense: row t).
 __global__ void __launch_bounds__(kThreads) pf_gather_fp8_kernel(PrefillArgs a) {
   const int lane = threadIdx.x & 31;
-  const int pos = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  const int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  if (t >= a.T) return;
   const int rows = a.T * a.k;
-  if (pos >= rows) return;
-  const int t = a.dense_T ? pos : a.rb.pair[pos] / a.k;
+  const int k = a.dense_T ? 1 : a.k;
+  const int dst = a.dense_T ? t : (lane < k ? __ldg(a.pos_of + (size_t)t * k + lane) : 0);
   uint8_t* codes = reinterpret_cast<uint8_t*>(a.xg);
-  quant_row_fp8(a.x + (size_t)t * a.H, a.H, codes + (size_t)pos * a.H,
-                fp8_scales_after(codes, rows, a.H) + (size_t)pos * (a.H / 128), lane);
+  quant_row_fp8(a.x + (size_t)t * a.H, a.H, codes, fp8_scales_after(codes, rows, a.H), dst, k, lane);
 }
 
 // The FP8-activation lever's h operand: each h row (BF16, after the gate/up
@@ -309,8 +315,7 @@ __global__ void __launch_bounds__(kThreads) pf_hquant_fp8_kernel(PrefillArgs a) 
   const int rows = a.T * a.k;
   if (pos >= rows) return;
   uint8_t* codes = reinterpret_cast<uint8_t*>(a.h16);
-  quant_row_fp8(a.h + (size_t)pos * a.I, a.I, codes + (size_t)pos * a.I,
-                fp8_scales_after(codes, rows, a.I) + (size_t)pos * (a.I / 128), lane);
+  quant_row_fp8(a.h + (size_t)pos * a.I, a.I, codes, fp8_scales_after(codes, rows, a.I), pos, 1, lane);
 }
 
 __global__ void __launch_bounds__(kThreads) pf_gather_kernel(PrefillArgs a) {
@@ -485,7 +490,7 @@ cudaError_t launch_prefill_route(const PrefillArgs& a, cudaStream_t s, Marks mk)
     if (e2 != cudaSuccess) return e2;
     pf_gather_q_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
   } else if (a.xg) {
-    if (fp8_lever(a)) pf_gather_fp8_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
+    if (fp8_lever(a)) pf_gather_fp8_kernel<<<(a.T + wpb - 1) / wpb, kThreads, 0, s>>>(a);
     else pf_gather_kernel<<<(a.T * a.k + wpb - 1) / wpb, kThreads, 0, s>>>(a);
   }
   mk(3);

@@ -605,6 +605,16 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
 #pragma unroll
           for (int mm = 0; mm < C::NMAT; ++mm)
             sc[mm] = group_scale<F>(DOWN ? a.down : (mm == 0 ? a.gate : a.up), e, N, K, erow, rt, gi);
+          // F8: the group's activation scales of this warp's columns, fetched before the wait (lane j < 16
+          // of chunk ch holds column chalf * 64 + ch * 16 + j)
+          float asv[4] = {0.f, 0.f, 0.f, 0.f};
+          if constexpr (F8) {
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              const int cj = chalf * 64 + ch * 16 + (lane & 15);
+              asv[ch] = cj < n_valid ? __ldg(a.asc + (size_t)(pos0 + cj) * (K / 128) + gi) : 0.f;
+            }
+          }
           const bool ready = tc::bar_wait(&acc_full[0], gg & 1, a.wait_ns);
           if (!ready) report_error(ctrl, (uint32_t)MOE_ERR_DEVICE_TIMEOUT, 0x310 | (DOWN ? 1 : 0));
           // all epilogue warps go on, or all stop; the barrier also frees the staging tile
@@ -625,8 +635,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
 #pragma unroll
             for (int j = 0; j < 16; ++j) fa[j] = 1.f;
             if constexpr (F8) {
-              const int cj = c0 + (lane & 15);
-              const float asl = cj < n_valid ? __ldg(a.asc + (size_t)(pos0 + cj) * (K / 128) + gi) : 0.f;
+              const float asl = ch == 0 ? asv[0] : ch == 1 ? asv[1] : ch == 2 ? asv[2] : asv[3];
 #pragma unroll
               for (int j = 0; j < 16; ++j) fa[j] = __shfl_sync(0xFFFFFFFFu, asl, j);
             }
