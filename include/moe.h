@@ -268,9 +268,12 @@ int32_t moe_experts_forward(const moe_layer* layer, const void* x /* device bf16
  * moe_quantize_act_nvfp4), 2 for MXFP4 routed experts (MXFP4 32-element
  * blocks, the rule of moe_quantize_act_mxfp4); the projections then run as
  * block-scaled FP4 GEMMs.  It needs no shared expert, hidden and inter
- * multiples of 256 and 16-byte aligned scale arrays.  Routing outputs are left in the workspace; in its logits
- * array only the experts the router recomputed exactly (every selected one
- * among them) hold their FP32 logit, the others hold -inf.
+ * multiples of 256 and 16-byte aligned scale arrays.  opts->fold_scales and
+ * opts->fp8_act select the other two prefill levers (see moe_options); each
+ * changes only the experts of its formats and needs no other condition.
+ * Routing outputs are left in the workspace; in its logits array only the
+ * experts the router recomputed exactly (every selected one among them) hold
+ * their FP32 logit, the others hold -inf.
  */
 int32_t moe_prefill_forward(const moe_layer* layer, const void* x /* device bf16 [T, H] */, int32_t T,
                             void* y /* device bf16 [T, H] */, const moe_options* opts, void* ws, size_t ws_bytes,
