@@ -32,9 +32,10 @@
 //              loop, one elected lane issues);
 //              tcgen05.commit releases each stage and publishes each tile;
 //   warps 10-17 the epilogue, from TMEM accumulators that are double
-//              buffered so the next tile's MMAs overlap it; outputs are
-//              staged in shared memory and written with bulk copies (h and P
-//              rows in sorted-position order).
+//              buffered so the next tile's MMAs overlap it; h is staged in
+//              shared memory and written with bulk copies, P is stored from
+//              registers (coalesced: a warp's lanes hold consecutive rows);
+//              both by sorted position.
 // Every wait on an mbarrier is bounded; a wait that gives up records
 // MOE_ERR_DEVICE_TIMEOUT and the CTA winds down (draining its MMAs before
 // TMEM is released).
@@ -663,10 +664,11 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
                   if (!DOWN) {
                     const float gv = r[0][j] * un, uv = r[C::NMAT - 1][j] * un;
                     reinterpret_cast<uint16_t*>(stg)[(size_t)(c0 + j) * BM + row] = float_to_bf16_bits(silu(gv) * uv);
-                  } else if (a.p_bf16) {
-                    reinterpret_cast<uint16_t*>(stg)[(size_t)(c0 + j) * BM + row] = float_to_bf16_bits(r[0][j] * un);
                   } else {
-                    reinterpret_cast<float*>(stg)[(size_t)(c0 + j) * BM + row] = r[0][j] * un;
+                    // P row of sorted position pos0 + c0 + j: the warp's 32 lanes write 32 consecutive rows
+                    const size_t o = (size_t)(pos0 + c0 + j) * H + rt * BM + row;
+                    if (a.p_bf16) reinterpret_cast<uint16_t*>(a.P)[o] = float_to_bf16_bits(r[0][j] * un);
+                    else a.P[o] = r[0][j] * un;
                   }
                 }
               }
@@ -724,15 +726,17 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
             uint32_t dv[32];
             tc::tmem_ld32(acc + c0, dv);
             tc::tmem_ld_wait();
-            float* st32 = reinterpret_cast<float*>(stg) + (size_t)c0 * BM + row;
-            uint16_t* sb16 = reinterpret_cast<uint16_t*>(stg) + (size_t)c0 * BM + row;  // bf16-partials lever
+            // P straight from registers: for each column (sorted position) the warp's 32 lanes write
+            // 32 consecutive rows of P, one coalesced 128-byte store (64 bytes under bf16 partials)
+            float* p32 = a.P + (size_t)(pos0 + c0) * H + rt * BM + row;
+            uint16_t* p16 = reinterpret_cast<uint16_t*>(a.P) + (size_t)(pos0 + c0) * H + rt * BM + row;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float un = __shfl_sync(0xFFFFFFFFu, un_c[i], j);
               if (j < ncol) {
                 const float v = __uint_as_float(dv[j]) * (rf[0] * un);
-                if (a.p_bf16) sb16[j * BM] = float_to_bf16_bits(v);
-                else st32[j * BM] = v;
+                if (a.p_bf16) p16[(size_t)j * H] = float_to_bf16_bits(v);
+                else p32[(size_t)j * H] = v;
               }
             }
           }
@@ -740,21 +744,16 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1) pf_gemm_kernel(PrefillArgs 
         tc::fence_before_sync();
         tc::bar_arrive(&acc_empty[buf]);  // TMEM buffer free for the MMA of a later tile
       }
-      tc::fence_proxy_async();          // staging writes -> bulk copy reads
-      tc::named_sync(1, kEpiThreads);
-      if (ew == 0) {
-        for (int c = lane; c < n_valid; c += 32) {
-          const int pos = pos0 + c;
-          if (DOWN && a.p_bf16) {
-            tc::bulk_store(reinterpret_cast<uint16_t*>(a.P) + (size_t)pos * H + rt * BM, stg + c * BM * 2, BM * 2);
-          } else if (DOWN) {
-            tc::bulk_store(a.P + (size_t)pos * H + rt * BM, stg + c * BM * 4, BM * 4);
-          } else {
-            tc::bulk_store(a.h + (size_t)pos * I + rt * BM, stg + c * BM * 2, BM * 2);
-          }
+      if constexpr (!DOWN) {
+        // h leaves through the staging tile: one bulk copy per column (a contiguous run of its row)
+        tc::fence_proxy_async();          // staging writes -> bulk copy reads
+        tc::named_sync(1, kEpiThreads);
+        if (ew == 0) {
+          for (int c = lane; c < n_valid; c += 32)
+            tc::bulk_store(a.h + (size_t)(pos0 + c) * I + rt * BM, stg + c * BM * 2, BM * 2);
+          tc::bulk_commit();
+          tc::bulk_wait_read();
         }
-        tc::bulk_commit();
-        tc::bulk_wait_read();
       }
     }
     if (ew == 0) tc::bulk_wait();

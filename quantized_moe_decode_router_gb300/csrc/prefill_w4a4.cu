@@ -329,14 +329,15 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
           uint32_t dv[32];
           tc::tmem_ld32(acc + c0, dv);
           tc::tmem_ld_wait();
-          float* st32 = reinterpret_cast<float*>(stg) + (size_t)c0 * BM + row;
-          uint16_t* sb16 = reinterpret_cast<uint16_t*>(stg) + (size_t)c0 * BM + row;  // bf16-partials lever
+          // P straight from registers: per column the warp's 32 lanes write 32 consecutive rows
+          float* p32 = a.P + (size_t)(pos0 + c0) * H + rt * BM + row;
+          uint16_t* p16 = reinterpret_cast<uint16_t*>(a.P) + (size_t)(pos0 + c0) * H + rt * BM + row;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (j < ncol) {
               const float v = __uint_as_float(dv[j]) * ts0;
-              if (a.p_bf16) sb16[j * BM] = float_to_bf16_bits(v);
-              else st32[j * BM] = v;
+              if (a.p_bf16) p16[(size_t)j * H] = float_to_bf16_bits(v);
+              else p32[(size_t)j * H] = v;
             }
         }
       }
@@ -404,18 +405,17 @@ __global__ void __launch_bounds__(kThreads, 1) pf_w4a4_kernel(PrefillArgs a, con
           a.hsf[(size_t)(pos0 + c) * (I / 16) + rt * (BM / 16) + b] = (uint8_t)sc;
         }
       }
-      tc::fence_proxy_async();  // staging writes -> bulk copy reads
-      tc::named_sync(1, kEpiThreads);
-      if (ew == 0) {
-        for (int c = lane; c < n_valid; c += 32) {
-          const int pos = pos0 + c;
-          if (DOWN && a.p_bf16)
-            tc::bulk_store(reinterpret_cast<uint16_t*>(a.P) + (size_t)pos * H + rt * BM, stg + c * BM * 2, BM * 2);
-          else if (DOWN) tc::bulk_store(a.P + (size_t)pos * H + rt * BM, stg + c * BM * 4, BM * 4);
-          else tc::bulk_store(a.hq + (size_t)pos * (I / 2) + rt * (BM / 2), stg + NT * BM * 2 + c * (BM / 2), BM / 2);
+      if constexpr (!DOWN) {
+        // the h codes leave through the staging tile: one bulk copy per column
+        tc::fence_proxy_async();  // staging writes -> bulk copy reads
+        tc::named_sync(1, kEpiThreads);
+        if (ew == 0) {
+          for (int c = lane; c < n_valid; c += 32)
+            tc::bulk_store(a.hq + (size_t)(pos0 + c) * (I / 2) + rt * (BM / 2), stg + NT * BM * 2 + c * (BM / 2),
+                           BM / 2);
+          tc::bulk_commit();
+          tc::bulk_wait_read();
         }
-        tc::bulk_commit();
-        tc::bulk_wait_read();
       }
     }
     if (ew == 0) tc::bulk_wait();
