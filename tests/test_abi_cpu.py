@@ -162,3 +162,32 @@ def test_noalloc_rejects_bad_calls_before_touching_the_device(lib):
 def test_check_reports_short_workspaces(lib):
     assert lib.moe_check(None, 16, None) == B.MOE_ERR_WORKSPACE
     assert lib.moe_check(FAKE, 4, None) == B.MOE_ERR_WORKSPACE
+
+
+def test_binding_structs_match_the_header_layout(tmp_path):
+    # every struct the binding passes across the boundary has the C header's size and field offsets:
+    # a small C program compiled against include/moe.h prints them (gcc, no GPU)
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    header = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe.h")
+    structs = {"moe_qweight": B.moe_qweight, "moe_layer": B.moe_layer, "moe_options": B.moe_options,
+               "moe_ws_layout": B.moe_ws_layout, "moe_decode_plan_info": B.moe_decode_plan_info}
+    lines = [f'#include "{header}"', "#include <stdio.h>", "#include <stddef.h>", "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'  printf("{name} sizeof %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'  printf("{name} {field} %zu\\n", offsetof({name}, {field}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-std=c11", "-o", str(exe), str(src)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    c_vals = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for name, cls in structs.items():
+        assert c_vals[(name, "sizeof")] == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert c_vals[(name, field)] == getattr(cls, field).offset, (name, field)
