@@ -395,6 +395,10 @@ PREFILL_EXTRA = {
 }
 
 
+# the prefill workloads a default run measures beside prefill_nvfp4
+MORE_PREFILL = "prefill_mxfp4,prefill_int4,prefill_int4g128,prefill_fp8"
+
+
 def prefill_config(name: str):
     return PREFILL_EXTRA[name]() if name in PREFILL_EXTRA else synth.CONFIGS[name]
 
@@ -664,7 +668,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill workload's measurement")
     ap.add_argument("--prefill-steps", type=int, default=60)
-    ap.add_argument("--more-prefill", default="prefill_mxfp4,prefill_int4,prefill_int4g128,prefill_fp8",
+    ap.add_argument("--more-prefill", default=MORE_PREFILL,
                     help="further prefill workloads measured beside prefill_nvfp4 (the exact chain and the levers "
                          "that apply to their formats)")
     ap.add_argument("--prefill-only", action="store_true",

@@ -45,3 +45,19 @@ def test_aggregate_two_gloo_ranks():
 
 def test_aggregate_single_process_is_identity():
     assert bench.aggregate_ranks(3.5, 7.0) == (3.5, 7.0)
+
+
+def test_bench_workloads_resolve_on_cpu():
+    # every workload the default bench run names resolves to a layer the prefill and decode entry points
+    # accept (shapes multiples of 128; a lever's formats present), and has its data description
+    import synth
+    for name in bench.PREFILL_EXTRA:
+        cfg = bench.prefill_config(name)
+        assert cfg.name == name and cfg.batches[0] == 4096
+        assert cfg.H % 128 == 0 and cfg.I % 128 == 0 and (not cfg.shared_fmt or cfg.shared_I % 128 == 0)
+    assert bench.prefill_config("prefill_int4g128").fmt == synth.configs.FMT_INT4_G128
+    assert bench.prefill_config("prefill_fp8").fmt == synth.configs.FMT_FP8_B128
+    for name in bench.MORE_PREFILL.split(","):
+        assert name in bench.PREFILL_EXTRA, name
+    for name in ("decode_nvfp4", "decode_mxfp4", "decode_int4"):
+        assert name in bench.DATA_DESC
