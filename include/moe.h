@@ -13,7 +13,8 @@
  *    specifies; reduced-precision levers are explicit and off by default).
  *  - DGPP README, "Execution and performance" table: engine.prefill_bf16_partials
  *    (per-expert partials summed in fp32 by default), engine.prefill_fold_scales
- *    (per-group scale fma by default), engine.expert_tile_list (expert GEMM over
+ *    (per-group scale fma by default), engine.prefill_fp8_gemm (per-token 1x128
+ *    e4m3 activations for FP8 weights, off by default), engine.expert_tile_list (expert GEMM over
  *    a compact list of routed segments' tiles), engine.expert_gemm_pair (gate
  *    and up in one launch).
  *  - "DGPP: a GB10-optimized C/CUDA inference engine" (NVIDIA Developer Forums),
